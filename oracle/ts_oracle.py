@@ -1,0 +1,323 @@
+"""CPU oracle for the TokenSwift per-step decode hot path.
+
+TEST INFRASTRUCTURE ONLY.  This module is the slow, plain, fp64 statement of
+what the hot path computes, used to check the CUDA library.  Only the test
+suite, the package's smoke check and the benchmark's CPU-baseline leg may
+import it; the product path never does.  It shares no code with the CUDA
+path: its only inputs are numpy arrays (bf16 arrives as uint16 bit patterns,
+decoded here).
+
+Source: "TokenSwift: Lossless Acceleration of Ultra Long Sequence Generation"
+(Wu, Shen, Jia, Wang, Zheng; ICML 2025), as summarised on the pages studied:
+  * §3.1 Overview / Figure 2: drafting on a partial KV cache, verification on
+    the full cache, exact-match acceptance of the longest valid draft, then
+    n-gram table and KV cache update.
+  * §E Tree-Based Attention: each tree token attends only to its predecessors.
+  * §3.3 Dynamic KV Cache Management: fixed budget, the initial |S| pairs are
+    kept, importance = query-key dot products, GQA scores aggregated per group.
+  * §3.4 Contextual Penalty: a penalty on the most recent W tokens.
+  * §D.1 Sampling algorithms: top-p keeps the smallest set whose cumulative
+    probability exceeds p; min-p keeps tokens above p_base * p_max.
+  * Table 11: k=20, temperature 1.0, top-p 0.9, min-p 0.05, penalty 1.2,
+    penalty length 1024.
+
+Readings taken where the pages are silent (each also listed in the design
+notes): CTRL-style penalty is sign-aware (positive logits divided by theta,
+non-positive multiplied); a windowed token is penalised once whatever its
+count; top-p and min-p are intersected on the same post-temperature
+distribution; one uniform per node drives an inverse-CDF draw over the kept
+set in (p desc, id asc) order; importance is the raw scaled dot product summed
+over the group's heads and the last n_imp tree queries; sinks and the recent
+window are kept outside the top-B competition; ties in importance go to the
+lower position.
+
+Precision: scores, softmax and importance in fp64.  Where floating point
+decides an integer, the decision is taken in the precision the library
+stores the deciding quantity in: importance is rounded to fp32 before the
+top-B ranking (the library's imp array is fp32), and the penalised,
+temperature-scaled logits are formed with fp32 operations before ranking
+(the logits arrive as fp32).  Probabilities and their sums stay fp64.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+
+# --------------------------------------------------------------------------
+# input decoding
+# --------------------------------------------------------------------------
+def bf16_to_f64(bits: np.ndarray) -> np.ndarray:
+    """bf16 bit patterns (uint16) -> float64, exactly."""
+    u32 = np.asarray(bits, dtype=np.uint16).astype(np.uint32) << np.uint32(16)
+    return u32.view(np.float32).astype(np.float64)
+
+
+# --------------------------------------------------------------------------
+# draft tree
+# --------------------------------------------------------------------------
+def root_paths(parents) -> list[list[int]]:
+    """For every node i, the nodes from the root down to i (inclusive).
+
+    §E Tree-Based Attention: a tree token attends to its predecessors, i.e.
+    the chain of parents up to the root, plus itself."""
+    T = len(parents)
+    paths = []
+    for i in range(T):
+        chain = []
+        a = i
+        while a != -1:
+            chain.append(a)
+            a = int(parents[a])
+        paths.append(chain[::-1])
+    return paths
+
+
+# --------------------------------------------------------------------------
+# (a1, a2) tree verification attention + attention importance
+# --------------------------------------------------------------------------
+def verify_attention(q, k, v, L: int, parents, n_imp: int = 0):
+    """Tree-masked GQA/MHA attention of the T draft-tree queries against the
+    full KV cache, and the per-position importance of the cache.
+
+    q: [T, Hq, d] float64 (post-RoPE queries of the tree tokens)
+    k, v: [Hkv, >= L+T, d] float64; rows [0, L) are the committed cache,
+          row L+a holds tree node a's own key/value.
+    parents: [T] int, parents[0] = -1, parents[i] < i.
+
+    For node i and query head h (KV head kv = h // G, contiguous grouping):
+        s_j = q[i,h] . k[kv,j] / sqrt(d),  j in [0, L)  or  j = L+a, a on the
+              root path of i                                   (§3.1, §E)
+        O[i,h]   = sum_j exp(s_j - m) v_j / sum_j exp(s_j - m),  m = max_j s_j
+        LSE[i,h] = m + ln sum_j exp(s_j - m)
+    Importance (§3.3: query-key dot products; GQA queries partitioned, their
+    scores aggregated per group):
+        imp[kv, j] = sum over the last n_imp nodes i and the heads h of group
+                     kv of s_{i,h,j},  for cache positions j in [0, L) only.
+    Returns O [T,Hq,d], LSE [T,Hq], imp [Hkv, L] (all float64).
+    """
+    q = np.asarray(q, dtype=np.float64)
+    k = np.asarray(k, dtype=np.float64)
+    v = np.asarray(v, dtype=np.float64)
+    T, Hq, d = q.shape
+    Hkv = k.shape[0]
+    assert Hq % Hkv == 0
+    G = Hq // Hkv
+    n_imp = T if n_imp <= 0 else n_imp
+    scale = 1.0 / np.sqrt(d)
+    paths = root_paths(parents)
+
+    O = np.zeros((T, Hq, d))
+    LSE = np.zeros((T, Hq))
+    imp = np.zeros((Hkv, L))
+    for h in range(Hq):
+        kv = h // G
+        # scores of every tree query of head h against the committed cache
+        s_cache = (q[:, h, :] @ k[kv, :L, :].T) * scale           # [T, L]
+        for i in range(T):
+            tree_rows = [L + a for a in paths[i]]
+            s_tree = (k[kv, tree_rows, :] @ q[i, h, :]) * scale     # [depth+1]
+            m = max(s_cache[i].max() if L > 0 else -np.inf, s_tree.max())
+            w_cache = np.exp(s_cache[i] - m)
+            w_tree = np.exp(s_tree - m)
+            Z = w_cache.sum() + w_tree.sum()
+            O[i, h] = (w_cache @ v[kv, :L, :] + w_tree @ v[kv, tree_rows, :]) / Z
+            LSE[i, h] = m + np.log(Z)
+        for i in range(T - n_imp, T):
+            imp[kv] += s_cache[i]
+    return O, LSE, imp
+
+
+# --------------------------------------------------------------------------
+# (a3, a4) partial KV cache: top-B selection + gather
+# --------------------------------------------------------------------------
+def select_partial(imp_row, L: int, B: int, S: int, R: int) -> np.ndarray:
+    """Positions kept in one KV head's partial (draft) cache, ascending.
+
+    §3.3: a fixed budget; the initial |S| pairs (attention sinks) are always
+    preserved and less important pairs are replaced.  The recent window of R
+    positions is also always kept.  The top-B competition runs over
+    [S, L-R) ranked by (importance desc, position asc).  When the whole
+    cache fits the budget (L <= S+B+R) every position is kept.
+
+    imp_row: importance of positions [0, L), in the precision the library
+    ranks it (fp32 values, carried here as float64)."""
+    imp_row = np.asarray(imp_row, dtype=np.float64)
+    if L <= S + B + R:
+        return np.arange(L, dtype=np.int64)
+    cand = np.arange(S, L - R, dtype=np.int64)
+    order = np.lexsort((cand, -imp_row[cand]))   # primary: -imp asc; then position asc
+    top = cand[order[:B]]
+    keep = np.concatenate([np.arange(S), top, np.arange(L - R, L)])
+    return np.sort(keep)
+
+
+def gather_rows(cache_head, idx) -> np.ndarray:
+    """Compact draft cache of one KV head: rows idx of the full cache, copied
+    bit for bit (§3.1: the partial KV cache used for drafting)."""
+    return np.asarray(cache_head)[np.asarray(idx, dtype=np.int64)].copy()
+
+
+def select_cut_margin(imp_row, L: int, B: int, S: int, R: int) -> tuple[float, np.ndarray]:
+    """The B-th best candidate score s_cut, and for every candidate its
+    distance to s_cut (used to count near-ties between implementations)."""
+    imp_row = np.asarray(imp_row, dtype=np.float64)
+    if L <= S + B + R:
+        return np.inf, np.zeros(0)
+    cand = imp_row[S:L - R]
+    s_cut = np.sort(cand)[::-1][B - 1]
+    return float(s_cut), np.abs(cand - s_cut)
+
+
+# --------------------------------------------------------------------------
+# (a5, a6) contextual penalty + temperature + top-p / min-p + draw
+# --------------------------------------------------------------------------
+def penalty_window(prior, path_tokens, W: int) -> np.ndarray:
+    """The most recent W tokens at a tree node (§3.4): the committed history
+    `prior` (which ends with the root token) followed by the drafted tokens
+    on the root path of the node, root excluded; the last W of these."""
+    seq = np.concatenate([np.asarray(prior, dtype=np.int64),
+                          np.asarray(path_tokens, dtype=np.int64)])
+    return seq[len(seq) - W:] if W > 0 else seq[:0]
+
+
+def penalised_logits(x, window, penalty: float, temperature: float) -> np.ndarray:
+    """CTRL-style contextual penalty on the windowed tokens, then temperature.
+
+    Each distinct token in the window is penalised once: x/theta if x > 0,
+    x*theta otherwise (§3.4, §4.3.3, Table 11 theta = 1.2); every logit is
+    then divided by the temperature.  Formed with fp32 operations, the
+    precision the logits arrive in."""
+    x = np.asarray(x, dtype=np.float32).copy()
+    th = np.float32(penalty)
+    for t in np.unique(np.asarray(window, dtype=np.int64)):
+        xt = x[t]
+        x[t] = xt / th if xt > 0 else xt * th
+    return (x / np.float32(temperature)).astype(np.float32)
+
+
+def sample_from_logits(x_pen, top_p: float, min_p: float, u: float, return_info: bool = False):
+    """Draw one token from penalised logits with top-p and min-p truncation.
+
+    p = softmax(x') in fp64.  Tokens are ranked by (p desc, id asc).
+    top-p (§D.1): keep the smallest prefix of ranks whose mass reaches p, i.e.
+        rank r is kept iff the mass of ranks before r is < top_p.
+    min-p (§D.1): keep tokens with p >= min_p * p_max.
+    Both are applied (Table 11 sets both); the kept set K is their
+    intersection, which always holds rank 0.  The draw is the smallest rank r
+    in K whose cumulative mass over K exceeds u * mass(K).
+    """
+    x = np.asarray(x_pen, dtype=np.float64)
+    V = x.shape[0]
+    m = x.max()
+    e = np.exp(x - m)
+    p = e / e.sum()
+    ids = np.arange(V)
+    order = np.lexsort((ids, -p))
+    ps = p[order]
+    before = np.concatenate([[0.0], np.cumsum(ps)[:-1]])
+    keep = (before < top_p) & (ps >= min_p * ps[0])
+    keep[0] = True
+    n_keep = int(np.argmin(keep)) if not keep.all() else V   # keep is a prefix
+    kept = ps[:n_keep]
+    c = np.cumsum(kept)
+    target = u * c[-1]
+    r = int(np.argmax(c > target)) if (c > target).any() else n_keep - 1
+    tok = int(order[r])
+    if not return_info:
+        return tok
+    # distances of the three cut quantities to their cuts (probability units)
+    margins = [abs(before[n_keep] - top_p) if n_keep < V else np.inf,
+               abs(before[n_keep - 1] - top_p),
+               abs(ps[n_keep - 1] - min_p * ps[0]),
+               abs(ps[n_keep] - min_p * ps[0]) if n_keep < V else np.inf,
+               abs(c[r] - target) / c[-1],
+               abs((c[r - 1] if r > 0 else 0.0) - target) / c[-1]]
+    return tok, dict(n_keep=n_keep, rank=r, margin=float(min(margins)))
+
+
+def sample_node(logits_row, prior, path_tokens, W, penalty, temperature, top_p,
+                min_p, u, return_info=False):
+    """One tree node's draw: window, penalty, temperature, truncation, draw."""
+    win = penalty_window(prior, path_tokens, W)
+    xp = penalised_logits(logits_row, win, penalty, temperature)
+    return sample_from_logits(xp, top_p, min_p, u, return_info)
+
+
+# --------------------------------------------------------------------------
+# (a7) exact-match tree acceptance
+# --------------------------------------------------------------------------
+def accept_from_samples(parents, tree_tokens, sampled):
+    """Parallel form: every node has its own target sample.  The root is
+    accepted; node c is accepted iff its parent is accepted and its drafted
+    token equals the parent's sample (§3.1: exact-match verification).  The
+    longest accepted root path wins (deepest node; ties to the smaller node
+    index), and the bonus token is the sample at that node.
+    Returns (path list, bonus token)."""
+    T = len(parents)
+    accepted = np.zeros(T, dtype=bool)
+    depth = np.zeros(T, dtype=np.int64)
+    accepted[0] = True
+    for c in range(1, T):
+        p = int(parents[c])
+        depth[c] = depth[p] + 1
+        accepted[c] = accepted[p] and int(tree_tokens[c]) == int(sampled[p])
+    best = 0
+    for c in range(T):
+        if accepted[c] and depth[c] > depth[best]:
+            best = c
+    path = root_paths(parents)[best]
+    return path, int(sampled[best])
+
+
+def sample_accept_sequential(logits, prior, parents, tree_tokens, W, penalty,
+                             temperature, top_p, min_p, uniforms):
+    """Sequential form of one verification step: starting at the root, sample
+    the current node, move to the lowest-index child whose drafted token
+    equals that sample, repeat; stop when no child matches.  Only nodes on
+    the accepted path are sampled.  Returns (path, bonus token)."""
+    T = len(parents)
+    children = [[] for _ in range(T)]
+    for c in range(1, T):
+        children[int(parents[c])].append(c)
+    node, path, drafted = 0, [0], []
+    while True:
+        tok = sample_node(logits[node], prior, drafted, W, penalty, temperature,
+                          top_p, min_p, float(uniforms[node]))
+        nxt = [c for c in children[node] if int(tree_tokens[c]) == tok]
+        if not nxt:
+            return path, tok
+        node = min(nxt)
+        path.append(node)
+        drafted.append(int(tree_tokens[node]))
+
+
+def sample_all_nodes(logits, prior, parents, tree_tokens, W, penalty,
+                     temperature, top_p, min_p, uniforms, return_info=False):
+    """Every node's draw (the parallel form's input).  Node i's window holds
+    the drafted tokens on its root path, root excluded."""
+    paths = root_paths(parents)
+    out, infos = [], []
+    for i in range(len(parents)):
+        drafted = [int(tree_tokens[a]) for a in paths[i][1:]]
+        r = sample_node(logits[i], prior, drafted, W, penalty, temperature,
+                        top_p, min_p, float(uniforms[i]), return_info)
+        if return_info:
+            out.append(r[0])
+            infos.append(r[1])
+        else:
+            out.append(r)
+    out = np.asarray(out, dtype=np.int64)
+    return (out, infos) if return_info else out
+
+
+# --------------------------------------------------------------------------
+# (a8) KV commit of the accepted path
+# --------------------------------------------------------------------------
+def kv_commit(cache, L: int, path) -> np.ndarray:
+    """After acceptance the cache update (§3.1) keeps the accepted tree rows:
+    row L+path[t] moves to row L+t for t = 1..len(path)-1 (the root's row is
+    already at L).  cache: [Hkv, L_cap, d]; returns the updated copy."""
+    out = np.array(cache, copy=True)
+    for t in range(1, len(path)):
+        out[:, L + t] = cache[:, L + path[t]]
+    return out

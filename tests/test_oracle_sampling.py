@@ -1,0 +1,156 @@
+"""Pins for the oracle's contextual penalty, truncation, draw and acceptance
+(CPU only)."""
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import scipy.special
+
+from oracle import ts_oracle as orc
+import ts_synth as syn
+
+GOLD = os.path.join(os.path.dirname(__file__), "golden", "sampling_hand_worked.json")
+
+
+def _gold():
+    with open(GOLD) as f:
+        g = json.load(f)
+    ln = math.log
+    logits = np.array([1.2 * ln(8), ln(4), -ln(2) / 1.2, ln(2), 0.0, -ln(4) / 1.2], dtype=np.float32)
+    return g, logits
+
+
+def test_hand_worked_probabilities_at_root():
+    g, x = _gold()
+    win = orc.penalty_window(g["prior"], [], g["W"])
+    xp = orc.penalised_logits(x, win, g["penalty"], g["temperature"])
+    p = scipy.special.softmax(xp.astype(np.float64))
+    np.testing.assert_allclose(p, g["expected_probabilities_root"], rtol=2e-6)
+
+
+@pytest.mark.parametrize("case", range(8))
+def test_hand_worked_draws(case):
+    g, x = _gold()
+    c = g["draws"][case]
+    tok = orc.sample_node(x, g["prior"], [], g["W"], g["penalty"], g["temperature"],
+                          c["top_p"], c["min_p"], c["u"])
+    assert tok == c["token"]
+
+
+def test_hand_worked_window_slides_along_the_tree_path():
+    g, x = _gold()
+    win = orc.penalty_window(g["prior"], g["depth1_drafted"], g["W"])
+    assert list(win) == [2, 2, 5, 1]
+    xp = orc.penalised_logits(x, win, g["penalty"], g["temperature"])
+    expect = [8 ** 1.2, 4 ** (1 / 1.2), 0.5, 2.0, 1.0, 0.25]
+    np.testing.assert_allclose(np.exp(xp.astype(np.float64)), expect, rtol=2e-6)
+
+
+def test_penalty_direction_and_once_per_token():
+    x = np.array([2.0, -2.0, 0.0, 1.0], dtype=np.float32)
+    xp = orc.penalised_logits(x, [0, 0, 0, 1, 2], 1.2, 1.0)
+    assert xp[0] < 2.0 and abs(xp[0] - 2 / 1.2) < 1e-6      # once, not three times
+    assert xp[1] < -2.0 and abs(xp[1] + 2.4) < 1e-6
+    assert xp[2] == 0.0 and xp[3] == 1.0
+
+
+def test_temperature_scales_logits():
+    rng = np.random.default_rng(1)
+    x = rng.standard_normal(50).astype(np.float32)
+    a = orc.penalised_logits(x, [], 1.2, 2.0)
+    np.testing.assert_allclose(a, x / 2, rtol=1e-7)
+
+
+def test_untruncated_draw_is_the_categorical_distribution():
+    """top_p = 1, min_p = 0: the inverse-CDF draw maps the interval of u of
+    length p_t to token t, so a uniform grid of N values of u hits token t
+    N*p_t times up to one (p from the library softmax)."""
+    rng = np.random.default_rng(2)
+    x = (rng.standard_normal(12) * 1.5).astype(np.float32)
+    p = scipy.special.softmax(x.astype(np.float64))
+    N = 20000
+    counts = np.zeros(12)
+    for n in range(N):
+        counts[orc.sample_from_logits(x, 1.0, 0.0, (n + 0.5) / N)] += 1
+    assert np.all(np.abs(counts - N * p) <= 1.0 + 1e-9)
+
+
+@pytest.mark.parametrize("top_p,min_p", [(1e-9, 0.0), (1.0, 1.0), (0.9, 1.0)])
+def test_degenerate_truncation_is_greedy(top_p, min_p):
+    rng = np.random.default_rng(4)
+    x = rng.standard_normal(300).astype(np.float32)
+    for u in (0.0, 0.3, 0.999):
+        assert orc.sample_from_logits(x, top_p, min_p, u) == int(np.argmax(x))
+
+
+def test_equal_probabilities_rank_by_token_id():
+    x = np.zeros(5, dtype=np.float32)
+    # five equal probabilities 0.2: top-p 0.5 keeps ranks with mass-before < .5 -> ids 0,1,2
+    assert orc.sample_from_logits(x, 0.5, 0.0, 0.99) == 2
+    assert orc.sample_from_logits(x, 0.5, 0.0, 0.0) == 0
+
+
+def _chain(depth, V=50):
+    parents = np.array([-1] + list(range(depth)), dtype=np.int32)
+    toks = np.arange(10, 10 + depth + 1, dtype=np.int32)
+    return parents, toks
+
+
+def test_chain_tree_known_path():
+    parents, toks = _chain(3)
+    V = 50
+    logits = np.zeros((4, V), dtype=np.float32)
+    logits[0, 11] = 40.0    # root predicts node 1's token
+    logits[1, 12] = 40.0    # node 1 predicts node 2's token
+    logits[2, 33] = 40.0    # node 2 predicts something else -> stop at node 2
+    logits[3, 5] = 40.0
+    prior = np.arange(20, 30, dtype=np.int32)
+    prior[-1] = toks[0]
+    u = np.full(4, 0.5, dtype=np.float32)
+    args = (logits, prior, parents, toks, 8, 1.2, 1.0, 0.9, 0.05, u)
+    path, bonus = orc.sample_accept_sequential(*args)
+    assert path == [0, 1, 2] and bonus == 33
+    samp = orc.sample_all_nodes(*args)
+    assert orc.accept_from_samples(parents, toks, samp) == (path, bonus)
+
+
+@pytest.mark.parametrize("wname,seed", [("tiny", 0), ("tiny", 1), ("tiny", 2)])
+def test_parallel_form_equals_sequential_form(wname, seed):
+    w = syn.scaled(syn.WORKLOADS[wname], V=2000, seed=seed)
+    inp = syn.sampling_inputs(w, step=seed)
+    args = (inp["logits"], inp["prior"], inp["parents"], inp["tokens"], w.W, w.penalty,
+            w.temperature, w.top_p, w.min_p, inp["uniforms"])
+    samp = orc.sample_all_nodes(*args)
+    path, bonus = orc.accept_from_samples(inp["parents"], inp["tokens"], samp)
+    assert (path, bonus) == orc.sample_accept_sequential(*args)
+    # invariants: a root path whose every drafted token matches its parent's draw
+    assert path[0] == 0
+    for a, b in zip(path[:-1], path[1:]):
+        assert inp["parents"][b] == a and inp["tokens"][b] == samp[a]
+    assert bonus == samp[path[-1]]
+
+
+def test_deepest_path_ties_go_to_lower_node():
+    parents = np.array([-1, 0, 0, 1, 2], dtype=np.int32)
+    toks = np.array([0, 7, 7, 8, 8], dtype=np.int32)
+    sampled = np.array([7, 8, 8, 1, 2])
+    path, bonus = orc.accept_from_samples(parents, toks, sampled)
+    assert path == [0, 1, 3] and bonus == 1
+
+
+def test_kv_commit_moves_accepted_rows():
+    cache = np.arange(2 * 12 * 3).reshape(2, 12, 3)
+    out = orc.kv_commit(cache, 5, [0, 2, 4])
+    np.testing.assert_array_equal(out[:, 6], cache[:, 7])
+    np.testing.assert_array_equal(out[:, 7], cache[:, 9])
+    np.testing.assert_array_equal(out[:, :6], cache[:, :6])
+
+
+def test_top_p_boundary_is_strict():
+    """Four equal probabilities 0.25, top_p 0.5: mass before rank 2 is
+    exactly 0.5, which is not < 0.5, so only ranks 0 and 1 are kept."""
+    x = np.zeros(4, dtype=np.float32)
+    assert orc.sample_from_logits(x, 0.5, 0.0, 0.99) == 1
+    assert orc.sample_from_logits(x, 0.5000001, 0.0, 0.99) == 2
