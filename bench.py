@@ -1,0 +1,482 @@
+#!/usr/bin/env python3
+"""Benchmark of the TokenSwift per-step decode hot path on one GB300.
+
+A step is one pass of the whole hot path over one batch of synthetic input:
+for every layer, tree verification attention with fused importance
+(ts_verify_attention) and the partial-KV top-B refresh (ts_partial_kv_select_gather);
+then the penalised sampling + tree acceptance of the step
+(ts_penalized_sample_accept) and the KV commit of the accepted path
+(ts_kv_commit).  Every layer has its own K/V buffers, so one step streams
+~13 GB (LLaMA3.1-8B shape, 102,400 cached tokens) -- far more than L2.
+
+metric: algorithmic HBM bytes of the step / step time (GB/s), with decode
+steps/s beside it.  `--impl reference` times the CPU oracle instead.
+
+Run:  python bench.py [--gpus N --steps K --warmup W --workload NAME]
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+# the CPU oracle legs run single-threaded; set before numpy is imported
+for _v in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
+    os.environ.setdefault(_v, "1")
+
+import numpy as np  # noqa: E402
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import ts_synth as syn  # noqa: E402
+
+METRIC = "verify-attn+KV-select HBM GB/s (% of GB300 peak); decode steps/s @100K ctx"
+UNIT = "GB/s"
+
+
+# ---------------------------------------------------------------------------
+# algorithmic bytes (the minimum traffic each call must move)
+# ---------------------------------------------------------------------------
+def verify_bytes(w: syn.Workload) -> int:
+    kv = 2 * 2 * (w.L + w.T) * w.Hkv * w.d          # K and V read once, bf16
+    q = 2 * w.T * w.Hq * w.d                         # queries
+    out = 4 * w.T * w.Hq * w.d + 4 * w.T * w.Hq      # o + lse, fp32
+    imp = 4 * w.L * w.Hkv                            # importance written
+    return kv + q + out + imp
+
+
+def select_bytes(w: syn.Workload) -> int:
+    imp = 4 * w.L * w.Hkv                            # importance read
+    gather = 2 * 2 * 2 * w.N * w.Hkv * w.d           # K,V rows read + written
+    idx = 4 * w.N * w.Hkv
+    return imp + gather + idx
+
+
+def sample_bytes(w: syn.Workload) -> int:
+    return 4 * w.T * w.V + 4 * w.W + 16 * w.T
+
+
+def commit_bytes(w: syn.Workload, n_moved: int = 3) -> int:
+    return 2 * 2 * 2 * n_moved * w.Hkv * w.d
+
+
+def step_bytes(w: syn.Workload) -> int:
+    return w.layers * (verify_bytes(w) + select_bytes(w)) + sample_bytes(w) + commit_bytes(w)
+
+
+# ---------------------------------------------------------------------------
+# measured peaks and profile-derived traffic
+# ---------------------------------------------------------------------------
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+def verify_source_sha1() -> str:
+    h = hashlib.sha1()
+    for name in ("verify_attn.cu", "ts_common.cuh"):
+        with open(os.path.join(ROOT, "self_speculative_ultra_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:12]
+
+
+def profiled_traffic(workload: str):
+    """dram bytes per verify launch from the committed ncu summary, if it was
+    taken on the current kernel source (else None)."""
+    p = os.path.join(ROOT, "profiles", f"verify_attention_{workload}.md")
+    if not os.path.exists(p):
+        return None
+    txt = open(p).read()
+    m = re.search(r"traffic_bytes_per_call:\s*([0-9.eE+]+)\s+source_sha1:\s*([0-9a-f]+)", txt)
+    if not m or m.group(2) != verify_source_sha1():
+        return None
+    return float(m.group(1))
+
+
+# ---------------------------------------------------------------------------
+# clocks sampled during the timed region
+# ---------------------------------------------------------------------------
+class ClockSampler:
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines: list[str] = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except (FileNotFoundError, OSError):
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.thread.join(timeout=2)
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, val in zip(names, f[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# GPU arm
+# ---------------------------------------------------------------------------
+class Step:
+    """Device-resident state of one benchmark replica and its step()."""
+
+    def __init__(self, w: syn.Workload, device, seed: int = 0):
+        import torch
+        import self_speculative_ultra_gb300 as ts
+        self.ts, self.torch, self.w = ts, torch, w
+        dev = self.dev = device
+        g = torch.Generator(device=dev)
+        g.manual_seed(seed)
+        T, Hq, Hkv, d, L = w.T, w.Hq, w.Hkv, w.d, w.L
+        L_cap = L + T
+        self.L, self.L_cap = L, L_cap
+        tree = syn.make_tree(w, np.random.default_rng(seed))
+        self.parents = torch.from_numpy(tree[0]).to(dev)
+        self.tokens = torch.from_numpy(tree[1]).to(dev)
+        self.q, self.k, self.v = [], [], []
+        n_pl = w.planted
+        for layer in range(w.layers):
+            q = torch.randn((T, Hq, d), generator=g, device=dev, dtype=torch.float32)
+            k = torch.randn((Hkv, L_cap, d), generator=g, device=dev, dtype=torch.float32)
+            v = torch.randn((Hkv, L_cap, d), generator=g, device=dev, dtype=torch.float32)
+            # heavy hitters: keys aligned with the group's summed importance queries
+            G = w.G
+            qs = q[T - w.n_imp:].reshape(w.n_imp, Hkv, G, d).sum(dim=(0, 2))
+            qhat = qs / qs.norm(dim=-1, keepdim=True)
+            pos = torch.randint(w.S, L - w.R, (Hkv, n_pl), generator=g, device=dev)
+            xi = torch.randn((Hkv, n_pl, d), generator=g, device=dev)
+            xi = xi / xi.norm(dim=-1, keepdim=True)
+            kk = 0.9 * qhat[:, None, :] + 0.1 * xi
+            kk = (d ** 0.5) * kk / kk.norm(dim=-1, keepdim=True)
+            k.scatter_(1, pos[..., None].expand(-1, -1, d), kk)
+            self.q.append(q.to(torch.bfloat16))
+            self.k.append(k.to(torch.bfloat16))
+            self.v.append(v.to(torch.bfloat16))
+            del q, k, v
+        N = w.N
+        self.imp = [torch.empty((Hkv, L), dtype=torch.float32, device=dev) for _ in range(w.layers)]
+        self.o = [torch.empty((T, Hq, d), dtype=torch.float32, device=dev) for _ in range(w.layers)]
+        self.lse = [torch.empty((T, Hq), dtype=torch.float32, device=dev) for _ in range(w.layers)]
+        self.idx = [torch.empty((Hkv, N), dtype=torch.int32, device=dev) for _ in range(w.layers)]
+        self.kd = [torch.empty((Hkv, N, d), dtype=torch.bfloat16, device=dev) for _ in range(w.layers)]
+        self.vd = [torch.empty((Hkv, N, d), dtype=torch.bfloat16, device=dev) for _ in range(w.layers)]
+        sin = syn.sampling_inputs(w, step=0, tree=tree)
+        self.logits = torch.from_numpy(sin["logits"]).to(dev)
+        self.prior = torch.from_numpy(sin["prior"]).to(dev)
+        self.uniforms = torch.from_numpy(sin["uniforms"]).to(dev)
+        i32 = dict(dtype=torch.int32, device=dev)
+        self.sampled, self.path = torch.empty(T, **i32), torch.empty(T, **i32)
+        self.n_path, self.bonus = torch.empty(1, **i32), torch.empty(1, **i32)
+        self.status = torch.zeros(1, **i32)
+        u8 = dict(dtype=torch.uint8, device=dev)
+        self.ws_v = torch.empty(max(ts.ts_verify_workspace_bytes(T, Hq, Hkv, d, L), 256), **u8)
+        self.ws_s = torch.empty(max(ts.ts_select_workspace_bytes(Hkv, L), 256), **u8)
+        self.ws_p = torch.empty(max(ts.ts_sample_workspace_bytes(T, w.V), 256), **u8)
+        # pinned host copies of the per-step inputs and results (end-to-end leg)
+        self.h_q = [torch.empty_like(x, device="cpu").pin_memory() for x in self.q]
+        tree_rows = lambda x: x[:, L:L + T]  # noqa: E731
+        self.h_ktree = [torch.empty_like(tree_rows(x), device="cpu").pin_memory() for x in self.k]
+        self.h_vtree = [torch.empty_like(tree_rows(x), device="cpu").pin_memory() for x in self.v]
+        for a, b in zip(self.h_q, self.q):
+            a.copy_(b)
+        for a, b in zip(self.h_ktree, self.k):
+            a.copy_(tree_rows(b))
+        for a, b in zip(self.h_vtree, self.v):
+            a.copy_(tree_rows(b))
+        self.h_logits = self.logits.cpu().pin_memory()
+        self.h_small = torch.cat([self.parents, self.tokens, self.prior,
+                                  self.uniforms.view(torch.int32)]).cpu().pin_memory()
+        self.h_out = torch.empty(T + 2, dtype=torch.int32).pin_memory()
+        self.v_events = None
+        torch.cuda.synchronize()
+
+    def h2d_bytes(self) -> int:
+        n = sum(x.numel() * x.element_size() for x in self.h_q)
+        n += sum(x.numel() * x.element_size() for x in self.h_ktree + self.h_vtree)
+        n += self.h_logits.numel() * 4 + self.h_small.numel() * 4
+        return n
+
+    def d2h_bytes(self) -> int:
+        return self.h_out.numel() * 4
+
+    def upload_inputs(self):
+        w, L, T = self.w, self.L, self.w.T
+        for layer in range(w.layers):
+            self.q[layer].copy_(self.h_q[layer], non_blocking=True)
+            self.k[layer][:, L:L + T].copy_(self.h_ktree[layer], non_blocking=True)
+            self.v[layer][:, L:L + T].copy_(self.h_vtree[layer], non_blocking=True)
+        self.logits.copy_(self.h_logits, non_blocking=True)
+        small = self.h_small.to(self.dev, non_blocking=True)
+        n = T
+        self.parents.copy_(small[:n])
+        self.tokens.copy_(small[n:2 * n])
+        self.prior.copy_(small[2 * n:2 * n + self.prior.numel()])
+        self.uniforms.copy_(small[2 * n + self.prior.numel():].view(self.torch.float32))
+
+    def download_result(self):
+        self.h_out[:self.w.T].copy_(self.path, non_blocking=True)
+        self.h_out[self.w.T:self.w.T + 1].copy_(self.n_path, non_blocking=True)
+        self.h_out[self.w.T + 1:].copy_(self.bonus, non_blocking=True)
+
+    def step(self, events=None):
+        ts, w = self.ts, self.w
+        for layer in range(w.layers):
+            if events is not None:
+                events[layer][0].record()
+            ts.ts_verify_attention(self.q[layer], self.k[layer], self.v[layer], self.L, self.parents,
+                                   n_imp=w.n_imp, o=self.o[layer], lse=self.lse[layer],
+                                   imp=self.imp[layer], workspace=self.ws_v, status=self.status)
+            if events is not None:
+                events[layer][1].record()
+            ts.ts_partial_kv_select_gather(self.imp[layer], self.k[layer], self.v[layer], self.L,
+                                           w.B, w.S, w.R, idx=self.idx[layer], kd=self.kd[layer],
+                                           vd=self.vd[layer], workspace=self.ws_s,
+                                           status=self.status)
+        ts.ts_penalized_sample_accept(self.logits, self.tokens, self.parents, self.prior, w.W,
+                                      w.penalty, w.temperature, w.top_p, w.min_p, self.uniforms,
+                                      sampled=self.sampled, path=self.path, n_path=self.n_path,
+                                      bonus=self.bonus, workspace=self.ws_p, status=self.status)
+        ts.ts_kv_commit(self.k[0], self.v[0], self.L, w.T, self.path, self.n_path,
+                        status=self.status)
+
+    def launches_per_step(self) -> int:
+        # verify: split kernel + merge; select: threshold + gather; sample; commit
+        return self.w.layers * 4 + 2
+
+
+def run_gpu(args, w: syn.Workload):
+    import torch
+    import torch.distributed as dist
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    import self_speculative_ultra_gb300 as ts
+    ts.build()
+    st = Step(w, dev, seed=rank)
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    for _ in range(args.warmup):
+        st.step()
+    barrier()
+    # device-timed region: inputs resident in HBM
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(w.layers)]
+    clocks = ClockSampler(local)
+    clocks.start()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    barrier()
+    t0.record()
+    for _ in range(args.steps):
+        st.step(events=ev)      # the last step's per-layer verify events are read below
+    t1.record()
+    barrier()
+    clk = clocks.stop()
+    ms_total = t0.elapsed_time(t1)
+    # verify-call durations of the last timed step (events are re-recorded each step)
+    ver_ms = [ev[i][0].elapsed_time(ev[i][1]) for i in range(w.layers)]
+    ms = torch.tensor([ms_total], device=dev)
+    if world > 1:
+        dist.all_reduce(ms, op=dist.ReduceOp.MAX)
+    ms_step = float(ms.item()) / args.steps
+
+    # end-to-end leg: pinned host inputs in, result out, every step
+    for _ in range(2):
+        st.upload_inputs()
+        st.step()
+        st.download_result()
+    barrier()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(args.steps):
+        st.upload_inputs()
+        st.step()
+        st.download_result()
+    e1.record()
+    barrier()
+    e2e_ms = torch.tensor([e0.elapsed_time(e1) / args.steps], device=dev)
+    if world > 1:
+        dist.all_reduce(e2e_ms, op=dist.ReduceOp.MAX)
+    e2e_ms = float(e2e_ms.item())
+    status = int(st.status.item())
+
+    if rank == 0:
+        peak, peak_kind = load_peaks()
+        sb = step_bytes(w)
+        value = world * sb / (ms_step * 1e-3) / 1e9
+        vb = verify_bytes(w)
+        v_avg_ms = statistics.mean(ver_ms)
+        achieved = vb / (v_avg_ms * 1e-3) / 1e9
+        traffic = profiled_traffic(w.name)
+        line = {
+            "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 4),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic (seeded N(0,1) bf16 K/V with planted heavy hitters, "
+                    "N(0,9) fp32 logits)",
+            "config": {"workload": w.name, "layers": w.layers, "Hq": w.Hq, "Hkv": w.Hkv,
+                       "d": w.d, "L": w.L, "tree_nodes": w.T, "budget_B": w.B, "sinks": w.S,
+                       "recent": w.R, "vocab": w.V, "penalty_window": w.W,
+                       "bytes_per_step": sb, "l2": "inputs larger than L2 (distinct K/V per layer, "
+                                                   f"{sb / 1e9:.1f} GB per step)",
+                       "parallelism": f"replicas x{world}"},
+            "steps_per_s": round(world / (ms_step * 1e-3), 2),
+            "pct_of_hbm_peak": round(100 * value / world / peak, 2),
+            "roofline": {"bound": "hbm", "kernel": "ts_verify_attention (split + merge)",
+                         "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                         "frac": round(achieved / peak, 4), "traffic": traffic,
+                         "peak_source": peak_kind,
+                         "bytes_per_call": vb, "avg_call_ms": round(v_avg_ms, 4)},
+            "e2e": {"value": round(world * sb / (e2e_ms * 1e-3) / 1e9, 2), "unit": UNIT,
+                    "h2d_bytes_per_step": st.h2d_bytes(), "d2h_bytes_per_step": st.d2h_bytes(),
+                    "ms_per_step": round(e2e_ms, 4)},
+            "gpu_launches": st.launches_per_step() * args.steps,
+            "clocks": clk,
+            "device_status": status,
+        }
+        if not args.no_cpu_baseline:
+            line["cpu_baseline"] = cpu_baseline(w)
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle legs
+# ---------------------------------------------------------------------------
+def _oracle_layer_unit(w: syn.Workload, heads: int, sample_nodes: int, seed: int = 0):
+    """Time the oracle on `heads` KV heads of one layer (verify + select +
+    gather) and `sample_nodes` tree nodes of the sampling step.  Returns
+    (seconds, algorithmic bytes processed)."""
+    from oracle import ts_oracle as orc
+    sub = syn.scaled(w, Hkv=heads, Hq=heads * w.G)
+    inp = syn.attention_inputs(sub, layer=seed)
+    sin = syn.sampling_inputs(w, step=seed)
+    q, k, v = (orc.bf16_to_f64(inp[n]) for n in ("q", "k", "v"))
+    t = time.perf_counter()
+    _, _, imp = orc.verify_attention(q, k, v, sub.L, inp["parents"], sub.n_imp)
+    for h in range(heads):
+        idx = orc.select_partial(imp[h].astype(np.float32), sub.L, sub.B, sub.S, sub.R)
+        orc.gather_rows(inp["k"][h], idx)
+        orc.gather_rows(inp["v"][h], idx)
+    paths = orc.root_paths(sin["parents"])
+    for i in range(sample_nodes):
+        drafted = [int(sin["tokens"][a]) for a in paths[i][1:]]
+        orc.sample_node(sin["logits"][i], sin["prior"], drafted, w.W, w.penalty, w.temperature,
+                        w.top_p, w.min_p, float(sin["uniforms"][i]))
+    secs = time.perf_counter() - t
+    nbytes = verify_bytes(sub) + select_bytes(sub) + sample_nodes * 4 * w.V
+    return secs, nbytes
+
+
+def cpu_baseline(w: syn.Workload):
+    heads, nodes = min(w.Hkv, 4), 16
+    secs, nbytes = _oracle_layer_unit(w, heads=heads, sample_nodes=nodes)
+    return {"value": round(nbytes / secs / 1e9, 4), "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"fp64 numpy oracle, 1 thread: verify+select+gather of {heads} of {w.Hkv} "
+                      f"KV heads of one layer + {nodes} of {w.T} node draws "
+                      f"({nbytes / 1e6:.1f} MB of algorithmic traffic in {secs:.1f} s)"}
+
+
+def run_reference(args, w: syn.Workload):
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    if rank != 0:
+        return
+    for i in range(args.warmup):
+        _oracle_layer_unit(w, heads=1, sample_nodes=1, seed=100 + i)
+    tot_s, tot_b = 0.0, 0
+    for i in range(args.steps):
+        s, b = _oracle_layer_unit(w, heads=1, sample_nodes=1, seed=i)
+        tot_s += s
+        tot_b += b
+    value = tot_b / tot_s / 1e9
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": UNIT,
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(1e3 * tot_s / args.steps, 2), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name},
+        "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": 1, "kind": "oracle",
+                         "sample": f"each step: verify+select+gather of 1 of {w.Hkv} KV heads "
+                                   f"of one layer + 1 node draw, fp64 numpy, 1 thread"},
+        "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="gpu", choices=["gpu", "reference"])
+    ap.add_argument("--workload", default="llama3.1-8b", choices=sorted(syn.WORKLOADS))
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    w = syn.WORKLOADS[args.workload]
+    if args.impl == "reference":
+        run_reference(args, w)
+    else:
+        run_gpu(args, w)
+
+
+if __name__ == "__main__":
+    main()

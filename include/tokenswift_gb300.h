@@ -1,0 +1,174 @@
+/*
+ * tokenswift_gb300.h — C ABI of the GB300 (sm_103a) per-step decode hot path of
+ * TokenSwift-style lossless ultra-long generation.
+ *
+ * Source method: "TokenSwift: Lossless Acceleration of Ultra Long Sequence
+ * Generation" (Wu, Shen, Jia, Wang, Zheng; ICML 2025).  One decoding step
+ * drafts with a partial KV cache, verifies the draft tree with the full KV
+ * cache, samples with a contextual penalty and accepts the longest exactly
+ * matching draft, then updates the KV cache (§3.1 Overview, Figure 2).
+ *
+ * Conventions shared by every call:
+ *   - Every tensor pointer is a DEVICE pointer owned by the caller, unless a
+ *     parameter says "host".  Tensors are dense row-major in the layout given.
+ *     bf16 tensors are passed as `const void*` holding IEEE bfloat16 values.
+ *   - The library allocates no device memory.  Scratch space is a caller
+ *     buffer (`workspace`, 256-byte aligned) of at least the size reported by
+ *     the matching *_workspace_bytes() query.
+ *   - Every call only enqueues work on `stream` (a cudaStream_t; NULL = the
+ *     legacy default stream) and returns without synchronising.
+ *   - Return value: TS_OK, or a ts_status code for arguments rejected on the
+ *     host before anything was enqueued (a message is then available from
+ *     ts_last_error(), per calling thread), or TS_ERR_CUDA if a launch failed.
+ *   - `status` is an optional (may be NULL) device int32 the caller zeroes;
+ *     kernels write a nonzero ts_status into it when they meet bad device-side
+ *     data (a parent index or token id out of range) or a bounded wait that
+ *     ran out.  They never trap.  Read it after synchronising the stream.
+ *   - Limits: 1 <= T <= 64 tree nodes (parents[0] = -1, parents[i] < i);
+ *     Hq % Hkv == 0; d in {64, 128}; T*Hq/Hkv <= 512; vocabulary V <= 262144.
+ *   - Concurrent calls that share a workspace buffer race; give each stream
+ *     its own workspace.
+ */
+#ifndef TOKENSWIFT_GB300_H
+#define TOKENSWIFT_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum ts_status {
+  TS_OK = 0,
+  TS_ERR_INVALID_ARG = 1,  /* argument out of its documented domain        */
+  TS_ERR_UNSUPPORTED = 2,  /* valid but outside this build's limits        */
+  TS_ERR_CUDA = 3,         /* a CUDA launch or runtime call failed          */
+  TS_ERR_TIMEOUT = 4,      /* a bounded device-side wait ran out            */
+  TS_ERR_WORKSPACE = 5     /* workspace missing, too small or misaligned    */
+} ts_status;
+
+/* Static description of a status code. */
+const char* ts_status_string(int status);
+/* Message of the last failed call on this thread ("" if none). */
+const char* ts_last_error(void);
+/* Library ABI version (major*100 + minor). */
+int ts_version(void);
+
+/* ------------------------------------------------------------------------
+ * (1) Tree verification attention + attention importance.
+ *
+ * §3.1 Overview: the target model verifies the draft with the FULL KV cache;
+ * §E Tree-Based Attention: each tree token attends only to its predecessors;
+ * §3.3 Dynamic KV Cache Management: importance of a cached pair is the
+ * query-key dot product, with GQA query heads partitioned per KV head and
+ * their scores aggregated.
+ *
+ * For tree node i, query head h, KV head kv = h / (Hq/Hkv):
+ *   s_j = q[i,h,:] . k[kv,j,:] / sqrt(d) over j in [0, L) and j = L + a for
+ *   every node a on the root path of i (i itself included);
+ *   o[i,h,:] = softmax_j(s) . v[kv,j,:]  (fp32),
+ *   lse[i,h] = ln sum_j exp(s_j)          (fp32),
+ *   imp[kv,j] = sum over the last n_imp nodes i and the heads h of group kv
+ *               of s_{i,h,j}, for j in [0, L)   (fp32).
+ *
+ * q       [T, Hq, d] bf16 (post-RoPE tree queries)
+ * k, v    [Hkv, L_cap, d] bf16; rows [0,L) = committed cache, rows
+ *         [L, L+T) = the tree tokens' own keys/values.  L + T <= L_cap.
+ * parents [T] int32, device; parents[0] = -1, 0 <= parents[i] < i.
+ * n_imp   number of trailing tree queries used for importance (<= 0: all T).
+ * o       [T, Hq, d] fp32 out.   lse [T, Hq] fp32 out, or NULL.
+ * imp     [Hkv, L] fp32 out, or NULL to skip importance.
+ * workspace >= ts_verify_workspace_bytes(T, Hq, Hkv, d, L).
+ * ------------------------------------------------------------------------ */
+size_t ts_verify_workspace_bytes(int T, int Hq, int Hkv, int d, int64_t L);
+int ts_verify_attention(const void* q, const void* k, const void* v,
+                        int64_t L, int64_t L_cap, const int32_t* parents,
+                        int T, int Hq, int Hkv, int d, int n_imp,
+                        float* o, float* lse, float* imp,
+                        void* workspace, size_t workspace_bytes,
+                        int32_t* status, void* stream);
+
+/* ------------------------------------------------------------------------
+ * (2) Dynamic partial KV cache: top-B selection and gather.
+ *
+ * §3.3 Dynamic KV Cache Management: a fixed budget; the initial |S| pairs are
+ * preserved and less important pairs are replaced; §3.1: the partial cache is
+ * what drafting attends to.
+ *
+ * Per KV head: if L <= S+B+R every position is kept; otherwise the kept set
+ * is [0,S) (sinks) + [L-R, L) (recent) + the B best positions of [S, L-R)
+ * ranked by (imp desc, position asc).  The N = min(L, S+B+R) kept positions
+ * are written in ascending order to idx[kv, 0:N] and their K/V rows are
+ * copied bit for bit into kd/vd[kv, 0:N, :].
+ *
+ * imp     [Hkv, L] fp32 (typically from ts_verify_attention)
+ * k, v    [Hkv, L_cap, d] bf16 full cache
+ * idx     [Hkv, N] int32 out;  kd, vd [Hkv, N, d] bf16 out
+ * n_out   HOST int64 out (may be NULL): N
+ * workspace >= ts_select_workspace_bytes(Hkv, L).
+ * ------------------------------------------------------------------------ */
+size_t ts_select_workspace_bytes(int Hkv, int64_t L);
+int ts_partial_kv_select_gather(const float* imp, const void* k, const void* v,
+                                int64_t L, int64_t L_cap, int Hkv, int d,
+                                int B, int S, int R,
+                                int32_t* idx, void* kd, void* vd, int64_t* n_out,
+                                void* workspace, size_t workspace_bytes,
+                                int32_t* status, void* stream);
+
+/* ------------------------------------------------------------------------
+ * (3) Contextual-penalty sampling and exact-match tree acceptance.
+ *
+ * §3.4 Contextual Penalty: penalise the most recent W tokens; §D.1: top-p
+ * keeps the smallest set of tokens whose probability mass reaches top_p,
+ * min-p keeps tokens with p >= min_p * p_max; Table 11 sets penalty 1.2,
+ * window 1024, temperature 1.0, top-p 0.9, min-p 0.05; §3.1: the longest
+ * draft that matches the target's own tokens is accepted.
+ *
+ * For every node i (in parallel): the window is the last W tokens of
+ * (prior[0:n_prior] followed by the drafted tokens on the root path of i,
+ * root excluded); each distinct windowed token t gets x_t/penalty if x_t > 0,
+ * else x_t*penalty; all logits are divided by temperature; p = softmax;
+ * tokens ranked by (p desc, id asc); rank r is kept iff the mass of the ranks
+ * before it is < top_p AND p >= min_p * p_max (rank 0 always kept); the draw
+ * is the first kept rank whose cumulative kept mass exceeds uniforms[i] times
+ * the kept mass.  sampled[i] receives it.
+ * Acceptance: root accepted; node c accepted iff its parent is accepted and
+ * tree_tokens[c] == sampled[parents[c]]; the deepest accepted node (ties to
+ * the lower index) gives path[0:n_path] (root first) and bonus = its sample.
+ *
+ * logits [T, V] fp32; tree_tokens [T] int32 (tree_tokens[0] = root token,
+ * which is also prior[n_prior-1]); parents [T]; prior [n_prior] int32;
+ * uniforms [T] fp32 in [0,1); sampled [T] int32 out; path [T] int32 out;
+ * n_path [1] int32 out; bonus [1] int32 out.  All device pointers.
+ * temperature > 0, penalty > 0, 0 < top_p, 0 <= min_p.
+ * workspace >= ts_sample_workspace_bytes(T, V).
+ * ------------------------------------------------------------------------ */
+size_t ts_sample_workspace_bytes(int T, int V);
+int ts_penalized_sample_accept(const float* logits, const int32_t* tree_tokens,
+                               const int32_t* parents, int T,
+                               const int32_t* prior, int n_prior, int W, int V,
+                               float penalty, float temperature, float top_p, float min_p,
+                               const float* uniforms,
+                               int32_t* sampled, int32_t* path, int32_t* n_path,
+                               int32_t* bonus,
+                               void* workspace, size_t workspace_bytes,
+                               int32_t* status, void* stream);
+
+/* ------------------------------------------------------------------------
+ * (4) KV commit of the accepted path.
+ *
+ * §3.1: after verification the KV cache is updated with the accepted draft.
+ * For t = 1 .. n_path-1: row L + path[t] of every KV head is copied to row
+ * L + t (the root's row is already at L), in k and v, in place.  path and
+ * n_path are device arrays as written by ts_penalized_sample_accept, so no
+ * host synchronisation is needed between the two calls.  1 <= n_path <= T.
+ * ------------------------------------------------------------------------ */
+int ts_kv_commit(void* k, void* v, int64_t L, int64_t L_cap, int Hkv, int d, int T,
+                 const int32_t* path, const int32_t* n_path,
+                 int32_t* status, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* TOKENSWIFT_GB300_H */

@@ -113,15 +113,19 @@ def verify_attention(q, k, v, L: int, parents, n_imp: int = 0):
         kv = h // G
         # scores of every tree query of head h against the committed cache
         s_cache = (q[:, h, :] @ k[kv, :L, :].T) * scale           # [T, L]
+        # scores against the tree rows each node may see (its root path)
+        s_tree = [(k[kv, [L + a for a in paths[i]], :] @ q[i, h, :]) * scale for i in range(T)]
+        m = np.array([max(s_cache[i].max() if L > 0 else -np.inf, s_tree[i].max())
+                      for i in range(T)])                          # row maxima
+        w_cache = np.exp(s_cache - m[:, None])                     # [T, L]
+        num = w_cache @ v[kv, :L, :]                               # [T, d]
+        Z = w_cache.sum(axis=1)
         for i in range(T):
-            tree_rows = [L + a for a in paths[i]]
-            s_tree = (k[kv, tree_rows, :] @ q[i, h, :]) * scale     # [depth+1]
-            m = max(s_cache[i].max() if L > 0 else -np.inf, s_tree.max())
-            w_cache = np.exp(s_cache[i] - m)
-            w_tree = np.exp(s_tree - m)
-            Z = w_cache.sum() + w_tree.sum()
-            O[i, h] = (w_cache @ v[kv, :L, :] + w_tree @ v[kv, tree_rows, :]) / Z
-            LSE[i, h] = m + np.log(Z)
+            w_tree = np.exp(s_tree[i] - m[i])
+            num[i] += w_tree @ v[kv, [L + a for a in paths[i]], :]
+            Z[i] += w_tree.sum()
+        O[:, h, :] = num / Z[:, None]
+        LSE[:, h] = m + np.log(Z)
         for i in range(T - n_imp, T):
             imp[kv] += s_cache[i]
     return O, LSE, imp

@@ -1,0 +1,220 @@
+"""GB300 (sm_103a) decode hot path of TokenSwift-style ultra-long generation.
+
+Thin Python binding over the C-ABI library libtokenswift_gb300.so (see
+include/tokenswift_gb300.h).  The functions carry the C names and only
+marshal arguments: torch tensors supply device memory and the current CUDA
+stream; every step of the computation runs in the library's CUDA kernels.
+There is no CPU fallback: if the library is missing, every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+from ._build import LIB_PATH, build  # noqa: F401
+
+__all__ = [
+    "TsError", "lib", "build", "ts_status_string", "ts_last_error", "ts_version",
+    "ts_verify_workspace_bytes", "ts_verify_attention",
+    "ts_select_workspace_bytes", "ts_partial_kv_select_gather",
+    "ts_sample_workspace_bytes", "ts_penalized_sample_accept", "ts_kv_commit",
+]
+
+TS_OK, TS_ERR_INVALID_ARG, TS_ERR_UNSUPPORTED, TS_ERR_CUDA, TS_ERR_TIMEOUT, TS_ERR_WORKSPACE = range(6)
+
+_c_void_p, _i32, _i64, _sz, _f32 = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_size_t, ctypes.c_float
+
+_SIGNATURES = {
+    "ts_status_string": (ctypes.c_char_p, [_i32]),
+    "ts_last_error": (ctypes.c_char_p, []),
+    "ts_version": (_i32, []),
+    "ts_verify_workspace_bytes": (_sz, [_i32, _i32, _i32, _i32, _i64]),
+    "ts_verify_attention": (_i32, [_c_void_p, _c_void_p, _c_void_p, _i64, _i64, _c_void_p,
+                                   _i32, _i32, _i32, _i32, _i32, _c_void_p, _c_void_p, _c_void_p,
+                                   _c_void_p, _sz, _c_void_p, _c_void_p]),
+    "ts_select_workspace_bytes": (_sz, [_i32, _i64]),
+    "ts_partial_kv_select_gather": (_i32, [_c_void_p, _c_void_p, _c_void_p, _i64, _i64, _i32, _i32,
+                                           _i32, _i32, _i32, _c_void_p, _c_void_p, _c_void_p,
+                                           ctypes.POINTER(_i64), _c_void_p, _sz, _c_void_p,
+                                           _c_void_p]),
+    "ts_sample_workspace_bytes": (_sz, [_i32, _i32]),
+    "ts_penalized_sample_accept": (_i32, [_c_void_p, _c_void_p, _c_void_p, _i32, _c_void_p, _i32,
+                                          _i32, _i32, _f32, _f32, _f32, _f32, _c_void_p,
+                                          _c_void_p, _c_void_p, _c_void_p, _c_void_p,
+                                          _c_void_p, _sz, _c_void_p, _c_void_p]),
+    "ts_kv_commit": (_i32, [_c_void_p, _c_void_p, _i64, _i64, _i32, _i32, _i32, _c_void_p,
+                            _c_void_p, _c_void_p, _c_void_p]),
+}
+
+_LIB = None
+
+
+class TsError(RuntimeError):
+    def __init__(self, code: int, msg: str):
+        super().__init__(f"[{code}] {msg}")
+        self.code = code
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded library; raises if it has not been built."""
+    global _LIB
+    if _LIB is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{os.path.basename(LIB_PATH)} is not built: call "
+                               "self_speculative_ultra_gb300.build() first")
+        h = ctypes.CDLL(LIB_PATH)
+        for name, (res, args) in _SIGNATURES.items():
+            fn = getattr(h, name)
+            fn.restype = res
+            fn.argtypes = args
+        _LIB = h
+    return _LIB
+
+
+def ts_status_string(code: int) -> str:
+    return lib().ts_status_string(code).decode()
+
+
+def ts_last_error() -> str:
+    return lib().ts_last_error().decode()
+
+
+def ts_version() -> int:
+    return lib().ts_version()
+
+
+def _check(rc: int):
+    if rc != TS_OK:
+        raise TsError(rc, f"{ts_status_string(rc)}: {ts_last_error()}")
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _dev(t, dtype, name, shape=None):
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+    return t
+
+
+def _stream(stream):
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _workspace(nbytes, device, workspace):
+    if nbytes == 0:
+        return None, 0
+    if workspace is None:
+        workspace = torch.empty(nbytes, dtype=torch.uint8, device=device)
+    if workspace.numel() * workspace.element_size() < nbytes:
+        raise ValueError(f"workspace too small: {nbytes} bytes needed")
+    return workspace, workspace.numel() * workspace.element_size()
+
+
+def ts_verify_workspace_bytes(T, Hq, Hkv, d, L) -> int:
+    return lib().ts_verify_workspace_bytes(T, Hq, Hkv, d, L)
+
+
+def ts_verify_attention(q, k, v, L, parents, n_imp=0, o=None, lse=None, imp=None,
+                        want_lse=True, want_imp=True, workspace=None, status=None, stream=None):
+    """Tree verification attention + importance.  q [T,Hq,d] bf16, k/v
+    [Hkv,L_cap,d] bf16, parents [T] int32.  Returns (o, lse, imp)."""
+    T, Hq, d = q.shape
+    Hkv, L_cap = k.shape[0], k.shape[1]
+    _dev(q, torch.bfloat16, "q")
+    _dev(k, torch.bfloat16, "k", (Hkv, L_cap, d))
+    _dev(v, torch.bfloat16, "v", (Hkv, L_cap, d))
+    _dev(parents, torch.int32, "parents", (T,))
+    dev = q.device
+    if o is None:
+        o = torch.empty((T, Hq, d), dtype=torch.float32, device=dev)
+    if lse is None and want_lse:
+        lse = torch.empty((T, Hq), dtype=torch.float32, device=dev)
+    if imp is None and want_imp:
+        imp = torch.empty((Hkv, L), dtype=torch.float32, device=dev)
+    ws, nb = _workspace(ts_verify_workspace_bytes(T, Hq, Hkv, d, L), dev, workspace)
+    rc = lib().ts_verify_attention(_ptr(q), _ptr(k), _ptr(v), L, L_cap, _ptr(parents), T, Hq, Hkv,
+                                   d, n_imp, _ptr(o), _ptr(lse), _ptr(imp), _ptr(ws), nb,
+                                   _ptr(status), _stream(stream))
+    _check(rc)
+    return o, lse, imp
+
+
+def ts_select_workspace_bytes(Hkv, L) -> int:
+    return lib().ts_select_workspace_bytes(Hkv, L)
+
+
+def ts_partial_kv_select_gather(imp, k, v, L, B, S, R, idx=None, kd=None, vd=None,
+                                workspace=None, status=None, stream=None):
+    """Top-B + sinks + recent selection and gather.  Returns (idx, kd, vd)."""
+    Hkv, L_cap, d = k.shape
+    _dev(imp, torch.float32, "imp", (Hkv, L))
+    _dev(k, torch.bfloat16, "k")
+    _dev(v, torch.bfloat16, "v", (Hkv, L_cap, d))
+    N = min(L, S + B + R)
+    dev = k.device
+    if idx is None:
+        idx = torch.empty((Hkv, N), dtype=torch.int32, device=dev)
+    if kd is None:
+        kd = torch.empty((Hkv, N, d), dtype=torch.bfloat16, device=dev)
+    if vd is None:
+        vd = torch.empty((Hkv, N, d), dtype=torch.bfloat16, device=dev)
+    ws, nb = _workspace(ts_select_workspace_bytes(Hkv, L), dev, workspace)
+    n_out = _i64(0)
+    rc = lib().ts_partial_kv_select_gather(_ptr(imp), _ptr(k), _ptr(v), L, L_cap, Hkv, d, B, S, R,
+                                           _ptr(idx), _ptr(kd), _ptr(vd), ctypes.byref(n_out),
+                                           _ptr(ws), nb, _ptr(status), _stream(stream))
+    _check(rc)
+    assert n_out.value == N
+    return idx, kd, vd
+
+
+def ts_sample_workspace_bytes(T, V) -> int:
+    return lib().ts_sample_workspace_bytes(T, V)
+
+
+def ts_penalized_sample_accept(logits, tree_tokens, parents, prior, W, penalty, temperature,
+                               top_p, min_p, uniforms, sampled=None, path=None, n_path=None,
+                               bonus=None, workspace=None, status=None, stream=None):
+    """Penalised top-p/min-p draw at every node + exact-match acceptance.
+    Returns (sampled [T], path [T], n_path [1], bonus [1]) device int32."""
+    T, V = logits.shape
+    _dev(logits, torch.float32, "logits")
+    _dev(tree_tokens, torch.int32, "tree_tokens", (T,))
+    _dev(parents, torch.int32, "parents", (T,))
+    _dev(prior, torch.int32, "prior")
+    _dev(uniforms, torch.float32, "uniforms", (T,))
+    dev = logits.device
+    mk = lambda n: torch.empty(n, dtype=torch.int32, device=dev)  # noqa: E731
+    sampled = mk(T) if sampled is None else sampled
+    path = mk(T) if path is None else path
+    n_path = mk(1) if n_path is None else n_path
+    bonus = mk(1) if bonus is None else bonus
+    ws, nb = _workspace(ts_sample_workspace_bytes(T, V), dev, workspace)
+    rc = lib().ts_penalized_sample_accept(_ptr(logits), _ptr(tree_tokens), _ptr(parents), T,
+                                          _ptr(prior), prior.numel(), W, V, penalty, temperature,
+                                          top_p, min_p, _ptr(uniforms), _ptr(sampled), _ptr(path),
+                                          _ptr(n_path), _ptr(bonus), _ptr(ws), nb, _ptr(status),
+                                          _stream(stream))
+    _check(rc)
+    return sampled, path, n_path, bonus
+
+
+def ts_kv_commit(k, v, L, T, path, n_path, status=None, stream=None):
+    """Move the accepted tree rows L+path[t] to L+t (in place)."""
+    Hkv, L_cap, d = k.shape
+    _dev(k, torch.bfloat16, "k")
+    _dev(v, torch.bfloat16, "v", (Hkv, L_cap, d))
+    rc = lib().ts_kv_commit(_ptr(k), _ptr(v), L, L_cap, Hkv, d, T, _ptr(path), _ptr(n_path),
+                            _ptr(status), _stream(stream))
+    _check(rc)

@@ -1,0 +1,399 @@
+// Contextual-penalty sampling of every draft-tree node, exact-match tree
+// acceptance, and the KV commit of the accepted path.
+//
+// "TokenSwift: Lossless Acceleration of Ultra Long Sequence Generation":
+// §3.4 Contextual Penalty (penalty on the most recent W tokens), §D.1
+// (top-p: smallest set whose probability mass reaches p; min-p: tokens with
+// p >= p_base * p_max), Table 11 (penalty 1.2 over 1024 tokens, temperature
+// 1.0, top-p 0.9, min-p 0.05), §3.1 Overview (exact-match verification, the
+// longest valid draft is kept, then the KV cache is updated).
+//
+// One CTA per tree node.  The node's window is marked in a shared-memory
+// bitmap, the penalised/tempered logits x' are written once to the
+// workspace, and e_t = exp(x'_t - max x') gives the unnormalised
+// probabilities.  In rank order (x' desc, id asc) both truncations keep a
+// prefix: top-p keeps ranks up to the first whose inclusive mass reaches
+// top_p * Z, min-p keeps the ranks with e >= min_p.  "First rank whose
+// inclusive mass crosses a target" is found without sorting by a radix
+// descent over the 50-bit key (x' key, reversed id) that carries a
+// (count, mass) histogram per digit: 3 levels on the fp32 key, 2 on the id.
+// The last CTA to finish walks the tree and writes the accepted path.
+#include "ts_common.cuh"
+
+namespace ts {
+
+namespace {
+
+constexpr int kThreads = 1024;
+constexpr int kMaxBuckets = 2048;
+constexpr uint32_t kIdMask = 0x3FFFFu;   // V <= 2^18
+
+enum FindMode { kMassGE = 0, kMassGT = 1, kRank = 2 };
+
+struct Found {
+  int id;
+  int rank;        // number of tokens ranked before it
+  float cum_incl;  // sum of e over ranks <= its rank
+};
+
+struct SampleSmem {
+  int cnt[kMaxBuckets];
+  float mass[kMaxBuckets];
+  float red_f[32];
+  int red_i[32];
+  uint32_t kpre, kmask, ipre, imask;
+  float mb;     // mass ranked before the current bucket range
+  int cb;       // count ranked before the current bucket range
+  int32_t ptok[64];
+  int plen;
+  int last;
+};
+
+__device__ float block_max(float v, SampleSmem& sm) {
+  v = warp_max(v);
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  if (lane == 0) sm.red_f[w] = v;
+  __syncthreads();
+  float r = lane < (int)(blockDim.x >> 5) ? sm.red_f[lane] : -INFINITY;
+  r = warp_max(r);
+  __syncthreads();
+  return r;
+}
+__device__ float block_sum(float v, SampleSmem& sm) {
+  v = warp_sum(v);
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  if (lane == 0) sm.red_f[w] = v;
+  __syncthreads();
+  float r = lane < (int)(blockDim.x >> 5) ? sm.red_f[lane] : 0.f;
+  r = warp_sum(r);
+  __syncthreads();
+  return r;
+}
+__device__ int block_sum_int(int v, SampleSmem& sm) {
+  v = warp_sum_int(v);
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  if (lane == 0) sm.red_i[w] = v;
+  __syncthreads();
+  int r = lane < (int)(blockDim.x >> 5) ? sm.red_i[lane] : 0;
+  r = warp_sum_int(r);
+  __syncthreads();
+  return r;
+}
+
+// One radix level: histogram the tokens matching the digits fixed so far,
+// then (warp 0) pick the bucket holding the target and fold the buckets
+// ranked above it into (mb, cb).  Returns nothing; updates the prefixes.
+__device__ void radix_level(const float* __restrict__ xs, int V, float xmax, int mode,
+                            float target_mass, int target_rank, bool on_id, int shift, int bits,
+                            SampleSmem& sm) {
+  const int nb = 1 << bits;
+  for (int b = threadIdx.x; b < nb; b += blockDim.x) {
+    sm.cnt[b] = 0;
+    sm.mass[b] = 0.f;
+  }
+  __syncthreads();
+  const uint32_t kpre = sm.kpre, kmask = sm.kmask, ipre = sm.ipre, imask = sm.imask;
+  for (int t = threadIdx.x; t < V; t += blockDim.x) {
+    const float x = xs[t];
+    const uint32_t key = float_key(x), rid = kIdMask - (uint32_t)t;
+    if ((key & kmask) != kpre || (rid & imask) != ipre) continue;
+    const uint32_t dig = ((on_id ? rid : key) >> shift) & (uint32_t)(nb - 1);
+    atomicAdd(&sm.cnt[dig], 1);
+    if (mode != kRank) atomicAdd(&sm.mass[dig], expf(x - xmax));
+  }
+  __syncthreads();
+  if (threadIdx.x < 32) {
+    const int lane = threadIdx.x, per = nb / 32;
+    // lane 0 owns the highest buckets (ranked first)
+    const int top = nb - 1 - lane * per;
+    float lm = 0.f;
+    int lc = 0;
+    for (int x = 0; x < per; ++x) {
+      lm += sm.mass[top - x];
+      lc += sm.cnt[top - x];
+    }
+    float im = lm;
+    int ic = lc;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      float ym = __shfl_up_sync(0xffffffffu, im, o);
+      int yc = __shfl_up_sync(0xffffffffu, ic, o);
+      if (lane >= o) {
+        im += ym;
+        ic += yc;
+      }
+    }
+    const float mb = sm.mb;
+    const int cb = sm.cb;
+    bool cross;
+    if (mode == kMassGE) cross = lc > 0 && mb + im >= target_mass;
+    else if (mode == kMassGT) cross = lc > 0 && mb + im > target_mass;
+    else cross = lc > 0 && cb + ic > target_rank;
+    unsigned bal = __ballot_sync(0xffffffffu, cross);
+    int src;
+    if (bal) {
+      src = __ffs(bal) - 1;
+    } else {
+      // rounding left the target beyond the last token: take the last one
+      unsigned ne = __ballot_sync(0xffffffffu, lc > 0);
+      src = 31 - __clz(ne);
+    }
+    if (lane == src) {
+      float m = mb + im - lm;   // mass ranked before this lane's buckets
+      int c = cb + ic - lc;
+      int chosen = -1, last_ne = -1;
+      float m_at = m;
+      int c_at = c;
+      for (int x = 0; x < per; ++x) {
+        const int b = top - x;
+        if (sm.cnt[b] == 0) continue;
+        last_ne = b;
+        m_at = m;
+        c_at = c;
+        const float mn = m + sm.mass[b];
+        const int cn = c + sm.cnt[b];
+        bool hit = (mode == kMassGE) ? (mn >= target_mass)
+                 : (mode == kMassGT) ? (mn > target_mass) : (cn > target_rank);
+        if (hit) {
+          chosen = b;
+          break;
+        }
+        m = mn;
+        c = cn;
+      }
+      if (chosen < 0) chosen = last_ne;   // rounding fallback: last non-empty bucket
+      sm.mb = m_at;
+      sm.cb = c_at;
+      const uint32_t dmask = (uint32_t)(nb - 1) << shift;
+      if (on_id) {
+        sm.ipre = ipre | ((uint32_t)chosen << shift);
+        sm.imask = imask | dmask;
+      } else {
+        sm.kpre = kpre | ((uint32_t)chosen << shift);
+        sm.kmask = kmask | dmask;
+      }
+    }
+  }
+  __syncthreads();
+}
+
+__device__ Found radix_find(const float* __restrict__ xs, int V, float xmax, int mode,
+                            float target_mass, int target_rank, SampleSmem& sm) {
+  if (threadIdx.x == 0) {
+    sm.kpre = sm.kmask = sm.ipre = sm.imask = 0;
+    sm.mb = 0.f;
+    sm.cb = 0;
+  }
+  __syncthreads();
+  radix_level(xs, V, xmax, mode, target_mass, target_rank, false, 21, 11, sm);
+  radix_level(xs, V, xmax, mode, target_mass, target_rank, false, 10, 11, sm);
+  radix_level(xs, V, xmax, mode, target_mass, target_rank, false, 0, 10, sm);
+  radix_level(xs, V, xmax, mode, target_mass, target_rank, true, 9, 9, sm);
+  radix_level(xs, V, xmax, mode, target_mass, target_rank, true, 0, 9, sm);
+  Found f;
+  f.id = (int)(kIdMask - sm.ipre);
+  f.rank = sm.cb;
+  // the token is fully determined: its own e completes the inclusive mass
+  float xv = xs[f.id];
+  f.cum_incl = sm.mb + expf(xv - xmax);
+  __syncthreads();
+  return f;
+}
+
+__global__ void __launch_bounds__(kThreads)
+sample_accept_kernel(const float* __restrict__ logits, const int32_t* __restrict__ tree_tokens,
+                     const int32_t* __restrict__ parents, int T, const int32_t* __restrict__ prior,
+                     int n_prior, int W, int V, float penalty, float temperature, float top_p,
+                     float min_p, const float* __restrict__ uniforms, int32_t* sampled,
+                     int32_t* __restrict__ path, int32_t* __restrict__ n_path,
+                     int32_t* __restrict__ bonus, int32_t* counter, float* __restrict__ xs_all,
+                     int32_t* status) {
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  SampleSmem& sm = *reinterpret_cast<SampleSmem*>(smem_raw);
+  uint32_t* bitmap = reinterpret_cast<uint32_t*>(smem_raw + sizeof(SampleSmem));
+  const int i = blockIdx.x, tid = threadIdx.x;
+  const int nwords = (V + 31) / 32;
+  for (int w = tid; w < nwords; w += kThreads) bitmap[w] = 0u;
+  if (tid == 0) {
+    // drafted tokens on the root path of node i, root excluded, root first
+    int tmp[64], n = 0, a = i;
+    bool ok = true;
+    while (a > 0 && n < 64) {
+      tmp[n++] = a;
+      int p = parents[a];
+      if (p < 0 || p >= a) {
+        ok = false;
+        break;
+      }
+      a = p;
+    }
+    if (!ok || a != 0) {
+      set_status(status, TS_ERR_INVALID_ARG);
+      n = 0;
+    }
+    for (int x = 0; x < n; ++x) sm.ptok[x] = tree_tokens[tmp[n - 1 - x]];
+    sm.plen = n;
+  }
+  __syncthreads();
+  // window = last W tokens of prior ++ path tokens
+  const int total = n_prior + sm.plen;
+  const int start = total > W ? total - W : 0;
+  for (int c = start + tid; c < total; c += kThreads) {
+    int t = c < n_prior ? prior[c] : sm.ptok[c - n_prior];
+    if (t < 0 || t >= V) {
+      set_status(status, TS_ERR_INVALID_ARG);
+      continue;
+    }
+    atomicOr(&bitmap[t >> 5], 1u << (t & 31));
+  }
+  __syncthreads();
+
+  // x' = penalised / tempered logits; running max
+  const float* x_in = logits + (size_t)i * V;
+  float* xs = xs_all + (size_t)i * V;
+  float lmax = -INFINITY;
+  for (int t = tid; t < V; t += kThreads) {
+    float x = x_in[t];
+    if ((bitmap[t >> 5] >> (t & 31)) & 1u) x = (x > 0.f) ? __fdiv_rn(x, penalty) : __fmul_rn(x, penalty);
+    x = __fdiv_rn(x, temperature);
+    xs[t] = x;
+    lmax = fmaxf(lmax, x);
+  }
+  const float xmax = block_max(lmax, sm);
+  __syncthreads();   // xs visible to the whole block
+
+  float z = 0.f, zmin = 0.f;
+  int nmin = 0;
+  for (int t = tid; t < V; t += kThreads) {
+    float e = expf(xs[t] - xmax);
+    z += e;
+    if (e >= min_p) {
+      zmin += e;
+      ++nmin;
+    }
+  }
+  const float Z = block_sum(z, sm);
+  float Zmin = block_sum(zmin, sm);
+  int n_minp = block_sum_int(nmin, sm);
+  if (n_minp == 0) {   // min_p > 1: only rank 0 (e = 1) survives
+    n_minp = 1;
+    Zmin = 1.f;
+  }
+
+  const Found f1 = radix_find(xs, V, xmax, kMassGE, top_p * Z, 0, sm);
+  const int k_keep = min(n_minp, f1.rank + 1);
+  const float ZK = (k_keep == f1.rank + 1) ? f1.cum_incl : Zmin;
+  const float u = uniforms[i];
+  Found f2 = radix_find(xs, V, xmax, kMassGT, u * ZK, 0, sm);
+  if (f2.rank >= k_keep) f2 = radix_find(xs, V, xmax, kRank, 0.f, k_keep - 1, sm);
+
+  // publish this node's draw; the last CTA walks the tree
+  if (tid == 0) {
+    sampled[i] = f2.id;
+    __threadfence();
+    int prev = atomicAdd(counter, 1);
+    sm.last = (prev == T - 1);
+  }
+  __syncthreads();
+  if (sm.last && tid == 0) {
+    __threadfence();
+    volatile const int32_t* vs = sampled;
+    bool acc[64];
+    int depth[64];
+    acc[0] = true;
+    depth[0] = 0;
+    int best = 0;
+    for (int c = 1; c < T; ++c) {
+      int p = parents[c];
+      if (p < 0 || p >= c) {
+        acc[c] = false;
+        depth[c] = 0;
+        continue;
+      }
+      depth[c] = depth[p] + 1;
+      acc[c] = acc[p] && tree_tokens[c] == vs[p];
+      if (acc[c] && depth[c] > depth[best]) best = c;
+    }
+    const int n = depth[best] + 1;
+    int a = best;
+    for (int d = n - 1; d >= 0; --d) {
+      path[d] = a;
+      a = parents[a];
+    }
+    *n_path = n;
+    *bonus = vs[best];
+    *counter = 0;
+  }
+}
+
+template <int D>
+__global__ void kv_commit_kernel(__nv_bfloat16* __restrict__ k, __nv_bfloat16* __restrict__ v,
+                                 int64_t L, int64_t L_cap, int T, const int32_t* __restrict__ path,
+                                 const int32_t* __restrict__ n_path, int32_t* status) {
+  constexpr int V16 = D / 8;
+  __shared__ uint4 kb[63][V16], vb[63][V16];
+  const int kv = blockIdx.x;
+  const int n = *n_path;
+  if (n < 1 || n > T) {
+    if (threadIdx.x == 0) set_status(status, TS_ERR_INVALID_ARG);
+    return;
+  }
+  uint4* kh = reinterpret_cast<uint4*>(k + (size_t)kv * L_cap * D);
+  uint4* vh = reinterpret_cast<uint4*>(v + (size_t)kv * L_cap * D);
+  bool bad = false;
+  for (int e = threadIdx.x; e < (n - 1) * V16; e += blockDim.x) {
+    int t = e / V16 + 1, x = e % V16;
+    int src = path[t];
+    if (src < t || src >= T) {
+      bad = true;
+      continue;
+    }
+    kb[t - 1][x] = kh[(L + src) * V16 + x];
+    vb[t - 1][x] = vh[(L + src) * V16 + x];
+  }
+  bad = __syncthreads_or(bad);
+  if (bad) {
+    if (threadIdx.x == 0) set_status(status, TS_ERR_INVALID_ARG);
+    return;
+  }
+  for (int e = threadIdx.x; e < (n - 1) * V16; e += blockDim.x) {
+    int t = e / V16 + 1, x = e % V16;
+    kh[(L + t) * V16 + x] = kb[t - 1][x];
+    vh[(L + t) * V16 + x] = vb[t - 1][x];
+  }
+}
+
+}  // namespace
+
+size_t sample_ws_bytes(int T, int V) { return 256 + align_up((size_t)T * V * sizeof(float), 256); }
+
+int launch_sample_accept(const float* logits, const int32_t* tree_tokens, const int32_t* parents,
+                         int T, const int32_t* prior, int n_prior, int W, int V, float penalty,
+                         float temperature, float top_p, float min_p, const float* uniforms,
+                         int32_t* sampled, int32_t* path, int32_t* n_path, int32_t* bonus,
+                         void* ws, int32_t* status, cudaStream_t st) {
+  int32_t* counter = static_cast<int32_t*>(ws);
+  float* xs = reinterpret_cast<float*>(static_cast<char*>(ws) + 256);
+  if (cudaMemsetAsync(counter, 0, sizeof(int32_t), st) != cudaSuccess)
+    return launch_status("sample counter reset");
+  size_t smem = sizeof(SampleSmem) + (size_t)((V + 31) / 32) * sizeof(uint32_t);
+  cudaFuncSetAttribute(sample_accept_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  sample_accept_kernel<<<T, kThreads, smem, st>>>(logits, tree_tokens, parents, T, prior, n_prior, W,
+                                                  V, penalty, temperature, top_p, min_p, uniforms,
+                                                  sampled, path, n_path, bonus, counter, xs, status);
+  return launch_status("sample_accept_kernel");
+}
+
+int launch_kv_commit(void* k, void* v, int64_t L, int64_t L_cap, int Hkv, int d, int T,
+                     const int32_t* path, const int32_t* n_path, int32_t* status,
+                     cudaStream_t st) {
+  auto kb = static_cast<__nv_bfloat16*>(k);
+  auto vb = static_cast<__nv_bfloat16*>(v);
+  if (d == 128)
+    kv_commit_kernel<128><<<Hkv, 256, 0, st>>>(kb, vb, L, L_cap, T, path, n_path, status);
+  else
+    kv_commit_kernel<64><<<Hkv, 256, 0, st>>>(kb, vb, L, L_cap, T, path, n_path, status);
+  return launch_status("kv_commit_kernel");
+}
+
+}  // namespace ts

@@ -1,0 +1,171 @@
+// C-ABI entry points: host-side argument checks, then the launchers.
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+
+#include "ts_common.cuh"
+
+namespace ts {
+
+static thread_local char g_last_error[512] = {0};
+
+int fail(int code, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_last_error, sizeof(g_last_error), fmt, ap);
+  va_end(ap);
+  return code;
+}
+
+void clear_error() { g_last_error[0] = 0; }
+
+int launch_status(const char* what) {
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return fail(TS_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+  return TS_OK;
+}
+
+static int check_ws(const void* ws, size_t have, size_t need, const char* what) {
+  if (need == 0) return TS_OK;
+  if (!ws) return fail(TS_ERR_WORKSPACE, "%s: workspace is NULL (%zu bytes needed)", what, need);
+  if (reinterpret_cast<uintptr_t>(ws) % 256)
+    return fail(TS_ERR_WORKSPACE, "%s: workspace must be 256-byte aligned", what);
+  if (have < need)
+    return fail(TS_ERR_WORKSPACE, "%s: workspace has %zu bytes, %zu needed", what, have, need);
+  return TS_OK;
+}
+
+static int check_attn_shape(int T, int Hq, int Hkv, int d, const char* what) {
+  if (T < 1 || Hq < 1 || Hkv < 1)
+    return fail(TS_ERR_INVALID_ARG, "%s: T, Hq, Hkv must be >= 1 (T=%d Hq=%d Hkv=%d)", what, T, Hq, Hkv);
+  if (T > 64) return fail(TS_ERR_UNSUPPORTED, "%s: T=%d > 64 tree nodes", what, T);
+  if (Hq % Hkv) return fail(TS_ERR_INVALID_ARG, "%s: Hq=%d not a multiple of Hkv=%d", what, Hq, Hkv);
+  if (d != 64 && d != 128) return fail(TS_ERR_UNSUPPORTED, "%s: head dim %d not in {64,128}", what, d);
+  if (T * (Hq / Hkv) > 512)
+    return fail(TS_ERR_UNSUPPORTED, "%s: T*Hq/Hkv = %d > 512 query rows per KV head", what, T * (Hq / Hkv));
+  return TS_OK;
+}
+
+}  // namespace ts
+
+using namespace ts;
+
+extern "C" {
+
+const char* ts_status_string(int s) {
+  switch (s) {
+    case TS_OK: return "ok";
+    case TS_ERR_INVALID_ARG: return "invalid argument";
+    case TS_ERR_UNSUPPORTED: return "unsupported configuration";
+    case TS_ERR_CUDA: return "CUDA error";
+    case TS_ERR_TIMEOUT: return "device-side wait timed out";
+    case TS_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
+    default: return "unknown status";
+  }
+}
+
+const char* ts_last_error(void) { return g_last_error; }
+
+int ts_version(void) { return 100; }
+
+size_t ts_verify_workspace_bytes(int T, int Hq, int Hkv, int d, int64_t L) {
+  if (check_attn_shape(T, Hq, Hkv, d, "ts_verify_workspace_bytes") != TS_OK || L < 0) return 0;
+  return verify_plan(T, Hq, Hkv, d, L).ws_bytes;
+}
+
+int ts_verify_attention(const void* q, const void* k, const void* v, int64_t L, int64_t L_cap,
+                        const int32_t* parents, int T, int Hq, int Hkv, int d, int n_imp,
+                        float* o, float* lse, float* imp, void* workspace,
+                        size_t workspace_bytes, int32_t* status, void* stream) {
+  clear_error();
+  const char* W = "ts_verify_attention";
+  int rc = check_attn_shape(T, Hq, Hkv, d, W);
+  if (rc) return rc;
+  if (!q || !k || !v || !parents || !o) return fail(TS_ERR_INVALID_ARG, "%s: NULL tensor", W);
+  if (L < 0 || L + T > L_cap)
+    return fail(TS_ERR_INVALID_ARG, "%s: need 0 <= L and L+T <= L_cap (L=%lld T=%d L_cap=%lld)", W,
+                (long long)L, T, (long long)L_cap);
+  if (L_cap > (int64_t(1) << 31) - 1) return fail(TS_ERR_UNSUPPORTED, "%s: L_cap >= 2^31", W);
+  if (n_imp > T) return fail(TS_ERR_INVALID_ARG, "%s: n_imp=%d > T=%d", W, n_imp, T);
+  if (n_imp <= 0) n_imp = T;
+  VerifyPlan p = verify_plan(T, Hq, Hkv, d, L);
+  rc = check_ws(workspace, workspace_bytes, p.ws_bytes, W);
+  if (rc) return rc;
+  return launch_verify(q, k, v, L, L_cap, parents, T, Hq, Hkv, d, n_imp, o, lse, imp, workspace,
+                       status, static_cast<cudaStream_t>(stream));
+}
+
+size_t ts_select_workspace_bytes(int Hkv, int64_t L) {
+  if (Hkv < 1 || L < 0) return 0;
+  return select_plan(Hkv, L).ws_bytes;
+}
+
+int ts_partial_kv_select_gather(const float* imp, const void* k, const void* v, int64_t L,
+                                int64_t L_cap, int Hkv, int d, int B, int S, int R,
+                                int32_t* idx, void* kd, void* vd, int64_t* n_out,
+                                void* workspace, size_t workspace_bytes, int32_t* status,
+                                void* stream) {
+  clear_error();
+  const char* W = "ts_partial_kv_select_gather";
+  if (Hkv < 1) return fail(TS_ERR_INVALID_ARG, "%s: Hkv=%d", W, Hkv);
+  if (d != 64 && d != 128) return fail(TS_ERR_UNSUPPORTED, "%s: head dim %d not in {64,128}", W, d);
+  if (B < 0 || S < 0 || R < 0) return fail(TS_ERR_INVALID_ARG, "%s: B, S, R must be >= 0", W);
+  if (L < 0 || L > L_cap) return fail(TS_ERR_INVALID_ARG, "%s: need 0 <= L <= L_cap", W);
+  if (L_cap > (int64_t(1) << 31) - 1) return fail(TS_ERR_UNSUPPORTED, "%s: L_cap >= 2^31", W);
+  int64_t N = L < (int64_t)S + B + R ? L : (int64_t)S + B + R;
+  if (n_out) *n_out = N;
+  if (L == 0) return TS_OK;
+  if (!imp || !k || !v || !idx || !kd || !vd) return fail(TS_ERR_INVALID_ARG, "%s: NULL tensor", W);
+  SelectPlan p = select_plan(Hkv, L);
+  int rc = check_ws(workspace, workspace_bytes, p.ws_bytes, W);
+  if (rc) return rc;
+  return launch_select_gather(imp, k, v, L, L_cap, Hkv, d, B, S, R, idx, kd, vd, N, workspace,
+                              status, static_cast<cudaStream_t>(stream));
+}
+
+size_t ts_sample_workspace_bytes(int T, int V) {
+  if (T < 1 || T > 64 || V < 1 || V > 262144) return 0;
+  return sample_ws_bytes(T, V);
+}
+
+int ts_penalized_sample_accept(const float* logits, const int32_t* tree_tokens,
+                               const int32_t* parents, int T, const int32_t* prior, int n_prior,
+                               int W, int V, float penalty, float temperature, float top_p,
+                               float min_p, const float* uniforms, int32_t* sampled,
+                               int32_t* path, int32_t* n_path, int32_t* bonus, void* workspace,
+                               size_t workspace_bytes, int32_t* status, void* stream) {
+  clear_error();
+  const char* F = "ts_penalized_sample_accept";
+  if (T < 1) return fail(TS_ERR_INVALID_ARG, "%s: T=%d", F, T);
+  if (T > 64) return fail(TS_ERR_UNSUPPORTED, "%s: T=%d > 64", F, T);
+  if (V < 1) return fail(TS_ERR_INVALID_ARG, "%s: V=%d", F, V);
+  if (V > 262144) return fail(TS_ERR_UNSUPPORTED, "%s: V=%d > 262144", F, V);
+  if (n_prior < 0 || W < 0) return fail(TS_ERR_INVALID_ARG, "%s: n_prior, W must be >= 0", F);
+  if (!(penalty > 0.f) || !(temperature > 0.f))
+    return fail(TS_ERR_INVALID_ARG, "%s: penalty and temperature must be > 0", F);
+  if (!(top_p > 0.f) || !(min_p >= 0.f))
+    return fail(TS_ERR_INVALID_ARG, "%s: need top_p > 0 and min_p >= 0", F);
+  if (!logits || !tree_tokens || !parents || !uniforms || !sampled || !path || !n_path || !bonus ||
+      (n_prior > 0 && !prior))
+    return fail(TS_ERR_INVALID_ARG, "%s: NULL tensor", F);
+  int rc = check_ws(workspace, workspace_bytes, sample_ws_bytes(T, V), F);
+  if (rc) return rc;
+  return launch_sample_accept(logits, tree_tokens, parents, T, prior, n_prior, W, V, penalty,
+                              temperature, top_p, min_p, uniforms, sampled, path, n_path, bonus,
+                              workspace, status, static_cast<cudaStream_t>(stream));
+}
+
+int ts_kv_commit(void* k, void* v, int64_t L, int64_t L_cap, int Hkv, int d, int T,
+                 const int32_t* path, const int32_t* n_path, int32_t* status, void* stream) {
+  clear_error();
+  const char* F = "ts_kv_commit";
+  if (Hkv < 1 || T < 1) return fail(TS_ERR_INVALID_ARG, "%s: Hkv, T must be >= 1", F);
+  if (T > 64) return fail(TS_ERR_UNSUPPORTED, "%s: T=%d > 64", F, T);
+  if (d != 64 && d != 128) return fail(TS_ERR_UNSUPPORTED, "%s: head dim %d", F, d);
+  if (L < 0 || L + T > L_cap) return fail(TS_ERR_INVALID_ARG, "%s: need L+T <= L_cap", F);
+  if (!k || !v || !path || !n_path) return fail(TS_ERR_INVALID_ARG, "%s: NULL tensor", F);
+  return launch_kv_commit(k, v, L, L_cap, Hkv, d, T, path, n_path, status,
+                          static_cast<cudaStream_t>(stream));
+}
+
+}  // extern "C"

@@ -1,0 +1,112 @@
+// Shared internals of the tokenswift_gb300 library (host + device helpers).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+#include <stddef.h>
+
+#include "tokenswift_gb300.h"
+
+namespace ts {
+
+// ---------------------------------------------------------------- host side
+int fail(int code, const char* fmt, ...);     // record message, return code
+void clear_error();
+int launch_status(const char* what);          // TS_ERR_CUDA if the last launch failed
+
+inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// ---------------------------------------------------------------- device side
+__device__ __forceinline__ float bf2f(__nv_bfloat16 x) { return __bfloat162float(x); }
+
+__device__ __forceinline__ void unpack_bf16x8(const uint4& u, float* f) {
+  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    f[2 * i] = __uint_as_float(w[i] << 16);
+    f[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+  }
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+__device__ __forceinline__ int warp_sum_int(int v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+// Order-preserving map float -> uint32 (larger float -> larger key).
+__device__ __forceinline__ uint32_t float_key(float f) {
+  uint32_t u = __float_as_uint(f);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+__device__ __forceinline__ void set_status(int32_t* status, int code) {
+  if (status) atomicCAS(status, 0, code);
+}
+
+// Ancestor-or-self bit masks of the draft tree (T <= 64), computed by one
+// thread; invalid parent indices are reported and treated as the root.
+__device__ __forceinline__ void tree_masks(const int32_t* parents, int T,
+                                           unsigned long long* anc, int32_t* status) {
+  for (int i = 0; i < T; ++i) {
+    int p = parents[i];
+    unsigned long long m = 1ull << i;
+    if (i == 0) {
+      if (p != -1) set_status(status, TS_ERR_INVALID_ARG);
+    } else if (p < 0 || p >= i) {
+      set_status(status, TS_ERR_INVALID_ARG);
+    } else {
+      m |= anc[p];
+    }
+    anc[i] = m;
+  }
+}
+
+// ---------------------------------------------------------------- launchers
+struct VerifyPlan {
+  int M;               // packed query rows per KV head (T * G)
+  int n_split;         // KV splits per head
+  int64_t keys_per_split;
+  int rows_per_cta;
+  int n_rowblk;
+  size_t part_o_bytes, part_ml_bytes, ws_bytes;
+};
+VerifyPlan verify_plan(int T, int Hq, int Hkv, int d, int64_t L);
+int launch_verify(const void* q, const void* k, const void* v, int64_t L, int64_t L_cap,
+                  const int32_t* parents, int T, int Hq, int Hkv, int d, int n_imp,
+                  float* o, float* lse, float* imp, void* ws, int32_t* status,
+                  cudaStream_t st);
+
+struct SelectPlan {
+  int64_t chunk;       // positions per gather CTA
+  int64_t n_chunks;
+  size_t ws_bytes;
+};
+SelectPlan select_plan(int Hkv, int64_t L);
+int launch_select_gather(const float* imp, const void* k, const void* v, int64_t L,
+                         int64_t L_cap, int Hkv, int d, int B, int S, int R, int32_t* idx,
+                         void* kd, void* vd, int64_t N, void* ws, int32_t* status,
+                         cudaStream_t st);
+
+size_t sample_ws_bytes(int T, int V);
+int launch_sample_accept(const float* logits, const int32_t* tree_tokens, const int32_t* parents,
+                         int T, const int32_t* prior, int n_prior, int W, int V, float penalty,
+                         float temperature, float top_p, float min_p, const float* uniforms,
+                         int32_t* sampled, int32_t* path, int32_t* n_path, int32_t* bonus,
+                         void* ws, int32_t* status, cudaStream_t st);
+int launch_kv_commit(void* k, void* v, int64_t L, int64_t L_cap, int Hkv, int d, int T,
+                     const int32_t* path, const int32_t* n_path, int32_t* status,
+                     cudaStream_t st);
+
+}  // namespace ts

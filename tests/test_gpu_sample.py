@@ -1,0 +1,116 @@
+"""GPU parity: contextual-penalty sampling, tree acceptance and KV commit
+(ts_penalized_sample_accept, ts_kv_commit) against the oracle."""
+import numpy as np
+import pytest
+import torch
+
+import ts_synth as syn
+from oracle import ts_oracle as orc
+import parity_util as pu
+
+pytestmark = pytest.mark.gpu
+
+
+def _run(w, step=0, logits=None, prior=None, top_p=None, min_p=None, temperature=None,
+         penalty=None, W=None, tree=None, uniforms=None):
+    import self_speculative_ultra_gb300 as ts
+    inp = syn.sampling_inputs(w, step=step, tree=tree)
+    logits = inp["logits"] if logits is None else logits
+    prior = inp["prior"] if prior is None else prior
+    u = inp["uniforms"] if uniforms is None else uniforms
+    top_p = w.top_p if top_p is None else top_p
+    min_p = w.min_p if min_p is None else min_p
+    temperature = w.temperature if temperature is None else temperature
+    penalty = w.penalty if penalty is None else penalty
+    W = w.W if W is None else W
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    sampled, path, n_path, bonus = ts.ts_penalized_sample_accept(
+        pu.to_dev(logits), pu.to_dev(inp["tokens"]), pu.to_dev(inp["parents"]),
+        pu.to_dev(np.asarray(prior, np.int32)), W, penalty, temperature, top_p, min_p,
+        pu.to_dev(u), status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    sampled = sampled.cpu().numpy()
+    n = int(n_path.item())
+    path = path.cpu().numpy()[:n].tolist()
+    bonus = int(bonus.item())
+    ref, infos = orc.sample_all_nodes(logits, prior, inp["parents"], inp["tokens"], W, penalty,
+                                      temperature, top_p, min_p, u, return_info=True)
+    ties = 0
+    for i in range(len(ref)):
+        if sampled[i] != ref[i]:
+            assert infos[i]["margin"] < pu.TIE, (
+                f"node {i}: gpu {sampled[i]} oracle {ref[i]} margin {infos[i]['margin']:.2e}")
+            ties += 1
+    # acceptance is exact given the GPU's own draws (integer work)
+    p_ref, b_ref = orc.accept_from_samples(inp["parents"], inp["tokens"], sampled)
+    assert path == p_ref and bonus == b_ref
+    if ties == 0:
+        assert (path, bonus) == orc.sample_accept_sequential(
+            logits, prior, inp["parents"], inp["tokens"], W, penalty, temperature, top_p, min_p, u)
+    return sampled, path, bonus, ties
+
+
+@pytest.mark.parametrize("name", ["tiny", "qwen2.5-1.5b", "llama3.1-8b", "mha-7b", "qwen2.5-14b"])
+def test_configs(name):
+    _, path, _, ties = _run(syn.WORKLOADS[name])
+    print(name, "path", path, "ties", ties)
+
+
+@pytest.mark.parametrize("step", [1, 2, 3])
+def test_more_steps_llama(step):
+    _run(syn.WORKLOADS["llama3.1-8b"], step=step)
+
+
+@pytest.mark.parametrize("top_p,min_p,temp", [(1.0, 0.0, 1.0), (0.9, 0.0, 1.0), (0.5, 0.0, 0.7),
+                                              (1.0, 0.05, 1.0), (0.9, 0.05, 2.0),
+                                              (0.9, 1.5, 1.0), (1e-6, 0.0, 1.0)])
+def test_truncation_settings(top_p, min_p, temp):
+    w = syn.scaled(syn.WORKLOADS["tiny"], V=50000)
+    _run(w, top_p=top_p, min_p=min_p, temperature=temp)
+
+
+def test_flat_distribution_ranks_by_id():
+    w = syn.scaled(syn.WORKLOADS["tiny"], V=4096)
+    logits = np.zeros((w.T, w.V), dtype=np.float32)
+    u = np.linspace(0.01, 0.99, w.T).astype(np.float32)
+    _run(w, logits=logits, W=0, top_p=0.5, min_p=0.0, uniforms=u)
+
+
+def test_heavily_tied_logits():
+    w = syn.scaled(syn.WORKLOADS["tiny"], V=30000)
+    rng = np.random.default_rng(5)
+    logits = rng.integers(-3, 4, size=(w.T, w.V)).astype(np.float32)
+    _run(w, logits=logits, top_p=0.3, min_p=0.0)
+
+
+def test_no_window_and_short_prior():
+    w = syn.scaled(syn.WORKLOADS["tiny"], V=10000)
+    _run(w, W=0)
+    inp = syn.sampling_inputs(w)
+    _run(w, prior=np.asarray([inp["tokens"][0]], np.int32), W=1024)
+
+
+def test_single_node_and_tiny_vocab():
+    _run(syn.scaled(syn.WORKLOADS["tiny"], T=1, V=1))
+    _run(syn.scaled(syn.WORKLOADS["tiny"], T=1, V=7))
+
+
+def test_max_vocab():
+    _run(syn.scaled(syn.WORKLOADS["tiny"], T=4, V=262144))
+
+
+def test_kv_commit_matches_oracle():
+    import self_speculative_ultra_gb300 as ts
+    rng = np.random.default_rng(9)
+    Hkv, L, T, d = 3, 500, 16, 128
+    kb = rng.integers(0, 2 ** 16, size=(Hkv, L + T, d), dtype=np.uint16)
+    vb = rng.integers(0, 2 ** 16, size=(Hkv, L + T, d), dtype=np.uint16)
+    path = [0, 2, 7, 11]
+    k, v = pu.to_dev_bf16(kb), pu.to_dev_bf16(vb)
+    pdev = pu.to_dev(np.array(path + [0] * (T - 4), np.int32))
+    ndev = pu.to_dev(np.array([4], np.int32))
+    ts.ts_kv_commit(k, v, L, T, pdev, ndev)
+    torch.cuda.synchronize()
+    assert pu.bf16_dev_to_bits(k).tobytes() == orc.kv_commit(kb, L, path).tobytes()
+    assert pu.bf16_dev_to_bits(v).tobytes() == orc.kv_commit(vb, L, path).tobytes()

@@ -276,3 +276,22 @@ def sampling_inputs(w: Workload, step: int = 0, tree=None, plant_accept: float =
     u = node_uniforms(w.seed, step, T)
     return dict(logits=logits, prior=prior, parents=np.asarray(parents, np.int32),
                 tokens=np.asarray(tokens, np.int32), uniforms=u)
+
+
+# --------------------------------------------------------------------------
+# standalone importance scores (selection tests)
+# --------------------------------------------------------------------------
+def importance_scores(Hkv: int, L: int, seed: int, std: float = 16.0,
+                      grid: float | None = None, n_heavy: int = 256):
+    """fp32 importance-like scores [Hkv, L]: N(0, std^2), optionally rounded
+    to a grid (creating exact ties), with n_heavy positions raised far above
+    the rest (the heavy hitters)."""
+    rng = np.random.Generator(np.random.PCG64([seed, 77]))
+    s = rng.standard_normal((Hkv, L)) * std
+    if grid:
+        s = np.round(s / grid) * grid
+    for h in range(Hkv):
+        if n_heavy and L > 0:
+            pos = rng.choice(L, size=min(n_heavy, L), replace=False)
+            s[h, pos] += 10 * std
+    return s.astype(np.float32)
