@@ -45,9 +45,11 @@ __device__ __forceinline__ int warp_sum_int(int v) {
   return v;
 }
 
-// Order-preserving map float -> uint32 (larger float -> larger key).
+// Order-preserving map float -> uint32 (larger float -> larger key); -0.0 and
+// +0.0 compare equal as floats, so both map to the key of +0.0.
 __device__ __forceinline__ uint32_t float_key(float f) {
   uint32_t u = __float_as_uint(f);
+  if ((u << 1) == 0u) u = 0u;
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
@@ -74,7 +76,10 @@ __device__ __forceinline__ void tree_masks(const int32_t* parents, int T,
 }
 
 // ---------------------------------------------------------------- launchers
+constexpr int kGb300Sms = 152;   // streaming multiprocessors of one GB300
+
 struct VerifyPlan {
+  bool tc;             // tcgen05 kernel (else the CUDA-core kernel)
   int M;               // packed query rows per KV head (T * G)
   int n_split;         // KV splits per head
   int64_t keys_per_split;
@@ -83,6 +88,11 @@ struct VerifyPlan {
   size_t part_o_bytes, part_ml_bytes, ws_bytes;
 };
 VerifyPlan verify_plan(int T, int Hq, int Hkv, int d, int64_t L);
+int tc_splits(int Hkv, int n_rg, int64_t L, int nsm);
+int launch_verify_tc(const void* q, const void* k, const void* v, int64_t L, int64_t L_cap,
+                     const int32_t* parents, int T, int Hq, int Hkv, int d, int n_imp,
+                     int64_t keys_per_split, int n_split, int n_rg, float* part_o,
+                     float* part_ml, float* imp, int32_t* status, cudaStream_t st);
 int launch_verify(const void* q, const void* k, const void* v, int64_t L, int64_t L_cap,
                   const int32_t* parents, int T, int Hq, int Hkv, int d, int n_imp,
                   float* o, float* lse, float* imp, void* ws, int32_t* status,

@@ -16,6 +16,9 @@
 //   imp[kv,j] = (sum of the group's last n_imp queries) . k_j / sqrt(d)
 // is computed once per key by the row-block-0 CTAs from the K tile they
 // already hold.
+#include <cstdlib>
+#include <cstring>
+
 #include "ts_common.cuh"
 
 namespace ts {
@@ -200,20 +203,43 @@ __global__ void verify_merge(const float* __restrict__ part_o, const float* __re
 
 }  // namespace
 
+static bool use_simple_path() {
+  static int v = -1;
+  if (v < 0) {
+    const char* e = getenv("TS_VERIFY_IMPL");
+    v = (e && strcmp(e, "simple") == 0) ? 1 : 0;
+  }
+  return v == 1;
+}
+
 VerifyPlan verify_plan(int T, int Hq, int Hkv, int d, int64_t L) {
   VerifyPlan p{};
   p.M = T * (Hq / Hkv);
-  p.rows_per_cta = kRows;
-  p.n_rowblk = (p.M + kRows - 1) / kRows;
-  // aim for ~4 waves of 152 SMs, keys_per_split a multiple of the key tile
-  int64_t target_ctas = 4 * 152;
-  int64_t per_head = (target_ctas + (int64_t)Hkv * p.n_rowblk - 1) / ((int64_t)Hkv * p.n_rowblk);
-  if (per_head < 1) per_head = 1;
-  int64_t kps = (L + per_head - 1) / per_head;
-  kps = (kps + kKeys - 1) / kKeys * kKeys;
-  if (kps < kKeys) kps = kKeys;
-  p.keys_per_split = kps;
-  p.n_split = (int)((L + kps - 1) / kps);
+  if (!use_simple_path()) {
+    // tcgen05 path: row groups of up to 256 packed query rows
+    p.tc = true;
+    p.n_rowblk = (p.M + 255) / 256;
+    p.rows_per_cta = 256;
+    int n = tc_splits(Hkv, p.n_rowblk, L, kGb300Sms);
+    int64_t kps = (L + n - 1) / n;
+    kps = (kps + 127) / 128 * 128;
+    if (kps < 128) kps = 128;
+    p.keys_per_split = kps;
+    p.n_split = (int)((L + kps - 1) / kps);
+  } else {
+    p.tc = false;
+    p.rows_per_cta = kRows;
+    p.n_rowblk = (p.M + kRows - 1) / kRows;
+    // aim for ~4 waves of the SMs, keys_per_split a multiple of the key tile
+    int64_t target_ctas = 4 * kGb300Sms;
+    int64_t per_head = (target_ctas + (int64_t)Hkv * p.n_rowblk - 1) / ((int64_t)Hkv * p.n_rowblk);
+    if (per_head < 1) per_head = 1;
+    int64_t kps = (L + per_head - 1) / per_head;
+    kps = (kps + kKeys - 1) / kKeys * kKeys;
+    if (kps < kKeys) kps = kKeys;
+    p.keys_per_split = kps;
+    p.n_split = (int)((L + kps - 1) / kps);
+  }
   if (p.n_split < 1) p.n_split = 1;
   p.part_o_bytes = align_up((size_t)Hkv * p.n_split * p.M * d * sizeof(float), 256);
   p.part_ml_bytes = align_up((size_t)Hkv * p.n_split * p.M * 2 * sizeof(float), 256);
@@ -227,24 +253,30 @@ int launch_verify(const void* q, const void* k, const void* v, int64_t L, int64_
   VerifyPlan p = verify_plan(T, Hq, Hkv, d, L);
   float* part_o = static_cast<float*>(ws);
   float* part_ml = reinterpret_cast<float*>(static_cast<char*>(ws) + p.part_o_bytes);
-  dim3 grid(p.n_rowblk, p.n_split, Hkv);
-  auto qb = static_cast<const __nv_bfloat16*>(q);
-  auto kb = static_cast<const __nv_bfloat16*>(k);
-  auto vb = static_cast<const __nv_bfloat16*>(v);
-  if (d == 128) {
-    size_t sm = sizeof(SimpleSmem<128>);
-    cudaFuncSetAttribute(verify_split_simple<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
-    verify_split_simple<128><<<grid, kThreads, sm, st>>>(qb, kb, vb, L, L_cap, parents, T, Hq, Hkv,
-                                                         n_imp, p.keys_per_split, p.n_split, part_o,
-                                                         part_ml, imp, status);
+  int rc;
+  if (p.tc) {
+    rc = launch_verify_tc(q, k, v, L, L_cap, parents, T, Hq, Hkv, d, n_imp, p.keys_per_split,
+                          p.n_split, p.n_rowblk, part_o, part_ml, imp, status, st);
   } else {
-    size_t sm = sizeof(SimpleSmem<64>);
-    cudaFuncSetAttribute(verify_split_simple<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
-    verify_split_simple<64><<<grid, kThreads, sm, st>>>(qb, kb, vb, L, L_cap, parents, T, Hq, Hkv,
-                                                        n_imp, p.keys_per_split, p.n_split, part_o,
-                                                        part_ml, imp, status);
+    dim3 grid(p.n_rowblk, p.n_split, Hkv);
+    auto qb = static_cast<const __nv_bfloat16*>(q);
+    auto kb = static_cast<const __nv_bfloat16*>(k);
+    auto vb = static_cast<const __nv_bfloat16*>(v);
+    if (d == 128) {
+      size_t sm = sizeof(SimpleSmem<128>);
+      cudaFuncSetAttribute(verify_split_simple<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
+      verify_split_simple<128><<<grid, kThreads, sm, st>>>(qb, kb, vb, L, L_cap, parents, T, Hq, Hkv,
+                                                           n_imp, p.keys_per_split, p.n_split, part_o,
+                                                           part_ml, imp, status);
+    } else {
+      size_t sm = sizeof(SimpleSmem<64>);
+      cudaFuncSetAttribute(verify_split_simple<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
+      verify_split_simple<64><<<grid, kThreads, sm, st>>>(qb, kb, vb, L, L_cap, parents, T, Hq, Hkv,
+                                                          n_imp, p.keys_per_split, p.n_split, part_o,
+                                                          part_ml, imp, status);
+    }
+    rc = launch_status("verify_split_simple");
   }
-  int rc = launch_status("verify_split_simple");
   if (rc) return rc;
   verify_merge<<<T * Hq, 128, 0, st>>>(part_o, part_ml, T, Hq, Hkv, d, p.n_split, o, lse);
   return launch_status("verify_merge");

@@ -1,0 +1,562 @@
+// Tree verification attention on the 5th-generation tensor cores (tcgen05):
+// split-KV flash-decode with the GQA group and the draft tree packed into the
+// query tile, importance fused into the same K pass.
+//
+// "TokenSwift: Lossless Acceleration of Ultra Long Sequence Generation":
+// §3.1 Overview (verification with the full KV cache), §E Tree-Based
+// Attention (a tree token attends only to its predecessors), §3.3 Dynamic KV
+// Cache Management (importance = query-key dot products, GQA scores
+// aggregated per group).
+//
+// One CTA = (key split, KV head, row group).  The M = T*G query rows of the
+// KV head's group are packed (row r = node (r / G), head kv*G + r % G) into up
+// to two 128-row tiles held in shared memory for the whole CTA, so every K/V
+// tile is read from HBM once per step.  Per 128-key tile:
+//   TMA (warp 0)        K and V tiles -> 2-stage shared-memory rings
+//                       (128-byte swizzle, L2 evict-first)
+//   MMA (warp 1)        S_g = Q_g K^T into TMEM (fp32), then after the
+//                       softmax wrote P_g (bf16) over S_g, O_g += P_g V
+//                       with P from TMEM; the two row tiles ping-pong so
+//                       the tensor core works on one while the other's
+//                       softmax runs
+//   importance (2,3)    imp_j = (sum of the group's last n_imp queries) . k_j
+//                       / sqrt(d) on CUDA cores from the same shared K tile
+//                       (the importance is linear in the queries)
+//   softmax (4..11)     one thread per query row: tile max, lazy running-max
+//                       update (O and l are rescaled only when the max grows
+//                       by more than 2^8), P = 2^(s*log2e/sqrt(d) - m), row
+//                       sums; tree mask and split boundaries applied only in
+//                       the tiles that need them
+// Each CTA writes an unnormalised partial (O, m, l) in the log2 domain; the
+// merge kernel of verify_attn.cu combines the splits.
+//
+// Every mbarrier wait is bounded (~1 s of SM clocks); on expiry the CTA
+// records TS_ERR_TIMEOUT in the status word, drains its own in-flight copies
+// and MMAs (again bounded), frees its TMEM and returns.
+#include "tc_ptx.cuh"
+#include "ts_common.cuh"
+
+namespace ts {
+
+namespace {
+
+constexpr int kNk = 128;                 // keys per tile
+constexpr int kStages = 2;               // K and V ring depth
+constexpr int kThreadsTc = 384;          // 12 warps
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLazy = 8.0f;            // running max refreshed only past +2^8
+constexpr long long kWaitCycles = 1ll << 31;
+// P is fed to the P.V product as hi + lo bf16 terms (error ~2^-17 instead of
+// the 2^-9 of a single bf16 rounding).
+constexpr bool kSplitP = true;
+
+struct TcAux {
+  uint64_t k_full[kStages], k_empty[kStages], v_full[kStages], v_empty[kStages];
+  uint64_t s_full[2], p_ready[2], o_final, drain;
+  unsigned long long anc[64];
+  uint32_t tmem_base;
+  volatile int32_t abort_flag;
+};
+
+template <int D>
+struct TcLayout {
+  static constexpr int kPanel = 128 * 128;         // 128 rows x 64 bf16 (128 B rows)
+  static constexpr int kTile = 128 * D * 2;        // 128 rows x D bf16
+  static constexpr int kQ = 0;
+  static constexpr int kK = kQ + 2 * kTile;
+  static constexpr int kV = kK + kStages * kTile;
+  static constexpr int kQsum = kV + kStages * kTile;
+  static constexpr int kAux = kQsum + D * 4;
+  static constexpr int kBytes = kAux + (int)sizeof(TcAux);
+  static constexpr int kAlloc = kBytes + 1024;     // slack to align the base to 1024 B
+  static constexpr uint32_t kTmemCols = 512;
+  __host__ __device__ static constexpr uint32_t obase(int g) { return (uint32_t)(g * D); }
+  __host__ __device__ static constexpr uint32_t sbase(int g) { return (uint32_t)(2 * D + g * kNk); }
+};
+
+__device__ __forceinline__ void timeout(TcAux* aux, int32_t* status) {
+  aux->abort_flag = 1;
+  set_status(status, TS_ERR_TIMEOUT);
+}
+
+template <int D>
+__global__ void __launch_bounds__(kThreadsTc, 1)
+verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v,
+                 const __nv_bfloat16* __restrict__ q, const int32_t* __restrict__ parents, int T,
+                 int Hq, int Hkv, int n_imp, int64_t L, int64_t L_cap, int64_t keys_per_split,
+                 int n_split, float* __restrict__ part_o, float* __restrict__ part_ml,
+                 float* __restrict__ imp, int32_t* status) {
+  using Ly = TcLayout<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                           ~uintptr_t(1023));
+  uint8_t* sq = sm + Ly::kQ;
+  uint8_t* sk = sm + Ly::kK;
+  uint8_t* sv = sm + Ly::kV;
+  float* qsum = reinterpret_cast<float*>(sm + Ly::kQsum);
+  TcAux* aux = reinterpret_cast<TcAux*>(sm + Ly::kAux);
+
+  const int split = blockIdx.x, kv = blockIdx.y, rg = blockIdx.z;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int G = Hq / Hkv, M = T * G;
+  const int r0 = rg * 256;
+  const int nt = min(2, (M - r0 + 127) / 128);
+  const int64_t j0 = (int64_t)split * keys_per_split;
+  const int64_t j1 = min(L, j0 + keys_per_split);
+  const bool last = (split == n_split - 1);
+  const int64_t jend = last ? L + T : j1;
+  const int64_t jlim = last ? L : j1;           // keys below need no mask
+  const int n_tiles = (int)((jend - j0 + kNk - 1) / kNk);
+  const bool do_imp = (imp != nullptr) && rg == 0;
+  const float scale = 1.0f / sqrtf((float)D);
+  const float sl2 = scale * kLog2e;
+
+  // ---------------------------------------------------------------- set-up
+  if (tid == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      ptx::mbar_init(&aux->k_full[s], 1);
+      ptx::mbar_init(&aux->k_empty[s], 1 + 2);   // MMA commit + two importance warps
+      ptx::mbar_init(&aux->v_full[s], 1);
+      ptx::mbar_init(&aux->v_empty[s], 1);
+    }
+    for (int g = 0; g < 2; ++g) {
+      ptx::mbar_init(&aux->s_full[g], 1);
+      ptx::mbar_init(&aux->p_ready[g], 128);
+    }
+    ptx::mbar_init(&aux->o_final, 1);
+    ptx::mbar_init(&aux->drain, 1);
+    aux->abort_flag = 0;
+    ptx::fence_mbar_init();
+    tree_masks(parents, T, aux->anc, (split == 0 && kv == 0 && rg == 0) ? status : nullptr);
+  }
+  if (warp == 1) {
+    ptx::tmem_alloc(&aux->tmem_base, Ly::kTmemCols);
+    ptx::tmem_relinquish();
+  }
+  if (warp == 0 && lane == 0) {
+    ptx::prefetch_tmap(&tmap_k);
+    ptx::prefetch_tmap(&tmap_v);
+  }
+  // Q tiles -> shared memory in the 128-byte-swizzled K-major layout
+  constexpr int C16 = D / 8;                     // 16-byte chunks per row
+  for (int e = tid; e < 2 * 128 * C16; e += kThreadsTc) {
+    const int g = e / (128 * C16), rem = e % (128 * C16);
+    const int t = rem / C16, c = rem % C16;
+    const int R = r0 + g * 128 + t;
+    uint4 val = make_uint4(0, 0, 0, 0);
+    if (g < nt && R < M) {
+      const int i = R / G, h = kv * G + R % G;
+      val = *reinterpret_cast<const uint4*>(q + ((size_t)i * Hq + h) * D + c * 8);
+    }
+    const int p = c >> 3, cc = c & 7;
+    *reinterpret_cast<uint4*>(sq + g * Ly::kTile + p * Ly::kPanel + t * 128 +
+                              ((cc ^ (t & 7)) << 4)) = val;
+  }
+  if (do_imp) {
+    for (int c = tid; c < D; c += kThreadsTc) {
+      float s = 0.f;
+      for (int i = T - n_imp; i < T; ++i)
+        for (int g = 0; g < G; ++g) s += bf2f(q[((size_t)i * Hq + kv * G + g) * D + c]);
+      qsum[c] = s;
+    }
+  }
+  ptx::fence_proxy_async_smem();
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem = aux->tmem_base;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      const uint64_t pol = ptx::l2_evict_first_policy();
+      const int row0 = (int)(kv * L_cap + j0);
+      int j = 0;
+      for (; j < n_tiles && !aux->abort_flag; ++j) {
+        const int s = j % kStages;
+        const uint32_t ph = (uint32_t)((j / kStages) - 1) & 1u;
+        if (j >= kStages && !ptx::mbar_wait(&aux->k_empty[s], ph, kWaitCycles)) {
+          timeout(aux, status);
+          break;
+        }
+        ptx::mbar_arrive_expect_tx(&aux->k_full[s], Ly::kTile);
+        for (int p = 0; p < D / 64; ++p)
+          ptx::tma_load_2d(sk + s * Ly::kTile + p * Ly::kPanel, &tmap_k, &aux->k_full[s], p * 64,
+                           row0 + j * kNk, pol);
+        if (j >= kStages && !ptx::mbar_wait(&aux->v_empty[s], ph, kWaitCycles)) {
+          timeout(aux, status);
+          ++j;   // the K load of this tile is in flight
+          break;
+        }
+        ptx::mbar_arrive_expect_tx(&aux->v_full[s], Ly::kTile);
+        for (int p = 0; p < D / 64; ++p)
+          ptx::tma_load_2d(sv + s * Ly::kTile + p * Ly::kPanel, &tmap_v, &aux->v_full[s], p * 64,
+                           row0 + j * kNk, pol);
+      }
+      if (aux->abort_flag) {
+        // drain: wait (bounded) for the last loads issued into each stage
+        for (int jj = max(0, j - kStages); jj < j; ++jj) {
+          const int s = jj % kStages;
+          const uint32_t ph = (uint32_t)(jj / kStages) & 1u;
+          ptx::mbar_wait(&aux->k_full[s], ph, kWaitCycles);
+          ptx::mbar_wait(&aux->v_full[s], ph, kWaitCycles);
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc_qk = ptx::idesc_bf16_f32(128, kNk, false);
+      constexpr uint32_t idesc_pv = ptx::idesc_bf16_f32(128, D, true);
+      const uint32_t sq_a = ptx::smem_u32(sq), sk_a = ptx::smem_u32(sk), sv_a = ptx::smem_u32(sv);
+      auto qk = [&](int g, int s) {
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks) {
+          const uint32_t off = (ks >> 2) * Ly::kPanel + (ks & 3) * 32;
+          const uint64_t a = ptx::sdesc_sw128(sq_a + g * Ly::kTile + off, 16, 1024);
+          const uint64_t b = ptx::sdesc_sw128(sk_a + s * Ly::kTile + off, 16, 1024);
+          ptx::mma_ss(tmem + Ly::sbase(g), a, b, idesc_qk, ks > 0 ? 1u : 0u);
+        }
+      };
+      // O += P_hi V + P_lo V: P is carried as a two-term bf16 expansion whose
+      // halves sit in columns [0, kNk/2) and [kNk/2, kNk) of the S tile
+      auto pv = [&](int g, int s, bool acc) {
+#pragma unroll
+        for (int half = 0; half < (kSplitP ? 2 : 1); ++half) {
+#pragma unroll
+          for (int ks = 0; ks < kNk / 16; ++ks) {
+            const uint64_t b =
+                ptx::sdesc_sw128(sv_a + s * Ly::kTile + ks * 2048, Ly::kPanel, 1024);
+            ptx::mma_ts(tmem + Ly::obase(g), tmem + Ly::sbase(g) + half * (kNk / 2) + ks * 8, b,
+                        idesc_pv, (acc || half > 0 || ks > 0) ? 1u : 0u);
+          }
+        }
+      };
+      bool ok = ptx::mbar_wait(&aux->k_full[0], 0, kWaitCycles);
+      if (ok) {
+        ptx::tc_fence_after();
+        for (int g = 0; g < nt; ++g) {
+          qk(g, 0);
+          ptx::mma_commit(&aux->s_full[g]);
+        }
+        ptx::mma_commit(&aux->k_empty[0]);
+      }
+      for (int j = 0; ok && j < n_tiles; ++j) {
+        const int s = j % kStages;
+        if (!ptx::mbar_wait(&aux->v_full[s], (uint32_t)(j / kStages) & 1u, kWaitCycles)) {
+          ok = false;
+          break;
+        }
+        const bool more = j + 1 < n_tiles;
+        const int s2 = (j + 1) % kStages;
+        for (int g = 0; g < nt && ok; ++g) {
+          if (!ptx::mbar_wait(&aux->p_ready[g], (uint32_t)j & 1u, kWaitCycles)) {
+            ok = false;
+            break;
+          }
+          ptx::tc_fence_after();
+          pv(g, s, j > 0);
+          if (more) {
+            if (g == 0) {
+              if (!ptx::mbar_wait(&aux->k_full[s2], (uint32_t)((j + 1) / kStages) & 1u,
+                                  kWaitCycles)) {
+                ok = false;
+                break;
+              }
+              ptx::tc_fence_after();
+            }
+            qk(g, s2);
+            ptx::mma_commit(&aux->s_full[g]);
+          }
+        }
+        if (!ok) break;
+        ptx::mma_commit(&aux->v_empty[s]);
+        if (more) ptx::mma_commit(&aux->k_empty[s2]);
+      }
+      if (!ok) timeout(aux, status);
+      ptx::mma_commit(&aux->o_final);
+      // drain this thread's MMAs before TMEM is freed
+      ptx::mma_commit(&aux->drain);
+      ptx::mbar_wait(&aux->drain, 0, kWaitCycles);
+    }
+  } else if (warp < 4) {
+    // ------------------------------------------------------------ importance
+    const int t = tid - 64;   // 0..63: keys t and t + 64 of each tile
+    for (int j = 0; j < n_tiles; ++j) {
+      const int s = j % kStages;
+      if (aux->abort_flag || !ptx::mbar_wait(&aux->k_full[s], (uint32_t)(j / kStages) & 1u,
+                                             kWaitCycles)) {
+        timeout(aux, status);
+        break;
+      }
+      if (do_imp) {
+        const int64_t key0 = j0 + (int64_t)j * kNk;
+#pragma unroll
+        for (int h2 = 0; h2 < 2; ++h2) {
+          const int kr = t + 64 * h2;
+          const int64_t jj = key0 + kr;
+          if (jj < j1) {
+            const uint8_t* row = sk + s * Ly::kTile + kr * 128;
+            float acc = 0.f;
+#pragma unroll
+            for (int c = 0; c < C16; ++c) {
+              const int p = c >> 3, cc = c & 7;
+              const uint4 u = *reinterpret_cast<const uint4*>(row + p * Ly::kPanel +
+                                                              ((cc ^ (kr & 7)) << 4));
+              float f[8];
+              unpack_bf16x8(u, f);
+              const float4 qa = *reinterpret_cast<const float4*>(qsum + c * 8);
+              const float4 qb = *reinterpret_cast<const float4*>(qsum + c * 8 + 4);
+              acc = fmaf(f[0], qa.x, acc);
+              acc = fmaf(f[1], qa.y, acc);
+              acc = fmaf(f[2], qa.z, acc);
+              acc = fmaf(f[3], qa.w, acc);
+              acc = fmaf(f[4], qb.x, acc);
+              acc = fmaf(f[5], qb.y, acc);
+              acc = fmaf(f[6], qb.z, acc);
+              acc = fmaf(f[7], qb.w, acc);
+            }
+            imp[(size_t)kv * L + jj] = acc * scale;
+          }
+        }
+      }
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(&aux->k_empty[s]);
+    }
+  } else {
+    // ------------------------------------------------------------ softmax
+    const int g = (warp - 4) >> 2;
+    const int quarter = warp & 3;
+    const int t = quarter * 32 + lane;            // row within the tile
+    const int R = r0 + g * 128 + t;
+    const bool valid = (g < nt) && (R < M);
+    const unsigned long long anc = valid ? aux->anc[R / G] : 0ull;
+    const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+    const uint32_t s_addr = tmem + lane_off + Ly::sbase(g);
+    const uint32_t o_addr = tmem + lane_off + Ly::obase(g);
+    float m_used = -INFINITY, l = 0.f;
+    bool ok = true;
+    if (g < nt) {
+      // tcgen05.ld/st are warp-collective: every branch around them is warp-uniform
+      for (int j = 0; j < n_tiles; ++j) {
+        bool got = !aux->abort_flag &&
+                   ptx::mbar_wait(&aux->s_full[g], (uint32_t)j & 1u, kWaitCycles);
+        if (!__all_sync(0xffffffffu, got)) {
+          ok = false;
+          break;
+        }
+        ptx::tc_fence_after();
+        const int64_t key0 = j0 + (int64_t)j * kNk;
+        const bool edge = key0 + kNk > jlim;     // uniform: depends on the tile only
+        uint32_t r[32];
+        // pass 1: tile maximum of the visible scores
+        float mx = -INFINITY;
+#pragma unroll
+        for (int c = 0; c < kNk / 32; ++c) {
+          ptx::tmem_ld32(s_addr + c * 32, r);
+          ptx::tmem_ld_wait();
+          if (!edge) {
+#pragma unroll
+            for (int x = 0; x < 32; ++x) mx = fmaxf(mx, __uint_as_float(r[x]));
+          } else {
+#pragma unroll
+            for (int x = 0; x < 32; ++x) {
+              const int64_t key = key0 + c * 32 + x;
+              const bool vis = key < jlim ||
+                               (key < jend && key >= L && ((anc >> (key - L)) & 1ull));
+              if (vis) mx = fmaxf(mx, __uint_as_float(r[x]));
+            }
+          }
+        }
+        // lazy running max: raise it only when the tile max exceeds it by 2^8
+        const float ms = mx * sl2;
+        const bool raise = ms > m_used + kLazy;
+        const float f = raise ? ptx::ex2(m_used - ms) : 1.f;   // 0 when m_used = -inf
+        if (raise) {
+          l *= f;
+          m_used = ms;
+        }
+        if (j > 0 && __any_sync(0xffffffffu, raise)) {
+#pragma unroll 1
+          for (int c = 0; c < D / 32; ++c) {
+            uint32_t o[32];
+            ptx::tmem_ld32(o_addr + c * 32, o);
+            ptx::tmem_ld_wait();
+#pragma unroll
+            for (int x = 0; x < 32; ++x) o[x] = __float_as_uint(__uint_as_float(o[x]) * f);
+            ptx::tmem_st32(o_addr + c * 32, o);
+          }
+          ptx::tmem_st_wait();
+        }
+        // pass 2: P = 2^(s*sl2 - m) over the S columns, row sum.  P goes to
+        // TMEM as bf16 hi = rn(P) in columns [16c, 16c+16) and, when split,
+        // lo = rn(P - hi) in columns [64+16c, 64+16c+16).  A column is only
+        // overwritten after its S value was loaded: lo of chunks 0,1 waits
+        // for chunk 2's load, lo of chunks 2,3 for chunk 3's.
+        const bool live = m_used != -INFINITY;
+        uint32_t lo_a[16], lo_b[16];
+#pragma unroll
+        for (int c = 0; c < kNk / 32; ++c) {
+          ptx::tmem_ld32(s_addr + c * 32, r);
+          ptx::tmem_ld_wait();
+          float p[32];
+#pragma unroll
+          for (int x = 0; x < 32; ++x) {
+            float e = live ? ptx::ex2(fmaf(__uint_as_float(r[x]), sl2, -m_used)) : 0.f;
+            if (edge) {
+              const int64_t key = key0 + c * 32 + x;
+              const bool vis = key < jlim ||
+                               (key < jend && key >= L && ((anc >> (key - L)) & 1ull));
+              e = vis ? e : 0.f;
+            }
+            p[x] = e;
+            l += e;
+          }
+          uint32_t pk[16];
+#pragma unroll
+          for (int x = 0; x < 16; ++x) pk[x] = ptx::pack_bf16x2(p[2 * x], p[2 * x + 1]);
+          ptx::tmem_st16(s_addr + c * 16, pk);
+          if constexpr (kSplitP) {
+            uint32_t* lo = (c & 1) ? lo_b : lo_a;
+            if (c == 2) ptx::tmem_st16(s_addr + 64, lo_a);        // chunk 0's residual
+            if (c == 3) {
+              ptx::tmem_st16(s_addr + 80, lo_b);                    // chunk 1's residual
+            }
+#pragma unroll
+            for (int x = 0; x < 16; ++x) {
+              const float h0 = __uint_as_float(pk[x] << 16);
+              const float h1 = __uint_as_float(pk[x] & 0xFFFF0000u);
+              lo[x] = ptx::pack_bf16x2(p[2 * x] - h0, p[2 * x + 1] - h1);
+            }
+            if (c == 3) {
+              ptx::tmem_st16(s_addr + 96, lo_a);                    // chunk 2's residual
+              ptx::tmem_st16(s_addr + 112, lo_b);                   // chunk 3's residual
+            }
+          }
+        }
+        ptx::tmem_st_wait();
+        ptx::tc_fence_before();
+        ptx::mbar_arrive(&aux->p_ready[g]);
+      }
+      // epilogue: final O row -> unnormalised partial
+      bool fin = ok && !aux->abort_flag && ptx::mbar_wait(&aux->o_final, 0, kWaitCycles);
+      if (__all_sync(0xffffffffu, fin)) {
+        ptx::tc_fence_after();
+        const size_t base = ((size_t)kv * n_split + split) * M + R;
+#pragma unroll 1
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t o[32];
+          ptx::tmem_ld32(o_addr + c * 32, o);
+          ptx::tmem_ld_wait();
+          if (valid) {
+            float4* dst = reinterpret_cast<float4*>(part_o + base * D + c * 32);
+#pragma unroll
+            for (int x = 0; x < 8; ++x)
+              dst[x] = make_float4(__uint_as_float(o[4 * x]), __uint_as_float(o[4 * x + 1]),
+                                   __uint_as_float(o[4 * x + 2]), __uint_as_float(o[4 * x + 3]));
+          }
+        }
+        if (valid) {
+          part_ml[base * 2] = m_used;
+          part_ml[base * 2 + 1] = l;
+        }
+      } else {
+        timeout(aux, status);
+      }
+    }
+  }
+
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem, Ly::kTmemCols);
+  }
+}
+
+// ------------------------------------------------------------------ host side
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static bool tried = false;
+  if (!tried) {
+    tried = true;
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  }
+  return fn;
+}
+
+int make_kv_map(CUtensorMap* map, const void* base, int Hkv, int64_t L_cap, int d) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return fail(TS_ERR_CUDA, "cuTensorMapEncodeTiled is unavailable");
+  cuuint64_t dims[2] = {(cuuint64_t)d, (cuuint64_t)Hkv * (cuuint64_t)L_cap};
+  cuuint64_t strides[1] = {(cuuint64_t)d * 2};
+  cuuint32_t box[2] = {64, (cuuint32_t)kNk};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides,
+                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(TS_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
+  return TS_OK;
+}
+
+}  // namespace
+
+// Key splits per (KV head, row group): the count minimising waves x tiles per
+// CTA (+ a fixed per-CTA cost), so the grid fills whole waves of the SMs.
+int tc_splits(int Hkv, int n_rg, int64_t L, int nsm) {
+  int64_t max_split = (L + kNk - 1) / kNk;
+  if (max_split < 1) max_split = 1;
+  if (max_split > 1024) max_split = 1024;
+  int best = 1;
+  int64_t best_cost = INT64_MAX;
+  for (int n = 1; n <= max_split; ++n) {
+    int64_t kps = ((L + n - 1) / n + kNk - 1) / kNk;    // tiles per split
+    int64_t ctas = (int64_t)Hkv * n_rg * n;
+    int64_t waves = (ctas + nsm - 1) / nsm;
+    int64_t cost = waves * (kps + 3);
+    if (cost < best_cost) {
+      best_cost = cost;
+      best = n;
+    }
+  }
+  return best;
+}
+
+int launch_verify_tc(const void* q, const void* k, const void* v, int64_t L, int64_t L_cap,
+                     const int32_t* parents, int T, int Hq, int Hkv, int d, int n_imp,
+                     int64_t keys_per_split, int n_split, int n_rg, float* part_o,
+                     float* part_ml, float* imp, int32_t* status, cudaStream_t st) {
+  CUtensorMap mk, mv;
+  int rc = make_kv_map(&mk, k, Hkv, L_cap, d);
+  if (rc) return rc;
+  rc = make_kv_map(&mv, v, Hkv, L_cap, d);
+  if (rc) return rc;
+  dim3 grid(n_split, Hkv, n_rg);
+  auto qb = static_cast<const __nv_bfloat16*>(q);
+  if (d == 128) {
+    constexpr int smem = TcLayout<128>::kAlloc;
+    cudaFuncSetAttribute(verify_tc_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    verify_tc_kernel<128><<<grid, kThreadsTc, smem, st>>>(mk, mv, qb, parents, T, Hq, Hkv, n_imp, L,
+                                                          L_cap, keys_per_split, n_split, part_o,
+                                                          part_ml, imp, status);
+  } else {
+    constexpr int smem = TcLayout<64>::kAlloc;
+    cudaFuncSetAttribute(verify_tc_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    verify_tc_kernel<64><<<grid, kThreadsTc, smem, st>>>(mk, mv, qb, parents, T, Hq, Hkv, n_imp, L,
+                                                         L_cap, keys_per_split, n_split, part_o,
+                                                         part_ml, imp, status);
+  }
+  return launch_status("verify_tc_kernel");
+}
+
+}  // namespace ts

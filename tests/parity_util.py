@@ -53,6 +53,8 @@ def check_importance(imp, imp_ref, q64, k64, n_imp, G):
     T, Hq, d = q64.shape
     Hkv, L = imp_ref.shape
     worst = 0.0
+    if L == 0:
+        return worst
     for kv in range(Hkv):
         qs = q64[T - n_imp:, kv * G:(kv + 1) * G, :].sum(axis=(0, 1))
         bound = 1e-5 * np.linalg.norm(qs) * np.linalg.norm(k64[kv, :L], axis=1) / np.sqrt(d)

@@ -43,6 +43,17 @@ def test_standalone_exact_ties_break_to_lower_position(grid):
     _standalone(4, 20000, 3000, 4, 64, grid=grid)
 
 
+def test_standalone_signed_zero_ties():
+    """-0.0 and +0.0 are equal scores: ties between them go to the lower position."""
+    import self_speculative_ultra_gb300 as ts
+    L, B = 3000, 500
+    imp = np.where(np.arange(L) % 2 == 0, np.float32(0.0), np.float32(-0.0)).astype(np.float32)[None]
+    kb = np.zeros((1, L + 1, 64), np.uint16)
+    idx, _, _ = ts.ts_partial_kv_select_gather(pu.to_dev(imp), pu.to_dev_bf16(kb), pu.to_dev_bf16(kb),
+                                               L, B, 4, 64)
+    np.testing.assert_array_equal(idx.cpu().numpy()[0], orc.select_partial(imp[0], L, B, 4, 64))
+
+
 @pytest.mark.parametrize("L,B,S,R", [(1, 10, 4, 64), (60, 10, 4, 64), (78, 10, 4, 64),
                                      (79, 10, 4, 64), (2000, 0, 4, 64), (2000, 100, 0, 0),
                                      (3000, 2931, 4, 64)])
