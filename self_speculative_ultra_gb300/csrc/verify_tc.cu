@@ -9,30 +9,35 @@
 // aggregated per group).
 //
 // One CTA = (key split, KV head, row group).  The M = T*G query rows of the
-// KV head's group are packed (row r = node (r / G), head kv*G + r % G) into up
+// KV head's group are packed (row r = node r / G, head kv*G + r % G) into up
 // to two 128-row tiles held in shared memory for the whole CTA, so every K/V
-// tile is read from HBM once per step.  Per 128-key tile:
+// tile is read from HBM once per step.  Per 128-key tile j:
 //   TMA (warp 0)        K and V tiles -> 2-stage shared-memory rings
 //                       (128-byte swizzle, L2 evict-first)
-//   MMA (warp 1)        S_g = Q_g K^T into TMEM (fp32), then after the
-//                       softmax wrote P_g (bf16) over S_g, O_g += P_g V
-//                       with P from TMEM; the two row tiles ping-pong so
-//                       the tensor core works on one while the other's
-//                       softmax runs
+//   MMA (warp 1)        S_g = Q_g K^T (M=128, N=128, fp32 in TMEM); once the
+//                       softmax has written P_g over S_g, O_g += P_g V with P
+//                       read from TMEM, then at once S_g of tile j+1.  The two
+//                       row tiles ping-pong: the tensor core works on one
+//                       while the other's softmax runs.
 //   importance (2,3)    imp_j = (sum of the group's last n_imp queries) . k_j
 //                       / sqrt(d) on CUDA cores from the same shared K tile
 //                       (the importance is linear in the queries)
-//   softmax (4..11)     one thread per query row: tile max, lazy running-max
-//                       update (O and l are rescaled only when the max grows
-//                       by more than 2^8), P = 2^(s*log2e/sqrt(d) - m), row
-//                       sums; tree mask and split boundaries applied only in
-//                       the tiles that need them
+//   softmax (4..11)     one thread per query row, its 128 scores in
+//                       registers: tile max, lazy running max (O and l are
+//                       rescaled only when the max grows past 2^8),
+//                       P = 2^(s*log2e/sqrt(d) - m) back to TMEM in bf16 (or
+//                       as a two-term bf16 expansion hi + lo when SPLIT),
+//                       row sums.  Tree mask and split limits only touch the
+//                       tiles that need them.
 // Each CTA writes an unnormalised partial (O, m, l) in the log2 domain; the
 // merge kernel of verify_attn.cu combines the splits.
 //
 // Every mbarrier wait is bounded (~1 s of SM clocks); on expiry the CTA
 // records TS_ERR_TIMEOUT in the status word, drains its own in-flight copies
 // and MMAs (again bounded), frees its TMEM and returns.
+#include <cstdlib>
+#include <cstring>
+
 #include "tc_ptx.cuh"
 #include "ts_common.cuh"
 
@@ -41,35 +46,36 @@ namespace ts {
 namespace {
 
 constexpr int kNk = 128;                 // keys per tile
-constexpr int kStages = 2;               // K and V ring depth
+constexpr int kSK = 2;                   // K ring depth
+constexpr int kSV = 2;                   // V ring depth
 constexpr int kThreadsTc = 384;          // 12 warps
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLazy = 8.0f;            // running max refreshed only past +2^8
 constexpr long long kWaitCycles = 1ll << 31;
-// P is fed to the P.V product as hi + lo bf16 terms (error ~2^-17 instead of
-// the 2^-9 of a single bf16 rounding).
-constexpr bool kSplitP = true;
+constexpr uint32_t kNegInf = 0xFF800000u;
 
 struct TcAux {
-  uint64_t k_full[kStages], k_empty[kStages], v_full[kStages], v_empty[kStages];
+  uint64_t k_full[kSK], k_empty[kSK], v_full[kSV], v_empty[kSV];
   uint64_t s_full[2], p_ready[2], o_final, drain;
   unsigned long long anc[64];
+  int32_t par[64];
   uint32_t tmem_base;
   volatile int32_t abort_flag;
 };
 
 template <int D>
 struct TcLayout {
-  static constexpr int kPanel = 128 * 128;         // 128 rows x 64 bf16 (128 B rows)
+  static constexpr int kPanel = 128 * 128;         // 128 rows x 64 bf16 (128-byte rows)
   static constexpr int kTile = 128 * D * 2;        // 128 rows x D bf16
   static constexpr int kQ = 0;
   static constexpr int kK = kQ + 2 * kTile;
-  static constexpr int kV = kK + kStages * kTile;
-  static constexpr int kQsum = kV + kStages * kTile;
+  static constexpr int kV = kK + kSK * kTile;
+  static constexpr int kQsum = kV + kSV * kTile;
   static constexpr int kAux = kQsum + D * 4;
   static constexpr int kBytes = kAux + (int)sizeof(TcAux);
   static constexpr int kAlloc = kBytes + 1024;     // slack to align the base to 1024 B
   static constexpr uint32_t kTmemCols = 512;
+  // TMEM columns: O_g at g*D, S_g (128 fp32; later P) after both O tiles
   __host__ __device__ static constexpr uint32_t obase(int g) { return (uint32_t)(g * D); }
   __host__ __device__ static constexpr uint32_t sbase(int g) { return (uint32_t)(2 * D + g * kNk); }
 };
@@ -79,7 +85,18 @@ __device__ __forceinline__ void timeout(TcAux* aux, int32_t* status) {
   set_status(status, TS_ERR_TIMEOUT);
 }
 
-template <int D>
+__device__ __forceinline__ float fmax32(const uint32_t (&r)[32]) {
+  float a = ptx::max3(__uint_as_float(r[0]), __uint_as_float(r[1]), __uint_as_float(r[2]));
+  float b = ptx::max3(__uint_as_float(r[3]), __uint_as_float(r[4]), __uint_as_float(r[5]));
+#pragma unroll
+  for (int x = 6; x < 30; x += 4) {
+    a = ptx::max3(a, __uint_as_float(r[x]), __uint_as_float(r[x + 1]));
+    b = ptx::max3(b, __uint_as_float(r[x + 2]), __uint_as_float(r[x + 3]));
+  }
+  return ptx::max3(a, b, fmaxf(__uint_as_float(r[30]), __uint_as_float(r[31])));
+}
+
+template <int D, bool SPLIT>
 __global__ void __launch_bounds__(kThreadsTc, 1)
 verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v,
                  const __nv_bfloat16* __restrict__ q, const int32_t* __restrict__ parents, int T,
@@ -113,9 +130,11 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
 
   // ---------------------------------------------------------------- set-up
   if (tid == 0) {
-    for (int s = 0; s < kStages; ++s) {
+    for (int s = 0; s < kSK; ++s) {
       ptx::mbar_init(&aux->k_full[s], 1);
       ptx::mbar_init(&aux->k_empty[s], 1 + 2);   // MMA commit + two importance warps
+    }
+    for (int s = 0; s < kSV; ++s) {
       ptx::mbar_init(&aux->v_full[s], 1);
       ptx::mbar_init(&aux->v_empty[s], 1);
     }
@@ -127,8 +146,9 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
     ptx::mbar_init(&aux->drain, 1);
     aux->abort_flag = 0;
     ptx::fence_mbar_init();
-    tree_masks(parents, T, aux->anc, (split == 0 && kv == 0 && rg == 0) ? status : nullptr);
   }
+  if (tid < T) aux->par[tid] = parents[tid];
+  if (tid < D) qsum[tid] = 0.f;
   if (warp == 1) {
     ptx::tmem_alloc(&aux->tmem_base, Ly::kTmemCols);
     ptx::tmem_relinquish();
@@ -152,55 +172,86 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
     *reinterpret_cast<uint4*>(sq + g * Ly::kTile + p * Ly::kPanel + t * 128 +
                               ((cc ^ (t & 7)) << 4)) = val;
   }
+  __syncthreads();
+  // summed importance queries: (16-byte column chunk, row slice) per thread
   if (do_imp) {
-    for (int c = tid; c < D; c += kThreadsTc) {
-      float s = 0.f;
-      for (int i = T - n_imp; i < T; ++i)
-        for (int g = 0; g < G; ++g) s += bf2f(q[((size_t)i * Hq + kv * G + g) * D + c]);
-      qsum[c] = s;
+    const int cg = tid % C16, slice = tid / C16, nslices = kThreadsTc / C16;
+    const int rows = n_imp * G;
+    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    for (int rr = slice; rr < rows; rr += nslices) {
+      const int i = T - n_imp + rr / G, h = kv * G + rr % G;
+      const uint4 u = *reinterpret_cast<const uint4*>(q + ((size_t)i * Hq + h) * D + cg * 8);
+      float f[8];
+      unpack_bf16x8(u, f);
+#pragma unroll
+      for (int x = 0; x < 8; ++x) acc[x] += f[x];
     }
+#pragma unroll
+    for (int x = 0; x < 8; ++x) atomicAdd(&qsum[cg * 8 + x], acc[x]);
+  }
+  // ancestor-or-self masks: node t walks its parent chain (depth < 64)
+  if (tid < T) {
+    unsigned long long m = 0ull;
+    bool bad = (tid == 0) ? (aux->par[0] != -1) : false;
+    int a = tid;
+    for (int step = 0; step < 64; ++step) {
+      m |= 1ull << a;
+      if (a == 0) break;
+      const int pa = aux->par[a];
+      if (pa < 0 || pa >= a) {
+        bad = true;
+        break;
+      }
+      a = pa;
+    }
+    aux->anc[tid] = m;
+    if (bad && split == 0 && kv == 0 && rg == 0) set_status(status, TS_ERR_INVALID_ARG);
   }
   ptx::fence_proxy_async_smem();
   ptx::tc_fence_before();
   __syncthreads();
   ptx::tc_fence_after();
   const uint32_t tmem = aux->tmem_base;
-
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       const uint64_t pol = ptx::l2_evict_first_policy();
       const int row0 = (int)(kv * L_cap + j0);
-      int j = 0;
-      for (; j < n_tiles && !aux->abort_flag; ++j) {
-        const int s = j % kStages;
-        const uint32_t ph = (uint32_t)((j / kStages) - 1) & 1u;
-        if (j >= kStages && !ptx::mbar_wait(&aux->k_empty[s], ph, kWaitCycles)) {
+      int jk = 0, jv = 0;   // tiles whose K / V load has been issued
+      for (; jk < n_tiles; ++jk) {
+        const int s = jk % kSK;
+        if (jk >= kSK &&
+            !ptx::mbar_wait(&aux->k_empty[s], (uint32_t)(jk / kSK - 1) & 1u, kWaitCycles)) {
           timeout(aux, status);
           break;
         }
         ptx::mbar_arrive_expect_tx(&aux->k_full[s], Ly::kTile);
         for (int p = 0; p < D / 64; ++p)
           ptx::tma_load_2d(sk + s * Ly::kTile + p * Ly::kPanel, &tmap_k, &aux->k_full[s], p * 64,
-                           row0 + j * kNk, pol);
-        if (j >= kStages && !ptx::mbar_wait(&aux->v_empty[s], ph, kWaitCycles)) {
+                           row0 + jk * kNk, pol);
+        const int sv_ = jv % kSV;
+        if (jv >= kSV &&
+            !ptx::mbar_wait(&aux->v_empty[sv_], (uint32_t)(jv / kSV - 1) & 1u, kWaitCycles)) {
           timeout(aux, status);
-          ++j;   // the K load of this tile is in flight
+          ++jk;
           break;
         }
-        ptx::mbar_arrive_expect_tx(&aux->v_full[s], Ly::kTile);
+        ptx::mbar_arrive_expect_tx(&aux->v_full[sv_], Ly::kTile);
         for (int p = 0; p < D / 64; ++p)
-          ptx::tma_load_2d(sv + s * Ly::kTile + p * Ly::kPanel, &tmap_v, &aux->v_full[s], p * 64,
-                           row0 + j * kNk, pol);
+          ptx::tma_load_2d(sv + sv_ * Ly::kTile + p * Ly::kPanel, &tmap_v, &aux->v_full[sv_],
+                           p * 64, row0 + jv * kNk, pol);
+        ++jv;
+        if (aux->abort_flag) {
+          ++jk;
+          break;
+        }
       }
       if (aux->abort_flag) {
-        // drain: wait (bounded) for the last loads issued into each stage
-        for (int jj = max(0, j - kStages); jj < j; ++jj) {
-          const int s = jj % kStages;
-          const uint32_t ph = (uint32_t)(jj / kStages) & 1u;
-          ptx::mbar_wait(&aux->k_full[s], ph, kWaitCycles);
-          ptx::mbar_wait(&aux->v_full[s], ph, kWaitCycles);
-        }
+        // drain: wait (bounded) for the loads issued into each stage
+        for (int t = max(0, jk - kSK); t < jk; ++t)
+          ptx::mbar_wait(&aux->k_full[t % kSK], (uint32_t)(t / kSK) & 1u, kWaitCycles);
+        for (int t = max(0, jv - kSV); t < jv; ++t)
+          ptx::mbar_wait(&aux->v_full[t % kSV], (uint32_t)(t / kSV) & 1u, kWaitCycles);
       }
     }
   } else if (warp == 1) {
@@ -209,7 +260,8 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
       constexpr uint32_t idesc_qk = ptx::idesc_bf16_f32(128, kNk, false);
       constexpr uint32_t idesc_pv = ptx::idesc_bf16_f32(128, D, true);
       const uint32_t sq_a = ptx::smem_u32(sq), sk_a = ptx::smem_u32(sk), sv_a = ptx::smem_u32(sv);
-      auto qk = [&](int g, int s) {
+      auto qk = [&](int g, int j) {
+        const int s = j % kSK;
 #pragma unroll
         for (int ks = 0; ks < D / 16; ++ks) {
           const uint32_t off = (ks >> 2) * Ly::kPanel + (ks & 3) * 32;
@@ -217,61 +269,59 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
           const uint64_t b = ptx::sdesc_sw128(sk_a + s * Ly::kTile + off, 16, 1024);
           ptx::mma_ss(tmem + Ly::sbase(g), a, b, idesc_qk, ks > 0 ? 1u : 0u);
         }
+        ptx::mma_commit(&aux->s_full[g]);
       };
-      // O += P_hi V + P_lo V: P is carried as a two-term bf16 expansion whose
-      // halves sit in columns [0, kNk/2) and [kNk/2, kNk) of the S tile
-      auto pv = [&](int g, int s, bool acc) {
+      // O += P V (P = hi [+ lo]).  Keys [32c, 32c+32) of the tile keep their
+      // bf16 hi words in S_g columns [32c, 32c+16) and lo words in
+      // [32c+16, 32c+32): K-step ks (16 keys) reads 8 columns at
+      // 32*(ks/2) + 8*(ks%2) (+16 for lo).
+      auto pv = [&](int g, int j) {
+        const int s = j % kSV;
 #pragma unroll
-        for (int half = 0; half < (kSplitP ? 2 : 1); ++half) {
+        for (int half = 0; half < (SPLIT ? 2 : 1); ++half) {
 #pragma unroll
           for (int ks = 0; ks < kNk / 16; ++ks) {
-            const uint64_t b =
-                ptx::sdesc_sw128(sv_a + s * Ly::kTile + ks * 2048, Ly::kPanel, 1024);
-            ptx::mma_ts(tmem + Ly::obase(g), tmem + Ly::sbase(g) + half * (kNk / 2) + ks * 8, b,
-                        idesc_pv, (acc || half > 0 || ks > 0) ? 1u : 0u);
+            const uint64_t b = ptx::sdesc_sw128(sv_a + s * Ly::kTile + ks * 2048, Ly::kPanel, 1024);
+            const uint32_t acol = 32 * (ks >> 1) + 8 * (ks & 1) + 16 * half;
+            ptx::mma_ts(tmem + Ly::obase(g), tmem + Ly::sbase(g) + acol, b, idesc_pv,
+                        (j > 0 || half > 0 || ks > 0) ? 1u : 0u);
           }
         }
       };
       bool ok = ptx::mbar_wait(&aux->k_full[0], 0, kWaitCycles);
       if (ok) {
         ptx::tc_fence_after();
-        for (int g = 0; g < nt; ++g) {
-          qk(g, 0);
-          ptx::mma_commit(&aux->s_full[g]);
-        }
+        for (int g = 0; g < nt; ++g) qk(g, 0);
         ptx::mma_commit(&aux->k_empty[0]);
       }
       for (int j = 0; ok && j < n_tiles; ++j) {
-        const int s = j % kStages;
-        if (!ptx::mbar_wait(&aux->v_full[s], (uint32_t)(j / kStages) & 1u, kWaitCycles)) {
+        if (!ptx::mbar_wait(&aux->v_full[j % kSV], (uint32_t)(j / kSV) & 1u, kWaitCycles)) {
           ok = false;
           break;
         }
         const bool more = j + 1 < n_tiles;
-        const int s2 = (j + 1) % kStages;
         for (int g = 0; g < nt && ok; ++g) {
           if (!ptx::mbar_wait(&aux->p_ready[g], (uint32_t)j & 1u, kWaitCycles)) {
             ok = false;
             break;
           }
           ptx::tc_fence_after();
-          pv(g, s, j > 0);
+          pv(g, j);
           if (more) {
             if (g == 0) {
-              if (!ptx::mbar_wait(&aux->k_full[s2], (uint32_t)((j + 1) / kStages) & 1u,
+              if (!ptx::mbar_wait(&aux->k_full[(j + 1) % kSK], (uint32_t)((j + 1) / kSK) & 1u,
                                   kWaitCycles)) {
                 ok = false;
                 break;
               }
               ptx::tc_fence_after();
             }
-            qk(g, s2);
-            ptx::mma_commit(&aux->s_full[g]);
+            qk(g, j + 1);
           }
         }
         if (!ok) break;
-        ptx::mma_commit(&aux->v_empty[s]);
-        if (more) ptx::mma_commit(&aux->k_empty[s2]);
+        ptx::mma_commit(&aux->v_empty[j % kSV]);
+        if (more) ptx::mma_commit(&aux->k_empty[(j + 1) % kSK]);
       }
       if (!ok) timeout(aux, status);
       ptx::mma_commit(&aux->o_final);
@@ -281,42 +331,42 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
     }
   } else if (warp < 4) {
     // ------------------------------------------------------------ importance
-    const int t = tid - 64;   // 0..63: keys t and t + 64 of each tile
+    const int t = tid - 64;   // key rows t and t + 64 of each tile
     for (int j = 0; j < n_tiles; ++j) {
-      const int s = j % kStages;
-      if (aux->abort_flag || !ptx::mbar_wait(&aux->k_full[s], (uint32_t)(j / kStages) & 1u,
+      const int s = j % kSK;
+      if (aux->abort_flag || !ptx::mbar_wait(&aux->k_full[s], (uint32_t)(j / kSK) & 1u,
                                              kWaitCycles)) {
         timeout(aux, status);
         break;
       }
       if (do_imp) {
-        const int64_t key0 = j0 + (int64_t)j * kNk;
 #pragma unroll
         for (int h2 = 0; h2 < 2; ++h2) {
           const int kr = t + 64 * h2;
-          const int64_t jj = key0 + kr;
+          const int64_t jj = j0 + (int64_t)j * kNk + kr;
           if (jj < j1) {
             const uint8_t* row = sk + s * Ly::kTile + kr * 128;
-            float acc = 0.f;
+            uint64_t acc0 = 0, acc1 = 0;   // two packed fp32 pairs
 #pragma unroll
             for (int c = 0; c < C16; ++c) {
               const int p = c >> 3, cc = c & 7;
               const uint4 u = *reinterpret_cast<const uint4*>(row + p * Ly::kPanel +
                                                               ((cc ^ (kr & 7)) << 4));
-              float f[8];
-              unpack_bf16x8(u, f);
               const float4 qa = *reinterpret_cast<const float4*>(qsum + c * 8);
               const float4 qb = *reinterpret_cast<const float4*>(qsum + c * 8 + 4);
-              acc = fmaf(f[0], qa.x, acc);
-              acc = fmaf(f[1], qa.y, acc);
-              acc = fmaf(f[2], qa.z, acc);
-              acc = fmaf(f[3], qa.w, acc);
-              acc = fmaf(f[4], qb.x, acc);
-              acc = fmaf(f[5], qb.y, acc);
-              acc = fmaf(f[6], qb.z, acc);
-              acc = fmaf(f[7], qb.w, acc);
+              acc0 = ptx::fma2(ptx::f2(__uint_as_float(u.x << 16), __uint_as_float(u.x & 0xFFFF0000u)),
+                               ptx::f2(qa.x, qa.y), acc0);
+              acc1 = ptx::fma2(ptx::f2(__uint_as_float(u.y << 16), __uint_as_float(u.y & 0xFFFF0000u)),
+                               ptx::f2(qa.z, qa.w), acc1);
+              acc0 = ptx::fma2(ptx::f2(__uint_as_float(u.z << 16), __uint_as_float(u.z & 0xFFFF0000u)),
+                               ptx::f2(qb.x, qb.y), acc0);
+              acc1 = ptx::fma2(ptx::f2(__uint_as_float(u.w << 16), __uint_as_float(u.w & 0xFFFF0000u)),
+                               ptx::f2(qb.z, qb.w), acc1);
             }
-            imp[(size_t)kv * L + jj] = acc * scale;
+            float a0, a1, b0, b1;
+            ptx::f2_split(acc0, a0, a1);
+            ptx::f2_split(acc1, b0, b1);
+            imp[(size_t)kv * L + jj] = ((a0 + a1) + (b0 + b1)) * scale;
           }
         }
       }
@@ -347,28 +397,43 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
         }
         ptx::tc_fence_after();
         const int64_t key0 = j0 + (int64_t)j * kNk;
-        const bool edge = key0 + kNk > jlim;     // uniform: depends on the tile only
-        uint32_t r[32];
-        // pass 1: tile maximum of the visible scores
-        float mx = -INFINITY;
+        const bool edge = key0 + kNk > jlim;       // uniform: depends on the tile only
+        // key0 + x is visible iff x < lim or (t_lo <= x < t_hi and its tree
+        // node x + sh is on this row's root path)
+        auto clampk = [](int64_t v) { return (int)(v < 0 ? 0 : (v > kNk ? kNk : v)); };
+        const int lim = clampk(jlim - key0);
+        const int t_lo = clampk(L - key0);
+        const int t_hi = clampk(jend - key0);
+        const int sh = (int)(key0 - L);
+        auto mask = [&](uint32_t (&r)[32], int c) {
 #pragma unroll
-        for (int c = 0; c < kNk / 32; ++c) {
-          ptx::tmem_ld32(s_addr + c * 32, r);
-          ptx::tmem_ld_wait();
-          if (!edge) {
-#pragma unroll
-            for (int x = 0; x < 32; ++x) mx = fmaxf(mx, __uint_as_float(r[x]));
-          } else {
-#pragma unroll
-            for (int x = 0; x < 32; ++x) {
-              const int64_t key = key0 + c * 32 + x;
-              const bool vis = key < jlim ||
-                               (key < jend && key >= L && ((anc >> (key - L)) & 1ull));
-              if (vis) mx = fmaxf(mx, __uint_as_float(r[x]));
-            }
+          for (int x = 0; x < 32; ++x) {
+            const int xx = 32 * c + x;
+            const bool vis = xx < lim ||
+                             (xx >= t_lo && xx < t_hi && ((anc >> ((xx + sh) & 63)) & 1ull));
+            if (!vis) r[x] = kNegInf;
           }
+        };
+        // pass 1: tile maximum
+        float mx;
+        {
+          uint32_t a0[32], a1[32], a2[32], a3[32];
+          ptx::tmem_ld32(s_addr, a0);
+          ptx::tmem_ld32(s_addr + 32, a1);
+          ptx::tmem_ld32(s_addr + 64, a2);
+          ptx::tmem_ld32(s_addr + 96, a3);
+          ptx::tmem_ld_wait();
+          if (edge) {
+            mask(a0, 0);
+            mask(a1, 1);
+            mask(a2, 2);
+            mask(a3, 3);
+          }
+          mx = fmaxf(fmaxf(fmax32(a0), fmax32(a1)), fmaxf(fmax32(a2), fmax32(a3)));
         }
-        // lazy running max: raise it only when the tile max exceeds it by 2^8
+        // lazy running max: raise it only when the tile max exceeds it by 2^8.
+        // S_g of this tile completing implies P_g V of the previous tile did
+        // (MMAs of one thread complete in order), so O_g may be rescaled.
         const float ms = mx * sl2;
         const bool raise = ms > m_used + kLazy;
         const float f = raise ? ptx::ex2(m_used - ms) : 1.f;   // 0 when m_used = -inf
@@ -388,51 +453,53 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
           }
           ptx::tmem_st_wait();
         }
-        // pass 2: P = 2^(s*sl2 - m) over the S columns, row sum.  P goes to
-        // TMEM as bf16 hi = rn(P) in columns [16c, 16c+16) and, when split,
-        // lo = rn(P - hi) in columns [64+16c, 64+16c+16).  A column is only
-        // overwritten after its S value was loaded: lo of chunks 0,1 waits
-        // for chunk 2's load, lo of chunks 2,3 for chunk 3's.
+        // pass 2: P = 2^(s*sl2 - m) -> bf16 hi [+ lo = rn(P - hi)], written over
+        // the chunk's own columns once it has been loaded; two chunks in flight
         const bool live = m_used != -INFINITY;
-        uint32_t lo_a[16], lo_b[16];
+        const uint64_t sl2x2 = ptx::f2(sl2, sl2);
+        const uint64_t negm = ptx::f2(-m_used, -m_used);
+        uint64_t lsum = 0;
+        uint32_t ca[32], cb[32];
+        auto process = [&](uint32_t (&r)[32], int c) {
+          if (edge) mask(r, c);
+          uint32_t hw[16], lw[16];
 #pragma unroll
-        for (int c = 0; c < kNk / 32; ++c) {
-          ptx::tmem_ld32(s_addr + c * 32, r);
-          ptx::tmem_ld_wait();
-          float p[32];
-#pragma unroll
-          for (int x = 0; x < 32; ++x) {
-            float e = live ? ptx::ex2(fmaf(__uint_as_float(r[x]), sl2, -m_used)) : 0.f;
-            if (edge) {
-              const int64_t key = key0 + c * 32 + x;
-              const bool vis = key < jlim ||
-                               (key < jend && key >= L && ((anc >> (key - L)) & 1ull));
-              e = vis ? e : 0.f;
-            }
-            p[x] = e;
-            l += e;
-          }
-          uint32_t pk[16];
-#pragma unroll
-          for (int x = 0; x < 16; ++x) pk[x] = ptx::pack_bf16x2(p[2 * x], p[2 * x + 1]);
-          ptx::tmem_st16(s_addr + c * 16, pk);
-          if constexpr (kSplitP) {
-            uint32_t* lo = (c & 1) ? lo_b : lo_a;
-            if (c == 2) ptx::tmem_st16(s_addr + 64, lo_a);        // chunk 0's residual
-            if (c == 3) {
-              ptx::tmem_st16(s_addr + 80, lo_b);                    // chunk 1's residual
-            }
-#pragma unroll
-            for (int x = 0; x < 16; ++x) {
-              const float h0 = __uint_as_float(pk[x] << 16);
-              const float h1 = __uint_as_float(pk[x] & 0xFFFF0000u);
-              lo[x] = ptx::pack_bf16x2(p[2 * x] - h0, p[2 * x + 1] - h1);
-            }
-            if (c == 3) {
-              ptx::tmem_st16(s_addr + 96, lo_a);                    // chunk 2's residual
-              ptx::tmem_st16(s_addr + 112, lo_b);                   // chunk 3's residual
+          for (int x = 0; x < 16; ++x) {
+            float t0, t1;
+            ptx::f2_split(ptx::fma2(ptx::f2(__uint_as_float(r[2 * x]), __uint_as_float(r[2 * x + 1])),
+                                    sl2x2, negm),
+                          t0, t1);
+            const float p0 = live ? ptx::ex2(t0) : 0.f;
+            const float p1 = live ? ptx::ex2(t1) : 0.f;
+            const uint64_t pp = ptx::f2(p0, p1);
+            lsum = ptx::add2(lsum, pp);
+            hw[x] = ptx::pack_bf16x2(p0, p1);
+            if constexpr (SPLIT) {
+              const uint64_t hh = ptx::f2(__uint_as_float(hw[x] << 16),
+                                          __uint_as_float(hw[x] & 0xFFFF0000u));
+              float r0f, r1f;
+              ptx::f2_split(ptx::sub2(pp, hh), r0f, r1f);
+              lw[x] = ptx::pack_bf16x2(r0f, r1f);
             }
           }
+          ptx::tmem_st16(s_addr + 32 * c, hw);
+          if constexpr (SPLIT) ptx::tmem_st16(s_addr + 32 * c + 16, lw);
+        };
+        ptx::tmem_ld32(s_addr, ca);
+        ptx::tmem_ld32(s_addr + 32, cb);
+        ptx::tmem_ld_wait();
+        process(ca, 0);
+        ptx::tmem_ld32(s_addr + 64, ca);
+        process(cb, 1);
+        ptx::tmem_ld_wait();
+        ptx::tmem_ld32(s_addr + 96, cb);
+        process(ca, 2);
+        ptx::tmem_ld_wait();
+        process(cb, 3);
+        {
+          float a, c;
+          ptx::f2_split(lsum, a, c);
+          l += a + c;
         }
         ptx::tmem_st_wait();
         ptx::tc_fence_before();
@@ -509,6 +576,17 @@ int make_kv_map(CUtensorMap* map, const void* base, int Hkv, int64_t L_cap, int 
   return TS_OK;
 }
 
+// P enters the P.V product as a two-term bf16 expansion unless
+// TS_ATTN_P=bf16 selects the single bf16 rounding.
+bool p_split_mode() {
+  static int v = -1;
+  if (v < 0) {
+    const char* e = getenv("TS_ATTN_P");
+    v = (e && strcmp(e, "bf16") == 0) ? 0 : 1;
+  }
+  return v == 1;
+}
+
 }  // namespace
 
 // Key splits per (KV head, row group): the count minimising waves x tiles per
@@ -543,19 +621,18 @@ int launch_verify_tc(const void* q, const void* k, const void* v, int64_t L, int
   if (rc) return rc;
   dim3 grid(n_split, Hkv, n_rg);
   auto qb = static_cast<const __nv_bfloat16*>(q);
-  if (d == 128) {
-    constexpr int smem = TcLayout<128>::kAlloc;
-    cudaFuncSetAttribute(verify_tc_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    verify_tc_kernel<128><<<grid, kThreadsTc, smem, st>>>(mk, mv, qb, parents, T, Hq, Hkv, n_imp, L,
-                                                          L_cap, keys_per_split, n_split, part_o,
-                                                          part_ml, imp, status);
-  } else {
-    constexpr int smem = TcLayout<64>::kAlloc;
-    cudaFuncSetAttribute(verify_tc_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    verify_tc_kernel<64><<<grid, kThreadsTc, smem, st>>>(mk, mv, qb, parents, T, Hq, Hkv, n_imp, L,
-                                                         L_cap, keys_per_split, n_split, part_o,
-                                                         part_ml, imp, status);
-  }
+  auto go = [&](auto kern, int smem) {
+    cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    kern<<<grid, kThreadsTc, smem, st>>>(mk, mv, qb, parents, T, Hq, Hkv, n_imp, L, L_cap,
+                                         keys_per_split, n_split, part_o, part_ml, imp, status);
+  };
+  const bool split_p = p_split_mode();
+  if (d == 128)
+    split_p ? go(verify_tc_kernel<128, true>, TcLayout<128>::kAlloc)
+            : go(verify_tc_kernel<128, false>, TcLayout<128>::kAlloc);
+  else
+    split_p ? go(verify_tc_kernel<64, true>, TcLayout<64>::kAlloc)
+            : go(verify_tc_kernel<64, false>, TcLayout<64>::kAlloc);
   return launch_status("verify_tc_kernel");
 }
 
