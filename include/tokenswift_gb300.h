@@ -80,6 +80,11 @@ int ts_version(void);
  * o       [T, Hq, d] fp32 out.   lse [T, Hq] fp32 out, or NULL.
  * imp     [Hkv, L] fp32 out, or NULL to skip importance.
  * workspace >= ts_verify_workspace_bytes(T, Hq, Hkv, d, L).
+ *
+ * Precision: Q.K^T in bf16 with fp32 accumulation; the probabilities are
+ * rounded to fp16 for the P.V product (fp32 accumulation), so V values must
+ * lie in the fp16 range |v| < 65504.  Larger values saturate to +-65504 and
+ * the kernel writes TS_ERR_UNSUPPORTED into `status`.
  * ------------------------------------------------------------------------ */
 size_t ts_verify_workspace_bytes(int T, int Hq, int Hkv, int d, int64_t L);
 int ts_verify_attention(const void* q, const void* k, const void* v,

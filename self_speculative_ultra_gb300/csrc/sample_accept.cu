@@ -13,9 +13,13 @@
 // workspace, and e_t = exp(x'_t - max x') gives the unnormalised
 // probabilities.  In rank order (x' desc, id asc) both truncations keep a
 // prefix: top-p keeps ranks up to the first whose inclusive mass reaches
-// top_p * Z, min-p keeps the ranks with e >= min_p.  "First rank whose
-// inclusive mass crosses a target" is found without sorting by a radix
-// descent over the 50-bit key (x' key, reversed id) that carries a
+// top_p * Z, min-p keeps the ranks with e >= min_p.  So the kept set always
+// lies inside the min-p set; when that set is small (the usual case:
+// min-p 0.05 keeps the tokens within ln 20 of the top logit) its members are
+// collected in the same pass that sums Z, sorted in shared memory, and the
+// top-p cut and the draw are read off their prefix sums.  Otherwise "first
+// rank whose inclusive mass crosses a target" is found without sorting by a
+// radix descent over the 50-bit key (x' key, reversed id) carrying a
 // (count, mass) histogram per digit: 3 levels on the fp32 key, 2 on the id.
 // The last CTA to finish walks the tree and writes the accepted path.
 #include "ts_common.cuh"
@@ -36,9 +40,14 @@ struct Found {
   float cum_incl;  // sum of e over ranks <= its rank
 };
 
+constexpr int kCap = 4096;               // min-p candidates sorted in shared memory
+
 struct SampleSmem {
   int cnt[kMaxBuckets];
   float mass[kMaxBuckets];
+  uint32_t ckey[kCap];                    // float_key(x') of the min-p candidates
+  int32_t cid[kCap];                      // their token ids
+  int ncand;
   float red_f[32];
   int red_i[32];
   uint32_t kpre, kmask, ipre, imask;
@@ -48,6 +57,11 @@ struct SampleSmem {
   int plen;
   int last;
 };
+
+// inverse of float_key
+__device__ __forceinline__ float key_float(uint32_t k) {
+  return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
+}
 
 __device__ float block_max(float v, SampleSmem& sm) {
   v = warp_max(v);
@@ -262,34 +276,145 @@ sample_accept_kernel(const float* __restrict__ logits, const int32_t* __restrict
   const float xmax = block_max(lmax, sm);
   __syncthreads();   // xs visible to the whole block
 
+  // Z, the min-p set {e >= min_p} (count, mass) and, while it fits, its members
+  if (tid == 0) sm.ncand = 0;
+  __syncthreads();
   float z = 0.f, zmin = 0.f;
   int nmin = 0;
-  for (int t = tid; t < V; t += kThreads) {
-    float e = expf(xs[t] - xmax);
-    z += e;
-    if (e >= min_p) {
+  const int lane = tid & 31;
+  for (int t0 = 0; t0 < V; t0 += kThreads) {
+    const int t = t0 + tid;
+    float e = 0.f, x = 0.f;
+    if (t < V) {
+      x = xs[t];
+      e = expf(x - xmax);
+      z += e;
+    }
+    const bool in = t < V && e >= min_p;
+    if (in) {
       zmin += e;
       ++nmin;
+    }
+    const unsigned m = __ballot_sync(0xffffffffu, in);
+    if (m) {
+      int base = 0;
+      if (lane == __ffs(m) - 1) base = atomicAdd(&sm.ncand, __popc(m));
+      base = __shfl_sync(0xffffffffu, base, __ffs(m) - 1);
+      const int slot = base + __popc(m & ((1u << lane) - 1));
+      if (in && slot < kCap) {
+        sm.ckey[slot] = float_key(x);
+        sm.cid[slot] = t;
+      }
     }
   }
   const float Z = block_sum(z, sm);
   float Zmin = block_sum(zmin, sm);
   int n_minp = block_sum_int(nmin, sm);
-  if (n_minp == 0) {   // min_p > 1: only rank 0 (e = 1) survives
-    n_minp = 1;
-    Zmin = 1.f;
+  int token;
+  if (n_minp >= 1 && n_minp <= kCap) {
+    // ---- fast path: the kept set is a rank prefix inside the min-p set.
+    // Sort the candidates by (x' desc, id asc) (bitonic, padded to 2^k),
+    // prefix-sum their e, cut at top-p, draw.
+    int np = 32;
+    while (np < n_minp) np <<= 1;
+    for (int q = n_minp + tid; q < np; q += kThreads) {
+      sm.ckey[q] = 0u;            // below every real key
+      sm.cid[q] = 0x7FFFFFFF;
+    }
+    __syncthreads();
+    for (int size = 2; size <= np; size <<= 1) {
+      for (int stride = size >> 1; stride > 0; stride >>= 1) {
+        for (int q = tid; q < np; q += kThreads) {
+          const int qx = q ^ stride;
+          if (qx > q) {
+            const uint32_t ka = sm.ckey[q], kb = sm.ckey[qx];
+            const int32_t ia = sm.cid[q], ib = sm.cid[qx];
+            // a ranks before b: larger key, then smaller id
+            const bool a_first = ka > kb || (ka == kb && ia < ib);
+            const bool desc = (q & size) == 0;
+            if (desc != a_first) {
+              sm.ckey[q] = kb;
+              sm.ckey[qx] = ka;
+              sm.cid[q] = ib;
+              sm.cid[qx] = ia;
+            }
+          }
+        }
+        __syncthreads();
+      }
+    }
+    if (tid < 32) {
+      // warp 0 walks the ranks: top-p cut (first inclusive mass >= top_p*Z),
+      // then the draw (first inclusive mass > u * kept mass)
+      const float tp = top_p * Z;
+      float run = 0.f, zk = 0.f;
+      int k_keep = 0;
+      for (int b0 = 0; b0 < n_minp; b0 += 32) {
+        const int r = b0 + lane;
+        const float e = r < n_minp ? expf(key_float(sm.ckey[r]) - xmax) : 0.f;
+        float incl = e;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const float y = __shfl_up_sync(0xffffffffu, incl, o);
+          if (lane >= o) incl += y;
+        }
+        incl += run;
+        const unsigned hit = __ballot_sync(0xffffffffu, r < n_minp && incl >= tp);
+        if (hit) {
+          const int src = __ffs(hit) - 1;
+          k_keep = b0 + src + 1;
+          zk = __shfl_sync(0xffffffffu, incl, src);
+          break;
+        }
+        run = __shfl_sync(0xffffffffu, incl, 31);
+      }
+      if (k_keep == 0) {             // top-p reaches past the min-p set
+        k_keep = n_minp;
+        zk = run;
+      }
+      const float target = uniforms[i] * zk;
+      run = 0.f;
+      int pick = k_keep - 1;
+      for (int b0 = 0; b0 < k_keep; b0 += 32) {
+        const int r = b0 + lane;
+        const float e = r < k_keep ? expf(key_float(sm.ckey[r]) - xmax) : 0.f;
+        float incl = e;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const float y = __shfl_up_sync(0xffffffffu, incl, o);
+          if (lane >= o) incl += y;
+        }
+        incl += run;
+        const unsigned hit = __ballot_sync(0xffffffffu, r < k_keep && incl > target);
+        if (hit) {
+          pick = b0 + __ffs(hit) - 1;
+          break;
+        }
+        run = __shfl_sync(0xffffffffu, incl, 31);
+      }
+      if (lane == 0) sm.kpre = (uint32_t)sm.cid[pick];
+    }
+    __syncthreads();
+    token = (int)sm.kpre;
+    __syncthreads();
+  } else {
+    // ---- general path: radix descent with (count, mass) histograms
+    if (n_minp == 0) {   // min_p > 1: only rank 0 (e = 1) survives
+      n_minp = 1;
+      Zmin = 1.f;
+    }
+    const Found f1 = radix_find(xs, V, xmax, kMassGE, top_p * Z, 0, sm);
+    const int k_keep = min(n_minp, f1.rank + 1);
+    const float ZK = (k_keep == f1.rank + 1) ? f1.cum_incl : Zmin;
+    const float u = uniforms[i];
+    Found f2 = radix_find(xs, V, xmax, kMassGT, u * ZK, 0, sm);
+    if (f2.rank >= k_keep) f2 = radix_find(xs, V, xmax, kRank, 0.f, k_keep - 1, sm);
+    token = f2.id;
   }
-
-  const Found f1 = radix_find(xs, V, xmax, kMassGE, top_p * Z, 0, sm);
-  const int k_keep = min(n_minp, f1.rank + 1);
-  const float ZK = (k_keep == f1.rank + 1) ? f1.cum_incl : Zmin;
-  const float u = uniforms[i];
-  Found f2 = radix_find(xs, V, xmax, kMassGT, u * ZK, 0, sm);
-  if (f2.rank >= k_keep) f2 = radix_find(xs, V, xmax, kRank, 0.f, k_keep - 1, sm);
 
   // publish this node's draw; the last CTA walks the tree
   if (tid == 0) {
-    sampled[i] = f2.id;
+    sampled[i] = token;
     __threadfence();
     int prev = atomicAdd(counter, 1);
     sm.last = (prev == T - 1);

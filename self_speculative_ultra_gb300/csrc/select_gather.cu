@@ -8,28 +8,82 @@
 // The ranking (imp desc, position asc) is a total order, so the kept
 // candidates are exactly those ranked at or above the B-th one, (tau, j_tie):
 //   keep(j) = key(j) > tau  or  (key(j) == tau and j <= j_tie),
-// with key() the order-preserving uint32 image of the fp32 score.  Stage 1
-// (one CTA per KV head) finds tau by a 4-pass 8-bit radix select over the
-// candidates, j_tie by an ordered count of the positions whose key equals
-// tau, and the number of kept positions in every chunk of the cache.  Stage 2
-// (one CTA per chunk and KV head) re-evaluates keep(), compacts the kept
-// positions in ascending order, and copies their K/V rows with 16-byte loads.
+// with key() the order-preserving uint32 image of the fp32 score.  Three
+// kernels, each over (chunk of positions, KV head), the last CTA of a head
+// finishing that head's stage (atomic ticket, no waiting):
+//   select_hist     12-bit histogram of the candidate keys [S, L-R);
+//                   last CTA: the bucket b holding the B-th best key
+//   select_collect  count keys above bucket b per chunk, append the keys of
+//                   bucket b to a list; last CTA: radix-select (tau, j_tie)
+//                   inside the list, then kept positions per chunk and their
+//                   exclusive offsets
+//   select_gather   re-evaluate keep(), compact the kept positions in
+//                   ascending order, copy their K/V rows with 16-byte loads
 #include "ts_common.cuh"
 
 namespace ts {
 
 namespace {
 
-constexpr int kSelThreads = 1024;
-constexpr int kChunk = 1024;        // positions per stage-2 CTA
-constexpr int kGatherThreads = 256;
+constexpr int kChunk = 2048;        // positions per CTA
+constexpr int kThreads = 256;
+constexpr int kResolveThreads = 1024;
+constexpr int kHistBits = 12;
+constexpr int kBins = 1 << kHistBits;
 
 struct SelectState {
   uint32_t tau;        // key of the B-th ranked candidate
   int32_t j_tie;       // largest kept position among those with key == tau
   int32_t select_all;  // L <= S+B+R: keep everything
-  int32_t pad;
+  int32_t bucket;      // top-12-bit bucket of tau
+  int32_t above;       // candidates in buckets above `bucket`
+  int32_t need;        // candidates to take from `bucket`
+  int32_t pad[2];
 };
+
+struct Counters {
+  uint32_t hist_ticket, collect_ticket, n_list, pad;
+};
+
+struct Ws {
+  SelectState* state;   // [Hkv]
+  Counters* cnt;        // [Hkv]
+  uint32_t* hist;       // [Hkv][kBins]
+  int32_t* gt;          // [Hkv][n_chunks]
+  int32_t* off;         // [Hkv][n_chunks + 1]
+  uint2* list;          // [Hkv][L]  (key, position)
+  size_t zero_bytes;    // prefix (counters + histograms) zeroed per call
+};
+
+__host__ __device__ inline size_t a256(size_t x) { return (x + 255) / 256 * 256; }
+
+__host__ __device__ inline Ws carve(void* base, int Hkv, int64_t L, int64_t n_chunks) {
+  Ws w;
+  char* p = static_cast<char*>(base);
+  size_t o = 0;
+  w.cnt = reinterpret_cast<Counters*>(p + o);
+  o += a256((size_t)Hkv * sizeof(Counters));
+  w.hist = reinterpret_cast<uint32_t*>(p + o);
+  o += a256((size_t)Hkv * kBins * sizeof(uint32_t));
+  w.zero_bytes = o;
+  w.state = reinterpret_cast<SelectState*>(p + o);
+  o += a256((size_t)Hkv * sizeof(SelectState));
+  w.gt = reinterpret_cast<int32_t*>(p + o);
+  o += a256((size_t)Hkv * n_chunks * sizeof(int32_t));
+  w.off = reinterpret_cast<int32_t*>(p + o);
+  o += a256((size_t)Hkv * (n_chunks + 1) * sizeof(int32_t));
+  w.list = reinterpret_cast<uint2*>(p + o);
+  return w;
+}
+
+__host__ inline size_t ws_total(int Hkv, int64_t L, int64_t n_chunks) {
+  size_t o = a256((size_t)Hkv * sizeof(Counters)) + a256((size_t)Hkv * kBins * sizeof(uint32_t)) +
+             a256((size_t)Hkv * sizeof(SelectState)) +
+             a256((size_t)Hkv * n_chunks * sizeof(int32_t)) +
+             a256((size_t)Hkv * (n_chunks + 1) * sizeof(int32_t)) +
+             a256((size_t)Hkv * (L > 0 ? L : 1) * sizeof(uint2));
+  return o;
+}
 
 __device__ __forceinline__ bool keep_pos(const float* __restrict__ imp_h, int64_t j, int64_t L,
                                          int S, int R, const SelectState& st) {
@@ -38,8 +92,8 @@ __device__ __forceinline__ bool keep_pos(const float* __restrict__ imp_h, int64_
   return key > st.tau || (key == st.tau && j <= st.j_tie);
 }
 
+// exclusive prefix over the block (blockDim.x a multiple of 32)
 __device__ int block_excl_scan(int x, int* warp_buf, int* total) {
-  // exclusive prefix over the block (blockDim.x multiple of 32, <= 1024)
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
   int incl = x;
 #pragma unroll
@@ -66,119 +120,215 @@ __device__ int block_excl_scan(int x, int* warp_buf, int* total) {
   return r;
 }
 
-__global__ void __launch_bounds__(kSelThreads)
-select_threshold(const float* __restrict__ imp, int64_t L, int B, int S, int R, int64_t n_chunks,
-                 SelectState* __restrict__ state, int32_t* __restrict__ chunk_off) {
-  const int kv = blockIdx.x, tid = threadIdx.x;
-  const float* imp_h = imp + (size_t)kv * L;
-  __shared__ int hist[256];
-  __shared__ uint32_t s_prefix, s_mask;
-  __shared__ int s_krem;
-  __shared__ int warp_buf[32];
-  __shared__ int s_total;
-  __shared__ SelectState st;
-
-  if (tid == 0) {
-    st.select_all = (L <= (int64_t)S + B + R) ? 1 : 0;
-    st.tau = 0;
-    st.j_tie = -1;
-    s_prefix = 0;
-    s_mask = 0;
-    s_krem = B;
+// Block-parallel bucket search: thread t takes bucket (desc ? nb-1-t : t)
+// (blockDim >= nb); finds the bucket where the running count first reaches
+// `need`; writes it and the count ranked before it (all threads return them).
+__device__ void find_bucket(const uint32_t* cnt, int nb, int need, bool desc, int* warp_buf,
+                           int* s_total, int* s_b, int* s_before) {
+  const int t = threadIdx.x;
+  const int b = desc ? nb - 1 - t : t;
+  const int c = t < nb ? (int)cnt[b] : 0;
+  const int before = block_excl_scan(c, warp_buf, s_total);
+  if (t < nb && c > 0 && before < need && before + c >= need) {
+    *s_b = b;
+    *s_before = before;
   }
   __syncthreads();
-  const int64_t lo = S, hi = L - R;
-  if (!st.select_all && B > 0) {
-    for (int pass = 0; pass < 4; ++pass) {
-      const int shift = 24 - 8 * pass;
-      for (int b = tid; b < 256; b += kSelThreads) hist[b] = 0;
-      __syncthreads();
-      const uint32_t pre = s_prefix, msk = s_mask;
-      for (int64_t j = lo + tid; j < hi; j += kSelThreads) {
-        uint32_t key = float_key(imp_h[j]);
-        if ((key & msk) == pre) atomicAdd(&hist[(key >> shift) & 255], 1);
-      }
-      __syncthreads();
-      if (tid == 0) {
-        int krem = s_krem, cum = 0, b = 255;
-        for (; b > 0; --b) {
-          if (cum + hist[b] >= krem) break;
-          cum += hist[b];
-        }
-        s_krem = krem - cum;
-        s_prefix = pre | ((uint32_t)b << shift);
-        s_mask = msk | (255u << shift);
-      }
-      __syncthreads();
-    }
-    // j_tie: the s_krem-th candidate (in position order) whose key == tau
-    const uint32_t tau = s_prefix;
-    const int need = s_krem;
-    const int64_t n = hi - lo;
-    const int64_t per = (n + kSelThreads - 1) / kSelThreads;
-    const int64_t a = lo + tid * per, e = min(hi, a + per);
-    int cnt = 0;
-    for (int64_t j = a; j < e; ++j) cnt += float_key(imp_h[j]) == tau;
-    int before = block_excl_scan(cnt, warp_buf, &s_total);
-    if (before < need && before + cnt >= need) {
-      int c = before;
-      for (int64_t j = a; j < e; ++j) {
-        if (float_key(imp_h[j]) == tau && ++c == need) {
-          st.j_tie = (int32_t)j;
+}
+
+// Ticket taken by every CTA of a head once its writes are done; true in the
+// last CTA to arrive (which then sees all of them).
+__device__ bool last_of_head(uint32_t* ticket, uint32_t n, int* s_flag) {
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();
+    *s_flag = (atomicAdd(ticket, 1u) == n - 1) ? 1 : 0;
+  }
+  __syncthreads();
+  if (*s_flag) __threadfence();
+  return *s_flag != 0;
+}
+
+__global__ void __launch_bounds__(kThreads)
+select_hist(const float* __restrict__ imp, int64_t L, int B, int S, int R, int64_t n_chunks, Ws w) {
+  const int kv = blockIdx.y, tid = threadIdx.x;
+  const int64_t c = blockIdx.x;
+  const float* imp_h = imp + (size_t)kv * L;
+  __shared__ uint32_t h[kBins];
+  __shared__ int warp_buf[32], s_total, s_last;
+  __shared__ int s_b, s_above;
+  const bool all = L <= (int64_t)S + B + R;
+  if (!all && B > 0) {
+    for (int b = tid; b < kBins; b += kThreads) h[b] = 0;
+    __syncthreads();
+    const int64_t lo = imax64(S, c * kChunk), hi = imin64(L - R, (c + 1) * kChunk);
+    for (int64_t j = lo + tid; j < hi; j += kThreads)
+      atomicAdd(&h[float_key(imp_h[j]) >> (32 - kHistBits)], 1u);
+    __syncthreads();
+    uint32_t* gh = w.hist + (size_t)kv * kBins;
+    for (int b = tid; b < kBins; b += kThreads)
+      if (h[b]) atomicAdd(&gh[b], h[b]);
+  }
+  if (!last_of_head(&w.cnt[kv].hist_ticket, (uint32_t)n_chunks, &s_last)) return;
+  // last CTA of this head: find the bucket of the B-th best key
+  SelectState st{};
+  st.select_all = all ? 1 : 0;
+  st.tau = 0xFFFFFFFFu;   // B == 0: nothing beyond sinks and recent
+  st.j_tie = -1;
+  st.bucket = -1;
+  if (!all && B > 0) {
+    volatile uint32_t* gh = w.hist + (size_t)kv * kBins;
+    // thread t owns buckets [kBins-16(t+1), kBins-16t), highest first
+    constexpr int per = kBins / kThreads;
+    const int top = kBins - 1 - tid * per;
+    int mine = 0;
+    for (int x = 0; x < per; ++x) mine += (int)gh[top - x];
+    const int before = block_excl_scan(mine, warp_buf, &s_total);
+    if (before < B && before + mine >= B) {
+      int cum = before;
+      for (int x = 0; x < per; ++x) {
+        const int cnt = (int)gh[top - x];
+        if (cum + cnt >= B) {
+          s_b = top - x;
+          s_above = cum;
           break;
         }
+        cum += cnt;
       }
     }
-    if (tid == 0) st.tau = tau;
     __syncthreads();
-  } else if (!st.select_all) {
-    // B == 0: keep only sinks and recent
-    if (tid == 0) {
-      st.tau = 0xFFFFFFFFu;
-      st.j_tie = -1;
-    }
-    __syncthreads();
+    st.bucket = s_b;
+    st.above = s_above;
+    st.need = B - s_above;
   }
-  // kept positions per chunk, then exclusive offsets
-  SelectState s = st;
-  int32_t* off = chunk_off + (size_t)kv * (n_chunks + 1);
-  const int warp = tid >> 5, lane = tid & 31;
-  for (int64_t c = warp; c < n_chunks; c += kSelThreads / 32) {
-    int cnt = 0;
-    const int64_t a = c * kChunk, e = min(L, a + kChunk);
-    for (int64_t j = a + lane; j < e; j += 32) cnt += keep_pos(imp_h, j, L, S, R, s);
-    cnt = warp_sum_int(cnt);
-    if (lane == 0) off[c] = cnt;
+  if (tid == 0) w.state[kv] = st;
+}
+
+__global__ void __launch_bounds__(kResolveThreads)
+select_collect(const float* __restrict__ imp, int64_t L, int S, int R, int64_t n_chunks, Ws w) {
+  const int kv = blockIdx.y, tid = threadIdx.x, lane = tid & 31, nthr = blockDim.x;
+  const int64_t c = blockIdx.x;
+  const float* imp_h = imp + (size_t)kv * L;
+  __shared__ int warp_buf[32], s_total, s_last;
+  __shared__ uint32_t s_cnt[1024];
+  const SelectState st0 = w.state[kv];
+  const bool work = !st0.select_all && st0.bucket >= 0;
+  uint2* list = w.list + (size_t)kv * L;
+  if (work) {
+    const uint32_t b = (uint32_t)st0.bucket;
+    const int64_t lo = imax64(S, c * kChunk), hi = imin64(L - R, (c + 1) * kChunk);
+    int gt = 0;
+    for (int64_t j0 = lo; j0 < hi; j0 += nthr) {
+      const int64_t j = j0 + tid;
+      uint32_t key = 0, bk = 0;
+      if (j < hi) {
+        key = float_key(imp_h[j]);
+        bk = key >> (32 - kHistBits);
+        gt += bk > b;
+      }
+      const bool eq = j < hi && bk == b;
+      const unsigned m = __ballot_sync(0xffffffffu, eq);
+      if (m) {
+        uint32_t base = 0;
+        if (lane == __ffs(m) - 1) base = atomicAdd(&w.cnt[kv].n_list, (uint32_t)__popc(m));
+        base = __shfl_sync(0xffffffffu, base, __ffs(m) - 1);
+        if (eq) list[base + __popc(m & ((1u << lane) - 1))] = make_uint2(key, (uint32_t)j);
+      }
+    }
+    block_excl_scan(gt, warp_buf, &s_total);
+    if (tid == 0) w.gt[(size_t)kv * n_chunks + c] = s_total;
+  }
+  if (!last_of_head(&w.cnt[kv].collect_ticket, (uint32_t)n_chunks, &s_last)) return;
+
+  // ---- last CTA of this head: (tau, j_tie) inside bucket b, then offsets
+  SelectState st = st0;
+  for (int x = tid; x < 1024; x += nthr) s_cnt[x] = 0;
+  __shared__ int s_b, s_before;
+  if (work) {
+    const uint32_t n = *(volatile uint32_t*)&w.cnt[kv].n_list;
+    uint32_t pre = (uint32_t)st.bucket << (32 - kHistBits);
+    uint32_t msk = 0xFFFFFFFFu << (32 - kHistBits);
+    int need = st.need;
+    // the remaining 20 key bits, two 10-bit levels, largest keys first
+    for (int lvl = 0; lvl < 2; ++lvl) {
+      const int shift = 10 - 10 * lvl;
+      __syncthreads();
+      for (uint32_t e = tid; e < n; e += nthr) {
+        const uint32_t key = __ldcg(&list[e].x);
+        if ((key & msk) == pre) atomicAdd(&s_cnt[(key >> shift) & 1023u], 1u);
+      }
+      __syncthreads();
+      find_bucket(s_cnt, 1024, need, true, warp_buf, &s_total, &s_b, &s_before);
+      need -= s_before;
+      pre |= (uint32_t)s_b << shift;
+      msk |= 1023u << shift;
+      for (int x = tid; x < 1024; x += nthr) s_cnt[x] = 0;
+    }
+    const uint32_t tau = pre;
+    // the need-th smallest position among keys == tau: four 8-bit levels
+    uint32_t ppre = 0, pmsk = 0;
+    for (int lvl = 0; lvl < 4; ++lvl) {
+      const int shift = 24 - 8 * lvl;
+      __syncthreads();
+      for (uint32_t e = tid; e < n; e += nthr) {
+        const uint2 v = __ldcg(&list[e]);
+        if (v.x == tau && (v.y & pmsk) == ppre) atomicAdd(&s_cnt[(v.y >> shift) & 255u], 1u);
+      }
+      __syncthreads();
+      find_bucket(s_cnt, 256, need, false, warp_buf, &s_total, &s_b, &s_before);
+      need -= s_before;
+      ppre |= (uint32_t)s_b << shift;
+      pmsk |= 255u << shift;
+      for (int x = tid; x < 1024; x += nthr) s_cnt[x] = 0;
+    }
+    st.tau = tau;
+    st.j_tie = (int32_t)ppre;
+    __syncthreads();
+    // kept positions of bucket b per chunk (n_chunks <= 1024)
+    for (uint32_t e = tid; e < n; e += nthr) {
+      const uint2 v = __ldcg(&list[e]);
+      if (v.x > tau || (v.x == tau && (int32_t)v.y <= st.j_tie)) atomicAdd(&s_cnt[v.y / kChunk], 1u);
+    }
   }
   __syncthreads();
-  if (tid == 0) {
-    int run = 0;
-    for (int64_t c = 0; c < n_chunks; ++c) {
-      int x = off[c];
-      off[c] = run;
-      run += x;
+  // offsets: forced (sinks, recent) + above-bucket + bucket picks, one chunk per thread
+  int cnt = 0;
+  const int64_t ch = tid;
+  if (ch < n_chunks) {
+    const int64_t a = ch * kChunk, e = imin64(L, a + kChunk);
+    if (st.select_all) {
+      cnt = (int)(e - a);
+    } else {
+      const int64_t f1 = imax64(0, imin64(e, S) - a);
+      const int64_t f2 = imax64(0, e - imax64(a, L - R));
+      cnt = (int)(f1 + f2);
+      if (work) cnt += __ldcg(&w.gt[(size_t)kv * n_chunks + ch]) + (int)s_cnt[ch];
     }
-    off[n_chunks] = run;
-    state[kv] = s;
+  }
+  const int before = block_excl_scan(cnt, warp_buf, &s_total);
+  int32_t* off = w.off + (size_t)kv * (n_chunks + 1);
+  if (ch < n_chunks) off[ch] = before;
+  if (tid == 0) {
+    off[n_chunks] = s_total;
+    w.state[kv] = st;
   }
 }
 
 template <int D>
-__global__ void __launch_bounds__(kGatherThreads)
+__global__ void __launch_bounds__(kThreads)
 select_gather(const float* __restrict__ imp, const __nv_bfloat16* __restrict__ k,
               const __nv_bfloat16* __restrict__ v, int64_t L, int64_t L_cap, int S, int R,
-              int64_t N, int64_t n_chunks, const SelectState* __restrict__ state,
-              const int32_t* __restrict__ chunk_off, int32_t* __restrict__ idx,
+              int64_t N, int64_t n_chunks, Ws w, int32_t* __restrict__ idx,
               __nv_bfloat16* __restrict__ kd, __nv_bfloat16* __restrict__ vd, int32_t* status) {
   const int64_t c = blockIdx.x;
   const int kv = blockIdx.y, tid = threadIdx.x;
   const float* imp_h = imp + (size_t)kv * L;
-  const SelectState s = state[kv];
-  const int32_t* off = chunk_off + (size_t)kv * (n_chunks + 1);
+  const SelectState s = w.state[kv];
+  const int32_t* off = w.off + (size_t)kv * (n_chunks + 1);
   __shared__ int warp_buf[32];
   __shared__ int s_total;
   __shared__ int32_t sel[kChunk];
-  constexpr int PER = kChunk / kGatherThreads;   // positions per thread
+  constexpr int PER = kChunk / kThreads;   // positions per thread
   const int64_t a = c * kChunk + tid * PER;
   int flags = 0, cnt = 0;
 #pragma unroll
@@ -191,7 +341,8 @@ select_gather(const float* __restrict__ imp, const __nv_bfloat16* __restrict__ k
   }
   int pos = block_excl_scan(cnt, warp_buf, &s_total);
   const int base = off[c];
-  if (tid == 0 && base + s_total > N) set_status(status, TS_ERR_INVALID_ARG);
+  if (tid == 0 && (base + s_total > N || (c == n_chunks - 1 && off[n_chunks] != N)))
+    set_status(status, TS_ERR_INVALID_ARG);
 #pragma unroll
   for (int x = 0; x < PER; ++x) {
     if (flags & (1 << x)) {
@@ -208,7 +359,7 @@ select_gather(const float* __restrict__ imp, const __nv_bfloat16* __restrict__ k
   const uint4* vsrc = reinterpret_cast<const uint4*>(v + (size_t)kv * L_cap * D);
   uint4* kdst = reinterpret_cast<uint4*>(kd + (size_t)kv * N * D);
   uint4* vdst = reinterpret_cast<uint4*>(vd + (size_t)kv * N * D);
-  for (int e = tid; e < total * V16; e += kGatherThreads) {
+  for (int e = tid; e < total * V16; e += kThreads) {
     int r = e / V16, x = e % V16;
     int64_t out = base + r;
     if (out >= N) continue;
@@ -224,9 +375,8 @@ SelectPlan select_plan(int Hkv, int64_t L) {
   SelectPlan p{};
   p.chunk = kChunk;
   p.n_chunks = (L + kChunk - 1) / kChunk;
-  size_t st = align_up((size_t)Hkv * sizeof(SelectState), 256);
-  size_t off = align_up((size_t)Hkv * (p.n_chunks + 1) * sizeof(int32_t), 256);
-  p.ws_bytes = st + off;
+  if (p.n_chunks < 1) p.n_chunks = 1;
+  p.ws_bytes = ws_total(Hkv, L, p.n_chunks);
   return p;
 }
 
@@ -235,25 +385,28 @@ int launch_select_gather(const float* imp, const void* k, const void* v, int64_t
                          void* kd, void* vd, int64_t N, void* ws, int32_t* status,
                          cudaStream_t st) {
   SelectPlan p = select_plan(Hkv, L);
-  SelectState* state = static_cast<SelectState*>(ws);
-  int32_t* off = reinterpret_cast<int32_t*>(static_cast<char*>(ws) +
-                                            align_up((size_t)Hkv * sizeof(SelectState), 256));
-  select_threshold<<<Hkv, kSelThreads, 0, st>>>(imp, L, B, S, R, p.n_chunks, state, off);
-  int rc = launch_status("select_threshold");
-  if (rc) return rc;
+  if (p.n_chunks > 1024)
+    return fail(TS_ERR_UNSUPPORTED, "ts_partial_kv_select_gather: L > %d", 1024 * kChunk);
+  Ws w = carve(ws, Hkv, L, p.n_chunks);
+  if (cudaMemsetAsync(ws, 0, w.zero_bytes, st) != cudaSuccess)
+    return launch_status("select workspace reset");
   dim3 grid((unsigned)p.n_chunks, Hkv);
+  select_hist<<<grid, kThreads, 0, st>>>(imp, L, B, S, R, p.n_chunks, w);
+  int rc = launch_status("select_hist");
+  if (rc) return rc;
+  select_collect<<<grid, kResolveThreads, 0, st>>>(imp, L, S, R, p.n_chunks, w);
+  rc = launch_status("select_collect");
+  if (rc) return rc;
   auto kb = static_cast<const __nv_bfloat16*>(k);
   auto vb = static_cast<const __nv_bfloat16*>(v);
   if (d == 128)
-    select_gather<128><<<grid, kGatherThreads, 0, st>>>(imp, kb, vb, L, L_cap, S, R, N, p.n_chunks,
-                                                        state, off, idx,
-                                                        static_cast<__nv_bfloat16*>(kd),
-                                                        static_cast<__nv_bfloat16*>(vd), status);
+    select_gather<128><<<grid, kThreads, 0, st>>>(imp, kb, vb, L, L_cap, S, R, N, p.n_chunks, w,
+                                                  idx, static_cast<__nv_bfloat16*>(kd),
+                                                  static_cast<__nv_bfloat16*>(vd), status);
   else
-    select_gather<64><<<grid, kGatherThreads, 0, st>>>(imp, kb, vb, L, L_cap, S, R, N, p.n_chunks,
-                                                       state, off, idx,
-                                                       static_cast<__nv_bfloat16*>(kd),
-                                                       static_cast<__nv_bfloat16*>(vd), status);
+    select_gather<64><<<grid, kThreads, 0, st>>>(imp, kb, vb, L, L_cap, S, R, N, p.n_chunks, w,
+                                                 idx, static_cast<__nv_bfloat16*>(kd),
+                                                 static_cast<__nv_bfloat16*>(vd), status);
   return launch_status("select_gather");
 }
 

@@ -174,31 +174,60 @@ verify_split_simple(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __
   }
 }
 
-// One CTA per (node, query head): combine the split partials.
-__global__ void verify_merge(const float* __restrict__ part_o, const float* __restrict__ part_ml,
-                             int T, int Hq, int Hkv, int D, int n_split, float* __restrict__ o,
-                             float* __restrict__ lse) {
+// One CTA per (node, query head): combine the split partials.  The split
+// weights 2^(m_s - max m) are formed once in shared memory; the partial rows
+// are then summed with independent loads.
+constexpr int kMaxSplits = 1024;
+__global__ void __launch_bounds__(128)
+verify_merge(const float* __restrict__ part_o, const float* __restrict__ part_ml,
+             int T, int Hq, int Hkv, int D, int n_split, float* __restrict__ o,
+             float* __restrict__ lse) {
+  __shared__ float wsp[kMaxSplits];
+  __shared__ float red[4], s_mx, s_l;
   const int i = blockIdx.x / Hq, h = blockIdx.x % Hq;
   const int G = Hq / Hkv, kv = h / G, row = i * G + h % G, M = T * G;
+  const int tid = threadIdx.x;
+  const size_t base = (size_t)kv * n_split * M + row;   // + s*M
   float mx = -INFINITY;
-  for (int s = 0; s < n_split; ++s) mx = fmaxf(mx, part_ml[(((size_t)kv * n_split + s) * M + row) * 2]);
+  for (int s = tid; s < n_split; s += blockDim.x) {
+    const float m = part_ml[(base + (size_t)s * M) * 2];
+    wsp[s] = m;
+    mx = fmaxf(mx, m);
+  }
+  mx = warp_max(mx);
+  if ((tid & 31) == 0) red[tid >> 5] = mx;
+  __syncthreads();
+  if (tid == 0) s_mx = fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3]));
+  __syncthreads();
+  mx = s_mx;
   float lsum = 0.f;
-  for (int s = 0; s < n_split; ++s) {
-    size_t b = ((size_t)kv * n_split + s) * M + row;
-    float ms = part_ml[b * 2];
-    if (ms != -INFINITY) lsum += part_ml[b * 2 + 1] * exp2f(ms - mx);
+  for (int s = tid; s < n_split; s += blockDim.x) {
+    const float m = wsp[s];
+    const float wgt = (m == -INFINITY) ? 0.f : exp2f(m - mx);
+    wsp[s] = wgt;
+    lsum += wgt * part_ml[(base + (size_t)s * M) * 2 + 1];
   }
+  lsum = warp_sum(lsum);
+  __syncthreads();
+  if ((tid & 31) == 0) red[tid >> 5] = lsum;
+  __syncthreads();
+  if (tid == 0) s_l = red[0] + red[1] + red[2] + red[3];
+  __syncthreads();
+  lsum = s_l;
   const float inv = 1.f / lsum;
-  for (int c = threadIdx.x; c < D; c += blockDim.x) {
-    float a = 0.f;
-    for (int s = 0; s < n_split; ++s) {
-      size_t b = ((size_t)kv * n_split + s) * M + row;
-      float ms = part_ml[b * 2];
-      if (ms != -INFINITY) a += part_o[b * D + c] * exp2f(ms - mx);
+  for (int c = tid; c < D; c += blockDim.x) {
+    float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+    int s = 0;
+    for (; s + 4 <= n_split; s += 4) {
+      a0 += wsp[s] * part_o[(base + (size_t)s * M) * D + c];
+      a1 += wsp[s + 1] * part_o[(base + (size_t)(s + 1) * M) * D + c];
+      a2 += wsp[s + 2] * part_o[(base + (size_t)(s + 2) * M) * D + c];
+      a3 += wsp[s + 3] * part_o[(base + (size_t)(s + 3) * M) * D + c];
     }
-    o[((size_t)i * Hq + h) * D + c] = a * inv;
+    for (; s < n_split; ++s) a0 += wsp[s] * part_o[(base + (size_t)s * M) * D + c];
+    o[((size_t)i * Hq + h) * D + c] = ((a0 + a1) + (a2 + a3)) * inv;
   }
-  if (lse && threadIdx.x == 0) lse[(size_t)i * Hq + h] = (mx + log2f(lsum)) * 0.6931471805599453f;
+  if (lse && tid == 0) lse[(size_t)i * Hq + h] = (mx + log2f(lsum)) * 0.6931471805599453f;
 }
 
 }  // namespace
@@ -241,6 +270,10 @@ VerifyPlan verify_plan(int T, int Hq, int Hkv, int d, int64_t L) {
     p.n_split = (int)((L + kps - 1) / kps);
   }
   if (p.n_split < 1) p.n_split = 1;
+  if (p.n_split > kMaxSplits) {   // the merge kernel holds one weight per split
+    p.keys_per_split = ((L + kMaxSplits - 1) / kMaxSplits + 127) / 128 * 128;
+    p.n_split = (int)((L + p.keys_per_split - 1) / p.keys_per_split);
+  }
   p.part_o_bytes = align_up((size_t)Hkv * p.n_split * p.M * d * sizeof(float), 256);
   p.part_ml_bytes = align_up((size_t)Hkv * p.n_split * p.M * 2 * sizeof(float), 256);
   p.ws_bytes = p.part_o_bytes + p.part_ml_bytes;

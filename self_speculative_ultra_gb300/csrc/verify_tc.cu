@@ -14,21 +14,24 @@
 // tile is read from HBM once per step.  Per 128-key tile j:
 //   TMA (warp 0)        K and V tiles -> 2-stage shared-memory rings
 //                       (128-byte swizzle, L2 evict-first)
-//   MMA (warp 1)        S_g = Q_g K^T (M=128, N=128, fp32 in TMEM); once the
-//                       softmax has written P_g over S_g, O_g += P_g V with P
-//                       read from TMEM, then at once S_g of tile j+1.  The two
-//                       row tiles ping-pong: the tensor core works on one
-//                       while the other's softmax runs.
+//   MMA (warp 1)        S_g = Q_g K^T (bf16, M=128, N=128, fp32 in TMEM); once
+//                       the softmax has written P_g over S_g, O_g += P_g V in
+//                       fp16 with P read from TMEM, then at once S_g of tile
+//                       j+1.  The two row tiles ping-pong: the tensor core
+//                       works on one while the other's softmax runs.
 //   importance (2,3)    imp_j = (sum of the group's last n_imp queries) . k_j
 //                       / sqrt(d) on CUDA cores from the same shared K tile
-//                       (the importance is linear in the queries)
-//   softmax (4..11)     one thread per query row, its 128 scores in
-//                       registers: tile max, lazy running max (O and l are
-//                       rescaled only when the max grows past 2^8),
-//                       P = 2^(s*log2e/sqrt(d) - m) back to TMEM in bf16 (or
-//                       as a two-term bf16 expansion hi + lo when SPLIT),
-//                       row sums.  Tree mask and split limits only touch the
-//                       tiles that need them.
+//                       (the importance is linear in the queries); then the
+//                       V tile is converted in place from bf16 to fp16 (exact
+//                       for |v| < 65504; larger values saturate and are
+//                       reported in the status word)
+//   softmax (4..11)     one thread per query row, its scores read from TMEM
+//                       twice (max pass, then exponent pass): tile max, lazy
+//                       running max (O and l are rescaled only when the max
+//                       grows past 2^8), P = 2^(s*log2e/sqrt(d) - m) written
+//                       back over S in fp16 (relative rounding 2^-11, four
+//                       times finer than bf16), row sums.  Tree mask and
+//                       split limits only touch the tiles that need them.
 // Each CTA writes an unnormalised partial (O, m, l) in the log2 domain; the
 // merge kernel of verify_attn.cu combines the splits.
 //
@@ -55,7 +58,7 @@ constexpr long long kWaitCycles = 1ll << 31;
 constexpr uint32_t kNegInf = 0xFF800000u;
 
 struct TcAux {
-  uint64_t k_full[kSK], k_empty[kSK], v_full[kSV], v_empty[kSV];
+  uint64_t k_full[kSK], k_empty[kSK], v_full[kSV], v_conv[kSV], v_empty[kSV];
   uint64_t s_full[2], p_ready[2], o_final, drain;
   unsigned long long anc[64];
   int32_t par[64];
@@ -96,7 +99,7 @@ __device__ __forceinline__ float fmax32(const uint32_t (&r)[32]) {
   return ptx::max3(a, b, fmaxf(__uint_as_float(r[30]), __uint_as_float(r[31])));
 }
 
-template <int D, bool SPLIT>
+template <int D>
 __global__ void __launch_bounds__(kThreadsTc, 1)
 verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v,
                  const __nv_bfloat16* __restrict__ q, const int32_t* __restrict__ parents, int T,
@@ -136,6 +139,7 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
     }
     for (int s = 0; s < kSV; ++s) {
       ptx::mbar_init(&aux->v_full[s], 1);
+      ptx::mbar_init(&aux->v_conv[s], 2);      // the two converting warps
       ptx::mbar_init(&aux->v_empty[s], 1);
     }
     for (int g = 0; g < 2; ++g) {
@@ -258,7 +262,7 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       constexpr uint32_t idesc_qk = ptx::idesc_bf16_f32(128, kNk, false);
-      constexpr uint32_t idesc_pv = ptx::idesc_bf16_f32(128, D, true);
+      constexpr uint32_t idesc_pv = ptx::idesc_f16_f32(128, D, true);
       const uint32_t sq_a = ptx::smem_u32(sq), sk_a = ptx::smem_u32(sk), sv_a = ptx::smem_u32(sv);
       auto qk = [&](int g, int j) {
         const int s = j % kSK;
@@ -271,21 +275,17 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
         }
         ptx::mma_commit(&aux->s_full[g]);
       };
-      // O += P V (P = hi [+ lo]).  Keys [32c, 32c+32) of the tile keep their
-      // bf16 hi words in S_g columns [32c, 32c+16) and lo words in
-      // [32c+16, 32c+32): K-step ks (16 keys) reads 8 columns at
-      // 32*(ks/2) + 8*(ks%2) (+16 for lo).
+      // O += P V in fp16.  Keys [32c, 32c+32) of the tile keep their fp16 P
+      // pairs in S_g columns [32c, 32c+16): K-step ks (16 keys) reads the 8
+      // columns at 32*(ks/2) + 8*(ks%2).
       auto pv = [&](int g, int j) {
         const int s = j % kSV;
 #pragma unroll
-        for (int half = 0; half < (SPLIT ? 2 : 1); ++half) {
-#pragma unroll
-          for (int ks = 0; ks < kNk / 16; ++ks) {
-            const uint64_t b = ptx::sdesc_sw128(sv_a + s * Ly::kTile + ks * 2048, Ly::kPanel, 1024);
-            const uint32_t acol = 32 * (ks >> 1) + 8 * (ks & 1) + 16 * half;
-            ptx::mma_ts(tmem + Ly::obase(g), tmem + Ly::sbase(g) + acol, b, idesc_pv,
-                        (j > 0 || half > 0 || ks > 0) ? 1u : 0u);
-          }
+        for (int ks = 0; ks < kNk / 16; ++ks) {
+          const uint64_t b = ptx::sdesc_sw128(sv_a + s * Ly::kTile + ks * 2048, Ly::kPanel, 1024);
+          const uint32_t acol = 32 * (ks >> 1) + 8 * (ks & 1);
+          ptx::mma_ts(tmem + Ly::obase(g), tmem + Ly::sbase(g) + acol, b, idesc_pv,
+                      (j > 0 || ks > 0) ? 1u : 0u);
         }
       };
       bool ok = ptx::mbar_wait(&aux->k_full[0], 0, kWaitCycles);
@@ -295,7 +295,7 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
         ptx::mma_commit(&aux->k_empty[0]);
       }
       for (int j = 0; ok && j < n_tiles; ++j) {
-        if (!ptx::mbar_wait(&aux->v_full[j % kSV], (uint32_t)(j / kSV) & 1u, kWaitCycles)) {
+        if (!ptx::mbar_wait(&aux->v_conv[j % kSV], (uint32_t)(j / kSV) & 1u, kWaitCycles)) {
           ok = false;
           break;
         }
@@ -332,6 +332,7 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
   } else if (warp < 4) {
     // ------------------------------------------------------------ importance
     const int t = tid - 64;   // key rows t and t + 64 of each tile
+    float vmax = 0.f;         // largest |v| converted (fp16 range check)
     for (int j = 0; j < n_tiles; ++j) {
       const int s = j % kSK;
       if (aux->abort_flag || !ptx::mbar_wait(&aux->k_full[s], (uint32_t)(j / kSK) & 1u,
@@ -372,7 +373,31 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
       }
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(&aux->k_empty[s]);
+      // V tile j: bf16 -> fp16 in place (element positions unchanged)
+      const int sv_ = j % kSV;
+      if (aux->abort_flag || !ptx::mbar_wait(&aux->v_full[sv_], (uint32_t)(j / kSV) & 1u,
+                                             kWaitCycles)) {
+        timeout(aux, status);
+        break;
+      }
+      uint4* vt = reinterpret_cast<uint4*>(sv + sv_ * Ly::kTile);
+#pragma unroll 4
+      for (int e = t; e < Ly::kTile / 16; e += 64) {
+        uint4 u = vt[e];
+        uint32_t* wd = reinterpret_cast<uint32_t*>(&u);
+#pragma unroll
+        for (int x = 0; x < 4; ++x) {
+          const float lo = __uint_as_float(wd[x] << 16), hi = __uint_as_float(wd[x] & 0xFFFF0000u);
+          vmax = ptx::max3(vmax, fabsf(lo), fabsf(hi));
+          wd[x] = ptx::pack_f16x2_sat(lo, hi);
+        }
+        vt[e] = u;
+      }
+      ptx::fence_proxy_async_smem();   // generic writes -> the MMA's async-proxy reads
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(&aux->v_conv[sv_]);
     }
+    if (!(vmax <= 65504.f)) set_status(status, TS_ERR_UNSUPPORTED);
   } else {
     // ------------------------------------------------------------ softmax
     const int g = (warp - 4) >> 2;
@@ -453,8 +478,8 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
           }
           ptx::tmem_st_wait();
         }
-        // pass 2: P = 2^(s*sl2 - m) -> bf16 hi [+ lo = rn(P - hi)], written over
-        // the chunk's own columns once it has been loaded; two chunks in flight
+        // pass 2: P = 2^(s*sl2 - m) -> fp16 pairs, written over the chunk's
+        // own columns once it has been loaded; two chunks in flight
         const bool live = m_used != -INFINITY;
         const uint64_t sl2x2 = ptx::f2(sl2, sl2);
         const uint64_t negm = ptx::f2(-m_used, -m_used);
@@ -462,7 +487,7 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
         uint32_t ca[32], cb[32];
         auto process = [&](uint32_t (&r)[32], int c) {
           if (edge) mask(r, c);
-          uint32_t hw[16], lw[16];
+          uint32_t pw[16];
 #pragma unroll
           for (int x = 0; x < 16; ++x) {
             float t0, t1;
@@ -471,19 +496,10 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
                           t0, t1);
             const float p0 = live ? ptx::ex2(t0) : 0.f;
             const float p1 = live ? ptx::ex2(t1) : 0.f;
-            const uint64_t pp = ptx::f2(p0, p1);
-            lsum = ptx::add2(lsum, pp);
-            hw[x] = ptx::pack_bf16x2(p0, p1);
-            if constexpr (SPLIT) {
-              const uint64_t hh = ptx::f2(__uint_as_float(hw[x] << 16),
-                                          __uint_as_float(hw[x] & 0xFFFF0000u));
-              float r0f, r1f;
-              ptx::f2_split(ptx::sub2(pp, hh), r0f, r1f);
-              lw[x] = ptx::pack_bf16x2(r0f, r1f);
-            }
+            lsum = ptx::add2(lsum, ptx::f2(p0, p1));
+            pw[x] = ptx::pack_f16x2(p0, p1);
           }
-          ptx::tmem_st16(s_addr + 32 * c, hw);
-          if constexpr (SPLIT) ptx::tmem_st16(s_addr + 32 * c + 16, lw);
+          ptx::tmem_st16(s_addr + 32 * c, pw);
         };
         ptx::tmem_ld32(s_addr, ca);
         ptx::tmem_ld32(s_addr + 32, cb);
@@ -576,17 +592,6 @@ int make_kv_map(CUtensorMap* map, const void* base, int Hkv, int64_t L_cap, int 
   return TS_OK;
 }
 
-// P enters the P.V product as a two-term bf16 expansion unless
-// TS_ATTN_P=bf16 selects the single bf16 rounding.
-bool p_split_mode() {
-  static int v = -1;
-  if (v < 0) {
-    const char* e = getenv("TS_ATTN_P");
-    v = (e && strcmp(e, "bf16") == 0) ? 0 : 1;
-  }
-  return v == 1;
-}
-
 }  // namespace
 
 // Key splits per (KV head, row group): the count minimising waves x tiles per
@@ -626,13 +631,10 @@ int launch_verify_tc(const void* q, const void* k, const void* v, int64_t L, int
     kern<<<grid, kThreadsTc, smem, st>>>(mk, mv, qb, parents, T, Hq, Hkv, n_imp, L, L_cap,
                                          keys_per_split, n_split, part_o, part_ml, imp, status);
   };
-  const bool split_p = p_split_mode();
   if (d == 128)
-    split_p ? go(verify_tc_kernel<128, true>, TcLayout<128>::kAlloc)
-            : go(verify_tc_kernel<128, false>, TcLayout<128>::kAlloc);
+    go(verify_tc_kernel<128>, TcLayout<128>::kAlloc);
   else
-    split_p ? go(verify_tc_kernel<64, true>, TcLayout<64>::kAlloc)
-            : go(verify_tc_kernel<64, false>, TcLayout<64>::kAlloc);
+    go(verify_tc_kernel<64>, TcLayout<64>::kAlloc);
   return launch_status("verify_tc_kernel");
 }
 

@@ -73,3 +73,19 @@ def test_bad_parent_sets_status():
     ts.ts_verify_attention(q, k, v, 100, pu.to_dev(par), status=status)
     torch.cuda.synchronize()
     assert int(status.item()) == 1
+
+
+def test_value_beyond_fp16_range_is_reported():
+    """P.V runs in fp16: a V entry of 1e5 cannot be represented, and the call
+    reports TS_ERR_UNSUPPORTED (2) in the status word instead of failing
+    silently."""
+    import self_speculative_ultra_gb300 as ts
+    w = syn.scaled(syn.WORKLOADS["tiny"], planted=0)
+    inp = syn.attention_inputs(w, L=300)
+    vb = inp["v"].copy()
+    vb[0, 17, 5] = syn.f32_to_bf16_bits(np.array([1e5], np.float32))[0]
+    q, k, v = pu.to_dev_bf16(inp["q"]), pu.to_dev_bf16(inp["k"]), pu.to_dev_bf16(vb)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    ts.ts_verify_attention(q, k, v, 300, pu.to_dev(inp["parents"]), status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 2
