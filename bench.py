@@ -218,7 +218,8 @@ class Step:
         self.status = torch.zeros(1, **i32)
         u8 = dict(dtype=torch.uint8, device=dev)
         self.ws_v = torch.empty(max(ts.ts_verify_workspace_bytes(T, Hq, Hkv, d, L), 256), **u8)
-        self.ws_s = torch.empty(max(ts.ts_select_workspace_bytes(Hkv, L), 256), **u8)
+        self.ws_s = torch.empty(max(ts.ts_select_batched_workspace_bytes(w.layers, Hkv, L), 256), **u8)
+        self.sel_table = ts.layer_pointer_table(self.imp, self.k, self.v, self.idx, self.kd, self.vd)
         self.ws_p = torch.empty(max(ts.ts_sample_workspace_bytes(T, w.V), 256), **u8)
         # pinned host copies of the per-step inputs and results (end-to-end leg)
         self.h_q = [torch.empty_like(x, device="cpu").pin_memory() for x in self.q]
@@ -276,10 +277,11 @@ class Step:
                                    imp=self.imp[layer], workspace=self.ws_v, status=self.status)
             if events is not None:
                 events[layer][1].record()
-            ts.ts_partial_kv_select_gather(self.imp[layer], self.k[layer], self.v[layer], self.L,
-                                           w.B, w.S, w.R, idx=self.idx[layer], kd=self.kd[layer],
-                                           vd=self.vd[layer], workspace=self.ws_s,
-                                           status=self.status)
+        # partial-cache refresh of every layer in one batched pipeline (read by
+        # the next step's drafting only)
+        ts.ts_partial_kv_select_gather_batched(self.imp, self.k, self.v, self.L, w.B, w.S, w.R,
+                                               self.idx, self.kd, self.vd, table=self.sel_table,
+                                               workspace=self.ws_s, status=self.status)
         ts.ts_penalized_sample_accept(self.logits, self.tokens, self.parents, self.prior, w.W,
                                       w.penalty, w.temperature, w.top_p, w.min_p, self.uniforms,
                                       sampled=self.sampled, path=self.path, n_path=self.n_path,
@@ -288,8 +290,9 @@ class Step:
                         status=self.status)
 
     def launches_per_step(self) -> int:
-        # verify: split kernel + merge; select: threshold + gather; sample; commit
-        return self.w.layers * 4 + 2
+        # verify: split kernel + merge per layer; batched select: histogram,
+        # collect, gather; sample; commit
+        return self.w.layers * 2 + 3 + 2
 
 
 def run_gpu(args, w: syn.Workload):

@@ -121,6 +121,22 @@ int ts_partial_kv_select_gather(const float* imp, const void* k, const void* v,
                                 void* workspace, size_t workspace_bytes,
                                 int32_t* status, void* stream);
 
+/* Batched form of (2): the same selection and gather for n_layers layers in
+ * one pipeline of launches.  The refreshed partial cache of a layer is only
+ * read by the next step's drafting, so a step may verify every layer first
+ * and refresh all partial caches together.  imp, k, v, idx, kd, vd are DEVICE
+ * arrays of n_layers pointers (each pointing at that layer's tensor with the
+ * single-layer layout above); L, L_cap, Hkv, d, B, S, R are shared.
+ * workspace >= ts_select_batched_workspace_bytes(n_layers, Hkv, L). */
+size_t ts_select_batched_workspace_bytes(int n_layers, int Hkv, int64_t L);
+int ts_partial_kv_select_gather_batched(int n_layers, const float* const* imp,
+                                        const void* const* k, const void* const* v,
+                                        int64_t L, int64_t L_cap, int Hkv, int d,
+                                        int B, int S, int R,
+                                        int32_t* const* idx, void* const* kd, void* const* vd,
+                                        int64_t* n_out, void* workspace, size_t workspace_bytes,
+                                        int32_t* status, void* stream);
+
 /* ------------------------------------------------------------------------
  * (3) Contextual-penalty sampling and exact-match tree acceptance.
  *

@@ -19,6 +19,7 @@ __all__ = [
     "TsError", "lib", "build", "ts_status_string", "ts_last_error", "ts_version",
     "ts_verify_workspace_bytes", "ts_verify_attention",
     "ts_select_workspace_bytes", "ts_partial_kv_select_gather",
+    "ts_select_batched_workspace_bytes", "ts_partial_kv_select_gather_batched", "layer_pointer_table",
     "ts_sample_workspace_bytes", "ts_penalized_sample_accept", "ts_kv_commit",
 ]
 
@@ -39,6 +40,11 @@ _SIGNATURES = {
                                            _i32, _i32, _i32, _c_void_p, _c_void_p, _c_void_p,
                                            ctypes.POINTER(_i64), _c_void_p, _sz, _c_void_p,
                                            _c_void_p]),
+    "ts_select_batched_workspace_bytes": (_sz, [_i32, _i32, _i64]),
+    "ts_partial_kv_select_gather_batched": (_i32, [_i32, _c_void_p, _c_void_p, _c_void_p, _i64, _i64,
+                                                   _i32, _i32, _i32, _i32, _i32, _c_void_p,
+                                                   _c_void_p, _c_void_p, ctypes.POINTER(_i64),
+                                                   _c_void_p, _sz, _c_void_p, _c_void_p]),
     "ts_sample_workspace_bytes": (_sz, [_i32, _i32]),
     "ts_penalized_sample_accept": (_i32, [_c_void_p, _c_void_p, _c_void_p, _i32, _c_void_p, _i32,
                                           _i32, _i32, _f32, _f32, _f32, _f32, _c_void_p,
@@ -177,6 +183,43 @@ def ts_partial_kv_select_gather(imp, k, v, L, B, S, R, idx=None, kd=None, vd=Non
     _check(rc)
     assert n_out.value == N
     return idx, kd, vd
+
+
+def ts_select_batched_workspace_bytes(n_layers, Hkv, L) -> int:
+    return lib().ts_select_batched_workspace_bytes(n_layers, Hkv, L)
+
+
+def layer_pointer_table(imps, ks, vs, idxs, kds, vds):
+    """Device table [6, n_layers] of the per-layer tensor addresses the batched
+    selection reads (build it once and reuse it while the tensors live)."""
+    rows = [imps, ks, vs, idxs, kds, vds]
+    n = len(imps)
+    if any(len(r) != n for r in rows):
+        raise ValueError("every per-layer list must have n_layers entries")
+    host = torch.tensor([[t.data_ptr() for t in r] for r in rows], dtype=torch.int64)
+    return host.to(imps[0].device)
+
+
+def ts_partial_kv_select_gather_batched(imps, ks, vs, L, B, S, R, idxs, kds, vds, table=None,
+                                        workspace=None, status=None, stream=None):
+    """Selection + gather for several layers in one pipeline of launches.
+    Lists of per-layer tensors with the single-layer shapes."""
+    n = len(imps)
+    Hkv, L_cap, d = ks[0].shape
+    for i in range(n):
+        _dev(imps[i], torch.float32, "imp", (Hkv, L))
+        _dev(ks[i], torch.bfloat16, "k", (Hkv, L_cap, d))
+        _dev(vs[i], torch.bfloat16, "v", (Hkv, L_cap, d))
+    if table is None:
+        table = layer_pointer_table(imps, ks, vs, idxs, kds, vds)
+    ws, nb = _workspace(ts_select_batched_workspace_bytes(n, Hkv, L), ks[0].device, workspace)
+    n_out = _i64(0)
+    row = lambda r: ctypes.c_void_p(table[r].data_ptr())  # noqa: E731
+    rc = lib().ts_partial_kv_select_gather_batched(n, row(0), row(1), row(2), L, L_cap, Hkv, d, B,
+                                                   S, R, row(3), row(4), row(5), ctypes.byref(n_out),
+                                                   _ptr(ws), nb, _ptr(status), _stream(stream))
+    _check(rc)
+    return idxs, kds, vds
 
 
 def ts_sample_workspace_bytes(T, V) -> int:

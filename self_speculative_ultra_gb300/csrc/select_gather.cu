@@ -9,8 +9,8 @@
 // candidates are exactly those ranked at or above the B-th one, (tau, j_tie):
 //   keep(j) = key(j) > tau  or  (key(j) == tau and j <= j_tie),
 // with key() the order-preserving uint32 image of the fp32 score.  Three
-// kernels, each over (chunk of positions, KV head), the last CTA of a head
-// finishing that head's stage (atomic ticket, no waiting):
+// kernels, each over (chunk of positions, KV head, layer), the last CTA of a
+// (layer, head) finishing its stage (atomic ticket, no waiting):
 //   select_hist     12-bit histogram of the candidate keys [S, L-R);
 //                   last CTA: the bucket b holding the B-th best key
 //   select_collect  count keys above bucket b per chunk, append the keys of
@@ -25,9 +25,10 @@ namespace ts {
 
 namespace {
 
-constexpr int kChunk = 2048;        // positions per CTA
+constexpr int kChunk = 2048;        // positions per gather CTA (and per offset)
+constexpr int kScan = 8192;         // positions per histogram / collect CTA
+constexpr int kPerScan = kScan / kChunk;
 constexpr int kThreads = 256;
-constexpr int kResolveThreads = 1024;
 constexpr int kHistBits = 12;
 constexpr int kBins = 1 << kHistBits;
 
@@ -85,6 +86,24 @@ __host__ inline size_t ws_total(int Hkv, int64_t L, int64_t n_chunks) {
   return o;
 }
 
+// Per-layer tensors: device arrays of per-layer pointers (batched call) or,
+// when those are null, the single layer's pointers.
+struct Layers {
+  const float* const* imp;
+  const __nv_bfloat16* const* k;
+  const __nv_bfloat16* const* v;
+  int32_t* const* idx;
+  __nv_bfloat16* const* kd;
+  __nv_bfloat16* const* vd;
+  const float* imp1;
+  const __nv_bfloat16* k1;
+  const __nv_bfloat16* v1;
+  int32_t* idx1;
+  __nv_bfloat16* kd1;
+  __nv_bfloat16* vd1;
+};
+__device__ __forceinline__ const float* imp_of(const Layers& P, int l) { return P.imp ? P.imp[l] : P.imp1; }
+
 __device__ __forceinline__ bool keep_pos(const float* __restrict__ imp_h, int64_t j, int64_t L,
                                          int S, int R, const SelectState& st) {
   if (st.select_all || j < S || j >= L - R) return true;
@@ -120,18 +139,31 @@ __device__ int block_excl_scan(int x, int* warp_buf, int* total) {
   return r;
 }
 
-// Block-parallel bucket search: thread t takes bucket (desc ? nb-1-t : t)
-// (blockDim >= nb); finds the bucket where the running count first reaches
-// `need`; writes it and the count ranked before it (all threads return them).
+// Block-parallel bucket search over nb buckets (nb a multiple of blockDim):
+// thread t takes a run of nb/blockDim consecutive buckets in scan order
+// (descending bucket index if `desc`), finds the bucket where the running
+// count first reaches `need`, and publishes it with the count before it.
 __device__ void find_bucket(const uint32_t* cnt, int nb, int need, bool desc, int* warp_buf,
                            int* s_total, int* s_b, int* s_before) {
-  const int t = threadIdx.x;
-  const int b = desc ? nb - 1 - t : t;
-  const int c = t < nb ? (int)cnt[b] : 0;
-  const int before = block_excl_scan(c, warp_buf, s_total);
-  if (t < nb && c > 0 && before < need && before + c >= need) {
-    *s_b = b;
-    *s_before = before;
+  const int per = nb / blockDim.x, t = threadIdx.x;
+  int mine = 0;
+  for (int x = 0; x < per; ++x) {
+    const int r = t * per + x;
+    mine += (int)cnt[desc ? nb - 1 - r : r];
+  }
+  const int before = block_excl_scan(mine, warp_buf, s_total);
+  if (mine > 0 && before < need && before + mine >= need) {
+    int cum = before;
+    for (int x = 0; x < per; ++x) {
+      const int r = t * per + x, b = desc ? nb - 1 - r : r;
+      const int c = (int)cnt[b];
+      if (cum + c >= need) {
+        *s_b = b;
+        *s_before = cum;
+        break;
+      }
+      cum += c;
+    }
   }
   __syncthreads();
 }
@@ -150,10 +182,11 @@ __device__ bool last_of_head(uint32_t* ticket, uint32_t n, int* s_flag) {
 }
 
 __global__ void __launch_bounds__(kThreads)
-select_hist(const float* __restrict__ imp, int64_t L, int B, int S, int R, int64_t n_chunks, Ws w) {
-  const int kv = blockIdx.y, tid = threadIdx.x;
+select_hist(Layers P, int64_t L, int B, int S, int R, int64_t n_chunks, Ws w) {
+  const int kv = blockIdx.y, tid = threadIdx.x, layer = blockIdx.z;
+  const int hh = layer * gridDim.y + kv;   // (layer, KV head) slot in the workspace
   const int64_t c = blockIdx.x;
-  const float* imp_h = imp + (size_t)kv * L;
+  const float* imp_h = imp_of(P, layer) + (size_t)kv * L;
   __shared__ uint32_t h[kBins];
   __shared__ int warp_buf[32], s_total, s_last;
   __shared__ int s_b, s_above;
@@ -161,15 +194,15 @@ select_hist(const float* __restrict__ imp, int64_t L, int B, int S, int R, int64
   if (!all && B > 0) {
     for (int b = tid; b < kBins; b += kThreads) h[b] = 0;
     __syncthreads();
-    const int64_t lo = imax64(S, c * kChunk), hi = imin64(L - R, (c + 1) * kChunk);
+    const int64_t lo = imax64(S, c * kScan), hi = imin64(L - R, (c + 1) * kScan);
     for (int64_t j = lo + tid; j < hi; j += kThreads)
       atomicAdd(&h[float_key(imp_h[j]) >> (32 - kHistBits)], 1u);
     __syncthreads();
-    uint32_t* gh = w.hist + (size_t)kv * kBins;
+    uint32_t* gh = w.hist + (size_t)hh * kBins;
     for (int b = tid; b < kBins; b += kThreads)
       if (h[b]) atomicAdd(&gh[b], h[b]);
   }
-  if (!last_of_head(&w.cnt[kv].hist_ticket, (uint32_t)n_chunks, &s_last)) return;
+  if (!last_of_head(&w.cnt[hh].hist_ticket, (uint32_t)gridDim.x, &s_last)) return;
   // last CTA of this head: find the bucket of the B-th best key
   SelectState st{};
   st.select_all = all ? 1 : 0;
@@ -177,7 +210,7 @@ select_hist(const float* __restrict__ imp, int64_t L, int B, int S, int R, int64
   st.j_tie = -1;
   st.bucket = -1;
   if (!all && B > 0) {
-    volatile uint32_t* gh = w.hist + (size_t)kv * kBins;
+    volatile uint32_t* gh = w.hist + (size_t)hh * kBins;
     // thread t owns buckets [kBins-16(t+1), kBins-16t), highest first
     constexpr int per = kBins / kThreads;
     const int top = kBins - 1 - tid * per;
@@ -201,51 +234,57 @@ select_hist(const float* __restrict__ imp, int64_t L, int B, int S, int R, int64
     st.above = s_above;
     st.need = B - s_above;
   }
-  if (tid == 0) w.state[kv] = st;
+  if (tid == 0) w.state[hh] = st;
 }
 
-__global__ void __launch_bounds__(kResolveThreads)
-select_collect(const float* __restrict__ imp, int64_t L, int S, int R, int64_t n_chunks, Ws w) {
+__global__ void __launch_bounds__(kThreads)
+select_collect(Layers P, int64_t L, int S, int R, int64_t n_chunks, Ws w) {
   const int kv = blockIdx.y, tid = threadIdx.x, lane = tid & 31, nthr = blockDim.x;
+  const int layer = blockIdx.z, hh = layer * gridDim.y + kv;
   const int64_t c = blockIdx.x;
-  const float* imp_h = imp + (size_t)kv * L;
+  const float* imp_h = imp_of(P, layer) + (size_t)kv * L;
   __shared__ int warp_buf[32], s_total, s_last;
   __shared__ uint32_t s_cnt[1024];
-  const SelectState st0 = w.state[kv];
+  __shared__ int s_gt[kPerScan];
+  const SelectState st0 = w.state[hh];
   const bool work = !st0.select_all && st0.bucket >= 0;
-  uint2* list = w.list + (size_t)kv * L;
+  uint2* list = w.list + (size_t)hh * L;
   if (work) {
     const uint32_t b = (uint32_t)st0.bucket;
-    const int64_t lo = imax64(S, c * kChunk), hi = imin64(L - R, (c + 1) * kChunk);
-    int gt = 0;
+    if (tid < kPerScan) s_gt[tid] = 0;
+    __syncthreads();
+    const int64_t lo = imax64(S, c * kScan), hi = imin64(L - R, (c + 1) * kScan);
     for (int64_t j0 = lo; j0 < hi; j0 += nthr) {
       const int64_t j = j0 + tid;
       uint32_t key = 0, bk = 0;
       if (j < hi) {
         key = float_key(imp_h[j]);
         bk = key >> (32 - kHistBits);
-        gt += bk > b;
       }
+      // keys above bucket b, counted per gather chunk
+      if (j < hi && bk > b) atomicAdd(&s_gt[(int)(j / kChunk - c * kPerScan)], 1);
       const bool eq = j < hi && bk == b;
       const unsigned m = __ballot_sync(0xffffffffu, eq);
       if (m) {
         uint32_t base = 0;
-        if (lane == __ffs(m) - 1) base = atomicAdd(&w.cnt[kv].n_list, (uint32_t)__popc(m));
+        if (lane == __ffs(m) - 1) base = atomicAdd(&w.cnt[hh].n_list, (uint32_t)__popc(m));
         base = __shfl_sync(0xffffffffu, base, __ffs(m) - 1);
         if (eq) list[base + __popc(m & ((1u << lane) - 1))] = make_uint2(key, (uint32_t)j);
       }
     }
-    block_excl_scan(gt, warp_buf, &s_total);
-    if (tid == 0) w.gt[(size_t)kv * n_chunks + c] = s_total;
+    __syncthreads();
+    if (tid < kPerScan && c * kPerScan + tid < n_chunks)
+      w.gt[(size_t)hh * n_chunks + c * kPerScan + tid] = s_gt[tid];
   }
-  if (!last_of_head(&w.cnt[kv].collect_ticket, (uint32_t)n_chunks, &s_last)) return;
+  if (!last_of_head(&w.cnt[hh].collect_ticket, (uint32_t)gridDim.x, &s_last)) return;
 
   // ---- last CTA of this head: (tau, j_tie) inside bucket b, then offsets
   SelectState st = st0;
   for (int x = tid; x < 1024; x += nthr) s_cnt[x] = 0;
+  __syncthreads();
   __shared__ int s_b, s_before;
   if (work) {
-    const uint32_t n = *(volatile uint32_t*)&w.cnt[kv].n_list;
+    const uint32_t n = *(volatile uint32_t*)&w.cnt[hh].n_list;
     uint32_t pre = (uint32_t)st.bucket << (32 - kHistBits);
     uint32_t msk = 0xFFFFFFFFu << (32 - kHistBits);
     int need = st.need;
@@ -291,40 +330,56 @@ select_collect(const float* __restrict__ imp, int64_t L, int S, int R, int64_t n
     }
   }
   __syncthreads();
-  // offsets: forced (sinks, recent) + above-bucket + bucket picks, one chunk per thread
-  int cnt = 0;
-  const int64_t ch = tid;
-  if (ch < n_chunks) {
-    const int64_t a = ch * kChunk, e = imin64(L, a + kChunk);
-    if (st.select_all) {
-      cnt = (int)(e - a);
-    } else {
-      const int64_t f1 = imax64(0, imin64(e, S) - a);
-      const int64_t f2 = imax64(0, e - imax64(a, L - R));
-      cnt = (int)(f1 + f2);
-      if (work) cnt += __ldcg(&w.gt[(size_t)kv * n_chunks + ch]) + (int)s_cnt[ch];
+  // offsets: forced (sinks, recent) + above-bucket + bucket picks; thread t
+  // takes gather chunks [4t, 4t+4)
+  int cnts[4], mine = 0;
+#pragma unroll
+  for (int x = 0; x < 4; ++x) {
+    const int64_t ch = (int64_t)tid * 4 + x;
+    int cnt = 0;
+    if (ch < n_chunks) {
+      const int64_t a = ch * kChunk, e = imin64(L, a + kChunk);
+      if (st.select_all) {
+        cnt = (int)(e - a);
+      } else {
+        const int64_t f1 = imax64(0, imin64(e, S) - a);
+        const int64_t f2 = imax64(0, e - imax64(a, L - R));
+        cnt = (int)(f1 + f2);
+        if (work) cnt += __ldcg(&w.gt[(size_t)hh * n_chunks + ch]) + (int)s_cnt[ch];
+      }
     }
+    cnts[x] = cnt;
+    mine += cnt;
   }
-  const int before = block_excl_scan(cnt, warp_buf, &s_total);
-  int32_t* off = w.off + (size_t)kv * (n_chunks + 1);
-  if (ch < n_chunks) off[ch] = before;
+  int before = block_excl_scan(mine, warp_buf, &s_total);
+  int32_t* off = w.off + (size_t)hh * (n_chunks + 1);
+#pragma unroll
+  for (int x = 0; x < 4; ++x) {
+    const int64_t ch = (int64_t)tid * 4 + x;
+    if (ch < n_chunks) off[ch] = before;
+    before += cnts[x];
+  }
   if (tid == 0) {
     off[n_chunks] = s_total;
-    w.state[kv] = st;
+    w.state[hh] = st;
   }
 }
 
 template <int D>
 __global__ void __launch_bounds__(kThreads)
-select_gather(const float* __restrict__ imp, const __nv_bfloat16* __restrict__ k,
-              const __nv_bfloat16* __restrict__ v, int64_t L, int64_t L_cap, int S, int R,
-              int64_t N, int64_t n_chunks, Ws w, int32_t* __restrict__ idx,
-              __nv_bfloat16* __restrict__ kd, __nv_bfloat16* __restrict__ vd, int32_t* status) {
+select_gather(Layers P, int64_t L, int64_t L_cap, int S, int R, int64_t N, int64_t n_chunks,
+              Ws w, int32_t* status) {
   const int64_t c = blockIdx.x;
-  const int kv = blockIdx.y, tid = threadIdx.x;
-  const float* imp_h = imp + (size_t)kv * L;
-  const SelectState s = w.state[kv];
-  const int32_t* off = w.off + (size_t)kv * (n_chunks + 1);
+  const int kv = blockIdx.y, tid = threadIdx.x, layer = blockIdx.z;
+  const int hh = layer * gridDim.y + kv;
+  const float* imp_h = imp_of(P, layer) + (size_t)kv * L;
+  const __nv_bfloat16* k = P.k ? P.k[layer] : P.k1;
+  const __nv_bfloat16* v = P.v ? P.v[layer] : P.v1;
+  int32_t* idx = P.idx ? P.idx[layer] : P.idx1;
+  __nv_bfloat16* kd = P.kd ? P.kd[layer] : P.kd1;
+  __nv_bfloat16* vd = P.vd ? P.vd[layer] : P.vd1;
+  const SelectState s = w.state[hh];
+  const int32_t* off = w.off + (size_t)hh * (n_chunks + 1);
   __shared__ int warp_buf[32];
   __shared__ int s_total;
   __shared__ int32_t sel[kChunk];
@@ -371,43 +426,65 @@ select_gather(const float* __restrict__ imp, const __nv_bfloat16* __restrict__ k
 
 }  // namespace
 
-SelectPlan select_plan(int Hkv, int64_t L) {
+SelectPlan select_plan(int Hkv, int64_t L, int n_layers) {
   SelectPlan p{};
   p.chunk = kChunk;
   p.n_chunks = (L + kChunk - 1) / kChunk;
   if (p.n_chunks < 1) p.n_chunks = 1;
-  p.ws_bytes = ws_total(Hkv, L, p.n_chunks);
+  p.ws_bytes = ws_total(Hkv * n_layers, L, p.n_chunks);
   return p;
+}
+
+static int run_select(const Layers& P, int n_layers, int64_t L, int64_t L_cap, int Hkv, int d,
+                      int B, int S, int R, int64_t N, void* ws, int32_t* status, cudaStream_t st) {
+  SelectPlan p = select_plan(Hkv, L, n_layers);
+  if (p.n_chunks > 1024)
+    return fail(TS_ERR_UNSUPPORTED, "ts_partial_kv_select_gather: L > %d", 1024 * kChunk);
+  Ws w = carve(ws, Hkv * n_layers, L, p.n_chunks);
+  if (cudaMemsetAsync(ws, 0, w.zero_bytes, st) != cudaSuccess)
+    return launch_status("select workspace reset");
+  dim3 grid((unsigned)p.n_chunks, Hkv, n_layers);
+  dim3 sgrid((unsigned)((L + kScan - 1) / kScan), Hkv, n_layers);
+  select_hist<<<sgrid, kThreads, 0, st>>>(P, L, B, S, R, p.n_chunks, w);
+  int rc = launch_status("select_hist");
+  if (rc) return rc;
+  select_collect<<<sgrid, kThreads, 0, st>>>(P, L, S, R, p.n_chunks, w);
+  rc = launch_status("select_collect");
+  if (rc) return rc;
+  if (d == 128)
+    select_gather<128><<<grid, kThreads, 0, st>>>(P, L, L_cap, S, R, N, p.n_chunks, w, status);
+  else
+    select_gather<64><<<grid, kThreads, 0, st>>>(P, L, L_cap, S, R, N, p.n_chunks, w, status);
+  return launch_status("select_gather");
 }
 
 int launch_select_gather(const float* imp, const void* k, const void* v, int64_t L,
                          int64_t L_cap, int Hkv, int d, int B, int S, int R, int32_t* idx,
                          void* kd, void* vd, int64_t N, void* ws, int32_t* status,
                          cudaStream_t st) {
-  SelectPlan p = select_plan(Hkv, L);
-  if (p.n_chunks > 1024)
-    return fail(TS_ERR_UNSUPPORTED, "ts_partial_kv_select_gather: L > %d", 1024 * kChunk);
-  Ws w = carve(ws, Hkv, L, p.n_chunks);
-  if (cudaMemsetAsync(ws, 0, w.zero_bytes, st) != cudaSuccess)
-    return launch_status("select workspace reset");
-  dim3 grid((unsigned)p.n_chunks, Hkv);
-  select_hist<<<grid, kThreads, 0, st>>>(imp, L, B, S, R, p.n_chunks, w);
-  int rc = launch_status("select_hist");
-  if (rc) return rc;
-  select_collect<<<grid, kResolveThreads, 0, st>>>(imp, L, S, R, p.n_chunks, w);
-  rc = launch_status("select_collect");
-  if (rc) return rc;
-  auto kb = static_cast<const __nv_bfloat16*>(k);
-  auto vb = static_cast<const __nv_bfloat16*>(v);
-  if (d == 128)
-    select_gather<128><<<grid, kThreads, 0, st>>>(imp, kb, vb, L, L_cap, S, R, N, p.n_chunks, w,
-                                                  idx, static_cast<__nv_bfloat16*>(kd),
-                                                  static_cast<__nv_bfloat16*>(vd), status);
-  else
-    select_gather<64><<<grid, kThreads, 0, st>>>(imp, kb, vb, L, L_cap, S, R, N, p.n_chunks, w,
-                                                 idx, static_cast<__nv_bfloat16*>(kd),
-                                                 static_cast<__nv_bfloat16*>(vd), status);
-  return launch_status("select_gather");
+  Layers P{};
+  P.imp1 = imp;
+  P.k1 = static_cast<const __nv_bfloat16*>(k);
+  P.v1 = static_cast<const __nv_bfloat16*>(v);
+  P.idx1 = idx;
+  P.kd1 = static_cast<__nv_bfloat16*>(kd);
+  P.vd1 = static_cast<__nv_bfloat16*>(vd);
+  return run_select(P, 1, L, L_cap, Hkv, d, B, S, R, N, ws, status, st);
+}
+
+int launch_select_gather_batched(int n_layers, const float* const* imp, const void* const* k,
+                                 const void* const* v, int64_t L, int64_t L_cap, int Hkv, int d,
+                                 int B, int S, int R, int32_t* const* idx, void* const* kd,
+                                 void* const* vd, int64_t N, void* ws, int32_t* status,
+                                 cudaStream_t st) {
+  Layers P{};
+  P.imp = imp;
+  P.k = reinterpret_cast<const __nv_bfloat16* const*>(k);
+  P.v = reinterpret_cast<const __nv_bfloat16* const*>(v);
+  P.idx = idx;
+  P.kd = reinterpret_cast<__nv_bfloat16* const*>(kd);
+  P.vd = reinterpret_cast<__nv_bfloat16* const*>(vd);
+  return run_select(P, n_layers, L, L_cap, Hkv, d, B, S, R, N, ws, status, st);
 }
 
 }  // namespace ts

@@ -97,7 +97,12 @@ int ts_verify_attention(const void* q, const void* k, const void* v, int64_t L, 
 
 size_t ts_select_workspace_bytes(int Hkv, int64_t L) {
   if (Hkv < 1 || L < 0) return 0;
-  return select_plan(Hkv, L).ws_bytes;
+  return select_plan(Hkv, L, 1).ws_bytes;
+}
+
+size_t ts_select_batched_workspace_bytes(int n_layers, int Hkv, int64_t L) {
+  if (n_layers < 1 || Hkv < 1 || L < 0) return 0;
+  return select_plan(Hkv, L, n_layers).ws_bytes;
 }
 
 int ts_partial_kv_select_gather(const float* imp, const void* k, const void* v, int64_t L,
@@ -116,11 +121,37 @@ int ts_partial_kv_select_gather(const float* imp, const void* k, const void* v, 
   if (n_out) *n_out = N;
   if (L == 0) return TS_OK;
   if (!imp || !k || !v || !idx || !kd || !vd) return fail(TS_ERR_INVALID_ARG, "%s: NULL tensor", W);
-  SelectPlan p = select_plan(Hkv, L);
+  SelectPlan p = select_plan(Hkv, L, 1);
   int rc = check_ws(workspace, workspace_bytes, p.ws_bytes, W);
   if (rc) return rc;
   return launch_select_gather(imp, k, v, L, L_cap, Hkv, d, B, S, R, idx, kd, vd, N, workspace,
                               status, static_cast<cudaStream_t>(stream));
+}
+
+int ts_partial_kv_select_gather_batched(int n_layers, const float* const* imp,
+                                        const void* const* k, const void* const* v, int64_t L,
+                                        int64_t L_cap, int Hkv, int d, int B, int S, int R,
+                                        int32_t* const* idx, void* const* kd, void* const* vd,
+                                        int64_t* n_out, void* workspace, size_t workspace_bytes,
+                                        int32_t* status, void* stream) {
+  clear_error();
+  const char* W = "ts_partial_kv_select_gather_batched";
+  if (n_layers < 1 || n_layers > 65535)
+    return fail(TS_ERR_INVALID_ARG, "%s: n_layers=%d", W, n_layers);
+  if (Hkv < 1) return fail(TS_ERR_INVALID_ARG, "%s: Hkv=%d", W, Hkv);
+  if (d != 64 && d != 128) return fail(TS_ERR_UNSUPPORTED, "%s: head dim %d not in {64,128}", W, d);
+  if (B < 0 || S < 0 || R < 0) return fail(TS_ERR_INVALID_ARG, "%s: B, S, R must be >= 0", W);
+  if (L < 0 || L > L_cap) return fail(TS_ERR_INVALID_ARG, "%s: need 0 <= L <= L_cap", W);
+  if (L_cap > (int64_t(1) << 31) - 1) return fail(TS_ERR_UNSUPPORTED, "%s: L_cap >= 2^31", W);
+  int64_t N = L < (int64_t)S + B + R ? L : (int64_t)S + B + R;
+  if (n_out) *n_out = N;
+  if (L == 0) return TS_OK;
+  if (!imp || !k || !v || !idx || !kd || !vd) return fail(TS_ERR_INVALID_ARG, "%s: NULL array", W);
+  SelectPlan p = select_plan(Hkv, L, n_layers);
+  int rc = check_ws(workspace, workspace_bytes, p.ws_bytes, W);
+  if (rc) return rc;
+  return launch_select_gather_batched(n_layers, imp, k, v, L, L_cap, Hkv, d, B, S, R, idx, kd, vd,
+                                      N, workspace, status, static_cast<cudaStream_t>(stream));
 }
 
 size_t ts_sample_workspace_bytes(int T, int V) {

@@ -105,11 +105,17 @@ struct SelectPlan {
   int64_t n_chunks;
   size_t ws_bytes;
 };
-SelectPlan select_plan(int Hkv, int64_t L);
+SelectPlan select_plan(int Hkv, int64_t L, int n_layers);
 int launch_select_gather(const float* imp, const void* k, const void* v, int64_t L,
                          int64_t L_cap, int Hkv, int d, int B, int S, int R, int32_t* idx,
                          void* kd, void* vd, int64_t N, void* ws, int32_t* status,
                          cudaStream_t st);
+
+int launch_select_gather_batched(int n_layers, const float* const* imp, const void* const* k,
+                                 const void* const* v, int64_t L, int64_t L_cap, int Hkv, int d,
+                                 int B, int S, int R, int32_t* const* idx, void* const* kd,
+                                 void* const* vd, int64_t N, void* ws, int32_t* status,
+                                 cudaStream_t st);
 
 size_t sample_ws_bytes(int T, int V);
 int launch_sample_accept(const float* logits, const int32_t* tree_tokens, const int32_t* parents,

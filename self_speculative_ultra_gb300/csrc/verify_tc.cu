@@ -21,10 +21,7 @@
 //                       works on one while the other's softmax runs.
 //   importance (2,3)    imp_j = (sum of the group's last n_imp queries) . k_j
 //                       / sqrt(d) on CUDA cores from the same shared K tile
-//                       (the importance is linear in the queries); then the
-//                       V tile is converted in place from bf16 to fp16 (exact
-//                       for |v| < 65504; larger values saturate and are
-//                       reported in the status word)
+//                       (the importance is linear in the queries)
 //   softmax (4..11)     one thread per query row, its scores read from TMEM
 //                       twice (max pass, then exponent pass): tile max, lazy
 //                       running max (O and l are rescaled only when the max
@@ -32,6 +29,9 @@
 //                       back over S in fp16 (relative rounding 2^-11, four
 //                       times finer than bf16), row sums.  Tree mask and
 //                       split limits only touch the tiles that need them.
+//                       The same warps convert the next V tile in place from
+//                       bf16 to fp16 (exact for |v| < 65504; larger values
+//                       saturate and are reported in the status word).
 // Each CTA writes an unnormalised partial (O, m, l) in the log2 domain; the
 // merge kernel of verify_attn.cu combines the splits.
 //
@@ -139,7 +139,7 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
     }
     for (int s = 0; s < kSV; ++s) {
       ptx::mbar_init(&aux->v_full[s], 1);
-      ptx::mbar_init(&aux->v_conv[s], 2);      // the two converting warps
+      ptx::mbar_init(&aux->v_conv[s], 4 * nt);   // one arrival per softmax warp
       ptx::mbar_init(&aux->v_empty[s], 1);
     }
     for (int g = 0; g < 2; ++g) {
@@ -332,7 +332,9 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
   } else if (warp < 4) {
     // ------------------------------------------------------------ importance
     const int t = tid - 64;   // key rows t and t + 64 of each tile
-    float vmax = 0.f;         // largest |v| converted (fp16 range check)
+    uint64_t qs[D / 2];       // the summed queries as fp32 pairs, in registers
+#pragma unroll
+    for (int c = 0; c < D / 2; ++c) qs[c] = ptx::f2(qsum[2 * c], qsum[2 * c + 1]);
     for (int j = 0; j < n_tiles; ++j) {
       const int s = j % kSK;
       if (aux->abort_flag || !ptx::mbar_wait(&aux->k_full[s], (uint32_t)(j / kSK) & 1u,
@@ -340,64 +342,36 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
         timeout(aux, status);
         break;
       }
-      if (do_imp) {
+      const int64_t ja = j0 + (int64_t)j * kNk + t, jb = ja + 64;
+      if (do_imp && ja < j1) {
+        const uint8_t* ra = sk + s * Ly::kTile + t * 128;
+        const uint8_t* rb = ra + 64 * 128;
+        uint64_t a0 = 0, a1 = 0, b0 = 0, b1 = 0;
 #pragma unroll
-        for (int h2 = 0; h2 < 2; ++h2) {
-          const int kr = t + 64 * h2;
-          const int64_t jj = j0 + (int64_t)j * kNk + kr;
-          if (jj < j1) {
-            const uint8_t* row = sk + s * Ly::kTile + kr * 128;
-            uint64_t acc0 = 0, acc1 = 0;   // two packed fp32 pairs
+        for (int c = 0; c < C16; ++c) {
+          const int p = c >> 3, cc = c & 7;
+          const int off = p * Ly::kPanel + ((cc ^ (t & 7)) << 4);   // rows t, t+64: same swizzle
+          const uint4 u = *reinterpret_cast<const uint4*>(ra + off);
+          const uint4 v = *reinterpret_cast<const uint4*>(rb + off);
+          const uint32_t uw[4] = {u.x, u.y, u.z, u.w}, vw[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-            for (int c = 0; c < C16; ++c) {
-              const int p = c >> 3, cc = c & 7;
-              const uint4 u = *reinterpret_cast<const uint4*>(row + p * Ly::kPanel +
-                                                              ((cc ^ (kr & 7)) << 4));
-              const float4 qa = *reinterpret_cast<const float4*>(qsum + c * 8);
-              const float4 qb = *reinterpret_cast<const float4*>(qsum + c * 8 + 4);
-              acc0 = ptx::fma2(ptx::f2(__uint_as_float(u.x << 16), __uint_as_float(u.x & 0xFFFF0000u)),
-                               ptx::f2(qa.x, qa.y), acc0);
-              acc1 = ptx::fma2(ptx::f2(__uint_as_float(u.y << 16), __uint_as_float(u.y & 0xFFFF0000u)),
-                               ptx::f2(qa.z, qa.w), acc1);
-              acc0 = ptx::fma2(ptx::f2(__uint_as_float(u.z << 16), __uint_as_float(u.z & 0xFFFF0000u)),
-                               ptx::f2(qb.x, qb.y), acc0);
-              acc1 = ptx::fma2(ptx::f2(__uint_as_float(u.w << 16), __uint_as_float(u.w & 0xFFFF0000u)),
-                               ptx::f2(qb.z, qb.w), acc1);
-            }
-            float a0, a1, b0, b1;
-            ptx::f2_split(acc0, a0, a1);
-            ptx::f2_split(acc1, b0, b1);
-            imp[(size_t)kv * L + jj] = ((a0 + a1) + (b0 + b1)) * scale;
+          for (int x = 0; x < 4; ++x) {
+            const uint64_t qa = qs[c * 4 + x];
+            uint64_t& aa = (x & 1) ? a1 : a0;
+            uint64_t& bb = (x & 1) ? b1 : b0;
+            aa = ptx::fma2(ptx::f2(__uint_as_float(uw[x] << 16), __uint_as_float(uw[x] & 0xFFFF0000u)), qa, aa);
+            bb = ptx::fma2(ptx::f2(__uint_as_float(vw[x] << 16), __uint_as_float(vw[x] & 0xFFFF0000u)), qa, bb);
           }
         }
+        float x0, x1, y0, y1;
+        ptx::f2_split(ptx::add2(a0, a1), x0, x1);
+        ptx::f2_split(ptx::add2(b0, b1), y0, y1);
+        imp[(size_t)kv * L + ja] = (x0 + x1) * scale;
+        if (jb < j1) imp[(size_t)kv * L + jb] = (y0 + y1) * scale;
       }
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(&aux->k_empty[s]);
-      // V tile j: bf16 -> fp16 in place (element positions unchanged)
-      const int sv_ = j % kSV;
-      if (aux->abort_flag || !ptx::mbar_wait(&aux->v_full[sv_], (uint32_t)(j / kSV) & 1u,
-                                             kWaitCycles)) {
-        timeout(aux, status);
-        break;
-      }
-      uint4* vt = reinterpret_cast<uint4*>(sv + sv_ * Ly::kTile);
-#pragma unroll 4
-      for (int e = t; e < Ly::kTile / 16; e += 64) {
-        uint4 u = vt[e];
-        uint32_t* wd = reinterpret_cast<uint32_t*>(&u);
-#pragma unroll
-        for (int x = 0; x < 4; ++x) {
-          const float lo = __uint_as_float(wd[x] << 16), hi = __uint_as_float(wd[x] & 0xFFFF0000u);
-          vmax = ptx::max3(vmax, fabsf(lo), fabsf(hi));
-          wd[x] = ptx::pack_f16x2_sat(lo, hi);
-        }
-        vt[e] = u;
-      }
-      ptx::fence_proxy_async_smem();   // generic writes -> the MMA's async-proxy reads
-      __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(&aux->v_conv[sv_]);
     }
-    if (!(vmax <= 65504.f)) set_status(status, TS_ERR_UNSUPPORTED);
   } else {
     // ------------------------------------------------------------ softmax
     const int g = (warp - 4) >> 2;
@@ -411,7 +385,38 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
     const uint32_t o_addr = tmem + lane_off + Ly::obase(g);
     float m_used = -INFINITY, l = 0.f;
     bool ok = true;
-    if (g < nt) {
+    // V tiles are converted in place from bf16 to fp16 by the softmax warps:
+    // with two row tiles each group converts half of a tile, else group 0
+    // converts all of it.  Tile j+1 is converted right after P of tile j is
+    // published, off the softmax -> MMA critical path.
+    float vmax = 0.f;         // largest |v| converted (fp16 range check)
+    auto convert_v = [&](int j) -> bool {
+      const int sv_ = j % kSV;
+      bool got = !aux->abort_flag &&
+                 ptx::mbar_wait(&aux->v_full[sv_], (uint32_t)(j / kSV) & 1u, kWaitCycles);
+      if (!__all_sync(0xffffffffu, got)) return false;
+      constexpr int kChunks = Ly::kTile / 16;
+      const int per = kChunks / nt;
+      uint4* vt = reinterpret_cast<uint4*>(sv + sv_ * Ly::kTile) + g * per;
+#pragma unroll 4
+      for (int e = t; e < per; e += 128) {
+        uint4 u = vt[e];
+        uint32_t wd[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+        for (int x = 0; x < 4; ++x) {
+          const float lo = __uint_as_float(wd[x] << 16), hi = __uint_as_float(wd[x] & 0xFFFF0000u);
+          vmax = ptx::max3(vmax, fabsf(lo), fabsf(hi));
+          wd[x] = ptx::pack_f16x2_sat(lo, hi);
+        }
+        vt[e] = make_uint4(wd[0], wd[1], wd[2], wd[3]);
+      }
+      ptx::fence_proxy_async_smem();   // generic writes -> the MMA's async-proxy reads
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(&aux->v_conv[sv_]);
+      return true;
+    };
+    if (g < nt && !convert_v(0)) ok = false;
+    if (g < nt && ok) {
       // tcgen05.ld/st are warp-collective: every branch around them is warp-uniform
       for (int j = 0; j < n_tiles; ++j) {
         bool got = !aux->abort_flag &&
@@ -520,6 +525,10 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
         ptx::tmem_st_wait();
         ptx::tc_fence_before();
         ptx::mbar_arrive(&aux->p_ready[g]);
+        if (j + 1 < n_tiles && !convert_v(j + 1)) {
+          ok = false;
+          break;
+        }
       }
       // epilogue: final O row -> unnormalised partial
       bool fin = ok && !aux->abort_flag && ptx::mbar_wait(&aux->o_final, 0, kWaitCycles);
@@ -547,6 +556,8 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
         timeout(aux, status);
       }
     }
+    if (!ok) timeout(aux, status);
+    if (!(vmax <= 65504.f)) set_status(status, TS_ERR_UNSUPPORTED);
   }
 
   ptx::tc_fence_before();

@@ -87,3 +87,38 @@ def test_chained_after_verification(name):
     kd_bits = pu.bf16_dev_to_bits(kd)
     for h in range(w.Hkv):
         assert kd_bits[h].tobytes() == inp["k"][h][idx_g[h]].tobytes()
+
+
+@pytest.mark.parametrize("n_layers,Hkv,L,B", [(3, 2, 9000, 1000), (4, 8, 102400, 4096), (2, 1, 50, 10)])
+def test_batched_equals_per_layer_and_oracle(n_layers, Hkv, L, B):
+    """The batched call returns exactly what the single-layer call returns for
+    each layer, and both match the oracle bit for bit."""
+    import self_speculative_ultra_gb300 as ts
+    S, R, d = 4, 64, 128
+    N = min(L, S + B + R)
+    imps, ks, vs, bits = [], [], [], []
+    for layer in range(n_layers):
+        imp = syn.importance_scores(Hkv, L, 10 + layer, grid=1.0 if layer == 1 else None)
+        rng = np.random.default_rng(layer)
+        kb = rng.integers(0, 2 ** 16, size=(Hkv, L + 8, d), dtype=np.uint16)
+        vb = rng.integers(0, 2 ** 16, size=(Hkv, L + 8, d), dtype=np.uint16)
+        bits.append((imp, kb, vb))
+        imps.append(pu.to_dev(imp))
+        ks.append(pu.to_dev_bf16(kb))
+        vs.append(pu.to_dev_bf16(vb))
+    mk = lambda shape, dt: [torch.empty(shape, dtype=dt, device="cuda") for _ in range(n_layers)]  # noqa: E731
+    idxs, kds, vds = mk((Hkv, N), torch.int32), mk((Hkv, N, d), torch.bfloat16), mk((Hkv, N, d), torch.bfloat16)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    ts.ts_partial_kv_select_gather_batched(imps, ks, vs, L, B, S, R, idxs, kds, vds, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    for layer in range(n_layers):
+        i1, k1, v1 = ts.ts_partial_kv_select_gather(imps[layer], ks[layer], vs[layer], L, B, S, R)
+        torch.cuda.synchronize()
+        assert torch.equal(i1, idxs[layer])
+        assert torch.equal(k1.view(torch.int16), kds[layer].view(torch.int16))
+        assert torch.equal(v1.view(torch.int16), vds[layer].view(torch.int16))
+        imp, kb, vb = bits[layer]
+        got = idxs[layer].cpu().numpy()
+        for h in range(Hkv):
+            np.testing.assert_array_equal(got[h], orc.select_partial(imp[h].astype(np.float64), L, B, S, R))
