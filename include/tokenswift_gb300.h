@@ -121,6 +121,29 @@ int ts_partial_kv_select_gather(const float* imp, const void* k, const void* v,
                                 void* workspace, size_t workspace_bytes,
                                 int32_t* status, void* stream);
 
+/* Allocation-free form of (2).  The pages have no counterpart: this entry
+ * point exists for callers that may not allocate device memory -- a plugin
+ * running inside a host runtime that owns every device allocation, or a
+ * serving loop that forbids allocation (and the synchronisation it can bring)
+ * once running.  It takes no workspace: its scratch is one fixed 10 MiB array
+ * of device memory inside the library, which every GPU that loads the library
+ * holds until the process exits.  That covers Hkv*L up to about 1.2 million
+ * cached positions (e.g. 8 KV heads at 102,400 tokens); larger shapes return
+ * TS_ERR_UNSUPPORTED with the size they would need.  Inputs and outputs are
+ * the caller's, exactly as in ts_partial_kv_select_gather, and the results are
+ * identical.  The first call on a device looks up the array's device address
+ * (with that device current) and caches it; make that first call before any
+ * stream capture.  All calls on a device share the array and each call
+ * overwrites what the previous one left there (the parts that must start at
+ * zero are cleared on the stream by every call), so calls that overlap on the
+ * GPU -- on different streams, or from different host threads -- race and
+ * must be serialised by the caller. */
+int ts_partial_kv_select_gather_noalloc(const float* imp, const void* k, const void* v,
+                                        int64_t L, int64_t L_cap, int Hkv, int d,
+                                        int B, int S, int R,
+                                        int32_t* idx, void* kd, void* vd, int64_t* n_out,
+                                        int32_t* status, void* stream);
+
 /* Batched form of (2): the same selection and gather for n_layers layers in
  * one pipeline of launches.  The refreshed partial cache of a layer is only
  * read by the next step's drafting, so a step may verify every layer first

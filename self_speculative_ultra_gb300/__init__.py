@@ -18,7 +18,7 @@ from ._build import LIB_PATH, build  # noqa: F401
 __all__ = [
     "TsError", "lib", "build", "ts_status_string", "ts_last_error", "ts_version",
     "ts_verify_workspace_bytes", "ts_verify_attention",
-    "ts_select_workspace_bytes", "ts_partial_kv_select_gather",
+    "ts_select_workspace_bytes", "ts_partial_kv_select_gather", "ts_partial_kv_select_gather_noalloc",
     "ts_select_batched_workspace_bytes", "ts_partial_kv_select_gather_batched", "layer_pointer_table",
     "ts_sample_workspace_bytes", "ts_penalized_sample_accept", "ts_kv_commit",
 ]
@@ -40,6 +40,10 @@ _SIGNATURES = {
                                            _i32, _i32, _i32, _c_void_p, _c_void_p, _c_void_p,
                                            ctypes.POINTER(_i64), _c_void_p, _sz, _c_void_p,
                                            _c_void_p]),
+    "ts_partial_kv_select_gather_noalloc": (_i32, [_c_void_p, _c_void_p, _c_void_p, _i64, _i64,
+                                                   _i32, _i32, _i32, _i32, _i32, _c_void_p,
+                                                   _c_void_p, _c_void_p, ctypes.POINTER(_i64),
+                                                   _c_void_p, _c_void_p]),
     "ts_select_batched_workspace_bytes": (_sz, [_i32, _i32, _i64]),
     "ts_partial_kv_select_gather_batched": (_i32, [_i32, _c_void_p, _c_void_p, _c_void_p, _i64, _i64,
                                                    _i32, _i32, _i32, _i32, _i32, _c_void_p,
@@ -182,6 +186,29 @@ def ts_partial_kv_select_gather(imp, k, v, L, B, S, R, idx=None, kd=None, vd=Non
                                            _ptr(ws), nb, _ptr(status), _stream(stream))
     _check(rc)
     assert n_out.value == N
+    return idx, kd, vd
+
+
+def ts_partial_kv_select_gather_noalloc(imp, k, v, L, B, S, R, idx, kd, vd, status=None,
+                                        stream=None):
+    """Selection + gather without a workspace, for callers that may not
+    allocate device memory: the library keeps its scratch in a fixed device
+    array (see the C header for the size limit and the sharing rules).  The
+    outputs idx [Hkv,N] int32, kd/vd [Hkv,N,d] bf16 are the caller's."""
+    Hkv, L_cap, d = k.shape
+    _dev(imp, torch.float32, "imp", (Hkv, L))
+    _dev(k, torch.bfloat16, "k")
+    _dev(v, torch.bfloat16, "v", (Hkv, L_cap, d))
+    N = min(L, S + B + R)
+    _dev(idx, torch.int32, "idx", (Hkv, N))
+    _dev(kd, torch.bfloat16, "kd", (Hkv, N, d))
+    _dev(vd, torch.bfloat16, "vd", (Hkv, N, d))
+    n_out = _i64(0)
+    rc = lib().ts_partial_kv_select_gather_noalloc(_ptr(imp), _ptr(k), _ptr(v), L, L_cap, Hkv, d,
+                                                   B, S, R, _ptr(idx), _ptr(kd), _ptr(vd),
+                                                   ctypes.byref(n_out), _ptr(status),
+                                                   _stream(stream))
+    _check(rc)
     return idx, kd, vd
 
 

@@ -19,6 +19,8 @@
 //                   exclusive offsets
 //   select_gather   re-evaluate keep(), compact the kept positions in
 //                   ascending order, copy their K/V rows with 16-byte loads
+#include <mutex>
+
 #include "ts_common.cuh"
 
 namespace ts {
@@ -470,6 +472,34 @@ int launch_select_gather(const float* imp, const void* k, const void* v, int64_t
   P.kd1 = static_cast<__nv_bfloat16*>(kd);
   P.vd1 = static_cast<__nv_bfloat16*>(vd);
   return run_select(P, 1, L, L_cap, Hkv, d, B, S, R, N, ws, status, st);
+}
+
+// ---------------------------------------------------------------------------
+// Allocation-free variant: the scratch lives in one fixed device array of the
+// library instead of a caller workspace.  Its device address is looked up once
+// per device (with that device current) and cached; every call on a device
+// shares the array, so calls that overlap on the GPU race on it.
+namespace {
+static __device__ __align__(256) unsigned char g_select_scratch[kNoAllocScratchBytes];
+}
+
+int select_scratch(void** out) {
+  static std::mutex mu;
+  static void* cached[64] = {nullptr};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return fail(TS_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
+  if (dev < 0 || dev >= 64) return fail(TS_ERR_UNSUPPORTED, "device ordinal %d >= 64", dev);
+  std::lock_guard<std::mutex> lock(mu);
+  if (!cached[dev]) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_select_scratch);
+    if (e != cudaSuccess || !p)
+      return fail(TS_ERR_CUDA, "cudaGetSymbolAddress(select scratch): %s", cudaGetErrorString(e));
+    cached[dev] = p;
+  }
+  *out = cached[dev];
+  return TS_OK;
 }
 
 int launch_select_gather_batched(int n_layers, const float* const* imp, const void* const* k,

@@ -128,6 +128,34 @@ int ts_partial_kv_select_gather(const float* imp, const void* k, const void* v, 
                               status, static_cast<cudaStream_t>(stream));
 }
 
+int ts_partial_kv_select_gather_noalloc(const float* imp, const void* k, const void* v,
+                                        int64_t L, int64_t L_cap, int Hkv, int d, int B, int S,
+                                        int R, int32_t* idx, void* kd, void* vd, int64_t* n_out,
+                                        int32_t* status, void* stream) {
+  clear_error();
+  const char* W = "ts_partial_kv_select_gather_noalloc";
+  if (Hkv < 1) return fail(TS_ERR_INVALID_ARG, "%s: Hkv=%d", W, Hkv);
+  if (d != 64 && d != 128) return fail(TS_ERR_UNSUPPORTED, "%s: head dim %d not in {64,128}", W, d);
+  if (B < 0 || S < 0 || R < 0) return fail(TS_ERR_INVALID_ARG, "%s: B, S, R must be >= 0", W);
+  if (L < 0 || L > L_cap) return fail(TS_ERR_INVALID_ARG, "%s: need 0 <= L <= L_cap", W);
+  if (L_cap > (int64_t(1) << 31) - 1) return fail(TS_ERR_UNSUPPORTED, "%s: L_cap >= 2^31", W);
+  const size_t need = select_plan(Hkv, L, 1).ws_bytes;
+  if (need > kNoAllocScratchBytes)
+    return fail(TS_ERR_UNSUPPORTED,
+                "%s: Hkv=%d, L=%lld needs %zu bytes of scratch; the fixed array holds %zu "
+                "(about Hkv*L <= 1.2M positions); use ts_partial_kv_select_gather with a workspace",
+                W, Hkv, (long long)L, need, kNoAllocScratchBytes);
+  int64_t N = L < (int64_t)S + B + R ? L : (int64_t)S + B + R;
+  if (n_out) *n_out = N;
+  if (L == 0) return TS_OK;
+  if (!imp || !k || !v || !idx || !kd || !vd) return fail(TS_ERR_INVALID_ARG, "%s: NULL tensor", W);
+  void* scratch = nullptr;
+  int rc = select_scratch(&scratch);
+  if (rc) return rc;
+  return launch_select_gather(imp, k, v, L, L_cap, Hkv, d, B, S, R, idx, kd, vd, N, scratch,
+                              status, static_cast<cudaStream_t>(stream));
+}
+
 int ts_partial_kv_select_gather_batched(int n_layers, const float* const* imp,
                                         const void* const* k, const void* const* v, int64_t L,
                                         int64_t L_cap, int Hkv, int d, int B, int S, int R,

@@ -117,6 +117,10 @@ int launch_select_gather_batched(int n_layers, const float* const* imp, const vo
                                  void* const* vd, int64_t N, void* ws, int32_t* status,
                                  cudaStream_t st);
 
+// Fixed scratch of the allocation-free selection entry point.
+constexpr size_t kNoAllocScratchBytes = size_t(10) << 20;
+int select_scratch(void** out);   // device address of that scratch (current device)
+
 size_t sample_ws_bytes(int T, int V);
 int launch_sample_accept(const float* logits, const int32_t* tree_tokens, const int32_t* parents,
                          int T, const int32_t* prior, int n_prior, int W, int V, float penalty,
