@@ -86,7 +86,7 @@ def load_peaks():
 
 def verify_source_sha1() -> str:
     h = hashlib.sha1()
-    for name in ("verify_attn.cu", "ts_common.cuh"):
+    for name in ("verify_tc.cu", "tc_ptx.cuh", "verify_attn.cu", "ts_common.cuh"):
         with open(os.path.join(ROOT, "self_speculative_ultra_gb300", "csrc", name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:12]
@@ -465,6 +465,47 @@ def run_reference(args, w: syn.Workload):
     print(json.dumps(line), flush=True)
 
 
+def run_profile_case(kind: str, w: syn.Workload):
+    """Small, fixed cases for ncu captures (a few GB on the device):
+    verify -- 2 layers of the workload's K/V, 3 + 5*2 ts_verify_attention calls;
+    select -- 4 layers through the batched partial-KV refresh and the sampling
+    step, 3 rounds."""
+    import torch
+    import self_speculative_ultra_gb300 as ts
+    ts.build()
+    dev = torch.device("cuda", 0)
+    g = torch.Generator(device=dev)
+    g.manual_seed(0)
+    T, Hq, Hkv, d, L = w.T, w.Hq, w.Hkv, w.d, w.L
+    nl = 2 if kind == "verify" else 4
+    ks = [torch.randn((Hkv, L + T, d), generator=g, device=dev).to(torch.bfloat16) for _ in range(nl)]
+    vs = [torch.randn((Hkv, L + T, d), generator=g, device=dev).to(torch.bfloat16) for _ in range(nl)]
+    tree = syn.make_tree(w, np.random.default_rng(0))
+    parents = torch.from_numpy(tree[0]).to(dev)
+    if kind == "verify":
+        q = torch.randn((T, Hq, d), generator=g, device=dev).to(torch.bfloat16)
+        ws = torch.empty(ts.ts_verify_workspace_bytes(T, Hq, Hkv, d, L), dtype=torch.uint8, device=dev)
+        for i in range(3 + 5 * nl):
+            ts.ts_verify_attention(q, ks[i % nl], vs[i % nl], L, parents, n_imp=w.n_imp, workspace=ws)
+    else:
+        imps = [torch.randn((Hkv, L), generator=g, device=dev) * 16 for _ in range(nl)]
+        N = w.N
+        idx = [torch.empty((Hkv, N), dtype=torch.int32, device=dev) for _ in range(nl)]
+        kd = [torch.empty((Hkv, N, d), dtype=torch.bfloat16, device=dev) for _ in range(nl)]
+        vd = [torch.empty((Hkv, N, d), dtype=torch.bfloat16, device=dev) for _ in range(nl)]
+        sin = syn.sampling_inputs(w, tree=tree)
+        logits = torch.from_numpy(sin["logits"]).to(dev)
+        toks = torch.from_numpy(sin["tokens"]).to(dev)
+        prior = torch.from_numpy(sin["prior"]).to(dev)
+        u = torch.from_numpy(sin["uniforms"]).to(dev)
+        for _ in range(3):
+            ts.ts_partial_kv_select_gather_batched(imps, ks, vs, L, w.B, w.S, w.R, idx, kd, vd)
+            ts.ts_penalized_sample_accept(logits, toks, parents, prior, w.W, w.penalty,
+                                          w.temperature, w.top_p, w.min_p, u)
+    torch.cuda.synchronize()
+    print(json.dumps({"profile_case": kind, "workload": w.name, "layers": nl}))
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -473,9 +514,13 @@ def main():
     ap.add_argument("--impl", default="gpu", choices=["gpu", "reference"])
     ap.add_argument("--workload", default="llama3.1-8b", choices=sorted(syn.WORKLOADS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--profile", choices=["verify", "select"],
+                    help="run a small fixed case for ncu captures and exit")
     args = ap.parse_args()
     w = syn.WORKLOADS[args.workload]
-    if args.impl == "reference":
+    if args.profile:
+        run_profile_case(args.profile, w)
+    elif args.impl == "reference":
         run_reference(args, w)
     else:
         run_gpu(args, w)
