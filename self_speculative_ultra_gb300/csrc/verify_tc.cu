@@ -12,7 +12,7 @@
 // KV head's group are packed (row r = node r / G, head kv*G + r % G) into up
 // to two 128-row tiles held in shared memory for the whole CTA, so every K/V
 // tile is read from HBM once per step.  Per 128-key tile j:
-//   TMA (warp 0)        K and V tiles -> 2-stage shared-memory rings
+//   TMA (warp 0)        K (2-stage) and V (3-stage) shared-memory rings
 //                       (128-byte swizzle, L2 evict-first)
 //   MMA (warp 1)        S_g = Q_g K^T (bf16, M=128, N=128, fp32 in TMEM); once
 //                       the softmax has written P_g over S_g, O_g += P_g V in
@@ -50,7 +50,7 @@ namespace {
 
 constexpr int kNk = 128;                 // keys per tile
 constexpr int kSK = 2;                   // K ring depth
-constexpr int kSV = 2;                   // V ring depth
+constexpr int kSV = 3;                   // V ring depth
 constexpr int kThreadsTc = 384;          // 12 warps
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLazy = 8.0f;            // running max refreshed only past +2^8
@@ -332,9 +332,6 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
   } else if (warp < 4) {
     // ------------------------------------------------------------ importance
     const int t = tid - 64;   // key rows t and t + 64 of each tile
-    uint64_t qs[D / 2];       // the summed queries as fp32 pairs, in registers
-#pragma unroll
-    for (int c = 0; c < D / 2; ++c) qs[c] = ptx::f2(qsum[2 * c], qsum[2 * c + 1]);
     for (int j = 0; j < n_tiles; ++j) {
       const int s = j % kSK;
       if (aux->abort_flag || !ptx::mbar_wait(&aux->k_full[s], (uint32_t)(j / kSK) & 1u,
@@ -353,15 +350,21 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
           const int off = p * Ly::kPanel + ((cc ^ (t & 7)) << 4);   // rows t, t+64: same swizzle
           const uint4 u = *reinterpret_cast<const uint4*>(ra + off);
           const uint4 v = *reinterpret_cast<const uint4*>(rb + off);
-          const uint32_t uw[4] = {u.x, u.y, u.z, u.w}, vw[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-          for (int x = 0; x < 4; ++x) {
-            const uint64_t qa = qs[c * 4 + x];
-            uint64_t& aa = (x & 1) ? a1 : a0;
-            uint64_t& bb = (x & 1) ? b1 : b0;
-            aa = ptx::fma2(ptx::f2(__uint_as_float(uw[x] << 16), __uint_as_float(uw[x] & 0xFFFF0000u)), qa, aa);
-            bb = ptx::fma2(ptx::f2(__uint_as_float(vw[x] << 16), __uint_as_float(vw[x] & 0xFFFF0000u)), qa, bb);
-          }
+          const float4 q0 = *reinterpret_cast<const float4*>(qsum + 8 * c);
+          const float4 q1 = *reinterpret_cast<const float4*>(qsum + 8 * c + 4);
+          const uint64_t qa = ptx::f2(q0.x, q0.y), qb = ptx::f2(q0.z, q0.w);
+          const uint64_t qc = ptx::f2(q1.x, q1.y), qd = ptx::f2(q1.z, q1.w);
+          auto lohi = [](uint32_t w) {
+            return ptx::f2(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
+          };
+          a0 = ptx::fma2(lohi(u.x), qa, a0);
+          a1 = ptx::fma2(lohi(u.y), qb, a1);
+          a0 = ptx::fma2(lohi(u.z), qc, a0);
+          a1 = ptx::fma2(lohi(u.w), qd, a1);
+          b0 = ptx::fma2(lohi(v.x), qa, b0);
+          b1 = ptx::fma2(lohi(v.y), qb, b1);
+          b0 = ptx::fma2(lohi(v.z), qc, b0);
+          b1 = ptx::fma2(lohi(v.w), qd, b1);
         }
         float x0, x1, y0, y1;
         ptx::f2_split(ptx::add2(a0, a1), x0, x1);
