@@ -80,6 +80,16 @@ __device__ __forceinline__ void tree_masks(const int32_t* parents, int T,
 // ---------------------------------------------------------------- launchers
 constexpr int kGb300Sms = 152;   // streaming multiprocessors of one GB300
 
+// Split partials of the verification attention.  part_o is column-quad
+// major: the float4 holding columns [4*c4, 4*c4+4) of packed row R of split
+// s of KV head kv sits at ((kv * n_split + s) * (D/4) + c4) * M + R, so
+// consecutive rows are consecutive float4s (a warp holding 32 rows stores
+// 512 contiguous bytes).  part_ml holds (m, l) pairs at (kv * n_split + s) * M + R.
+__host__ __device__ __forceinline__ size_t part_o4_index(int kv, int s, int n_split, int c4,
+                                                         int D, int M, int R) {
+  return (((size_t)kv * n_split + s) * (D / 4) + c4) * M + R;
+}
+
 struct VerifyPlan {
   bool tc;             // tcgen05 kernel (else the CUDA-core kernel)
   int M;               // packed query rows per KV head (T * G)

@@ -166,7 +166,10 @@ verify_split_simple(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __
     if (row >= M) continue;
     size_t base = ((size_t)kv * n_split + split) * M + row;
 #pragma unroll
-    for (int c = 0; c < DL; ++c) part_o[base * D + lane + 32 * c] = acc[rr][c];
+    for (int c = 0; c < DL; ++c) {
+      const int col = lane + 32 * c;
+      part_o[part_o4_index(kv, split, n_split, col >> 2, D, M, row) * 4 + (col & 3)] = acc[rr][c];
+    }
     if (lane == 0) {
       part_ml[base * 2] = m[rr];
       part_ml[base * 2 + 1] = l[rr];
@@ -174,60 +177,79 @@ verify_split_simple(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __
   }
 }
 
-// One CTA per (node, query head): combine the split partials.  The split
-// weights 2^(m_s - max m) are formed once in shared memory; the partial rows
-// are then summed with independent loads.
+// One CTA per (KV head, block of 8 packed rows): combine the split
+// partials.  Thread (c4, r) owns columns [4*c4, 4*c4+4) of row r, so each
+// warp reads four 128-byte runs of a split's column-quad-major partial.  The
+// split weights 2^(m_s - max m) of the 8 rows are formed once in shared memory.
 constexpr int kMaxSplits = 1024;
-__global__ void __launch_bounds__(128)
-verify_merge(const float* __restrict__ part_o, const float* __restrict__ part_ml,
-             int T, int Hq, int Hkv, int D, int n_split, float* __restrict__ o,
-             float* __restrict__ lse) {
-  __shared__ float wsp[kMaxSplits];
-  __shared__ float red[4], s_mx, s_l;
-  const int i = blockIdx.x / Hq, h = blockIdx.x % Hq;
-  const int G = Hq / Hkv, kv = h / G, row = i * G + h % G, M = T * G;
-  const int tid = threadIdx.x;
-  const size_t base = (size_t)kv * n_split * M + row;   // + s*M
+constexpr int kMergeRows = 8;
+__global__ void __launch_bounds__(256)
+verify_merge(const float* __restrict__ part_o, const float* __restrict__ part_ml, int T, int Hq,
+             int Hkv, int D, int n_split, float* __restrict__ o, float* __restrict__ lse) {
+  __shared__ float wsp[kMaxSplits][kMergeRows];
+  __shared__ float red[8][kMergeRows];
+  const int kv = blockIdx.y;
+  const int G = Hq / Hkv, M = T * G;
+  const int tid = threadIdx.x, r = tid % kMergeRows, c4 = tid / kMergeRows;
+  const int nq = D / 4;                       // threads per row
+  const int warp = tid >> 5, lane = tid & 31, n_warps = blockDim.x >> 5;
+  const int R = blockIdx.x * kMergeRows + r;
+  const bool valid = R < M;
+  const size_t ml0 = (size_t)kv * n_split * M + R;   // + s*M
+  // lanes sharing r within a warp differ in lane bits 3 and 4
+  auto row_reduce = [&](float v, bool is_max) {
+    for (int off = 8; off < 32; off <<= 1) {
+      const float u = __shfl_xor_sync(0xffffffffu, v, off);
+      v = is_max ? fmaxf(v, u) : v + u;
+    }
+    __syncthreads();
+    if (lane < kMergeRows) red[warp][lane] = v;
+    __syncthreads();
+    float x = red[0][r];
+    for (int w = 1; w < n_warps; ++w) x = is_max ? fmaxf(x, red[w][r]) : x + red[w][r];
+    return x;
+  };
   float mx = -INFINITY;
-  for (int s = tid; s < n_split; s += blockDim.x) {
-    const float m = part_ml[(base + (size_t)s * M) * 2];
-    wsp[s] = m;
+  for (int s = c4; s < n_split; s += nq) {
+    const float m = valid ? part_ml[(ml0 + (size_t)s * M) * 2] : -INFINITY;
+    wsp[s][r] = m;
     mx = fmaxf(mx, m);
   }
-  mx = warp_max(mx);
-  if ((tid & 31) == 0) red[tid >> 5] = mx;
-  __syncthreads();
-  if (tid == 0) s_mx = fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3]));
-  __syncthreads();
-  mx = s_mx;
+  mx = row_reduce(mx, true);
   float lsum = 0.f;
-  for (int s = tid; s < n_split; s += blockDim.x) {
-    const float m = wsp[s];
+  for (int s = c4; s < n_split; s += nq) {
+    const float m = wsp[s][r];
     const float wgt = (m == -INFINITY) ? 0.f : exp2f(m - mx);
-    wsp[s] = wgt;
-    lsum += wgt * part_ml[(base + (size_t)s * M) * 2 + 1];
+    wsp[s][r] = wgt;
+    if (wgt != 0.f) lsum += wgt * part_ml[(ml0 + (size_t)s * M) * 2 + 1];
   }
-  lsum = warp_sum(lsum);
-  __syncthreads();
-  if ((tid & 31) == 0) red[tid >> 5] = lsum;
-  __syncthreads();
-  if (tid == 0) s_l = red[0] + red[1] + red[2] + red[3];
-  __syncthreads();
-  lsum = s_l;
+  lsum = row_reduce(lsum, false);   // its barriers also publish wsp
+  if (!valid) return;
+  const float4* p4 = reinterpret_cast<const float4*>(part_o);
+  const size_t step = (size_t)nq * M;                 // float4s between splits
+  const float4* src = p4 + part_o4_index(kv, 0, n_split, c4, D, M, R);
+  float4 a = make_float4(0.f, 0.f, 0.f, 0.f), b = a;
+  auto acc = [](float4& x, float w, const float4& v) {
+    x.x += w * v.x;
+    x.y += w * v.y;
+    x.z += w * v.z;
+    x.w += w * v.w;
+  };
+  int s = 0;
+  for (; s + 4 <= n_split; s += 4) {
+    const float4 v0 = src[(size_t)s * step], v1 = src[(size_t)(s + 1) * step];
+    const float4 v2 = src[(size_t)(s + 2) * step], v3 = src[(size_t)(s + 3) * step];
+    acc(a, wsp[s][r], v0);
+    acc(b, wsp[s + 1][r], v1);
+    acc(a, wsp[s + 2][r], v2);
+    acc(b, wsp[s + 3][r], v3);
+  }
+  for (; s < n_split; ++s) acc(a, wsp[s][r], src[(size_t)s * step]);
   const float inv = 1.f / lsum;
-  for (int c = tid; c < D; c += blockDim.x) {
-    float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
-    int s = 0;
-    for (; s + 4 <= n_split; s += 4) {
-      a0 += wsp[s] * part_o[(base + (size_t)s * M) * D + c];
-      a1 += wsp[s + 1] * part_o[(base + (size_t)(s + 1) * M) * D + c];
-      a2 += wsp[s + 2] * part_o[(base + (size_t)(s + 2) * M) * D + c];
-      a3 += wsp[s + 3] * part_o[(base + (size_t)(s + 3) * M) * D + c];
-    }
-    for (; s < n_split; ++s) a0 += wsp[s] * part_o[(base + (size_t)s * M) * D + c];
-    o[((size_t)i * Hq + h) * D + c] = ((a0 + a1) + (a2 + a3)) * inv;
-  }
-  if (lse && tid == 0) lse[(size_t)i * Hq + h] = (mx + log2f(lsum)) * 0.6931471805599453f;
+  const int i = R / G, h = kv * G + R % G;
+  reinterpret_cast<float4*>(o + ((size_t)i * Hq + h) * D)[c4] =
+      make_float4((a.x + b.x) * inv, (a.y + b.y) * inv, (a.z + b.z) * inv, (a.w + b.w) * inv);
+  if (lse && c4 == 0) lse[(size_t)i * Hq + h] = (mx + log2f(lsum)) * 0.6931471805599453f;
 }
 
 }  // namespace
@@ -311,7 +333,9 @@ int launch_verify(const void* q, const void* k, const void* v, int64_t L, int64_
     rc = launch_status("verify_split_simple");
   }
   if (rc) return rc;
-  verify_merge<<<T * Hq, 128, 0, st>>>(part_o, part_ml, T, Hq, Hkv, d, p.n_split, o, lse);
+  dim3 mgrid((p.M + kMergeRows - 1) / kMergeRows, Hkv);
+  verify_merge<<<mgrid, kMergeRows * (d / 4), 0, st>>>(part_o, part_ml, T, Hq, Hkv, d, p.n_split, o,
+                                                       lse);
   return launch_status("verify_merge");
 }
 

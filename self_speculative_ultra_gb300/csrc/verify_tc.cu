@@ -130,6 +130,8 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
   const bool do_imp = (imp != nullptr) && rg == 0;
   const float scale = 1.0f / sqrtf((float)D);
   const float sl2 = scale * kLog2e;
+  const int n_pre = min(n_tiles, kSK);          // tiles loaded during the set-up
+  static_assert(kSK < kSV, "early loads fill K and V stages alike; the last V stage is set-up scratch");
 
   // ---------------------------------------------------------------- set-up
   if (tid == 0) {
@@ -150,48 +152,99 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
     ptx::mbar_init(&aux->drain, 1);
     aux->abort_flag = 0;
     ptx::fence_mbar_init();
+    // the first K and V tiles go out before the rest of the set-up, which
+    // then runs under their HBM latency; every stage is free at this point
+    const uint64_t pol = ptx::l2_evict_first_policy();
+    const int row0 = (int)(kv * L_cap + j0);
+    for (int jj = 0; jj < n_pre; ++jj) {
+      ptx::mbar_arrive_expect_tx(&aux->k_full[jj], Ly::kTile);
+      for (int p = 0; p < D / 64; ++p)
+        ptx::tma_load_2d(sk + jj * Ly::kTile + p * Ly::kPanel, &tmap_k, &aux->k_full[jj], p * 64,
+                         row0 + jj * kNk, pol);
+      ptx::mbar_arrive_expect_tx(&aux->v_full[jj], Ly::kTile);
+      for (int p = 0; p < D / 64; ++p)
+        ptx::tma_load_2d(sv + jj * Ly::kTile + p * Ly::kPanel, &tmap_v, &aux->v_full[jj], p * 64,
+                         row0 + jj * kNk, pol);
+    }
   }
   if (tid < T) aux->par[tid] = parents[tid];
-  if (tid < D) qsum[tid] = 0.f;
   if (warp == 1) {
     ptx::tmem_alloc(&aux->tmem_base, Ly::kTmemCols);
     ptx::tmem_relinquish();
   }
-  if (warp == 0 && lane == 0) {
-    ptx::prefetch_tmap(&tmap_k);
-    ptx::prefetch_tmap(&tmap_v);
-  }
   // Q tiles -> shared memory in the 128-byte-swizzled K-major layout
   constexpr int C16 = D / 8;                     // 16-byte chunks per row
-  for (int e = tid; e < 2 * 128 * C16; e += kThreadsTc) {
-    const int g = e / (128 * C16), rem = e % (128 * C16);
-    const int t = rem / C16, c = rem % C16;
-    const int R = r0 + g * 128 + t;
-    uint4 val = make_uint4(0, 0, 0, 0);
-    if (g < nt && R < M) {
-      const int i = R / G, h = kv * G + R % G;
-      val = *reinterpret_cast<const uint4*>(q + ((size_t)i * Hq + h) * D + c * 8);
+  constexpr int kQAll = 2 * 128 * C16, kQPer = (kQAll + kThreadsTc - 1) / kThreadsTc;
+  {
+    // all loads of a thread are in flight together, then all stores
+    uint4 val[kQPer];
+#pragma unroll
+    for (int k = 0; k < kQPer; ++k) {
+      const int e = tid + k * kThreadsTc;
+      const int g = e / (128 * C16), rem = e % (128 * C16);
+      const int t = rem / C16, c = rem % C16;
+      const int R = r0 + g * 128 + t;
+      val[k] = make_uint4(0, 0, 0, 0);
+      if (e < kQAll && g < nt && R < M) {
+        const int i = R / G, h = kv * G + R % G;
+        val[k] = __ldg(reinterpret_cast<const uint4*>(q + ((size_t)i * Hq + h) * D + c * 8));
+      }
     }
-    const int p = c >> 3, cc = c & 7;
-    *reinterpret_cast<uint4*>(sq + g * Ly::kTile + p * Ly::kPanel + t * 128 +
-                              ((cc ^ (t & 7)) << 4)) = val;
+#pragma unroll
+    for (int k = 0; k < kQPer; ++k) {
+      const int e = tid + k * kThreadsTc;
+      if (e < kQAll) {
+        const int g = e / (128 * C16), rem = e % (128 * C16);
+        const int t = rem / C16, c = rem % C16;
+        const int p = c >> 3, cc = c & 7;
+        *reinterpret_cast<uint4*>(sq + g * Ly::kTile + p * Ly::kPanel + t * 128 +
+                                  ((cc ^ (t & 7)) << 4)) = val[k];
+      }
+    }
   }
   __syncthreads();
-  // summed importance queries: (16-byte column chunk, row slice) per thread
+  // summed importance queries over the packed rows (T - n_imp) * G .. M - 1:
+  // thread (16-byte column chunk, row slice) partial sums, rows of this
+  // CTA's Q tiles (r0 = 0 here) read back from shared memory; the slices are
+  // folded by shuffles, then across warps through the last V stage, which
+  // the producer fills only after the set-up
+  float* qpart = reinterpret_cast<float*>(sv + (kSV - 1) * Ly::kTile);
   if (do_imp) {
-    const int cg = tid % C16, slice = tid / C16, nslices = kThreadsTc / C16;
-    const int rows = n_imp * G;
-    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-    for (int rr = slice; rr < rows; rr += nslices) {
-      const int i = T - n_imp + rr / G, h = kv * G + rr % G;
-      const uint4 u = *reinterpret_cast<const uint4*>(q + ((size_t)i * Hq + h) * D + cg * 8);
-      float f[8];
-      unpack_bf16x8(u, f);
+    const int cg = tid % C16, slice = tid / C16, nsl = kThreadsTc / C16;
+    const int p = cg >> 3, cc = cg & 7;
+    const int in_smem = min(M, nt * 128);
+    uint64_t acc[4] = {0, 0, 0, 0};
+    auto add8 = [&](const uint4& u) {
+      const uint32_t w[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
-      for (int x = 0; x < 8; ++x) acc[x] += f[x];
+      for (int x = 0; x < 4; ++x)
+        acc[x] = ptx::add2(acc[x], ptx::f2(__uint_as_float(w[x] << 16),
+                                           __uint_as_float(w[x] & 0xFFFF0000u)));
+    };
+    int R = (T - n_imp) * G + slice;
+#pragma unroll 4
+    for (; R < in_smem; R += nsl) {
+      const int tr = R & 127;
+      add8(*reinterpret_cast<const uint4*>(sq + (R >> 7) * Ly::kTile + p * Ly::kPanel + tr * 128 +
+                                           ((cc ^ (tr & 7)) << 4)));
     }
+#pragma unroll 4
+    for (; R < M; R += nsl) {
+      const int i = R / G, h = kv * G + R % G;
+      add8(__ldg(reinterpret_cast<const uint4*>(q + ((size_t)i * Hq + h) * D + cg * 8)));
+    }
+    float f[8];
 #pragma unroll
-    for (int x = 0; x < 8; ++x) atomicAdd(&qsum[cg * 8 + x], acc[x]);
+    for (int x = 0; x < 4; ++x) ptx::f2_split(acc[x], f[2 * x], f[2 * x + 1]);
+#pragma unroll
+    for (int off = C16; off < 32; off <<= 1)
+#pragma unroll
+      for (int x = 0; x < 8; ++x) f[x] += __shfl_xor_sync(0xffffffffu, f[x], off);
+    if (lane < C16) {
+      float4* dst = reinterpret_cast<float4*>(qpart + warp * D + lane * 8);
+      dst[0] = make_float4(f[0], f[1], f[2], f[3]);
+      dst[1] = make_float4(f[4], f[5], f[6], f[7]);
+    }
   }
   // ancestor-or-self masks: node t walks its parent chain (depth < 64)
   if (tid < T) {
@@ -211,6 +264,15 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
     aux->anc[tid] = m;
     if (bad && split == 0 && kv == 0 && rg == 0) set_status(status, TS_ERR_INVALID_ARG);
   }
+  if (do_imp) {
+    __syncthreads();
+    if (tid < D) {
+      float sum = 0.f;
+#pragma unroll
+      for (int w = 0; w < kThreadsTc / 32; ++w) sum += qpart[w * D + tid];
+      qsum[tid] = sum;
+    }
+  }
   ptx::fence_proxy_async_smem();
   ptx::tc_fence_before();
   __syncthreads();
@@ -221,7 +283,7 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
     if (lane == 0) {
       const uint64_t pol = ptx::l2_evict_first_policy();
       const int row0 = (int)(kv * L_cap + j0);
-      int jk = 0, jv = 0;   // tiles whose K / V load has been issued
+      int jk = n_pre, jv = n_pre;   // tiles whose K / V load has been issued
       for (; jk < n_tiles; ++jk) {
         const int s = jk % kSK;
         if (jk >= kSK &&
@@ -488,9 +550,11 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
         }
         // pass 2: P = 2^(s*sl2 - m) -> fp16 pairs, written over the chunk's
         // own columns once it has been loaded; two chunks in flight
-        const bool live = m_used != -INFINITY;
+        // when the running max is still -inf every score of the row seen so
+        // far, this tile included, is -inf: reference 0 then gives 2^-inf = 0
+        const float mref = (m_used == -INFINITY) ? 0.f : m_used;
         const uint64_t sl2x2 = ptx::f2(sl2, sl2);
-        const uint64_t negm = ptx::f2(-m_used, -m_used);
+        const uint64_t negm = ptx::f2(-mref, -mref);
         uint64_t lsum = 0;
         uint32_t ca[32], cb[32];
         auto process = [&](uint32_t (&r)[32], int c) {
@@ -502,8 +566,7 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
             ptx::f2_split(ptx::fma2(ptx::f2(__uint_as_float(r[2 * x]), __uint_as_float(r[2 * x + 1])),
                                     sl2x2, negm),
                           t0, t1);
-            const float p0 = live ? ptx::ex2(t0) : 0.f;
-            const float p1 = live ? ptx::ex2(t1) : 0.f;
+            const float p0 = ptx::ex2(t0), p1 = ptx::ex2(t1);
             lsum = ptx::add2(lsum, ptx::f2(p0, p1));
             pw[x] = ptx::pack_f16x2(p0, p1);
           }
@@ -537,20 +600,25 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
       bool fin = ok && !aux->abort_flag && ptx::mbar_wait(&aux->o_final, 0, kWaitCycles);
       if (__all_sync(0xffffffffu, fin)) {
         ptx::tc_fence_after();
-        const size_t base = ((size_t)kv * n_split + split) * M + R;
+        // column-quad-major partial: for each float4 column the warp's 32
+        // rows are 512 contiguous bytes
+        float4* dst = reinterpret_cast<float4*>(part_o) +
+                      part_o4_index(kv, split, n_split, 0, D, M, valid ? R : 0);
+        const size_t c4_stride = (size_t)M;
 #pragma unroll 1
         for (int c = 0; c < D / 32; ++c) {
           uint32_t o[32];
           ptx::tmem_ld32(o_addr + c * 32, o);
           ptx::tmem_ld_wait();
           if (valid) {
-            float4* dst = reinterpret_cast<float4*>(part_o + base * D + c * 32);
 #pragma unroll
             for (int x = 0; x < 8; ++x)
-              dst[x] = make_float4(__uint_as_float(o[4 * x]), __uint_as_float(o[4 * x + 1]),
-                                   __uint_as_float(o[4 * x + 2]), __uint_as_float(o[4 * x + 3]));
+              dst[(size_t)(c * 8 + x) * c4_stride] =
+                  make_float4(__uint_as_float(o[4 * x]), __uint_as_float(o[4 * x + 1]),
+                              __uint_as_float(o[4 * x + 2]), __uint_as_float(o[4 * x + 3]));
           }
         }
+        const size_t base = ((size_t)kv * n_split + split) * M + R;
         if (valid) {
           part_ml[base * 2] = m_used;
           part_ml[base * 2 + 1] = l;
