@@ -77,6 +77,29 @@ __device__ __forceinline__ void tree_masks(const int32_t* parents, int T,
   }
 }
 
+// Programmatic dependent launch: a kernel launched with pdl_config may
+// become resident while the previous kernel of its stream is finishing; it
+// must call griddep_wait() before reading anything that kernel wrote.  A
+// kernel calls griddep_launch_dependents() once the next kernel may be
+// scheduled (that kernel still waits for this one's completion and memory).
+__device__ __forceinline__ void griddep_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+inline void pdl_config(cudaLaunchConfig_t* cfg, cudaLaunchAttribute* attr, dim3 grid, dim3 block,
+                       size_t smem, cudaStream_t st) {
+  cfg->gridDim = grid;
+  cfg->blockDim = block;
+  cfg->dynamicSmemBytes = smem;
+  cfg->stream = st;
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg->attrs = attr;
+  cfg->numAttrs = 1;
+}
+
 // ---------------------------------------------------------------- launchers
 constexpr int kGb300Sms = 152;   // streaming multiprocessors of one GB300
 

@@ -177,79 +177,67 @@ verify_split_simple(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __
   }
 }
 
-// One CTA per (KV head, block of 8 packed rows): combine the split
-// partials.  Thread (c4, r) owns columns [4*c4, 4*c4+4) of row r, so each
-// warp reads four 128-byte runs of a split's column-quad-major partial.  The
-// split weights 2^(m_s - max m) of the 8 rows are formed once in shared memory.
+// One CTA per (KV head, block of 8 packed rows); thread (c4, r) owns
+// columns [4*c4, 4*c4+4) of row r and folds the splits in with the
+// online-softmax recurrence (running maximum, rescaled sum and accumulator),
+// the loads of kMergeBatch splits in flight at once.  Launched as a
+// programmatic dependent of the verification kernel: it waits for that grid's
+// partials before its first load.
 constexpr int kMaxSplits = 1024;
 constexpr int kMergeRows = 8;
-__global__ void __launch_bounds__(256)
+constexpr int kMergeBatch = 8;
+__global__ void __launch_bounds__(256, 2)
 verify_merge(const float* __restrict__ part_o, const float* __restrict__ part_ml, int T, int Hq,
              int Hkv, int D, int n_split, float* __restrict__ o, float* __restrict__ lse) {
-  __shared__ float wsp[kMaxSplits][kMergeRows];
-  __shared__ float red[8][kMergeRows];
+  griddep_wait();
   const int kv = blockIdx.y;
   const int G = Hq / Hkv, M = T * G;
   const int tid = threadIdx.x, r = tid % kMergeRows, c4 = tid / kMergeRows;
-  const int nq = D / 4;                       // threads per row
-  const int warp = tid >> 5, lane = tid & 31, n_warps = blockDim.x >> 5;
   const int R = blockIdx.x * kMergeRows + r;
-  const bool valid = R < M;
-  const size_t ml0 = (size_t)kv * n_split * M + R;   // + s*M
-  // lanes sharing r within a warp differ in lane bits 3 and 4
-  auto row_reduce = [&](float v, bool is_max) {
-    for (int off = 8; off < 32; off <<= 1) {
-      const float u = __shfl_xor_sync(0xffffffffu, v, off);
-      v = is_max ? fmaxf(v, u) : v + u;
+  if (R >= M) return;
+  const float4* src =
+      reinterpret_cast<const float4*>(part_o) + part_o4_index(kv, 0, n_split, c4, D, M, R);
+  const size_t step = (size_t)(D / 4) * M;              // float4s between splits
+  const float2* ml = reinterpret_cast<const float2*>(part_ml) + (size_t)kv * n_split * M + R;
+  float mrun = -INFINITY, lrun = 0.f;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int s0 = 0; s0 < n_split; s0 += kMergeBatch) {
+    float4 ov[kMergeBatch];
+    float2 mv[kMergeBatch];
+#pragma unroll
+    for (int k = 0; k < kMergeBatch; ++k) {
+      const int s = s0 + k;
+      if (s < n_split) {
+        ov[k] = src[(size_t)s * step];
+        mv[k] = ml[(size_t)s * M];
+      } else {
+        ov[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+        mv[k] = make_float2(-INFINITY, 0.f);
+      }
     }
-    __syncthreads();
-    if (lane < kMergeRows) red[warp][lane] = v;
-    __syncthreads();
-    float x = red[0][r];
-    for (int w = 1; w < n_warps; ++w) x = is_max ? fmaxf(x, red[w][r]) : x + red[w][r];
-    return x;
-  };
-  float mx = -INFINITY;
-  for (int s = c4; s < n_split; s += nq) {
-    const float m = valid ? part_ml[(ml0 + (size_t)s * M) * 2] : -INFINITY;
-    wsp[s][r] = m;
-    mx = fmaxf(mx, m);
+    float mb = mrun;
+#pragma unroll
+    for (int k = 0; k < kMergeBatch; ++k) mb = fmaxf(mb, mv[k].x);
+    if (mb == -INFINITY) continue;                      // no key seen yet
+    const float fr = exp2f(mrun - mb);                  // 0 while mrun = -inf
+    lrun *= fr;
+    acc = make_float4(acc.x * fr, acc.y * fr, acc.z * fr, acc.w * fr);
+#pragma unroll
+    for (int k = 0; k < kMergeBatch; ++k) {
+      const float w = exp2f(mv[k].x - mb);              // 0 for an empty split
+      lrun += w * mv[k].y;
+      acc.x += w * ov[k].x;
+      acc.y += w * ov[k].y;
+      acc.z += w * ov[k].z;
+      acc.w += w * ov[k].w;
+    }
+    mrun = mb;
   }
-  mx = row_reduce(mx, true);
-  float lsum = 0.f;
-  for (int s = c4; s < n_split; s += nq) {
-    const float m = wsp[s][r];
-    const float wgt = (m == -INFINITY) ? 0.f : exp2f(m - mx);
-    wsp[s][r] = wgt;
-    if (wgt != 0.f) lsum += wgt * part_ml[(ml0 + (size_t)s * M) * 2 + 1];
-  }
-  lsum = row_reduce(lsum, false);   // its barriers also publish wsp
-  if (!valid) return;
-  const float4* p4 = reinterpret_cast<const float4*>(part_o);
-  const size_t step = (size_t)nq * M;                 // float4s between splits
-  const float4* src = p4 + part_o4_index(kv, 0, n_split, c4, D, M, R);
-  float4 a = make_float4(0.f, 0.f, 0.f, 0.f), b = a;
-  auto acc = [](float4& x, float w, const float4& v) {
-    x.x += w * v.x;
-    x.y += w * v.y;
-    x.z += w * v.z;
-    x.w += w * v.w;
-  };
-  int s = 0;
-  for (; s + 4 <= n_split; s += 4) {
-    const float4 v0 = src[(size_t)s * step], v1 = src[(size_t)(s + 1) * step];
-    const float4 v2 = src[(size_t)(s + 2) * step], v3 = src[(size_t)(s + 3) * step];
-    acc(a, wsp[s][r], v0);
-    acc(b, wsp[s + 1][r], v1);
-    acc(a, wsp[s + 2][r], v2);
-    acc(b, wsp[s + 3][r], v3);
-  }
-  for (; s < n_split; ++s) acc(a, wsp[s][r], src[(size_t)s * step]);
-  const float inv = 1.f / lsum;
+  const float inv = 1.f / lrun;
   const int i = R / G, h = kv * G + R % G;
   reinterpret_cast<float4*>(o + ((size_t)i * Hq + h) * D)[c4] =
-      make_float4((a.x + b.x) * inv, (a.y + b.y) * inv, (a.z + b.z) * inv, (a.w + b.w) * inv);
-  if (lse && c4 == 0) lse[(size_t)i * Hq + h] = (mx + log2f(lsum)) * 0.6931471805599453f;
+      make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+  if (lse && c4 == 0) lse[(size_t)i * Hq + h] = (mrun + log2f(lrun)) * 0.6931471805599453f;
 }
 
 }  // namespace
@@ -292,7 +280,7 @@ VerifyPlan verify_plan(int T, int Hq, int Hkv, int d, int64_t L) {
     p.n_split = (int)((L + kps - 1) / kps);
   }
   if (p.n_split < 1) p.n_split = 1;
-  if (p.n_split > kMaxSplits) {   // the merge kernel holds one weight per split
+  if (p.n_split > kMaxSplits) {   // bounds the split partials of very long caches
     p.keys_per_split = ((L + kMaxSplits - 1) / kMaxSplits + 127) / 128 * 128;
     p.n_split = (int)((L + p.keys_per_split - 1) / p.keys_per_split);
   }
@@ -334,8 +322,11 @@ int launch_verify(const void* q, const void* k, const void* v, int64_t L, int64_
   }
   if (rc) return rc;
   dim3 mgrid((p.M + kMergeRows - 1) / kMergeRows, Hkv);
-  verify_merge<<<mgrid, kMergeRows * (d / 4), 0, st>>>(part_o, part_ml, T, Hq, Hkv, d, p.n_split, o,
-                                                       lse);
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  pdl_config(&cfg, attr, mgrid, dim3(kMergeRows * (d / 4)), 0, st);
+  cudaLaunchKernelEx(&cfg, verify_merge, static_cast<const float*>(part_o),
+                     static_cast<const float*>(part_ml), T, Hq, Hkv, d, p.n_split, o, lse);
   return launch_status("verify_merge");
 }
 

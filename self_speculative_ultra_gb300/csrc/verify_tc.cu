@@ -134,6 +134,9 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
   static_assert(kSK < kSV, "early loads fill K and V stages alike; the last V stage is set-up scratch");
 
   // ---------------------------------------------------------------- set-up
+  // launched as a programmatic dependent: nothing the previous kernel of the
+  // stream wrote is read before this
+  griddep_wait();
   if (tid == 0) {
     for (int s = 0; s < kSK; ++s) {
       ptx::mbar_init(&aux->k_full[s], 1);
@@ -278,6 +281,7 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
   __syncthreads();
   ptx::tc_fence_after();
   const uint32_t tmem = aux->tmem_base;
+  griddep_launch_dependents();   // the merge kernel may take SMs as CTAs retire
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
@@ -710,8 +714,11 @@ int launch_verify_tc(const void* q, const void* k, const void* v, int64_t L, int
   auto qb = static_cast<const __nv_bfloat16*>(q);
   auto go = [&](auto kern, int smem) {
     cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    kern<<<grid, kThreadsTc, smem, st>>>(mk, mv, qb, parents, T, Hq, Hkv, n_imp, L, L_cap,
-                                         keys_per_split, n_split, part_o, part_ml, imp, status);
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    pdl_config(&cfg, attr, grid, dim3(kThreadsTc), smem, st);
+    cudaLaunchKernelEx(&cfg, kern, mk, mv, qb, parents, T, Hq, Hkv, n_imp, L, L_cap,
+                       keys_per_split, n_split, part_o, part_ml, imp, status);
   };
   if (d == 128)
     go(verify_tc_kernel<128>, TcLayout<128>::kAlloc);
