@@ -29,9 +29,9 @@
 //                       back over S in fp16 (relative rounding 2^-11, four
 //                       times finer than bf16), row sums.  Tree mask and
 //                       split limits only touch the tiles that need them.
-//                       The same warps convert the next V tile in place from
-//                       bf16 to fp16 (exact for |v| < 65504; larger values
-//                       saturate and are reported in the status word).
+//   V conversion (12..15) each V tile is converted in place from bf16 to fp16
+//                       as soon as it lands (exact for |v| < 65504; larger
+//                       values saturate and are reported in the status word).
 // Each CTA writes an unnormalised partial (O, m, l) in the log2 domain; the
 // merge kernel of verify_attn.cu combines the splits.
 //
@@ -51,7 +51,7 @@ namespace {
 constexpr int kNk = 128;                 // keys per tile
 constexpr int kSK = 2;                   // K ring depth
 constexpr int kSV = 3;                   // V ring depth
-constexpr int kThreadsTc = 384;          // 12 warps
+constexpr int kThreadsTc = 512;          // 16 warps
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLazy = 8.0f;            // running max refreshed only past +2^8
 constexpr long long kWaitCycles = 1ll << 31;
@@ -144,7 +144,7 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
     }
     for (int s = 0; s < kSV; ++s) {
       ptx::mbar_init(&aux->v_full[s], 1);
-      ptx::mbar_init(&aux->v_conv[s], 4 * nt);   // one arrival per softmax warp
+      ptx::mbar_init(&aux->v_conv[s], 4);        // one arrival per conversion warp
       ptx::mbar_init(&aux->v_empty[s], 1);
     }
     for (int g = 0; g < 2; ++g) {
@@ -329,29 +329,33 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
     if (lane == 0) {
       constexpr uint32_t idesc_qk = ptx::idesc_bf16_f32(128, kNk, false);
       constexpr uint32_t idesc_pv = ptx::idesc_f16_f32(128, D, true);
-      const uint32_t sq_a = ptx::smem_u32(sq), sk_a = ptx::smem_u32(sk), sv_a = ptx::smem_u32(sv);
+      // operand descriptors: built once; a descriptor's start address is its
+      // low field in 16-byte units, so tile, stage and K-step offsets are adds
+      const uint64_t qd0 = ptx::sdesc_sw128(ptx::smem_u32(sq), 16, 1024);
+      const uint64_t kd0 = ptx::sdesc_sw128(ptx::smem_u32(sk), 16, 1024);
+      const uint64_t vd0 = ptx::sdesc_sw128(ptx::smem_u32(sv), Ly::kPanel, 1024);
+      constexpr uint32_t kTile16 = Ly::kTile >> 4, kPanel16 = Ly::kPanel >> 4;
       auto qk = [&](int g, int j) {
-        const int s = j % kSK;
+        const uint64_t a0 = qd0 + (uint64_t)(g * kTile16);
+        const uint64_t b0 = kd0 + (uint64_t)((j % kSK) * kTile16);
 #pragma unroll
         for (int ks = 0; ks < D / 16; ++ks) {
-          const uint32_t off = (ks >> 2) * Ly::kPanel + (ks & 3) * 32;
-          const uint64_t a = ptx::sdesc_sw128(sq_a + g * Ly::kTile + off, 16, 1024);
-          const uint64_t b = ptx::sdesc_sw128(sk_a + s * Ly::kTile + off, 16, 1024);
-          ptx::mma_ss(tmem + Ly::sbase(g), a, b, idesc_qk, ks > 0 ? 1u : 0u);
+          const uint32_t off = (ks >> 2) * kPanel16 + (ks & 3) * 2;   // 64-element panels, 32-byte K-steps
+          ptx::mma_ss(tmem + Ly::sbase(g), a0 + off, b0 + off, idesc_qk, ks > 0 ? 1u : 0u);
         }
         ptx::mma_commit(&aux->s_full[g]);
       };
       // O += P V in fp16.  Keys [32c, 32c+32) of the tile keep their fp16 P
       // pairs in S_g columns [32c, 32c+16): K-step ks (16 keys) reads the 8
-      // columns at 32*(ks/2) + 8*(ks%2).
+      // columns at 32*(ks/2) + 8*(ks%2); V advances 16 rows (2048 bytes).
       auto pv = [&](int g, int j) {
-        const int s = j % kSV;
+        const uint64_t b0 = vd0 + (uint64_t)((j % kSV) * kTile16);
+        const uint32_t acc = j > 0 ? 1u : 0u;
 #pragma unroll
         for (int ks = 0; ks < kNk / 16; ++ks) {
-          const uint64_t b = ptx::sdesc_sw128(sv_a + s * Ly::kTile + ks * 2048, Ly::kPanel, 1024);
           const uint32_t acol = 32 * (ks >> 1) + 8 * (ks & 1);
-          ptx::mma_ts(tmem + Ly::obase(g), tmem + Ly::sbase(g) + acol, b, idesc_pv,
-                      (j > 0 || ks > 0) ? 1u : 0u);
+          ptx::mma_ts(tmem + Ly::obase(g), tmem + Ly::sbase(g) + acol, b0 + (uint64_t)(ks * 128),
+                      idesc_pv, ks > 0 ? 1u : acc);
         }
       };
       bool ok = ptx::mbar_wait(&aux->k_full[0], 0, kWaitCycles);
@@ -441,34 +445,25 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(&aux->k_empty[s]);
     }
-  } else {
-    // ------------------------------------------------------------ softmax
-    const int g = (warp - 4) >> 2;
-    const int quarter = warp & 3;
-    const int t = quarter * 32 + lane;            // row within the tile
-    const int R = r0 + g * 128 + t;
-    const bool valid = (g < nt) && (R < M);
-    const unsigned long long anc = valid ? aux->anc[R / G] : 0ull;
-    const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
-    const uint32_t s_addr = tmem + lane_off + Ly::sbase(g);
-    const uint32_t o_addr = tmem + lane_off + Ly::obase(g);
-    float m_used = -INFINITY, l = 0.f;
-    bool ok = true;
-    // V tiles are converted in place from bf16 to fp16 by the softmax warps:
-    // with two row tiles each group converts half of a tile, else group 0
-    // converts all of it.  Tile j+1 is converted right after P of tile j is
-    // published, off the softmax -> MMA critical path.
-    float vmax = 0.f;         // largest |v| converted (fp16 range check)
-    auto convert_v = [&](int j) -> bool {
+  } else if (warp >= 12) {
+    // ------------------------------------------------------------ V conversion
+    // V tiles are converted in place from bf16 to fp16 as soon as they land,
+    // ahead of the MMA's P V (the V ring is three tiles deep)
+    const int t = tid - 12 * 32;
+    constexpr int kChunks = Ly::kTile / 16;          // 16-byte chunks per V tile
+    constexpr int kConvThreads = kThreadsTc - 12 * 32;
+    float vmax = 0.f;                                // largest |v| (fp16 range check)
+    for (int j = 0; j < n_tiles; ++j) {
       const int sv_ = j % kSV;
-      bool got = !aux->abort_flag &&
-                 ptx::mbar_wait(&aux->v_full[sv_], (uint32_t)(j / kSV) & 1u, kWaitCycles);
-      if (!__all_sync(0xffffffffu, got)) return false;
-      constexpr int kChunks = Ly::kTile / 16;
-      const int per = kChunks / nt;
-      uint4* vt = reinterpret_cast<uint4*>(sv + sv_ * Ly::kTile) + g * per;
-#pragma unroll 4
-      for (int e = t; e < per; e += 128) {
+      const bool got = !aux->abort_flag &&
+                       ptx::mbar_wait(&aux->v_full[sv_], (uint32_t)(j / kSV) & 1u, kWaitCycles);
+      if (!__all_sync(0xffffffffu, got)) {
+        timeout(aux, status);
+        break;
+      }
+      uint4* vt = reinterpret_cast<uint4*>(sv + sv_ * Ly::kTile);
+#pragma unroll 8
+      for (int e = t; e < kChunks; e += kConvThreads) {
         uint4 u = vt[e];
         uint32_t wd[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
@@ -482,9 +477,21 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
       ptx::fence_proxy_async_smem();   // generic writes -> the MMA's async-proxy reads
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(&aux->v_conv[sv_]);
-      return true;
-    };
-    if (g < nt && !convert_v(0)) ok = false;
+    }
+    if (!(vmax <= 65504.f)) set_status(status, TS_ERR_UNSUPPORTED);
+  } else {
+    // ------------------------------------------------------------ softmax
+    const int g = (warp - 4) >> 2;
+    const int quarter = warp & 3;
+    const int t = quarter * 32 + lane;            // row within the tile
+    const int R = r0 + g * 128 + t;
+    const bool valid = (g < nt) && (R < M);
+    const unsigned long long anc = valid ? aux->anc[R / G] : 0ull;
+    const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+    const uint32_t s_addr = tmem + lane_off + Ly::sbase(g);
+    const uint32_t o_addr = tmem + lane_off + Ly::obase(g);
+    float m_used = -INFINITY, l = 0.f;
+    bool ok = true;
     if (g < nt && ok) {
       // tcgen05.ld/st are warp-collective: every branch around them is warp-uniform
       for (int j = 0; j < n_tiles; ++j) {
@@ -513,23 +520,26 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
             if (!vis) r[x] = kNegInf;
           }
         };
-        // pass 1: tile maximum
+        // pass 1: tile maximum; chunks 0 and 1 are loaded last and stay in
+        // registers for pass 2
         float mx;
-        {
-          uint32_t a0[32], a1[32], a2[32], a3[32];
-          ptx::tmem_ld32(s_addr, a0);
-          ptx::tmem_ld32(s_addr + 32, a1);
-          ptx::tmem_ld32(s_addr + 64, a2);
-          ptx::tmem_ld32(s_addr + 96, a3);
-          ptx::tmem_ld_wait();
-          if (edge) {
-            mask(a0, 0);
-            mask(a1, 1);
-            mask(a2, 2);
-            mask(a3, 3);
-          }
-          mx = fmaxf(fmaxf(fmax32(a0), fmax32(a1)), fmaxf(fmax32(a2), fmax32(a3)));
+        uint32_t ca[32], cb[32];
+        ptx::tmem_ld32(s_addr + 64, ca);
+        ptx::tmem_ld32(s_addr + 96, cb);
+        ptx::tmem_ld_wait();
+        if (edge) {
+          mask(ca, 2);
+          mask(cb, 3);
         }
+        mx = fmaxf(fmax32(ca), fmax32(cb));
+        ptx::tmem_ld32(s_addr, ca);
+        ptx::tmem_ld32(s_addr + 32, cb);
+        ptx::tmem_ld_wait();
+        if (edge) {
+          mask(ca, 0);
+          mask(cb, 1);
+        }
+        mx = fmaxf(mx, fmaxf(fmax32(ca), fmax32(cb)));
         // lazy running max: raise it only when the tile max exceeds it by 2^8.
         // S_g of this tile completing implies P_g V of the previous tile did
         // (MMAs of one thread complete in order), so O_g may be rescaled.
@@ -542,13 +552,13 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
         }
         if (j > 0 && __any_sync(0xffffffffu, raise)) {
 #pragma unroll 1
-          for (int c = 0; c < D / 32; ++c) {
-            uint32_t o[32];
-            ptx::tmem_ld32(o_addr + c * 32, o);
+          for (int c = 0; c < D / 16; ++c) {
+            uint32_t o[16];
+            ptx::tmem_ld16(o_addr + c * 16, o);
             ptx::tmem_ld_wait();
 #pragma unroll
-            for (int x = 0; x < 32; ++x) o[x] = __float_as_uint(__uint_as_float(o[x]) * f);
-            ptx::tmem_st32(o_addr + c * 32, o);
+            for (int x = 0; x < 16; ++x) o[x] = __float_as_uint(__uint_as_float(o[x]) * f);
+            ptx::tmem_st16(o_addr + c * 16, o);
           }
           ptx::tmem_st_wait();
         }
@@ -560,9 +570,9 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
         const uint64_t sl2x2 = ptx::f2(sl2, sl2);
         const uint64_t negm = ptx::f2(-mref, -mref);
         uint64_t lsum = 0;
-        uint32_t ca[32], cb[32];
+        // chunks 0 and 1 arrive masked from pass 1; chunks 2 and 3 are reloaded
         auto process = [&](uint32_t (&r)[32], int c) {
-          if (edge) mask(r, c);
+          if (edge && c >= 2) mask(r, c);
           uint32_t pw[16];
 #pragma unroll
           for (int x = 0; x < 16; ++x) {
@@ -576,9 +586,6 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
           }
           ptx::tmem_st16(s_addr + 32 * c, pw);
         };
-        ptx::tmem_ld32(s_addr, ca);
-        ptx::tmem_ld32(s_addr + 32, cb);
-        ptx::tmem_ld_wait();
         process(ca, 0);
         ptx::tmem_ld32(s_addr + 64, ca);
         process(cb, 1);
@@ -595,10 +602,6 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
         ptx::tmem_st_wait();
         ptx::tc_fence_before();
         ptx::mbar_arrive(&aux->p_ready[g]);
-        if (j + 1 < n_tiles && !convert_v(j + 1)) {
-          ok = false;
-          break;
-        }
       }
       // epilogue: final O row -> unnormalised partial
       bool fin = ok && !aux->abort_flag && ptx::mbar_wait(&aux->o_final, 0, kWaitCycles);
@@ -632,7 +635,6 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
       }
     }
     if (!ok) timeout(aux, status);
-    if (!(vmax <= 65504.f)) set_status(status, TS_ERR_UNSUPPORTED);
   }
 
   ptx::tc_fence_before();
