@@ -506,6 +506,52 @@ def run_profile_case(kind: str, w: syn.Workload):
     print(json.dumps({"profile_case": kind, "workload": w.name, "layers": nl}))
 
 
+def run_draft_case(w: syn.Workload, steps: int, warmup: int):
+    """Draft-side attention over the compact cache (the partial-cache half of a
+    step): ts_verify_attention with a 4-token draft chain over the S+B+R
+    gathered rows plus the draft rows, one call per layer, distinct buffers
+    per layer (inputs larger than L2).  Prints one JSON line."""
+    import torch
+    import self_speculative_ultra_gb300 as ts
+    ts.build()
+    dev = torch.device("cuda", 0)
+    g = torch.Generator(device=dev)
+    g.manual_seed(0)
+    T_d, Hq, Hkv, d = 4, w.Hq, w.Hkv, w.d
+    N = min(w.L, w.S + w.B + w.R)
+    layers = w.layers
+    ks = [torch.randn((Hkv, N + T_d, d), generator=g, device=dev).to(torch.bfloat16) for _ in range(layers)]
+    vs = [torch.randn((Hkv, N + T_d, d), generator=g, device=dev).to(torch.bfloat16) for _ in range(layers)]
+    q = torch.randn((T_d, Hq, d), generator=g, device=dev).to(torch.bfloat16)
+    par = torch.tensor([-1] + list(range(T_d - 1)), dtype=torch.int32, device=dev)
+    ws = torch.empty(ts.ts_verify_workspace_bytes(T_d, Hq, Hkv, d, N), dtype=torch.uint8, device=dev)
+    o = torch.empty((T_d, Hq, d), device=dev)
+    lse = torch.empty((T_d, Hq), device=dev)
+    def one_pass():
+        for i in range(layers):
+            ts.ts_verify_attention(q, ks[i], vs[i], N, par, n_imp=T_d, o=o, lse=lse,
+                                   want_imp=False, workspace=ws)
+    for _ in range(warmup):
+        one_pass()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(steps):
+        one_pass()
+    e1.record()
+    torch.cuda.synchronize()
+    us = e0.elapsed_time(e1) * 1e3 / (steps * layers)
+    nbytes = 2 * Hkv * (N + T_d) * d * 2 + T_d * Hq * d * 2 + T_d * Hq * (d + 1) * 4
+    peak, peak_src = load_peaks()
+    gbs = nbytes / (us * 1e-6) / 1e9
+    print(json.dumps({"metric": "draft attention over the compact cache (GB/s)", "value": round(gbs, 1),
+                      "unit": "GB/s", "us_per_call": round(us, 2), "calls": steps * layers,
+                      "config": {"workload": w.name, "draft_tokens": T_d, "compact_rows": N,
+                                 "Hq": Hq, "Hkv": Hkv, "d": d, "bytes_per_call": nbytes,
+                                 "l2": f"{layers} distinct per-layer caches, {layers * 2 * Hkv * (N + T_d) * d * 2 / 1e6:.0f} MB"},
+                      "frac_of_peak": round(gbs / peak, 3), "peak_source": peak_src}))
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -516,9 +562,13 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--profile", choices=["verify", "select"],
                     help="run a small fixed case for ncu captures and exit")
+    ap.add_argument("--draft", action="store_true",
+                    help="time draft-side attention over the compact cache and exit")
     args = ap.parse_args()
     w = syn.WORKLOADS[args.workload]
-    if args.profile:
+    if args.draft:
+        run_draft_case(w, args.steps, args.warmup)
+    elif args.profile:
         run_profile_case(args.profile, w)
     elif args.impl == "reference":
         run_reference(args, w)
