@@ -8,10 +8,14 @@
 // 1.0, top-p 0.9, min-p 0.05), §3.1 Overview (exact-match verification, the
 // longest valid draft is kept, then the KV cache is updated).
 //
-// One CTA per tree node.  The node's window is marked in a shared-memory
-// bitmap, the penalised/tempered logits x' are written once to the
-// workspace, and e_t = exp(x'_t - max x') gives the unnormalised
-// probabilities.  In rank order (x' desc, id asc) both truncations keep a
+// Each tree node's vocabulary is split over kParts CTAs.  Every CTA marks
+// the node's window in a shared-memory bitmap, writes the penalised/tempered
+// logits x' of its slice once to the workspace, and publishes its slice
+// maximum m_c, Z_c = sum exp(x' - m_c) and the tokens with
+// exp(x' - m_c) >= min_p (a superset of the node's min-p set, as m_c <= the
+// node maximum).  The last CTA of the node (atomic ticket, no waiting) takes
+// the maximum over the slices, rescales and adds the Z_c, and keeps the
+// candidates with e_t = exp(x'_t - max x') >= min_p.  In rank order (x' desc, id asc) both truncations keep a
 // prefix: top-p keeps ranks up to the first whose inclusive mass reaches
 // top_p * Z, min-p keeps the ranks with e >= min_p.  So the kept set always
 // lies inside the min-p set; when that set is small (the usual case:
@@ -28,7 +32,9 @@ namespace ts {
 
 namespace {
 
-constexpr int kThreads = 1024;
+constexpr int kThreads = 512;
+constexpr int kParts = 4;                // CTAs per tree node
+constexpr int kCapPart = 4096;           // candidates one slice may publish
 constexpr int kMaxBuckets = 2048;
 constexpr uint32_t kIdMask = 0x3FFFFu;   // V <= 2^18
 
@@ -54,9 +60,43 @@ struct SampleSmem {
   float mb;     // mass ranked before the current bucket range
   int cb;       // count ranked before the current bucket range
   int32_t ptok[64];
+  int32_t par[64], tok[64], smp[64];     // the tree, staged once (T <= 64)
+  int32_t dep[64];
+  uint8_t acc[64];
   int plen;
   int last;
 };
+
+struct PartStat {
+  float m;     // slice maximum of x'
+  float z;     // sum over the slice of exp(x' - m)
+  int n;       // tokens with exp(x' - m) >= min_p (may exceed kCapPart)
+  int pad;
+};
+
+// workspace: [counters | PartStat [T][kParts] | candidates [T][kParts][kCapPart] | x' [T][V]]
+constexpr size_t kCounterBytes = 1024;   // node tickets [64] + step counter
+struct SampleWs {
+  int32_t* node_ticket;
+  int32_t* counter;
+  PartStat* stat;
+  uint2* cand;     // (float_key(x'), token id)
+  float* xs;
+};
+__host__ __device__ inline size_t a256s(size_t x) { return (x + 255) / 256 * 256; }
+__host__ __device__ inline SampleWs carve_sample(void* base, int T) {
+  char* p = static_cast<char*>(base);
+  SampleWs w;
+  w.node_ticket = reinterpret_cast<int32_t*>(p);
+  w.counter = w.node_ticket + 64;
+  size_t o = kCounterBytes;
+  w.stat = reinterpret_cast<PartStat*>(p + o);
+  o += a256s((size_t)T * kParts * sizeof(PartStat));
+  w.cand = reinterpret_cast<uint2*>(p + o);
+  o += a256s((size_t)T * kParts * kCapPart * sizeof(uint2));
+  w.xs = reinterpret_cast<float*>(p + o);
+  return w;
+}
 
 // inverse of float_key
 __device__ __forceinline__ float key_float(uint32_t k) {
@@ -214,27 +254,32 @@ __device__ Found radix_find(const float* __restrict__ xs, int V, float xmax, int
   return f;
 }
 
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kThreads, 2)
 sample_accept_kernel(const float* __restrict__ logits, const int32_t* __restrict__ tree_tokens,
                      const int32_t* __restrict__ parents, int T, const int32_t* __restrict__ prior,
                      int n_prior, int W, int V, float penalty, float temperature, float top_p,
                      float min_p, const float* __restrict__ uniforms, int32_t* sampled,
                      int32_t* __restrict__ path, int32_t* __restrict__ n_path,
-                     int32_t* __restrict__ bonus, int32_t* counter, float* __restrict__ xs_all,
-                     int32_t* status) {
+                     int32_t* __restrict__ bonus, SampleWs ws, int32_t* status) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
   SampleSmem& sm = *reinterpret_cast<SampleSmem*>(smem_raw);
   uint32_t* bitmap = reinterpret_cast<uint32_t*>(smem_raw + sizeof(SampleSmem));
-  const int i = blockIdx.x, tid = threadIdx.x;
+  const int part = blockIdx.x, i = blockIdx.y, tid = threadIdx.x;
+  const int lane = tid & 31;
   const int nwords = (V + 31) / 32;
   for (int w = tid; w < nwords; w += kThreads) bitmap[w] = 0u;
+  if (tid < T) {
+    sm.par[tid] = parents[tid];
+    sm.tok[tid] = tree_tokens[tid];
+  }
+  __syncthreads();
   if (tid == 0) {
     // drafted tokens on the root path of node i, root excluded, root first
     int tmp[64], n = 0, a = i;
     bool ok = true;
     while (a > 0 && n < 64) {
       tmp[n++] = a;
-      int p = parents[a];
+      int p = sm.par[a];
       if (p < 0 || p >= a) {
         ok = false;
         break;
@@ -245,8 +290,9 @@ sample_accept_kernel(const float* __restrict__ logits, const int32_t* __restrict
       set_status(status, TS_ERR_INVALID_ARG);
       n = 0;
     }
-    for (int x = 0; x < n; ++x) sm.ptok[x] = tree_tokens[tmp[n - 1 - x]];
+    for (int x = 0; x < n; ++x) sm.ptok[x] = sm.tok[tmp[n - 1 - x]];
     sm.plen = n;
+    sm.ncand = 0;
   }
   __syncthreads();
   // window = last W tokens of prior ++ path tokens
@@ -262,56 +308,154 @@ sample_accept_kernel(const float* __restrict__ logits, const int32_t* __restrict
   }
   __syncthreads();
 
-  // x' = penalised / tempered logits; running max
+  // this CTA's slice of the vocabulary: x' = penalised / tempered logits
+  // slices are whole float4s when rows are 16-byte aligned (V % 4 == 0)
+  const bool vec = (V & 3) == 0;
+  int per = (V + kParts - 1) / kParts;
+  if (vec) per = (per + 3) & ~3;
+  const int t0 = min(V, part * per), t1 = min(V, t0 + per);
   const float* x_in = logits + (size_t)i * V;
-  float* xs = xs_all + (size_t)i * V;
-  float lmax = -INFINITY;
-  for (int t = tid; t < V; t += kThreads) {
-    float x = x_in[t];
+  float* xs = ws.xs + (size_t)i * V;
+  const bool unit_temp = temperature == 1.0f;     // x / 1 is x exactly
+  auto xprime = [&](float x, int t) {
     if ((bitmap[t >> 5] >> (t & 31)) & 1u) x = (x > 0.f) ? __fdiv_rn(x, penalty) : __fmul_rn(x, penalty);
-    x = __fdiv_rn(x, temperature);
-    xs[t] = x;
-    lmax = fmaxf(lmax, x);
+    if (!unit_temp) x = __fdiv_rn(x, temperature);
+    return x;
+  };
+  float lmax = -INFINITY;
+  if (vec) {
+    const float4* in4 = reinterpret_cast<const float4*>(x_in);
+    float4* xs4 = reinterpret_cast<float4*>(xs);
+#pragma unroll 2
+    for (int q = t0 / 4 + tid; q < t1 / 4; q += kThreads) {
+      float4 a = in4[q];
+      const int t = 4 * q;
+      a.x = xprime(a.x, t);
+      a.y = xprime(a.y, t + 1);
+      a.z = xprime(a.z, t + 2);
+      a.w = xprime(a.w, t + 3);
+      xs4[q] = a;
+      lmax = fmaxf(lmax, fmaxf(fmaxf(a.x, a.y), fmaxf(a.z, a.w)));
+    }
+  } else {
+    for (int t = t0 + tid; t < t1; t += kThreads) {
+      const float x = xprime(x_in[t], t);
+      xs[t] = x;
+      lmax = fmaxf(lmax, x);
+    }
   }
-  const float xmax = block_max(lmax, sm);
-  __syncthreads();   // xs visible to the whole block
-
-  // Z, the min-p set {e >= min_p} (count, mass) and, while it fits, its members
-  if (tid == 0) sm.ncand = 0;
-  __syncthreads();
-  float z = 0.f, zmin = 0.f;
-  int nmin = 0;
-  const int lane = tid & 31;
-  for (int t0 = 0; t0 < V; t0 += kThreads) {
-    const int t = t0 + tid;
-    float e = 0.f, x = 0.f;
-    if (t < V) {
-      x = xs[t];
-      e = expf(x - xmax);
+  const float mc = block_max(lmax, sm);
+  // Z_c and the slice's tokens with exp(x' - m_c) >= min_p (each thread
+  // rereads the values it wrote)
+  uint2* cand = ws.cand + ((size_t)i * kParts + part) * kCapPart;
+  float z = 0.f;
+  auto consider = [&](bool valid, float x, int t) {
+    float e = 0.f;
+    if (valid) {
+      e = expf(x - mc);
       z += e;
     }
-    const bool in = t < V && e >= min_p;
-    if (in) {
-      zmin += e;
-      ++nmin;
-    }
+    const bool in = valid && e >= min_p;
     const unsigned m = __ballot_sync(0xffffffffu, in);
     if (m) {
       int base = 0;
       if (lane == __ffs(m) - 1) base = atomicAdd(&sm.ncand, __popc(m));
       base = __shfl_sync(0xffffffffu, base, __ffs(m) - 1);
       const int slot = base + __popc(m & ((1u << lane) - 1));
-      if (in && slot < kCap) {
-        sm.ckey[slot] = float_key(x);
-        sm.cid[slot] = t;
+      if (in && slot < kCapPart) cand[slot] = make_uint2(float_key(x), (uint32_t)t);
+    }
+  };
+  if (vec) {
+    const float4* xs4 = reinterpret_cast<const float4*>(xs);
+    for (int b0 = t0 / 4; b0 < t1 / 4; b0 += kThreads) {
+      const int q = b0 + tid;
+      const bool valid = q < t1 / 4;
+      const float4 a = valid ? xs4[q] : make_float4(0.f, 0.f, 0.f, 0.f);
+      consider(valid, a.x, 4 * q);
+      consider(valid, a.y, 4 * q + 1);
+      consider(valid, a.z, 4 * q + 2);
+      consider(valid, a.w, 4 * q + 3);
+    }
+  } else {
+    for (int b0 = t0; b0 < t1; b0 += kThreads) {
+      const int t = b0 + tid;
+      consider(t < t1, t < t1 ? xs[t] : 0.f, t);
+    }
+  }
+  const float zc = block_sum(z, sm);
+  if (tid == 0) {
+    ws.stat[i * kParts + part] = PartStat{mc, zc, sm.ncand, 0};
+    __threadfence();
+    sm.last = atomicAdd(&ws.node_ticket[i], 1) == kParts - 1;
+  }
+  __syncthreads();
+  if (!sm.last) return;
+
+  // ---- last CTA of node i: merge the slices
+  __threadfence();
+  const volatile PartStat* vst = ws.stat + i * kParts;
+  float xmax = -INFINITY;
+  bool overflow = false;
+  for (int p = 0; p < kParts; ++p) {
+    xmax = fmaxf(xmax, vst[p].m);
+    overflow |= vst[p].n > kCapPart;
+  }
+  float Z = 0.f;
+  for (int p = 0; p < kParts; ++p) {
+    const float m = vst[p].m;
+    if (m != -INFINITY) Z += vst[p].z * expf(m - xmax);
+  }
+  if (tid == 0) {
+    sm.ncand = 0;
+    ws.node_ticket[i] = 0;
+  }
+  __syncthreads();
+  // the node's min-p set {e >= min_p}, e = exp(x' - max x'), from the slices' supersets
+  float zmin = 0.f;
+  int nmin = 0;
+  if (!overflow) {
+    for (int p = 0; p < kParts; ++p) {
+      const int np_ = vst[p].n;
+      const uint2* pc = ws.cand + ((size_t)i * kParts + p) * kCapPart;
+      for (int b0 = 0; b0 < np_; b0 += kThreads) {
+        const int r = b0 + tid;
+        uint2 c = make_uint2(0u, 0u);
+        float e = 0.f;
+        if (r < np_) {
+          c = __ldcg(pc + r);
+          e = expf(key_float(c.x) - xmax);
+        }
+        const bool in = r < np_ && e >= min_p;
+        if (in) {
+          zmin += e;
+          ++nmin;
+        }
+        const unsigned m = __ballot_sync(0xffffffffu, in);
+        if (m) {
+          int base = 0;
+          if (lane == __ffs(m) - 1) base = atomicAdd(&sm.ncand, __popc(m));
+          base = __shfl_sync(0xffffffffu, base, __ffs(m) - 1);
+          const int slot = base + __popc(m & ((1u << lane) - 1));
+          if (in && slot < kCap) {
+            sm.ckey[slot] = c.x;
+            sm.cid[slot] = (int32_t)c.y;
+          }
+        }
+      }
+    }
+  } else {
+    for (int t = tid; t < V; t += kThreads) {
+      const float e = expf(xs[t] - xmax);
+      if (e >= min_p) {
+        zmin += e;
+        ++nmin;
       }
     }
   }
-  const float Z = block_sum(z, sm);
   float Zmin = block_sum(zmin, sm);
   int n_minp = block_sum_int(nmin, sm);
   int token;
-  if (n_minp >= 1 && n_minp <= kCap) {
+  if (!overflow && n_minp >= 1 && n_minp <= kCap) {
     // ---- fast path: the kept set is a rank prefix inside the min-p set.
     // Sort the candidates by (x' desc, id asc) (bitonic, padded to 2^k),
     // prefix-sum their e, cut at top-p, draw.
@@ -416,38 +560,40 @@ sample_accept_kernel(const float* __restrict__ logits, const int32_t* __restrict
   if (tid == 0) {
     sampled[i] = token;
     __threadfence();
-    int prev = atomicAdd(counter, 1);
+    int prev = atomicAdd(ws.counter, 1);
     sm.last = (prev == T - 1);
   }
   __syncthreads();
-  if (sm.last && tid == 0) {
-    __threadfence();
-    volatile const int32_t* vs = sampled;
-    bool acc[64];
-    int depth[64];
-    acc[0] = true;
-    depth[0] = 0;
+  if (!sm.last) return;
+  // the last node: every draw is published; stage them, then walk the tree
+  // in shared memory
+  __threadfence();
+  if (tid < T) sm.smp[tid] = __ldcg(sampled + tid);
+  __syncthreads();
+  if (tid == 0) {
+    sm.acc[0] = 1;
+    sm.dep[0] = 0;
     int best = 0;
     for (int c = 1; c < T; ++c) {
-      int p = parents[c];
+      const int p = sm.par[c];
       if (p < 0 || p >= c) {
-        acc[c] = false;
-        depth[c] = 0;
+        sm.acc[c] = 0;
+        sm.dep[c] = 0;
         continue;
       }
-      depth[c] = depth[p] + 1;
-      acc[c] = acc[p] && tree_tokens[c] == vs[p];
-      if (acc[c] && depth[c] > depth[best]) best = c;
+      sm.dep[c] = sm.dep[p] + 1;
+      sm.acc[c] = sm.acc[p] && sm.tok[c] == sm.smp[p];
+      if (sm.acc[c] && sm.dep[c] > sm.dep[best]) best = c;
     }
-    const int n = depth[best] + 1;
+    const int n = sm.dep[best] + 1;
     int a = best;
     for (int d = n - 1; d >= 0; --d) {
       path[d] = a;
-      a = parents[a];
+      a = sm.par[a];
     }
     *n_path = n;
-    *bonus = vs[best];
-    *counter = 0;
+    *bonus = sm.smp[best];
+    *ws.counter = 0;
   }
 }
 
@@ -490,22 +636,24 @@ __global__ void kv_commit_kernel(__nv_bfloat16* __restrict__ k, __nv_bfloat16* _
 
 }  // namespace
 
-size_t sample_ws_bytes(int T, int V) { return 256 + align_up((size_t)T * V * sizeof(float), 256); }
+size_t sample_ws_bytes(int T, int V) {
+  return kCounterBytes + a256s((size_t)T * kParts * sizeof(PartStat)) +
+         a256s((size_t)T * kParts * kCapPart * sizeof(uint2)) + a256s((size_t)T * V * sizeof(float));
+}
 
 int launch_sample_accept(const float* logits, const int32_t* tree_tokens, const int32_t* parents,
                          int T, const int32_t* prior, int n_prior, int W, int V, float penalty,
                          float temperature, float top_p, float min_p, const float* uniforms,
                          int32_t* sampled, int32_t* path, int32_t* n_path, int32_t* bonus,
                          void* ws, int32_t* status, cudaStream_t st) {
-  int32_t* counter = static_cast<int32_t*>(ws);
-  float* xs = reinterpret_cast<float*>(static_cast<char*>(ws) + 256);
-  if (cudaMemsetAsync(counter, 0, sizeof(int32_t), st) != cudaSuccess)
+  const SampleWs w = carve_sample(ws, T);
+  if (cudaMemsetAsync(ws, 0, kCounterBytes, st) != cudaSuccess)
     return launch_status("sample counter reset");
   size_t smem = sizeof(SampleSmem) + (size_t)((V + 31) / 32) * sizeof(uint32_t);
   cudaFuncSetAttribute(sample_accept_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  sample_accept_kernel<<<T, kThreads, smem, st>>>(logits, tree_tokens, parents, T, prior, n_prior, W,
-                                                  V, penalty, temperature, top_p, min_p, uniforms,
-                                                  sampled, path, n_path, bonus, counter, xs, status);
+  sample_accept_kernel<<<dim3(kParts, T), kThreads, smem, st>>>(
+      logits, tree_tokens, parents, T, prior, n_prior, W, V, penalty, temperature, top_p, min_p,
+      uniforms, sampled, path, n_path, bonus, w, status);
   return launch_status("sample_accept_kernel");
 }
 
