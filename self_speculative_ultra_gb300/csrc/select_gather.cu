@@ -113,6 +113,50 @@ __device__ __forceinline__ bool keep_pos(const float* __restrict__ imp_h, int64_
   return key > st.tau || (key == st.tau && j <= st.j_tie);
 }
 
+// Visit positions [lo, hi) of one importance row: f(j, imp[j], valid) is
+// called the same number of times by every lane (valid = false past the
+// end), so f may use warp votes.  The aligned interior is read as float4s,
+// four per thread in flight.
+template <typename F>
+__device__ __forceinline__ void for_each_pos(const float* __restrict__ imp_h, int64_t lo,
+                                             int64_t hi, F f) {
+  const int tid = threadIdx.x, nthr = blockDim.x;
+  int64_t vlo = hi, vhi = hi;
+  if ((reinterpret_cast<uintptr_t>(imp_h) & 15) == 0 && lo < hi) {
+    vlo = imin64(hi, (lo + 3) & ~int64_t(3));
+    vhi = imax64(vlo, hi & ~int64_t(3));
+  }
+  auto scalar = [&](int64_t a, int64_t b) {
+    for (int64_t j0 = a; j0 < b; j0 += nthr) {
+      const int64_t j = j0 + tid;
+      const bool ok = j < b;
+      f(j, ok ? imp_h[j] : 0.f, ok);
+    }
+  };
+  scalar(lo, vlo);
+  const float4* p4 = reinterpret_cast<const float4*>(imp_h) + vlo / 4;
+  const int64_t nq = (vhi - vlo) / 4;
+  for (int64_t q0 = 0; q0 < nq; q0 += 4 * nthr) {
+    float4 v[4];
+    bool ok[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int64_t q = q0 + k * nthr + tid;
+      ok[k] = q < nq;
+      v[k] = ok[k] ? __ldg(p4 + q) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int64_t j = vlo + 4 * (q0 + k * nthr + tid);
+      f(j, v[k].x, ok[k]);
+      f(j + 1, v[k].y, ok[k]);
+      f(j + 2, v[k].z, ok[k]);
+      f(j + 3, v[k].w, ok[k]);
+    }
+  }
+  scalar(vhi, hi);
+}
+
 // exclusive prefix over the block (blockDim.x a multiple of 32)
 __device__ int block_excl_scan(int x, int* warp_buf, int* total) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
@@ -197,8 +241,9 @@ select_hist(Layers P, int64_t L, int B, int S, int R, int64_t n_chunks, Ws w) {
     for (int b = tid; b < kBins; b += kThreads) h[b] = 0;
     __syncthreads();
     const int64_t lo = imax64(S, c * kScan), hi = imin64(L - R, (c + 1) * kScan);
-    for (int64_t j = lo + tid; j < hi; j += kThreads)
-      atomicAdd(&h[float_key(imp_h[j]) >> (32 - kHistBits)], 1u);
+    for_each_pos(imp_h, lo, hi, [&](int64_t, float x, bool ok) {
+      if (ok) atomicAdd(&h[float_key(x) >> (32 - kHistBits)], 1u);
+    });
     __syncthreads();
     uint32_t* gh = w.hist + (size_t)hh * kBins;
     for (int b = tid; b < kBins; b += kThreads)
@@ -239,7 +284,7 @@ select_hist(Layers P, int64_t L, int B, int S, int R, int64_t n_chunks, Ws w) {
   if (tid == 0) w.state[hh] = st;
 }
 
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kThreads, 6)
 select_collect(Layers P, int64_t L, int S, int R, int64_t n_chunks, Ws w) {
   const int kv = blockIdx.y, tid = threadIdx.x, lane = tid & 31, nthr = blockDim.x;
   const int layer = blockIdx.z, hh = layer * gridDim.y + kv;
@@ -248,32 +293,44 @@ select_collect(Layers P, int64_t L, int S, int R, int64_t n_chunks, Ws w) {
   __shared__ int warp_buf[32], s_total, s_last;
   __shared__ uint32_t s_cnt[1024];
   __shared__ int s_gt[kPerScan];
+  // bucket members gathered per CTA, then appended to the head's list with
+  // one global reservation (a global atomic round trip per warp vote stalls)
+  constexpr int kListBuf = 2048;
+  __shared__ uint2 s_list[kListBuf];
+  __shared__ int s_nlist, s_gbase;
   const SelectState st0 = w.state[hh];
   const bool work = !st0.select_all && st0.bucket >= 0;
   uint2* list = w.list + (size_t)hh * L;
   if (work) {
     const uint32_t b = (uint32_t)st0.bucket;
     if (tid < kPerScan) s_gt[tid] = 0;
+    if (tid == 0) s_nlist = 0;
     __syncthreads();
     const int64_t lo = imax64(S, c * kScan), hi = imin64(L - R, (c + 1) * kScan);
-    for (int64_t j0 = lo; j0 < hi; j0 += nthr) {
-      const int64_t j = j0 + tid;
-      uint32_t key = 0, bk = 0;
-      if (j < hi) {
-        key = float_key(imp_h[j]);
-        bk = key >> (32 - kHistBits);
-      }
+    for_each_pos(imp_h, lo, hi, [&](int64_t j, float x, bool ok) {
+      const uint32_t key = ok ? float_key(x) : 0u, bk = key >> (32 - kHistBits);
       // keys above bucket b, counted per gather chunk
-      if (j < hi && bk > b) atomicAdd(&s_gt[(int)(j / kChunk - c * kPerScan)], 1);
-      const bool eq = j < hi && bk == b;
+      if (ok && bk > b) atomicAdd(&s_gt[(int)(j / kChunk - c * kPerScan)], 1);
+      const bool eq = ok && bk == b;
       const unsigned m = __ballot_sync(0xffffffffu, eq);
       if (m) {
-        uint32_t base = 0;
-        if (lane == __ffs(m) - 1) base = atomicAdd(&w.cnt[hh].n_list, (uint32_t)__popc(m));
+        int base = 0;
+        if (lane == __ffs(m) - 1) base = atomicAdd(&s_nlist, __popc(m));
         base = __shfl_sync(0xffffffffu, base, __ffs(m) - 1);
-        if (eq) list[base + __popc(m & ((1u << lane) - 1))] = make_uint2(key, (uint32_t)j);
+        const int slot = base + __popc(m & ((1u << lane) - 1));
+        if (eq) {
+          if (slot < kListBuf)
+            s_list[slot] = make_uint2(key, (uint32_t)j);
+          else   // buffer full: straight to the head's list
+            list[atomicAdd(&w.cnt[hh].n_list, 1u)] = make_uint2(key, (uint32_t)j);
+        }
       }
-    }
+    });
+    __syncthreads();
+    const int nloc = min(s_nlist, kListBuf);
+    if (tid == 0) s_gbase = nloc ? (int)atomicAdd(&w.cnt[hh].n_list, (uint32_t)nloc) : 0;
+    __syncthreads();
+    for (int e = tid; e < nloc; e += nthr) list[s_gbase + e] = s_list[e];
     __syncthreads();
     if (tid < kPerScan && c * kPerScan + tid < n_chunks)
       w.gt[(size_t)hh * n_chunks + c * kPerScan + tid] = s_gt[tid];
@@ -287,6 +344,11 @@ select_collect(Layers P, int64_t L, int S, int R, int64_t n_chunks, Ws w) {
   __shared__ int s_b, s_before;
   if (work) {
     const uint32_t n = *(volatile uint32_t*)&w.cnt[hh].n_list;
+    // the head's bucket members, staged in shared memory when they fit
+    const bool staged = n <= (uint32_t)kListBuf;
+    if (staged)
+      for (uint32_t e = tid; e < n; e += nthr) s_list[e] = __ldcg(&list[e]);
+    auto member = [&](uint32_t e) { return staged ? s_list[e] : __ldcg(&list[e]); };
     uint32_t pre = (uint32_t)st.bucket << (32 - kHistBits);
     uint32_t msk = 0xFFFFFFFFu << (32 - kHistBits);
     int need = st.need;
@@ -295,7 +357,7 @@ select_collect(Layers P, int64_t L, int S, int R, int64_t n_chunks, Ws w) {
       const int shift = 10 - 10 * lvl;
       __syncthreads();
       for (uint32_t e = tid; e < n; e += nthr) {
-        const uint32_t key = __ldcg(&list[e].x);
+        const uint32_t key = member(e).x;
         if ((key & msk) == pre) atomicAdd(&s_cnt[(key >> shift) & 1023u], 1u);
       }
       __syncthreads();
@@ -312,7 +374,7 @@ select_collect(Layers P, int64_t L, int S, int R, int64_t n_chunks, Ws w) {
       const int shift = 24 - 8 * lvl;
       __syncthreads();
       for (uint32_t e = tid; e < n; e += nthr) {
-        const uint2 v = __ldcg(&list[e]);
+        const uint2 v = member(e);
         if (v.x == tau && (v.y & pmsk) == ppre) atomicAdd(&s_cnt[(v.y >> shift) & 255u], 1u);
       }
       __syncthreads();
@@ -327,7 +389,7 @@ select_collect(Layers P, int64_t L, int S, int R, int64_t n_chunks, Ws w) {
     __syncthreads();
     // kept positions of bucket b per chunk (n_chunks <= 1024)
     for (uint32_t e = tid; e < n; e += nthr) {
-      const uint2 v = __ldcg(&list[e]);
+      const uint2 v = member(e);
       if (v.x > tau || (v.x == tau && (int32_t)v.y <= st.j_tie)) atomicAdd(&s_cnt[v.y / kChunk], 1u);
     }
   }
