@@ -257,9 +257,11 @@ VerifyPlan verify_plan(int T, int Hq, int Hkv, int d, int64_t L) {
   if (!use_simple_path()) {
     // tcgen05 path: row groups of up to 256 packed query rows
     p.tc = true;
+    p.pair = verify_pair_eligible(T, Hq, Hkv, d);
     p.n_rowblk = (p.M + 255) / 256;
     p.rows_per_cta = 256;
-    int n = tc_splits(Hkv, p.n_rowblk, L, kGb300Sms);
+    // a CTA pair per (split, head) when the pair kernel applies
+    int n = tc_splits(Hkv, p.pair ? 2 : p.n_rowblk, L, kGb300Sms);
     int64_t kps = (L + n - 1) / n;
     kps = (kps + 127) / 128 * 128;
     if (kps < 128) kps = 128;
@@ -297,7 +299,10 @@ int launch_verify(const void* q, const void* k, const void* v, int64_t L, int64_
   float* part_o = static_cast<float*>(ws);
   float* part_ml = reinterpret_cast<float*>(static_cast<char*>(ws) + p.part_o_bytes);
   int rc;
-  if (p.tc) {
+  if (p.pair) {
+    rc = launch_verify_pair(q, k, v, L, L_cap, parents, T, Hq, Hkv, n_imp, p.keys_per_split,
+                            p.n_split, part_o, part_ml, imp, status, st);
+  } else if (p.tc) {
     rc = launch_verify_tc(q, k, v, L, L_cap, parents, T, Hq, Hkv, d, n_imp, p.keys_per_split,
                           p.n_split, p.n_rowblk, part_o, part_ml, imp, status, st);
   } else {

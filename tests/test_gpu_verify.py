@@ -89,3 +89,21 @@ def test_value_beyond_fp16_range_is_reported():
     ts.ts_verify_attention(q, k, v, 300, pu.to_dev(inp["parents"]), status=status)
     torch.cuda.synchronize()
     assert int(status.item()) == 2
+
+
+@pytest.mark.parametrize("L", [1000, 4133, 102400])
+def test_cta_pair_kernel(L):
+    """The opt-in CTA-pair (tcgen05 .cta_group::2) kernel for M = T*G = 256,
+    d = 128 against the oracle, in a child process with TS_VERIFY_PAIR=1."""
+    import os
+    import subprocess
+    import sys
+    code = ("import sys; sys.path[:0] = ['tests', '.']\n"
+            "import test_gpu_verify as t, ts_synth as syn\n"
+            f"t._run(syn.WORKLOADS['llama3.1-8b'], L={L}, layer=1)\n"
+            "print('ok')\n")
+    env = dict(os.environ, TS_VERIFY_PAIR="1")
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    r = subprocess.run([sys.executable, "-c", code], cwd=root, env=env, capture_output=True,
+                       text=True, timeout=600)
+    assert r.returncode == 0 and "ok" in r.stdout, r.stdout[-2000:] + r.stderr[-2000:]
