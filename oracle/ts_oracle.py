@@ -325,3 +325,88 @@ def kv_commit(cache, L: int, path) -> np.ndarray:
     for t in range(1, len(path)):
         out[:, L + t] = cache[:, L + path[t]]
     return out
+
+
+# --------------------------------------------------------------------------
+# (NEXT-2) token reutilization: the 4-gram table and the draft-tree builder
+# --------------------------------------------------------------------------
+# §3.1 Overview: after verification the n-gram table is updated; §3.2 and
+# §3.4: frequent n-grams supply extra draft candidates, with random selection
+# among several valid ones; §B.2 Inference Details / Table 10: 4-grams, at
+# most k retrieved n-grams (k = 20, Table 11); §4.4.1 / §B.2: the extra heads'
+# candidates form the ternary full tree [1,3,3,3].
+#
+# Readings (the pages give no data structure): a 4-gram (a, b, c, d) is
+# stored under its first token a as the continuation (b, c, d); each key keeps
+# its distinct continuations, at most `cap` of them, oldest dropped first, a
+# repeated continuation neither duplicated nor moved.  Retrieval for the root
+# token returns every stored continuation (oldest first) when there are at
+# most k, else the k whose caller-supplied random keys are smallest (ties to
+# the lower slot), in that order.  The tree is the root, then the head tree in
+# breadth-first order (depth-d nodes carry head d's candidates), then each
+# retrieved continuation merged as a path from the root: an existing child
+# with the same token is followed, else a node is appended while fewer than
+# T_max nodes exist.
+
+
+def ngram_insert(table: dict, tokens, start: int, cap: int) -> dict:
+    """Insert the 4-grams ending at positions start .. len(tokens)-1 (those
+    with a full 4-gram, p >= 3) into `table` (key -> list of continuations,
+    oldest first), in position order.  Returns the table."""
+    toks = [int(t) for t in tokens]
+    for p in range(max(start, 3), len(toks)):
+        key = toks[p - 3]
+        cont = (toks[p - 2], toks[p - 1], toks[p])
+        lst = table.setdefault(key, [])
+        if cont in lst:
+            continue
+        lst.append(cont)
+        if len(lst) > cap:
+            lst.pop(0)
+    return table
+
+
+def ngram_retrieve(table: dict, root: int, k: int, rand_keys) -> list:
+    """Continuations stored under `root`: all of them (oldest first) if there
+    are at most k, else the k with the smallest (rand_keys[slot], slot), where
+    slot is the entry's position oldest-first, in increasing key order."""
+    lst = table.get(int(root), [])
+    if len(lst) <= k:
+        return list(lst)
+    order = sorted(range(len(lst)), key=lambda s: (int(rand_keys[s]), s))
+    return [lst[s] for s in order[:k]]
+
+
+def build_draft_tree(root_token: int, head_topk, chains, T_max: int):
+    """Draft tree of the root, the extra heads' ternary tree and the retrieved
+    chains, as (parents, tokens) int32 arrays of n <= T_max nodes with
+    parents[i] < i.  head_topk[d][c]: candidate c of head d+1."""
+    parents, tokens = [-1], [int(root_token)]
+    children = [[]]
+
+    def add(p, tok):
+        parents.append(p)
+        tokens.append(int(tok))
+        children.append([])
+        children[p].append(len(parents) - 1)
+        return len(parents) - 1
+
+    level = [0]
+    for d in range(len(head_topk)):
+        nxt = []
+        for p in level:
+            for tok in head_topk[d]:
+                if len(parents) >= T_max:
+                    break
+                nxt.append(add(p, tok))
+        level = nxt
+    for chain in chains:
+        cur = 0
+        for tok in chain:
+            hit = next((c for c in children[cur] if tokens[c] == int(tok)), None)
+            if hit is None:
+                if len(parents) >= T_max:
+                    break
+                hit = add(cur, tok)
+            cur = hit
+    return np.asarray(parents, dtype=np.int32), np.asarray(tokens, dtype=np.int32)
