@@ -552,6 +552,57 @@ def run_draft_case(w: syn.Workload, steps: int, warmup: int):
                       "frac_of_peak": round(gbs / peak, 3), "peak_source": peak_src}))
 
 
+def run_ngram_case(w: syn.Workload, steps: int, warmup: int):
+    """Token reutilization per decode step: insert the 4-grams of the newly
+    committed tokens (4 per step), then build the next draft tree (heads'
+    [1,3,3,3] tree + up to k=20 retrieved 4-gram continuations, T <= 64),
+    on a table prefilled from an 8K-token synthetic history.  Prints one
+    JSON line with the device time per step."""
+    import torch
+    import self_speculative_ultra_gb300 as ts
+    ts.build()
+    dev = torch.device("cuda", 0)
+    V, cap, k, T_max = w.V, 64, 20, min(64, w.T)
+    rng = np.random.default_rng(0)
+    # a Zipf-like token stream: frequent tokens repeat, as in text
+    n_hist = 8192 + 4 * (steps + warmup)
+    toks = np.minimum(rng.zipf(1.2, size=n_hist), V) - 1
+    hist = torch.from_numpy(toks.astype(np.int32)).to(dev)
+    table = ts.ngram_table(V, cap)
+    e_pre0, e_pre1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e_pre0.record()
+    ts.ts_ngram_insert(table, V, cap, hist, 0, n_tokens=8192)
+    e_pre1.record()
+    heads = torch.from_numpy(rng.integers(0, V, size=(3, 3)).astype(np.int32)).to(dev)
+    keys = [torch.from_numpy(syn.ngram_rand_keys(1, s_, cap)).to(dev) for s_ in range(steps + warmup)]
+    par = torch.empty(T_max, dtype=torch.int32, device=dev)
+    tok = torch.empty(T_max, dtype=torch.int32, device=dev)
+    nn = torch.empty(1, dtype=torch.int32, device=dev)
+    n = 8192
+
+    def step(i, n):
+        ts.ts_ngram_insert(table, V, cap, hist, n, n_tokens=n + 4)
+        ts.ts_ngram_build_tree(table, V, cap, hist[n + 3:n + 4], heads, k, keys[i], T_max,
+                               parents=par, tokens=tok, n_nodes=nn)
+        return n + 4
+    for i in range(warmup):
+        n = step(i, n)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for i in range(warmup, warmup + steps):
+        n = step(i, n)
+    e1.record()
+    torch.cuda.synchronize()
+    print(json.dumps({"metric": "token reutilization per decode step (us)",
+                      "value": round(e0.elapsed_time(e1) * 1e3 / steps, 2), "unit": "us",
+                      "higher_is_better": False, "steps": steps,
+                      "prefill_8192_tokens_us": round(e_pre0.elapsed_time(e_pre1) * 1e3, 1),
+                      "mean_tree_nodes": int(nn.item()),
+                      "config": {"workload": w.name, "V": V, "cap": cap, "k": k, "T_max": T_max,
+                                 "new_tokens_per_step": 4}}))
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -564,10 +615,14 @@ def main():
                     help="run a small fixed case for ncu captures and exit")
     ap.add_argument("--draft", action="store_true",
                     help="time draft-side attention over the compact cache and exit")
+    ap.add_argument("--ngram", action="store_true",
+                    help="time the token-reutilization step (4-gram table + tree) and exit")
     args = ap.parse_args()
     w = syn.WORKLOADS[args.workload]
     if args.draft:
         run_draft_case(w, args.steps, args.warmup)
+    elif args.ngram:
+        run_ngram_case(w, args.steps, args.warmup)
     elif args.profile:
         run_profile_case(args.profile, w)
     elif args.impl == "reference":

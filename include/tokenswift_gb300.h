@@ -212,6 +212,49 @@ int ts_kv_commit(void* k, void* v, int64_t L, int64_t L_cap, int Hkv, int d, int
                  const int32_t* path, const int32_t* n_path,
                  int32_t* status, void* stream);
 
+/* ------------------------------------------------------------------------
+ * (5) Token reutilization: the 4-gram table and the draft-tree builder.
+ *
+ * §3.1: after verification the n-gram table is updated; §3.2 / §3.4:
+ * frequent n-grams supply extra draft candidates, with random selection
+ * among several valid ones; §B.2 / Table 10: 4-grams, at most k retrieved
+ * (k = 20, Table 11); §4.4.1 / §B.2: the extra heads' candidates form the
+ * ternary full tree [1,3,3,3].
+ *
+ * Table: one int32 device buffer of ts_ngram_table_bytes(V, cap) bytes,
+ * zeroed by the caller before first use, owned by the caller.  The 4-gram
+ * (a, b, c, d) is stored under key a as the continuation (b, c, d); each key
+ * keeps at most cap distinct continuations (cap <= 64), the oldest
+ * overwritten first; a repeated continuation is neither duplicated nor moved.
+ * ------------------------------------------------------------------------ */
+size_t ts_ngram_table_bytes(int V, int cap);
+
+/* Insert the 4-grams ending at positions start .. n_tokens-1 of tokens
+ * [n_tokens] (device int32; positions below 3 have no 4-gram), in position
+ * order.  A token outside [0, V) skips its 4-grams and sets
+ * TS_ERR_INVALID_ARG in *status (device word, may be NULL). */
+int ts_ngram_insert(int32_t* table, int V, int cap, const int32_t* tokens, int n_tokens,
+                    int start, int32_t* status, void* stream);
+
+/* Draft tree for the next step.  root_token [1] (device; e.g. the bonus
+ * token written by ts_penalized_sample_accept), head_topk [n_heads][head_k]
+ * (device int32: candidate c of extra head d+1), rand_keys [cap] (device
+ * uint32, the random keys of the root's stored continuations, oldest slot
+ * first).  The root's continuations are selected: all of them (oldest
+ * first) when at most k are stored, else the k with the smallest
+ * (rand_keys[slot], slot) in that order.  The tree is the root, then the
+ * heads' tree in breadth-first order (depth-d nodes carry head d's
+ * candidates), then each selected continuation merged as a path from the
+ * root (an existing child with the same token is followed, else a node is
+ * appended while fewer than T_max exist).  Outputs (device int32): parents
+ * [T_max] (parents[0] = -1, parents[i] < i), tokens [T_max], n_nodes [1];
+ * entries past n_nodes are left untouched.  1 <= T_max <= 64,
+ * 0 <= n_heads * head_k, k <= cap. */
+int ts_ngram_build_tree(const int32_t* table, int V, int cap, const int32_t* root_token,
+                        const int32_t* head_topk, int n_heads, int head_k, int k,
+                        const uint32_t* rand_keys, int T_max, int32_t* parents,
+                        int32_t* tokens, int32_t* n_nodes, int32_t* status, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

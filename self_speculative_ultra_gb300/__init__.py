@@ -56,6 +56,12 @@ _SIGNATURES = {
                                           _c_void_p, _sz, _c_void_p, _c_void_p]),
     "ts_kv_commit": (_i32, [_c_void_p, _c_void_p, _i64, _i64, _i32, _i32, _i32, _c_void_p,
                             _c_void_p, _c_void_p, _c_void_p]),
+    "ts_ngram_table_bytes": (_sz, [_i32, _i32]),
+    "ts_ngram_insert": (_i32, [_c_void_p, _i32, _i32, _c_void_p, _i32, _i32, _c_void_p,
+                               _c_void_p]),
+    "ts_ngram_build_tree": (_i32, [_c_void_p, _i32, _i32, _c_void_p, _c_void_p, _i32, _i32, _i32,
+                                   _c_void_p, _i32, _c_void_p, _c_void_p, _c_void_p, _c_void_p,
+                                   _c_void_p]),
 }
 
 _LIB = None
@@ -288,3 +294,47 @@ def ts_kv_commit(k, v, L, T, path, n_path, status=None, stream=None):
     rc = lib().ts_kv_commit(_ptr(k), _ptr(v), L, L_cap, Hkv, d, T, _ptr(path), _ptr(n_path),
                             _ptr(status), _stream(stream))
     _check(rc)
+
+
+def ts_ngram_table_bytes(V, cap) -> int:
+    return lib().ts_ngram_table_bytes(V, cap)
+
+
+def ngram_table(V, cap, device="cuda"):
+    """A zeroed (empty) 4-gram table: int32 device buffer."""
+    nb = ts_ngram_table_bytes(V, cap)
+    if nb == 0:
+        raise ValueError(f"unsupported table shape V={V}, cap={cap}")
+    return torch.zeros(nb // 4, dtype=torch.int32, device=device)
+
+
+def ts_ngram_insert(table, V, cap, tokens, start, n_tokens=None, status=None, stream=None):
+    """Insert the 4-grams ending at positions start .. n_tokens-1 of tokens."""
+    _dev(table, torch.int32, "table")
+    _dev(tokens, torch.int32, "tokens")
+    n = tokens.numel() if n_tokens is None else n_tokens
+    _check(lib().ts_ngram_insert(_ptr(table), V, cap, _ptr(tokens), n, start, _ptr(status),
+                                 _stream(stream)))
+
+
+def ts_ngram_build_tree(table, V, cap, root_token, head_topk, k, rand_keys, T_max,
+                        parents=None, tokens=None, n_nodes=None, status=None, stream=None):
+    """Draft tree from the heads' candidates [n_heads, head_k] and the root's
+    retrieved continuations.  Returns (parents [T_max], tokens [T_max],
+    n_nodes [1]) device int32; entries past n_nodes are untouched."""
+    _dev(table, torch.int32, "table")
+    _dev(root_token, torch.int32, "root_token", (1,))
+    _dev(head_topk, torch.int32, "head_topk")
+    _dev(rand_keys, torch.int32, "rand_keys", (cap,))
+    n_heads, head_k = head_topk.shape
+    dev = table.device
+    if parents is None:
+        parents = torch.full((T_max,), -2, dtype=torch.int32, device=dev)
+    if tokens is None:
+        tokens = torch.full((T_max,), -2, dtype=torch.int32, device=dev)
+    if n_nodes is None:
+        n_nodes = torch.zeros(1, dtype=torch.int32, device=dev)
+    _check(lib().ts_ngram_build_tree(_ptr(table), V, cap, _ptr(root_token), _ptr(head_topk),
+                                     n_heads, head_k, k, _ptr(rand_keys), T_max, _ptr(parents),
+                                     _ptr(tokens), _ptr(n_nodes), _ptr(status), _stream(stream)))
+    return parents, tokens, n_nodes

@@ -227,4 +227,40 @@ int ts_kv_commit(void* k, void* v, int64_t L, int64_t L_cap, int Hkv, int d, int
                           static_cast<cudaStream_t>(stream));
 }
 
+size_t ts_ngram_table_bytes(int V, int cap) {
+  if (V < 1 || cap < 1 || cap > 64) return 0;
+  return ngram_table_bytes(V, cap);
+}
+
+int ts_ngram_insert(int32_t* table, int V, int cap, const int32_t* tokens, int n_tokens,
+                    int start, int32_t* status, void* stream) {
+  clear_error();
+  const char* F = "ts_ngram_insert";
+  if (V < 1) return fail(TS_ERR_INVALID_ARG, "%s: V must be >= 1", F);
+  if (cap < 1 || cap > 64) return fail(TS_ERR_UNSUPPORTED, "%s: cap=%d outside [1, 64]", F, cap);
+  if (n_tokens < 0 || start < 0) return fail(TS_ERR_INVALID_ARG, "%s: negative length", F);
+  if (!table || (n_tokens > 0 && !tokens)) return fail(TS_ERR_INVALID_ARG, "%s: NULL tensor", F);
+  return launch_ngram_insert(table, V, cap, tokens, n_tokens, start, status,
+                             static_cast<cudaStream_t>(stream));
+}
+
+int ts_ngram_build_tree(const int32_t* table, int V, int cap, const int32_t* root_token,
+                        const int32_t* head_topk, int n_heads, int head_k, int k,
+                        const uint32_t* rand_keys, int T_max, int32_t* parents,
+                        int32_t* tokens, int32_t* n_nodes, int32_t* status, void* stream) {
+  clear_error();
+  const char* F = "ts_ngram_build_tree";
+  if (V < 1) return fail(TS_ERR_INVALID_ARG, "%s: V must be >= 1", F);
+  if (cap < 1 || cap > 64) return fail(TS_ERR_UNSUPPORTED, "%s: cap=%d outside [1, 64]", F, cap);
+  if (T_max < 1 || T_max > 64) return fail(TS_ERR_UNSUPPORTED, "%s: T_max=%d outside [1, 64]", F, T_max);
+  if (n_heads < 0 || head_k < 0 || k < 0 || k > cap)
+    return fail(TS_ERR_INVALID_ARG, "%s: need n_heads, head_k >= 0 and 0 <= k <= cap", F);
+  if (!table || !root_token || !parents || !tokens || !n_nodes || (k > 0 && !rand_keys) ||
+      (n_heads * head_k > 0 && !head_topk))
+    return fail(TS_ERR_INVALID_ARG, "%s: NULL tensor", F);
+  return launch_ngram_tree(table, V, cap, root_token, head_topk, n_heads, head_k, k, rand_keys,
+                           T_max, parents, tokens, n_nodes, status,
+                           static_cast<cudaStream_t>(stream));
+}
+
 }  // extern "C"

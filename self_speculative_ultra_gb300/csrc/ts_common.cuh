@@ -166,6 +166,13 @@ int launch_sample_accept(const float* logits, const int32_t* tree_tokens, const 
                          float temperature, float top_p, float min_p, const float* uniforms,
                          int32_t* sampled, int32_t* path, int32_t* n_path, int32_t* bonus,
                          void* ws, int32_t* status, cudaStream_t st);
+size_t ngram_table_bytes(int V, int cap);
+int launch_ngram_insert(int32_t* table, int V, int cap, const int32_t* tokens, int n_tokens,
+                        int start, int32_t* status, cudaStream_t st);
+int launch_ngram_tree(const int32_t* table, int V, int cap, const int32_t* root_token,
+                      const int32_t* head_topk, int n_heads, int head_k, int k,
+                      const uint32_t* rand_keys, int T_max, int32_t* parents, int32_t* tokens,
+                      int32_t* n_nodes, int32_t* status, cudaStream_t st);
 int launch_kv_commit(void* k, void* v, int64_t L, int64_t L_cap, int Hkv, int d, int T,
                      const int32_t* path, const int32_t* n_path, int32_t* status,
                      cudaStream_t st);

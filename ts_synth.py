@@ -117,6 +117,17 @@ def node_uniforms(seed: int, step: int, T: int) -> np.ndarray:
     return out
 
 
+def ngram_rand_keys(seed: int, step: int, cap: int) -> np.ndarray:
+    """Random keys of the root's stored n-gram continuations for one step
+    (slot i, oldest first): top 31 bits of splitmix64(seed ^ step<<32 ^
+    (1<<31 | i)), as int32 (non-negative)."""
+    out = np.empty(cap, dtype=np.int32)
+    for i in range(cap):
+        z = splitmix64((seed ^ ((step << 32) & MASK64) ^ (0x80000000 | i)) & MASK64)
+        out[i] = np.int32(z >> 33)
+    return out
+
+
 # --------------------------------------------------------------------------
 # draft trees
 # --------------------------------------------------------------------------
