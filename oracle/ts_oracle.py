@@ -247,6 +247,65 @@ def sample_node(logits_row, prior, path_tokens, W, penalty, temperature, top_p,
     return sample_from_logits(xp, top_p, min_p, u, return_info)
 
 
+def eta_threshold(p, epsilon: float, alpha: float) -> float:
+    """η of η-sampling (§D.1: the pool is the tokens with probability at
+    least η; η is formed from the entropy, α and ε): η = min(ε, α·exp(-H)),
+    H = -sum p log p the entropy in nats of the (penalised, tempered)
+    distribution, the truncation-sampling form of the paper the pages cite
+    for it (§5.2)."""
+    p = np.asarray(p, dtype=np.float64)
+    nz = p[p > 0]
+    H = float(-(nz * np.log(nz)).sum())
+    return min(float(epsilon), float(alpha) * float(np.exp(-H)))
+
+
+def sample_from_logits_eta(x_pen, epsilon: float, alpha: float, u: float,
+                           return_info: bool = False):
+    """Draw one token with η-sampling: p = softmax(x') in fp64, ranks by
+    (p desc, id asc), the kept set K = {p >= η} (a rank prefix holding rank
+    0, as α <= 1 puts η at or below p_max), and the smallest rank in K whose
+    cumulative mass exceeds u * mass(K)."""
+    x = np.asarray(x_pen, dtype=np.float64)
+    V = x.shape[0]
+    e = np.exp(x - x.max())
+    p = e / e.sum()
+    eta = eta_threshold(p, epsilon, alpha)
+    order = np.lexsort((np.arange(V), -p))
+    ps = p[order]
+    keep = ps >= eta
+    keep[0] = True
+    n_keep = int(np.argmin(keep)) if not keep.all() else V
+    c = np.cumsum(ps[:n_keep])
+    target = u * c[-1]
+    r = int(np.argmax(c > target)) if (c > target).any() else n_keep - 1
+    tok = int(order[r])
+    if not return_info:
+        return tok
+    margins = [abs(ps[n_keep - 1] - eta), abs(ps[n_keep] - eta) if n_keep < V else np.inf,
+               abs(c[r] - target) / c[-1],
+               abs((c[r - 1] if r > 0 else 0.0) - target) / c[-1]]
+    return tok, dict(n_keep=n_keep, rank=r, margin=float(min(margins)), eta=eta)
+
+
+def sample_all_nodes_eta(logits, prior, parents, tree_tokens, W, penalty, temperature,
+                         epsilon, alpha, uniforms, return_info=False):
+    """Every node's η-sampling draw (window and penalty as sample_node)."""
+    paths = root_paths(parents)
+    out, infos = [], []
+    for i in range(len(parents)):
+        drafted = [int(tree_tokens[a]) for a in paths[i][1:]]
+        win = penalty_window(prior, drafted, W)
+        xp = penalised_logits(logits[i], win, penalty, temperature)
+        r = sample_from_logits_eta(xp, epsilon, alpha, float(uniforms[i]), return_info)
+        if return_info:
+            out.append(r[0])
+            infos.append(r[1])
+        else:
+            out.append(r)
+    out = np.asarray(out, dtype=np.int64)
+    return (out, infos) if return_info else out
+
+
 # --------------------------------------------------------------------------
 # (a7) exact-match tree acceptance
 # --------------------------------------------------------------------------

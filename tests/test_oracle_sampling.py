@@ -154,3 +154,36 @@ def test_top_p_boundary_is_strict():
     x = np.zeros(4, dtype=np.float32)
     assert orc.sample_from_logits(x, 0.5, 0.0, 0.99) == 1
     assert orc.sample_from_logits(x, 0.5000001, 0.0, 0.99) == 2
+
+
+# --------------------------------------------------------------------------
+# η-sampling (hand-worked: p = [1/2, 1/4, 1/8, 1/8])
+# H = 1/2 ln 2 + 1/4 ln 4 + 2 * 1/8 ln 8 = (1/2 + 1/2 + 3/4) ln 2 = 1.75 ln 2
+# exp(-H) = 2^-1.75 = 0.29730; with eps = 0.2, alpha = sqrt(0.2) = 0.44721:
+# alpha exp(-H) = 0.13296 -> eta = 0.13296: K = {0, 1} (1/8 < eta), mass 3/4
+# with eps = 0.1: alpha = sqrt(0.1), alpha exp(-H) = 0.09401 = eta -> K = all four
+# --------------------------------------------------------------------------
+def test_eta_hand_worked():
+    x = np.log(np.array([0.5, 0.25, 0.125, 0.125]))
+    p = np.array([0.5, 0.25, 0.125, 0.125])
+    assert orc.eta_threshold(p, 0.2, np.sqrt(0.2)) == pytest.approx(np.sqrt(0.2) * 2 ** -1.75, rel=1e-12)
+    assert orc.eta_threshold(p, 0.1, np.sqrt(0.1)) == pytest.approx(np.sqrt(0.1) * 2 ** -1.75, rel=1e-12)
+    assert orc.eta_threshold(p, 0.05, 1.0) == pytest.approx(0.05, rel=1e-12)
+    # K = {0, 1}: u*0.75 against cumulative 0.5, 0.75
+    assert orc.sample_from_logits_eta(x, 0.2, np.sqrt(0.2), 0.5) == 0    # target .375
+    assert orc.sample_from_logits_eta(x, 0.2, np.sqrt(0.2), 0.8) == 1    # target .6
+    # K = all: ties between ids 2 and 3 rank id 2 first; cumulative .5 .75 .875 1
+    assert orc.sample_from_logits_eta(x, 0.1, np.sqrt(0.1), 0.86) == 2   # target .86
+    assert orc.sample_from_logits_eta(x, 0.1, np.sqrt(0.1), 0.9) == 3    # target .9
+
+
+def test_eta_zero_epsilon_is_plain_categorical():
+    rng = np.random.default_rng(5)
+    x = rng.normal(0, 3, size=200)
+    p = np.exp(x - x.max())
+    p /= p.sum()
+    order = np.lexsort((np.arange(200), -p))
+    c = np.cumsum(p[order])
+    for u in rng.random(50):
+        ref = int(order[int(np.argmax(c > u))])
+        assert orc.sample_from_logits_eta(x, 0.0, 0.0, u) == ref
