@@ -199,6 +199,23 @@ int ts_penalized_sample_accept(const float* logits, const int32_t* tree_tokens,
                                void* workspace, size_t workspace_bytes,
                                int32_t* status, void* stream);
 
+/* eta-sampling variant (§D.1, Table 12): the same window, penalty,
+ * temperature, draw and acceptance, with the kept set {p >= eta},
+ * eta = min(eta_epsilon, eta_alpha * exp(-H)) and H the entropy (nats) of
+ * the penalised, tempered distribution, in place of top-p and min-p.
+ * eta_epsilon >= 0, 0 <= eta_alpha <= 1 (then eta <= p_max and the kept set
+ * is never empty).  Same workspace as ts_penalized_sample_accept. */
+int ts_penalized_sample_accept_eta(const float* logits, const int32_t* tree_tokens,
+                                   const int32_t* parents, int T,
+                                   const int32_t* prior, int n_prior, int W, int V,
+                                   float penalty, float temperature,
+                                   float eta_epsilon, float eta_alpha,
+                                   const float* uniforms,
+                                   int32_t* sampled, int32_t* path, int32_t* n_path,
+                                   int32_t* bonus,
+                                   void* workspace, size_t workspace_bytes,
+                                   int32_t* status, void* stream);
+
 /* ------------------------------------------------------------------------
  * (4) KV commit of the accepted path.
  *

@@ -54,6 +54,10 @@ _SIGNATURES = {
                                           _i32, _i32, _f32, _f32, _f32, _f32, _c_void_p,
                                           _c_void_p, _c_void_p, _c_void_p, _c_void_p,
                                           _c_void_p, _sz, _c_void_p, _c_void_p]),
+    "ts_penalized_sample_accept_eta": (_i32, [_c_void_p, _c_void_p, _c_void_p, _i32, _c_void_p,
+                                              _i32, _i32, _i32, _f32, _f32, _f32, _f32,
+                                              _c_void_p, _c_void_p, _c_void_p, _c_void_p,
+                                              _c_void_p, _c_void_p, _sz, _c_void_p, _c_void_p]),
     "ts_kv_commit": (_i32, [_c_void_p, _c_void_p, _i64, _i64, _i32, _i32, _i32, _c_void_p,
                             _c_void_p, _c_void_p, _c_void_p]),
     "ts_ngram_table_bytes": (_sz, [_i32, _i32]),
@@ -282,6 +286,34 @@ def ts_penalized_sample_accept(logits, tree_tokens, parents, prior, W, penalty, 
                                           top_p, min_p, _ptr(uniforms), _ptr(sampled), _ptr(path),
                                           _ptr(n_path), _ptr(bonus), _ptr(ws), nb, _ptr(status),
                                           _stream(stream))
+    _check(rc)
+    return sampled, path, n_path, bonus
+
+
+def ts_penalized_sample_accept_eta(logits, tree_tokens, parents, prior, W, penalty, temperature,
+                                   eta_epsilon, eta_alpha, uniforms, sampled=None, path=None,
+                                   n_path=None, bonus=None, workspace=None, status=None,
+                                   stream=None):
+    """Penalised eta-sampling draw at every node + exact-match acceptance.
+    Returns (sampled [T], path [T], n_path [1], bonus [1]) device int32."""
+    T, V = logits.shape
+    _dev(logits, torch.float32, "logits")
+    _dev(tree_tokens, torch.int32, "tree_tokens", (T,))
+    _dev(parents, torch.int32, "parents", (T,))
+    _dev(prior, torch.int32, "prior")
+    _dev(uniforms, torch.float32, "uniforms", (T,))
+    dev = logits.device
+    mk = lambda n: torch.empty(n, dtype=torch.int32, device=dev)  # noqa: E731
+    sampled = mk(T) if sampled is None else sampled
+    path = mk(T) if path is None else path
+    n_path = mk(1) if n_path is None else n_path
+    bonus = mk(1) if bonus is None else bonus
+    ws, nb = _workspace(ts_sample_workspace_bytes(T, V), dev, workspace)
+    rc = lib().ts_penalized_sample_accept_eta(_ptr(logits), _ptr(tree_tokens), _ptr(parents), T,
+                                              _ptr(prior), prior.numel(), W, V, penalty,
+                                              temperature, eta_epsilon, eta_alpha, _ptr(uniforms),
+                                              _ptr(sampled), _ptr(path), _ptr(n_path), _ptr(bonus),
+                                              _ptr(ws), nb, _ptr(status), _stream(stream))
     _check(rc)
     return sampled, path, n_path, bonus
 

@@ -71,7 +71,7 @@ struct PartStat {
   float m;     // slice maximum of x'
   float z;     // sum over the slice of exp(x' - m)
   int n;       // tokens with exp(x' - m) >= min_p (may exceed kCapPart)
-  int pad;
+  float s;     // eta mode: sum over the slice of exp(x' - m) (x' - m)
 };
 
 // workspace: [counters | PartStat [T][kParts] | candidates [T][kParts][kCapPart] | x' [T][V]]
@@ -258,7 +258,8 @@ __global__ void __launch_bounds__(kThreads, 2)
 sample_accept_kernel(const float* __restrict__ logits, const int32_t* __restrict__ tree_tokens,
                      const int32_t* __restrict__ parents, int T, const int32_t* __restrict__ prior,
                      int n_prior, int W, int V, float penalty, float temperature, float top_p,
-                     float min_p, const float* __restrict__ uniforms, int32_t* sampled,
+                     float min_p, int eta_mode, float eta_eps, float eta_alpha,
+                     const float* __restrict__ uniforms, int32_t* sampled,
                      int32_t* __restrict__ path, int32_t* __restrict__ n_path,
                      int32_t* __restrict__ bonus, SampleWs ws, int32_t* status) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
@@ -348,14 +349,16 @@ sample_accept_kernel(const float* __restrict__ logits, const int32_t* __restrict
   // Z_c and the slice's tokens with exp(x' - m_c) >= min_p (each thread
   // rereads the values it wrote)
   uint2* cand = ws.cand + ((size_t)i * kParts + part) * kCapPart;
-  float z = 0.f;
+  float z = 0.f, se = 0.f;
   auto consider = [&](bool valid, float x, int t) {
     float e = 0.f;
     if (valid) {
       e = expf(x - mc);
       z += e;
+      if (eta_mode) se += e * (x - mc);   // entropy term
     }
-    const bool in = valid && e >= min_p;
+    // eta's threshold is only known after the merge: the last CTA scans
+    const bool in = valid && !eta_mode && e >= min_p;
     const unsigned m = __ballot_sync(0xffffffffu, in);
     if (m) {
       int base = 0;
@@ -383,8 +386,9 @@ sample_accept_kernel(const float* __restrict__ logits, const int32_t* __restrict
     }
   }
   const float zc = block_sum(z, sm);
+  const float sc = eta_mode ? block_sum(se, sm) : 0.f;
   if (tid == 0) {
-    ws.stat[i * kParts + part] = PartStat{mc, zc, sm.ncand, 0};
+    ws.stat[i * kParts + part] = PartStat{mc, zc, sm.ncand, sc};
     __threadfence();
     sm.last = atomicAdd(&ws.node_ticket[i], 1) == kParts - 1;
   }
@@ -400,10 +404,23 @@ sample_accept_kernel(const float* __restrict__ logits, const int32_t* __restrict
     xmax = fmaxf(xmax, vst[p].m);
     overflow |= vst[p].n > kCapPart;
   }
-  float Z = 0.f;
+  float Z = 0.f, Sx = 0.f;
   for (int p = 0; p < kParts; ++p) {
     const float m = vst[p].m;
-    if (m != -INFINITY) Z += vst[p].z * expf(m - xmax);
+    if (m != -INFINITY) {
+      const float f = expf(m - xmax);
+      Z += vst[p].z * f;
+      Sx += (vst[p].s + vst[p].z * (m - xmax)) * f;
+    }
+  }
+  // min-p keeps e >= min_p (relative to the maximum).  eta keeps
+  // p >= eta = min(eps, alpha exp(-H)), i.e. e >= eta Z, with the entropy
+  // H = ln Z - sum e (x' - max) / Z; it needs the full scan below.
+  float thr = min_p;
+  if (eta_mode) {
+    const float H = logf(Z) - Sx / Z;
+    thr = fminf(eta_eps, eta_alpha * expf(-H)) * Z;
+    overflow = true;
   }
   if (tid == 0) {
     sm.ncand = 0;
@@ -444,18 +461,37 @@ sample_accept_kernel(const float* __restrict__ logits, const int32_t* __restrict
       }
     }
   } else {
-    for (int t = tid; t < V; t += kThreads) {
-      const float e = expf(xs[t] - xmax);
-      if (e >= min_p) {
+    // full scan of the node's x' (a slice overflowed, or eta); members
+    // are collected while they fit
+    for (int b0 = 0; b0 < V; b0 += kThreads) {
+      const int t = b0 + tid;
+      float x = 0.f, e = 0.f;
+      if (t < V) {
+        x = __ldcg(xs + t);
+        e = expf(x - xmax);
+      }
+      const bool in = t < V && e >= thr;
+      if (in) {
         zmin += e;
         ++nmin;
+      }
+      const unsigned m = __ballot_sync(0xffffffffu, in);
+      if (m) {
+        int base = 0;
+        if (lane == __ffs(m) - 1) base = atomicAdd(&sm.ncand, __popc(m));
+        base = __shfl_sync(0xffffffffu, base, __ffs(m) - 1);
+        const int slot = base + __popc(m & ((1u << lane) - 1));
+        if (in && slot < kCap) {
+          sm.ckey[slot] = float_key(x);
+          sm.cid[slot] = t;
+        }
       }
     }
   }
   float Zmin = block_sum(zmin, sm);
   int n_minp = block_sum_int(nmin, sm);
   int token;
-  if (!overflow && n_minp >= 1 && n_minp <= kCap) {
+  if (n_minp >= 1 && n_minp <= kCap) {
     // ---- fast path: the kept set is a rank prefix inside the min-p set.
     // Sort the candidates by (x' desc, id asc) (bitonic, padded to 2^k),
     // prefix-sum their e, cut at top-p, draw.
@@ -490,7 +526,7 @@ sample_accept_kernel(const float* __restrict__ logits, const int32_t* __restrict
     if (tid < 32) {
       // warp 0 walks the ranks: top-p cut (first inclusive mass >= top_p*Z),
       // then the draw (first inclusive mass > u * kept mass)
-      const float tp = top_p * Z;
+      const float tp = eta_mode ? INFINITY : top_p * Z;   // eta: no top-p cut
       float run = 0.f, zk = 0.f;
       int k_keep = 0;
       for (int b0 = 0; b0 < n_minp; b0 += 32) {
@@ -547,9 +583,13 @@ sample_accept_kernel(const float* __restrict__ logits, const int32_t* __restrict
       n_minp = 1;
       Zmin = 1.f;
     }
-    const Found f1 = radix_find(xs, V, xmax, kMassGE, top_p * Z, 0, sm);
-    const int k_keep = min(n_minp, f1.rank + 1);
-    const float ZK = (k_keep == f1.rank + 1) ? f1.cum_incl : Zmin;
+    int k_keep = n_minp;
+    float ZK = Zmin;
+    if (!eta_mode) {
+      const Found f1 = radix_find(xs, V, xmax, kMassGE, top_p * Z, 0, sm);
+      k_keep = min(n_minp, f1.rank + 1);
+      ZK = (k_keep == f1.rank + 1) ? f1.cum_incl : Zmin;
+    }
     const float u = uniforms[i];
     Found f2 = radix_find(xs, V, xmax, kMassGT, u * ZK, 0, sm);
     if (f2.rank >= k_keep) f2 = radix_find(xs, V, xmax, kRank, 0.f, k_keep - 1, sm);
@@ -643,9 +683,10 @@ size_t sample_ws_bytes(int T, int V) {
 
 int launch_sample_accept(const float* logits, const int32_t* tree_tokens, const int32_t* parents,
                          int T, const int32_t* prior, int n_prior, int W, int V, float penalty,
-                         float temperature, float top_p, float min_p, const float* uniforms,
-                         int32_t* sampled, int32_t* path, int32_t* n_path, int32_t* bonus,
-                         void* ws, int32_t* status, cudaStream_t st) {
+                         float temperature, float top_p, float min_p, int eta_mode, float eta_eps,
+                         float eta_alpha, const float* uniforms, int32_t* sampled, int32_t* path,
+                         int32_t* n_path, int32_t* bonus, void* ws, int32_t* status,
+                         cudaStream_t st) {
   const SampleWs w = carve_sample(ws, T);
   if (cudaMemsetAsync(ws, 0, kCounterBytes, st) != cudaSuccess)
     return launch_status("sample counter reset");
@@ -653,7 +694,7 @@ int launch_sample_accept(const float* logits, const int32_t* tree_tokens, const 
   cudaFuncSetAttribute(sample_accept_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   sample_accept_kernel<<<dim3(kParts, T), kThreads, smem, st>>>(
       logits, tree_tokens, parents, T, prior, n_prior, W, V, penalty, temperature, top_p, min_p,
-      uniforms, sampled, path, n_path, bonus, w, status);
+      eta_mode, eta_eps, eta_alpha, uniforms, sampled, path, n_path, bonus, w, status);
   return launch_status("sample_accept_kernel");
 }
 

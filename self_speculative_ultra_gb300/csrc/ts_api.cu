@@ -210,8 +210,37 @@ int ts_penalized_sample_accept(const float* logits, const int32_t* tree_tokens,
   int rc = check_ws(workspace, workspace_bytes, sample_ws_bytes(T, V), F);
   if (rc) return rc;
   return launch_sample_accept(logits, tree_tokens, parents, T, prior, n_prior, W, V, penalty,
-                              temperature, top_p, min_p, uniforms, sampled, path, n_path, bonus,
-                              workspace, status, static_cast<cudaStream_t>(stream));
+                              temperature, top_p, min_p, 0, 0.f, 0.f, uniforms, sampled, path,
+                              n_path, bonus, workspace, status, static_cast<cudaStream_t>(stream));
+}
+
+int ts_penalized_sample_accept_eta(const float* logits, const int32_t* tree_tokens,
+                                   const int32_t* parents, int T, const int32_t* prior,
+                                   int n_prior, int W, int V, float penalty, float temperature,
+                                   float eta_epsilon, float eta_alpha, const float* uniforms,
+                                   int32_t* sampled, int32_t* path, int32_t* n_path,
+                                   int32_t* bonus, void* workspace, size_t workspace_bytes,
+                                   int32_t* status, void* stream) {
+  clear_error();
+  const char* F = "ts_penalized_sample_accept_eta";
+  if (T < 1) return fail(TS_ERR_INVALID_ARG, "%s: T=%d", F, T);
+  if (T > 64) return fail(TS_ERR_UNSUPPORTED, "%s: T=%d > 64", F, T);
+  if (V < 1) return fail(TS_ERR_INVALID_ARG, "%s: V=%d", F, V);
+  if (V > 262144) return fail(TS_ERR_UNSUPPORTED, "%s: V=%d > 262144", F, V);
+  if (n_prior < 0 || W < 0) return fail(TS_ERR_INVALID_ARG, "%s: n_prior, W must be >= 0", F);
+  if (!(penalty > 0.f) || !(temperature > 0.f))
+    return fail(TS_ERR_INVALID_ARG, "%s: penalty and temperature must be > 0", F);
+  if (!(eta_epsilon >= 0.f) || !(eta_alpha >= 0.f) || !(eta_alpha <= 1.f))
+    return fail(TS_ERR_INVALID_ARG, "%s: need eta_epsilon >= 0 and 0 <= eta_alpha <= 1", F);
+  if (!logits || !tree_tokens || !parents || !uniforms || !sampled || !path || !n_path || !bonus ||
+      (n_prior > 0 && !prior))
+    return fail(TS_ERR_INVALID_ARG, "%s: NULL tensor", F);
+  int rc = check_ws(workspace, workspace_bytes, sample_ws_bytes(T, V), F);
+  if (rc) return rc;
+  return launch_sample_accept(logits, tree_tokens, parents, T, prior, n_prior, W, V, penalty,
+                              temperature, 1.f, 0.f, 1, eta_epsilon, eta_alpha, uniforms, sampled,
+                              path, n_path, bonus, workspace, status,
+                              static_cast<cudaStream_t>(stream));
 }
 
 int ts_kv_commit(void* k, void* v, int64_t L, int64_t L_cap, int Hkv, int d, int T,

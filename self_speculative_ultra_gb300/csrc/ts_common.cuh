@@ -163,9 +163,10 @@ int select_scratch(void** out);   // device address of that scratch (current dev
 size_t sample_ws_bytes(int T, int V);
 int launch_sample_accept(const float* logits, const int32_t* tree_tokens, const int32_t* parents,
                          int T, const int32_t* prior, int n_prior, int W, int V, float penalty,
-                         float temperature, float top_p, float min_p, const float* uniforms,
-                         int32_t* sampled, int32_t* path, int32_t* n_path, int32_t* bonus,
-                         void* ws, int32_t* status, cudaStream_t st);
+                         float temperature, float top_p, float min_p, int eta_mode, float eta_eps,
+                         float eta_alpha, const float* uniforms, int32_t* sampled, int32_t* path,
+                         int32_t* n_path, int32_t* bonus, void* ws, int32_t* status,
+                         cudaStream_t st);
 size_t ngram_table_bytes(int V, int cap);
 int launch_ngram_insert(int32_t* table, int V, int cap, const int32_t* tokens, int n_tokens,
                         int start, int32_t* status, cudaStream_t st);
