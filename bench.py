@@ -53,6 +53,12 @@ def verify_bytes(w: syn.Workload) -> int:
     return kv + q + out + imp
 
 
+def verify_flops(w: syn.Workload) -> int:
+    """Contraction work of one call: S = Q K^T and O += P V, 2 flops per
+    multiply-add, over the L+T keys of every KV head for its T*G query rows."""
+    return 4 * w.T * (w.Hq // w.Hkv) * w.d * (w.L + w.T) * w.Hkv
+
+
 def select_bytes(w: syn.Workload) -> int:
     imp = 4 * w.L * w.Hkv                            # importance read
     gather = 2 * 2 * 2 * w.N * w.Hkv * w.d           # K,V rows read + written
@@ -82,6 +88,18 @@ def load_peaks():
             d = json.load(f)
         return float(d["hbm_gbs"]), "measured"
     return 6800.0, "fallback"
+
+
+def load_tensor_peak():
+    """Dense bf16 TFLOP/s for a kernel inside a long step (the sustained
+    figure), measured when available."""
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        if "bf16_tflops_sustained" in d:
+            return float(d["bf16_tflops_sustained"]), "measured (sustained)"
+    return 1700.0, "fallback (sustained)"
 
 
 def verify_source_sha1() -> str:
@@ -366,6 +384,8 @@ def run_gpu(args, w: syn.Workload):
         vb = verify_bytes(w)
         v_avg_ms = statistics.mean(ver_ms)
         achieved = vb / (v_avg_ms * 1e-3) / 1e9
+        tf_peak, tf_kind = load_tensor_peak()
+        tf_achieved = verify_flops(w) / (v_avg_ms * 1e-3) / 1e12
         traffic = profiled_traffic(w.name)
         line = {
             "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
@@ -385,7 +405,10 @@ def run_gpu(args, w: syn.Workload):
                          "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                          "frac": round(achieved / peak, 4), "traffic": traffic,
                          "peak_source": peak_kind,
-                         "bytes_per_call": vb, "avg_call_ms": round(v_avg_ms, 4)},
+                         "bytes_per_call": vb, "avg_call_ms": round(v_avg_ms, 4),
+                         "tensor": {"achieved": round(tf_achieved, 1), "peak": tf_peak,
+                                    "unit": "TFLOP/s", "frac": round(tf_achieved / tf_peak, 4),
+                                    "flops_per_call": verify_flops(w), "peak_source": tf_kind}},
             "e2e": {"value": round(world * sb / (e2e_ms * 1e-3) / 1e9, 2), "unit": UNIT,
                     "h2d_bytes_per_step": st.h2d_bytes(), "d2h_bytes_per_step": st.d2h_bytes(),
                     "ms_per_step": round(e2e_ms, 4)},
