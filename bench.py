@@ -239,46 +239,64 @@ class Step:
         self.ws_s = torch.empty(max(ts.ts_select_batched_workspace_bytes(w.layers, Hkv, L), 256), **u8)
         self.sel_table = ts.layer_pointer_table(self.imp, self.k, self.v, self.idx, self.kd, self.vd)
         self.ws_p = torch.empty(max(ts.ts_sample_workspace_bytes(T, w.V), 256), **u8)
-        # pinned host copies of the per-step inputs and results (end-to-end leg)
-        self.h_q = [torch.empty_like(x, device="cpu").pin_memory() for x in self.q]
+        # end-to-end leg: the per-step inputs live in one pinned host buffer
+        # (uploaded with a single copy) and are unpacked on the device by a
+        # multi-tensor copy into their places (queries, the tree's K/V rows
+        # inside every layer's cache, logits, tree, window, uniforms)
         tree_rows = lambda x: x[:, L:L + T]  # noqa: E731
-        self.h_ktree = [torch.empty_like(tree_rows(x), device="cpu").pin_memory() for x in self.k]
-        self.h_vtree = [torch.empty_like(tree_rows(x), device="cpu").pin_memory() for x in self.v]
-        for a, b in zip(self.h_q, self.q):
-            a.copy_(b)
-        for a, b in zip(self.h_ktree, self.k):
-            a.copy_(tree_rows(b))
-        for a, b in zip(self.h_vtree, self.v):
-            a.copy_(tree_rows(b))
-        self.h_logits = self.logits.cpu().pin_memory()
-        self.h_small = torch.cat([self.parents, self.tokens, self.prior,
-                                  self.uniforms.view(torch.int32)]).cpu().pin_memory()
+        self.e2e_dst = (list(self.q) + [tree_rows(x) for x in self.k] +
+                        [tree_rows(x) for x in self.v] +
+                        [self.logits, self.parents, self.tokens, self.prior, self.uniforms])
+        offs, off = [], 0
+        for t in self.e2e_dst:
+            offs.append(off)
+            off += (t.numel() * t.element_size() + 255) // 256 * 256
+        self.h_stage = torch.empty(off, dtype=torch.uint8).pin_memory()
+        # two device staging buffers: step s+1's upload (on a copy stream)
+        # overlaps step s's kernels
+        self.d_stage = [torch.empty(off, dtype=torch.uint8, device=dev) for _ in range(2)]
+        self.copy_stream = torch.cuda.Stream(device=dev)
+        self.staged = [torch.cuda.Event() for _ in range(2)]
+        self.unpacked = [torch.cuda.Event() for _ in range(2)]
+
+        def view(buf, o, t):
+            n = t.numel() * t.element_size()
+            return buf[o:o + n].view(t.dtype).view(t.shape)
+        self.e2e_src = [[view(b, o, t) for o, t in zip(offs, self.e2e_dst)] for b in self.d_stage]
+        for o, t in zip(offs, self.e2e_dst):
+            view(self.h_stage, o, t).copy_(t.cpu())
         self.h_out = torch.empty(T + 2, dtype=torch.int32).pin_memory()
         self.v_events = None
         torch.cuda.synchronize()
 
     def h2d_bytes(self) -> int:
-        n = sum(x.numel() * x.element_size() for x in self.h_q)
-        n += sum(x.numel() * x.element_size() for x in self.h_ktree + self.h_vtree)
-        n += self.h_logits.numel() * 4 + self.h_small.numel() * 4
-        return n
+        return sum(t.numel() * t.element_size() for t in self.e2e_dst)
 
     def d2h_bytes(self) -> int:
         return self.h_out.numel() * 4
 
-    def upload_inputs(self):
-        w, L, T = self.w, self.L, self.w.T
-        for layer in range(w.layers):
-            self.q[layer].copy_(self.h_q[layer], non_blocking=True)
-            self.k[layer][:, L:L + T].copy_(self.h_ktree[layer], non_blocking=True)
-            self.v[layer][:, L:L + T].copy_(self.h_vtree[layer], non_blocking=True)
-        self.logits.copy_(self.h_logits, non_blocking=True)
-        small = self.h_small.to(self.dev, non_blocking=True)
-        n = T
-        self.parents.copy_(small[:n])
-        self.tokens.copy_(small[n:2 * n])
-        self.prior.copy_(small[2 * n:2 * n + self.prior.numel()])
-        self.uniforms.copy_(small[2 * n + self.prior.numel():].view(self.torch.float32))
+    def stage_inputs(self, s: int, after=None):
+        """Upload step s's inputs from pinned host memory into staging
+        buffer s % 2 on the copy stream (after `after`, and after that
+        buffer's previous unpack)."""
+        torch, b = self.torch, s % 2
+        with torch.cuda.stream(self.copy_stream):
+            if after is not None:
+                self.copy_stream.wait_event(after)
+            if s >= 2:
+                self.copy_stream.wait_event(self.unpacked[b])
+            self.d_stage[b].copy_(self.h_stage, non_blocking=True)
+            self.staged[b].record(self.copy_stream)
+
+    def unpack_inputs(self, s: int):
+        b = s % 2
+        self.torch.cuda.current_stream().wait_event(self.staged[b])
+        self.torch._foreach_copy_(self.e2e_dst, self.e2e_src[b])
+        self.unpacked[b].record()
+
+    def upload_inputs(self, s: int = 0):
+        self.stage_inputs(s)
+        self.unpack_inputs(s)
 
     def download_result(self):
         self.h_out[:self.w.T].copy_(self.path, non_blocking=True)
@@ -357,16 +375,19 @@ def run_gpu(args, w: syn.Workload):
     ms_step = float(ms.item()) / args.steps
 
     # end-to-end leg: pinned host inputs in, result out, every step
-    for _ in range(2):
-        st.upload_inputs()
+    for i in range(2):
+        st.upload_inputs(i)
         st.step()
         st.download_result()
     barrier()
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     e0.record()
-    for _ in range(args.steps):
-        st.upload_inputs()
+    st.stage_inputs(0, after=e0)
+    for s_ in range(args.steps):
+        if s_ + 1 < args.steps:
+            st.stage_inputs(s_ + 1)
+        st.unpack_inputs(s_)
         st.step()
         st.download_result()
     e1.record()
