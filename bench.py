@@ -17,6 +17,7 @@ Run:  python bench.py [--gpus N --steps K --warmup W --workload NAME]
 from __future__ import annotations
 
 import argparse
+import ctypes
 import hashlib
 import json
 import os
@@ -647,6 +648,133 @@ def run_ngram_case(w: syn.Workload, steps: int, warmup: int):
                                  "new_tokens_per_step": 4}}))
 
 
+def run_loop_case(w: syn.Workload, until: int, L0: int = 2048):
+    """A whole generation loop on synthetic tokens: from a prefix of L0
+    cached tokens until the cache holds `until` tokens.  Every step appends
+    the draft tree's fresh N(0,1) K/V rows to every layer's cache, verifies
+    every layer (importance on), refreshes every layer's partial cache,
+    draws fresh N(0, 3^2) logits in which each node's first child's token is
+    raised by 30 with probability 0.7 (about 2.5 committed tokens per step),
+    samples and accepts, commits the accepted rows in every layer and
+    advances by the accepted length, which is read back to the host each
+    step.  Prints one JSON line."""
+    import torch
+    import self_speculative_ultra_gb300 as ts
+    ts.build()
+    lib, P = ts.lib(), ts._ptr
+    dev = torch.device("cuda", 0)
+    g = torch.Generator(device=dev)
+    g.manual_seed(w.seed)
+    T, Hq, Hkv, d, V, nl = w.T, w.Hq, w.Hkv, w.d, w.V, w.layers
+    L_cap = until + T
+    bf = dict(dtype=torch.bfloat16, device=dev)
+    i32 = dict(dtype=torch.int32, device=dev)
+    ks = [torch.empty((Hkv, L_cap, d), **bf).normal_(generator=g) for _ in range(nl)]
+    vs = [torch.empty((Hkv, L_cap, d), **bf).normal_(generator=g) for _ in range(nl)]
+    qs = [torch.empty((T, Hq, d), **bf).normal_(generator=g) for _ in range(nl)]
+    # fresh tree K/V per step: rows drawn from a pool of 4 variants per layer
+    pool = [[torch.empty((Hkv, T, d), **bf).normal_(generator=g) for _ in range(2 * nl)]
+            for _ in range(4)]
+    parents_np, tokens_np = syn.make_tree(w, np.random.default_rng(w.seed))
+    parents = torch.from_numpy(np.asarray(parents_np, np.int32)).to(dev)
+    tokens = torch.from_numpy(np.asarray(tokens_np, np.int32)).to(dev)
+    first_child = np.full(T, -1, dtype=np.int64)
+    for i in range(T - 1, 0, -1):
+        first_child[parents_np[i]] = i
+    has_fc = torch.from_numpy(first_child >= 0).to(dev)
+    fc_tok = torch.from_numpy(np.asarray(tokens_np, np.int64)[np.maximum(first_child, 0)]).to(dev)
+    rows = torch.arange(T, device=dev)
+    prior_np = np.random.default_rng(w.seed + 1).integers(0, V, size=w.W).astype(np.int32)
+    prior_np[-1] = tokens_np[0]
+    prior = torch.from_numpy(prior_np).to(dev)
+    logits = torch.empty((T, V), dtype=torch.float32, device=dev)
+    uniforms = torch.empty(T, dtype=torch.float32, device=dev)
+    o = [torch.empty((T, Hq, d), dtype=torch.float32, device=dev) for _ in range(nl)]
+    lse = [torch.empty((T, Hq), dtype=torch.float32, device=dev) for _ in range(nl)]
+    imp = [torch.empty(Hkv * until, dtype=torch.float32, device=dev) for _ in range(nl)]
+    N = w.S + w.B + w.R
+    idx = [torch.empty((Hkv, N), **i32) for _ in range(nl)]
+    kd = [torch.empty((Hkv, N, d), **bf) for _ in range(nl)]
+    vd = [torch.empty((Hkv, N, d), **bf) for _ in range(nl)]
+    u8 = dict(dtype=torch.uint8, device=dev)
+    ws_v = torch.empty(max(ts.ts_verify_workspace_bytes(T, Hq, Hkv, d, Lx)
+                           for Lx in range(L0, until + 256, 256)), **u8)
+    ws_s = torch.empty(max(ts.ts_select_batched_workspace_bytes(nl, Hkv, Lx)
+                           for Lx in range(L0, until + 256, 256)), **u8)
+    ws_p = torch.empty(ts.ts_sample_workspace_bytes(T, V), **u8)
+    sampled, path, n_path, bonus = (torch.empty(T, **i32), torch.empty(T, **i32),
+                                    torch.empty(1, **i32), torch.empty(1, **i32))
+    status = torch.zeros(1, **i32)
+    n_path_h = torch.empty(1, dtype=torch.int32).pin_memory()
+    table = ts.layer_pointer_table(imp, ks, vs, idx, kd, vd)
+    trow = [ctypes.c_void_p(table[r].data_ptr()) for r in range(6)]
+    stream = ts._stream(None)
+    n_out = ctypes.c_int64(0)
+    lay = [(P(qs[i]), P(ks[i]), P(vs[i]), P(o[i]), P(lse[i]), P(imp[i])) for i in range(nl)]
+    nb_v, nb_s, nb_p = ws_v.numel(), ws_s.numel(), ws_p.numel()
+    torch.cuda.synchronize()
+    launches = [0]
+
+    def step(s_, L):
+        torch._foreach_copy_([x[:, L:L + T] for x in ks] + [x[:, L:L + T] for x in vs],
+                             pool[s_ % 4])
+        torch.randn((T, V), generator=g, device=dev, out=logits)
+        logits.mul_(3.0)
+        plant = (torch.rand(T, generator=g, device=dev) < 0.7) & has_fc
+        logits.index_put_((rows, fc_tok), plant.float() * 30.0, accumulate=True)
+        torch.rand(T, generator=g, device=dev, out=uniforms)
+        for (q_, k_, v_, o_, lse_, imp_) in lay:
+            ts._check(lib.ts_verify_attention(q_, k_, v_, L, L_cap, P(parents), T, Hq, Hkv, d,
+                                              w.n_imp, o_, lse_, imp_, P(ws_v), nb_v, P(status),
+                                              stream))
+        ts._check(lib.ts_partial_kv_select_gather_batched(
+            nl, trow[0], trow[1], trow[2], L, L_cap, Hkv, d, w.B, w.S, w.R, trow[3], trow[4],
+            trow[5], ctypes.byref(n_out), P(ws_s), nb_s, P(status), stream))
+        ts._check(lib.ts_penalized_sample_accept(
+            P(logits), P(tokens), P(parents), T, P(prior), prior.numel(), w.W, V, w.penalty,
+            w.temperature, w.top_p, w.min_p, P(uniforms), P(sampled), P(path), P(n_path),
+            P(bonus), P(ws_p), nb_p, P(status), stream))
+        for (q_, k_, v_, o_, lse_, imp_) in lay:
+            ts._check(lib.ts_kv_commit(k_, v_, L, L_cap, Hkv, d, T, P(path), P(n_path), P(status),
+                                       stream))
+        n_path_h.copy_(n_path, non_blocking=True)
+        torch.cuda.current_stream().synchronize()
+        return int(n_path_h.item())
+
+    for s_ in range(3):                     # warm-up at the prefix length
+        step(s_, L0)
+    torch.cuda.synchronize()
+    L, steps, committed, hist = L0, 0, 0, [0] * (T + 1)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0 = time.perf_counter()
+    e0.record()
+    while L < until:
+        n = step(steps, L)
+        if not 1 <= n <= T:
+            raise RuntimeError(f"accepted length {n} at L={L} (device status "
+                               f"{int(status.item())})")
+        hist[n] += 1
+        L += n
+        committed += n
+        steps += 1
+    e1.record()
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - t0
+    print(json.dumps({
+        "metric": "generation loop wall time", "value": round(wall, 3), "unit": "s",
+        "higher_is_better": False, "steps": steps, "tokens_committed": committed,
+        "tokens_per_s": round(committed / wall, 1),
+        "mean_accepted_per_step": round(committed / max(steps, 1), 4),
+        "accepted_length_histogram": {str(i): c for i, c in enumerate(hist) if c},
+        "ms_per_step": round(1e3 * wall / max(steps, 1), 4),
+        "device_status": int(status.item()), "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": w.name, "layers": nl, "Hq": Hq, "Hkv": Hkv, "d": d,
+                   "prefix_L0": L0, "until_L": until, "tree_nodes": T, "B": w.B, "S": w.S,
+                   "R": w.R, "V": V, "acceptance": "first child's token +30 with p=0.7",
+                   "per_step": f"{nl} verify + 1 batched select/gather over {nl} layers + "
+                               f"1 sample/accept + {nl} commits"}}))
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -659,11 +787,16 @@ def main():
                     help="run a small fixed case for ncu captures and exit")
     ap.add_argument("--draft", action="store_true",
                     help="time draft-side attention over the compact cache and exit")
+    ap.add_argument("--loop", type=int, default=0, metavar="L_END",
+                    help="time a whole generation loop from a 2048-token prefix to L_END "
+                         "cached tokens and exit")
     ap.add_argument("--ngram", action="store_true",
                     help="time the token-reutilization step (4-gram table + tree) and exit")
     args = ap.parse_args()
     w = syn.WORKLOADS[args.workload]
-    if args.draft:
+    if args.loop:
+        run_loop_case(w, args.loop)
+    elif args.draft:
         run_draft_case(w, args.steps, args.warmup)
     elif args.ngram:
         run_ngram_case(w, args.steps, args.warmup)

@@ -131,6 +131,41 @@ def verify_attention(q, k, v, L: int, parents, n_imp: int = 0):
     return O, LSE, imp
 
 
+def importance_softmax(q, k, L: int, lse, n_imp: int = 0):
+    """(NEXT-4) Softmax-weighted importance: the attention probability each
+    committed cache position receives from the importance queries of its
+    KV head's group.
+
+    §3.3 Dynamic KV Cache Management ranks cache pairs by query-key scores,
+    the queries of a GQA group partitioned and their scores aggregated.  This
+    variant aggregates the normalised attention weights instead of the raw
+    scores (reading 17 of the design notes):
+
+        imp[kv, j] = sum over the last n_imp nodes i and the heads h of
+                     group kv of exp(q[i,h] . k[kv,j] / sqrt(d) - lse[i,h]),
+                     j in [0, L),
+
+    lse [T, Hq] being each row's log-sum-exp over everything the row attends
+    to (the committed cache and its root path of the tree), as returned by
+    verify_attention.  q [T,Hq,d], k [Hkv, >= L, d] float64.  Returns
+    imp [Hkv, L] float64."""
+    q = np.asarray(q, dtype=np.float64)
+    k = np.asarray(k, dtype=np.float64)
+    lse = np.asarray(lse, dtype=np.float64)
+    T, Hq, d = q.shape
+    Hkv = k.shape[0]
+    G = Hq // Hkv
+    n_imp = T if n_imp <= 0 else n_imp
+    scale = 1.0 / np.sqrt(d)
+    imp = np.zeros((Hkv, L))
+    for h in range(Hq):
+        kv = h // G
+        for i in range(T - n_imp, T):
+            s = (k[kv, :L, :] @ q[i, h, :]) * scale
+            imp[kv] += np.exp(s - lse[i, h])
+    return imp
+
+
 # --------------------------------------------------------------------------
 # (a3, a4) partial KV cache: top-B selection + gather
 # --------------------------------------------------------------------------

@@ -146,3 +146,65 @@ def test_bf16_decode_is_exact():
     back = orc.bf16_to_f64(bits)
     assert back[0] == 1.0 and back[1] == -2.5 and back[2] == 3.140625 and back[3] == 65280.0
     assert abs(back[4] - 1e-3) / 1e-3 < 2 ** -8
+
+
+# ---- softmax-weighted importance (the variant of the importance score)
+@pytest.mark.parametrize("seed,n_imp", [(0, 0), (1, 3), (2, 1)])
+def test_softmax_importance_equals_library_attention_weights(seed, n_imp):
+    """The importance is the column sum, over the group's heads and the last
+    n_imp nodes, of the masked attention weights that torch's softmax gives
+    (mask from the independent transitive closure)."""
+    q, k, v, L, parents = _case(seed)
+    T, Hq, d = q.shape
+    Hkv = k.shape[0]
+    G = Hq // Hkv
+    _, LSE, _ = orc.verify_attention(q, k, v, L, parents)
+    imp = orc.importance_softmax(q, k, L, LSE, n_imp=n_imp)
+    mask = np.ones((T, L + T), dtype=bool)
+    mask[:, L:] = _reach(parents)
+    kt = torch.from_numpy(k[:, :L + T]).repeat_interleave(G, dim=0)   # [Hq, L+T, d]
+    qt = torch.from_numpy(q).permute(1, 0, 2)                           # [Hq, T, d]
+    scores = (qt @ kt.transpose(1, 2)) / np.sqrt(d)
+    w = torch.softmax(scores.masked_fill(~torch.from_numpy(mask), float("-inf")), dim=-1)
+    rows = T if n_imp == 0 else n_imp
+    ref = w[:, T - rows:, :L].sum(dim=1).reshape(Hkv, G, L).sum(dim=1).numpy()
+    np.testing.assert_allclose(imp, ref, rtol=1e-12, atol=1e-15)
+
+
+def test_softmax_importance_uniform_keys_closed_form():
+    """All keys equal: every row spreads its weight evenly over the L cache
+    rows and its root path, so imp[kv, j] = G * sum_i 1 / (L + depth_i + 1)
+    over the importance nodes, whatever the queries."""
+    rng = np.random.default_rng(5)
+    T, Hq, Hkv, d, L = 9, 6, 3, 8, 30
+    parents, _ = syn.random_tree(rng, T, 50)
+    q = rng.standard_normal((T, Hq, d))
+    k = np.broadcast_to(rng.standard_normal(d), (Hkv, L + T, d)).copy()
+    v = rng.standard_normal((Hkv, L + T, d))
+    _, LSE, _ = orc.verify_attention(q, k, v, L, parents)
+    path_len = _reach(parents).sum(axis=1)            # ancestors-or-self of each node
+    for n_imp in (1, 4, T):
+        imp = orc.importance_softmax(q, k, L, LSE, n_imp=n_imp)
+        want = (Hq // Hkv) * sum(1.0 / (L + path_len[i]) for i in range(T - n_imp, T))
+        np.testing.assert_allclose(imp, np.full((Hkv, L), want), rtol=1e-12)
+
+
+def test_softmax_importance_planted_key_takes_the_group_mass():
+    """Queries of group 1's last n_imp nodes aligned with key j* of KV head 1
+    put almost all their weight there: imp[1, j*] ~ n_imp * G; head 0 and
+    the earlier nodes do not see it."""
+    rng = np.random.default_rng(9)
+    T, Hq, Hkv, d, L, n_imp, js = 6, 4, 2, 16, 50, 2, 17
+    parents = np.array([-1, 0, 1, 1, 2, 4], dtype=np.int32)
+    q = rng.standard_normal((T, Hq, d)) * 0.1
+    k = rng.standard_normal((Hkv, L + T, d)) * 0.1
+    u = rng.standard_normal(d)
+    u /= np.linalg.norm(u)
+    k[1, js] = 12.0 * u
+    q[T - n_imp:, 2:4, :] += 12.0 * u                 # heads 2, 3 = group 1
+    v = rng.standard_normal((Hkv, L + T, d))
+    _, LSE, _ = orc.verify_attention(q, k, v, L, parents)
+    imp = orc.importance_softmax(q, k, L, LSE, n_imp=n_imp)
+    G = Hq // Hkv
+    assert imp[1, js] == pytest.approx(n_imp * G, rel=1e-6)
+    assert imp[0].sum() < n_imp * G and imp[0].max() < 0.2
