@@ -5,8 +5,8 @@ A step is one pass of the whole hot path over one batch of synthetic input:
 for every layer, tree verification attention with fused importance
 (ts_verify_attention) and the partial-KV top-B refresh (ts_partial_kv_select_gather);
 then the penalised sampling + tree acceptance of the step
-(ts_penalized_sample_accept) and the KV commit of the accepted path
-(ts_kv_commit).  Every layer has its own K/V buffers, so one step streams
+(ts_penalized_sample_accept) and the KV commit of the accepted path in every
+layer (ts_kv_commit_batched).  Every layer has its own K/V buffers, so one step streams
 ~13 GB (LLaMA3.1-8B shape, 102,400 cached tokens) -- far more than L2.
 
 metric: algorithmic HBM bytes of the step / step time (GB/s), with decode
@@ -72,7 +72,8 @@ def sample_bytes(w: syn.Workload) -> int:
 
 
 def commit_bytes(w: syn.Workload, n_moved: int = 3) -> int:
-    return 2 * 2 * 2 * n_moved * w.Hkv * w.d
+    # every layer: n_moved accepted rows of K and V read and written
+    return w.layers * 2 * 2 * 2 * n_moved * w.Hkv * w.d
 
 
 def step_bytes(w: syn.Workload) -> int:
@@ -239,6 +240,7 @@ class Step:
         self.ws_v = torch.empty(max(ts.ts_verify_workspace_bytes(T, Hq, Hkv, d, L), 256), **u8)
         self.ws_s = torch.empty(max(ts.ts_select_batched_workspace_bytes(w.layers, Hkv, L), 256), **u8)
         self.sel_table = ts.layer_pointer_table(self.imp, self.k, self.v, self.idx, self.kd, self.vd)
+        self.commit_table = ts.commit_pointer_table(self.k, self.v)
         self.ws_p = torch.empty(max(ts.ts_sample_workspace_bytes(T, w.V), 256), **u8)
         # end-to-end leg: the per-step inputs live in one pinned host buffer
         # (uploaded with a single copy) and are unpacked on the device by a
@@ -323,8 +325,8 @@ class Step:
                                       w.penalty, w.temperature, w.top_p, w.min_p, self.uniforms,
                                       sampled=self.sampled, path=self.path, n_path=self.n_path,
                                       bonus=self.bonus, workspace=self.ws_p, status=self.status)
-        ts.ts_kv_commit(self.k[0], self.v[0], self.L, w.T, self.path, self.n_path,
-                        status=self.status)
+        ts.ts_kv_commit_batched(self.k, self.v, self.L, w.T, self.path, self.n_path,
+                                table=self.commit_table, status=self.status)
 
     def launches_per_step(self) -> int:
         # verify: split kernel + merge per layer; batched select: histogram,
@@ -514,7 +516,8 @@ def run_profile_case(kind: str, w: syn.Workload):
     """Small, fixed cases for ncu captures (a few GB on the device):
     verify -- 2 layers of the workload's K/V, 3 + 5*2 ts_verify_attention calls;
     select -- 4 layers through the batched partial-KV refresh and the sampling
-    step, 3 rounds."""
+    step, 3 rounds;
+    imp -- 2 layers of K, 3 + 2*2 ts_importance_softmax calls."""
     import torch
     import self_speculative_ultra_gb300 as ts
     ts.build()
@@ -522,8 +525,16 @@ def run_profile_case(kind: str, w: syn.Workload):
     g = torch.Generator(device=dev)
     g.manual_seed(0)
     T, Hq, Hkv, d, L = w.T, w.Hq, w.Hkv, w.d, w.L
-    nl = 2 if kind == "verify" else 4
+    nl = 4 if kind == "select" else 2
     ks = [torch.randn((Hkv, L + T, d), generator=g, device=dev).to(torch.bfloat16) for _ in range(nl)]
+    if kind == "imp":
+        q = torch.randn((T, Hq, d), generator=g, device=dev).to(torch.bfloat16)
+        lse = torch.full((T, Hq), 12.0, dtype=torch.float32, device=dev)
+        for i in range(3 + 2 * nl):
+            ts.ts_importance_softmax(q, ks[i % nl], L, lse, n_imp=w.n_imp)
+        torch.cuda.synchronize()
+        print(json.dumps({"profile_case": kind, "workload": w.name, "layers": nl}))
+        return
     vs = [torch.randn((Hkv, L + T, d), generator=g, device=dev).to(torch.bfloat16) for _ in range(nl)]
     tree = syn.make_tree(w, np.random.default_rng(0))
     parents = torch.from_numpy(tree[0]).to(dev)
@@ -595,6 +606,124 @@ def run_draft_case(w: syn.Workload, steps: int, warmup: int):
                                  "Hq": Hq, "Hkv": Hkv, "d": d, "bytes_per_call": nbytes,
                                  "l2": f"{layers} distinct per-layer caches, {layers * 2 * Hkv * (N + T_d) * d * 2 / 1e6:.0f} MB"},
                       "frac_of_peak": round(gbs / peak, 3), "peak_source": peak_src}))
+
+
+def run_imp_softmax_case(w: syn.Workload, steps: int, warmup: int):
+    """Softmax-weighted importance pass (ts_importance_softmax) at the
+    workload's full cache length: one call per layer over distinct per-layer
+    K caches (inputs larger than L2), timed with CUDA events.  Algorithmic
+    bytes per call: K rows [0, L) once + imp written + q and lse read.
+    Prints one JSON line."""
+    import torch
+    import self_speculative_ultra_gb300 as ts
+    ts.build()
+    dev = torch.device("cuda", 0)
+    g = torch.Generator(device=dev)
+    g.manual_seed(0)
+    T, Hq, Hkv, d, L, layers = w.T, w.Hq, w.Hkv, w.d, w.L, w.layers
+    n_imp = w.n_imp if w.n_imp > 0 else T
+    ks = [torch.empty((Hkv, L + T, d), dtype=torch.bfloat16, device=dev).normal_(generator=g)
+          for _ in range(layers)]
+    q = torch.randn((T, Hq, d), generator=g, device=dev).to(torch.bfloat16)
+    lse = torch.full((T, Hq), 12.0, dtype=torch.float32, device=dev)
+    imp = torch.empty((Hkv, L), dtype=torch.float32, device=dev)
+
+    def one_pass():
+        for i in range(layers):
+            ts.ts_importance_softmax(q, ks[i], L, lse, n_imp=n_imp, imp=imp)
+    for _ in range(max(warmup, 3)):
+        one_pass()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(steps):
+        one_pass()
+    e1.record()
+    torch.cuda.synchronize()
+    us = e0.elapsed_time(e1) * 1e3 / (steps * layers)
+    nbytes = Hkv * L * d * 2 + Hkv * L * 4 + T * Hq * d * 2 + T * Hq * 4
+    flops = 2 * n_imp * (Hq // Hkv) * d * L * Hkv
+    peak, peak_src = load_peaks()
+    gbs = nbytes / (us * 1e-6) / 1e9
+    print(json.dumps({"metric": "softmax-weighted importance pass (GB/s)", "value": round(gbs, 1),
+                      "unit": "GB/s", "us_per_call": round(us, 2), "calls": steps * layers,
+                      "tflops": round(flops / (us * 1e-6) / 1e12, 1),
+                      "frac_of_peak": round(gbs / peak, 3), "peak_source": peak_src,
+                      "config": {"workload": w.name, "L": L, "Hq": Hq, "Hkv": Hkv, "d": d,
+                                 "importance_rows": n_imp * (Hq // Hkv), "bytes_per_call": nbytes,
+                                 "l2": f"{layers} distinct per-layer K caches, "
+                                       f"{layers * Hkv * (L + T) * d * 2 / 1e9:.1f} GB"}}))
+
+
+def run_refresh_case(w: syn.Workload, steps: int, warmup: int, drift: float = 0.3):
+    """Partial-cache refresh of all layers per step, full rewrite
+    (ts_partial_kv_select_gather_batched) against the incremental update
+    (ts_partial_kv_refresh_incremental_batched), on the same sequence of
+    importance rows: a fixed per-layer base score ~ N(0, 4^2) plus fresh
+    N(0, drift^2) noise each step (importance that drifts between steps), the
+    cache growing by 2 tokens per step.  Each call is timed with CUDA events;
+    drawing the importance is outside the timed region.  Prints one JSON
+    line."""
+    import torch
+    import self_speculative_ultra_gb300 as ts
+    ts.build()
+    dev = torch.device("cuda", 0)
+    g = torch.Generator(device=dev)
+    g.manual_seed(0)
+    Hkv, d, nl, B, S, R = w.Hkv, w.d, w.layers, w.B, w.S, w.R
+    n_all = max(warmup, 3) + steps
+    L0 = w.L - 2 * n_all
+    L_cap = w.L + w.T
+    N_cap = S + B + R
+    ks = [torch.empty((Hkv, L_cap, d), dtype=torch.bfloat16, device=dev).normal_(generator=g)
+          for _ in range(nl)]
+    vs = [torch.empty((Hkv, L_cap, d), dtype=torch.bfloat16, device=dev).normal_(generator=g)
+          for _ in range(nl)]
+    base = [torch.randn((Hkv, w.L), generator=g, device=dev) * 4.0 for _ in range(nl)]
+    imp_buf = [torch.empty(Hkv * w.L, device=dev) for _ in range(nl)]
+    mk = lambda shape, dt: [torch.empty(shape, dtype=dt, device=dev) for _ in range(nl)]  # noqa: E731
+    f_idx, f_kd, f_vd = mk((Hkv, N_cap), torch.int32), mk((Hkv, N_cap, d), torch.bfloat16), \
+        mk((Hkv, N_cap, d), torch.bfloat16)
+    i_idx, i_kd, i_vd = mk((Hkv, N_cap), torch.int32), mk((Hkv, N_cap, d), torch.bfloat16), \
+        mk((Hkv, N_cap, d), torch.bfloat16)
+    ws_f = torch.empty(ts.ts_select_batched_workspace_bytes(nl, Hkv, w.L), dtype=torch.uint8,
+                       device=dev)
+    ws_i = torch.empty(ts.ts_refresh_workspace_bytes(nl, Hkv, w.L, N_cap), dtype=torch.uint8,
+                       device=dev)
+    written = torch.zeros(nl * Hkv, dtype=torch.int32, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(n_all)]
+    w_sum, N_prev = 0, 0
+    for s_ in range(n_all):
+        L = L0 + 2 * s_
+        imps = [x[:Hkv * L].view(Hkv, L) for x in imp_buf]
+        for x, b_ in zip(imps, base):
+            torch.randn((Hkv, L), generator=g, device=dev, out=x)
+            x.mul_(drift).add_(b_[:, :L])
+        ev[s_][0].record()
+        ts.ts_partial_kv_select_gather_batched(imps, ks, vs, L, B, S, R, f_idx, f_kd, f_vd,
+                                               workspace=ws_f, status=status)
+        ev[s_][1].record()
+        N_prev = ts.ts_partial_kv_refresh_incremental_batched(
+            imps, ks, vs, L, B, S, R, i_idx, i_kd, i_vd, N_prev, n_written=written,
+            workspace=ws_i, status=status)
+        ev[s_][2].record()
+        if s_ >= n_all - steps:
+            w_sum += int(written.sum().item())
+    torch.cuda.synchronize()
+    timed = range(n_all - steps, n_all)
+    full_us = sum(ev[i][0].elapsed_time(ev[i][1]) for i in timed) * 1e3 / steps
+    inc_us = sum(ev[i][1].elapsed_time(ev[i][2]) for i in timed) * 1e3 / steps
+    rows_full = nl * Hkv * N_cap
+    print(json.dumps({
+        "metric": "partial-cache refresh of all layers per step (us)", "unit": "us",
+        "full_rewrite_us": round(full_us, 1), "incremental_us": round(inc_us, 1),
+        "speedup": round(full_us / inc_us, 3),
+        "rows_written_frac": round(w_sum / (steps * rows_full), 4),
+        "device_status": int(status.item()), "steps": steps,
+        "config": {"workload": w.name, "layers": nl, "Hkv": Hkv, "L": w.L, "B": B, "S": S, "R": R,
+                   "importance": f"fixed base N(0,16) + N(0,{drift}^2) per step",
+                   "growth": "2 tokens per step"}}))
 
 
 def run_ngram_case(w: syn.Workload, steps: int, warmup: int):
@@ -708,6 +837,8 @@ def run_loop_case(w: syn.Workload, until: int, L0: int = 2048):
     n_path_h = torch.empty(1, dtype=torch.int32).pin_memory()
     table = ts.layer_pointer_table(imp, ks, vs, idx, kd, vd)
     trow = [ctypes.c_void_p(table[r].data_ptr()) for r in range(6)]
+    ctable = ts.commit_pointer_table(ks, vs)
+    crow = [ctypes.c_void_p(ctable[r].data_ptr()) for r in range(2)]
     stream = ts._stream(None)
     n_out = ctypes.c_int64(0)
     lay = [(P(qs[i]), P(ks[i]), P(vs[i]), P(o[i]), P(lse[i]), P(imp[i])) for i in range(nl)]
@@ -734,9 +865,8 @@ def run_loop_case(w: syn.Workload, until: int, L0: int = 2048):
             P(logits), P(tokens), P(parents), T, P(prior), prior.numel(), w.W, V, w.penalty,
             w.temperature, w.top_p, w.min_p, P(uniforms), P(sampled), P(path), P(n_path),
             P(bonus), P(ws_p), nb_p, P(status), stream))
-        for (q_, k_, v_, o_, lse_, imp_) in lay:
-            ts._check(lib.ts_kv_commit(k_, v_, L, L_cap, Hkv, d, T, P(path), P(n_path), P(status),
-                                       stream))
+        ts._check(lib.ts_kv_commit_batched(nl, crow[0], crow[1], L, L_cap, Hkv, d, T, P(path),
+                                           P(n_path), P(status), stream))
         n_path_h.copy_(n_path, non_blocking=True)
         torch.cuda.current_stream().synchronize()
         return int(n_path_h.item())
@@ -772,7 +902,7 @@ def run_loop_case(w: syn.Workload, until: int, L0: int = 2048):
                    "prefix_L0": L0, "until_L": until, "tree_nodes": T, "B": w.B, "S": w.S,
                    "R": w.R, "V": V, "acceptance": "first child's token +30 with p=0.7",
                    "per_step": f"{nl} verify + 1 batched select/gather over {nl} layers + "
-                               f"1 sample/accept + {nl} commits"}}))
+                               f"1 sample/accept + 1 batched commit over {nl} layers"}}))
 
 
 def main():
@@ -783,18 +913,26 @@ def main():
     ap.add_argument("--impl", default="gpu", choices=["gpu", "reference"])
     ap.add_argument("--workload", default="llama3.1-8b", choices=sorted(syn.WORKLOADS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--profile", choices=["verify", "select"],
+    ap.add_argument("--profile", choices=["verify", "select", "imp"],
                     help="run a small fixed case for ncu captures and exit")
     ap.add_argument("--draft", action="store_true",
                     help="time draft-side attention over the compact cache and exit")
     ap.add_argument("--loop", type=int, default=0, metavar="L_END",
                     help="time a whole generation loop from a 2048-token prefix to L_END "
                          "cached tokens and exit")
+    ap.add_argument("--imp-softmax", action="store_true",
+                    help="time the softmax-weighted importance pass and exit")
+    ap.add_argument("--refresh", action="store_true",
+                    help="time the full against the incremental partial-cache refresh and exit")
     ap.add_argument("--ngram", action="store_true",
                     help="time the token-reutilization step (4-gram table + tree) and exit")
     args = ap.parse_args()
     w = syn.WORKLOADS[args.workload]
-    if args.loop:
+    if args.refresh:
+        run_refresh_case(w, args.steps, args.warmup)
+    elif args.imp_softmax:
+        run_imp_softmax_case(w, args.steps, args.warmup)
+    elif args.loop:
         run_loop_case(w, args.loop)
     elif args.draft:
         run_draft_case(w, args.steps, args.warmup)

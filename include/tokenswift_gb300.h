@@ -95,6 +95,37 @@ int ts_verify_attention(const void* q, const void* k, const void* v,
                         int32_t* status, void* stream);
 
 /* ------------------------------------------------------------------------
+ * (1b) Softmax-weighted importance (a variant of the importance of (1)).
+ *
+ * §3.3 Dynamic KV Cache Management ranks cached pairs by query-key scores,
+ * GQA query heads partitioned per KV head and their scores aggregated.  This
+ * call aggregates the normalised attention weights instead: the probability
+ * mass each committed position receives from the importance queries.
+ *
+ *   imp[kv,j] = sum over the last n_imp nodes i and the heads h of group kv
+ *               of exp(q[i,h,:] . k[kv,j,:] / sqrt(d) - lse[i,h]),
+ *               for j in [0, L)   (fp32)
+ *
+ * q       [T, Hq, d] bf16, the same tree queries given to (1).
+ * k       [Hkv, L_cap, d] bf16; only rows [0, L) are read.  0 <= L <= L_cap.
+ * lse     [T, Hq] fp32, device: each row's natural-log log-sum-exp over
+ *         everything it attends to, as (1) returns it.
+ * n_imp   number of trailing tree queries (<= 0: all T), n_imp <= T.
+ * imp     [Hkv, L] fp32 out (row stride L); call (1) with imp = NULL and pass
+ *         this array to (2).
+ * L = 0 writes nothing and accepts NULL buffers.
+ * No workspace: every position is written by one thread.  The K cache is
+ * read once more (V is not read); the scores use bf16 operands with fp32
+ * accumulation, the exponentials fp32.  Unsupported: n_imp*Hq/Hkv query
+ * rows whose staging exceeds the shared memory of one SM (more than 448 rows
+ * at d = 128).  The caller owns every buffer; nothing is allocated.
+ * ------------------------------------------------------------------------ */
+int ts_importance_softmax(const void* q, const void* k, const float* lse,
+                          int64_t L, int64_t L_cap, int T, int Hq, int Hkv,
+                          int d, int n_imp, float* imp,
+                          int32_t* status, void* stream);
+
+/* ------------------------------------------------------------------------
  * (2) Dynamic partial KV cache: top-B selection and gather.
  *
  * §3.3 Dynamic KV Cache Management: a fixed budget; the initial |S| pairs are
@@ -159,6 +190,54 @@ int ts_partial_kv_select_gather_batched(int n_layers, const float* const* imp,
                                         int32_t* const* idx, void* const* kd, void* const* vd,
                                         int64_t* n_out, void* workspace, size_t workspace_bytes,
                                         int32_t* status, void* stream);
+
+/* ------------------------------------------------------------------------
+ * (2b) Incremental partial-cache refresh.
+ *
+ * §3.3 Dynamic KV Cache Management: the budgeted cache keeps the initial |S|
+ * pairs and replaces the less important pairs as generation proceeds.  The
+ * kept set is the one (2) computes (same ranking, same tie rule); instead of
+ * rewriting the compact cache in position order it is updated in place:
+ *   - slot s < N_prev keeps its row while idx[kv,s] stays selected;
+ *   - the newly selected positions, ascending, take the freed slots in
+ *     ascending slot order, then slots N_prev .. N_new-1, where
+ *     N_new = min(L, S+B+R) (the cache grows until it reaches the budget);
+ *   - only those rows are copied (K and V, bit for bit).
+ * Afterwards idx[kv, 0:N_new] holds exactly the kept set, in slot order, and
+ * kd/vd[kv, s, :] = k/v[kv, idx[kv, s], :].  Attention over the compact
+ * cache does not depend on the slot order.
+ *
+ * imp     [Hkv, L] fp32.   k, v [Hkv, L_cap, d] bf16.
+ * idx     [Hkv, N_cap] int32, in/out; kd, vd [Hkv, N_cap, d] bf16, in/out;
+ *         N_cap >= min(L, S+B+R) is the fixed row stride.
+ * N_prev  slots valid before the call, 0 <= N_prev <= N_new (0 on the first
+ *         call: the result then equals (2)'s ascending output).
+ * n_out   N_new (may be NULL).
+ * n_written [n_layers * Hkv] int32 device out, or NULL: rows written per
+ *         (layer, KV head).
+ * workspace >= ts_refresh_workspace_bytes(n_layers, Hkv, L, N_cap).
+ * Previous slots holding a position outside [0, L), or the same position
+ * twice, are reported as TS_ERR_INVALID_ARG in `status`; the contents are
+ * then unspecified, but no access leaves the buffers.  The batched form
+ * takes device arrays of per-layer pointers, as in (2).
+ * ------------------------------------------------------------------------ */
+size_t ts_refresh_workspace_bytes(int n_layers, int Hkv, int64_t L, int64_t N_cap);
+int ts_partial_kv_refresh_incremental(const float* imp, const void* k, const void* v,
+                                      int64_t L, int64_t L_cap, int Hkv, int d,
+                                      int B, int S, int R, int32_t* idx, void* kd,
+                                      void* vd, int64_t N_cap, int64_t N_prev,
+                                      int64_t* n_out, int32_t* n_written,
+                                      void* workspace, size_t workspace_bytes,
+                                      int32_t* status, void* stream);
+int ts_partial_kv_refresh_incremental_batched(int n_layers, const float* const* imp,
+                                              const void* const* k, const void* const* v,
+                                              int64_t L, int64_t L_cap, int Hkv, int d,
+                                              int B, int S, int R, int32_t* const* idx,
+                                              void* const* kd, void* const* vd,
+                                              int64_t N_cap, int64_t N_prev,
+                                              int64_t* n_out, int32_t* n_written,
+                                              void* workspace, size_t workspace_bytes,
+                                              int32_t* status, void* stream);
 
 /* ------------------------------------------------------------------------
  * (3) Contextual-penalty sampling and exact-match tree acceptance.
@@ -228,6 +307,12 @@ int ts_penalized_sample_accept_eta(const float* logits, const int32_t* tree_toke
 int ts_kv_commit(void* k, void* v, int64_t L, int64_t L_cap, int Hkv, int d, int T,
                  const int32_t* path, const int32_t* n_path,
                  int32_t* status, void* stream);
+/* Every layer in one launch: k and v are device arrays of n_layers pointers,
+ * each layer's cache [Hkv, L_cap, d] bf16 as above; the same path moves the
+ * same rows in every layer. */
+int ts_kv_commit_batched(int n_layers, void* const* k, void* const* v, int64_t L,
+                         int64_t L_cap, int Hkv, int d, int T, const int32_t* path,
+                         const int32_t* n_path, int32_t* status, void* stream);
 
 /* ------------------------------------------------------------------------
  * (5) Token reutilization: the 4-gram table and the draft-tree builder.

@@ -196,6 +196,40 @@ def gather_rows(cache_head, idx) -> np.ndarray:
     return np.asarray(cache_head)[np.asarray(idx, dtype=np.int64)].copy()
 
 
+def refresh_incremental(slots_prev, kept_new, cache_head, compact_prev):
+    """(NEXT-4) Incremental update of one KV head's partial cache.
+
+    §3.3: the budgeted cache keeps its initial |S| pairs and replaces the
+    less important pairs as generation proceeds.  Reading 18 of the design
+    notes: a slot keeps its row while its position stays selected; the rows
+    of newly selected positions are written into the slots whose positions
+    left the selection, and past the old slot count while the cache is still
+    growing (L <= S+B+R).  Freed slots are filled in ascending slot order by
+    the added positions in ascending position order.  Attention over the
+    partial cache does not depend on the slot order.
+
+    slots_prev   [N_prev] positions held by slots 0..N_prev-1 (distinct)
+    kept_new     the new kept positions (select_partial's output)
+    cache_head   [>= L, d] the full cache rows of this head
+    compact_prev [>= N_new, d] the partial cache rows before the update
+    Returns (slots_new [N_new], compact_new [N_new, d], rows_written)."""
+    slots_prev = [int(x) for x in slots_prev]
+    kept = [int(x) for x in kept_new]
+    N_prev, N_new = len(slots_prev), len(kept)
+    assert N_new >= N_prev, "the kept set never shrinks"
+    kept_set, prev_set = set(kept), set(slots_prev)
+    freed = [s for s in range(N_prev) if slots_prev[s] not in kept_set]
+    added = sorted(j for j in kept if j not in prev_set)
+    targets = freed + list(range(N_prev, N_new))
+    assert len(targets) == len(added)
+    slots = slots_prev + [-1] * (N_new - N_prev)
+    out = np.array(compact_prev[:N_new], copy=True)
+    for s, j in zip(targets, added):
+        slots[s] = j
+        out[s] = cache_head[j]
+    return np.asarray(slots, dtype=np.int64), out, len(added)
+
+
 def select_cut_margin(imp_row, L: int, B: int, S: int, R: int) -> tuple[float, np.ndarray]:
     """The B-th best candidate score s_cut, and for every candidate its
     distance to s_cut (used to count near-ties between implementations)."""

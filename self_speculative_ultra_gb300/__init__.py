@@ -17,10 +17,13 @@ from ._build import LIB_PATH, build  # noqa: F401
 
 __all__ = [
     "TsError", "lib", "build", "ts_status_string", "ts_last_error", "ts_version",
-    "ts_verify_workspace_bytes", "ts_verify_attention",
+    "ts_verify_workspace_bytes", "ts_verify_attention", "ts_importance_softmax",
     "ts_select_workspace_bytes", "ts_partial_kv_select_gather", "ts_partial_kv_select_gather_noalloc",
     "ts_select_batched_workspace_bytes", "ts_partial_kv_select_gather_batched", "layer_pointer_table",
+    "ts_refresh_workspace_bytes", "ts_partial_kv_refresh_incremental",
+    "ts_partial_kv_refresh_incremental_batched",
     "ts_sample_workspace_bytes", "ts_penalized_sample_accept", "ts_kv_commit",
+    "ts_kv_commit_batched", "commit_pointer_table",
 ]
 
 TS_OK, TS_ERR_INVALID_ARG, TS_ERR_UNSUPPORTED, TS_ERR_CUDA, TS_ERR_TIMEOUT, TS_ERR_WORKSPACE = range(6)
@@ -36,6 +39,8 @@ _SIGNATURES = {
                                    _i32, _i32, _i32, _i32, _i32, _c_void_p, _c_void_p, _c_void_p,
                                    _c_void_p, _sz, _c_void_p, _c_void_p]),
     "ts_select_workspace_bytes": (_sz, [_i32, _i64]),
+    "ts_importance_softmax": (_i32, [_c_void_p, _c_void_p, _c_void_p, _i64, _i64, _i32, _i32, _i32,
+                                     _i32, _i32, _c_void_p, _c_void_p, _c_void_p]),
     "ts_partial_kv_select_gather": (_i32, [_c_void_p, _c_void_p, _c_void_p, _i64, _i64, _i32, _i32,
                                            _i32, _i32, _i32, _c_void_p, _c_void_p, _c_void_p,
                                            ctypes.POINTER(_i64), _c_void_p, _sz, _c_void_p,
@@ -50,6 +55,16 @@ _SIGNATURES = {
                                                    _c_void_p, _c_void_p, ctypes.POINTER(_i64),
                                                    _c_void_p, _sz, _c_void_p, _c_void_p]),
     "ts_sample_workspace_bytes": (_sz, [_i32, _i32]),
+    "ts_refresh_workspace_bytes": (_sz, [_i32, _i32, _i64, _i64]),
+    "ts_partial_kv_refresh_incremental": (_i32, [_c_void_p, _c_void_p, _c_void_p, _i64, _i64, _i32,
+                                                 _i32, _i32, _i32, _i32, _c_void_p, _c_void_p,
+                                                 _c_void_p, _i64, _i64, ctypes.POINTER(_i64),
+                                                 _c_void_p, _c_void_p, _sz, _c_void_p, _c_void_p]),
+    "ts_partial_kv_refresh_incremental_batched": (_i32, [_i32, _c_void_p, _c_void_p, _c_void_p,
+                                                         _i64, _i64, _i32, _i32, _i32, _i32, _i32,
+                                                         _c_void_p, _c_void_p, _c_void_p, _i64,
+                                                         _i64, ctypes.POINTER(_i64), _c_void_p,
+                                                         _c_void_p, _sz, _c_void_p, _c_void_p]),
     "ts_penalized_sample_accept": (_i32, [_c_void_p, _c_void_p, _c_void_p, _i32, _c_void_p, _i32,
                                           _i32, _i32, _f32, _f32, _f32, _f32, _c_void_p,
                                           _c_void_p, _c_void_p, _c_void_p, _c_void_p,
@@ -61,6 +76,8 @@ _SIGNATURES = {
     "ts_kv_commit": (_i32, [_c_void_p, _c_void_p, _i64, _i64, _i32, _i32, _i32, _c_void_p,
                             _c_void_p, _c_void_p, _c_void_p]),
     "ts_ngram_table_bytes": (_sz, [_i32, _i32]),
+    "ts_kv_commit_batched": (_i32, [_i32, _c_void_p, _c_void_p, _i64, _i64, _i32, _i32, _i32,
+                                    _c_void_p, _c_void_p, _c_void_p, _c_void_p]),
     "ts_ngram_insert": (_i32, [_c_void_p, _i32, _i32, _c_void_p, _i32, _i32, _c_void_p,
                                _c_void_p]),
     "ts_ngram_build_tree": (_i32, [_c_void_p, _i32, _i32, _c_void_p, _c_void_p, _i32, _i32, _i32,
@@ -170,6 +187,24 @@ def ts_verify_attention(q, k, v, L, parents, n_imp=0, o=None, lse=None, imp=None
     return o, lse, imp
 
 
+def ts_importance_softmax(q, k, L, lse, n_imp=0, imp=None, status=None, stream=None):
+    """Softmax-weighted importance of cache positions [0, L): for each KV head
+    the attention probability its positions receive from the group's last
+    n_imp tree queries.  q [T,Hq,d] bf16, k [Hkv,L_cap,d] bf16, lse [T,Hq]
+    fp32 (from ts_verify_attention).  Returns imp [Hkv, L] fp32."""
+    T, Hq, d = q.shape
+    Hkv, L_cap = k.shape[0], k.shape[1]
+    _dev(q, torch.bfloat16, "q")
+    _dev(k, torch.bfloat16, "k", (Hkv, L_cap, d))
+    _dev(lse, torch.float32, "lse", (T, Hq))
+    if imp is None:
+        imp = torch.empty((Hkv, L), dtype=torch.float32, device=q.device)
+    rc = lib().ts_importance_softmax(_ptr(q), _ptr(k), _ptr(lse), L, L_cap, T, Hq, Hkv, d, n_imp,
+                                     _ptr(imp), _ptr(status), _stream(stream))
+    _check(rc)
+    return imp
+
+
 def ts_select_workspace_bytes(Hkv, L) -> int:
     return lib().ts_select_workspace_bytes(Hkv, L)
 
@@ -259,6 +294,62 @@ def ts_partial_kv_select_gather_batched(imps, ks, vs, L, B, S, R, idxs, kds, vds
     return idxs, kds, vds
 
 
+def ts_refresh_workspace_bytes(n_layers, Hkv, L, N_cap) -> int:
+    return lib().ts_refresh_workspace_bytes(n_layers, Hkv, L, N_cap)
+
+
+def ts_partial_kv_refresh_incremental(imp, k, v, L, B, S, R, idx, kd, vd, N_prev, n_written=None,
+                                      workspace=None, status=None, stream=None):
+    """Update one layer's compact cache in place: slots whose position stays
+    selected keep their row, newly selected positions fill the freed slots
+    (then the new ones while the cache grows).  idx [Hkv, N_cap] int32,
+    kd/vd [Hkv, N_cap, d] bf16 hold the previous state in slots [0, N_prev).
+    Returns N_new (the slots now valid)."""
+    Hkv, L_cap, d = k.shape
+    _dev(imp, torch.float32, "imp", (Hkv, L))
+    _dev(k, torch.bfloat16, "k")
+    _dev(v, torch.bfloat16, "v", (Hkv, L_cap, d))
+    N_cap = idx.shape[1]
+    _dev(idx, torch.int32, "idx", (Hkv, N_cap))
+    _dev(kd, torch.bfloat16, "kd", (Hkv, N_cap, d))
+    _dev(vd, torch.bfloat16, "vd", (Hkv, N_cap, d))
+    ws, nb = _workspace(ts_refresh_workspace_bytes(1, Hkv, L, N_cap), k.device, workspace)
+    n_out = _i64(0)
+    rc = lib().ts_partial_kv_refresh_incremental(_ptr(imp), _ptr(k), _ptr(v), L, L_cap, Hkv, d, B,
+                                                 S, R, _ptr(idx), _ptr(kd), _ptr(vd), N_cap,
+                                                 N_prev, ctypes.byref(n_out), _ptr(n_written),
+                                                 _ptr(ws), nb, _ptr(status), _stream(stream))
+    _check(rc)
+    return n_out.value
+
+
+def ts_partial_kv_refresh_incremental_batched(imps, ks, vs, L, B, S, R, idxs, kds, vds, N_prev,
+                                              table=None, n_written=None, workspace=None,
+                                              status=None, stream=None):
+    """The incremental refresh of several layers in one pipeline of launches
+    (per-layer lists with the single-layer shapes).  Returns N_new."""
+    n = len(imps)
+    Hkv, L_cap, d = ks[0].shape
+    N_cap = idxs[0].shape[1]
+    for i in range(n):
+        _dev(imps[i], torch.float32, "imp", (Hkv, L))
+        _dev(ks[i], torch.bfloat16, "k", (Hkv, L_cap, d))
+        _dev(vs[i], torch.bfloat16, "v", (Hkv, L_cap, d))
+        _dev(idxs[i], torch.int32, "idx", (Hkv, N_cap))
+        _dev(kds[i], torch.bfloat16, "kd", (Hkv, N_cap, d))
+        _dev(vds[i], torch.bfloat16, "vd", (Hkv, N_cap, d))
+    if table is None:
+        table = layer_pointer_table(imps, ks, vs, idxs, kds, vds)
+    ws, nb = _workspace(ts_refresh_workspace_bytes(n, Hkv, L, N_cap), ks[0].device, workspace)
+    n_out = _i64(0)
+    row = lambda r: ctypes.c_void_p(table[r].data_ptr())  # noqa: E731
+    rc = lib().ts_partial_kv_refresh_incremental_batched(
+        n, row(0), row(1), row(2), L, L_cap, Hkv, d, B, S, R, row(3), row(4), row(5), N_cap, N_prev,
+        ctypes.byref(n_out), _ptr(n_written), _ptr(ws), nb, _ptr(status), _stream(stream))
+    _check(rc)
+    return n_out.value
+
+
 def ts_sample_workspace_bytes(T, V) -> int:
     return lib().ts_sample_workspace_bytes(T, V)
 
@@ -325,6 +416,31 @@ def ts_kv_commit(k, v, L, T, path, n_path, status=None, stream=None):
     _dev(v, torch.bfloat16, "v", (Hkv, L_cap, d))
     rc = lib().ts_kv_commit(_ptr(k), _ptr(v), L, L_cap, Hkv, d, T, _ptr(path), _ptr(n_path),
                             _ptr(status), _stream(stream))
+    _check(rc)
+
+
+def commit_pointer_table(ks, vs):
+    """Device table [2, n_layers] of the per-layer K and V cache addresses the
+    batched commit reads (build it once and reuse it while the caches live)."""
+    if len(ks) != len(vs):
+        raise ValueError("ks and vs must have one entry per layer")
+    host = torch.tensor([[t.data_ptr() for t in ks], [t.data_ptr() for t in vs]],
+                        dtype=torch.int64)
+    return host.to(ks[0].device)
+
+
+def ts_kv_commit_batched(ks, vs, L, T, path, n_path, table=None, status=None, stream=None):
+    """ts_kv_commit for every layer in one launch (lists of per-layer caches
+    [Hkv, L_cap, d] bf16)."""
+    Hkv, L_cap, d = ks[0].shape
+    for x, y in zip(ks, vs):
+        _dev(x, torch.bfloat16, "k", (Hkv, L_cap, d))
+        _dev(y, torch.bfloat16, "v", (Hkv, L_cap, d))
+    if table is None:
+        table = commit_pointer_table(ks, vs)
+    rc = lib().ts_kv_commit_batched(len(ks), ctypes.c_void_p(table[0].data_ptr()),
+                                    ctypes.c_void_p(table[1].data_ptr()), L, L_cap, Hkv, d, T,
+                                    _ptr(path), _ptr(n_path), _ptr(status), _stream(stream))
     _check(rc)
 
 

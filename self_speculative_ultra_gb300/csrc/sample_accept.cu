@@ -637,13 +637,15 @@ sample_accept_kernel(const float* __restrict__ logits, const int32_t* __restrict
   }
 }
 
+// Rows L+path[t] -> L+t of one KV head (t = 1..n-1).  The sources are staged
+// in shared memory first, so overlapping moves are safe.
 template <int D>
-__global__ void kv_commit_kernel(__nv_bfloat16* __restrict__ k, __nv_bfloat16* __restrict__ v,
-                                 int64_t L, int64_t L_cap, int T, const int32_t* __restrict__ path,
-                                 const int32_t* __restrict__ n_path, int32_t* status) {
+__device__ __forceinline__ void commit_head(__nv_bfloat16* __restrict__ k,
+                                            __nv_bfloat16* __restrict__ v, int kv, int64_t L,
+                                            int64_t L_cap, int T, const int32_t* __restrict__ path,
+                                            const int32_t* __restrict__ n_path, int32_t* status) {
   constexpr int V16 = D / 8;
   __shared__ uint4 kb[63][V16], vb[63][V16];
-  const int kv = blockIdx.x;
   const int n = *n_path;
   if (n < 1 || n > T) {
     if (threadIdx.x == 0) set_status(status, TS_ERR_INVALID_ARG);
@@ -672,6 +674,23 @@ __global__ void kv_commit_kernel(__nv_bfloat16* __restrict__ k, __nv_bfloat16* _
     kh[(L + t) * V16 + x] = kb[t - 1][x];
     vh[(L + t) * V16 + x] = vb[t - 1][x];
   }
+}
+
+template <int D>
+__global__ void kv_commit_kernel(__nv_bfloat16* __restrict__ k, __nv_bfloat16* __restrict__ v,
+                                 int64_t L, int64_t L_cap, int T, const int32_t* __restrict__ path,
+                                 const int32_t* __restrict__ n_path, int32_t* status) {
+  commit_head<D>(k, v, blockIdx.x, L, L_cap, T, path, n_path, status);
+}
+
+// every layer in one launch: CTA (KV head, layer), per-layer caches from
+// device arrays of pointers
+template <int D>
+__global__ void kv_commit_batched_kernel(__nv_bfloat16* const* __restrict__ ks,
+                                         __nv_bfloat16* const* __restrict__ vs, int64_t L,
+                                         int64_t L_cap, int T, const int32_t* __restrict__ path,
+                                         const int32_t* __restrict__ n_path, int32_t* status) {
+  commit_head<D>(ks[blockIdx.y], vs[blockIdx.y], blockIdx.x, L, L_cap, T, path, n_path, status);
 }
 
 }  // namespace
@@ -708,6 +727,19 @@ int launch_kv_commit(void* k, void* v, int64_t L, int64_t L_cap, int Hkv, int d,
   else
     kv_commit_kernel<64><<<Hkv, 256, 0, st>>>(kb, vb, L, L_cap, T, path, n_path, status);
   return launch_status("kv_commit_kernel");
+}
+
+int launch_kv_commit_batched(int n_layers, void* const* k, void* const* v, int64_t L,
+                             int64_t L_cap, int Hkv, int d, int T, const int32_t* path,
+                             const int32_t* n_path, int32_t* status, cudaStream_t st) {
+  auto kb = reinterpret_cast<__nv_bfloat16* const*>(k);
+  auto vb = reinterpret_cast<__nv_bfloat16* const*>(v);
+  dim3 grid(Hkv, n_layers);
+  if (d == 128)
+    kv_commit_batched_kernel<128><<<grid, 256, 0, st>>>(kb, vb, L, L_cap, T, path, n_path, status);
+  else
+    kv_commit_batched_kernel<64><<<grid, 256, 0, st>>>(kb, vb, L, L_cap, T, path, n_path, status);
+  return launch_status("kv_commit_batched_kernel");
 }
 
 }  // namespace ts

@@ -21,6 +21,7 @@
 //                   ascending order, copy their K/V rows with 16-byte loads
 #include <mutex>
 
+#include "refresh.cuh"
 #include "ts_common.cuh"
 
 namespace ts {
@@ -488,6 +489,199 @@ select_gather(Layers P, int64_t L, int64_t L_cap, int S, int R, int64_t N, int64
   }
 }
 
+// ---------------------------------------------------------------------------
+// Incremental refresh (§3.3: the budgeted cache replaces its less important
+// pairs as generation proceeds).  A slot keeps its row while its position
+// stays selected; newly selected positions, in ascending order, take the
+// freed slots in ascending slot order, then the slots [N_prev, N_new) while
+// the cache still grows.  Only those rows are copied.  Stages after the
+// selection's histogram and collect kernels:
+//   refresh_bits    bitmap of the previous slots' positions
+//   refresh_mark    per chunk: count of selected positions not in the bitmap;
+//                   chunk 0 also lists the freed slots in slot order; the last
+//                   CTA of a head turns the counts into offsets
+//   refresh_patch   per chunk: rank the new positions, write idx and copy
+//                   their K/V rows into their slots
+struct RefreshWs {
+  uint32_t* bits;      // [heads][W32]
+  uint32_t* ticket;    // [heads]
+  int32_t* n_freed;    // [heads]
+  int32_t* cnt;        // [heads][n_chunks]
+  int32_t* off;        // [heads][n_chunks + 1]
+  int32_t* freed;      // [heads][N_cap]
+  int64_t w32;         // bitmap words per head
+  size_t zero_bytes;   // bits + tickets, zeroed per call
+};
+
+__host__ __device__ inline RefreshWs carve_refresh(void* base, int HH, int64_t L, int64_t n_chunks,
+                                                   int64_t N_cap) {
+  RefreshWs r;
+  char* p = static_cast<char*>(base);
+  size_t o = 0;
+  r.w32 = (L + 31) / 32 > 0 ? (L + 31) / 32 : 1;
+  r.bits = reinterpret_cast<uint32_t*>(p + o);
+  o += a256((size_t)HH * r.w32 * sizeof(uint32_t));
+  r.ticket = reinterpret_cast<uint32_t*>(p + o);
+  o += a256((size_t)HH * sizeof(uint32_t));
+  r.zero_bytes = o;
+  r.n_freed = reinterpret_cast<int32_t*>(p + o);
+  o += a256((size_t)HH * sizeof(int32_t));
+  r.cnt = reinterpret_cast<int32_t*>(p + o);
+  o += a256((size_t)HH * n_chunks * sizeof(int32_t));
+  r.off = reinterpret_cast<int32_t*>(p + o);
+  o += a256((size_t)HH * (n_chunks + 1) * sizeof(int32_t));
+  r.freed = reinterpret_cast<int32_t*>(p + o);
+  return r;
+}
+
+__host__ inline size_t refresh_area_bytes(int HH, int64_t L, int64_t n_chunks, int64_t N_cap) {
+  const int64_t w32 = (L + 31) / 32 > 0 ? (L + 31) / 32 : 1;
+  return a256((size_t)HH * w32 * sizeof(uint32_t)) + a256((size_t)HH * sizeof(uint32_t)) +
+         a256((size_t)HH * sizeof(int32_t)) + a256((size_t)HH * n_chunks * sizeof(int32_t)) +
+         a256((size_t)HH * (n_chunks + 1) * sizeof(int32_t)) +
+         a256((size_t)HH * (N_cap > 0 ? N_cap : 1) * sizeof(int32_t));
+}
+
+__device__ __forceinline__ bool bit_of(const uint32_t* bits, int64_t j) {
+  return (bits[j >> 5] >> (j & 31)) & 1u;
+}
+
+__global__ void __launch_bounds__(kThreads)
+refresh_bits(Layers P, int64_t L, int64_t N_prev, int64_t N_cap, RefreshWs r, int32_t* status) {
+  const int kv = blockIdx.y, layer = blockIdx.z, hh = layer * gridDim.y + kv;
+  const int32_t* idx = (P.idx ? P.idx[layer] : P.idx1) + (size_t)kv * N_cap;
+  uint32_t* bits = r.bits + (size_t)hh * r.w32;
+  const int64_t s = (int64_t)blockIdx.x * kThreads + threadIdx.x;
+  if (s < N_prev) {
+    const int32_t p = idx[s];
+    if (p >= 0 && p < L)
+      atomicOr(bits + (p >> 5), 1u << (p & 31));
+    else
+      set_status(status, TS_ERR_INVALID_ARG);
+  }
+}
+
+__global__ void __launch_bounds__(kThreads)
+refresh_mark(Layers P, int64_t L, int S, int R, int64_t N_prev, int64_t N_new, int64_t N_cap,
+             int64_t n_chunks, Ws w, RefreshWs r, int32_t* status) {
+  const int64_t c = blockIdx.x;
+  const int kv = blockIdx.y, tid = threadIdx.x, layer = blockIdx.z;
+  const int hh = layer * gridDim.y + kv;
+  const float* imp_h = imp_of(P, layer) + (size_t)kv * L;
+  const int32_t* idx = (P.idx ? P.idx[layer] : P.idx1) + (size_t)kv * N_cap;
+  const uint32_t* bits = r.bits + (size_t)hh * r.w32;
+  const SelectState st = w.state[hh];
+  __shared__ int warp_buf[32];
+  __shared__ int s_total, s_flag;
+  constexpr int PER = kChunk / kThreads;
+  const int64_t a = c * kChunk + tid * PER;
+  int cnt = 0;
+#pragma unroll
+  for (int x = 0; x < PER; ++x) {
+    const int64_t j = a + x;
+    if (j < L && keep_pos(imp_h, j, L, S, R, st) && !bit_of(bits, j)) ++cnt;
+  }
+  block_excl_scan(cnt, warp_buf, &s_total);
+  if (tid == 0) r.cnt[(size_t)hh * n_chunks + c] = s_total;
+  if (c == 0) {
+    // freed slots: their position is no longer selected (or was invalid)
+    int base = 0;
+    for (int64_t s0 = 0; s0 < N_prev; s0 += kThreads) {
+      const int64_t sl = s0 + tid;
+      int f = 0;
+      if (sl < N_prev) {
+        const int32_t p = idx[sl];
+        f = !(p >= 0 && p < L && keep_pos(imp_h, p, L, S, R, st));
+      }
+      const int pos = block_excl_scan(f, warp_buf, &s_total);
+      if (f) r.freed[(size_t)hh * N_cap + base + pos] = (int32_t)sl;
+      base += s_total;
+    }
+    if (tid == 0) r.n_freed[hh] = base;
+  }
+  if (last_of_head(&r.ticket[hh], (uint32_t)n_chunks, &s_flag)) {
+    int run = 0;
+    for (int64_t c0 = 0; c0 < n_chunks; c0 += kThreads) {
+      const int64_t cc = c0 + tid;
+      const int v = cc < n_chunks ? __ldcg(r.cnt + (size_t)hh * n_chunks + cc) : 0;
+      const int pos = block_excl_scan(v, warp_buf, &s_total);
+      if (cc < n_chunks) r.off[(size_t)hh * (n_chunks + 1) + cc] = run + pos;
+      run += s_total;
+    }
+    if (tid == 0) {
+      r.off[(size_t)hh * (n_chunks + 1) + n_chunks] = run;
+      if ((int64_t)run != (int64_t)__ldcg(r.n_freed + hh) + (N_new - N_prev))
+        set_status(status, TS_ERR_INVALID_ARG);   // duplicate or invalid previous slots
+    }
+  }
+}
+
+template <int D>
+__global__ void __launch_bounds__(kThreads)
+refresh_patch(Layers P, int64_t L, int64_t L_cap, int S, int R, int64_t N_prev, int64_t N_new,
+              int64_t N_cap, int64_t n_chunks, Ws w, RefreshWs r, int32_t* n_written,
+              int32_t* status) {
+  const int64_t c = blockIdx.x;
+  const int kv = blockIdx.y, tid = threadIdx.x, layer = blockIdx.z;
+  const int hh = layer * gridDim.y + kv;
+  const float* imp_h = imp_of(P, layer) + (size_t)kv * L;
+  const __nv_bfloat16* k = P.k ? P.k[layer] : P.k1;
+  const __nv_bfloat16* v = P.v ? P.v[layer] : P.v1;
+  int32_t* idx = (P.idx ? P.idx[layer] : P.idx1) + (size_t)kv * N_cap;
+  __nv_bfloat16* kd = P.kd ? P.kd[layer] : P.kd1;
+  __nv_bfloat16* vd = P.vd ? P.vd[layer] : P.vd1;
+  const uint32_t* bits = r.bits + (size_t)hh * r.w32;
+  const SelectState st = w.state[hh];
+  __shared__ int warp_buf[32];
+  __shared__ int s_total;
+  __shared__ int32_t s_pos[kChunk], s_slot[kChunk];
+  constexpr int PER = kChunk / kThreads;
+  const int64_t a = c * kChunk + tid * PER;
+  int flags = 0, cnt = 0;
+#pragma unroll
+  for (int x = 0; x < PER; ++x) {
+    const int64_t j = a + x;
+    if (j < L && keep_pos(imp_h, j, L, S, R, st) && !bit_of(bits, j)) {
+      flags |= 1 << x;
+      ++cnt;
+    }
+  }
+  int pos = block_excl_scan(cnt, warp_buf, &s_total);
+  const int base = __ldcg(r.off + (size_t)hh * (n_chunks + 1) + c);
+  const int nf = __ldcg(r.n_freed + hh);
+  if (c == 0 && tid == 0 && n_written)
+    n_written[hh] = __ldcg(r.off + (size_t)hh * (n_chunks + 1) + n_chunks);
+#pragma unroll
+  for (int x = 0; x < PER; ++x) {
+    if (flags & (1 << x)) {
+      const int g = base + pos;
+      const int64_t slot = g < nf ? (int64_t)__ldcg(r.freed + (size_t)hh * N_cap + g)
+                                  : N_prev + (g - nf);
+      const bool ok = slot >= 0 && slot < N_new;
+      if (ok) idx[slot] = (int32_t)(a + x);
+      else set_status(status, TS_ERR_INVALID_ARG);
+      s_pos[pos] = (int32_t)(a + x);
+      s_slot[pos] = ok ? (int32_t)slot : -1;
+      ++pos;
+    }
+  }
+  __syncthreads();
+  const int total = s_total;
+  constexpr int V16 = D / 8;
+  const uint4* ksrc = reinterpret_cast<const uint4*>(k + (size_t)kv * L_cap * D);
+  const uint4* vsrc = reinterpret_cast<const uint4*>(v + (size_t)kv * L_cap * D);
+  uint4* kdst = reinterpret_cast<uint4*>(kd + (size_t)kv * N_cap * D);
+  uint4* vdst = reinterpret_cast<uint4*>(vd + (size_t)kv * N_cap * D);
+  for (int e = tid; e < total * V16; e += kThreads) {
+    const int rr = e / V16, x = e % V16;
+    const int64_t slot = s_slot[rr];
+    if (slot < 0) continue;
+    const int64_t j = s_pos[rr];
+    kdst[slot * V16 + x] = ksrc[j * V16 + x];
+    vdst[slot * V16 + x] = vsrc[j * V16 + x];
+  }
+}
+
 }  // namespace
 
 SelectPlan select_plan(int Hkv, int64_t L, int n_layers) {
@@ -577,6 +771,68 @@ int launch_select_gather_batched(int n_layers, const float* const* imp, const vo
   P.kd = reinterpret_cast<__nv_bfloat16* const*>(kd);
   P.vd = reinterpret_cast<__nv_bfloat16* const*>(vd);
   return run_select(P, n_layers, L, L_cap, Hkv, d, B, S, R, N, ws, status, st);
+}
+
+size_t refresh_ws_bytes(int HH, int64_t L, int64_t N_cap) {
+  const SelectPlan p = select_plan(HH, L, 1);
+  return ws_total(HH, L, p.n_chunks) + refresh_area_bytes(HH, L, p.n_chunks, N_cap);
+}
+
+int launch_refresh_incremental(int n_layers, const float* imp1, const float* const* imp,
+                               const void* k1, const void* const* k, const void* v1,
+                               const void* const* v, int64_t L, int64_t L_cap, int Hkv, int d,
+                               int B, int S, int R, int64_t N_prev, int64_t N_new, int64_t N_cap,
+                               int32_t* idx1, int32_t* const* idx, void* kd1, void* const* kd,
+                               void* vd1, void* const* vd, int32_t* n_written, void* ws,
+                               int32_t* status, cudaStream_t st) {
+  Layers P{};
+  P.imp = imp;
+  P.k = reinterpret_cast<const __nv_bfloat16* const*>(k);
+  P.v = reinterpret_cast<const __nv_bfloat16* const*>(v);
+  P.idx = idx;
+  P.kd = reinterpret_cast<__nv_bfloat16* const*>(kd);
+  P.vd = reinterpret_cast<__nv_bfloat16* const*>(vd);
+  P.imp1 = imp1;
+  P.k1 = static_cast<const __nv_bfloat16*>(k1);
+  P.v1 = static_cast<const __nv_bfloat16*>(v1);
+  P.idx1 = idx1;
+  P.kd1 = static_cast<__nv_bfloat16*>(kd1);
+  P.vd1 = static_cast<__nv_bfloat16*>(vd1);
+  const int HH = Hkv * n_layers;
+  const SelectPlan p = select_plan(Hkv, L, n_layers);
+  if (p.n_chunks > 1024)
+    return fail(TS_ERR_UNSUPPORTED, "ts_partial_kv_refresh_incremental: L > %d", 1024 * kChunk);
+  Ws w = carve(ws, HH, L, p.n_chunks);
+  RefreshWs r = carve_refresh(static_cast<char*>(ws) + ws_total(HH, L, p.n_chunks), HH, L,
+                              p.n_chunks, N_cap);
+  if (cudaMemsetAsync(ws, 0, w.zero_bytes, st) != cudaSuccess ||
+      cudaMemsetAsync(r.bits, 0, r.zero_bytes, st) != cudaSuccess)
+    return launch_status("refresh workspace reset");
+  dim3 grid((unsigned)p.n_chunks, Hkv, n_layers);
+  dim3 sgrid((unsigned)((L + kScan - 1) / kScan), Hkv, n_layers);
+  if (N_prev > 0) {
+    dim3 bgrid((unsigned)((N_prev + kThreads - 1) / kThreads), Hkv, n_layers);
+    refresh_bits<<<bgrid, kThreads, 0, st>>>(P, L, N_prev, N_cap, r, status);
+    int rc = launch_status("refresh_bits");
+    if (rc) return rc;
+  }
+  select_hist<<<sgrid, kThreads, 0, st>>>(P, L, B, S, R, p.n_chunks, w);
+  int rc = launch_status("select_hist");
+  if (rc) return rc;
+  select_collect<<<sgrid, kThreads, 0, st>>>(P, L, S, R, p.n_chunks, w);
+  rc = launch_status("select_collect");
+  if (rc) return rc;
+  refresh_mark<<<grid, kThreads, 0, st>>>(P, L, S, R, N_prev, N_new, N_cap, p.n_chunks, w, r,
+                                          status);
+  rc = launch_status("refresh_mark");
+  if (rc) return rc;
+  if (d == 128)
+    refresh_patch<128><<<grid, kThreads, 0, st>>>(P, L, L_cap, S, R, N_prev, N_new, N_cap,
+                                                  p.n_chunks, w, r, n_written, status);
+  else
+    refresh_patch<64><<<grid, kThreads, 0, st>>>(P, L, L_cap, S, R, N_prev, N_new, N_cap,
+                                                 p.n_chunks, w, r, n_written, status);
+  return launch_status("refresh_patch");
 }
 
 }  // namespace ts

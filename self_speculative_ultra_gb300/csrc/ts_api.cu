@@ -3,6 +3,8 @@
 #include <cstdio>
 #include <cstring>
 
+#include "importance.cuh"
+#include "refresh.cuh"
 #include "ts_common.cuh"
 
 namespace ts {
@@ -45,6 +47,10 @@ static int check_attn_shape(int T, int Hq, int Hkv, int d, const char* what) {
     return fail(TS_ERR_UNSUPPORTED, "%s: T*Hq/Hkv = %d > 512 query rows per KV head", what, T * (Hq / Hkv));
   return TS_OK;
 }
+
+int launch_kv_commit_batched(int n_layers, void* const* k, void* const* v, int64_t L,
+                             int64_t L_cap, int Hkv, int d, int T, const int32_t* path,
+                             const int32_t* n_path, int32_t* status, cudaStream_t st);
 
 }  // namespace ts
 
@@ -93,6 +99,28 @@ int ts_verify_attention(const void* q, const void* k, const void* v, int64_t L, 
   if (rc) return rc;
   return launch_verify(q, k, v, L, L_cap, parents, T, Hq, Hkv, d, n_imp, o, lse, imp, workspace,
                        status, static_cast<cudaStream_t>(stream));
+}
+
+int ts_importance_softmax(const void* q, const void* k, const float* lse, int64_t L,
+                          int64_t L_cap, int T, int Hq, int Hkv, int d, int n_imp, float* imp,
+                          int32_t* status, void* stream) {
+  clear_error();
+  const char* W = "ts_importance_softmax";
+  int rc = check_attn_shape(T, Hq, Hkv, d, W);
+  if (rc) return rc;
+  if (L < 0 || L > L_cap)
+    return fail(TS_ERR_INVALID_ARG, "%s: need 0 <= L <= L_cap (L=%lld L_cap=%lld)", W,
+                (long long)L, (long long)L_cap);
+  if (L == 0) return TS_OK;   // nothing to write (imp may then be empty)
+  if (!q || !k || !lse || !imp) return fail(TS_ERR_INVALID_ARG, "%s: NULL tensor", W);
+  if (L_cap > (int64_t(1) << 31) - 1) return fail(TS_ERR_UNSUPPORTED, "%s: L_cap >= 2^31", W);
+  if (n_imp > T) return fail(TS_ERR_INVALID_ARG, "%s: n_imp=%d > T=%d", W, n_imp, T);
+  if (n_imp <= 0) n_imp = T;
+  if (importance_softmax_plan(T, Hq, Hkv, d, n_imp, L > 0 ? L : 1).smem > 227 * 1024)
+    return fail(TS_ERR_UNSUPPORTED, "%s: %d importance query rows exceed one SM's shared memory",
+                W, n_imp * (Hq / Hkv));
+  return launch_importance_softmax(q, k, lse, L, L_cap, T, Hq, Hkv, d, n_imp, imp, status,
+                                   static_cast<cudaStream_t>(stream));
 }
 
 size_t ts_select_workspace_bytes(int Hkv, int64_t L) {
@@ -154,6 +182,74 @@ int ts_partial_kv_select_gather_noalloc(const float* imp, const void* k, const v
   if (rc) return rc;
   return launch_select_gather(imp, k, v, L, L_cap, Hkv, d, B, S, R, idx, kd, vd, N, scratch,
                               status, static_cast<cudaStream_t>(stream));
+}
+
+size_t ts_refresh_workspace_bytes(int n_layers, int Hkv, int64_t L, int64_t N_cap) {
+  if (n_layers < 1 || Hkv < 1 || L < 0 || N_cap < 0) return 0;
+  return refresh_ws_bytes(n_layers * Hkv, L, N_cap);
+}
+
+static int refresh_common(const char* W, int n_layers, int64_t L, int64_t L_cap, int Hkv, int d,
+                          int B, int S, int R, int64_t N_cap, int64_t N_prev, int64_t* n_out,
+                          int64_t* N_new, void* workspace, size_t workspace_bytes) {
+  if (n_layers < 1 || n_layers > 65535)
+    return fail(TS_ERR_INVALID_ARG, "%s: n_layers=%d", W, n_layers);
+  if (Hkv < 1) return fail(TS_ERR_INVALID_ARG, "%s: Hkv=%d", W, Hkv);
+  if (d != 64 && d != 128) return fail(TS_ERR_UNSUPPORTED, "%s: head dim %d not in {64,128}", W, d);
+  if (B < 0 || S < 0 || R < 0) return fail(TS_ERR_INVALID_ARG, "%s: B, S, R must be >= 0", W);
+  if (L < 0 || L > L_cap) return fail(TS_ERR_INVALID_ARG, "%s: need 0 <= L <= L_cap", W);
+  if (L_cap > (int64_t(1) << 31) - 1) return fail(TS_ERR_UNSUPPORTED, "%s: L_cap >= 2^31", W);
+  const int64_t N = L < (int64_t)S + B + R ? L : (int64_t)S + B + R;
+  if (N_cap < N)
+    return fail(TS_ERR_INVALID_ARG, "%s: N_cap=%lld < min(L, S+B+R)=%lld", W, (long long)N_cap,
+                (long long)N);
+  if (N_prev < 0 || N_prev > N)
+    return fail(TS_ERR_INVALID_ARG, "%s: need 0 <= N_prev <= min(L, S+B+R) (N_prev=%lld, N=%lld)",
+                W, (long long)N_prev, (long long)N);
+  if (n_out) *n_out = N;
+  *N_new = N;
+  if (L == 0) return TS_OK;
+  return check_ws(workspace, workspace_bytes, refresh_ws_bytes(n_layers * Hkv, L, N_cap), W);
+}
+
+int ts_partial_kv_refresh_incremental(const float* imp, const void* k, const void* v, int64_t L,
+                                      int64_t L_cap, int Hkv, int d, int B, int S, int R,
+                                      int32_t* idx, void* kd, void* vd, int64_t N_cap,
+                                      int64_t N_prev, int64_t* n_out, int32_t* n_written,
+                                      void* workspace, size_t workspace_bytes, int32_t* status,
+                                      void* stream) {
+  clear_error();
+  const char* W = "ts_partial_kv_refresh_incremental";
+  int64_t N_new = 0;
+  int rc = refresh_common(W, 1, L, L_cap, Hkv, d, B, S, R, N_cap, N_prev, n_out, &N_new, workspace,
+                          workspace_bytes);
+  if (rc || L == 0) return rc;
+  if (!imp || !k || !v || !idx || !kd || !vd) return fail(TS_ERR_INVALID_ARG, "%s: NULL tensor", W);
+  return launch_refresh_incremental(1, imp, nullptr, k, nullptr, v, nullptr, L, L_cap, Hkv, d, B,
+                                    S, R, N_prev, N_new, N_cap, idx, nullptr, kd, nullptr, vd,
+                                    nullptr, n_written, workspace, status,
+                                    static_cast<cudaStream_t>(stream));
+}
+
+int ts_partial_kv_refresh_incremental_batched(int n_layers, const float* const* imp,
+                                              const void* const* k, const void* const* v,
+                                              int64_t L, int64_t L_cap, int Hkv, int d, int B,
+                                              int S, int R, int32_t* const* idx, void* const* kd,
+                                              void* const* vd, int64_t N_cap, int64_t N_prev,
+                                              int64_t* n_out, int32_t* n_written, void* workspace,
+                                              size_t workspace_bytes, int32_t* status,
+                                              void* stream) {
+  clear_error();
+  const char* W = "ts_partial_kv_refresh_incremental_batched";
+  int64_t N_new = 0;
+  int rc = refresh_common(W, n_layers, L, L_cap, Hkv, d, B, S, R, N_cap, N_prev, n_out, &N_new,
+                          workspace, workspace_bytes);
+  if (rc || L == 0) return rc;
+  if (!imp || !k || !v || !idx || !kd || !vd) return fail(TS_ERR_INVALID_ARG, "%s: NULL array", W);
+  return launch_refresh_incremental(n_layers, nullptr, imp, nullptr, k, nullptr, v, L, L_cap, Hkv,
+                                    d, B, S, R, N_prev, N_new, N_cap, nullptr, idx, nullptr, kd,
+                                    nullptr, vd, n_written, workspace, status,
+                                    static_cast<cudaStream_t>(stream));
 }
 
 int ts_partial_kv_select_gather_batched(int n_layers, const float* const* imp,
@@ -254,6 +350,21 @@ int ts_kv_commit(void* k, void* v, int64_t L, int64_t L_cap, int Hkv, int d, int
   if (!k || !v || !path || !n_path) return fail(TS_ERR_INVALID_ARG, "%s: NULL tensor", F);
   return launch_kv_commit(k, v, L, L_cap, Hkv, d, T, path, n_path, status,
                           static_cast<cudaStream_t>(stream));
+}
+
+int ts_kv_commit_batched(int n_layers, void* const* k, void* const* v, int64_t L, int64_t L_cap,
+                         int Hkv, int d, int T, const int32_t* path, const int32_t* n_path,
+                         int32_t* status, void* stream) {
+  clear_error();
+  const char* F = "ts_kv_commit_batched";
+  if (n_layers < 1 || n_layers > 65535) return fail(TS_ERR_INVALID_ARG, "%s: n_layers=%d", F, n_layers);
+  if (Hkv < 1 || T < 1) return fail(TS_ERR_INVALID_ARG, "%s: Hkv, T must be >= 1", F);
+  if (T > 64) return fail(TS_ERR_UNSUPPORTED, "%s: T=%d > 64", F, T);
+  if (d != 64 && d != 128) return fail(TS_ERR_UNSUPPORTED, "%s: head dim %d", F, d);
+  if (L < 0 || L + T > L_cap) return fail(TS_ERR_INVALID_ARG, "%s: need L+T <= L_cap", F);
+  if (!k || !v || !path || !n_path) return fail(TS_ERR_INVALID_ARG, "%s: NULL array", F);
+  return launch_kv_commit_batched(n_layers, k, v, L, L_cap, Hkv, d, T, path, n_path, status,
+                                  static_cast<cudaStream_t>(stream));
 }
 
 size_t ts_ngram_table_bytes(int V, int cap) {

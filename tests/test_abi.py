@@ -88,3 +88,23 @@ def test_select_and_sample_reject_bad_args(ts):
     assert s(*args) == 5                    # no workspace
     c = _c(ts).ts_kv_commit
     assert c(p, p, 10, 12, 1, 128, 4, p, p, None, None) == 1
+
+
+def test_importance_softmax_rejects_bad_args(ts):
+    f = _c(ts).ts_importance_softmax
+    p = ctypes.c_void_p(16)
+    # NULL lse (with a non-empty cache)
+    assert f(p, p, None, 10, 100, 4, 4, 1, 64, 0, p, None, None) == 1
+    # an empty cache needs no buffers
+    assert f(p, p, None, 0, 100, 4, 4, 1, 64, 0, None, None, None) == 0
+    # L > L_cap
+    assert f(p, p, p, 101, 100, 4, 4, 1, 64, 0, p, None, None) == 1
+    # n_imp > T
+    assert f(p, p, p, 10, 100, 4, 4, 1, 64, 5, p, None, None) == 1
+    # head dim 96
+    assert f(p, p, p, 10, 100, 4, 4, 1, 96, 0, p, None, None) == 2
+    # 64 nodes x 8 heads per group = 512 query rows do not fit one SM at d = 128
+    assert f(p, p, p, 10, 100, 64, 8, 1, 128, 0, p, None, None) == 2
+    assert "shared memory" in ts.ts_last_error()
+    # 448 rows fit: the call passes the checks; L = 0 launches nothing
+    assert f(p, p, p, 0, 100, 56, 8, 1, 128, 0, p, None, None) == 0

@@ -114,3 +114,24 @@ def test_kv_commit_matches_oracle():
     torch.cuda.synchronize()
     assert pu.bf16_dev_to_bits(k).tobytes() == orc.kv_commit(kb, L, path).tobytes()
     assert pu.bf16_dev_to_bits(v).tobytes() == orc.kv_commit(vb, L, path).tobytes()
+
+
+@pytest.mark.parametrize("d,path", [(128, [0, 2, 7, 11]), (64, [0, 1, 2, 3]), (128, [0])])
+def test_kv_commit_batched_matches_oracle(d, path):
+    """Every layer in one launch: each layer's caches move exactly as the
+    oracle's commit moves them (overlapping moves, a one-node path)."""
+    import self_speculative_ultra_gb300 as ts
+    rng = np.random.default_rng(10 + d)
+    n_layers, Hkv, L, T = 5, 4, 700, 16
+    kbs = [rng.integers(0, 2 ** 16, size=(Hkv, L + T, d), dtype=np.uint16) for _ in range(n_layers)]
+    vbs = [rng.integers(0, 2 ** 16, size=(Hkv, L + T, d), dtype=np.uint16) for _ in range(n_layers)]
+    ks, vs = [pu.to_dev_bf16(x) for x in kbs], [pu.to_dev_bf16(x) for x in vbs]
+    pdev = pu.to_dev(np.array(path + [0] * (T - len(path)), np.int32))
+    ndev = pu.to_dev(np.array([len(path)], np.int32))
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    ts.ts_kv_commit_batched(ks, vs, L, T, pdev, ndev, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    for i in range(n_layers):
+        assert pu.bf16_dev_to_bits(ks[i]).tobytes() == orc.kv_commit(kbs[i], L, path).tobytes()
+        assert pu.bf16_dev_to_bits(vs[i]).tobytes() == orc.kv_commit(vbs[i], L, path).tobytes()

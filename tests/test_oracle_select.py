@@ -73,3 +73,51 @@ def test_gather_is_a_bitwise_row_copy():
     out = orc.gather_rows(cache, idx)
     for r, j in enumerate(idx):
         assert out[r].tobytes() == cache[j].tobytes()
+
+
+# ---- incremental refresh of the partial cache
+def test_incremental_refresh_hand_worked():
+    # slot 2 (position 5) leaves; positions 7 and 8 join: 7 takes the freed
+    # slot 2, 8 the new slot 5 (the cache grew from 5 to 6 rows)
+    cache = np.arange(20 * 2, dtype=np.float64).reshape(20, 2)
+    prev = [0, 1, 5, 9, 3]
+    compact = np.zeros((6, 2))
+    compact[:5] = cache[prev]
+    slots, out, n = orc.refresh_incremental(prev, [0, 1, 3, 7, 8, 9], cache, compact)
+    assert slots.tolist() == [0, 1, 7, 9, 3, 8] and n == 2
+    np.testing.assert_array_equal(out, cache[[0, 1, 7, 9, 3, 8]])
+
+
+def test_incremental_refresh_from_empty_is_the_full_gather():
+    rng = np.random.default_rng(2)
+    cache = rng.standard_normal((300, 4))
+    imp = rng.standard_normal(300)
+    kept = orc.select_partial(imp, 300, 20, 4, 8)
+    slots, out, n = orc.refresh_incremental([], kept, cache, np.zeros((len(kept), 4)))
+    assert slots.tolist() == kept.tolist() and n == len(kept)
+    np.testing.assert_array_equal(out, orc.gather_rows(cache, kept))
+
+
+def test_incremental_refresh_tracks_the_kept_set_over_steps():
+    """Over a growing cache with drifting importance, the slots always hold
+    exactly the kept set, every slot holds its position's row, and only the
+    rows of newly kept positions are written."""
+    rng = np.random.default_rng(4)
+    S, B, R, d = 4, 40, 16, 3
+    cache = rng.standard_normal((2000, d))
+    base = rng.standard_normal(2000)
+    slots, compact = np.zeros(0, dtype=np.int64), np.zeros((0, d))
+    L = 30
+    for step in range(40):
+        imp = base + 0.3 * rng.standard_normal(2000)      # importance drifts step to step
+        kept = orc.select_partial(imp[:L], L, B, S, R)
+        grown = np.zeros((len(kept), d))
+        grown[:len(compact)] = compact
+        new_slots, compact, n = orc.refresh_incremental(slots, kept, cache, grown)
+        assert sorted(new_slots.tolist()) == kept.tolist()
+        np.testing.assert_array_equal(compact, cache[new_slots])
+        assert n == len(set(kept.tolist()) - set(slots.tolist()))
+        kept_slots = [s for s in range(len(slots)) if slots[s] in set(kept.tolist())]
+        assert all(new_slots[s] == slots[s] for s in kept_slots)   # unchanged slots stay
+        slots = new_slots
+        L += int(rng.integers(1, 5))
