@@ -846,7 +846,10 @@ def run_loop_case(w: syn.Workload, until: int, L0: int = 2048):
     torch.cuda.synchronize()
     launches = [0]
 
+    t_issue = [0.0]
+
     def step(s_, L):
+        t_s = time.perf_counter()
         torch._foreach_copy_([x[:, L:L + T] for x in ks] + [x[:, L:L + T] for x in vs],
                              pool[s_ % 4])
         torch.randn((T, V), generator=g, device=dev, out=logits)
@@ -868,6 +871,7 @@ def run_loop_case(w: syn.Workload, until: int, L0: int = 2048):
         ts._check(lib.ts_kv_commit_batched(nl, crow[0], crow[1], L, L_cap, Hkv, d, T, P(path),
                                            P(n_path), P(status), stream))
         n_path_h.copy_(n_path, non_blocking=True)
+        t_issue[0] += time.perf_counter() - t_s
         torch.cuda.current_stream().synchronize()
         return int(n_path_h.item())
 
@@ -875,6 +879,7 @@ def run_loop_case(w: syn.Workload, until: int, L0: int = 2048):
         step(s_, L0)
     torch.cuda.synchronize()
     L, steps, committed, hist = L0, 0, 0, [0] * (T + 1)
+    t_issue[0] = 0.0
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     t0 = time.perf_counter()
     e0.record()
@@ -897,6 +902,7 @@ def run_loop_case(w: syn.Workload, until: int, L0: int = 2048):
         "mean_accepted_per_step": round(committed / max(steps, 1), 4),
         "accepted_length_histogram": {str(i): c for i, c in enumerate(hist) if c},
         "ms_per_step": round(1e3 * wall / max(steps, 1), 4),
+        "host_issue_ms_per_step": round(1e3 * t_issue[0] / max(steps, 1), 4),
         "device_status": int(status.item()), "dtype": "bf16", "data": "synthetic",
         "config": {"workload": w.name, "layers": nl, "Hq": Hq, "Hkv": Hkv, "d": d,
                    "prefix_L0": L0, "until_L": until, "tree_nodes": T, "B": w.B, "S": w.S,
