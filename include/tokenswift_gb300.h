@@ -278,6 +278,22 @@ int ts_penalized_sample_accept(const float* logits, const int32_t* tree_tokens,
                                void* workspace, size_t workspace_bytes,
                                int32_t* status, void* stream);
 
+/* The same call with flags.  TS_PENALTY_CTRL_LITERAL: the literal CTRL
+ * penalty, every windowed logit divided by `penalty` whatever its sign
+ * (without the flag, non-positive windowed logits are multiplied by it).
+ * Unknown flag bits are rejected (TS_ERR_INVALID_ARG). */
+#define TS_PENALTY_CTRL_LITERAL 1
+int ts_penalized_sample_accept_flags(const float* logits, const int32_t* tree_tokens,
+                                     const int32_t* parents, int T,
+                                     const int32_t* prior, int n_prior, int W, int V,
+                                     float penalty, float temperature,
+                                     float top_p, float min_p,
+                                     const float* uniforms,
+                                     int32_t* sampled, int32_t* path, int32_t* n_path,
+                                     int32_t* bonus,
+                                     void* workspace, size_t workspace_bytes, int flags,
+                                     int32_t* status, void* stream);
+
 /* eta-sampling variant (§D.1, Table 12): the same window, penalty,
  * temperature, draw and acceptance, with the kept set {p >= eta},
  * eta = min(eta_epsilon, eta_alpha * exp(-H)) and H the entropy (nats) of

@@ -253,18 +253,20 @@ def penalty_window(prior, path_tokens, W: int) -> np.ndarray:
     return seq[len(seq) - W:] if W > 0 else seq[:0]
 
 
-def penalised_logits(x, window, penalty: float, temperature: float) -> np.ndarray:
+def penalised_logits(x, window, penalty: float, temperature: float,
+                     literal: bool = False) -> np.ndarray:
     """CTRL-style contextual penalty on the windowed tokens, then temperature.
 
     Each distinct token in the window is penalised once: x/theta if x > 0,
-    x*theta otherwise (§3.4, §4.3.3, Table 11 theta = 1.2); every logit is
+    x*theta otherwise (§3.4, §4.3.3, Table 11 theta = 1.2); with `literal`,
+    the CTRL form as written, x/theta whatever the sign.  Every logit is
     then divided by the temperature.  Formed with fp32 operations, the
     precision the logits arrive in."""
     x = np.asarray(x, dtype=np.float32).copy()
     th = np.float32(penalty)
     for t in np.unique(np.asarray(window, dtype=np.int64)):
         xt = x[t]
-        x[t] = xt / th if xt > 0 else xt * th
+        x[t] = xt / th if (literal or xt > 0) else xt * th
     return (x / np.float32(temperature)).astype(np.float32)
 
 
@@ -309,10 +311,10 @@ def sample_from_logits(x_pen, top_p: float, min_p: float, u: float, return_info:
 
 
 def sample_node(logits_row, prior, path_tokens, W, penalty, temperature, top_p,
-                min_p, u, return_info=False):
+                min_p, u, return_info=False, literal=False):
     """One tree node's draw: window, penalty, temperature, truncation, draw."""
     win = penalty_window(prior, path_tokens, W)
-    xp = penalised_logits(logits_row, win, penalty, temperature)
+    xp = penalised_logits(logits_row, win, penalty, temperature, literal)
     return sample_from_logits(xp, top_p, min_p, u, return_info)
 
 
@@ -402,7 +404,7 @@ def accept_from_samples(parents, tree_tokens, sampled):
 
 
 def sample_accept_sequential(logits, prior, parents, tree_tokens, W, penalty,
-                             temperature, top_p, min_p, uniforms):
+                             temperature, top_p, min_p, uniforms, literal=False):
     """Sequential form of one verification step: starting at the root, sample
     the current node, move to the lowest-index child whose drafted token
     equals that sample, repeat; stop when no child matches.  Only nodes on
@@ -414,7 +416,7 @@ def sample_accept_sequential(logits, prior, parents, tree_tokens, W, penalty,
     node, path, drafted = 0, [0], []
     while True:
         tok = sample_node(logits[node], prior, drafted, W, penalty, temperature,
-                          top_p, min_p, float(uniforms[node]))
+                          top_p, min_p, float(uniforms[node]), literal=literal)
         nxt = [c for c in children[node] if int(tree_tokens[c]) == tok]
         if not nxt:
             return path, tok
@@ -424,7 +426,8 @@ def sample_accept_sequential(logits, prior, parents, tree_tokens, W, penalty,
 
 
 def sample_all_nodes(logits, prior, parents, tree_tokens, W, penalty,
-                     temperature, top_p, min_p, uniforms, return_info=False):
+                     temperature, top_p, min_p, uniforms, return_info=False,
+                     literal=False):
     """Every node's draw (the parallel form's input).  Node i's window holds
     the drafted tokens on its root path, root excluded."""
     paths = root_paths(parents)
@@ -432,7 +435,7 @@ def sample_all_nodes(logits, prior, parents, tree_tokens, W, penalty,
     for i in range(len(parents)):
         drafted = [int(tree_tokens[a]) for a in paths[i][1:]]
         r = sample_node(logits[i], prior, drafted, W, penalty, temperature,
-                        top_p, min_p, float(uniforms[i]), return_info)
+                        top_p, min_p, float(uniforms[i]), return_info, literal)
         if return_info:
             out.append(r[0])
             infos.append(r[1])

@@ -69,6 +69,11 @@ _SIGNATURES = {
                                           _i32, _i32, _f32, _f32, _f32, _f32, _c_void_p,
                                           _c_void_p, _c_void_p, _c_void_p, _c_void_p,
                                           _c_void_p, _sz, _c_void_p, _c_void_p]),
+    "ts_penalized_sample_accept_flags": (_i32, [_c_void_p, _c_void_p, _c_void_p, _i32, _c_void_p,
+                                                _i32, _i32, _i32, _f32, _f32, _f32, _f32,
+                                                _c_void_p, _c_void_p, _c_void_p, _c_void_p,
+                                                _c_void_p, _c_void_p, _sz, _i32, _c_void_p,
+                                                _c_void_p]),
     "ts_penalized_sample_accept_eta": (_i32, [_c_void_p, _c_void_p, _c_void_p, _i32, _c_void_p,
                                               _i32, _i32, _i32, _f32, _f32, _f32, _f32,
                                               _c_void_p, _c_void_p, _c_void_p, _c_void_p,
@@ -354,10 +359,15 @@ def ts_sample_workspace_bytes(T, V) -> int:
     return lib().ts_sample_workspace_bytes(T, V)
 
 
+TS_PENALTY_CTRL_LITERAL = 1
+
+
 def ts_penalized_sample_accept(logits, tree_tokens, parents, prior, W, penalty, temperature,
                                top_p, min_p, uniforms, sampled=None, path=None, n_path=None,
-                               bonus=None, workspace=None, status=None, stream=None):
-    """Penalised top-p/min-p draw at every node + exact-match acceptance.
+                               bonus=None, workspace=None, status=None, stream=None,
+                               literal=False):
+    """Penalised top-p/min-p draw at every node + exact-match acceptance
+    (literal=True: the literal CTRL penalty, every windowed logit divided).
     Returns (sampled [T], path [T], n_path [1], bonus [1]) device int32."""
     T, V = logits.shape
     _dev(logits, torch.float32, "logits")
@@ -372,11 +382,11 @@ def ts_penalized_sample_accept(logits, tree_tokens, parents, prior, W, penalty, 
     n_path = mk(1) if n_path is None else n_path
     bonus = mk(1) if bonus is None else bonus
     ws, nb = _workspace(ts_sample_workspace_bytes(T, V), dev, workspace)
-    rc = lib().ts_penalized_sample_accept(_ptr(logits), _ptr(tree_tokens), _ptr(parents), T,
-                                          _ptr(prior), prior.numel(), W, V, penalty, temperature,
-                                          top_p, min_p, _ptr(uniforms), _ptr(sampled), _ptr(path),
-                                          _ptr(n_path), _ptr(bonus), _ptr(ws), nb, _ptr(status),
-                                          _stream(stream))
+    rc = lib().ts_penalized_sample_accept_flags(
+        _ptr(logits), _ptr(tree_tokens), _ptr(parents), T, _ptr(prior), prior.numel(), W, V,
+        penalty, temperature, top_p, min_p, _ptr(uniforms), _ptr(sampled), _ptr(path),
+        _ptr(n_path), _ptr(bonus), _ptr(ws), nb, TS_PENALTY_CTRL_LITERAL if literal else 0,
+        _ptr(status), _stream(stream))
     _check(rc)
     return sampled, path, n_path, bonus
 

@@ -258,11 +258,15 @@ __global__ void __launch_bounds__(kThreads, 2)
 sample_accept_kernel(const float* __restrict__ logits, const int32_t* __restrict__ tree_tokens,
                      const int32_t* __restrict__ parents, int T, const int32_t* __restrict__ prior,
                      int n_prior, int W, int V, float penalty, float temperature, float top_p,
-                     float min_p, int eta_mode, float eta_eps, float eta_alpha,
+                     float min_p, int mode, float eta_eps, float eta_alpha,
                      const float* __restrict__ uniforms, int32_t* sampled,
                      int32_t* __restrict__ path, int32_t* __restrict__ n_path,
                      int32_t* __restrict__ bonus, SampleWs ws, int32_t* status) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
+  // mode bit 0: eta-sampling pool instead of top-p / min-p; bit 1: literal
+  // CTRL penalty (every windowed logit divided by the penalty)
+  const bool eta_mode = (mode & 1) != 0;
+  const bool literal = (mode & 2) != 0;
   SampleSmem& sm = *reinterpret_cast<SampleSmem*>(smem_raw);
   uint32_t* bitmap = reinterpret_cast<uint32_t*>(smem_raw + sizeof(SampleSmem));
   const int part = blockIdx.x, i = blockIdx.y, tid = threadIdx.x;
@@ -319,7 +323,8 @@ sample_accept_kernel(const float* __restrict__ logits, const int32_t* __restrict
   float* xs = ws.xs + (size_t)i * V;
   const bool unit_temp = temperature == 1.0f;     // x / 1 is x exactly
   auto xprime = [&](float x, int t) {
-    if ((bitmap[t >> 5] >> (t & 31)) & 1u) x = (x > 0.f) ? __fdiv_rn(x, penalty) : __fmul_rn(x, penalty);
+    if ((bitmap[t >> 5] >> (t & 31)) & 1u)
+      x = (literal || x > 0.f) ? __fdiv_rn(x, penalty) : __fmul_rn(x, penalty);
     if (!unit_temp) x = __fdiv_rn(x, temperature);
     return x;
   };
@@ -702,7 +707,7 @@ size_t sample_ws_bytes(int T, int V) {
 
 int launch_sample_accept(const float* logits, const int32_t* tree_tokens, const int32_t* parents,
                          int T, const int32_t* prior, int n_prior, int W, int V, float penalty,
-                         float temperature, float top_p, float min_p, int eta_mode, float eta_eps,
+                         float temperature, float top_p, float min_p, int mode, float eta_eps,
                          float eta_alpha, const float* uniforms, int32_t* sampled, int32_t* path,
                          int32_t* n_path, int32_t* bonus, void* ws, int32_t* status,
                          cudaStream_t st) {
@@ -713,7 +718,7 @@ int launch_sample_accept(const float* logits, const int32_t* tree_tokens, const 
   cudaFuncSetAttribute(sample_accept_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   sample_accept_kernel<<<dim3(kParts, T), kThreads, smem, st>>>(
       logits, tree_tokens, parents, T, prior, n_prior, W, V, penalty, temperature, top_p, min_p,
-      eta_mode, eta_eps, eta_alpha, uniforms, sampled, path, n_path, bonus, w, status);
+      mode, eta_eps, eta_alpha, uniforms, sampled, path, n_path, bonus, w, status);
   return launch_status("sample_accept_kernel");
 }
 

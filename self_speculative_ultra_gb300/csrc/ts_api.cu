@@ -283,14 +283,16 @@ size_t ts_sample_workspace_bytes(int T, int V) {
   return sample_ws_bytes(T, V);
 }
 
-int ts_penalized_sample_accept(const float* logits, const int32_t* tree_tokens,
-                               const int32_t* parents, int T, const int32_t* prior, int n_prior,
-                               int W, int V, float penalty, float temperature, float top_p,
-                               float min_p, const float* uniforms, int32_t* sampled,
-                               int32_t* path, int32_t* n_path, int32_t* bonus, void* workspace,
-                               size_t workspace_bytes, int32_t* status, void* stream) {
+int ts_penalized_sample_accept_flags(const float* logits, const int32_t* tree_tokens,
+                                     const int32_t* parents, int T, const int32_t* prior,
+                                     int n_prior, int W, int V, float penalty, float temperature,
+                                     float top_p, float min_p, const float* uniforms,
+                                     int32_t* sampled, int32_t* path, int32_t* n_path,
+                                     int32_t* bonus, void* workspace, size_t workspace_bytes,
+                                     int flags, int32_t* status, void* stream) {
   clear_error();
   const char* F = "ts_penalized_sample_accept";
+  if (flags & ~TS_PENALTY_CTRL_LITERAL) return fail(TS_ERR_INVALID_ARG, "%s: unknown flags 0x%x", F, flags);
   if (T < 1) return fail(TS_ERR_INVALID_ARG, "%s: T=%d", F, T);
   if (T > 64) return fail(TS_ERR_UNSUPPORTED, "%s: T=%d > 64", F, T);
   if (V < 1) return fail(TS_ERR_INVALID_ARG, "%s: V=%d", F, V);
@@ -305,9 +307,23 @@ int ts_penalized_sample_accept(const float* logits, const int32_t* tree_tokens,
     return fail(TS_ERR_INVALID_ARG, "%s: NULL tensor", F);
   int rc = check_ws(workspace, workspace_bytes, sample_ws_bytes(T, V), F);
   if (rc) return rc;
+  // kernel mode word: bit 0 eta pool, bit 1 literal penalty
+  const int mode = (flags & TS_PENALTY_CTRL_LITERAL) ? 2 : 0;
   return launch_sample_accept(logits, tree_tokens, parents, T, prior, n_prior, W, V, penalty,
-                              temperature, top_p, min_p, 0, 0.f, 0.f, uniforms, sampled, path,
+                              temperature, top_p, min_p, mode, 0.f, 0.f, uniforms, sampled, path,
                               n_path, bonus, workspace, status, static_cast<cudaStream_t>(stream));
+}
+
+int ts_penalized_sample_accept(const float* logits, const int32_t* tree_tokens,
+                               const int32_t* parents, int T, const int32_t* prior, int n_prior,
+                               int W, int V, float penalty, float temperature, float top_p,
+                               float min_p, const float* uniforms, int32_t* sampled,
+                               int32_t* path, int32_t* n_path, int32_t* bonus, void* workspace,
+                               size_t workspace_bytes, int32_t* status, void* stream) {
+  return ts_penalized_sample_accept_flags(logits, tree_tokens, parents, T, prior, n_prior, W, V,
+                                          penalty, temperature, top_p, min_p, uniforms, sampled,
+                                          path, n_path, bonus, workspace, workspace_bytes, 0,
+                                          status, stream);
 }
 
 int ts_penalized_sample_accept_eta(const float* logits, const int32_t* tree_tokens,

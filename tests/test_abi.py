@@ -108,3 +108,11 @@ def test_importance_softmax_rejects_bad_args(ts):
     assert "shared memory" in ts.ts_last_error()
     # 448 rows fit: the call passes the checks; L = 0 launches nothing
     assert f(p, p, p, 0, 100, 56, 8, 1, 128, 0, p, None, None) == 0
+
+
+def test_sample_flags_reject_unknown_bits(ts):
+    p = ctypes.c_void_p(16)
+    f = _c(ts).ts_penalized_sample_accept_flags
+    assert f(p, p, p, 4, p, 8, 8, 100, 1.2, 1.0, 0.9, 0.05, p, p, p, p, p, p, 1 << 30, 4,
+             None, None) == 1
+    assert "flags" in ts.ts_last_error()

@@ -12,7 +12,7 @@ pytestmark = pytest.mark.gpu
 
 
 def _run(w, step=0, logits=None, prior=None, top_p=None, min_p=None, temperature=None,
-         penalty=None, W=None, tree=None, uniforms=None):
+         penalty=None, W=None, tree=None, uniforms=None, literal=False):
     import self_speculative_ultra_gb300 as ts
     inp = syn.sampling_inputs(w, step=step, tree=tree)
     logits = inp["logits"] if logits is None else logits
@@ -27,7 +27,7 @@ def _run(w, step=0, logits=None, prior=None, top_p=None, min_p=None, temperature
     sampled, path, n_path, bonus = ts.ts_penalized_sample_accept(
         pu.to_dev(logits), pu.to_dev(inp["tokens"]), pu.to_dev(inp["parents"]),
         pu.to_dev(np.asarray(prior, np.int32)), W, penalty, temperature, top_p, min_p,
-        pu.to_dev(u), status=status)
+        pu.to_dev(u), status=status, literal=literal)
     torch.cuda.synchronize()
     assert int(status.item()) == 0
     sampled = sampled.cpu().numpy()
@@ -35,7 +35,8 @@ def _run(w, step=0, logits=None, prior=None, top_p=None, min_p=None, temperature
     path = path.cpu().numpy()[:n].tolist()
     bonus = int(bonus.item())
     ref, infos = orc.sample_all_nodes(logits, prior, inp["parents"], inp["tokens"], W, penalty,
-                                      temperature, top_p, min_p, u, return_info=True)
+                                      temperature, top_p, min_p, u, return_info=True,
+                                      literal=literal)
     ties = 0
     for i in range(len(ref)):
         if sampled[i] != ref[i]:
@@ -47,7 +48,8 @@ def _run(w, step=0, logits=None, prior=None, top_p=None, min_p=None, temperature
     assert path == p_ref and bonus == b_ref
     if ties == 0:
         assert (path, bonus) == orc.sample_accept_sequential(
-            logits, prior, inp["parents"], inp["tokens"], W, penalty, temperature, top_p, min_p, u)
+            logits, prior, inp["parents"], inp["tokens"], W, penalty, temperature, top_p, min_p, u,
+            literal=literal)
     return sampled, path, bonus, ties
 
 
@@ -135,3 +137,11 @@ def test_kv_commit_batched_matches_oracle(d, path):
     for i in range(n_layers):
         assert pu.bf16_dev_to_bits(ks[i]).tobytes() == orc.kv_commit(kbs[i], L, path).tobytes()
         assert pu.bf16_dev_to_bits(vs[i]).tobytes() == orc.kv_commit(vbs[i], L, path).tobytes()
+
+
+@pytest.mark.parametrize("name", ["tiny", "llama3.1-8b", "qwen2.5-14b"])
+def test_literal_ctrl_penalty(name):
+    """The literal CTRL penalty (flag TS_PENALTY_CTRL_LITERAL) against the
+    oracle's literal form, with a strong penalty so that negative windowed
+    logits move visibly."""
+    _run(syn.WORKLOADS[name], step=3, penalty=3.0, literal=True)

@@ -187,3 +187,31 @@ def test_eta_zero_epsilon_is_plain_categorical():
     for u in rng.random(50):
         ref = int(order[int(np.argmax(c > u))])
         assert orc.sample_from_logits_eta(x, 0.0, 0.0, u) == ref
+
+
+def test_literal_ctrl_penalty_divides_every_windowed_logit():
+    """The literal CTRL form divides a windowed logit by theta whatever its
+    sign: a negative logit moves toward zero (its token becomes MORE likely,
+    the reason the sign-aware form is the default), zero stays zero."""
+    x = np.array([2.0, -2.0, 0.0, 1.0], dtype=np.float32)
+    xp = orc.penalised_logits(x, [0, 0, 1, 2], 1.2, 1.0, literal=True)
+    assert abs(xp[0] - 2 / 1.2) < 1e-6 and abs(xp[1] + 2 / 1.2) < 1e-6
+    assert xp[2] == 0.0 and xp[3] == 1.0
+    # with every windowed logit positive the two forms agree
+    y = np.array([0.5, 3.0, -1.0, 2.0], dtype=np.float32)
+    np.testing.assert_array_equal(orc.penalised_logits(y, [0, 1, 3], 1.2, 0.7, literal=True),
+                                  orc.penalised_logits(y, [0, 1, 3], 1.2, 0.7))
+
+
+def test_literal_penalty_hand_worked_draw():
+    """V = 3, logits [ln 2, -ln 2 * 1.2, 0], window {1}, theta 1.2, literal:
+    x' = [ln 2, -ln 2, 0] so p = [2, 1/2, 1] / 3.5; with top_p = 1, min_p = 0
+    the ranked order is (0, 2, 1) with cumulative [4/7, 6/7, 1]: u = 0.5 draws
+    token 0, u = 0.6 token 2, u = 0.88 token 1.  The sign-aware form gives
+    x'[1] = -1.44 ln 2 instead: p = [2, 2^-1.44, 1] / (3 + 2^-1.44), cumulative
+    [0.594, 0.891, 1], so u = 0.88 draws token 2 there."""
+    ln2 = math.log(2)
+    x = np.array([ln2, -ln2 * 1.2, 0.0], dtype=np.float32)
+    for u, tok in ((0.5, 0), (0.6, 2), (0.88, 1)):
+        assert orc.sample_node(x, [1], [], 1, 1.2, 1.0, 1.0, 0.0, u, literal=True) == tok
+    assert orc.sample_node(x, [1], [], 1, 1.2, 1.0, 1.0, 0.0, 0.88) == 2
