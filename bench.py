@@ -233,8 +233,11 @@ class Step:
         self.prior = torch.from_numpy(sin["prior"]).to(dev)
         self.uniforms = torch.from_numpy(sin["uniforms"]).to(dev)
         i32 = dict(dtype=torch.int32, device=dev)
-        self.sampled, self.path = torch.empty(T, **i32), torch.empty(T, **i32)
-        self.n_path, self.bonus = torch.empty(1, **i32), torch.empty(1, **i32)
+        self.sampled = torch.empty(T, **i32)
+        # path | n_path | bonus in one buffer, so the per-step readback is one copy
+        self.result = torch.empty(T + 2, **i32)
+        self.path, self.n_path, self.bonus = (self.result[:T], self.result[T:T + 1],
+                                              self.result[T + 1:T + 2])
         self.status = torch.zeros(1, **i32)
         u8 = dict(dtype=torch.uint8, device=dev)
         self.ws_v = torch.empty(max(ts.ts_verify_workspace_bytes(T, Hq, Hkv, d, L), 256), **u8)
@@ -242,76 +245,100 @@ class Step:
         self.sel_table = ts.layer_pointer_table(self.imp, self.k, self.v, self.idx, self.kd, self.vd)
         self.commit_table = ts.commit_pointer_table(self.k, self.v)
         self.ws_p = torch.empty(max(ts.ts_sample_workspace_bytes(T, w.V), 256), **u8)
-        # end-to-end leg: the per-step inputs live in one pinned host buffer
-        # (uploaded with a single copy) and are unpacked on the device by a
-        # multi-tensor copy into their places (queries, the tree's K/V rows
-        # inside every layer's cache, logits, tree, window, uniforms)
-        tree_rows = lambda x: x[:, L:L + T]  # noqa: E731
-        self.e2e_dst = (list(self.q) + [tree_rows(x) for x in self.k] +
-                        [tree_rows(x) for x in self.v] +
-                        [self.logits, self.parents, self.tokens, self.prior, self.uniforms])
-        offs, off = [], 0
-        for t in self.e2e_dst:
-            offs.append(off)
-            off += (t.numel() * t.element_size() + 255) // 256 * 256
+        # end-to-end leg: the per-step inputs live in one pinned host buffer,
+        # uploaded with a single copy into one of two device staging buffers.
+        # The step reads queries, logits, tree, window and uniforms in place
+        # there; only the tree's K/V rows move, into every layer's cache, by
+        # one batched append.
+        nl = w.layers
+        spec = [("q", (nl, T, Hq, d), torch.bfloat16), ("k_rows", (nl, Hkv, T, d), torch.bfloat16),
+                ("v_rows", (nl, Hkv, T, d), torch.bfloat16), ("logits", (T, w.V), torch.float32),
+                ("parents", (T,), torch.int32), ("tokens", (T,), torch.int32),
+                ("prior", tuple(self.prior.shape), torch.int32), ("uniforms", (T,), torch.float32)]
+        offs, off = {}, 0
+        for name, shape, dt in spec:
+            offs[name] = off
+            off += (int(np.prod(shape)) * torch.empty(0, dtype=dt).element_size() + 255) // 256 * 256
         self.h_stage = torch.empty(off, dtype=torch.uint8).pin_memory()
-        # two device staging buffers: step s+1's upload (on a copy stream)
-        # overlaps step s's kernels
         self.d_stage = [torch.empty(off, dtype=torch.uint8, device=dev) for _ in range(2)]
         self.copy_stream = torch.cuda.Stream(device=dev)
         self.staged = [torch.cuda.Event() for _ in range(2)]
-        self.unpacked = [torch.cuda.Event() for _ in range(2)]
+        self.consumed = [torch.cuda.Event() for _ in range(2)]
 
-        def view(buf, o, t):
-            n = t.numel() * t.element_size()
-            return buf[o:o + n].view(t.dtype).view(t.shape)
-        self.e2e_src = [[view(b, o, t) for o, t in zip(offs, self.e2e_dst)] for b in self.d_stage]
-        for o, t in zip(offs, self.e2e_dst):
-            view(self.h_stage, o, t).copy_(t.cpu())
+        def views(buf):
+            out = {}
+            for name, shape, dt in spec:
+                n = int(np.prod(shape)) * torch.empty(0, dtype=dt).element_size()
+                out[name] = buf[offs[name]:offs[name] + n].view(dt).view(shape)
+            return out
+        self.stage_views = [views(b) for b in self.d_stage]
+        hv = views(self.h_stage)
+        hv["q"].copy_(torch.stack(self.q).cpu())
+        hv["k_rows"].copy_(torch.stack([x[:, L:L + T] for x in self.k]).cpu())
+        hv["v_rows"].copy_(torch.stack([x[:, L:L + T] for x in self.v]).cpu())
+        for name in ("logits", "parents", "tokens", "prior", "uniforms"):
+            hv[name].copy_(getattr(self, name).cpu())
+        self.h_bytes = sum(int(np.prod(sh)) * torch.empty(0, dtype=dt).element_size()
+                           for _, sh, dt in spec)
         self.h_out = torch.empty(T + 2, dtype=torch.int32).pin_memory()
         self.v_events = None
         torch.cuda.synchronize()
 
     def h2d_bytes(self) -> int:
-        return sum(t.numel() * t.element_size() for t in self.e2e_dst)
+        return self.h_bytes
 
     def d2h_bytes(self) -> int:
         return self.h_out.numel() * 4
 
     def stage_inputs(self, s: int, after=None):
         """Upload step s's inputs from pinned host memory into staging
-        buffer s % 2 on the copy stream (after `after`, and after that
-        buffer's previous unpack)."""
+        buffer s % 2 on the copy stream (after `after`, and after the step
+        that last read that buffer)."""
         torch, b = self.torch, s % 2
         with torch.cuda.stream(self.copy_stream):
             if after is not None:
                 self.copy_stream.wait_event(after)
             if s >= 2:
-                self.copy_stream.wait_event(self.unpacked[b])
+                self.copy_stream.wait_event(self.consumed[b])
             self.d_stage[b].copy_(self.h_stage, non_blocking=True)
             self.staged[b].record(self.copy_stream)
 
     def unpack_inputs(self, s: int):
+        """Wait for step s's upload and append its tree K/V rows to every
+        layer's cache; returns the step's input views."""
         b = s % 2
         self.torch.cuda.current_stream().wait_event(self.staged[b])
-        self.torch._foreach_copy_(self.e2e_dst, self.e2e_src[b])
-        self.unpacked[b].record()
+        v = self.stage_views[b]
+        self.ts.ts_kv_append_batched(self.k, self.v, v["k_rows"], v["v_rows"], self.L,
+                                     table=self.commit_table)
+        return v
+
+    def release_inputs(self, s: int):
+        self.consumed[s % 2].record()
 
     def upload_inputs(self, s: int = 0):
         self.stage_inputs(s)
-        self.unpack_inputs(s)
+        return self.unpack_inputs(s)
 
     def download_result(self):
-        self.h_out[:self.w.T].copy_(self.path, non_blocking=True)
-        self.h_out[self.w.T:self.w.T + 1].copy_(self.n_path, non_blocking=True)
-        self.h_out[self.w.T + 1:].copy_(self.bonus, non_blocking=True)
+        self.h_out.copy_(self.result, non_blocking=True)
 
-    def step(self, events=None):
+    def step(self, events=None, inp=None):
+        """One pass of the hot path.  `inp` holds the step's inputs (q per
+        layer, logits, parents, tokens, prior, uniforms); default: the
+        resident copies."""
         ts, w = self.ts, self.w
+        if inp is None:
+            q, logits, parents, tokens, prior, uniforms = (self.q, self.logits, self.parents,
+                                                           self.tokens, self.prior, self.uniforms)
+        else:
+            q, logits, parents, tokens, prior, uniforms = (inp["q"], inp["logits"], inp["parents"],
+                                                           inp["tokens"], inp["prior"],
+                                                           inp["uniforms"])
         for layer in range(w.layers):
             if events is not None:
                 events[layer][0].record()
-            ts.ts_verify_attention(self.q[layer], self.k[layer], self.v[layer], self.L, self.parents,
+            ts.ts_verify_attention(q[layer], self.k[layer], self.v[layer], self.L, parents,
                                    n_imp=w.n_imp, o=self.o[layer], lse=self.lse[layer],
                                    imp=self.imp[layer], workspace=self.ws_v, status=self.status)
             if events is not None:
@@ -321,8 +348,8 @@ class Step:
         ts.ts_partial_kv_select_gather_batched(self.imp, self.k, self.v, self.L, w.B, w.S, w.R,
                                                self.idx, self.kd, self.vd, table=self.sel_table,
                                                workspace=self.ws_s, status=self.status)
-        ts.ts_penalized_sample_accept(self.logits, self.tokens, self.parents, self.prior, w.W,
-                                      w.penalty, w.temperature, w.top_p, w.min_p, self.uniforms,
+        ts.ts_penalized_sample_accept(logits, tokens, parents, prior, w.W,
+                                      w.penalty, w.temperature, w.top_p, w.min_p, uniforms,
                                       sampled=self.sampled, path=self.path, n_path=self.n_path,
                                       bonus=self.bonus, workspace=self.ws_p, status=self.status)
         ts.ts_kv_commit_batched(self.k, self.v, self.L, w.T, self.path, self.n_path,
@@ -356,22 +383,27 @@ def run_gpu(args, w: syn.Workload):
     for _ in range(args.warmup):
         st.step()
     barrier()
-    # device-timed region: inputs resident in HBM
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(w.layers)]
+    # device-timed region: inputs resident in HBM.  Per-call verify events are
+    # recorded in the last n_ev timed steps only: an event between two
+    # programmatic-dependent launches holds the next one back.
+    n_ev = min(3, args.steps)
+    ev = [[[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(w.layers)]
+          for _ in range(n_ev)]
     clocks = ClockSampler(local)
     clocks.start()
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
     barrier()
     t0.record()
-    for _ in range(args.steps):
-        st.step(events=ev)      # the last step's per-layer verify events are read below
+    for s_ in range(args.steps):
+        k_ev = s_ - (args.steps - n_ev)
+        st.step(events=ev[k_ev] if k_ev >= 0 else None)
     t1.record()
     barrier()
     clk = clocks.stop()
     ms_total = t0.elapsed_time(t1)
-    # verify-call durations of the last timed step (events are re-recorded each step)
-    ver_ms = [ev[i][0].elapsed_time(ev[i][1]) for i in range(w.layers)]
+    # verify-call durations over the last n_ev timed steps
+    ver_ms = [e[i][0].elapsed_time(e[i][1]) for e in ev for i in range(w.layers)]
     ms = torch.tensor([ms_total], device=dev)
     if world > 1:
         dist.all_reduce(ms, op=dist.ReduceOp.MAX)
@@ -379,23 +411,32 @@ def run_gpu(args, w: syn.Workload):
 
     # end-to-end leg: pinned host inputs in, result out, every step
     for i in range(2):
-        st.upload_inputs(i)
-        st.step()
+        st.step(inp=st.upload_inputs(i))
+        st.release_inputs(i)
         st.download_result()
     barrier()
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
+    # per-step phase events on the compute stream: unpack | step | readback
+    ph = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
     e0.record()
     st.stage_inputs(0, after=e0)
     for s_ in range(args.steps):
         if s_ + 1 < args.steps:
             st.stage_inputs(s_ + 1)
-        st.unpack_inputs(s_)
-        st.step()
+        ph[s_][0].record()
+        inp = st.unpack_inputs(s_)
+        ph[s_][1].record()
+        st.step(inp=inp)
+        st.release_inputs(s_)
+        ph[s_][2].record()
         st.download_result()
+        ph[s_][3].record()
     e1.record()
     barrier()
     e2e_ms = torch.tensor([e0.elapsed_time(e1) / args.steps], device=dev)
+    phase_ms = [sum(ph[i][k].elapsed_time(ph[i][k + 1]) for i in range(args.steps)) / args.steps
+                for k in range(3)]
     if world > 1:
         dist.all_reduce(e2e_ms, op=dist.ReduceOp.MAX)
     e2e_ms = float(e2e_ms.item())
@@ -435,7 +476,9 @@ def run_gpu(args, w: syn.Workload):
                                     "flops_per_call": verify_flops(w), "peak_source": tf_kind}},
             "e2e": {"value": round(world * sb / (e2e_ms * 1e-3) / 1e9, 2), "unit": UNIT,
                     "h2d_bytes_per_step": st.h2d_bytes(), "d2h_bytes_per_step": st.d2h_bytes(),
-                    "ms_per_step": round(e2e_ms, 4)},
+                    "ms_per_step": round(e2e_ms, 4),
+                    "phase_ms": {"unpack": round(phase_ms[0], 4), "step": round(phase_ms[1], 4),
+                                 "readback": round(phase_ms[2], 4)}},
             "gpu_launches": st.launches_per_step() * args.steps,
             "clocks": clk,
             "device_status": status,
@@ -779,8 +822,9 @@ def run_ngram_case(w: syn.Workload, steps: int, warmup: int):
 
 def run_loop_case(w: syn.Workload, until: int, L0: int = 2048):
     """A whole generation loop on synthetic tokens: from a prefix of L0
-    cached tokens until the cache holds `until` tokens.  Every step appends
-    the draft tree's fresh N(0,1) K/V rows to every layer's cache, verifies
+    cached tokens until the cache holds `until` tokens.  Every step draws the
+    draft tree's fresh N(0,1) K/V rows, appends them to every layer's cache
+    (one batched launch), verifies
     every layer (importance on), refreshes every layer's partial cache,
     draws fresh N(0, 3^2) logits in which each node's first child's token is
     raised by 30 with probability 0.7 (about 2.5 committed tokens per step),
@@ -801,9 +845,10 @@ def run_loop_case(w: syn.Workload, until: int, L0: int = 2048):
     ks = [torch.empty((Hkv, L_cap, d), **bf).normal_(generator=g) for _ in range(nl)]
     vs = [torch.empty((Hkv, L_cap, d), **bf).normal_(generator=g) for _ in range(nl)]
     qs = [torch.empty((T, Hq, d), **bf).normal_(generator=g) for _ in range(nl)]
-    # fresh tree K/V per step: rows drawn from a pool of 4 variants per layer
-    pool = [[torch.empty((Hkv, T, d), **bf).normal_(generator=g) for _ in range(2 * nl)]
-            for _ in range(4)]
+    # fresh N(0,1) tree K/V rows every step, drawn on the device and written
+    # into every layer's cache by one batched append
+    rows_f32 = torch.empty((2, nl, Hkv, T, d), dtype=torch.float32, device=dev)
+    rows = torch.empty((2, nl, Hkv, T, d), **bf)
     parents_np, tokens_np = syn.make_tree(w, np.random.default_rng(w.seed))
     parents = torch.from_numpy(np.asarray(parents_np, np.int32)).to(dev)
     tokens = torch.from_numpy(np.asarray(tokens_np, np.int32)).to(dev)
@@ -850,8 +895,10 @@ def run_loop_case(w: syn.Workload, until: int, L0: int = 2048):
 
     def step(s_, L):
         t_s = time.perf_counter()
-        torch._foreach_copy_([x[:, L:L + T] for x in ks] + [x[:, L:L + T] for x in vs],
-                             pool[s_ % 4])
+        torch.randn(rows_f32.shape, generator=g, device=dev, out=rows_f32)
+        rows.copy_(rows_f32)
+        ts._check(lib.ts_kv_append_batched(nl, crow[0], crow[1], P(rows[0]), P(rows[1]), L, L_cap,
+                                           Hkv, d, T, stream))
         torch.randn((T, V), generator=g, device=dev, out=logits)
         logits.mul_(3.0)
         plant = (torch.rand(T, generator=g, device=dev) < 0.7) & has_fc

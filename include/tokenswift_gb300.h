@@ -330,6 +330,16 @@ int ts_kv_commit_batched(int n_layers, void* const* k, void* const* v, int64_t L
                          int64_t L_cap, int Hkv, int d, int T, const int32_t* path,
                          const int32_t* n_path, int32_t* status, void* stream);
 
+/* The draft tree's own K/V rows written into every layer's cache (what the
+ * verification forward produces for the tree tokens, §3.1): rows [L, L+T)
+ * of KV head kv of layer l are set from k_rows / v_rows
+ * [n_layers][Hkv][T][d] bf16 (device, 16-byte aligned, packed).  k and v
+ * are device arrays of n_layers cache pointers as in ts_kv_commit_batched.
+ * L + T <= L_cap.  One launch; the copies are bit for bit. */
+int ts_kv_append_batched(int n_layers, void* const* k, void* const* v,
+                         const void* k_rows, const void* v_rows, int64_t L,
+                         int64_t L_cap, int Hkv, int d, int T, void* stream);
+
 /* ------------------------------------------------------------------------
  * (5) Token reutilization: the 4-gram table and the draft-tree builder.
  *

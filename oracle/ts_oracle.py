@@ -448,6 +448,16 @@ def sample_all_nodes(logits, prior, parents, tree_tokens, W, penalty,
 # --------------------------------------------------------------------------
 # (a8) KV commit of the accepted path
 # --------------------------------------------------------------------------
+def kv_append(cache, L: int, rows) -> np.ndarray:
+    """The tree tokens' own K (or V) rows written by the verification forward
+    (§3.1): rows [L, L+T) of every head take rows[h, 0:T].  cache
+    [Hkv, L_cap, d]; rows [Hkv, T, d]; returns the updated copy."""
+    out = np.array(cache, copy=True)
+    rows = np.asarray(rows)
+    out[:, L:L + rows.shape[1]] = rows
+    return out
+
+
 def kv_commit(cache, L: int, path) -> np.ndarray:
     """After acceptance the cache update (§3.1) keeps the accepted tree rows:
     row L+path[t] moves to row L+t for t = 1..len(path)-1 (the root's row is

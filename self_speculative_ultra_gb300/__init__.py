@@ -23,7 +23,7 @@ __all__ = [
     "ts_refresh_workspace_bytes", "ts_partial_kv_refresh_incremental",
     "ts_partial_kv_refresh_incremental_batched",
     "ts_sample_workspace_bytes", "ts_penalized_sample_accept", "ts_kv_commit",
-    "ts_kv_commit_batched", "commit_pointer_table",
+    "ts_kv_commit_batched", "commit_pointer_table", "ts_kv_append_batched",
 ]
 
 TS_OK, TS_ERR_INVALID_ARG, TS_ERR_UNSUPPORTED, TS_ERR_CUDA, TS_ERR_TIMEOUT, TS_ERR_WORKSPACE = range(6)
@@ -83,6 +83,8 @@ _SIGNATURES = {
     "ts_ngram_table_bytes": (_sz, [_i32, _i32]),
     "ts_kv_commit_batched": (_i32, [_i32, _c_void_p, _c_void_p, _i64, _i64, _i32, _i32, _i32,
                                     _c_void_p, _c_void_p, _c_void_p, _c_void_p]),
+    "ts_kv_append_batched": (_i32, [_i32, _c_void_p, _c_void_p, _c_void_p, _c_void_p, _i64, _i64,
+                                    _i32, _i32, _i32, _c_void_p]),
     "ts_ngram_insert": (_i32, [_c_void_p, _i32, _i32, _c_void_p, _i32, _i32, _c_void_p,
                                _c_void_p]),
     "ts_ngram_build_tree": (_i32, [_c_void_p, _i32, _i32, _c_void_p, _c_void_p, _i32, _i32, _i32,
@@ -451,6 +453,24 @@ def ts_kv_commit_batched(ks, vs, L, T, path, n_path, table=None, status=None, st
     rc = lib().ts_kv_commit_batched(len(ks), ctypes.c_void_p(table[0].data_ptr()),
                                     ctypes.c_void_p(table[1].data_ptr()), L, L_cap, Hkv, d, T,
                                     _ptr(path), _ptr(n_path), _ptr(status), _stream(stream))
+    _check(rc)
+
+
+def ts_kv_append_batched(ks, vs, k_rows, v_rows, L, table=None, stream=None):
+    """Write the tree's K/V rows [L, L+T) into every layer's cache in one
+    launch.  k_rows, v_rows [n_layers, Hkv, T, d] bf16 (contiguous)."""
+    Hkv, L_cap, d = ks[0].shape
+    n, T = len(ks), k_rows.shape[2]
+    _dev(k_rows, torch.bfloat16, "k_rows", (n, Hkv, T, d))
+    _dev(v_rows, torch.bfloat16, "v_rows", (n, Hkv, T, d))
+    for x, y in zip(ks, vs):
+        _dev(x, torch.bfloat16, "k", (Hkv, L_cap, d))
+        _dev(y, torch.bfloat16, "v", (Hkv, L_cap, d))
+    if table is None:
+        table = commit_pointer_table(ks, vs)
+    rc = lib().ts_kv_append_batched(n, ctypes.c_void_p(table[0].data_ptr()),
+                                    ctypes.c_void_p(table[1].data_ptr()), _ptr(k_rows),
+                                    _ptr(v_rows), L, L_cap, Hkv, d, T, _stream(stream))
     _check(rc)
 
 

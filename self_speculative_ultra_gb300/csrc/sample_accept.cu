@@ -698,6 +698,28 @@ __global__ void kv_commit_batched_kernel(__nv_bfloat16* const* __restrict__ ks,
   commit_head<D>(ks[blockIdx.y], vs[blockIdx.y], blockIdx.x, L, L_cap, T, path, n_path, status);
 }
 
+// The draft tree's own K/V rows into every layer's cache: rows [L, L+T) of
+// KV head kv of layer l come from the packed arrays [n_layers][Hkv][T][D].
+// CTA (KV head, layer); 16-byte copies (rows are 128 or 256 bytes).
+template <int D>
+__global__ void kv_append_batched_kernel(__nv_bfloat16* const* __restrict__ ks,
+                                         __nv_bfloat16* const* __restrict__ vs,
+                                         const __nv_bfloat16* __restrict__ krows,
+                                         const __nv_bfloat16* __restrict__ vrows, int64_t L,
+                                         int64_t L_cap, int T) {
+  constexpr int V16 = D / 8;
+  const int kv = blockIdx.x, layer = blockIdx.y, Hkv = gridDim.x;
+  const size_t src = ((size_t)layer * Hkv + kv) * T * V16;
+  const uint4* ksrc = reinterpret_cast<const uint4*>(krows) + src;
+  const uint4* vsrc = reinterpret_cast<const uint4*>(vrows) + src;
+  uint4* kdst = reinterpret_cast<uint4*>(ks[layer] + ((size_t)kv * L_cap + L) * D);
+  uint4* vdst = reinterpret_cast<uint4*>(vs[layer] + ((size_t)kv * L_cap + L) * D);
+  for (int e = threadIdx.x; e < T * V16; e += blockDim.x) {
+    kdst[e] = ksrc[e];
+    vdst[e] = vsrc[e];
+  }
+}
+
 }  // namespace
 
 size_t sample_ws_bytes(int T, int V) {
@@ -745,6 +767,21 @@ int launch_kv_commit_batched(int n_layers, void* const* k, void* const* v, int64
   else
     kv_commit_batched_kernel<64><<<grid, 256, 0, st>>>(kb, vb, L, L_cap, T, path, n_path, status);
   return launch_status("kv_commit_batched_kernel");
+}
+
+int launch_kv_append_batched(int n_layers, void* const* k, void* const* v, const void* krows,
+                             const void* vrows, int64_t L, int64_t L_cap, int Hkv, int d, int T,
+                             cudaStream_t st) {
+  auto kb = reinterpret_cast<__nv_bfloat16* const*>(k);
+  auto vb = reinterpret_cast<__nv_bfloat16* const*>(v);
+  auto kr = static_cast<const __nv_bfloat16*>(krows);
+  auto vr = static_cast<const __nv_bfloat16*>(vrows);
+  dim3 grid(Hkv, n_layers);
+  if (d == 128)
+    kv_append_batched_kernel<128><<<grid, 256, 0, st>>>(kb, vb, kr, vr, L, L_cap, T);
+  else
+    kv_append_batched_kernel<64><<<grid, 256, 0, st>>>(kb, vb, kr, vr, L, L_cap, T);
+  return launch_status("kv_append_batched_kernel");
 }
 
 }  // namespace ts

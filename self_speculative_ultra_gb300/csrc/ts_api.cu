@@ -52,6 +52,10 @@ int launch_kv_commit_batched(int n_layers, void* const* k, void* const* v, int64
                              int64_t L_cap, int Hkv, int d, int T, const int32_t* path,
                              const int32_t* n_path, int32_t* status, cudaStream_t st);
 
+int launch_kv_append_batched(int n_layers, void* const* k, void* const* v, const void* krows,
+                             const void* vrows, int64_t L, int64_t L_cap, int Hkv, int d, int T,
+                             cudaStream_t st);
+
 }  // namespace ts
 
 using namespace ts;
@@ -380,6 +384,23 @@ int ts_kv_commit_batched(int n_layers, void* const* k, void* const* v, int64_t L
   if (L < 0 || L + T > L_cap) return fail(TS_ERR_INVALID_ARG, "%s: need L+T <= L_cap", F);
   if (!k || !v || !path || !n_path) return fail(TS_ERR_INVALID_ARG, "%s: NULL array", F);
   return launch_kv_commit_batched(n_layers, k, v, L, L_cap, Hkv, d, T, path, n_path, status,
+                                  static_cast<cudaStream_t>(stream));
+}
+
+int ts_kv_append_batched(int n_layers, void* const* k, void* const* v, const void* k_rows,
+                         const void* v_rows, int64_t L, int64_t L_cap, int Hkv, int d, int T,
+                         void* stream) {
+  clear_error();
+  const char* F = "ts_kv_append_batched";
+  if (n_layers < 1 || n_layers > 65535) return fail(TS_ERR_INVALID_ARG, "%s: n_layers=%d", F, n_layers);
+  if (Hkv < 1 || T < 1) return fail(TS_ERR_INVALID_ARG, "%s: Hkv, T must be >= 1", F);
+  if (T > 64) return fail(TS_ERR_UNSUPPORTED, "%s: T=%d > 64", F, T);
+  if (d != 64 && d != 128) return fail(TS_ERR_UNSUPPORTED, "%s: head dim %d", F, d);
+  if (L < 0 || L + T > L_cap) return fail(TS_ERR_INVALID_ARG, "%s: need L+T <= L_cap", F);
+  if (!k || !v || !k_rows || !v_rows) return fail(TS_ERR_INVALID_ARG, "%s: NULL array", F);
+  if ((reinterpret_cast<uintptr_t>(k_rows) | reinterpret_cast<uintptr_t>(v_rows)) & 15)
+    return fail(TS_ERR_INVALID_ARG, "%s: k_rows and v_rows must be 16-byte aligned", F);
+  return launch_kv_append_batched(n_layers, k, v, k_rows, v_rows, L, L_cap, Hkv, d, T,
                                   static_cast<cudaStream_t>(stream));
 }
 

@@ -145,3 +145,20 @@ def test_literal_ctrl_penalty(name):
     oracle's literal form, with a strong penalty so that negative windowed
     logits move visibly."""
     _run(syn.WORKLOADS[name], step=3, penalty=3.0, literal=True)
+
+
+@pytest.mark.parametrize("d", [128, 64])
+def test_kv_append_batched_matches_oracle(d):
+    import self_speculative_ultra_gb300 as ts
+    rng = np.random.default_rng(20 + d)
+    n_layers, Hkv, L, T = 4, 8, 3000, 64
+    kbs = [rng.integers(0, 2 ** 16, size=(Hkv, L + T + 5, d), dtype=np.uint16) for _ in range(n_layers)]
+    vbs = [rng.integers(0, 2 ** 16, size=(Hkv, L + T + 5, d), dtype=np.uint16) for _ in range(n_layers)]
+    kr = rng.integers(0, 2 ** 16, size=(n_layers, Hkv, T, d), dtype=np.uint16)
+    vr = rng.integers(0, 2 ** 16, size=(n_layers, Hkv, T, d), dtype=np.uint16)
+    ks, vs = [pu.to_dev_bf16(x) for x in kbs], [pu.to_dev_bf16(x) for x in vbs]
+    ts.ts_kv_append_batched(ks, vs, pu.to_dev_bf16(kr), pu.to_dev_bf16(vr), L)
+    torch.cuda.synchronize()
+    for i in range(n_layers):
+        assert pu.bf16_dev_to_bits(ks[i]).tobytes() == orc.kv_append(kbs[i], L, kr[i]).tobytes()
+        assert pu.bf16_dev_to_bits(vs[i]).tobytes() == orc.kv_append(vbs[i], L, vr[i]).tobytes()

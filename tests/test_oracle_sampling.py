@@ -215,3 +215,14 @@ def test_literal_penalty_hand_worked_draw():
     for u, tok in ((0.5, 0), (0.6, 2), (0.88, 1)):
         assert orc.sample_node(x, [1], [], 1, 1.2, 1.0, 1.0, 0.0, u, literal=True) == tok
     assert orc.sample_node(x, [1], [], 1, 1.2, 1.0, 1.0, 0.0, 0.88) == 2
+
+
+def test_kv_append_places_rows_then_commit_moves_them():
+    """Append then commit: the accepted nodes' own rows end at L, L+1, ...
+    (hand-checked on a 1-head cache of 1-element rows)."""
+    cache = np.zeros((1, 10, 1))
+    rows = np.array([[[10.0], [11.0], [12.0], [13.0]]])       # nodes 0..3
+    c = orc.kv_append(cache, 5, rows)
+    assert c[0, :, 0].tolist() == [0, 0, 0, 0, 0, 10, 11, 12, 13, 0]
+    c = orc.kv_commit(c, 5, [0, 2, 3])                         # path root -> 2 -> 3
+    assert c[0, 5:8, 0].tolist() == [10, 12, 13]
