@@ -889,7 +889,6 @@ def run_loop_case(w: syn.Workload, until: int, L0: int = 2048):
     lay = [(P(qs[i]), P(ks[i]), P(vs[i]), P(o[i]), P(lse[i]), P(imp[i])) for i in range(nl)]
     nb_v, nb_s, nb_p = ws_v.numel(), ws_s.numel(), ws_p.numel()
     torch.cuda.synchronize()
-    launches = [0]
 
     t_issue = [0.0]
 
