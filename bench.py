@@ -847,8 +847,8 @@ def run_loop_case(w: syn.Workload, until: int, L0: int = 2048):
     qs = [torch.empty((T, Hq, d), **bf).normal_(generator=g) for _ in range(nl)]
     # fresh N(0,1) tree K/V rows every step, drawn on the device and written
     # into every layer's cache by one batched append
-    rows_f32 = torch.empty((2, nl, Hkv, T, d), dtype=torch.float32, device=dev)
-    rows = torch.empty((2, nl, Hkv, T, d), **bf)
+    tree_kv_f32 = torch.empty((2, nl, Hkv, T, d), dtype=torch.float32, device=dev)
+    tree_kv = torch.empty((2, nl, Hkv, T, d), **bf)
     parents_np, tokens_np = syn.make_tree(w, np.random.default_rng(w.seed))
     parents = torch.from_numpy(np.asarray(parents_np, np.int32)).to(dev)
     tokens = torch.from_numpy(np.asarray(tokens_np, np.int32)).to(dev)
@@ -894,9 +894,9 @@ def run_loop_case(w: syn.Workload, until: int, L0: int = 2048):
 
     def step(s_, L):
         t_s = time.perf_counter()
-        torch.randn(rows_f32.shape, generator=g, device=dev, out=rows_f32)
-        rows.copy_(rows_f32)
-        ts._check(lib.ts_kv_append_batched(nl, crow[0], crow[1], P(rows[0]), P(rows[1]), L, L_cap,
+        torch.randn(tree_kv_f32.shape, generator=g, device=dev, out=tree_kv_f32)
+        tree_kv.copy_(tree_kv_f32)
+        ts._check(lib.ts_kv_append_batched(nl, crow[0], crow[1], P(tree_kv[0]), P(tree_kv[1]), L, L_cap,
                                            Hkv, d, T, stream))
         torch.randn((T, V), generator=g, device=dev, out=logits)
         logits.mul_(3.0)
