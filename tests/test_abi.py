@@ -116,3 +116,16 @@ def test_sample_flags_reject_unknown_bits(ts):
     assert f(p, p, p, 4, p, 8, 8, 100, 1.2, 1.0, 0.9, 0.05, p, p, p, p, p, p, 1 << 30, 4,
              None, None) == 1
     assert "flags" in ts.ts_last_error()
+
+
+def test_binding_signatures_match_the_header(ts):
+    """Every function the header declares has a ctypes signature in the
+    binding with the same number of parameters."""
+    src = re.sub(r"/\*.*?\*/", "", open(HEADER).read(), flags=re.S)
+    decls = dict(re.findall(r"\b(ts_[a-z_]+)\s*\(([^;{]*?)\)\s*;", src, flags=re.S))
+    assert decls, "no declarations parsed"
+    for name, params in decls.items():
+        assert name in ts._SIGNATURES, f"{name} has no ctypes signature"
+        p = params.strip()
+        n = 0 if p in ("", "void") else p.count(",") + 1
+        assert len(ts._SIGNATURES[name][1]) == n, (name, n, len(ts._SIGNATURES[name][1]))
