@@ -446,6 +446,76 @@ def sample_all_nodes(logits, prior, parents, tree_tokens, W, penalty,
 
 
 # --------------------------------------------------------------------------
+# (NEXT-3) rejection-sampling acceptance (App. A)
+# --------------------------------------------------------------------------
+def target_distribution(x_pen, top_p: float, min_p: float) -> np.ndarray:
+    """The distribution the exact-match path draws from, as a vector: the
+    kept set of sample_from_logits (top-p and min-p on p = softmax(x')), its
+    probabilities renormalised over the set, zero elsewhere (fp64)."""
+    x = np.asarray(x_pen, dtype=np.float64)
+    e = np.exp(x - x.max())
+    p = e / e.sum()
+    order = np.lexsort((np.arange(x.shape[0]), -p))
+    ps = p[order]
+    before = np.concatenate([[0.0], np.cumsum(ps)[:-1]])
+    keep = (before < top_p) & (ps >= min_p * ps[0])
+    keep[0] = True
+    n_keep = int(np.argmin(keep)) if not keep.all() else x.shape[0]
+    out = np.zeros_like(p)
+    out[order[:n_keep]] = ps[:n_keep]
+    return out / out.sum()
+
+
+def draw_in_id_order(p, u: float) -> int:
+    """Inverse-CDF draw over token ids in ascending order: the smallest id
+    whose cumulative mass exceeds u * sum(p)."""
+    c = np.cumsum(np.asarray(p, dtype=np.float64))
+    hit = np.nonzero(c > u * c[-1])[0]
+    return int(hit[0]) if hit.size else int(np.nonzero(p)[0][-1])
+
+
+def accept_rejection(logits, q, prior, parents, tree_tokens, W, penalty, temperature, top_p,
+                     min_p, u_accept, u_draw, literal=False):
+    """Speculative-sampling acceptance over the draft tree (App. A: acceptance
+    and rejection cases together reproduce the target's distribution).
+
+    Reading 19 of the design notes (the pages give the chain argument only):
+    from the root, at each accepted node n the children are tried in index
+    order as draft candidates drawn from q[n] (the draft distribution that
+    proposed n's children, one row per node).  Child c with token x is
+    accepted iff u_accept[c] * q[n][x] < p(x), p being n's target
+    distribution (penalty window along n's root path, temperature, top-p and
+    min-p, as the exact-match path uses); on rejection p becomes
+    max(p - q[n], 0) renormalised and the next child is tried.  When no child
+    is accepted, the bonus token is drawn from the current p with u_draw[n]
+    (inverse CDF in token-id order).  Returns (path, bonus)."""
+    T = len(parents)
+    children = [[] for _ in range(T)]
+    for c in range(1, T):
+        children[int(parents[c])].append(c)
+    node, path, drafted = 0, [0], []
+    while True:
+        win = penalty_window(prior, drafted, W)
+        p = target_distribution(penalised_logits(logits[node], win, penalty, temperature, literal),
+                                top_p, min_p)
+        qn = np.asarray(q[node], dtype=np.float64)
+        nxt = None
+        for c in children[node]:
+            x = int(tree_tokens[c])
+            if float(u_accept[c]) * qn[x] < p[x]:
+                nxt = c
+                break
+            r = np.maximum(p - qn, 0.0)
+            if r.sum() > 0.0:   # r == 0 only if p == q, where a rejection leaves p as it is
+                p = r / r.sum()
+        if nxt is None:
+            return path, draw_in_id_order(p, float(u_draw[node]))
+        node = nxt
+        path.append(node)
+        drafted.append(int(tree_tokens[node]))
+
+
+# --------------------------------------------------------------------------
 # (a8) KV commit of the accepted path
 # --------------------------------------------------------------------------
 def kv_append(cache, L: int, rows) -> np.ndarray:
