@@ -20,6 +20,8 @@ Source: "TokenSwift: Lossless Acceleration of Ultra Long Sequence Generation"
     probability exceeds p; min-p keeps tokens above p_base * p_max.
   * Table 11: k=20, temperature 1.0, top-p 0.9, min-p 0.05, penalty 1.2,
     penalty length 1024.
+  * A. Lossless Nature of Speculative Decoding: acceptance and rejection
+    cases together reproduce the target distribution (accept_rejection).
 
 Readings taken where the pages are silent (each also listed in the design
 notes): CTRL-style penalty is sign-aware (positive logits divided by theta,
