@@ -769,6 +769,51 @@ def run_refresh_case(w: syn.Workload, steps: int, warmup: int, drift: float = 0.
                    "growth": "2 tokens per step"}}))
 
 
+def run_reject_case(w: syn.Workload, steps: int, warmup: int):
+    """Rejection-sampling acceptance (ts_rejection_sample_accept) on the
+    workload's tree, logits and penalty settings, with a draft distribution
+    per node correlated with the target (softmax of half the logits plus
+    N(0,1) noise).  Device time per call with CUDA events.  Prints one JSON
+    line."""
+    import torch
+    import self_speculative_ultra_gb300 as ts
+    ts.build()
+    dev = torch.device("cuda", 0)
+    inp = syn.sampling_inputs(w, step=0)
+    rng = np.random.default_rng(0)
+    z = 0.5 * inp["logits"].astype(np.float64) + rng.standard_normal(inp["logits"].shape)
+    q = np.exp(z - z.max(axis=1, keepdims=True))
+    q = (q / q.sum(axis=1, keepdims=True)).astype(np.float32)
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)  # noqa: E731
+    logits, qd, toks, par, prior = t(inp["logits"]), t(q), t(inp["tokens"]), t(inp["parents"]), \
+        t(inp["prior"])
+    ua, ud = t(syn.node_uniforms(w.seed, 0, w.T)), t(syn.node_uniforms(w.seed, 7919, w.T))
+    ws = torch.empty(ts.ts_reject_workspace_bytes(w.V), dtype=torch.uint8, device=dev)
+    i32 = dict(dtype=torch.int32, device=dev)
+    path, n_path, bonus = torch.empty(w.T, **i32), torch.empty(1, **i32), torch.empty(1, **i32)
+
+    def call():
+        ts.ts_rejection_sample_accept(logits, qd, toks, par, prior, w.W, w.penalty, w.temperature,
+                                      w.top_p, w.min_p, ua, ud, path=path, n_path=n_path,
+                                      bonus=bonus, workspace=ws)
+    for _ in range(max(warmup, 3)):
+        call()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(steps):
+        call()
+    e1.record()
+    torch.cuda.synchronize()
+    us = e0.elapsed_time(e1) * 1e3 / steps
+    n = int(n_path.item())
+    print(json.dumps({"metric": "rejection-sampling acceptance per step (us)", "value": round(us, 1),
+                      "unit": "us", "higher_is_better": False, "calls": steps,
+                      "accepted_path_nodes": n,
+                      "config": {"workload": w.name, "tree_nodes": w.T, "V": w.V,
+                                 "top_p": w.top_p, "min_p": w.min_p, "penalty_window": w.W}}))
+
+
 def run_ngram_case(w: syn.Workload, steps: int, warmup: int):
     """Token reutilization per decode step: insert the 4-grams of the newly
     committed tokens (4 per step), then build the next draft tree (heads'
@@ -976,11 +1021,15 @@ def main():
                     help="time the softmax-weighted importance pass and exit")
     ap.add_argument("--refresh", action="store_true",
                     help="time the full against the incremental partial-cache refresh and exit")
+    ap.add_argument("--reject", action="store_true",
+                    help="time the rejection-sampling acceptance and exit")
     ap.add_argument("--ngram", action="store_true",
                     help="time the token-reutilization step (4-gram table + tree) and exit")
     args = ap.parse_args()
     w = syn.WORKLOADS[args.workload]
-    if args.refresh:
+    if args.reject:
+        run_reject_case(w, args.steps, args.warmup)
+    elif args.refresh:
         run_refresh_case(w, args.steps, args.warmup)
     elif args.imp_softmax:
         run_imp_softmax_case(w, args.steps, args.warmup)

@@ -312,6 +312,42 @@ int ts_penalized_sample_accept_eta(const float* logits, const int32_t* tree_toke
                                    int32_t* status, void* stream);
 
 /* ------------------------------------------------------------------------
+ * (3b) Rejection-sampling acceptance (speculative sampling over the tree).
+ *
+ * A. Lossless Nature of Speculative Decoding: acceptance and rejection
+ * cases together reproduce the target distribution.  From the root, at each
+ * accepted node n the children are tried in index order as draws from
+ * q[n, :] (the draft distribution that proposed n's children).  Child c with
+ * token x is accepted iff u_accept[c] * q[n, x] < p_n(x); p_n is node n's
+ * target distribution, formed exactly as in (3): penalty window along n's
+ * root path, temperature, top-p and min-p, renormalised over the kept set.
+ * On a rejection p_n becomes max(p_n - q[n, :], 0), renormalised, and the
+ * next child is tried.  When no child is accepted, the bonus token is drawn
+ * from the current p_n with u_draw[n], by inverse CDF over token ids.
+ *
+ * logits [T, V] fp32; q [T, V] fp32 (rows sum to 1; row n is only read when
+ * n is on the accepted path); tree_tokens, parents [T] int32; prior
+ * [n_prior] int32 ending with the root token; u_accept, u_draw [T] fp32 in
+ * [0, 1); 0 <= min_p <= 1.  Outputs as in (3): path [T] int32 (node indices, root first),
+ * n_path [1], bonus [1].  flags: TS_PENALTY_CTRL_LITERAL as in (3).
+ * workspace >= ts_reject_workspace_bytes(V).
+ * One CTA walks the path: meant for a draft model that provides q, at a
+ * latency of a few passes over the vocabulary per visited node.
+ * Unsupported (TS_ERR_UNSUPPORTED): more than 2048 tokens passing min-p at
+ * a visited node when top_p < 1 (reported in `status`, path = [0],
+ * bonus = -1), and top_p < 1 with min_p = 0 for V > 2048 (returned).
+ * ------------------------------------------------------------------------ */
+size_t ts_reject_workspace_bytes(int V);
+int ts_rejection_sample_accept(const float* logits, const float* q,
+                               const int32_t* tree_tokens, const int32_t* parents, int T,
+                               const int32_t* prior, int n_prior, int W, int V,
+                               float penalty, float temperature, float top_p, float min_p,
+                               const float* u_accept, const float* u_draw,
+                               int32_t* path, int32_t* n_path, int32_t* bonus,
+                               void* workspace, size_t workspace_bytes, int flags,
+                               int32_t* status, void* stream);
+
+/* ------------------------------------------------------------------------
  * (4) KV commit of the accepted path.
  *
  * §3.1: after verification the KV cache is updated with the accepted draft.

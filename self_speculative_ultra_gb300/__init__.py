@@ -24,6 +24,7 @@ __all__ = [
     "ts_partial_kv_refresh_incremental_batched",
     "ts_sample_workspace_bytes", "ts_penalized_sample_accept", "ts_kv_commit",
     "ts_kv_commit_batched", "commit_pointer_table", "ts_kv_append_batched",
+    "ts_reject_workspace_bytes", "ts_rejection_sample_accept",
 ]
 
 TS_OK, TS_ERR_INVALID_ARG, TS_ERR_UNSUPPORTED, TS_ERR_CUDA, TS_ERR_TIMEOUT, TS_ERR_WORKSPACE = range(6)
@@ -85,6 +86,11 @@ _SIGNATURES = {
                                     _c_void_p, _c_void_p, _c_void_p, _c_void_p]),
     "ts_kv_append_batched": (_i32, [_i32, _c_void_p, _c_void_p, _c_void_p, _c_void_p, _i64, _i64,
                                     _i32, _i32, _i32, _c_void_p]),
+    "ts_reject_workspace_bytes": (_sz, [_i32]),
+    "ts_rejection_sample_accept": (_i32, [_c_void_p, _c_void_p, _c_void_p, _c_void_p, _i32,
+                                          _c_void_p, _i32, _i32, _i32, _f32, _f32, _f32, _f32,
+                                          _c_void_p, _c_void_p, _c_void_p, _c_void_p, _c_void_p,
+                                          _c_void_p, _sz, _i32, _c_void_p, _c_void_p]),
     "ts_ngram_insert": (_i32, [_c_void_p, _i32, _i32, _c_void_p, _i32, _i32, _c_void_p,
                                _c_void_p]),
     "ts_ngram_build_tree": (_i32, [_c_void_p, _i32, _i32, _c_void_p, _c_void_p, _i32, _i32, _i32,
@@ -472,6 +478,39 @@ def ts_kv_append_batched(ks, vs, k_rows, v_rows, L, table=None, stream=None):
                                     ctypes.c_void_p(table[1].data_ptr()), _ptr(k_rows),
                                     _ptr(v_rows), L, L_cap, Hkv, d, T, _stream(stream))
     _check(rc)
+
+
+def ts_reject_workspace_bytes(V) -> int:
+    return lib().ts_reject_workspace_bytes(V)
+
+
+def ts_rejection_sample_accept(logits, q, tree_tokens, parents, prior, W, penalty, temperature,
+                               top_p, min_p, u_accept, u_draw, path=None, n_path=None, bonus=None,
+                               workspace=None, status=None, stream=None, literal=False):
+    """Speculative-sampling acceptance over the draft tree: children tried in
+    index order against the draft distributions q [T, V].  Returns
+    (path [T], n_path [1], bonus [1]) device int32."""
+    T, V = logits.shape
+    _dev(logits, torch.float32, "logits")
+    _dev(q, torch.float32, "q", (T, V))
+    _dev(tree_tokens, torch.int32, "tree_tokens", (T,))
+    _dev(parents, torch.int32, "parents", (T,))
+    _dev(prior, torch.int32, "prior")
+    _dev(u_accept, torch.float32, "u_accept", (T,))
+    _dev(u_draw, torch.float32, "u_draw", (T,))
+    dev = logits.device
+    mk = lambda n: torch.empty(n, dtype=torch.int32, device=dev)  # noqa: E731
+    path = mk(T) if path is None else path
+    n_path = mk(1) if n_path is None else n_path
+    bonus = mk(1) if bonus is None else bonus
+    ws, nb = _workspace(ts_reject_workspace_bytes(V), dev, workspace)
+    rc = lib().ts_rejection_sample_accept(
+        _ptr(logits), _ptr(q), _ptr(tree_tokens), _ptr(parents), T, _ptr(prior), prior.numel(), W,
+        V, penalty, temperature, top_p, min_p, _ptr(u_accept), _ptr(u_draw), _ptr(path),
+        _ptr(n_path), _ptr(bonus), _ptr(ws), nb, TS_PENALTY_CTRL_LITERAL if literal else 0,
+        _ptr(status), _stream(stream))
+    _check(rc)
+    return path, n_path, bonus
 
 
 def ts_ngram_table_bytes(V, cap) -> int:

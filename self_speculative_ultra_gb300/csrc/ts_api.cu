@@ -52,6 +52,13 @@ int launch_kv_commit_batched(int n_layers, void* const* k, void* const* v, int64
                              int64_t L_cap, int Hkv, int d, int T, const int32_t* path,
                              const int32_t* n_path, int32_t* status, cudaStream_t st);
 
+size_t reject_ws_bytes(int V);
+int launch_reject_accept(const float* logits, const float* q, const int32_t* tree_tokens,
+                         const int32_t* parents, int T, const int32_t* prior, int n_prior, int W,
+                         int V, float penalty, float temperature, float top_p, float min_p,
+                         int literal, const float* u_accept, const float* u_draw, int32_t* path,
+                         int32_t* n_path, int32_t* bonus, void* ws, int32_t* status,
+                         cudaStream_t st);
 int launch_kv_append_batched(int n_layers, void* const* k, void* const* v, const void* krows,
                              const void* vrows, int64_t L, int64_t L_cap, int Hkv, int d, int T,
                              cudaStream_t st);
@@ -402,6 +409,43 @@ int ts_kv_append_batched(int n_layers, void* const* k, void* const* v, const voi
     return fail(TS_ERR_INVALID_ARG, "%s: k_rows and v_rows must be 16-byte aligned", F);
   return launch_kv_append_batched(n_layers, k, v, k_rows, v_rows, L, L_cap, Hkv, d, T,
                                   static_cast<cudaStream_t>(stream));
+}
+
+size_t ts_reject_workspace_bytes(int V) {
+  if (V < 1 || V > 262144) return 0;
+  return reject_ws_bytes(V);
+}
+
+int ts_rejection_sample_accept(const float* logits, const float* q, const int32_t* tree_tokens,
+                               const int32_t* parents, int T, const int32_t* prior, int n_prior,
+                               int W, int V, float penalty, float temperature, float top_p,
+                               float min_p, const float* u_accept, const float* u_draw,
+                               int32_t* path, int32_t* n_path, int32_t* bonus, void* workspace,
+                               size_t workspace_bytes, int flags, int32_t* status, void* stream) {
+  clear_error();
+  const char* F = "ts_rejection_sample_accept";
+  if (flags & ~TS_PENALTY_CTRL_LITERAL) return fail(TS_ERR_INVALID_ARG, "%s: unknown flags 0x%x", F, flags);
+  if (T < 1) return fail(TS_ERR_INVALID_ARG, "%s: T=%d", F, T);
+  if (T > 64) return fail(TS_ERR_UNSUPPORTED, "%s: T=%d > 64", F, T);
+  if (V < 1) return fail(TS_ERR_INVALID_ARG, "%s: V=%d", F, V);
+  if (V > 262144) return fail(TS_ERR_UNSUPPORTED, "%s: V=%d > 262144", F, V);
+  if (n_prior < 0 || W < 0) return fail(TS_ERR_INVALID_ARG, "%s: n_prior, W must be >= 0", F);
+  if (!(penalty > 0.f) || !(temperature > 0.f))
+    return fail(TS_ERR_INVALID_ARG, "%s: penalty and temperature must be > 0", F);
+  if (!(top_p > 0.f) || !(min_p >= 0.f))
+    return fail(TS_ERR_INVALID_ARG, "%s: need top_p > 0 and min_p >= 0", F);
+  if (min_p > 1.f) return fail(TS_ERR_INVALID_ARG, "%s: need min_p <= 1", F);
+  if (top_p < 1.f && !(min_p > 0.f) && V > 2048)
+    return fail(TS_ERR_UNSUPPORTED, "%s: a top-p cut needs min_p > 0 when V > 2048", F);
+  if (!logits || !q || !tree_tokens || !parents || !u_accept || !u_draw || !path || !n_path ||
+      !bonus || (n_prior > 0 && !prior))
+    return fail(TS_ERR_INVALID_ARG, "%s: NULL tensor", F);
+  int rc = check_ws(workspace, workspace_bytes, reject_ws_bytes(V), F);
+  if (rc) return rc;
+  return launch_reject_accept(logits, q, tree_tokens, parents, T, prior, n_prior, W, V, penalty,
+                              temperature, top_p, min_p, (flags & TS_PENALTY_CTRL_LITERAL) ? 1 : 0,
+                              u_accept, u_draw, path, n_path, bonus, workspace, status,
+                              static_cast<cudaStream_t>(stream));
 }
 
 size_t ts_ngram_table_bytes(int V, int cap) {

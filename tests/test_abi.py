@@ -129,3 +129,15 @@ def test_binding_signatures_match_the_header(ts):
         p = params.strip()
         n = 0 if p in ("", "void") else p.count(",") + 1
         assert len(ts._SIGNATURES[name][1]) == n, (name, n, len(ts._SIGNATURES[name][1]))
+
+
+def test_rejection_call_rejects_bad_args(ts):
+    p = ctypes.c_void_p(16)
+    f = _c(ts).ts_rejection_sample_accept
+    # top-p without min-p over a large vocabulary is not supported
+    assert f(p, p, p, p, 4, p, 8, 8, 100000, 1.2, 1.0, 0.9, 0.0, p, p, p, p, p, p, 1 << 30, 0,
+             None, None) == 2
+    # unknown flag bits
+    assert f(p, p, p, p, 4, p, 8, 8, 1000, 1.2, 1.0, 0.9, 0.05, p, p, p, p, p, p, 1 << 30, 8,
+             None, None) == 1
+    assert ts.ts_reject_workspace_bytes(128256) >= 128256 * 4

@@ -1,0 +1,106 @@
+"""GPU parity: rejection-sampling acceptance (ts_rejection_sample_accept)
+against the oracle's accept_rejection.
+
+Path and bonus are integers: they must equal the oracle's exactly, except in
+near-tie cases.  A case is a near-tie when the oracle's own result changes
+under a relative perturbation of 2e-5 of the uniforms (the kernel forms p in
+fp32, the oracle in fp64; 2e-5 covers their difference for these inputs).
+Near-ties are counted and reported.
+"""
+import numpy as np
+import pytest
+import scipy.special
+import torch
+
+import ts_synth as syn
+from oracle import ts_oracle as orc
+import parity_util as pu
+
+pytestmark = pytest.mark.gpu
+
+
+def _draft(logits, rng, mix=0.5):
+    """A draft distribution per node, correlated with the target's logits."""
+    z = mix * logits.astype(np.float64) + rng.standard_normal(logits.shape)
+    return scipy.special.softmax(z, axis=1).astype(np.float32)
+
+
+def _oracle(inp, q, W, penalty, temperature, top_p, min_p, ua, ud, literal):
+    return orc.accept_rejection(inp["logits"], q.astype(np.float64), inp["prior"], inp["parents"],
+                                inp["tokens"], W, penalty, temperature, top_p, min_p, ua, ud,
+                                literal=literal)
+
+
+def _run(w, step, top_p=None, min_p=None, literal=False, q=None, seed=0):
+    import self_speculative_ultra_gb300 as ts
+    inp = syn.sampling_inputs(w, step=step)
+    rng = np.random.default_rng([seed, step])
+    top_p = w.top_p if top_p is None else top_p
+    min_p = w.min_p if min_p is None else min_p
+    q = _draft(inp["logits"], rng) if q is None else q
+    ua = syn.node_uniforms(w.seed, step, w.T)
+    ud = syn.node_uniforms(w.seed, step + 7919, w.T)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    path, n_path, bonus = ts.ts_rejection_sample_accept(
+        pu.to_dev(inp["logits"]), pu.to_dev(q), pu.to_dev(inp["tokens"]), pu.to_dev(inp["parents"]),
+        pu.to_dev(inp["prior"]), w.W, w.penalty, w.temperature, top_p, min_p, pu.to_dev(ua),
+        pu.to_dev(ud), status=status, literal=literal)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0, f"status {int(status.item())}"
+    n = int(n_path.item())
+    got = (path.cpu().numpy()[:n].tolist(), int(bonus.item()))
+    args = (inp, q, w.W, w.penalty, w.temperature, top_p, min_p)
+    ref = _oracle(*args, ua, ud, literal)
+    variants = {tuple(map(tuple, [ref[0], [ref[1]]]))}
+    for f in (1 - 2e-5, 1 + 2e-5):
+        r = _oracle(*args, np.minimum(ua * f, 1 - 1e-7), np.minimum(ud * f, 1 - 1e-7), literal)
+        variants.add(tuple(map(tuple, [r[0], [r[1]]])))
+    if len(variants) > 1:
+        return "tie", got, ref
+    assert got == (list(ref[0]), ref[1]), f"step {step}: gpu {got} oracle {ref}"
+    return "exact", got, ref
+
+
+@pytest.mark.parametrize("name,steps", [("tiny", 8), ("llama3.1-8b", 4), ("qwen2.5-14b", 3)])
+def test_configs(name, steps):
+    w = syn.WORKLOADS[name]
+    outcomes = [_run(w, s) for s in range(steps)]
+    ties = sum(o[0] == "tie" for o in outcomes)
+    lengths = [len(o[1][0]) for o in outcomes]
+    print(f"{name}: {ties} near-ties of {steps}; accepted path lengths {lengths}")
+    assert ties <= steps // 2
+
+
+def test_untruncated_target():
+    w = syn.WORKLOADS["llama3.1-8b"]
+    for s in range(3):
+        _run(w, 10 + s, top_p=1.0, min_p=0.0)
+
+
+def test_literal_penalty():
+    w = syn.scaled(syn.WORKLOADS["tiny"], penalty=3.0)
+    for s in range(4):
+        _run(w, 20 + s, literal=True)
+
+
+def test_draft_equal_to_target_follows_first_children():
+    """q = the oracle's own target distribution at every node (same window,
+    penalty and truncation): every first child with nonzero target mass is
+    accepted, so the path follows first children as far as they carry mass."""
+    w = syn.WORKLOADS["tiny"]
+    inp = syn.sampling_inputs(w, step=3)
+    paths = orc.root_paths(inp["parents"])
+    q = np.stack([orc.target_distribution(
+        orc.penalised_logits(inp["logits"][i],
+                             orc.penalty_window(inp["prior"],
+                                                [int(inp["tokens"][a]) for a in paths[i][1:]], w.W),
+                             w.penalty, w.temperature), w.top_p, w.min_p)
+        for i in range(w.T)]).astype(np.float32)
+    kind, got, ref = _run(w, 3, q=q)
+    assert kind in ("exact", "tie")
+    if kind == "exact":
+        node = 0
+        for nxt in ref[0][1:]:
+            kids = [c for c in range(1, w.T) if inp["parents"][c] == node]
+            assert nxt == kids[0]
+            node = nxt
