@@ -23,11 +23,11 @@ Source: "TokenSwift: Lossless Acceleration of Ultra Long Sequence Generation"
   * A. Lossless Nature of Speculative Decoding: acceptance and rejection
     cases together reproduce the target distribution (accept_rejection).
 
-Readings taken where the pages are silent (each also listed in the design
-notes): CTRL-style penalty is sign-aware (positive logits divided by theta,
-non-positive multiplied); a windowed token is penalised once whatever its
-count; top-p and min-p are intersected on the same post-temperature
-distribution; one uniform per node drives an inverse-CDF draw over the kept
+Readings taken where the pages are silent: CTRL-style penalty is sign-aware
+(positive logits divided by theta, non-positive multiplied); a windowed token
+is penalised once whatever its count; top-p and min-p are intersected on the
+same post-temperature distribution; top-p keeps rank r iff the mass before r
+is <= p (the smallest set whose mass exceeds p), and everything when p >= 1; one uniform per node drives an inverse-CDF draw over the kept
 set in (p desc, id asc) order; importance is the raw scaled dot product summed
 over the group's heads and the last n_imp tree queries; sinks and the recent
 window are kept outside the top-B competition; ties in importance go to the
@@ -141,7 +141,8 @@ def importance_softmax(q, k, L: int, lse, n_imp: int = 0):
     §3.3 Dynamic KV Cache Management ranks cache pairs by query-key scores,
     the queries of a GQA group partitioned and their scores aggregated.  This
     variant aggregates the normalised attention weights instead of the raw
-    scores (reading 17 of the design notes):
+    scores (the pages do not define this variant; this is the plain reading
+    of "aggregate the group's attention" with softmax weights):
 
         imp[kv, j] = sum over the last n_imp nodes i and the heads h of
                      group kv of exp(q[i,h] . k[kv,j] / sqrt(d) - lse[i,h]),
@@ -202,9 +203,9 @@ def refresh_incremental(slots_prev, kept_new, cache_head, compact_prev):
     """(NEXT-4) Incremental update of one KV head's partial cache.
 
     §3.3: the budgeted cache keeps its initial |S| pairs and replaces the
-    less important pairs as generation proceeds.  Reading 18 of the design
-    notes: a slot keeps its row while its position stays selected; the rows
-    of newly selected positions are written into the slots whose positions
+    less important pairs as generation proceeds.  The pages give no slot
+    rule; the one taken here: a slot keeps its row while its position stays
+    selected; the rows of newly selected positions are written into the slots whose positions
     left the selection, and past the old slot count while the cache is still
     growing (L <= S+B+R).  Freed slots are filled in ascending slot order by
     the added positions in ascending position order.  Attention over the
@@ -272,16 +273,38 @@ def penalised_logits(x, window, penalty: float, temperature: float,
     return (x / np.float32(temperature)).astype(np.float32)
 
 
+def _top_p_keep(before, top_p: float) -> np.ndarray:
+    """top-p (§D.1): the smallest set of leading ranks whose cumulative
+    probability exceeds p.  Rank r belongs to it iff the ranks before r do
+    not yet exceed p, i.e. their mass is <= top_p.  With top_p >= 1 no set
+    can exceed p and every rank is kept."""
+    if top_p >= 1.0:
+        return np.ones(len(before), dtype=bool)
+    return before <= top_p
+
+
 def sample_from_logits(x_pen, top_p: float, min_p: float, u: float, return_info: bool = False):
     """Draw one token from penalised logits with top-p and min-p truncation.
 
     p = softmax(x') in fp64.  Tokens are ranked by (p desc, id asc).
-    top-p (§D.1): keep the smallest prefix of ranks whose mass reaches p, i.e.
-        rank r is kept iff the mass of ranks before r is < top_p.
+    top-p (§D.1): keep the smallest prefix of ranks whose mass exceeds p:
+        rank r is kept iff the mass of ranks before r is <= top_p
+        (top_p >= 1 keeps every rank).
     min-p (§D.1): keep tokens with p >= min_p * p_max.
     Both are applied (Table 11 sets both); the kept set K is their
     intersection, which always holds rank 0.  The draw is the smallest rank r
     in K whose cumulative mass over K exceeds u * mass(K).
+
+    With return_info, also the distance of each deciding quantity to its cut
+    (used to recognise near-ties between implementations):
+      top_p_last  mass before the last kept rank vs top_p
+      min_p_last  p/p_max of the last kept rank vs min_p
+      first_cut   the first cut rank: it would join K only if every filter
+                  that cuts it flipped, so the largest of their distances
+      draw_hi     cumulative kept mass at the drawn rank / mass(K) vs u
+      draw_lo     the same one rank earlier
+    Distances are inf where the quantity does not exist (rank 0 is never
+    cut; no rank follows the last).  margin = the smallest of them.
     """
     x = np.asarray(x_pen, dtype=np.float64)
     V = x.shape[0]
@@ -292,7 +315,8 @@ def sample_from_logits(x_pen, top_p: float, min_p: float, u: float, return_info:
     order = np.lexsort((ids, -p))
     ps = p[order]
     before = np.concatenate([[0.0], np.cumsum(ps)[:-1]])
-    keep = (before < top_p) & (ps >= min_p * ps[0])
+    ratio = ps / ps[0]
+    keep = _top_p_keep(before, top_p) & (ratio >= min_p)
     keep[0] = True
     n_keep = int(np.argmin(keep)) if not keep.all() else V   # keep is a prefix
     kept = ps[:n_keep]
@@ -302,14 +326,22 @@ def sample_from_logits(x_pen, top_p: float, min_p: float, u: float, return_info:
     tok = int(order[r])
     if not return_info:
         return tok
-    # distances of the three cut quantities to their cuts (probability units)
-    margins = [abs(before[n_keep] - top_p) if n_keep < V else np.inf,
-               abs(before[n_keep - 1] - top_p),
-               abs(ps[n_keep - 1] - min_p * ps[0]),
-               abs(ps[n_keep] - min_p * ps[0]) if n_keep < V else np.inf,
-               abs(c[r] - target) / c[-1],
-               abs((c[r - 1] if r > 0 else 0.0) - target) / c[-1]]
-    return tok, dict(n_keep=n_keep, rank=r, margin=float(min(margins)))
+    inf = float("inf")
+    last = n_keep - 1
+    dist = {"top_p_last": abs(before[last] - top_p) if (last > 0 and top_p < 1.0) else inf,
+            "min_p_last": abs(ratio[last] - min_p) if last > 0 else inf,
+            "first_cut": inf,
+            "draw_hi": abs(c[r] / c[-1] - u),
+            "draw_lo": abs(c[r - 1] / c[-1] - u) if r > 0 else inf}
+    if n_keep < V:
+        fails = []
+        if top_p < 1.0 and before[n_keep] > top_p:
+            fails.append(before[n_keep] - top_p)
+        if ratio[n_keep] < min_p:
+            fails.append(min_p - ratio[n_keep])
+        dist["first_cut"] = float(max(fails))
+    dist = {k: float(v) for k, v in dist.items()}
+    return tok, dict(n_keep=n_keep, rank=r, dist=dist, margin=min(dist.values()))
 
 
 def sample_node(logits_row, prior, path_tokens, W, penalty, temperature, top_p,
@@ -337,7 +369,13 @@ def sample_from_logits_eta(x_pen, epsilon: float, alpha: float, u: float,
     """Draw one token with η-sampling: p = softmax(x') in fp64, ranks by
     (p desc, id asc), the kept set K = {p >= η} (a rank prefix holding rank
     0, as α <= 1 puts η at or below p_max), and the smallest rank in K whose
-    cumulative mass exceeds u * mass(K)."""
+    cumulative mass exceeds u * mass(K).
+
+    With return_info, the distances of the deciding quantities to their cuts:
+      eta_last, eta_first_cut  p/η - 1 of the last kept and first cut rank
+                               (relative: η itself is small)
+      draw_hi, draw_lo         as in sample_from_logits
+    and margin = the smallest."""
     x = np.asarray(x_pen, dtype=np.float64)
     V = x.shape[0]
     e = np.exp(x - x.max())
@@ -354,10 +392,15 @@ def sample_from_logits_eta(x_pen, epsilon: float, alpha: float, u: float,
     tok = int(order[r])
     if not return_info:
         return tok
-    margins = [abs(ps[n_keep - 1] - eta), abs(ps[n_keep] - eta) if n_keep < V else np.inf,
-               abs(c[r] - target) / c[-1],
-               abs((c[r - 1] if r > 0 else 0.0) - target) / c[-1]]
-    return tok, dict(n_keep=n_keep, rank=r, margin=float(min(margins)), eta=eta)
+    inf = float("inf")
+    last = n_keep - 1
+    rel = (lambda v: abs(v / eta - 1.0)) if eta > 0 else (lambda v: inf)
+    dist = {"eta_last": rel(ps[last]) if last > 0 else inf,
+            "eta_first_cut": rel(ps[n_keep]) if n_keep < V else inf,
+            "draw_hi": abs(c[r] / c[-1] - u),
+            "draw_lo": abs(c[r - 1] / c[-1] - u) if r > 0 else inf}
+    dist = {k: float(v) for k, v in dist.items()}
+    return tok, dict(n_keep=n_keep, rank=r, dist=dist, margin=min(dist.values()), eta=eta)
 
 
 def sample_all_nodes_eta(logits, prior, parents, tree_tokens, W, penalty, temperature,
@@ -460,7 +503,7 @@ def target_distribution(x_pen, top_p: float, min_p: float) -> np.ndarray:
     order = np.lexsort((np.arange(x.shape[0]), -p))
     ps = p[order]
     before = np.concatenate([[0.0], np.cumsum(ps)[:-1]])
-    keep = (before < top_p) & (ps >= min_p * ps[0])
+    keep = _top_p_keep(before, top_p) & (ps / ps[0] >= min_p)
     keep[0] = True
     n_keep = int(np.argmin(keep)) if not keep.all() else x.shape[0]
     out = np.zeros_like(p)
@@ -481,8 +524,8 @@ def accept_rejection(logits, q, prior, parents, tree_tokens, W, penalty, tempera
     """Speculative-sampling acceptance over the draft tree (App. A: acceptance
     and rejection cases together reproduce the target's distribution).
 
-    Reading 19 of the design notes (the pages give the chain argument only):
-    from the root, at each accepted node n the children are tried in index
+    The pages give the chain argument only; the tree form taken here is
+    multi-candidate recursive rejection: from the root, at each accepted node n the children are tried in index
     order as draft candidates drawn from q[n] (the draft distribution that
     proposed n's children, one row per node).  Child c with token x is
     accepted iff u_accept[c] * q[n][x] < p(x), p being n's target

@@ -9,3 +9,14 @@ if ROOT not in sys.path:
 def pytest_configure(config):
     config.addinivalue_line("markers", "gpu: needs a CUDA GPU (sm_103a) and the built library")
     config.addinivalue_line("markers", "slow: long-running full-size case")
+
+
+def pytest_terminal_summary(terminalreporter, exitstatus, config):
+    """One line with the near-ties the parity tests counted (kind: ties of
+    compared items), so a run's tail records them."""
+    pu = sys.modules.get("parity_util")
+    counts = getattr(pu, "TIE_COUNTS", None) if pu is not None else None
+    if not counts:
+        return
+    parts = [f"{k}: {v[1]} of {v[0]}" for k, v in sorted(counts.items())]
+    terminalreporter.write_line("near-ties counted (tie band 1e-5): " + "; ".join(parts))

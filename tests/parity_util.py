@@ -12,6 +12,8 @@ Tolerances:
 """
 from __future__ import annotations
 
+import collections
+
 import numpy as np
 import torch
 
@@ -20,6 +22,36 @@ from oracle import ts_oracle as orc
 ATTN_RTOL = 2e-3
 LSE_ATOL = 2e-3
 TIE = 1e-5
+
+# near-ties seen in this pytest session, by kind ("draw", "selection", ...):
+# [number of compared items, number of counted ties]; printed by the
+# terminal-summary hook of conftest.py
+TIE_COUNTS: dict = collections.defaultdict(lambda: [0, 0])
+
+
+def record_ties(kind: str, compared: int, ties: int) -> None:
+    TIE_COUNTS[kind][0] += int(compared)
+    TIE_COUNTS[kind][1] += int(ties)
+
+
+def compare_draws(got, ref, infos, kind: str = "draw") -> int:
+    """Sampled tokens must equal the oracle's, except at nodes whose oracle
+    margin (the smallest distance of a deciding quantity to its cut, from
+    sample_from_logits / sample_from_logits_eta with return_info) is below
+    TIE.  Returns the number of such tied nodes that differ; raises on any
+    other difference."""
+    got = np.asarray(got).tolist()
+    ref = np.asarray(ref).tolist()
+    assert len(got) == len(ref), f"{len(got)} draws against {len(ref)}"
+    ties = 0
+    for i, (g, r) in enumerate(zip(got, ref)):
+        if g != r:
+            m = infos[i]["margin"]
+            assert m < TIE, (f"node {i}: gpu {g} oracle {r} margin {m:.2e} "
+                             f"({infos[i].get('dist')})")
+            ties += 1
+    record_ties(kind, len(ref), ties)
+    return ties
 
 
 def to_dev_bf16(bits: np.ndarray) -> torch.Tensor:
@@ -81,4 +113,5 @@ def compare_selection(idx_gpu, idx_ref, imp_rank, L, B, S, R):
                 f"head {kv}: position {j} score {imp_rank[kv][j]} differs outside the tie band "
                 f"around {s_cut}")
             ties += 1
+    record_ties("selection", int(np.asarray(idx_ref).size), ties)
     return ties

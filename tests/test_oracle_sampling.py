@@ -87,7 +87,7 @@ def test_degenerate_truncation_is_greedy(top_p, min_p):
 
 def test_equal_probabilities_rank_by_token_id():
     x = np.zeros(5, dtype=np.float32)
-    # five equal probabilities 0.2: top-p 0.5 keeps ranks with mass-before < .5 -> ids 0,1,2
+    # five equal probabilities 0.2: top-p 0.5 keeps ranks with mass-before <= .5 -> ids 0,1,2
     assert orc.sample_from_logits(x, 0.5, 0.0, 0.99) == 2
     assert orc.sample_from_logits(x, 0.5, 0.0, 0.0) == 0
 
@@ -148,12 +148,27 @@ def test_kv_commit_moves_accepted_rows():
     np.testing.assert_array_equal(out[:, :6], cache[:, :6])
 
 
-def test_top_p_boundary_is_strict():
-    """Four equal probabilities 0.25, top_p 0.5: mass before rank 2 is
-    exactly 0.5, which is not < 0.5, so only ranks 0 and 1 are kept."""
+def test_top_p_boundary_exceeds():
+    """§D.1: the smallest set whose cumulative probability exceeds p.  Four
+    equal probabilities 0.25, top_p 0.5: ranks 0 and 1 hold exactly 0.5,
+    which does not exceed 0.5, so rank 2 joins (mass 0.75 > 0.5) and rank 3
+    does not (the mass before it, 0.75, already exceeds 0.5)."""
     x = np.zeros(4, dtype=np.float32)
-    assert orc.sample_from_logits(x, 0.5, 0.0, 0.99) == 1
-    assert orc.sample_from_logits(x, 0.5000001, 0.0, 0.99) == 2
+    assert orc.sample_from_logits(x, 0.5, 0.0, 0.99) == 2
+    assert orc.sample_from_logits(x, 0.4999999, 0.0, 0.99) == 1
+    assert orc.sample_from_logits(x, 0.7500001, 0.0, 0.99) == 3
+
+
+def test_top_p_one_keeps_every_token():
+    """No set can exceed a probability of 1: top_p = 1 keeps the whole
+    vocabulary, so the last token of a long tail is still drawn at u near 1."""
+    rng = np.random.default_rng(8)
+    x = (rng.standard_normal(5000) * 3).astype(np.float32)
+    p = scipy.special.softmax(x.astype(np.float64))
+    last = int(np.lexsort((np.arange(5000), -p))[-1])
+    assert orc.sample_from_logits(x, 1.0, 0.0, 1.0 - 1e-12) == last
+    _, info = orc.sample_from_logits(x, 1.0, 0.0, 0.5, return_info=True)
+    assert info["n_keep"] == 5000
 
 
 # --------------------------------------------------------------------------
