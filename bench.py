@@ -80,6 +80,18 @@ def step_bytes(w: syn.Workload) -> int:
     return w.layers * (verify_bytes(w) + select_bytes(w)) + sample_bytes(w) + commit_bytes(w)
 
 
+def config_dict(w: syn.Workload, world: int = 1) -> dict:
+    """The workload's description, shared by the GPU arm and the oracle arm."""
+    sb = step_bytes(w)
+    return {"workload": w.name, "layers": w.layers, "Hq": w.Hq, "Hkv": w.Hkv,
+            "d": w.d, "L": w.L, "tree_nodes": w.T, "budget_B": w.B, "sinks": w.S,
+            "recent": w.R, "vocab": w.V, "penalty_window": w.W,
+            "bytes_per_step": sb,
+            "l2": (f"inputs larger than L2 (distinct K/V per layer, {sb / 1e9:.1f} GB per step)"
+                   if sb > 129e6 else "inputs fit in L2 (parity-size case)"),
+            "parallelism": f"replicas x{world}"}
+
+
 # ---------------------------------------------------------------------------
 # measured peaks and profile-derived traffic
 # ---------------------------------------------------------------------------
@@ -188,7 +200,7 @@ class ClockSampler:
 class Step:
     """Device-resident state of one benchmark replica and its step()."""
 
-    def __init__(self, w: syn.Workload, device, seed: int = 0):
+    def __init__(self, w: syn.Workload, device, seed: int = 0, e2e: bool = True):
         import torch
         import self_speculative_ultra_gb300 as ts
         self.ts, self.torch, self.w = ts, torch, w
@@ -245,6 +257,14 @@ class Step:
         self.sel_table = ts.layer_pointer_table(self.imp, self.k, self.v, self.idx, self.kd, self.vd)
         self.commit_table = ts.commit_pointer_table(self.k, self.v)
         self.ws_p = torch.empty(max(ts.ts_sample_workspace_bytes(T, w.V), 256), **u8)
+        self.v_events = None
+        if e2e:
+            self._init_e2e()
+        torch.cuda.synchronize()
+
+    def _init_e2e(self):
+        torch, w, dev = self.torch, self.w, self.dev
+        T, Hq, Hkv, d, L = w.T, w.Hq, w.Hkv, w.d, self.L
         # end-to-end leg: the per-step inputs live in one pinned host buffer,
         # uploaded with a single copy into one of two device staging buffers.
         # The step reads queries, logits, tree, window and uniforms in place
@@ -281,8 +301,6 @@ class Step:
         self.h_bytes = sum(int(np.prod(sh)) * torch.empty(0, dtype=dt).element_size()
                            for _, sh, dt in spec)
         self.h_out = torch.empty(T + 2, dtype=torch.int32).pin_memory()
-        self.v_events = None
-        torch.cuda.synchronize()
 
     def h2d_bytes(self) -> int:
         return self.h_bytes
@@ -359,6 +377,63 @@ class Step:
         # verify: split kernel + merge per layer; batched select: histogram,
         # collect, gather; sample; commit
         return self.w.layers * 2 + 3 + 2
+
+
+def time_steps(st: Step, steps: int, warmup: int):
+    """Device time of `steps` hot-path steps after `warmup` untimed ones
+    (CUDA events on the launching stream), and the verify calls' durations
+    from events in the last three timed steps.  Returns (ms per step, list of
+    verify-call ms)."""
+    torch, w = st.torch, st.w
+    for _ in range(warmup):
+        st.step()
+    torch.cuda.synchronize()
+    n_ev = min(3, steps)
+    ev = [[[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(w.layers)]
+          for _ in range(n_ev)]
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record()
+    for s_ in range(steps):
+        k_ev = s_ - (steps - n_ev)
+        st.step(events=ev[k_ev] if k_ev >= 0 else None)
+    t1.record()
+    torch.cuda.synchronize()
+    ver_ms = [e[i][0].elapsed_time(e[i][1]) for e in ev for i in range(w.layers)]
+    return t0.elapsed_time(t1) / steps, ver_ms
+
+
+def per_config_line(w: syn.Workload, ms_step: float, ver_ms, peak: float, tf_peak: float,
+                    steps: int) -> dict:
+    v_ms = statistics.mean(ver_ms)
+    gbs = step_bytes(w) / (ms_step * 1e-3) / 1e9
+    vgbs = verify_bytes(w) / (v_ms * 1e-3) / 1e9
+    return {"ms_per_step": round(ms_step, 4), "steps_per_s": round(1e3 / ms_step, 2),
+            "GB_per_s": round(gbs, 1), "hbm_frac": round(gbs / peak, 4),
+            "bytes_per_step": step_bytes(w), "verify_avg_call_ms": round(v_ms, 4),
+            "verify_GB_per_s": round(vgbs, 1), "verify_hbm_frac": round(vgbs / peak, 4),
+            "verify_tensor_frac": round(verify_flops(w) / (v_ms * 1e-3) / 1e12 / tf_peak, 4),
+            "timed_steps": steps}
+
+
+def measure_other_configs(dev, skip: str, steps: int, warmup: int, peak: float,
+                          tf_peak: float) -> dict:
+    """Every other workload of the suite, one after the other, each with its
+    own device-resident inputs (freed before the next)."""
+    import torch
+    out = {}
+    for name in ("tiny", "qwen2.5-1.5b", "llama3.1-8b", "mha-7b", "qwen2.5-14b"):
+        if name == skip:
+            continue
+        w = syn.WORKLOADS[name]
+        st = Step(w, dev, seed=0, e2e=False)
+        ms_step, ver_ms = time_steps(st, steps, warmup)
+        line = per_config_line(w, ms_step, ver_ms, peak, tf_peak, steps)
+        line["device_status"] = int(st.status.item())
+        out[name] = line
+        del st
+        torch.cuda.empty_cache()
+    return out
 
 
 def run_gpu(args, w: syn.Workload):
@@ -458,12 +533,7 @@ def run_gpu(args, w: syn.Workload):
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic (seeded N(0,1) bf16 K/V with planted heavy hitters, "
                     "N(0,9) fp32 logits)",
-            "config": {"workload": w.name, "layers": w.layers, "Hq": w.Hq, "Hkv": w.Hkv,
-                       "d": w.d, "L": w.L, "tree_nodes": w.T, "budget_B": w.B, "sinks": w.S,
-                       "recent": w.R, "vocab": w.V, "penalty_window": w.W,
-                       "bytes_per_step": sb, "l2": "inputs larger than L2 (distinct K/V per layer, "
-                                                   f"{sb / 1e9:.1f} GB per step)",
-                       "parallelism": f"replicas x{world}"},
+            "config": config_dict(w, world),
             "steps_per_s": round(world / (ms_step * 1e-3), 2),
             "pct_of_hbm_peak": round(100 * value / world / peak, 2),
             "roofline": {"bound": "hbm", "kernel": "ts_verify_attention (split + merge)",
@@ -483,6 +553,13 @@ def run_gpu(args, w: syn.Workload):
             "clocks": clk,
             "device_status": status,
         }
+        per = {w.name: per_config_line(w, ms_step, ver_ms, peak, tf_peak, args.steps)}
+        if world == 1 and not args.no_per_config:
+            del st
+            torch.cuda.empty_cache()
+            per.update(measure_other_configs(dev, w.name, max(20, min(args.steps, 50)),
+                                             max(3, args.warmup), peak, tf_peak))
+        line["per_config"] = per
         if not args.no_cpu_baseline:
             line["cpu_baseline"] = cpu_baseline(w)
         print(json.dumps(line), flush=True)
@@ -493,15 +570,20 @@ def run_gpu(args, w: syn.Workload):
 # ---------------------------------------------------------------------------
 # CPU oracle legs
 # ---------------------------------------------------------------------------
-def _oracle_layer_unit(w: syn.Workload, heads: int, sample_nodes: int, seed: int = 0):
+def _oracle_layer_unit(w: syn.Workload, heads: int, sample_nodes: int, seed: int = 0,
+                       barrier=None):
     """Time the oracle on `heads` KV heads of one layer (verify + select +
-    gather) and `sample_nodes` tree nodes of the sampling step.  Returns
-    (seconds, algorithmic bytes processed)."""
+    gather) and `sample_nodes` tree nodes of the sampling step.  The inputs
+    are generated first; with a barrier, every worker starts timing together.
+    Returns (start, end) perf_counter stamps and the algorithmic bytes
+    processed."""
     from oracle import ts_oracle as orc
     sub = syn.scaled(w, Hkv=heads, Hq=heads * w.G)
     inp = syn.attention_inputs(sub, layer=seed)
     sin = syn.sampling_inputs(w, step=seed)
     q, k, v = (orc.bf16_to_f64(inp[n]) for n in ("q", "k", "v"))
+    if barrier is not None:
+        barrier.wait()
     t = time.perf_counter()
     _, _, imp = orc.verify_attention(q, k, v, sub.L, inp["parents"], sub.n_imp)
     for h in range(heads):
@@ -513,42 +595,117 @@ def _oracle_layer_unit(w: syn.Workload, heads: int, sample_nodes: int, seed: int
         drafted = [int(sin["tokens"][a]) for a in paths[i][1:]]
         orc.sample_node(sin["logits"][i], sin["prior"], drafted, w.W, w.penalty, w.temperature,
                         w.top_p, w.min_p, float(sin["uniforms"][i]))
-    secs = time.perf_counter() - t
+    t1 = time.perf_counter()
     nbytes = verify_bytes(sub) + select_bytes(sub) + sample_nodes * 4 * w.V
-    return secs, nbytes
+    return t, t1, nbytes
+
+
+_POOL_BARRIER = None
+
+
+def _pool_init(barrier):
+    global _POOL_BARRIER
+    _POOL_BARRIER = barrier
+
+
+def _pool_unit(args):
+    name, heads, nodes, seed = args
+    return _oracle_layer_unit(syn.WORKLOADS[name], heads, nodes, seed, _POOL_BARRIER)
+
+
+def host_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+class OraclePool:
+    """One oracle worker process per host core (spawned: no state is
+    inherited from a process that already used the GPU).  A round gives
+    every worker one unit -- one KV head of one layer, verify + select +
+    gather, plus `nodes` node draws -- started together behind a barrier;
+    its throughput is the units' algorithmic bytes over the round's wall
+    time (first start to last end)."""
+
+    def __init__(self, cores: int):
+        import multiprocessing as mp
+        ctx = mp.get_context("spawn")
+        self.cores = cores
+        self.barrier = ctx.Barrier(cores)
+        self.pool = ctx.Pool(cores, initializer=_pool_init, initargs=(self.barrier,))
+
+    def round(self, w: syn.Workload, nodes: int, seed0: int):
+        units = [(w.name, 1, nodes, seed0 + i) for i in range(self.cores)]
+        res = self.pool.map(_pool_unit, units, chunksize=1)
+        wall = max(r[1] for r in res) - min(r[0] for r in res)
+        return wall, sum(r[2] for r in res)
+
+    def close(self):
+        self.pool.close()
+        self.pool.join()
 
 
 def cpu_baseline(w: syn.Workload):
-    heads, nodes = min(w.Hkv, 4), 16
-    secs, nbytes = _oracle_layer_unit(w, heads=heads, sample_nodes=nodes)
-    return {"value": round(nbytes / secs / 1e9, 4), "unit": UNIT, "cores": 1, "kind": "oracle",
-            "sample": f"fp64 numpy oracle, 1 thread: verify+select+gather of {heads} of {w.Hkv} "
-                      f"KV heads of one layer + {nodes} of {w.T} node draws "
-                      f"({nbytes / 1e6:.1f} MB of algorithmic traffic in {secs:.1f} s)"}
+    """The oracle as it stands, on the host cores: two rounds of the pool
+    (each: one KV head of one layer per core plus 2 node draws each), and one
+    such unit on one core for the single-thread figure."""
+    cores = host_cores()
+    t0, t1, b1 = _oracle_layer_unit(w, heads=1, sample_nodes=2, seed=0)
+    single = b1 / (t1 - t0) / 1e9
+    pool = OraclePool(cores)
+    try:
+        wall, nbytes = 0.0, 0
+        for r in range(2):
+            s_, b_ = pool.round(w, 2, seed0=r * cores)
+            wall += s_
+            nbytes += b_
+    finally:
+        pool.close()
+    return {"value": round(nbytes / wall / 1e9, 4), "unit": UNIT, "cores": cores,
+            "kind": "oracle",
+            "sample": f"fp64 numpy oracle, {cores} processes (one per host core), two rounds "
+                      f"of one unit each: verify+select+gather of 1 of {w.Hkv} KV heads of one "
+                      f"layer + 2 of {w.T} node draws ({nbytes / 1e6:.1f} MB of algorithmic "
+                      f"traffic in {wall:.2f} s wall)",
+            "single_thread": {"value": round(single, 4), "unit": UNIT, "cores": 1,
+                              "sample": f"one such unit on one core ({b1 / 1e6:.1f} MB in "
+                                        f"{t1 - t0:.2f} s)"}}
 
 
 def run_reference(args, w: syn.Workload):
+    """The oracle arm: each step is one round of the oracle pool over the
+    host cores (a bounded sample of the workload: one KV head of one layer
+    per core plus 2 node draws each), timed by the host clock."""
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
     if rank != 0:
         return
-    for i in range(args.warmup):
-        _oracle_layer_unit(w, heads=1, sample_nodes=1, seed=100 + i)
-    tot_s, tot_b = 0.0, 0
-    for i in range(args.steps):
-        s, b = _oracle_layer_unit(w, heads=1, sample_nodes=1, seed=i)
-        tot_s += s
-        tot_b += b
+    cores = host_cores()
+    pool = OraclePool(cores)
+    try:
+        for i in range(args.warmup):
+            pool.round(w, 2, seed0=1000 + i * cores)
+        tot_s, tot_b = 0.0, 0
+        for i in range(args.steps):
+            s, b = pool.round(w, 2, seed0=i * cores)
+            tot_s += s
+            tot_b += b
+    finally:
+        pool.close()
     value = tot_b / tot_s / 1e9
     line = {
         "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": UNIT,
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
-        "ms_per_step": round(1e3 * tot_s / args.steps, 2), "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": w.name},
-        "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": 1, "kind": "oracle",
-                         "sample": f"each step: verify+select+gather of 1 of {w.Hkv} KV heads "
-                                   f"of one layer + 1 node draw, fp64 numpy, 1 thread"},
+        "ms_per_step": round(1e3 * tot_s / max(args.steps, 1), 2), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded N(0,1) bf16 K/V with planted heavy hitters, N(0,9) fp32 "
+                "logits)",
+        "config": config_dict(w, world),
+        "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": f"each step: {cores} processes (one per host core), each "
+                                   f"verify+select+gather of 1 of {w.Hkv} KV heads of one layer "
+                                   f"+ 2 node draws, fp64 numpy"},
         "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
@@ -1010,6 +1167,8 @@ def main():
     ap.add_argument("--impl", default="gpu", choices=["gpu", "reference"])
     ap.add_argument("--workload", default="llama3.1-8b", choices=sorted(syn.WORKLOADS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-per-config", action="store_true",
+                    help="skip the timing of the other workloads")
     ap.add_argument("--profile", choices=["verify", "select", "imp"],
                     help="run a small fixed case for ncu captures and exit")
     ap.add_argument("--draft", action="store_true",

@@ -243,19 +243,20 @@ int ts_partial_kv_refresh_incremental_batched(int n_layers, const float* const* 
  * (3) Contextual-penalty sampling and exact-match tree acceptance.
  *
  * §3.4 Contextual Penalty: penalise the most recent W tokens; §D.1: top-p
- * keeps the smallest set of tokens whose probability mass reaches top_p,
- * min-p keeps tokens with p >= min_p * p_max; Table 11 sets penalty 1.2,
- * window 1024, temperature 1.0, top-p 0.9, min-p 0.05; §3.1: the longest
- * draft that matches the target's own tokens is accepted.
+ * keeps the smallest set of tokens whose cumulative probability exceeds
+ * top_p (every token when top_p >= 1), min-p keeps tokens with
+ * p >= min_p * p_max; Table 11 sets penalty 1.2, window 1024, temperature
+ * 1.0, top-p 0.9, min-p 0.05; §3.1: the longest draft that matches the
+ * target's own tokens is accepted.
  *
  * For every node i (in parallel): the window is the last W tokens of
  * (prior[0:n_prior] followed by the drafted tokens on the root path of i,
  * root excluded); each distinct windowed token t gets x_t/penalty if x_t > 0,
  * else x_t*penalty; all logits are divided by temperature; p = softmax;
  * tokens ranked by (p desc, id asc); rank r is kept iff the mass of the ranks
- * before it is < top_p AND p >= min_p * p_max (rank 0 always kept); the draw
- * is the first kept rank whose cumulative kept mass exceeds uniforms[i] times
- * the kept mass.  sampled[i] receives it.
+ * before it is <= top_p (or top_p >= 1) AND p >= min_p * p_max (rank 0
+ * always kept); the draw is the first kept rank whose cumulative kept mass
+ * exceeds uniforms[i] times the kept mass.  sampled[i] receives it.
  * Acceptance: root accepted; node c accepted iff its parent is accepted and
  * tree_tokens[c] == sampled[parents[c]]; the deepest accepted node (ties to
  * the lower index) gives path[0:n_path] (root first) and bonus = its sample.

@@ -20,10 +20,16 @@
 //   truncation     none when top_p >= 1 and min_p <= 0; otherwise the tokens
 //                  with exp(x' - M) >= min_p are collected (at most kCand),
 //                  bitonic-sorted by (x' desc, id asc), and the top-p cut is
-//                  read off their prefix masses (Z over the whole vocabulary)
+//                  read off their prefix masses (Z over the whole vocabulary):
+//                  rank r is kept while the mass before it is <= top_p * Z,
+//                  the smallest set whose mass exceeds top_p (§D.1)
 //   p pass         ws[t] = kept(t) ? exp(x'_t - M) / Z_kept : 0
-//   per rejection  ws[t] = max(ws[t] - q[t], 0), renormalised
-//   bonus          block exclusive scan of per-thread id-ordered segments
+//   per rejection  S = sum max(ws[t] - q[t], 0); when S > 0,
+//                  ws[t] = max(ws[t] - q[t], 0) / S (S = 0 only when nothing
+//                  of p is left above q, and p then stays as it is)
+//   bonus          block exclusive scan of per-thread id-ordered segments;
+//                  the last thread whose segment starts at or below the
+//                  target owns the draw
 // No waits on other CTAs or on barriers with timeouts: loops and block
 // barriers only.  Token ids and parents are range-checked; a violation is
 // reported in the status word.
@@ -110,7 +116,7 @@ reject_accept_kernel(const float* __restrict__ logits, const float* __restrict__
   __shared__ float red[32];
   __shared__ float s_ckey[kCand];
   __shared__ int32_t s_cid[kCand];
-  __shared__ int s_ncand, s_nkeep, s_bonus, s_bad;
+  __shared__ int s_ncand, s_nkeep, s_bonus, s_bad, s_owner, s_accept;
   __shared__ int s_path[64], s_drafted[64];
   __shared__ float s_tot, s_zk;
   const int tid = threadIdx.x;
@@ -204,11 +210,11 @@ reject_accept_kernel(const float* __restrict__ logits, const float* __restrict__
         }
       }
       if (tid == 0) {
-        const float cut = top_p * Zall;
+        const float cut = top_p >= 1.0f ? INFINITY : top_p * Zall;
         float before = 0.f, zk = 0.f;
         int nk = 0;
         for (int r = 0; r < nc; ++r) {
-          if (r > 0 && !(before < cut)) break;
+          if (r > 0 && before > cut) break;
           const float e = expf(s_ckey[r] - M);
           before += e;
           zk += e;
@@ -241,19 +247,18 @@ reject_accept_kernel(const float* __restrict__ logits, const float* __restrict__
         if (tid == 0) s_bad = 1;
         continue;
       }
-      if (u_accept[c] * qn[x] < ws[x]) {
+      // one thread decides, every thread branches on its decision
+      if (tid == 0) s_accept = (u_accept[c] * qn[x] < ws[x]) ? 1 : 0;
+      __syncthreads();
+      if (s_accept) {
         next = c;
         break;
       }
       float part = 0.f;
-      for (int t = tid; t < V; t += kRThreads) {
-        const float r = fmaxf(ws[t] - qn[t], 0.f);
-        ws[t] = r;
-        part += r;
-      }
+      for (int t = tid; t < V; t += kRThreads) part += fmaxf(ws[t] - qn[t], 0.f);
       const float S = block_sum(part, red);
       if (S > 0.f)
-        for (int t = tid; t < V; t += kRThreads) ws[t] = __fdiv_rn(ws[t], S);
+        for (int t = tid; t < V; t += kRThreads) ws[t] = __fdiv_rn(fmaxf(ws[t] - qn[t], 0.f), S);
       __syncthreads();
     }
     if (next >= 0) {
@@ -272,10 +277,19 @@ reject_accept_kernel(const float* __restrict__ logits, const float* __restrict__
     const int t0 = min(V, tid * per), t1 = min(V, t0 + per);
     float seg = 0.f;
     for (int t = t0; t < t1; ++t) seg += ws[t];
-    if (tid == 0) s_bonus = 0x7FFFFFFF;
+    if (tid == 0) {
+      s_bonus = 0x7FFFFFFF;
+      s_owner = -1;
+    }
     const float before = block_excl_scan_f(seg, red, &s_tot);
     const float target = u_draw[node] * s_tot;
-    if (seg > 0.f && before <= target && target < before + seg) {
+    // the owner is the last thread with mass whose segment starts at or
+    // below the target: the scan's rounding can leave a target between one
+    // segment's end and the next one's start, and the owner then takes its
+    // own last token with mass
+    if (seg > 0.f && before <= target) atomicMax(&s_owner, tid);
+    __syncthreads();
+    if (tid == s_owner) {
       float cum = before;
       int pick = -1, last = -1;
       for (int t = t0; t < t1; ++t) {
@@ -286,17 +300,10 @@ reject_accept_kernel(const float* __restrict__ logits, const float* __restrict__
           break;
         }
       }
-      if (pick < 0) pick = last;   // rounding at the segment's end
-      atomicMin(&s_bonus, pick);
+      s_bonus = pick >= 0 ? pick : last;
     }
     __syncthreads();
-    if (s_bonus == 0x7FFFFFFF && tid == 0) {   // target at the very end: the last token with mass
-      for (int t = V - 1; t >= 0; --t)
-        if (ws[t] > 0.f) {
-          s_bonus = t;
-          break;
-        }
-    }
+    if (s_owner < 0 && tid == 0) s_bad = 2;   // no mass left anywhere: not a distribution
     __syncthreads();
     break;
   }
@@ -310,6 +317,11 @@ reject_accept_kernel(const float* __restrict__ logits, const float* __restrict__
       for (int k = 0; k < np; ++k) path[k] = s_path[k];
       *n_path = np;
       *bonus = s_bonus;
+    }
+    if (s_bad == 2) {
+      // only reachable when every target and draft mass is zero or negative
+      // (invalid q rows): no token carries mass, so no bonus is emitted
+      *bonus = -1;
     }
     if (s_bad) set_status(status, TS_ERR_INVALID_ARG);
   }

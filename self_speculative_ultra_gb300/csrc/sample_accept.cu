@@ -3,8 +3,8 @@
 //
 // "TokenSwift: Lossless Acceleration of Ultra Long Sequence Generation":
 // §3.4 Contextual Penalty (penalty on the most recent W tokens), §D.1
-// (top-p: smallest set whose probability mass reaches p; min-p: tokens with
-// p >= p_base * p_max), Table 11 (penalty 1.2 over 1024 tokens, temperature
+// (top-p: smallest set whose cumulative probability exceeds p, every token
+// when p >= 1; min-p: tokens with p >= p_base * p_max), Table 11 (penalty 1.2 over 1024 tokens, temperature
 // 1.0, top-p 0.9, min-p 0.05), §3.1 Overview (exact-match verification, the
 // longest valid draft is kept, then the KV cache is updated).
 //
@@ -16,7 +16,7 @@
 // node maximum).  The last CTA of the node (atomic ticket, no waiting) takes
 // the maximum over the slices, rescales and adds the Z_c, and keeps the
 // candidates with e_t = exp(x'_t - max x') >= min_p.  In rank order (x' desc, id asc) both truncations keep a
-// prefix: top-p keeps ranks up to the first whose inclusive mass reaches
+// prefix: top-p keeps ranks up to the first whose inclusive mass exceeds
 // top_p * Z, min-p keeps the ranks with e >= min_p.  So the kept set always
 // lies inside the min-p set; when that set is small (the usual case:
 // min-p 0.05 keeps the tokens within ln 20 of the top logit) its members are
@@ -38,7 +38,7 @@ constexpr int kCapPart = 4096;           // candidates one slice may publish
 constexpr int kMaxBuckets = 2048;
 constexpr uint32_t kIdMask = 0x3FFFFu;   // V <= 2^18
 
-enum FindMode { kMassGE = 0, kMassGT = 1, kRank = 2 };
+enum FindMode { kMassGT = 1, kRank = 2 };
 
 struct Found {
   int id;
@@ -180,8 +180,7 @@ __device__ void radix_level(const float* __restrict__ xs, int V, float xmax, int
     const float mb = sm.mb;
     const int cb = sm.cb;
     bool cross;
-    if (mode == kMassGE) cross = lc > 0 && mb + im >= target_mass;
-    else if (mode == kMassGT) cross = lc > 0 && mb + im > target_mass;
+    if (mode == kMassGT) cross = lc > 0 && mb + im > target_mass;
     else cross = lc > 0 && cb + ic > target_rank;
     unsigned bal = __ballot_sync(0xffffffffu, cross);
     int src;
@@ -206,8 +205,7 @@ __device__ void radix_level(const float* __restrict__ xs, int V, float xmax, int
         c_at = c;
         const float mn = m + sm.mass[b];
         const int cn = c + sm.cnt[b];
-        bool hit = (mode == kMassGE) ? (mn >= target_mass)
-                 : (mode == kMassGT) ? (mn > target_mass) : (cn > target_rank);
+        bool hit = (mode == kMassGT) ? (mn > target_mass) : (cn > target_rank);
         if (hit) {
           chosen = b;
           break;
@@ -529,9 +527,9 @@ sample_accept_kernel(const float* __restrict__ logits, const int32_t* __restrict
       }
     }
     if (tid < 32) {
-      // warp 0 walks the ranks: top-p cut (first inclusive mass >= top_p*Z),
+      // warp 0 walks the ranks: top-p cut (first inclusive mass > top_p*Z),
       // then the draw (first inclusive mass > u * kept mass)
-      const float tp = eta_mode ? INFINITY : top_p * Z;   // eta: no top-p cut
+      const float tp = (eta_mode || top_p >= 1.0f) ? INFINITY : top_p * Z;   // eta: no top-p cut
       float run = 0.f, zk = 0.f;
       int k_keep = 0;
       for (int b0 = 0; b0 < n_minp; b0 += 32) {
@@ -544,7 +542,7 @@ sample_accept_kernel(const float* __restrict__ logits, const int32_t* __restrict
           if (lane >= o) incl += y;
         }
         incl += run;
-        const unsigned hit = __ballot_sync(0xffffffffu, r < n_minp && incl >= tp);
+        const unsigned hit = __ballot_sync(0xffffffffu, r < n_minp && incl > tp);
         if (hit) {
           const int src = __ffs(hit) - 1;
           k_keep = b0 + src + 1;
@@ -553,7 +551,7 @@ sample_accept_kernel(const float* __restrict__ logits, const int32_t* __restrict
         }
         run = __shfl_sync(0xffffffffu, incl, 31);
       }
-      if (k_keep == 0) {             // top-p reaches past the min-p set
+      if (k_keep == 0) {             // top-p keeps the whole min-p set
         k_keep = n_minp;
         zk = run;
       }
@@ -590,8 +588,8 @@ sample_accept_kernel(const float* __restrict__ logits, const int32_t* __restrict
     }
     int k_keep = n_minp;
     float ZK = Zmin;
-    if (!eta_mode) {
-      const Found f1 = radix_find(xs, V, xmax, kMassGE, top_p * Z, 0, sm);
+    if (!eta_mode && top_p < 1.0f) {
+      const Found f1 = radix_find(xs, V, xmax, kMassGT, top_p * Z, 0, sm);
       k_keep = min(n_minp, f1.rank + 1);
       ZK = (k_keep == f1.rank + 1) ? f1.cum_incl : Zmin;
     }

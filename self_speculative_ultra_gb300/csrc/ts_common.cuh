@@ -114,8 +114,6 @@ __host__ __device__ __forceinline__ size_t part_o4_index(int kv, int s, int n_sp
 }
 
 struct VerifyPlan {
-  bool tc;             // tcgen05 kernel (else the CUDA-core kernel)
-  bool pair;           // the CTA-pair tcgen05 kernel (M = 256, d = 128)
   int M;               // packed query rows per KV head (T * G)
   int n_split;         // KV splits per head
   int64_t keys_per_split;
@@ -129,11 +127,6 @@ int launch_verify_tc(const void* q, const void* k, const void* v, int64_t L, int
                      const int32_t* parents, int T, int Hq, int Hkv, int d, int n_imp,
                      int64_t keys_per_split, int n_split, int n_rg, float* part_o,
                      float* part_ml, float* imp, int32_t* status, cudaStream_t st);
-bool verify_pair_eligible(int T, int Hq, int Hkv, int d);
-int launch_verify_pair(const void* q, const void* k, const void* v, int64_t L, int64_t L_cap,
-                       const int32_t* parents, int T, int Hq, int Hkv, int n_imp,
-                       int64_t keys_per_split, int n_split, float* part_o, float* part_ml,
-                       float* imp, int32_t* status, cudaStream_t st);
 int launch_verify(const void* q, const void* k, const void* v, int64_t L, int64_t L_cap,
                   const int32_t* parents, int T, int Hq, int Hkv, int d, int n_imp,
                   float* o, float* lse, float* imp, void* ws, int32_t* status,

@@ -5,7 +5,8 @@ Path and bonus are integers: they must equal the oracle's exactly, except in
 near-tie cases.  A case is a near-tie when the oracle's own result changes
 under a relative perturbation of 2e-5 of the uniforms (the kernel forms p in
 fp32, the oracle in fp64; 2e-5 covers their difference for these inputs).
-Near-ties are counted and reported.
+In a near-tie the GPU's (path, bonus) must still be one of the oracle's
+results under the perturbations.  Near-ties are counted and reported.
 """
 import numpy as np
 import pytest
@@ -31,9 +32,9 @@ def _oracle(inp, q, W, penalty, temperature, top_p, min_p, ua, ud, literal):
                                 literal=literal)
 
 
-def _run(w, step, top_p=None, min_p=None, literal=False, q=None, seed=0):
+def _run(w, step, top_p=None, min_p=None, literal=False, q=None, seed=0, inp=None):
     import self_speculative_ultra_gb300 as ts
-    inp = syn.sampling_inputs(w, step=step)
+    inp = syn.sampling_inputs(w, step=step) if inp is None else inp
     rng = np.random.default_rng([seed, step])
     top_p = w.top_p if top_p is None else top_p
     min_p = w.min_p if min_p is None else min_p
@@ -51,14 +52,28 @@ def _run(w, step, top_p=None, min_p=None, literal=False, q=None, seed=0):
     got = (path.cpu().numpy()[:n].tolist(), int(bonus.item()))
     args = (inp, q, w.W, w.penalty, w.temperature, top_p, min_p)
     ref = _oracle(*args, ua, ud, literal)
-    variants = {tuple(map(tuple, [ref[0], [ref[1]]]))}
+    return _judge(got, ref, args, ua, ud, literal, step)
+
+
+def _judge(got, ref, args, ua, ud, literal, step):
+    """'exact' when got equals the oracle's result; 'tie' when the oracle's
+    result moves under the 2e-5 perturbations of the uniforms and got is one
+    of the perturbed results; anything else fails."""
+    key = lambda r: (tuple(r[0]), r[1])
+    variants = {key(ref)}
     for f in (1 - 2e-5, 1 + 2e-5):
-        r = _oracle(*args, np.minimum(ua * f, 1 - 1e-7), np.minimum(ud * f, 1 - 1e-7), literal)
-        variants.add(tuple(map(tuple, [r[0], [r[1]]])))
-    if len(variants) > 1:
-        return "tie", got, ref
-    assert got == (list(ref[0]), ref[1]), f"step {step}: gpu {got} oracle {ref}"
-    return "exact", got, ref
+        for fa, fd in ((f, 1.0), (1.0, f), (f, f)):
+            r = _oracle(*args, np.minimum(ua * fa, 1 - 1e-7), np.minimum(ud * fd, 1 - 1e-7),
+                        literal)
+            variants.add(key(r))
+    g = (tuple(got[0]), got[1])
+    if g == key(ref):
+        pu.record_ties("rejection step", 1, 0)
+        return "exact", got, ref
+    assert len(variants) > 1 and g in variants, (
+        f"step {step}: gpu {got} oracle {ref} (perturbed results {sorted(variants)})")
+    pu.record_ties("rejection step", 1, 1)
+    return "tie", got, ref
 
 
 @pytest.mark.parametrize("name,steps", [("tiny", 8), ("llama3.1-8b", 4), ("qwen2.5-14b", 3)])
@@ -68,19 +83,17 @@ def test_configs(name, steps):
     ties = sum(o[0] == "tie" for o in outcomes)
     lengths = [len(o[1][0]) for o in outcomes]
     print(f"{name}: {ties} near-ties of {steps}; accepted path lengths {lengths}")
-    assert ties <= steps // 2
+    assert ties <= 1
 
 
 def test_untruncated_target():
     w = syn.WORKLOADS["llama3.1-8b"]
-    for s in range(3):
-        _run(w, 10 + s, top_p=1.0, min_p=0.0)
+    assert sum(_run(w, 10 + s, top_p=1.0, min_p=0.0)[0] == "tie" for s in range(3)) <= 1
 
 
 def test_literal_penalty():
     w = syn.scaled(syn.WORKLOADS["tiny"], penalty=3.0)
-    for s in range(4):
-        _run(w, 20 + s, literal=True)
+    assert sum(_run(w, 20 + s, literal=True)[0] == "tie" for s in range(4)) <= 1
 
 
 def test_draft_equal_to_target_follows_first_children():
@@ -104,3 +117,30 @@ def test_draft_equal_to_target_follows_first_children():
             kids = [c for c in range(1, w.T) if inp["parents"][c] == node]
             assert nxt == kids[0]
             node = nxt
+
+
+def test_one_hot_target_and_draft_off_support_child():
+    """The root's target is one-hot on token a after truncation, the draft
+    row q[root] is one-hot on the same token, and the root's first child
+    proposes another token b.  That child is rejected (q(b) = 0 = p(b)); the
+    residual max(p - q, 0) is zero everywhere, so the target stays p (a
+    rejection leaves p unchanged when nothing is left) and the bonus drawn
+    from it is a."""
+    w = syn.WORKLOADS["tiny"]
+    inp = syn.sampling_inputs(w, step=5)
+    kids = [c for c in range(1, w.T) if inp["parents"][c] == 0]
+    a = 4321
+    b = (a + 1) % w.V
+    inp["tokens"] = inp["tokens"].copy()
+    inp["tokens"][kids[0]] = b
+    for c in kids[1:]:
+        if inp["tokens"][c] == a:
+            inp["tokens"][c] = (a + 2) % w.V
+    inp["logits"] = inp["logits"].copy()
+    inp["logits"][0, a] = 80.0                 # top-p 0.9 keeps a alone
+    q = _draft(inp["logits"], np.random.default_rng(9))
+    q[0] = 0.0
+    q[0, a] = 1.0
+    kind, got, ref = _run(w, 5, q=q, inp=inp)
+    assert kind == "exact"
+    assert got == ([0], a)

@@ -37,12 +37,7 @@ def _run(w, step=0, logits=None, prior=None, top_p=None, min_p=None, temperature
     ref, infos = orc.sample_all_nodes(logits, prior, inp["parents"], inp["tokens"], W, penalty,
                                       temperature, top_p, min_p, u, return_info=True,
                                       literal=literal)
-    ties = 0
-    for i in range(len(ref)):
-        if sampled[i] != ref[i]:
-            assert infos[i]["margin"] < pu.TIE, (
-                f"node {i}: gpu {sampled[i]} oracle {ref[i]} margin {infos[i]['margin']:.2e}")
-            ties += 1
+    ties = pu.compare_draws(sampled, ref, infos)
     # acceptance is exact given the GPU's own draws (integer work)
     p_ref, b_ref = orc.accept_from_samples(inp["parents"], inp["tokens"], sampled)
     assert path == p_ref and bonus == b_ref

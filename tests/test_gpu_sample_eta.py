@@ -29,12 +29,7 @@ def _run(w, eps, alpha, step=0, logits=None, temperature=None, W=None, uniforms=
     sampled = sampled.cpu().numpy()
     ref, infos = orc.sample_all_nodes_eta(logits, inp["prior"], inp["parents"], inp["tokens"], W,
                                           w.penalty, temperature, eps, alpha, u, return_info=True)
-    ties = 0
-    for i in range(len(ref)):
-        if sampled[i] != ref[i]:
-            assert infos[i]["margin"] < pu.TIE, (
-                f"node {i}: gpu {sampled[i]} oracle {ref[i]} margin {infos[i]['margin']:.2e}")
-            ties += 1
+    ties = pu.compare_draws(sampled, ref, infos, kind="eta draw")
     n = int(n_path.item())
     p_ref, b_ref = orc.accept_from_samples(inp["parents"], inp["tokens"], sampled)
     assert path.cpu().numpy()[:n].tolist() == p_ref and int(bonus.item()) == b_ref
