@@ -373,34 +373,95 @@ class Step:
         ts.ts_kv_commit_batched(self.k, self.v, self.L, w.T, self.path, self.n_path,
                                 table=self.commit_table, status=self.status)
 
+    def capture(self, n_ev: int = 3, e2e: bool = False):
+        """CUDA graphs of the step (the step's launches replay without host
+        issue cost): the resident-input step; n_ev copies that also record an
+        event pair around every verify call (event record nodes); and, for
+        the end-to-end leg, one step per staging buffer."""
+        torch, w = self.torch, self.w
+        self.step()                       # first calls set kernel attributes
+        torch.cuda.synchronize()
+
+        def cap(fn):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                fn()
+            return g
+        self.g_main = cap(self.step)
+        self.ev, self.g_ev = [], []
+        for _ in range(n_ev):
+            e = [[timing_event(external=True) for _ in range(2)] for _ in range(w.layers)]
+            if e[0][0] is None:
+                break
+            self.g_ev.append(cap(lambda e=e: self.step(events=e)))
+            self.ev.append(e)
+        if not self.g_ev:
+            # event record nodes unavailable: a graph of the verify calls alone
+            self.g_ver = cap(self.verify_only)
+        if e2e:
+            self.g_in = [cap(lambda b=b: self.step(inp=self.stage_views[b])) for b in range(2)]
+        torch.cuda.synchronize()
+
+    def verify_only(self):
+        w = self.w
+        for layer in range(w.layers):
+            self.ts.ts_verify_attention(self.q[layer], self.k[layer], self.v[layer], self.L,
+                                        self.parents, n_imp=w.n_imp, o=self.o[layer],
+                                        lse=self.lse[layer], imp=self.imp[layer],
+                                        workspace=self.ws_v, status=self.status)
+
     def launches_per_step(self) -> int:
         # verify: split kernel + merge per layer; batched select: histogram,
         # collect, gather; sample; commit
         return self.w.layers * 2 + 3 + 2
 
 
-def time_steps(st: Step, steps: int, warmup: int):
-    """Device time of `steps` hot-path steps after `warmup` untimed ones
-    (CUDA events on the launching stream), and the verify calls' durations
-    from events in the last three timed steps.  Returns (ms per step, list of
-    verify-call ms)."""
+def timing_event(external: bool = False):
+    """A timing CUDA event; with external=True one that stream capture turns
+    into an event record node (None where this torch cannot)."""
+    import torch
+    if not external:
+        return torch.cuda.Event(enable_timing=True)
+    try:
+        return torch.cuda.Event(enable_timing=True, external=True)
+    except TypeError:
+        return None
+
+
+def time_steps(st: Step, steps: int, warmup: int, barrier=None, clocks=None):
+    """Device time of `steps` hot-path steps (graph replays) after `warmup`
+    untimed ones, CUDA events on the launching stream; the last len(st.g_ev)
+    timed steps also carry an event pair around every verify call.  Returns
+    (ms per step, verify-call ms list, clock record)."""
     torch, w = st.torch, st.w
+    sync = barrier or torch.cuda.synchronize
     for _ in range(warmup):
-        st.step()
-    torch.cuda.synchronize()
-    n_ev = min(3, steps)
-    ev = [[[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(w.layers)]
-          for _ in range(n_ev)]
-    t0 = torch.cuda.Event(enable_timing=True)
-    t1 = torch.cuda.Event(enable_timing=True)
+        st.g_main.replay()
+    sync()
+    n_ev = min(len(st.g_ev), steps)
+    if clocks is not None:
+        clocks.start()
+    t0, t1 = timing_event(), timing_event()
+    sync()
     t0.record()
     for s_ in range(steps):
         k_ev = s_ - (steps - n_ev)
-        st.step(events=ev[k_ev] if k_ev >= 0 else None)
+        (st.g_ev[k_ev] if k_ev >= 0 else st.g_main).replay()
     t1.record()
-    torch.cuda.synchronize()
-    ver_ms = [e[i][0].elapsed_time(e[i][1]) for e in ev for i in range(w.layers)]
-    return t0.elapsed_time(t1) / steps, ver_ms
+    sync()
+    clk = clocks.stop() if clocks is not None else None
+    ms_step = t0.elapsed_time(t1) / steps
+    if n_ev:
+        ver_ms = [e[i][0].elapsed_time(e[i][1]) for e in st.ev[:n_ev] for i in range(w.layers)]
+    else:
+        # one replay of the verify calls alone, timed around the graph
+        v0, v1 = timing_event(), timing_event()
+        v0.record()
+        st.g_ver.replay()
+        v1.record()
+        torch.cuda.synchronize()
+        ver_ms = [v0.elapsed_time(v1) / w.layers]
+    return ms_step, ver_ms, clk
 
 
 def per_config_line(w: syn.Workload, ms_step: float, ver_ms, peak: float, tf_peak: float,
@@ -427,7 +488,8 @@ def measure_other_configs(dev, skip: str, steps: int, warmup: int, peak: float,
             continue
         w = syn.WORKLOADS[name]
         st = Step(w, dev, seed=0, e2e=False)
-        ms_step, ver_ms = time_steps(st, steps, warmup)
+        st.capture()
+        ms_step, ver_ms, _ = time_steps(st, steps, warmup)
         line = per_config_line(w, ms_step, ver_ms, peak, tf_peak, steps)
         line["device_status"] = int(st.status.item())
         out[name] = line
@@ -455,38 +517,22 @@ def run_gpu(args, w: syn.Workload):
             dist.barrier()
         torch.cuda.synchronize()
 
-    for _ in range(args.warmup):
-        st.step()
-    barrier()
-    # device-timed region: inputs resident in HBM.  Per-call verify events are
-    # recorded in the last n_ev timed steps only: an event between two
-    # programmatic-dependent launches holds the next one back.
-    n_ev = min(3, args.steps)
-    ev = [[[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(w.layers)]
-          for _ in range(n_ev)]
+    # the step is replayed from CUDA graphs; the device-timed region has its
+    # inputs resident in HBM.  Per-call verify events are recorded in the last
+    # three timed steps only: an event between two programmatic-dependent
+    # launches holds the next one back.
+    st.capture(n_ev=3, e2e=True)
     clocks = ClockSampler(local)
-    clocks.start()
-    t0 = torch.cuda.Event(enable_timing=True)
-    t1 = torch.cuda.Event(enable_timing=True)
-    barrier()
-    t0.record()
-    for s_ in range(args.steps):
-        k_ev = s_ - (args.steps - n_ev)
-        st.step(events=ev[k_ev] if k_ev >= 0 else None)
-    t1.record()
-    barrier()
-    clk = clocks.stop()
-    ms_total = t0.elapsed_time(t1)
-    # verify-call durations over the last n_ev timed steps
-    ver_ms = [e[i][0].elapsed_time(e[i][1]) for e in ev for i in range(w.layers)]
-    ms = torch.tensor([ms_total], device=dev)
+    ms_step, ver_ms, clk = time_steps(st, args.steps, args.warmup, barrier=barrier, clocks=clocks)
+    ms = torch.tensor([ms_step], device=dev)
     if world > 1:
         dist.all_reduce(ms, op=dist.ReduceOp.MAX)
-    ms_step = float(ms.item()) / args.steps
+    ms_step = float(ms.item())
 
     # end-to-end leg: pinned host inputs in, result out, every step
     for i in range(2):
-        st.step(inp=st.upload_inputs(i))
+        st.upload_inputs(i)
+        st.g_in[i].replay()
         st.release_inputs(i)
         st.download_result()
     barrier()
@@ -500,9 +546,9 @@ def run_gpu(args, w: syn.Workload):
         if s_ + 1 < args.steps:
             st.stage_inputs(s_ + 1)
         ph[s_][0].record()
-        inp = st.unpack_inputs(s_)
+        st.unpack_inputs(s_)
         ph[s_][1].record()
-        st.step(inp=inp)
+        st.g_in[s_ % 2].replay()
         st.release_inputs(s_)
         ph[s_][2].record()
         st.download_result()

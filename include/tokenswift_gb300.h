@@ -55,6 +55,17 @@ const char* ts_last_error(void);
 /* Library ABI version (major*100 + minor). */
 int ts_version(void);
 
+/* Limit of one bounded device-side wait, in SM clock cycles, for kernels
+ * launched after this call (from any thread): the verification kernel of (1)
+ * gives up a wait on another warp's or the copy engine's progress after
+ * `cycles` clocks, writes TS_ERR_TIMEOUT into `status`, waits for its own
+ * copies and tensor-core work in flight (with the default limit), releases
+ * its tensor memory and returns; that call's outputs are then undefined.
+ * `cycles` <= 0 restores the default, 2^31 cycles (about one second).  A
+ * small limit exists to exercise the expiry path; the paper has no
+ * counterpart.  Returns TS_OK. */
+int ts_set_wait_limit(int64_t cycles);
+
 /* ------------------------------------------------------------------------
  * (1) Tree verification attention + attention importance.
  *

@@ -17,6 +17,7 @@ from ._build import LIB_PATH, build  # noqa: F401
 
 __all__ = [
     "TsError", "lib", "build", "ts_status_string", "ts_last_error", "ts_version",
+    "ts_set_wait_limit",
     "ts_verify_workspace_bytes", "ts_verify_attention", "ts_importance_softmax",
     "ts_select_workspace_bytes", "ts_partial_kv_select_gather", "ts_partial_kv_select_gather_noalloc",
     "ts_select_batched_workspace_bytes", "ts_partial_kv_select_gather_batched", "layer_pointer_table",
@@ -35,6 +36,7 @@ _SIGNATURES = {
     "ts_status_string": (ctypes.c_char_p, [_i32]),
     "ts_last_error": (ctypes.c_char_p, []),
     "ts_version": (_i32, []),
+    "ts_set_wait_limit": (_i32, [_i64]),
     "ts_verify_workspace_bytes": (_sz, [_i32, _i32, _i32, _i32, _i64]),
     "ts_verify_attention": (_i32, [_c_void_p, _c_void_p, _c_void_p, _i64, _i64, _c_void_p,
                                    _i32, _i32, _i32, _i32, _i32, _c_void_p, _c_void_p, _c_void_p,
@@ -133,6 +135,12 @@ def ts_last_error() -> str:
 
 def ts_version() -> int:
     return lib().ts_version()
+
+
+def ts_set_wait_limit(cycles: int) -> None:
+    """Limit of one bounded device wait (SM clocks) for later launches;
+    cycles <= 0 restores the default (~1 s)."""
+    _check(lib().ts_set_wait_limit(int(cycles)))
 
 
 def _check(rc: int):

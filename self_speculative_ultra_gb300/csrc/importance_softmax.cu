@@ -205,10 +205,10 @@ importance_softmax_kernel(const __grid_constant__ CUtensorMap tmap_k,
           break;
         }
       }
-      if (aux->abort_flag) {
-        for (int t = max(0, jt - kStages); t < jt; ++t)
-          ptx::mbar_wait(&aux->k_full[t % kStages], (uint32_t)(t / kStages) & 1u, kWaitCycles);
-      }
+      // every issued load must land before the CTA exits, whether or not a
+      // consumer gave up waiting for it (normally these waits return at once)
+      for (int t = max(0, jt - kStages); t < jt; ++t)
+        ptx::mbar_wait(&aux->k_full[t % kStages], (uint32_t)(t / kStages) & 1u, kWaitCycles);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer

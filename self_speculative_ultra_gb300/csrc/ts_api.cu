@@ -1,4 +1,5 @@
 // C-ABI entry points: host-side argument checks, then the launchers.
+#include <atomic>
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
@@ -10,6 +11,9 @@
 namespace ts {
 
 static thread_local char g_last_error[512] = {0};
+
+std::atomic<long long> g_wait_limit{kDefaultWaitCycles};
+long long wait_limit_cycles() { return g_wait_limit.load(); }
 
 int fail(int code, const char* fmt, ...) {
   va_list ap;
@@ -84,6 +88,12 @@ const char* ts_status_string(int s) {
 const char* ts_last_error(void) { return g_last_error; }
 
 int ts_version(void) { return 100; }
+
+int ts_set_wait_limit(int64_t cycles) {
+  clear_error();
+  ts::g_wait_limit.store(cycles > 0 ? (long long)cycles : ts::kDefaultWaitCycles);
+  return TS_OK;
+}
 
 size_t ts_verify_workspace_bytes(int T, int Hq, int Hkv, int d, int64_t L) {
   if (check_attn_shape(T, Hq, Hkv, d, "ts_verify_workspace_bytes") != TS_OK || L < 0) return 0;

@@ -115,18 +115,24 @@ __host__ __device__ __forceinline__ size_t part_o4_index(int kv, int s, int n_sp
 
 struct VerifyPlan {
   int M;               // packed query rows per KV head (T * G)
+  int n_pt;            // row groups of up to 256 rows (pair-tile CTAs, one per split)
+  int n_two;           // a last group of <= 128 rows (two-stream CTAs, one per two splits)
   int n_split;         // KV splits per head
   int64_t keys_per_split;
-  int rows_per_cta;
-  int n_rowblk;
   size_t part_o_bytes, part_ml_bytes, ws_bytes;
 };
 VerifyPlan verify_plan(int T, int Hq, int Hkv, int d, int64_t L);
 int tc_splits(int Hkv, int n_rg, int64_t L, int nsm);
+int verify_splits(int Hkv, int n_pt, int n_two, int64_t L, int nsm);
 int launch_verify_tc(const void* q, const void* k, const void* v, int64_t L, int64_t L_cap,
                      const int32_t* parents, int T, int Hq, int Hkv, int d, int n_imp,
-                     int64_t keys_per_split, int n_split, int n_rg, float* part_o,
+                     int64_t keys_per_split, int n_split, int n_pt, int n_two, float* part_o,
                      float* part_ml, float* imp, int32_t* status, cudaStream_t st);
+
+// Limit (SM clock cycles) of one bounded device wait in the kernels with
+// cross-warp waits; ts_set_wait_limit sets it for later launches.
+constexpr long long kDefaultWaitCycles = 1ll << 31;
+long long wait_limit_cycles();
 int launch_verify(const void* q, const void* k, const void* v, int64_t L, int64_t L_cap,
                   const int32_t* parents, int T, int Hq, int Hkv, int d, int n_imp,
                   float* o, float* lse, float* imp, void* ws, int32_t* status,

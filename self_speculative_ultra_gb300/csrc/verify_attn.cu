@@ -8,8 +8,8 @@
 // Work decomposition: for KV head kv the M = T*G query rows of its group are
 // packed (row r = node r / G, head kv*G + r % G) and the committed cache
 // [0, L) is cut into n_split key ranges; the last range also takes the T
-// tree rows under the ancestor mask.  Each split CTA writes an unnormalised
-// partial (O, m, l) in the log2 domain per row; the merge kernel below
+// tree rows under the ancestor mask.  Every (row, split) gets one
+// unnormalised partial (O, m, l) in the log2 domain; the merge kernel below
 // combines the splits of every row.
 #include "ts_common.cuh"
 
@@ -85,10 +85,16 @@ verify_merge(const float* __restrict__ part_o, const float* __restrict__ part_ml
 VerifyPlan verify_plan(int T, int Hq, int Hkv, int d, int64_t L) {
   VerifyPlan p{};
   p.M = T * (Hq / Hkv);
-  // row groups of up to 256 packed query rows
-  p.n_rowblk = (p.M + 255) / 256;
-  p.rows_per_cta = 256;
-  int n = tc_splits(Hkv, p.n_rowblk, L, kGb300Sms);
+  // rows are taken 256 at a time while more than 128 remain; a remainder of
+  // at most 128 rows is served by two-stream CTAs
+  int rows = p.M;
+  p.n_pt = 0;
+  while (rows > 128) {
+    ++p.n_pt;
+    rows -= 256;
+  }
+  p.n_two = rows > 0 ? 1 : 0;
+  int n = verify_splits(Hkv, p.n_pt, p.n_two, L, kGb300Sms);
   int64_t kps = (L + n - 1) / n;
   kps = (kps + 127) / 128 * 128;
   if (kps < 128) kps = 128;
@@ -112,7 +118,7 @@ int launch_verify(const void* q, const void* k, const void* v, int64_t L, int64_
   float* part_o = static_cast<float*>(ws);
   float* part_ml = reinterpret_cast<float*>(static_cast<char*>(ws) + p.part_o_bytes);
   int rc = launch_verify_tc(q, k, v, L, L_cap, parents, T, Hq, Hkv, d, n_imp, p.keys_per_split,
-                            p.n_split, p.n_rowblk, part_o, part_ml, imp, status, st);
+                            p.n_split, p.n_pt, p.n_two, part_o, part_ml, imp, status, st);
   if (rc) return rc;
   dim3 mgrid((p.M + kMergeRows - 1) / kMergeRows, Hkv);
   cudaLaunchConfig_t cfg = {};

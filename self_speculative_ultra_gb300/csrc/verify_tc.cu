@@ -8,36 +8,52 @@
 // Cache Management (importance = query-key dot products, GQA scores
 // aggregated per group).
 //
-// One CTA = (key split, KV head, row group).  The M = T*G query rows of the
-// KV head's group are packed (row r = node r / G, head kv*G + r % G) into up
-// to two 128-row tiles held in shared memory for the whole CTA, so every K/V
-// tile is read from HBM once per step.  Per 128-key tile j:
-//   TMA (warp 0)        K (2-stage) and V (3-stage) shared-memory rings
-//                       (128-byte swizzle, L2 evict-first)
-//   MMA (warp 1)        S_g = Q_g K^T (bf16, M=128, N=128, fp32 in TMEM); once
-//                       the softmax has written P_g over S_g, O_g += P_g V in
-//                       fp16 with P read from TMEM, then at once S_g of tile
-//                       j+1.  The two row tiles ping-pong: the tensor core
-//                       works on one while the other's softmax runs.
-//   importance (2,3)    imp_j = (sum of the group's last n_imp queries) . k_j
-//                       / sqrt(d) on CUDA cores from the same shared K tile
-//                       (the importance is linear in the queries)
-//   softmax (4..11)     one thread per query row, its scores read from TMEM
-//                       twice (max pass, then exponent pass): tile max, lazy
-//                       running max (O and l are rescaled only when the max
-//                       grows past 2^8), P = 2^(s*log2e/sqrt(d) - m) written
-//                       back over S in fp16 (relative rounding 2^-11, four
-//                       times finer than bf16), row sums.  Tree mask and
-//                       split limits only touch the tiles that need them.
-//   V conversion (12..15) each V tile is converted in place from bf16 to fp16
-//                       as soon as it lands (exact for |v| < 65504; larger
-//                       values saturate and are reported in the status word).
-// Each CTA writes an unnormalised partial (O, m, l) in the log2 domain; the
-// merge kernel of verify_attn.cu combines the splits.
+// The M = T*G query rows of a KV head's group are packed (row r = node r / G,
+// head kv*G + r % G).  Rows are cut into groups of 256 (two 128-row query
+// tiles) while more than 128 remain; a remainder of at most 128 rows forms a
+// last group.  Two kinds of CTA:
+//   pair-tile CTA (a group of up to 256 rows, one key split): two query
+//     tiles in shared memory for the whole CTA, each K/V tile read once and
+//     used by both; the tensor core ping-pongs between the two tiles.
+//   two-stream CTA (a group of at most 128 rows, two consecutive key
+//     splits): one query tile; the two splits are two independent key
+//     streams (even / odd tiles of the sequence), each with its own S and O
+//     in TMEM, so two softmax chains overlap as in the pair-tile CTA.  Its
+//     streams cover the same key ranges as the pair-tile CTAs of the other
+//     rows, which read the same tiles at the same pace (the second read is
+//     an L2 hit).
+// Per 128-key tile:
+//   TMA (warp 0)         K (2 stages; 3 in a two-stream CTA, in the unused
+//                        second query slot) and V (3 stages) shared-memory
+//                        rings, 128-byte swizzle
+//   MMA (warp 1)         S_g = Q K^T (bf16, M=128, N=128, fp32 in TMEM); once
+//                        the softmax has written P_g over S_g, O_g += P_g V in
+//                        fp16 with P read from TMEM, then S_g of group g's
+//                        next tile
+//   importance (2, 3)    imp_j = (sum of the group's last n_imp queries) . k_j
+//                        / sqrt(d) on CUDA cores from the same shared K tile
+//                        (the importance is linear in the queries)
+//   V conversion (4..7)  each V tile converted in place from bf16 to fp16 as
+//                        it lands (exact for |v| < 65504; larger values
+//                        saturate and are reported in the status word)
+//   softmax (8..23)      two warps per TMEM lane quarter and query tile: each
+//                        thread owns one query row and one half (64 keys) of
+//                        the tile.  Tile maximum of its half, exchanged with
+//                        the partner thread through shared memory (both then
+//                        hold the same row maximum), lazy running max (O and
+//                        l rescaled only when the max grows past 2^8, each
+//                        half rescaling its half of O), P = 2^(s*log2e/sqrt(d)
+//                        - m) written back over its half of S in fp16, partial
+//                        row sum.  Tree mask and split limits only touch the
+//                        tiles that need them.
+// Each stream writes an unnormalised partial (O, m, l) per row in the log2
+// domain; the merge kernel of verify_attn.cu combines the splits.
 //
-// Every mbarrier wait is bounded (~1 s of SM clocks); on expiry the CTA
-// records TS_ERR_TIMEOUT in the status word, drains its own in-flight copies
-// and MMAs (again bounded), frees its TMEM and returns.
+// Every mbarrier wait is bounded (a caller-settable limit, ~1 s of SM clocks
+// by default); on expiry the CTA records TS_ERR_TIMEOUT in the status word,
+// waits (with the default limit) for its own in-flight copies and MMAs,
+// frees its TMEM and returns.  The two warps sharing a row exchange a
+// validity flag with every maximum, so they leave the tile loop together.
 #include <cstdlib>
 #include <cstring>
 
@@ -49,34 +65,46 @@ namespace ts {
 namespace {
 
 constexpr int kNk = 128;                 // keys per tile
-constexpr int kSK = 2;                   // K ring depth
 constexpr int kSV = 3;                   // V ring depth
-constexpr int kThreadsTc = 512;          // 16 warps
+constexpr int kThreadsTc = 768;          // 24 warps
+constexpr int kSoftmaxWarp0 = 8;         // warps 8..23
+constexpr int kRegsLaunch = 80;          // registers per thread at launch (768 threads)
+constexpr int kRegsLow = 48;             // warps 0..7 after the set-up
+constexpr int kRegsHigh = 96;            // softmax warps after the set-up
+static_assert(256 * kRegsLow + 512 * kRegsHigh <= kThreadsTc * kRegsLaunch,
+              "register split exceeds the launch's registers");
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLazy = 8.0f;            // running max refreshed only past +2^8
-constexpr long long kWaitCycles = 1ll << 31;
+constexpr long long kDrainCycles = 1ll << 31;
 constexpr uint32_t kNegInf = 0xFF800000u;
 
 struct TcAux {
-  uint64_t k_full[kSK], k_empty[kSK], v_full[kSV], v_conv[kSV], v_empty[kSV];
+  uint64_t k_full[3], k_empty[3], v_full[kSV], v_conv[kSV], v_empty[kSV];
   uint64_t s_full[2], p_ready[2], o_final, drain;
-  unsigned long long anc[64];
-  int32_t par[64];
   uint32_t tmem_base;
   volatile int32_t abort_flag;
 };
+
+// Shared row exchange of the softmax pairs: xch[g][half][row].  During the
+// set-up the same bytes hold the tree's parents and ancestor masks.
+struct SetupScratch {
+  unsigned long long anc[64];
+  int32_t par[64];
+};
+constexpr int kXchBytes = 2 * 2 * 128 * 4;
+static_assert(sizeof(SetupScratch) <= kXchBytes, "set-up scratch must fit the exchange area");
 
 template <int D>
 struct TcLayout {
   static constexpr int kPanel = 128 * 128;         // 128 rows x 64 bf16 (128-byte rows)
   static constexpr int kTile = 128 * D * 2;        // 128 rows x D bf16
-  static constexpr int kQ = 0;
-  static constexpr int kK = kQ + 2 * kTile;
-  static constexpr int kV = kK + kSK * kTile;
+  static constexpr int kQ = 0;                     // Q tile 0 | Q tile 1 (or K stage 2)
+  static constexpr int kK = kQ + 2 * kTile;        // K stages 0, 1
+  static constexpr int kV = kK + 2 * kTile;
   static constexpr int kQsum = kV + kSV * kTile;
-  static constexpr int kAux = kQsum + D * 4;
+  static constexpr int kXch = kQsum + D * 4;
+  static constexpr int kAux = kXch + kXchBytes;
   static constexpr int kBytes = kAux + (int)sizeof(TcAux);
-  static constexpr int kAlloc = kBytes + 1024;     // slack to align the base to 1024 B
   static constexpr uint32_t kTmemCols = 512;
   // TMEM columns: O_g at g*D, S_g (128 fp32; later P) after both O tiles
   __host__ __device__ static constexpr uint32_t obase(int g) { return (uint32_t)(g * D); }
@@ -88,7 +116,56 @@ __device__ __forceinline__ void timeout(TcAux* aux, int32_t* status) {
   set_status(status, TS_ERR_TIMEOUT);
 }
 
-__device__ __forceinline__ float fmax32(const uint32_t (&r)[32]) {
+// One key stream: the split it covers and its tiles.
+// Key positions fit 31 bits (the cache capacity is checked on the host).
+struct Stream {
+  int j0, j1, jend, jlim;   // keys [j0, jend); below jlim no mask is needed
+  int n;                    // tiles
+};
+__device__ __forceinline__ Stream make_stream(int split, int n_split, int64_t kps, int64_t L,
+                                              int T) {
+  Stream s;
+  if (split >= n_split) {
+    s.j0 = s.j1 = s.jend = s.jlim = 0;
+    s.n = 0;
+    return s;
+  }
+  const bool last = split == n_split - 1;
+  s.j0 = (int)((int64_t)split * kps);
+  s.j1 = (int)min(L, (int64_t)s.j0 + kps);
+  s.jend = last ? (int)L + T : s.j1;
+  s.jlim = last ? (int)L : s.j1;
+  s.n = (s.jend - s.j0 + kNk - 1) / kNk;
+  return s;
+}
+
+// Tile sequence of a CTA (the order of the K/V rings).  Pair-tile CTA: one
+// stream, tile s is (both groups, k = s).  Two-stream CTA: the streams'
+// tiles alternate (g0 k0, g1 k0, g0 k1, ...) while both have tiles, then the
+// longer stream's remainder follows.
+struct Seq {
+  bool two;
+  int n0, n1, nmin;
+  __device__ __forceinline__ int total() const { return two ? n0 + n1 : n0; }
+  __device__ __forceinline__ void decode(int s, int& g, int& k) const {
+    if (!two) {
+      g = 0;
+      k = s;
+    } else if (s < 2 * nmin) {
+      g = s & 1;
+      k = s >> 1;
+    } else {
+      g = n0 > n1 ? 0 : 1;
+      k = nmin + (s - 2 * nmin);
+    }
+  }
+  __device__ __forceinline__ int index(int g, int k) const {
+    if (!two) return k;
+    return k < nmin ? 2 * k + g : 2 * nmin + (k - nmin);
+  }
+};
+
+__device__ __forceinline__ float fmax32(const uint32_t* r) {
   float a = ptx::max3(__uint_as_float(r[0]), __uint_as_float(r[1]), __uint_as_float(r[2]));
   float b = ptx::max3(__uint_as_float(r[3]), __uint_as_float(r[4]), __uint_as_float(r[5]));
 #pragma unroll
@@ -104,41 +181,63 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
 verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v,
                  const __nv_bfloat16* __restrict__ q, const int32_t* __restrict__ parents, int T,
                  int Hq, int Hkv, int n_imp, int64_t L, int64_t L_cap, int64_t keys_per_split,
-                 int n_split, float* __restrict__ part_o, float* __restrict__ part_ml,
-                 float* __restrict__ imp, int32_t* status) {
+                 int n_split, int n_pairtile_groups, long long wait_limit,
+                 float* __restrict__ part_o, float* __restrict__ part_ml, float* __restrict__ imp,
+                 int32_t* status) {
   using Ly = TcLayout<D>;
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                           ~uintptr_t(1023));
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* sm = smem_raw;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  // the 128-byte swizzle needs 1024-byte aligned tiles
+  if ((ptx::smem_u32(sm) & 1023u) != 0) {
+    if (tid == 0) set_status(status, TS_ERR_CUDA);
+    return;
+  }
   uint8_t* sq = sm + Ly::kQ;
   uint8_t* sk = sm + Ly::kK;
   uint8_t* sv = sm + Ly::kV;
   float* qsum = reinterpret_cast<float*>(sm + Ly::kQsum);
+  float* xch = reinterpret_cast<float*>(sm + Ly::kXch);
+  SetupScratch* scr = reinterpret_cast<SetupScratch*>(sm + Ly::kXch);
   TcAux* aux = reinterpret_cast<TcAux*>(sm + Ly::kAux);
 
-  const int split = blockIdx.x, kv = blockIdx.y, rg = blockIdx.z;
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  // ---------------------------------------------------------------- which work
+  const int kv = blockIdx.y, x = blockIdx.x;
   const int G = Hq / Hkv, M = T * G;
-  const int r0 = rg * 256;
-  const int nt = min(2, (M - r0 + 127) / 128);
-  const int64_t j0 = (int64_t)split * keys_per_split;
-  const int64_t j1 = min(L, j0 + keys_per_split);
-  const bool last = (split == n_split - 1);
-  const int64_t jend = last ? L + T : j1;
-  const int64_t jlim = last ? L : j1;           // keys below need no mask
-  const int n_tiles = (int)((jend - j0 + kNk - 1) / kNk);
-  const bool do_imp = (imp != nullptr) && rg == 0;
+  const int n_pt = n_pairtile_groups * n_split;     // pair-tile CTAs per head
+  Seq seq;
+  seq.two = x >= n_pt;
+  int r0;
+  Stream st0, st1;
+  if (!seq.two) {
+    const int rg = x / n_split, split = x % n_split;
+    r0 = rg * 256;
+    st0 = make_stream(split, n_split, keys_per_split, L, T);
+    st1 = st0;
+  } else {
+    const int pair = x - n_pt;
+    r0 = n_pairtile_groups * 256;
+    st0 = make_stream(2 * pair, n_split, keys_per_split, L, T);
+    st1 = make_stream(2 * pair + 1, n_split, keys_per_split, L, T);
+  }
+  seq.n0 = st0.n;
+  seq.n1 = seq.two ? st1.n : 0;
+  seq.nmin = min(seq.n0, seq.n1);
+  const int n_seq = seq.total();
+  const int nt = seq.two ? 1 : min(2, (M - r0 + 127) / 128);   // query tiles held
+  const int nK = seq.two ? 3 : 2;                              // K ring depth
+  const bool do_imp = (imp != nullptr) && r0 == 0;
   const float scale = 1.0f / sqrtf((float)D);
   const float sl2 = scale * kLog2e;
-  const int n_pre = min(n_tiles, kSK);          // tiles loaded during the set-up
-  static_assert(kSK < kSV, "early loads fill K and V stages alike; the last V stage is set-up scratch");
+  const int n_pre = min(n_seq, 2);             // tiles loaded during the set-up
+  auto kaddr = [&](int st) -> uint8_t* { return st < 2 ? sk + st * Ly::kTile : sq + Ly::kTile; };
+  auto key0_of = [&](int g, int k) -> int { return (g ? st1.j0 : st0.j0) + k * kNk; };
 
   // ---------------------------------------------------------------- set-up
-  // launched as a programmatic dependent: nothing the previous kernel of the
-  // stream wrote is read before this
-  griddep_wait();
+  // barriers and TMEM first: neither reads what the previous kernel of the
+  // stream wrote, so they overlap its tail (programmatic dependent launch)
   if (tid == 0) {
-    for (int s = 0; s < kSK; ++s) {
+    for (int s = 0; s < 3; ++s) {
       ptx::mbar_init(&aux->k_full[s], 1);
       ptx::mbar_init(&aux->k_empty[s], 1 + 2);   // MMA commit + two importance warps
     }
@@ -149,32 +248,37 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
     }
     for (int g = 0; g < 2; ++g) {
       ptx::mbar_init(&aux->s_full[g], 1);
-      ptx::mbar_init(&aux->p_ready[g], 128);
+      ptx::mbar_init(&aux->p_ready[g], 256);     // both halves of the tile's 128 rows
     }
     ptx::mbar_init(&aux->o_final, 1);
     ptx::mbar_init(&aux->drain, 1);
     aux->abort_flag = 0;
     ptx::fence_mbar_init();
-    // the first K and V tiles go out before the rest of the set-up, which
-    // then runs under their HBM latency; every stage is free at this point
-    const uint64_t pol = ptx::l2_evict_first_policy();
-    const int row0 = (int)(kv * L_cap + j0);
-    for (int jj = 0; jj < n_pre; ++jj) {
-      ptx::mbar_arrive_expect_tx(&aux->k_full[jj], Ly::kTile);
-      for (int p = 0; p < D / 64; ++p)
-        ptx::tma_load_2d(sk + jj * Ly::kTile + p * Ly::kPanel, &tmap_k, &aux->k_full[jj], p * 64,
-                         row0 + jj * kNk, pol);
-      ptx::mbar_arrive_expect_tx(&aux->v_full[jj], Ly::kTile);
-      for (int p = 0; p < D / 64; ++p)
-        ptx::tma_load_2d(sv + jj * Ly::kTile + p * Ly::kPanel, &tmap_v, &aux->v_full[jj], p * 64,
-                         row0 + jj * kNk, pol);
-    }
   }
-  if (tid < T) aux->par[tid] = parents[tid];
   if (warp == 1) {
     ptx::tmem_alloc(&aux->tmem_base, Ly::kTmemCols);
     ptx::tmem_relinquish();
   }
+  griddep_wait();
+  __syncthreads();
+  if (tid == 0) {
+    // the first tiles go out before the rest of the set-up, which then runs
+    // under their HBM latency; every stage is free at this point
+    const uint64_t pol = ptx::l2_evict_first_policy();
+    for (int s = 0; s < n_pre; ++s) {
+      int g, k;
+      seq.decode(s, g, k);
+      const int row = (int)(kv * L_cap + key0_of(g, k));
+      ptx::mbar_arrive_expect_tx(&aux->k_full[s], Ly::kTile);
+      for (int p = 0; p < D / 64; ++p)
+        ptx::tma_load_2d(kaddr(s) + p * Ly::kPanel, &tmap_k, &aux->k_full[s], p * 64, row, pol);
+      ptx::mbar_arrive_expect_tx(&aux->v_full[s], Ly::kTile);
+      for (int p = 0; p < D / 64; ++p)
+        ptx::tma_load_2d(sv + s * Ly::kTile + p * Ly::kPanel, &tmap_v, &aux->v_full[s], p * 64,
+                         row, pol);
+    }
+  }
+  if (tid < T) scr->par[tid] = parents[tid];
   // Q tiles -> shared memory in the 128-byte-swizzled K-major layout
   constexpr int C16 = D / 8;                     // 16-byte chunks per row
   constexpr int kQAll = 2 * 128 * C16, kQPer = (kQAll + kThreadsTc - 1) / kThreadsTc;
@@ -196,8 +300,9 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
 #pragma unroll
     for (int k = 0; k < kQPer; ++k) {
       const int e = tid + k * kThreadsTc;
-      if (e < kQAll) {
-        const int g = e / (128 * C16), rem = e % (128 * C16);
+      const int g = e / (128 * C16);
+      if (e < kQAll && g < nt) {
+        const int rem = e % (128 * C16);
         const int t = rem / C16, c = rem % C16;
         const int p = c >> 3, cc = c & 7;
         *reinterpret_cast<uint4*>(sq + g * Ly::kTile + p * Ly::kPanel + t * 128 +
@@ -206,12 +311,14 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
     }
   }
   __syncthreads();
-  // summed importance queries over the packed rows (T - n_imp) * G .. M - 1:
-  // thread (16-byte column chunk, row slice) partial sums, rows of this
-  // CTA's Q tiles (r0 = 0 here) read back from shared memory; the slices are
-  // folded by shuffles, then across warps through the last V stage, which
-  // the producer fills only after the set-up
+  // summed importance queries over the packed rows (T - n_imp) * G .. M - 1
+  // (r0 = 0 here): thread (16-byte column chunk, row slice) partial sums, the
+  // rows of the CTA's query tiles read back from shared memory, the rest from
+  // global memory; the slices are folded by shuffles, then across warps
+  // through the last V stage, which the producer fills only after the set-up
   float* qpart = reinterpret_cast<float*>(sv + (kSV - 1) * Ly::kTile);
+  constexpr int kQpartWarps = kThreadsTc / 32;
+  static_assert(kQpartWarps * 128 * 4 <= 128 * 64 * 2, "qsum partials must fit one V stage");
   if (do_imp) {
     const int cg = tid % C16, slice = tid / C16, nsl = kThreadsTc / C16;
     const int p = cg >> 3, cc = cg & 7;
@@ -220,9 +327,9 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
     auto add8 = [&](const uint4& u) {
       const uint32_t w[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
-      for (int x = 0; x < 4; ++x)
-        acc[x] = ptx::add2(acc[x], ptx::f2(__uint_as_float(w[x] << 16),
-                                           __uint_as_float(w[x] & 0xFFFF0000u)));
+      for (int x2 = 0; x2 < 4; ++x2)
+        acc[x2] = ptx::add2(acc[x2], ptx::f2(__uint_as_float(w[x2] << 16),
+                                             __uint_as_float(w[x2] & 0xFFFF0000u)));
     };
     int R = (T - n_imp) * G + slice;
 #pragma unroll 4
@@ -238,11 +345,11 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
     }
     float f[8];
 #pragma unroll
-    for (int x = 0; x < 4; ++x) ptx::f2_split(acc[x], f[2 * x], f[2 * x + 1]);
+    for (int x2 = 0; x2 < 4; ++x2) ptx::f2_split(acc[x2], f[2 * x2], f[2 * x2 + 1]);
 #pragma unroll
     for (int off = C16; off < 32; off <<= 1)
 #pragma unroll
-      for (int x = 0; x < 8; ++x) f[x] += __shfl_xor_sync(0xffffffffu, f[x], off);
+      for (int x2 = 0; x2 < 8; ++x2) f[x2] += __shfl_xor_sync(0xffffffffu, f[x2], off);
     if (lane < C16) {
       float4* dst = reinterpret_cast<float4*>(qpart + warp * D + lane * 8);
       dst[0] = make_float4(f[0], f[1], f[2], f[3]);
@@ -252,29 +359,42 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
   // ancestor-or-self masks: node t walks its parent chain (depth < 64)
   if (tid < T) {
     unsigned long long m = 0ull;
-    bool bad = (tid == 0) ? (aux->par[0] != -1) : false;
+    bool bad = (tid == 0) ? (scr->par[0] != -1) : false;
     int a = tid;
     for (int step = 0; step < 64; ++step) {
       m |= 1ull << a;
       if (a == 0) break;
-      const int pa = aux->par[a];
+      const int pa = scr->par[a];
       if (pa < 0 || pa >= a) {
         bad = true;
         break;
       }
       a = pa;
     }
-    aux->anc[tid] = m;
-    if (bad && split == 0 && kv == 0 && rg == 0) set_status(status, TS_ERR_INVALID_ARG);
+    scr->anc[tid] = m;
+    if (bad && x == 0 && kv == 0) set_status(status, TS_ERR_INVALID_ARG);
   }
-  if (do_imp) {
-    __syncthreads();
-    if (tid < D) {
-      float sum = 0.f;
+  __syncthreads();
+  if (do_imp && tid < D) {
+    float sum = 0.f;
 #pragma unroll
-      for (int w = 0; w < kThreadsTc / 32; ++w) sum += qpart[w * D + tid];
-      qsum[tid] = sum;
-    }
+    for (int w = 0; w < kQpartWarps; ++w) sum += qpart[w * D + tid];
+    qsum[tid] = sum;
+  }
+  // each softmax thread takes its row's ancestor mask before the exchange
+  // area is reused
+  unsigned long long anc_row = 0ull;
+  int sm_g = 0, sm_half = 0, sm_t = 0, sm_R = 0;
+  bool sm_valid = false;
+  if (warp >= kSoftmaxWarp0) {
+    const int idx = warp - kSoftmaxWarp0;
+    sm_g = idx >> 3;
+    sm_half = (idx >> 2) & 1;
+    sm_t = (warp & 3) * 32 + lane;
+    sm_R = seq.two ? r0 + sm_t : r0 + sm_g * 128 + sm_t;
+    const bool active = seq.two ? (sm_g == 0 ? seq.n0 > 0 : seq.n1 > 0) : sm_g < nt;
+    sm_valid = active && sm_R < M;
+    anc_row = sm_valid ? scr->anc[sm_R / G] : 0ull;
   }
   ptx::fence_proxy_async_smem();
   ptx::tc_fence_before();
@@ -282,65 +402,74 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
   ptx::tc_fence_after();
   const uint32_t tmem = aux->tmem_base;
   griddep_launch_dependents();   // the merge kernel may take SMs as CTAs retire
+  // registers move from the producer, MMA, importance and conversion
+  // warpgroups (0, 1) to the four softmax warpgroups: 256 x kRegsLow +
+  // 512 x kRegsHigh <= 768 x the launch's 80 (checked on the host)
+  if (warp < kSoftmaxWarp0) {
+    ptx::regs_dec<kRegsLow>();
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       const uint64_t pol = ptx::l2_evict_first_policy();
-      const int row0 = (int)(kv * L_cap + j0);
-      int jk = n_pre, jv = n_pre;   // tiles whose K / V load has been issued
-      for (; jk < n_tiles; ++jk) {
-        const int s = jk % kSK;
-        if (jk >= kSK &&
-            !ptx::mbar_wait(&aux->k_empty[s], (uint32_t)(jk / kSK - 1) & 1u, kWaitCycles)) {
+      int s = n_pre, sv_next = n_pre;   // next tile to load (K), V loads issued
+      for (; s < n_seq; ++s) {
+        int g, k;
+        seq.decode(s, g, k);
+        const int row = (int)(kv * L_cap + key0_of(g, k));
+        const int stK = s % nK;
+        if (s >= nK &&
+            !ptx::mbar_wait(&aux->k_empty[stK], (uint32_t)(s / nK - 1) & 1u, wait_limit)) {
           timeout(aux, status);
           break;
         }
-        ptx::mbar_arrive_expect_tx(&aux->k_full[s], Ly::kTile);
+        ptx::mbar_arrive_expect_tx(&aux->k_full[stK], Ly::kTile);
         for (int p = 0; p < D / 64; ++p)
-          ptx::tma_load_2d(sk + s * Ly::kTile + p * Ly::kPanel, &tmap_k, &aux->k_full[s], p * 64,
-                           row0 + jk * kNk, pol);
-        const int sv_ = jv % kSV;
-        if (jv >= kSV &&
-            !ptx::mbar_wait(&aux->v_empty[sv_], (uint32_t)(jv / kSV - 1) & 1u, kWaitCycles)) {
+          ptx::tma_load_2d(kaddr(stK) + p * Ly::kPanel, &tmap_k, &aux->k_full[stK], p * 64, row,
+                           pol);
+        const int stV = s % kSV;
+        if (s >= kSV &&
+            !ptx::mbar_wait(&aux->v_empty[stV], (uint32_t)(s / kSV - 1) & 1u, wait_limit)) {
           timeout(aux, status);
-          ++jk;
+          ++s;          // this tile's K load is in flight
           break;
         }
-        ptx::mbar_arrive_expect_tx(&aux->v_full[sv_], Ly::kTile);
+        ptx::mbar_arrive_expect_tx(&aux->v_full[stV], Ly::kTile);
         for (int p = 0; p < D / 64; ++p)
-          ptx::tma_load_2d(sv + sv_ * Ly::kTile + p * Ly::kPanel, &tmap_v, &aux->v_full[sv_],
-                           p * 64, row0 + jv * kNk, pol);
-        ++jv;
+          ptx::tma_load_2d(sv + stV * Ly::kTile + p * Ly::kPanel, &tmap_v, &aux->v_full[stV],
+                           p * 64, row, pol);
+        sv_next = s + 1;
         if (aux->abort_flag) {
-          ++jk;
+          ++s;
           break;
         }
       }
-      if (aux->abort_flag) {
-        // drain: wait (bounded) for the loads issued into each stage
-        for (int t = max(0, jk - kSK); t < jk; ++t)
-          ptx::mbar_wait(&aux->k_full[t % kSK], (uint32_t)(t / kSK) & 1u, kWaitCycles);
-        for (int t = max(0, jv - kSV); t < jv; ++t)
-          ptx::mbar_wait(&aux->v_full[t % kSV], (uint32_t)(t / kSV) & 1u, kWaitCycles);
-      }
+      // drain: the copy engine writes this CTA's shared memory, so every
+      // issued load must land before the CTA exits, whether or not a
+      // consumer gave up waiting for it (in a normal run the consumers
+      // already saw each of them and these waits return at once).  Earlier
+      // loads into a stage completed before the stage was refilled.
+      for (int t = max(0, s - nK); t < s; ++t)
+        ptx::mbar_wait(&aux->k_full[t % nK], (uint32_t)(t / nK) & 1u, kDrainCycles);
+      for (int t = max(0, sv_next - kSV); t < sv_next; ++t)
+        ptx::mbar_wait(&aux->v_full[t % kSV], (uint32_t)(t / kSV) & 1u, kDrainCycles);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       constexpr uint32_t idesc_qk = ptx::idesc_bf16_f32(128, kNk, false);
       constexpr uint32_t idesc_pv = ptx::idesc_f16_f32(128, D, true);
-      // operand descriptors: built once; a descriptor's start address is its
-      // low field in 16-byte units, so tile, stage and K-step offsets are adds
+      // operand descriptors: a descriptor's start address is its low field
+      // in 16-byte units, so tile, stage and K-step offsets are adds
       const uint64_t qd0 = ptx::sdesc_sw128(ptx::smem_u32(sq), 16, 1024);
-      const uint64_t kd0 = ptx::sdesc_sw128(ptx::smem_u32(sk), 16, 1024);
       const uint64_t vd0 = ptx::sdesc_sw128(ptx::smem_u32(sv), Ly::kPanel, 1024);
-      constexpr uint32_t kTile16 = Ly::kTile >> 4, kPanel16 = Ly::kPanel >> 4;
-      auto qk = [&](int g, int j) {
-        const uint64_t a0 = qd0 + (uint64_t)(g * kTile16);
-        const uint64_t b0 = kd0 + (uint64_t)((j % kSK) * kTile16);
+      constexpr uint32_t kTile16 = Ly::kTile >> 4;
+      auto qk = [&](int g, int stK) {
+        const uint64_t a0 = qd0 + (uint64_t)((seq.two ? 0 : g) * kTile16);
+        const uint64_t b0 = ptx::sdesc_sw128(ptx::smem_u32(kaddr(stK)), 16, 1024);
 #pragma unroll
         for (int ks = 0; ks < D / 16; ++ks) {
-          const uint32_t off = (ks >> 2) * kPanel16 + (ks & 3) * 2;   // 64-element panels, 32-byte K-steps
+          // 64-element panels, 32-byte K-steps
+          const uint32_t off = (ks >> 2) * (Ly::kPanel >> 4) + (ks & 3) * 2;
           ptx::mma_ss(tmem + Ly::sbase(g), a0 + off, b0 + off, idesc_qk, ks > 0 ? 1u : 0u);
         }
         ptx::mma_commit(&aux->s_full[g]);
@@ -348,70 +477,109 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
       // O += P V in fp16.  Keys [32c, 32c+32) of the tile keep their fp16 P
       // pairs in S_g columns [32c, 32c+16): K-step ks (16 keys) reads the 8
       // columns at 32*(ks/2) + 8*(ks%2); V advances 16 rows (2048 bytes).
-      auto pv = [&](int g, int j) {
-        const uint64_t b0 = vd0 + (uint64_t)((j % kSV) * kTile16);
-        const uint32_t acc = j > 0 ? 1u : 0u;
+      auto pv = [&](int g, int stV, bool acc) {
+        const uint64_t b0 = vd0 + (uint64_t)(stV * kTile16);
 #pragma unroll
         for (int ks = 0; ks < kNk / 16; ++ks) {
           const uint32_t acol = 32 * (ks >> 1) + 8 * (ks & 1);
           ptx::mma_ts(tmem + Ly::obase(g), tmem + Ly::sbase(g) + acol, b0 + (uint64_t)(ks * 128),
-                      idesc_pv, ks > 0 ? 1u : acc);
+                      idesc_pv, (ks > 0 || acc) ? 1u : 0u);
         }
       };
-      bool ok = ptx::mbar_wait(&aux->k_full[0], 0, kWaitCycles);
-      if (ok) {
+      auto wait_k = [&](int s) {
+        if (!ptx::mbar_wait(&aux->k_full[s % nK], (uint32_t)(s / nK) & 1u, wait_limit)) return false;
         ptx::tc_fence_after();
-        for (int g = 0; g < nt; ++g) qk(g, 0);
-        ptx::mma_commit(&aux->k_empty[0]);
-      }
-      for (int j = 0; ok && j < n_tiles; ++j) {
-        if (!ptx::mbar_wait(&aux->v_conv[j % kSV], (uint32_t)(j / kSV) & 1u, kWaitCycles)) {
-          ok = false;
-          break;
+        return true;
+      };
+      bool ok = true;
+      if (!seq.two) {
+        if (n_seq > 0) {
+          ok = wait_k(0);
+          if (ok) {
+            for (int g = 0; g < nt; ++g) qk(g, 0);
+            ptx::mma_commit(&aux->k_empty[0]);
+          }
         }
-        const bool more = j + 1 < n_tiles;
-        for (int g = 0; g < nt && ok; ++g) {
-          if (!ptx::mbar_wait(&aux->p_ready[g], (uint32_t)j & 1u, kWaitCycles)) {
+        for (int s = 0; ok && s < n_seq; ++s) {
+          if (!ptx::mbar_wait(&aux->v_conv[s % kSV], (uint32_t)(s / kSV) & 1u, wait_limit)) {
+            ok = false;
+            break;
+          }
+          const bool more = s + 1 < n_seq;
+          for (int g = 0; g < nt && ok; ++g) {
+            if (!ptx::mbar_wait(&aux->p_ready[g], (uint32_t)s & 1u, wait_limit)) {
+              ok = false;
+              break;
+            }
+            ptx::tc_fence_after();
+            pv(g, s % kSV, s > 0);
+            if (more) {
+              if (g == 0 && !wait_k(s + 1)) {
+                ok = false;
+                break;
+              }
+              qk(g, (s + 1) % nK);
+            }
+          }
+          if (!ok) break;
+          ptx::mma_commit(&aux->v_empty[s % kSV]);
+          if (more) ptx::mma_commit(&aux->k_empty[(s + 1) % nK]);
+        }
+      } else {
+        // first tile of each stream
+        for (int g = 0; g < 2 && ok; ++g) {
+          if ((g ? seq.n1 : seq.n0) == 0) continue;
+          const int s = seq.index(g, 0);
+          ok = wait_k(s);
+          if (ok) {
+            qk(g, s % nK);
+            ptx::mma_commit(&aux->k_empty[s % nK]);
+          }
+        }
+        for (int s = 0; ok && s < n_seq; ++s) {
+          int g, k;
+          seq.decode(s, g, k);
+          if (!ptx::mbar_wait(&aux->v_conv[s % kSV], (uint32_t)(s / kSV) & 1u, wait_limit) ||
+              !ptx::mbar_wait(&aux->p_ready[g], (uint32_t)k & 1u, wait_limit)) {
             ok = false;
             break;
           }
           ptx::tc_fence_after();
-          pv(g, j);
-          if (more) {
-            if (g == 0) {
-              if (!ptx::mbar_wait(&aux->k_full[(j + 1) % kSK], (uint32_t)((j + 1) / kSK) & 1u,
-                                  kWaitCycles)) {
-                ok = false;
-                break;
-              }
-              ptx::tc_fence_after();
+          pv(g, s % kSV, k > 0);
+          ptx::mma_commit(&aux->v_empty[s % kSV]);
+          if (k + 1 < (g ? seq.n1 : seq.n0)) {
+            const int s2 = seq.index(g, k + 1);
+            if (!wait_k(s2)) {
+              ok = false;
+              break;
             }
-            qk(g, j + 1);
+            qk(g, s2 % nK);
+            ptx::mma_commit(&aux->k_empty[s2 % nK]);
           }
         }
-        if (!ok) break;
-        ptx::mma_commit(&aux->v_empty[j % kSV]);
-        if (more) ptx::mma_commit(&aux->k_empty[(j + 1) % kSK]);
       }
       if (!ok) timeout(aux, status);
       ptx::mma_commit(&aux->o_final);
       // drain this thread's MMAs before TMEM is freed
       ptx::mma_commit(&aux->drain);
-      ptx::mbar_wait(&aux->drain, 0, kWaitCycles);
+      ptx::mbar_wait(&aux->drain, 0, kDrainCycles);
     }
   } else if (warp < 4) {
     // ------------------------------------------------------------ importance
     const int t = tid - 64;   // key rows t and t + 64 of each tile
-    for (int j = 0; j < n_tiles; ++j) {
-      const int s = j % kSK;
-      if (aux->abort_flag || !ptx::mbar_wait(&aux->k_full[s], (uint32_t)(j / kSK) & 1u,
-                                             kWaitCycles)) {
+    for (int s = 0; s < n_seq; ++s) {
+      const int stK = s % nK;
+      if (aux->abort_flag ||
+          !ptx::mbar_wait(&aux->k_full[stK], (uint32_t)(s / nK) & 1u, wait_limit)) {
         timeout(aux, status);
         break;
       }
-      const int64_t ja = j0 + (int64_t)j * kNk + t, jb = ja + 64;
+      int g, k;
+      seq.decode(s, g, k);
+      const int ja = key0_of(g, k) + t, jb = ja + 64;
+      const int j1 = g ? st1.j1 : st0.j1;
       if (do_imp && ja < j1) {
-        const uint8_t* ra = sk + s * Ly::kTile + t * 128;
+        const uint8_t* ra = kaddr(stK) + t * 128;
         const uint8_t* rb = ra + 64 * 128;
         uint64_t a0 = 0, a1 = 0, b0 = 0, b1 = 0;
 #pragma unroll
@@ -443,106 +611,116 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
         if (jb < j1) imp[(size_t)kv * L + jb] = (y0 + y1) * scale;
       }
       __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(&aux->k_empty[s]);
+      if (lane == 0) ptx::mbar_arrive(&aux->k_empty[stK]);
     }
-  } else if (warp >= 12) {
+  } else {
     // ------------------------------------------------------------ V conversion
     // V tiles are converted in place from bf16 to fp16 as soon as they land,
     // ahead of the MMA's P V (the V ring is three tiles deep)
-    const int t = tid - 12 * 32;
+    const int t = tid - 4 * 32;
     constexpr int kChunks = Ly::kTile / 16;          // 16-byte chunks per V tile
-    constexpr int kConvThreads = kThreadsTc - 12 * 32;
+    constexpr int kConvThreads = 4 * 32;
     float vmax = 0.f;                                // largest |v| (fp16 range check)
-    for (int j = 0; j < n_tiles; ++j) {
-      const int sv_ = j % kSV;
+    for (int s = 0; s < n_seq; ++s) {
+      const int stV = s % kSV;
       const bool got = !aux->abort_flag &&
-                       ptx::mbar_wait(&aux->v_full[sv_], (uint32_t)(j / kSV) & 1u, kWaitCycles);
+                       ptx::mbar_wait(&aux->v_full[stV], (uint32_t)(s / kSV) & 1u, wait_limit);
       if (!__all_sync(0xffffffffu, got)) {
         timeout(aux, status);
         break;
       }
-      uint4* vt = reinterpret_cast<uint4*>(sv + sv_ * Ly::kTile);
-#pragma unroll 8
+      uint4* vt = reinterpret_cast<uint4*>(sv + stV * Ly::kTile);
+#pragma unroll 4
       for (int e = t; e < kChunks; e += kConvThreads) {
         uint4 u = vt[e];
         uint32_t wd[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
-        for (int x = 0; x < 4; ++x) {
-          const float lo = __uint_as_float(wd[x] << 16), hi = __uint_as_float(wd[x] & 0xFFFF0000u);
+        for (int x2 = 0; x2 < 4; ++x2) {
+          const float lo = __uint_as_float(wd[x2] << 16), hi = __uint_as_float(wd[x2] & 0xFFFF0000u);
           vmax = ptx::max3(vmax, fabsf(lo), fabsf(hi));
-          wd[x] = ptx::pack_f16x2_sat(lo, hi);
+          wd[x2] = ptx::pack_f16x2_sat(lo, hi);
         }
         vt[e] = make_uint4(wd[0], wd[1], wd[2], wd[3]);
       }
       ptx::fence_proxy_async_smem();   // generic writes -> the MMA's async-proxy reads
       __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(&aux->v_conv[sv_]);
+      if (lane == 0) ptx::mbar_arrive(&aux->v_conv[stV]);
     }
     if (!(vmax <= 65504.f)) set_status(status, TS_ERR_UNSUPPORTED);
+  }
   } else {
+    ptx::regs_inc<kRegsHigh>();
     // ------------------------------------------------------------ softmax
-    const int g = (warp - 4) >> 2;
-    const int quarter = warp & 3;
-    const int t = quarter * 32 + lane;            // row within the tile
-    const int R = r0 + g * 128 + t;
-    const bool valid = (g < nt) && (R < M);
-    const unsigned long long anc = valid ? aux->anc[R / G] : 0ull;
-    const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
-    const uint32_t s_addr = tmem + lane_off + Ly::sbase(g);
-    const uint32_t o_addr = tmem + lane_off + Ly::obase(g);
+    const int g = sm_g, half = sm_half, t = sm_t;
+    const bool active = seq.two ? (g == 0 ? seq.n0 > 0 : seq.n1 > 0) : g < nt;
+    const int n_mine = seq.two ? (g == 0 ? seq.n0 : seq.n1) : n_seq;
+    const Stream& my = (seq.two && g == 1) ? st1 : st0;
+    const int bar_id = 1 + g * 4 + (warp & 3);    // the two warps of this lane quarter
+    float* x_mine = xch + (g * 2 + half) * 128 + t;
+    const float* x_other = xch + (g * 2 + (half ^ 1)) * 128 + t;
+    const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
+    const uint32_t s_addr = tmem + lane_off + Ly::sbase(g) + 64 * half;
+    const uint32_t o_addr = tmem + lane_off + Ly::obase(g) + (D / 2) * half;
     float m_used = -INFINITY, l = 0.f;
     bool ok = true;
-    if (g < nt && ok) {
-      // tcgen05.ld/st are warp-collective: every branch around them is warp-uniform
-      for (int j = 0; j < n_tiles; ++j) {
+    if (active) {
+      // tcgen05.ld/st are warp-collective: every branch around them is
+      // warp-uniform, and the two warps of a quarter take the same branches
+      for (int k = 0; k < n_mine; ++k) {
         bool got = !aux->abort_flag &&
-                   ptx::mbar_wait(&aux->s_full[g], (uint32_t)j & 1u, kWaitCycles);
-        if (!__all_sync(0xffffffffu, got)) {
+                   ptx::mbar_wait(&aux->s_full[g], (uint32_t)k & 1u, wait_limit);
+        got = __all_sync(0xffffffffu, got);
+        uint32_t r[64];
+        float mh = -INFINITY;
+        const int key0 = my.j0 + k * kNk;
+        const bool edge = key0 + kNk > my.jlim;     // uniform: depends on the tile only
+        if (got) {
+          ptx::tc_fence_after();
+          ptx::tmem_ld32(s_addr, *reinterpret_cast<uint32_t(*)[32]>(&r[0]));
+          ptx::tmem_ld32(s_addr + 32, *reinterpret_cast<uint32_t(*)[32]>(&r[32]));
+          ptx::tmem_ld_wait();
+          if (edge) {
+            // key0 + xx is visible iff xx < lim or (t_lo <= xx < t_hi and its
+            // tree node xx + sh is on this row's root path); as a bit mask
+            // over this half's 64 keys (bit x2 <-> xx = 64*half + x2)
+            auto clampk = [](int v) { return v < 0 ? 0 : (v > kNk ? kNk : v); };
+            auto lowbits = [](int n) {
+              return n >= 64 ? ~0ull : (n <= 0 ? 0ull : ((1ull << n) - 1ull));
+            };
+            const int h0 = 64 * half;
+            const int lim = clampk(my.jlim - key0);
+            const int t_lo = clampk((int)L - key0);
+            const int t_hi = clampk(my.jend - key0);
+            uint64_t vis = lowbits(lim - h0);
+            const int a = max(t_lo - h0, 0), b = min(t_hi - h0, 64);
+            if (a < b) {
+              const int base = h0 + key0 - (int)L;   // tree node of bit 0
+              const uint64_t tb = base >= 0 ? (base < 64 ? (anc_row >> base) : 0ull)
+                                            : (base > -64 ? (anc_row << -base) : 0ull);
+              vis |= tb & (lowbits(b) & ~lowbits(a));
+            }
+            const uint32_t v0 = (uint32_t)vis, v1 = (uint32_t)(vis >> 32);
+#pragma unroll
+            for (int x2 = 0; x2 < 32; ++x2) {
+              if (!((v0 >> x2) & 1u)) r[x2] = kNegInf;
+              if (!((v1 >> x2) & 1u)) r[32 + x2] = kNegInf;
+            }
+          }
+          mh = fmaxf(fmax32(&r[0]), fmax32(&r[32]));
+        }
+        // exchange the half maxima; a NaN says "this warp gave up"
+        *x_mine = got ? mh : __int_as_float(0x7FFFFFFF);
+        ptx::named_bar_sync(bar_id, 64);
+        const float mo = *x_other;
+        if (!__all_sync(0xffffffffu, got && !isnan(mo))) {
           ok = false;
           break;
         }
-        ptx::tc_fence_after();
-        const int64_t key0 = j0 + (int64_t)j * kNk;
-        const bool edge = key0 + kNk > jlim;       // uniform: depends on the tile only
-        // key0 + x is visible iff x < lim or (t_lo <= x < t_hi and its tree
-        // node x + sh is on this row's root path)
-        auto clampk = [](int64_t v) { return (int)(v < 0 ? 0 : (v > kNk ? kNk : v)); };
-        const int lim = clampk(jlim - key0);
-        const int t_lo = clampk(L - key0);
-        const int t_hi = clampk(jend - key0);
-        const int sh = (int)(key0 - L);
-        auto mask = [&](uint32_t (&r)[32], int c) {
-#pragma unroll
-          for (int x = 0; x < 32; ++x) {
-            const int xx = 32 * c + x;
-            const bool vis = xx < lim ||
-                             (xx >= t_lo && xx < t_hi && ((anc >> ((xx + sh) & 63)) & 1ull));
-            if (!vis) r[x] = kNegInf;
-          }
-        };
-        // pass 1: tile maximum; chunks 0 and 1 are loaded last and stay in
-        // registers for pass 2
-        float mx;
-        uint32_t ca[32], cb[32];
-        ptx::tmem_ld32(s_addr + 64, ca);
-        ptx::tmem_ld32(s_addr + 96, cb);
-        ptx::tmem_ld_wait();
-        if (edge) {
-          mask(ca, 2);
-          mask(cb, 3);
-        }
-        mx = fmaxf(fmax32(ca), fmax32(cb));
-        ptx::tmem_ld32(s_addr, ca);
-        ptx::tmem_ld32(s_addr + 32, cb);
-        ptx::tmem_ld_wait();
-        if (edge) {
-          mask(ca, 0);
-          mask(cb, 1);
-        }
-        mx = fmaxf(mx, fmaxf(fmax32(ca), fmax32(cb)));
-        // lazy running max: raise it only when the tile max exceeds it by 2^8.
-        // S_g of this tile completing implies P_g V of the previous tile did
-        // (MMAs of one thread complete in order), so O_g may be rescaled.
+        const float mx = fmaxf(mh, mo);
+        // lazy running max: raise it only when the tile max exceeds it by
+        // 2^8.  S_g of this tile completing implies P_g V of group g's
+        // previous tile did (MMAs of one thread complete in order), so O_g
+        // may be rescaled (below, before this tile's P is released).
         const float ms = mx * sl2;
         const bool raise = ms > m_used + kLazy;
         const float f = raise ? ptx::ex2(m_used - ms) : 1.f;   // 0 when m_used = -inf
@@ -550,91 +728,93 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
           l *= f;
           m_used = ms;
         }
-        if (j > 0 && __any_sync(0xffffffffu, raise)) {
-#pragma unroll 1
-          for (int c = 0; c < D / 16; ++c) {
-            uint32_t o[16];
-            ptx::tmem_ld16(o_addr + c * 16, o);
-            ptx::tmem_ld_wait();
-#pragma unroll
-            for (int x = 0; x < 16; ++x) o[x] = __float_as_uint(__uint_as_float(o[x]) * f);
-            ptx::tmem_st16(o_addr + c * 16, o);
-          }
-          ptx::tmem_st_wait();
-        }
-        // pass 2: P = 2^(s*sl2 - m) -> fp16 pairs, written over the chunk's
-        // own columns once it has been loaded; two chunks in flight
-        // when the running max is still -inf every score of the row seen so
-        // far, this tile included, is -inf: reference 0 then gives 2^-inf = 0
+        // P = 2^(s*sl2 - m) -> fp16 pairs over the half's S columns: keys
+        // [32c, 32c+32) go to columns [32c, 32c+16).  While the running max
+        // is still -inf every score seen so far is -inf: reference 0 then
+        // gives 2^-inf = 0.
         const float mref = (m_used == -INFINITY) ? 0.f : m_used;
         const uint64_t sl2x2 = ptx::f2(sl2, sl2);
         const uint64_t negm = ptx::f2(-mref, -mref);
         uint64_t lsum = 0;
-        // chunks 0 and 1 arrive masked from pass 1; chunks 2 and 3 are reloaded
-        auto process = [&](uint32_t (&r)[32], int c) {
-          if (edge && c >= 2) mask(r, c);
-          uint32_t pw[16];
 #pragma unroll
-          for (int x = 0; x < 16; ++x) {
+        for (int c = 0; c < 2; ++c) {
+          // packed pairs overwrite the chunk's scores in order (word x2 is
+          // written after scores 2*x2 and 2*x2+1 are read)
+          uint32_t* w = &r[32 * c];
+#pragma unroll
+          for (int x2 = 0; x2 < 16; ++x2) {
             float t0, t1;
-            ptx::f2_split(ptx::fma2(ptx::f2(__uint_as_float(r[2 * x]), __uint_as_float(r[2 * x + 1])),
+            ptx::f2_split(ptx::fma2(ptx::f2(__uint_as_float(w[2 * x2]),
+                                            __uint_as_float(w[2 * x2 + 1])),
                                     sl2x2, negm),
                           t0, t1);
             const float p0 = ptx::ex2(t0), p1 = ptx::ex2(t1);
             lsum = ptx::add2(lsum, ptx::f2(p0, p1));
-            pw[x] = ptx::pack_f16x2(p0, p1);
+            w[x2] = ptx::pack_f16x2(p0, p1);
           }
-          ptx::tmem_st16(s_addr + 32 * c, pw);
-        };
-        process(ca, 0);
-        ptx::tmem_ld32(s_addr + 64, ca);
-        process(cb, 1);
-        ptx::tmem_ld_wait();
-        ptx::tmem_ld32(s_addr + 96, cb);
-        process(ca, 2);
-        ptx::tmem_ld_wait();
-        process(cb, 3);
+          ptx::tmem_st16(s_addr + 32 * c, *reinterpret_cast<uint32_t(*)[16]>(w));
+        }
         {
           float a, c;
           ptx::f2_split(lsum, a, c);
           l += a + c;
         }
         ptx::tmem_st_wait();
+        // O_g rescale for a raised max, once the scores and P words are no
+        // longer held in registers: P_g V of this tile is issued only after
+        // every thread has arrived below
+        if (k > 0 && __any_sync(0xffffffffu, raise)) {
+#pragma unroll 1
+          for (int c = 0; c < D / 32; ++c) {
+            uint32_t o[16];
+            ptx::tmem_ld16(o_addr + c * 16, o);
+            ptx::tmem_ld_wait();
+#pragma unroll
+            for (int x2 = 0; x2 < 16; ++x2) o[x2] = __float_as_uint(__uint_as_float(o[x2]) * f);
+            ptx::tmem_st16(o_addr + c * 16, o);
+          }
+          ptx::tmem_st_wait();
+        }
         ptx::tc_fence_before();
         ptx::mbar_arrive(&aux->p_ready[g]);
       }
-      // epilogue: final O row -> unnormalised partial
-      bool fin = ok && !aux->abort_flag && ptx::mbar_wait(&aux->o_final, 0, kWaitCycles);
-      if (__all_sync(0xffffffffu, fin)) {
+      // epilogue: final O half-row -> unnormalised partial; the halves
+      // exchange their row sums (NaN: this warp gave up)
+      bool fin = ok && !aux->abort_flag && ptx::mbar_wait(&aux->o_final, 0, wait_limit);
+      fin = __all_sync(0xffffffffu, fin);
+      *x_mine = fin ? l : __int_as_float(0x7FFFFFFF);
+      ptx::named_bar_sync(bar_id, 64);
+      const float lo = *x_other;
+      if (__all_sync(0xffffffffu, fin && !isnan(lo))) {
         ptx::tc_fence_after();
+        const int split = (int)(my.j0 / keys_per_split);
         // column-quad-major partial: for each float4 column the warp's 32
         // rows are 512 contiguous bytes
         float4* dst = reinterpret_cast<float4*>(part_o) +
-                      part_o4_index(kv, split, n_split, 0, D, M, valid ? R : 0);
+                      part_o4_index(kv, split, n_split, (D / 8) * half, D, M, sm_valid ? sm_R : 0);
         const size_t c4_stride = (size_t)M;
 #pragma unroll 1
-        for (int c = 0; c < D / 32; ++c) {
+        for (int c = 0; c < D / 64; ++c) {
           uint32_t o[32];
           ptx::tmem_ld32(o_addr + c * 32, o);
           ptx::tmem_ld_wait();
-          if (valid) {
+          if (sm_valid) {
 #pragma unroll
-            for (int x = 0; x < 8; ++x)
-              dst[(size_t)(c * 8 + x) * c4_stride] =
-                  make_float4(__uint_as_float(o[4 * x]), __uint_as_float(o[4 * x + 1]),
-                              __uint_as_float(o[4 * x + 2]), __uint_as_float(o[4 * x + 3]));
+            for (int x2 = 0; x2 < 8; ++x2)
+              dst[(size_t)(c * 8 + x2) * c4_stride] =
+                  make_float4(__uint_as_float(o[4 * x2]), __uint_as_float(o[4 * x2 + 1]),
+                              __uint_as_float(o[4 * x2 + 2]), __uint_as_float(o[4 * x2 + 3]));
           }
         }
-        const size_t base = ((size_t)kv * n_split + split) * M + R;
-        if (valid) {
+        if (sm_valid && half == 0) {
+          const size_t base = ((size_t)kv * n_split + split) * M + sm_R;
           part_ml[base * 2] = m_used;
-          part_ml[base * 2 + 1] = l;
+          part_ml[base * 2 + 1] = l + lo;
         }
       } else {
         timeout(aux, status);
       }
     }
-    if (!ok) timeout(aux, status);
   }
 
   ptx::tc_fence_before();
@@ -685,6 +865,13 @@ int make_kv_map(CUtensorMap* map, const void* base, int Hkv, int64_t L_cap, int 
 // Key splits per (KV head, row group): the count minimising waves x tiles per
 // CTA (+ a fixed per-CTA cost), so the grid fills whole waves of the SMs.
 int tc_splits(int Hkv, int n_rg, int64_t L, int nsm) {
+  return verify_splits(Hkv, n_rg, 0, L, nsm);
+}
+
+// The same for the verification grid: n_pt pair-tile row groups take one CTA
+// per split, n_two two-stream row groups one CTA per two splits; both kinds
+// of CTA take about one chain step per tile of a split.
+int verify_splits(int Hkv, int n_pt, int n_two, int64_t L, int nsm) {
   int64_t max_split = (L + kNk - 1) / kNk;
   if (max_split < 1) max_split = 1;
   if (max_split > 1024) max_split = 1024;
@@ -692,7 +879,7 @@ int tc_splits(int Hkv, int n_rg, int64_t L, int nsm) {
   int64_t best_cost = INT64_MAX;
   for (int n = 1; n <= max_split; ++n) {
     int64_t kps = ((L + n - 1) / n + kNk - 1) / kNk;    // tiles per split
-    int64_t ctas = (int64_t)Hkv * n_rg * n;
+    int64_t ctas = (int64_t)Hkv * ((int64_t)n_pt * n + (int64_t)n_two * ((n + 1) / 2));
     int64_t waves = (ctas + nsm - 1) / nsm;
     int64_t cost = waves * (kps + 3);
     if (cost < best_cost) {
@@ -703,29 +890,44 @@ int tc_splits(int Hkv, int n_rg, int64_t L, int nsm) {
   return best;
 }
 
+size_t verify_tc_smem_bytes(int d) {
+  return d == 128 ? (size_t)TcLayout<128>::kBytes : (size_t)TcLayout<64>::kBytes;
+}
+
 int launch_verify_tc(const void* q, const void* k, const void* v, int64_t L, int64_t L_cap,
                      const int32_t* parents, int T, int Hq, int Hkv, int d, int n_imp,
-                     int64_t keys_per_split, int n_split, int n_rg, float* part_o,
+                     int64_t keys_per_split, int n_split, int n_pt, int n_two, float* part_o,
                      float* part_ml, float* imp, int32_t* status, cudaStream_t st) {
   CUtensorMap mk, mv;
   int rc = make_kv_map(&mk, k, Hkv, L_cap, d);
   if (rc) return rc;
   rc = make_kv_map(&mv, v, Hkv, L_cap, d);
   if (rc) return rc;
-  dim3 grid(n_split, Hkv, n_rg);
+  const int per_head = n_pt * n_split + n_two * ((n_split + 1) / 2);
+  dim3 grid(per_head, Hkv);
   auto qb = static_cast<const __nv_bfloat16*>(q);
+  const long long limit = wait_limit_cycles();
   auto go = [&](auto kern, int smem) {
+    // the warpgroups' register split draws on the launch's registers: a
+    // kernel built with fewer than kRegsLaunch per thread would wait forever
+    cudaFuncAttributes fa{};
+    if (cudaFuncGetAttributes(&fa, kern) != cudaSuccess || fa.numRegs < kRegsLaunch) {
+      rc = fail(TS_ERR_CUDA, "verify_tc_kernel: built with %d registers per thread, %d needed",
+                fa.numRegs, kRegsLaunch);
+      return;
+    }
     cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[1];
     pdl_config(&cfg, attr, grid, dim3(kThreadsTc), smem, st);
     cudaLaunchKernelEx(&cfg, kern, mk, mv, qb, parents, T, Hq, Hkv, n_imp, L, L_cap,
-                       keys_per_split, n_split, part_o, part_ml, imp, status);
+                       keys_per_split, n_split, n_pt, limit, part_o, part_ml, imp, status);
   };
   if (d == 128)
-    go(verify_tc_kernel<128>, TcLayout<128>::kAlloc);
+    go(verify_tc_kernel<128>, TcLayout<128>::kBytes);
   else
-    go(verify_tc_kernel<64>, TcLayout<64>::kAlloc);
+    go(verify_tc_kernel<64>, TcLayout<64>::kBytes);
+  if (rc) return rc;
   return launch_status("verify_tc_kernel");
 }
 
