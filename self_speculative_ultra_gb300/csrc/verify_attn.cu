@@ -18,18 +18,20 @@ namespace ts {
 namespace {
 
 // One CTA per (KV head, block of 8 packed rows); thread (c4, r) owns
-// columns [4*c4, 4*c4+4) of row r and folds the splits in with the
-// online-softmax recurrence (running maximum, rescaled sum and accumulator),
-// the loads of kMergeBatch splits in flight at once.  Launched as a
-// programmatic dependent of the verification kernel: it waits for that grid's
-// partials before its first load.
+// columns [4*c4, 4*c4+4) of row r.  The row's (m, l) pairs give the maximum
+// over the splits first, so every split's weight 2^(m_s - max) is known
+// before its partial is read and the partial loads of all splits are
+// independent (unrolled, several in flight).  Launched as a programmatic
+// dependent of the verification kernel: it waits for that grid's partials
+// before its first load, then lets the next kernel of the stream start its
+// set-up as this grid's CTAs retire.
 constexpr int kMaxSplits = 1024;
 constexpr int kMergeRows = 8;
-constexpr int kMergeBatch = 8;
-__global__ void __launch_bounds__(256, 2)
+__global__ void __launch_bounds__(256)
 verify_merge(const float* __restrict__ part_o, const float* __restrict__ part_ml, int T, int Hq,
              int Hkv, int D, int n_split, float* __restrict__ o, float* __restrict__ lse) {
   griddep_wait();
+  griddep_launch_dependents();
   const int kv = blockIdx.y;
   const int G = Hq / Hkv, M = T * G;
   const int tid = threadIdx.x, r = tid % kMergeRows, c4 = tid / kMergeRows;
@@ -39,45 +41,29 @@ verify_merge(const float* __restrict__ part_o, const float* __restrict__ part_ml
       reinterpret_cast<const float4*>(part_o) + part_o4_index(kv, 0, n_split, c4, D, M, R);
   const size_t step = (size_t)(D / 4) * M;              // float4s between splits
   const float2* ml = reinterpret_cast<const float2*>(part_ml) + (size_t)kv * n_split * M + R;
-  float mrun = -INFINITY, lrun = 0.f;
+  float mmax = -INFINITY;
+#pragma unroll 8
+  for (int s = 0; s < n_split; ++s) mmax = fmaxf(mmax, __ldg(&ml[(size_t)s * M]).x);
+  // every row sees at least its own tree node, so mmax is finite; an empty
+  // split has m = -inf and weight 0
+  float lrun = 0.f;
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  for (int s0 = 0; s0 < n_split; s0 += kMergeBatch) {
-    float4 ov[kMergeBatch];
-    float2 mv[kMergeBatch];
-#pragma unroll
-    for (int k = 0; k < kMergeBatch; ++k) {
-      const int s = s0 + k;
-      if (s < n_split) {
-        ov[k] = src[(size_t)s * step];
-        mv[k] = ml[(size_t)s * M];
-      } else {
-        ov[k] = make_float4(0.f, 0.f, 0.f, 0.f);
-        mv[k] = make_float2(-INFINITY, 0.f);
-      }
-    }
-    float mb = mrun;
-#pragma unroll
-    for (int k = 0; k < kMergeBatch; ++k) mb = fmaxf(mb, mv[k].x);
-    if (mb == -INFINITY) continue;                      // no key seen yet
-    const float fr = exp2f(mrun - mb);                  // 0 while mrun = -inf
-    lrun *= fr;
-    acc = make_float4(acc.x * fr, acc.y * fr, acc.z * fr, acc.w * fr);
-#pragma unroll
-    for (int k = 0; k < kMergeBatch; ++k) {
-      const float w = exp2f(mv[k].x - mb);              // 0 for an empty split
-      lrun += w * mv[k].y;
-      acc.x += w * ov[k].x;
-      acc.y += w * ov[k].y;
-      acc.z += w * ov[k].z;
-      acc.w += w * ov[k].w;
-    }
-    mrun = mb;
+#pragma unroll 8
+  for (int s = 0; s < n_split; ++s) {
+    const float2 mv = __ldg(&ml[(size_t)s * M]);
+    const float4 ov = __ldg(&src[(size_t)s * step]);
+    const float w = exp2f(mv.x - mmax);
+    lrun += w * mv.y;
+    acc.x += w * ov.x;
+    acc.y += w * ov.y;
+    acc.z += w * ov.z;
+    acc.w += w * ov.w;
   }
   const float inv = 1.f / lrun;
   const int i = R / G, h = kv * G + R % G;
   reinterpret_cast<float4*>(o + ((size_t)i * Hq + h) * D)[c4] =
       make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
-  if (lse && c4 == 0) lse[(size_t)i * Hq + h] = (mrun + log2f(lrun)) * 0.6931471805599453f;
+  if (lse && c4 == 0) lse[(size_t)i * Hq + h] = (mmax + log2f(lrun)) * 0.6931471805599453f;
 }
 
 }  // namespace

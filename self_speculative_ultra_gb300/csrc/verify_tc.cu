@@ -36,24 +36,22 @@
 //   V conversion (4..7)  each V tile converted in place from bf16 to fp16 as
 //                        it lands (exact for |v| < 65504; larger values
 //                        saturate and are reported in the status word)
-//   softmax (8..23)      two warps per TMEM lane quarter and query tile: each
-//                        thread owns one query row and one half (64 keys) of
-//                        the tile.  Tile maximum of its half, exchanged with
-//                        the partner thread through shared memory (both then
-//                        hold the same row maximum), lazy running max (O and
-//                        l rescaled only when the max grows past 2^8, each
-//                        half rescaling its half of O), P = 2^(s*log2e/sqrt(d)
-//                        - m) written back over its half of S in fp16, partial
-//                        row sum.  Tree mask and split limits only touch the
-//                        tiles that need them.
+//   softmax (8..15)      one thread per query row, its scores read from TMEM
+//                        twice (max pass, then exponent pass): tile max, lazy
+//                        running max (O and l are rescaled only when the max
+//                        grows past 2^8, after the tile's P stores), P =
+//                        2^(s*log2e/sqrt(d) - m) written back over S in fp16
+//                        (relative rounding 2^-11), row sums.  Tree mask and
+//                        split limits (as bit masks over 64 keys) only touch
+//                        the tiles that need them.
 // Each stream writes an unnormalised partial (O, m, l) per row in the log2
 // domain; the merge kernel of verify_attn.cu combines the splits.
 //
 // Every mbarrier wait is bounded (a caller-settable limit, ~1 s of SM clocks
 // by default); on expiry the CTA records TS_ERR_TIMEOUT in the status word,
 // waits (with the default limit) for its own in-flight copies and MMAs,
-// frees its TMEM and returns.  The two warps sharing a row exchange a
-// validity flag with every maximum, so they leave the tile loop together.
+// frees its TMEM and returns.  The producer always waits for every copy it
+// issued before the CTA exits.
 #include <cstdlib>
 #include <cstring>
 
@@ -66,13 +64,8 @@ namespace {
 
 constexpr int kNk = 128;                 // keys per tile
 constexpr int kSV = 3;                   // V ring depth
-constexpr int kThreadsTc = 768;          // 24 warps
-constexpr int kSoftmaxWarp0 = 8;         // warps 8..23
-constexpr int kRegsLaunch = 80;          // registers per thread at launch (768 threads)
-constexpr int kRegsLow = 48;             // warps 0..7 after the set-up
-constexpr int kRegsHigh = 96;            // softmax warps after the set-up
-static_assert(256 * kRegsLow + 512 * kRegsHigh <= kThreadsTc * kRegsLaunch,
-              "register split exceeds the launch's registers");
+constexpr int kThreadsTc = 512;          // 16 warps
+constexpr int kSoftmaxWarp0 = 8;         // warps 8..15
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLazy = 8.0f;            // running max refreshed only past +2^8
 constexpr long long kDrainCycles = 1ll << 31;
@@ -85,14 +78,11 @@ struct TcAux {
   volatile int32_t abort_flag;
 };
 
-// Shared row exchange of the softmax pairs: xch[g][half][row].  During the
-// set-up the same bytes hold the tree's parents and ancestor masks.
+// The draft tree during the set-up: parents and ancestor-or-self masks.
 struct SetupScratch {
   unsigned long long anc[64];
   int32_t par[64];
 };
-constexpr int kXchBytes = 2 * 2 * 128 * 4;
-static_assert(sizeof(SetupScratch) <= kXchBytes, "set-up scratch must fit the exchange area");
 
 template <int D>
 struct TcLayout {
@@ -102,8 +92,8 @@ struct TcLayout {
   static constexpr int kK = kQ + 2 * kTile;        // K stages 0, 1
   static constexpr int kV = kK + 2 * kTile;
   static constexpr int kQsum = kV + kSV * kTile;
-  static constexpr int kXch = kQsum + D * 4;
-  static constexpr int kAux = kXch + kXchBytes;
+  static constexpr int kTree = kQsum + D * 4;
+  static constexpr int kAux = kTree + (int)sizeof(SetupScratch);
   static constexpr int kBytes = kAux + (int)sizeof(TcAux);
   static constexpr uint32_t kTmemCols = 512;
   // TMEM columns: O_g at g*D, S_g (128 fp32; later P) after both O tiles
@@ -197,8 +187,7 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
   uint8_t* sk = sm + Ly::kK;
   uint8_t* sv = sm + Ly::kV;
   float* qsum = reinterpret_cast<float*>(sm + Ly::kQsum);
-  float* xch = reinterpret_cast<float*>(sm + Ly::kXch);
-  SetupScratch* scr = reinterpret_cast<SetupScratch*>(sm + Ly::kXch);
+  SetupScratch* scr = reinterpret_cast<SetupScratch*>(sm + Ly::kTree);
   TcAux* aux = reinterpret_cast<TcAux*>(sm + Ly::kAux);
 
   // ---------------------------------------------------------------- which work
@@ -248,7 +237,7 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
     }
     for (int g = 0; g < 2; ++g) {
       ptx::mbar_init(&aux->s_full[g], 1);
-      ptx::mbar_init(&aux->p_ready[g], 256);     // both halves of the tile's 128 rows
+      ptx::mbar_init(&aux->p_ready[g], 128);     // one arrival per query row
     }
     ptx::mbar_init(&aux->o_final, 1);
     ptx::mbar_init(&aux->drain, 1);
@@ -381,15 +370,12 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
     for (int w = 0; w < kQpartWarps; ++w) sum += qpart[w * D + tid];
     qsum[tid] = sum;
   }
-  // each softmax thread takes its row's ancestor mask before the exchange
-  // area is reused
+  // each softmax thread: its query tile g and row t
   unsigned long long anc_row = 0ull;
-  int sm_g = 0, sm_half = 0, sm_t = 0, sm_R = 0;
+  int sm_g = 0, sm_t = 0, sm_R = 0;
   bool sm_valid = false;
   if (warp >= kSoftmaxWarp0) {
-    const int idx = warp - kSoftmaxWarp0;
-    sm_g = idx >> 3;
-    sm_half = (idx >> 2) & 1;
+    sm_g = (warp - kSoftmaxWarp0) >> 2;
     sm_t = (warp & 3) * 32 + lane;
     sm_R = seq.two ? r0 + sm_t : r0 + sm_g * 128 + sm_t;
     const bool active = seq.two ? (sm_g == 0 ? seq.n0 > 0 : seq.n1 > 0) : sm_g < nt;
@@ -402,11 +388,6 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
   ptx::tc_fence_after();
   const uint32_t tmem = aux->tmem_base;
   griddep_launch_dependents();   // the merge kernel may take SMs as CTAs retire
-  // registers move from the producer, MMA, importance and conversion
-  // warpgroups (0, 1) to the four softmax warpgroups: 256 x kRegsLow +
-  // 512 x kRegsHigh <= 768 x the launch's 80 (checked on the host)
-  if (warp < kSoftmaxWarp0) {
-    ptx::regs_dec<kRegsLow>();
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
@@ -613,7 +594,7 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(&aux->k_empty[stK]);
     }
-  } else {
+  } else if (warp < kSoftmaxWarp0) {
     // ------------------------------------------------------------ V conversion
     // V tiles are converted in place from bf16 to fp16 as soon as they land,
     // ahead of the MMA's P V (the V ring is three tiles deep)
@@ -647,76 +628,80 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
       if (lane == 0) ptx::mbar_arrive(&aux->v_conv[stV]);
     }
     if (!(vmax <= 65504.f)) set_status(status, TS_ERR_UNSUPPORTED);
-  }
   } else {
-    ptx::regs_inc<kRegsHigh>();
     // ------------------------------------------------------------ softmax
-    const int g = sm_g, half = sm_half, t = sm_t;
+    // one thread per query row t of tile g: all 128 keys of each key tile
+    const int g = sm_g;
     const bool active = seq.two ? (g == 0 ? seq.n0 > 0 : seq.n1 > 0) : g < nt;
     const int n_mine = seq.two ? (g == 0 ? seq.n0 : seq.n1) : n_seq;
     const Stream& my = (seq.two && g == 1) ? st1 : st0;
-    const int bar_id = 1 + g * 4 + (warp & 3);    // the two warps of this lane quarter
-    float* x_mine = xch + (g * 2 + half) * 128 + t;
-    const float* x_other = xch + (g * 2 + (half ^ 1)) * 128 + t;
     const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
-    const uint32_t s_addr = tmem + lane_off + Ly::sbase(g) + 64 * half;
-    const uint32_t o_addr = tmem + lane_off + Ly::obase(g) + (D / 2) * half;
+    const uint32_t s_addr = tmem + lane_off + Ly::sbase(g);
+    const uint32_t o_addr = tmem + lane_off + Ly::obase(g);
     float m_used = -INFINITY, l = 0.f;
     bool ok = true;
     if (active) {
       // tcgen05.ld/st are warp-collective: every branch around them is
-      // warp-uniform, and the two warps of a quarter take the same branches
+      // warp-uniform
       for (int k = 0; k < n_mine; ++k) {
         bool got = !aux->abort_flag &&
                    ptx::mbar_wait(&aux->s_full[g], (uint32_t)k & 1u, wait_limit);
         got = __all_sync(0xffffffffu, got);
-        uint32_t r[64];
-        float mh = -INFINITY;
         const int key0 = my.j0 + k * kNk;
         const bool edge = key0 + kNk > my.jlim;     // uniform: depends on the tile only
+        // visibility of the 64 keys [64*blk, 64*blk + 64) of the tile as a
+        // bit mask: key0 + xx is visible iff xx < lim or (t_lo <= xx < t_hi
+        // and its tree node xx + key0 - L is on this row's root path)
+        auto block_mask = [&](int blk) -> uint64_t {
+          auto clampk = [](int v) { return v < 0 ? 0 : (v > kNk ? kNk : v); };
+          auto lowbits = [](int n) {
+            return n >= 64 ? ~0ull : (n <= 0 ? 0ull : ((1ull << n) - 1ull));
+          };
+          const int h0 = 64 * blk;
+          const int lim = clampk(my.jlim - key0);
+          const int t_lo = clampk((int)L - key0);
+          const int t_hi = clampk(my.jend - key0);
+          uint64_t vis = lowbits(lim - h0);
+          const int a = max(t_lo - h0, 0), b = min(t_hi - h0, 64);
+          if (a < b) {
+            const int base = h0 + key0 - (int)L;   // tree node of bit 0
+            const uint64_t tb = base >= 0 ? (base < 64 ? (anc_row >> base) : 0ull)
+                                          : (base > -64 ? (anc_row << -base) : 0ull);
+            vis |= tb & (lowbits(b) & ~lowbits(a));
+          }
+          return vis;
+        };
+        auto apply = [](uint32_t* r, uint64_t vis) {
+          const uint32_t v0 = (uint32_t)vis, v1 = (uint32_t)(vis >> 32);
+#pragma unroll
+          for (int x2 = 0; x2 < 32; ++x2) {
+            if (!((v0 >> x2) & 1u)) r[x2] = kNegInf;
+            if (!((v1 >> x2) & 1u)) r[32 + x2] = kNegInf;
+          }
+        };
+        auto ld64 = [&](uint32_t col, uint32_t* r) {
+          ptx::tmem_ld32(s_addr + col, *reinterpret_cast<uint32_t(*)[32]>(r));
+          ptx::tmem_ld32(s_addr + col + 32, *reinterpret_cast<uint32_t(*)[32]>(r + 32));
+          ptx::tmem_ld_wait();
+        };
+        uint32_t r[64];
+        float mh = -INFINITY;
         if (got) {
           ptx::tc_fence_after();
-          ptx::tmem_ld32(s_addr, *reinterpret_cast<uint32_t(*)[32]>(&r[0]));
-          ptx::tmem_ld32(s_addr + 32, *reinterpret_cast<uint32_t(*)[32]>(&r[32]));
-          ptx::tmem_ld_wait();
-          if (edge) {
-            // key0 + xx is visible iff xx < lim or (t_lo <= xx < t_hi and its
-            // tree node xx + sh is on this row's root path); as a bit mask
-            // over this half's 64 keys (bit x2 <-> xx = 64*half + x2)
-            auto clampk = [](int v) { return v < 0 ? 0 : (v > kNk ? kNk : v); };
-            auto lowbits = [](int n) {
-              return n >= 64 ? ~0ull : (n <= 0 ? 0ull : ((1ull << n) - 1ull));
-            };
-            const int h0 = 64 * half;
-            const int lim = clampk(my.jlim - key0);
-            const int t_lo = clampk((int)L - key0);
-            const int t_hi = clampk(my.jend - key0);
-            uint64_t vis = lowbits(lim - h0);
-            const int a = max(t_lo - h0, 0), b = min(t_hi - h0, 64);
-            if (a < b) {
-              const int base = h0 + key0 - (int)L;   // tree node of bit 0
-              const uint64_t tb = base >= 0 ? (base < 64 ? (anc_row >> base) : 0ull)
-                                            : (base > -64 ? (anc_row << -base) : 0ull);
-              vis |= tb & (lowbits(b) & ~lowbits(a));
-            }
-            const uint32_t v0 = (uint32_t)vis, v1 = (uint32_t)(vis >> 32);
-#pragma unroll
-            for (int x2 = 0; x2 < 32; ++x2) {
-              if (!((v0 >> x2) & 1u)) r[x2] = kNegInf;
-              if (!((v1 >> x2) & 1u)) r[32 + x2] = kNegInf;
-            }
-          }
+          // keys 64..127 first (reloaded for the exponent pass), then keys
+          // 0..63, which stay in registers
+          ld64(64, r);
+          if (edge) apply(r, block_mask(1));
           mh = fmaxf(fmax32(&r[0]), fmax32(&r[32]));
+          ld64(0, r);
+          if (edge) apply(r, block_mask(0));
+          mh = fmaxf(mh, fmaxf(fmax32(&r[0]), fmax32(&r[32])));
         }
-        // exchange the half maxima; a NaN says "this warp gave up"
-        *x_mine = got ? mh : __int_as_float(0x7FFFFFFF);
-        ptx::named_bar_sync(bar_id, 64);
-        const float mo = *x_other;
-        if (!__all_sync(0xffffffffu, got && !isnan(mo))) {
+        const float mx = mh;
+        if (!got) {
           ok = false;
           break;
         }
-        const float mx = fmaxf(mh, mo);
         // lazy running max: raise it only when the tile max exceeds it by
         // 2^8.  S_g of this tile completing implies P_g V of group g's
         // previous tile did (MMAs of one thread complete in order), so O_g
@@ -728,32 +713,37 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
           l *= f;
           m_used = ms;
         }
-        // P = 2^(s*sl2 - m) -> fp16 pairs over the half's S columns: keys
-        // [32c, 32c+32) go to columns [32c, 32c+16).  While the running max
-        // is still -inf every score seen so far is -inf: reference 0 then
-        // gives 2^-inf = 0.
+        // P = 2^(s*sl2 - m) -> fp16 pairs: keys [32c, 32c+32) of the tile go
+        // to S columns [32c, 32c+16).  While the running max is still -inf
+        // every score seen so far is -inf: reference 0 then gives 2^-inf = 0.
         const float mref = (m_used == -INFINITY) ? 0.f : m_used;
         const uint64_t sl2x2 = ptx::f2(sl2, sl2);
         const uint64_t negm = ptx::f2(-mref, -mref);
         uint64_t lsum = 0;
+        auto exp_store = [&](uint32_t* rr, uint32_t col) {
 #pragma unroll
-        for (int c = 0; c < 2; ++c) {
-          // packed pairs overwrite the chunk's scores in order (word x2 is
-          // written after scores 2*x2 and 2*x2+1 are read)
-          uint32_t* w = &r[32 * c];
+          for (int c = 0; c < 2; ++c) {
+            // packed pairs overwrite the chunk's scores in order (word x2 is
+            // written after scores 2*x2 and 2*x2+1 are read)
+            uint32_t* w = rr + 32 * c;
 #pragma unroll
-          for (int x2 = 0; x2 < 16; ++x2) {
-            float t0, t1;
-            ptx::f2_split(ptx::fma2(ptx::f2(__uint_as_float(w[2 * x2]),
-                                            __uint_as_float(w[2 * x2 + 1])),
-                                    sl2x2, negm),
-                          t0, t1);
-            const float p0 = ptx::ex2(t0), p1 = ptx::ex2(t1);
-            lsum = ptx::add2(lsum, ptx::f2(p0, p1));
-            w[x2] = ptx::pack_f16x2(p0, p1);
+            for (int x2 = 0; x2 < 16; ++x2) {
+              float t0, t1;
+              ptx::f2_split(ptx::fma2(ptx::f2(__uint_as_float(w[2 * x2]),
+                                              __uint_as_float(w[2 * x2 + 1])),
+                                      sl2x2, negm),
+                            t0, t1);
+              const float p0 = ptx::ex2(t0), p1 = ptx::ex2(t1);
+              lsum = ptx::add2(lsum, ptx::f2(p0, p1));
+              w[x2] = ptx::pack_f16x2(p0, p1);
+            }
+            ptx::tmem_st16(s_addr + col + 32 * c, *reinterpret_cast<uint32_t(*)[16]>(w));
           }
-          ptx::tmem_st16(s_addr + 32 * c, *reinterpret_cast<uint32_t(*)[16]>(w));
-        }
+        };
+        exp_store(r, 0);
+        ld64(64, r);
+        if (edge) apply(r, block_mask(1));
+        exp_store(r, 64);
         {
           float a, c;
           ptx::f2_split(lsum, a, c);
@@ -765,7 +755,7 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
         // every thread has arrived below
         if (k > 0 && __any_sync(0xffffffffu, raise)) {
 #pragma unroll 1
-          for (int c = 0; c < D / 32; ++c) {
+          for (int c = 0; c < D / 16; ++c) {
             uint32_t o[16];
             ptx::tmem_ld16(o_addr + c * 16, o);
             ptx::tmem_ld_wait();
@@ -778,23 +768,18 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
         ptx::tc_fence_before();
         ptx::mbar_arrive(&aux->p_ready[g]);
       }
-      // epilogue: final O half-row -> unnormalised partial; the halves
-      // exchange their row sums (NaN: this warp gave up)
+      // epilogue: final O row -> unnormalised partial
       bool fin = ok && !aux->abort_flag && ptx::mbar_wait(&aux->o_final, 0, wait_limit);
-      fin = __all_sync(0xffffffffu, fin);
-      *x_mine = fin ? l : __int_as_float(0x7FFFFFFF);
-      ptx::named_bar_sync(bar_id, 64);
-      const float lo = *x_other;
-      if (__all_sync(0xffffffffu, fin && !isnan(lo))) {
+      if (__all_sync(0xffffffffu, fin)) {
         ptx::tc_fence_after();
         const int split = (int)(my.j0 / keys_per_split);
         // column-quad-major partial: for each float4 column the warp's 32
         // rows are 512 contiguous bytes
         float4* dst = reinterpret_cast<float4*>(part_o) +
-                      part_o4_index(kv, split, n_split, (D / 8) * half, D, M, sm_valid ? sm_R : 0);
+                      part_o4_index(kv, split, n_split, 0, D, M, sm_valid ? sm_R : 0);
         const size_t c4_stride = (size_t)M;
 #pragma unroll 1
-        for (int c = 0; c < D / 64; ++c) {
+        for (int c = 0; c < D / 32; ++c) {
           uint32_t o[32];
           ptx::tmem_ld32(o_addr + c * 32, o);
           ptx::tmem_ld_wait();
@@ -806,10 +791,10 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
                               __uint_as_float(o[4 * x2 + 2]), __uint_as_float(o[4 * x2 + 3]));
           }
         }
-        if (sm_valid && half == 0) {
+        if (sm_valid) {
           const size_t base = ((size_t)kv * n_split + split) * M + sm_R;
           part_ml[base * 2] = m_used;
-          part_ml[base * 2 + 1] = l + lo;
+          part_ml[base * 2 + 1] = l;
         }
       } else {
         timeout(aux, status);
@@ -908,14 +893,6 @@ int launch_verify_tc(const void* q, const void* k, const void* v, int64_t L, int
   auto qb = static_cast<const __nv_bfloat16*>(q);
   const long long limit = wait_limit_cycles();
   auto go = [&](auto kern, int smem) {
-    // the warpgroups' register split draws on the launch's registers: a
-    // kernel built with fewer than kRegsLaunch per thread would wait forever
-    cudaFuncAttributes fa{};
-    if (cudaFuncGetAttributes(&fa, kern) != cudaSuccess || fa.numRegs < kRegsLaunch) {
-      rc = fail(TS_ERR_CUDA, "verify_tc_kernel: built with %d registers per thread, %d needed",
-                fa.numRegs, kRegsLaunch);
-      return;
-    }
     cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[1];
