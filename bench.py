@@ -353,14 +353,14 @@ class Step:
             q, logits, parents, tokens, prior, uniforms = (inp["q"], inp["logits"], inp["parents"],
                                                            inp["tokens"], inp["prior"],
                                                            inp["uniforms"])
+        if events is not None:
+            events[0].record()
         for layer in range(w.layers):
-            if events is not None:
-                events[layer][0].record()
             ts.ts_verify_attention(q[layer], self.k[layer], self.v[layer], self.L, parents,
                                    n_imp=w.n_imp, o=self.o[layer], lse=self.lse[layer],
                                    imp=self.imp[layer], workspace=self.ws_v, status=self.status)
-            if events is not None:
-                events[layer][1].record()
+        if events is not None:
+            events[1].record()
         # partial-cache refresh of every layer in one batched pipeline (read by
         # the next step's drafting only)
         ts.ts_partial_kv_select_gather_batched(self.imp, self.k, self.v, self.L, w.B, w.S, w.R,
@@ -376,11 +376,12 @@ class Step:
     def capture(self, n_ev: int = 3, e2e: bool = False):
         """CUDA graphs of the step (the step's launches replay without host
         issue cost): the resident-input step; n_ev copies that also record an
-        event pair around every verify call (event record nodes); and, for
-        the end-to-end leg, one step per staging buffer."""
+        event pair around the step's block of verify calls (event record
+        nodes); and, for the end-to-end leg, one step per staging buffer."""
         torch, w = self.torch, self.w
         self.step()                       # first calls set kernel attributes
         torch.cuda.synchronize()
+        w = self.w
 
         def cap(fn):
             g = torch.cuda.CUDAGraph()
@@ -390,8 +391,8 @@ class Step:
         self.g_main = cap(self.step)
         self.ev, self.g_ev = [], []
         for _ in range(n_ev):
-            e = [[timing_event(external=True) for _ in range(2)] for _ in range(w.layers)]
-            if e[0][0] is None:
+            e = [timing_event(external=True) for _ in range(2)]
+            if e[0] is None:
                 break
             self.g_ev.append(cap(lambda e=e: self.step(events=e)))
             self.ev.append(e)
@@ -431,8 +432,9 @@ def timing_event(external: bool = False):
 def time_steps(st: Step, steps: int, warmup: int, barrier=None, clocks=None):
     """Device time of `steps` hot-path steps (graph replays) after `warmup`
     untimed ones, CUDA events on the launching stream; the last len(st.g_ev)
-    timed steps also carry an event pair around every verify call.  Returns
-    (ms per step, verify-call ms list, clock record)."""
+    timed steps also carry an event pair around their block of verify calls.
+    Returns (ms per step, list of mean verify-call ms per event-carrying step,
+    clock record)."""
     torch, w = st.torch, st.w
     sync = barrier or torch.cuda.synchronize
     for _ in range(warmup):
@@ -452,7 +454,9 @@ def time_steps(st: Step, steps: int, warmup: int, barrier=None, clocks=None):
     clk = clocks.stop() if clocks is not None else None
     ms_step = t0.elapsed_time(t1) / steps
     if n_ev:
-        ver_ms = [e[i][0].elapsed_time(e[i][1]) for e in st.ev[:n_ev] for i in range(w.layers)]
+        # per step: the block of verify calls (programmatic overlap between
+        # calls intact) / layers
+        ver_ms = [e[0].elapsed_time(e[1]) / w.layers for e in st.ev[:n_ev]]
     else:
         # one replay of the verify calls alone, timed around the graph
         v0, v1 = timing_event(), timing_event()

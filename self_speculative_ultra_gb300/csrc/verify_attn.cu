@@ -17,53 +17,97 @@ namespace ts {
 
 namespace {
 
-// One CTA per (KV head, block of 8 packed rows); thread (c4, r) owns
-// columns [4*c4, 4*c4+4) of row r.  The row's (m, l) pairs give the maximum
-// over the splits first, so every split's weight 2^(m_s - max) is known
-// before its partial is read and the partial loads of all splits are
-// independent (unrolled, several in flight).  Launched as a programmatic
-// dependent of the verification kernel: it waits for that grid's partials
-// before its first load, then lets the next kernel of the stream start its
-// set-up as this grid's CTAs retire.
+// Thread (row R, float4 column c4, split group j) folds splits j, j + NG,
+// j + 2*NG, ... of its row with the online-softmax recurrence, kPer partial
+// loads in flight at once (one round trip for up to NG * kPer splits); the
+// NG states of a (row, column) sit in lanes 32/NG apart of one warp and are
+// combined by shuffles.  A warp covers 32/NG consecutive rows x NG split
+// groups of one column, so each group's loads are contiguous.  NG (1, 2 or
+// 4) is the largest that keeps the grid within one wave of the SMs: a
+// second wave of merge CTAs holds SMs the next verification grid waits for.
+// Launched as a programmatic dependent of the verification kernel: it waits
+// for that grid's partials before its first load, then lets the next kernel
+// of the stream start its set-up as this grid's CTAs retire.
 constexpr int kMaxSplits = 1024;
-constexpr int kMergeRows = 8;
-__global__ void __launch_bounds__(256)
+constexpr int kPer = 5;              // loads in flight per thread
+constexpr int kMergeThreads = 256;   // 8 warps: 8 float4 columns per CTA
+constexpr int kMergeCtasPerSm = 5;   // at <= 48 registers
+template <int NG>
+__global__ void __launch_bounds__(kMergeThreads, kMergeCtasPerSm)
 verify_merge(const float* __restrict__ part_o, const float* __restrict__ part_ml, int T, int Hq,
              int Hkv, int D, int n_split, float* __restrict__ o, float* __restrict__ lse) {
+  constexpr int kRows = 32 / NG;      // rows per warp
   griddep_wait();
   griddep_launch_dependents();
-  const int kv = blockIdx.y;
+  const int kv = blockIdx.z;
   const int G = Hq / Hkv, M = T * G;
-  const int tid = threadIdx.x, r = tid % kMergeRows, c4 = tid / kMergeRows;
-  const int R = blockIdx.x * kMergeRows + r;
-  if (R >= M) return;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int r = lane % kRows, j = lane / kRows;                  // row in block, split group
+  const int c4 = blockIdx.y * (kMergeThreads / 32) + warp;       // float4 column
+  const int R = blockIdx.x * kRows + r;
+  const bool live = R < M && c4 < D / 4;
+  const int Rc = live ? R : 0, cc = live ? c4 : 0;
   const float4* src =
-      reinterpret_cast<const float4*>(part_o) + part_o4_index(kv, 0, n_split, c4, D, M, R);
+      reinterpret_cast<const float4*>(part_o) + part_o4_index(kv, 0, n_split, cc, D, M, Rc);
   const size_t step = (size_t)(D / 4) * M;              // float4s between splits
-  const float2* ml = reinterpret_cast<const float2*>(part_ml) + (size_t)kv * n_split * M + R;
-  float mmax = -INFINITY;
-#pragma unroll 8
-  for (int s = 0; s < n_split; ++s) mmax = fmaxf(mmax, __ldg(&ml[(size_t)s * M]).x);
-  // every row sees at least its own tree node, so mmax is finite; an empty
-  // split has m = -inf and weight 0
-  float lrun = 0.f;
+  const float2* ml = reinterpret_cast<const float2*>(part_ml) + (size_t)kv * n_split * M + Rc;
+  float mrun = -INFINITY, lrun = 0.f;
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 8
-  for (int s = 0; s < n_split; ++s) {
-    const float2 mv = __ldg(&ml[(size_t)s * M]);
-    const float4 ov = __ldg(&src[(size_t)s * step]);
-    const float w = exp2f(mv.x - mmax);
-    lrun += w * mv.y;
-    acc.x += w * ov.x;
-    acc.y += w * ov.y;
-    acc.z += w * ov.z;
-    acc.w += w * ov.w;
+  for (int s0 = j; s0 < n_split; s0 += NG * kPer) {
+    float4 ov[kPer];
+    float2 mv[kPer];
+#pragma unroll
+    for (int k = 0; k < kPer; ++k) {
+      const int s = s0 + k * NG;
+      if (live && s < n_split) {
+        ov[k] = __ldg(&src[(size_t)s * step]);
+        mv[k] = __ldg(&ml[(size_t)s * M]);
+      } else {
+        ov[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+        mv[k] = make_float2(-INFINITY, 0.f);
+      }
+    }
+    float mb = mrun;
+#pragma unroll
+    for (int k = 0; k < kPer; ++k) mb = fmaxf(mb, mv[k].x);
+    if (mb == -INFINITY) continue;                      // no key seen yet
+    const float fr = exp2f(mrun - mb);                  // 0 while mrun = -inf
+    lrun *= fr;
+    acc = make_float4(acc.x * fr, acc.y * fr, acc.z * fr, acc.w * fr);
+#pragma unroll
+    for (int k = 0; k < kPer; ++k) {
+      const float w = exp2f(mv[k].x - mb);              // 0 for an empty split
+      lrun += w * mv[k].y;
+      acc.x += w * ov[k].x;
+      acc.y += w * ov[k].y;
+      acc.z += w * ov[k].z;
+      acc.w += w * ov[k].w;
+    }
+    mrun = mb;
   }
+  // combine the split groups (lanes r, r + kRows, ...)
+#pragma unroll
+  for (int off = kRows; off < 32; off <<= 1) {
+    const float m2 = __shfl_xor_sync(0xffffffffu, mrun, off);
+    const float l2 = __shfl_xor_sync(0xffffffffu, lrun, off);
+    const float4 a2 = make_float4(__shfl_xor_sync(0xffffffffu, acc.x, off),
+                                  __shfl_xor_sync(0xffffffffu, acc.y, off),
+                                  __shfl_xor_sync(0xffffffffu, acc.z, off),
+                                  __shfl_xor_sync(0xffffffffu, acc.w, off));
+    const float mn = fmaxf(mrun, m2);
+    const float f1 = mrun == -INFINITY ? 0.f : exp2f(mrun - mn);
+    const float f2 = m2 == -INFINITY ? 0.f : exp2f(m2 - mn);
+    lrun = lrun * f1 + l2 * f2;
+    acc = make_float4(acc.x * f1 + a2.x * f2, acc.y * f1 + a2.y * f2, acc.z * f1 + a2.z * f2,
+                      acc.w * f1 + a2.w * f2);
+    mrun = mn;
+  }
+  if (!live || j != 0) return;
   const float inv = 1.f / lrun;
   const int i = R / G, h = kv * G + R % G;
   reinterpret_cast<float4*>(o + ((size_t)i * Hq + h) * D)[c4] =
       make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
-  if (lse && c4 == 0) lse[(size_t)i * Hq + h] = (mmax + log2f(lrun)) * 0.6931471805599453f;
+  if (lse && c4 == 0) lse[(size_t)i * Hq + h] = (mrun + log2f(lrun)) * 0.6931471805599453f;
 }
 
 }  // namespace
@@ -106,12 +150,22 @@ int launch_verify(const void* q, const void* k, const void* v, int64_t L, int64_
   int rc = launch_verify_tc(q, k, v, L, L_cap, parents, T, Hq, Hkv, d, n_imp, p.keys_per_split,
                             p.n_split, p.n_pt, p.n_two, part_o, part_ml, imp, status, st);
   if (rc) return rc;
-  dim3 mgrid((p.M + kMergeRows - 1) / kMergeRows, Hkv);
+  const int ny = (d / 4 + 7) / 8;
+  auto ctas = [&](int ng) { return (p.M + 32 / ng - 1) / (32 / ng) * ny * Hkv; };
+  const int wave = kMergeCtasPerSm * kGb300Sms;
+  const int ng = ctas(4) <= wave ? 4 : (ctas(2) <= wave ? 2 : 1);
+  dim3 mgrid((p.M + 32 / ng - 1) / (32 / ng), ny, Hkv);
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
-  pdl_config(&cfg, attr, mgrid, dim3(kMergeRows * (d / 4)), 0, st);
-  cudaLaunchKernelEx(&cfg, verify_merge, static_cast<const float*>(part_o),
-                     static_cast<const float*>(part_ml), T, Hq, Hkv, d, p.n_split, o, lse);
+  pdl_config(&cfg, attr, mgrid, dim3(kMergeThreads), 0, st);
+  auto po = static_cast<const float*>(part_o);
+  auto pm = static_cast<const float*>(part_ml);
+  if (ng == 4)
+    cudaLaunchKernelEx(&cfg, verify_merge<4>, po, pm, T, Hq, Hkv, d, p.n_split, o, lse);
+  else if (ng == 2)
+    cudaLaunchKernelEx(&cfg, verify_merge<2>, po, pm, T, Hq, Hkv, d, p.n_split, o, lse);
+  else
+    cudaLaunchKernelEx(&cfg, verify_merge<1>, po, pm, T, Hq, Hkv, d, p.n_split, o, lse);
   return launch_status("verify_merge");
 }
 

@@ -250,23 +250,6 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
   }
   griddep_wait();
   __syncthreads();
-  if (tid == 0) {
-    // the first tiles go out before the rest of the set-up, which then runs
-    // under their HBM latency; every stage is free at this point
-    const uint64_t pol = ptx::l2_evict_first_policy();
-    for (int s = 0; s < n_pre; ++s) {
-      int g, k;
-      seq.decode(s, g, k);
-      const int row = (int)(kv * L_cap + key0_of(g, k));
-      ptx::mbar_arrive_expect_tx(&aux->k_full[s], Ly::kTile);
-      for (int p = 0; p < D / 64; ++p)
-        ptx::tma_load_2d(kaddr(s) + p * Ly::kPanel, &tmap_k, &aux->k_full[s], p * 64, row, pol);
-      ptx::mbar_arrive_expect_tx(&aux->v_full[s], Ly::kTile);
-      for (int p = 0; p < D / 64; ++p)
-        ptx::tma_load_2d(sv + s * Ly::kTile + p * Ly::kPanel, &tmap_v, &aux->v_full[s], p * 64,
-                         row, pol);
-    }
-  }
   if (tid < T) scr->par[tid] = parents[tid];
   // Q tiles -> shared memory in the 128-byte-swizzled K-major layout
   constexpr int C16 = D / 8;                     // 16-byte chunks per row
@@ -284,6 +267,23 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
       if (e < kQAll && g < nt && R < M) {
         const int i = R / G, h = kv * G + R % G;
         val[k] = __ldg(reinterpret_cast<const uint4*>(q + ((size_t)i * Hq + h) * D + c * 8));
+      }
+    }
+    if (tid == 0) {
+      // the first K/V tiles go out right behind the query loads; the rest
+      // of the set-up runs under their HBM latency.  Every stage is free.
+      const uint64_t pol = ptx::l2_evict_first_policy();
+      for (int s = 0; s < n_pre; ++s) {
+        int g, k;
+        seq.decode(s, g, k);
+        const int row = (int)(kv * L_cap + key0_of(g, k));
+        ptx::mbar_arrive_expect_tx(&aux->k_full[s], Ly::kTile);
+        for (int p = 0; p < D / 64; ++p)
+          ptx::tma_load_2d(kaddr(s) + p * Ly::kPanel, &tmap_k, &aux->k_full[s], p * 64, row, pol);
+        ptx::mbar_arrive_expect_tx(&aux->v_full[s], Ly::kTile);
+        for (int p = 0; p < D / 64; ++p)
+          ptx::tma_load_2d(sv + s * Ly::kTile + p * Ly::kPanel, &tmap_v, &aux->v_full[s], p * 64,
+                           row, pol);
       }
     }
 #pragma unroll
@@ -455,10 +455,13 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
         }
         ptx::mma_commit(&aux->s_full[g]);
       };
-      // O += P V in fp16.  Keys [32c, 32c+32) of the tile keep their fp16 P
-      // pairs in S_g columns [32c, 32c+16): K-step ks (16 keys) reads the 8
-      // columns at 32*(ks/2) + 8*(ks%2); V advances 16 rows (2048 bytes).
-      auto pv = [&](int g, int stV, bool acc) {
+      // O += P V in fp16 once the softmax has stored P (phase ph of the P
+      // barrier).  Keys [32c, 32c+32) of the tile keep their fp16 P pairs in
+      // S_g columns [32c, 32c+16): K-step ks (16 keys) reads the 8 columns at
+      // 32*(ks/2) + 8*(ks%2); V advances 16 rows (2048 bytes).
+      auto pv = [&](int g, int stV, bool acc, uint32_t ph) {
+        if (!ptx::mbar_wait(&aux->p_ready[g], ph, wait_limit)) return false;
+        ptx::tc_fence_after();
         const uint64_t b0 = vd0 + (uint64_t)(stV * kTile16);
 #pragma unroll
         for (int ks = 0; ks < kNk / 16; ++ks) {
@@ -466,6 +469,7 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
           ptx::mma_ts(tmem + Ly::obase(g), tmem + Ly::sbase(g) + acol, b0 + (uint64_t)(ks * 128),
                       idesc_pv, (ks > 0 || acc) ? 1u : 0u);
         }
+        return true;
       };
       auto wait_k = [&](int s) {
         if (!ptx::mbar_wait(&aux->k_full[s % nK], (uint32_t)(s / nK) & 1u, wait_limit)) return false;
@@ -488,12 +492,10 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
           }
           const bool more = s + 1 < n_seq;
           for (int g = 0; g < nt && ok; ++g) {
-            if (!ptx::mbar_wait(&aux->p_ready[g], (uint32_t)s & 1u, wait_limit)) {
+            if (!pv(g, s % kSV, s > 0, (uint32_t)s & 1u)) {
               ok = false;
               break;
             }
-            ptx::tc_fence_after();
-            pv(g, s % kSV, s > 0);
             if (more) {
               if (g == 0 && !wait_k(s + 1)) {
                 ok = false;
@@ -521,12 +523,10 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
           int g, k;
           seq.decode(s, g, k);
           if (!ptx::mbar_wait(&aux->v_conv[s % kSV], (uint32_t)(s / kSV) & 1u, wait_limit) ||
-              !ptx::mbar_wait(&aux->p_ready[g], (uint32_t)k & 1u, wait_limit)) {
+              !pv(g, s % kSV, k > 0, (uint32_t)k & 1u)) {
             ok = false;
             break;
           }
-          ptx::tc_fence_after();
-          pv(g, s % kSV, k > 0);
           ptx::mma_commit(&aux->v_empty[s % kSV]);
           if (k + 1 < (g ? seq.n1 : seq.n0)) {
             const int s2 = seq.index(g, k + 1);
