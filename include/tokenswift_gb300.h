@@ -337,17 +337,16 @@ int ts_penalized_sample_accept_eta(const float* logits, const int32_t* tree_toke
  * next child is tried.  When no child is accepted, the bonus token is drawn
  * from the current p_n with u_draw[n], by inverse CDF over token ids.
  *
- * logits [T, V] fp32; q [T, V] fp32 (rows sum to 1; row n is only read when
- * n is on the accepted path); tree_tokens, parents [T] int32; prior
- * [n_prior] int32 ending with the root token; u_accept, u_draw [T] fp32 in
- * [0, 1); 0 <= min_p <= 1.  Outputs as in (3): path [T] int32 (node indices, root first),
- * n_path [1], bonus [1].  flags: TS_PENALTY_CTRL_LITERAL as in (3).
- * workspace >= ts_reject_workspace_bytes(V).
- * One CTA walks the path: meant for a draft model that provides q, at a
- * latency of a few passes over the vocabulary per visited node.
- * Unsupported (TS_ERR_UNSUPPORTED): more than 2048 tokens passing min-p at
- * a visited node when top_p < 1 (reported in `status`, path = [0],
- * bonus = -1), and top_p < 1 with min_p = 0 for V > 2048 (returned).
+ * logits [T, V] fp32; q [T, V] fp32 (rows sum to 1); tree_tokens, parents
+ * [T] int32; prior [n_prior] int32 ending with the root token; u_accept,
+ * u_draw [T] fp32 in [0, 1).  Outputs as in (3): path [T] int32 (node
+ * indices, root first), n_path [1], bonus [1].  flags:
+ * TS_PENALTY_CTRL_LITERAL as in (3).  workspace >=
+ * ts_reject_workspace_bytes(V).
+ * Every node's outcome (its accepted child, or its bonus token) depends only
+ * on that node's row, window and children, so all nodes are resolved in
+ * parallel (the slices and merge of (3), then the chain over the node's
+ * kept set) and the path follows the outcomes from the root.
  * ------------------------------------------------------------------------ */
 size_t ts_reject_workspace_bytes(int V);
 int ts_rejection_sample_accept(const float* logits, const float* q,

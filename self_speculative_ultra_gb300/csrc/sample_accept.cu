@@ -26,6 +26,20 @@
 // radix descent over the 50-bit key (x' key, reversed id) carrying a
 // (count, mass) histogram per digit: 3 levels on the fp32 key, 2 on the id.
 // The last CTA to finish walks the tree and writes the accepted path.
+//
+// Rejection mode (A. Lossless Nature of Speculative Decoding): the same
+// slice and merge phases give every node its truncated target p (the kept
+// set above, renormalised); then, instead of a draw, the node's CTA runs the
+// speculative-sampling chain over its children in index order: child c with
+// token x is accepted iff u_accept[c] * q[i][x] < p(x); on rejection p
+// becomes max(p - q[i], 0) renormalised (left as it is when nothing is
+// left); with no child accepted, the bonus token is drawn from the current p
+// by inverse CDF in token-id order with u_draw[i].  A node's outcome does not
+// depend on which nodes the walk visits, so every node is resolved in
+// parallel and the last CTA follows the outcomes from the root.  p and its
+// residuals live on the kept set (usually tens of tokens: one warp runs the
+// chain there); when the kept set overflows shared memory, or with no
+// truncation at all, the chain runs over the node's vocabulary row.
 #include "ts_common.cuh"
 
 namespace ts {
@@ -35,6 +49,7 @@ namespace {
 constexpr int kThreads = 512;
 constexpr int kParts = 4;                // CTAs per tree node
 constexpr int kCapPart = 4096;           // candidates one slice may publish
+constexpr int kBatch = 8;                // float4 loads of a thread in flight together
 constexpr int kMaxBuckets = 2048;
 constexpr uint32_t kIdMask = 0x3FFFFu;   // V <= 2^18
 
@@ -61,10 +76,13 @@ struct SampleSmem {
   int cb;       // count ranked before the current bucket range
   int32_t ptok[64];
   int32_t par[64], tok[64], smp[64];     // the tree, staged once (T <= 64)
-  int32_t dep[64];
-  uint8_t acc[64];
+  int best;    // acceptance: depth * 256 + (255 - node) of the best node
   int plen;
   int last;
+  int nkeep;   // rejection mode: the kept set's size, its mass, the outcome
+  float zk;
+  int outcome;
+  uint32_t cut_key, cut_rid;
 };
 
 struct PartStat {
@@ -252,6 +270,188 @@ __device__ Found radix_find(const float* __restrict__ xs, int V, float xmax, int
   return f;
 }
 
+
+// ---------------------------------------------------------------- rejection
+// The children of node i in index order are the nodes c > i with parents[c]
+// = i (sm.par, sm.tok staged).  Outcome codes: child c (>= 1) or -1 - token.
+
+// Bonus draw from the row p = xs[0, V) (all threads): per-thread contiguous
+// segments of token ids, a block exclusive scan of their sums; the owner is
+// the last thread with mass whose segment starts at or below the target
+// (rounding can leave the target between two segments) and it takes the
+// first token whose cumulative mass exceeds the target, else its last token
+// with mass.  Returns -1 - token.
+__device__ int bonus_dense(int i, int V, const float* __restrict__ xs,
+                           const float* __restrict__ u_draw, SampleSmem& sm) {
+  const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+  const int per = (V + kThreads - 1) / kThreads;
+  const int t0 = min(V, tid * per), t1 = min(V, t0 + per);
+  float seg = 0.f;
+  for (int t = t0; t < t1; ++t) seg += xs[t];
+  float incl = seg;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const float y = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  if (lane == 31) sm.red_f[w] = incl;
+  if (tid == 0) sm.best = -1;
+  __syncthreads();
+  if (w == 0) {
+    const float v = lane < (kThreads >> 5) ? sm.red_f[lane] : 0.f;
+    float wi = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const float y = __shfl_up_sync(0xffffffffu, wi, o);
+      if (lane >= o) wi += y;
+    }
+    if (lane < (kThreads >> 5)) sm.mass[lane] = wi - v;   // warps before this one
+    if (lane == 31) sm.zk = wi;                           // total
+  }
+  __syncthreads();
+  const float before = sm.mass[w] + incl - seg;
+  const float target = u_draw[i] * sm.zk;
+  if (seg > 0.f && before <= target) atomicMax(&sm.best, tid);
+  __syncthreads();
+  if (tid == sm.best) {
+    float cum = before;
+    int pick = -1, last = -1;
+    for (int t = t0; t < t1; ++t) {
+      if (xs[t] > 0.f) last = t;
+      cum += xs[t];
+      if (cum > target) {
+        pick = t;
+        break;
+      }
+    }
+    sm.outcome = -1 - (pick >= 0 ? pick : last);
+  }
+  __syncthreads();
+  const int oc = sm.best >= 0 ? sm.outcome : -1;   // no mass anywhere: token 0
+  __syncthreads();
+  return oc;
+}
+
+// Kept set in shared memory (ranks 0 .. nkeep-1 of sm.ckey / sm.cid, sorted
+// by (x' desc, id asc)); warp 0 runs the chain with p and q of the kept
+// tokens in two shared arrays, then the bonus draw in token-id order.
+__device__ int reject_sparse(int i, int T, int V, float xmax, const float* __restrict__ qrow,
+                             const float* __restrict__ u_accept, const float* __restrict__ u_draw,
+                             float* __restrict__ xs, SampleSmem& sm) {
+  const int tid = threadIdx.x, lane = tid & 31;
+  const int nk = sm.nkeep;
+  constexpr int kSparseBonus = 256;    // larger kept sets draw over the row
+  float* pk = reinterpret_cast<float*>(sm.cnt);        // kCap floats (cnt and mass)
+  float* qk = reinterpret_cast<float*>(sm.ckey);       // reuses the keys once p is formed
+  const float zk = sm.zk;
+  for (int r = tid; r < nk; r += kThreads) {
+    const float e = expf(key_float(sm.ckey[r]) - xmax);
+    pk[r] = __fdiv_rn(e, zk);
+  }
+  __syncthreads();
+  for (int r = tid; r < nk; r += kThreads) qk[r] = __ldg(qrow + sm.cid[r]);
+  __syncthreads();
+  if (tid < 32) {
+    int outcome = 0;
+    for (int c = i + 1; c < T && outcome == 0; ++c) {
+      if (sm.par[c] != i) continue;
+      const int x = sm.tok[c];
+      if (x < 0 || x >= V) continue;               // reported by the window pass
+      float px = 0.f;
+      for (int r = lane; r < nk; r += 32)
+        if (sm.cid[r] == x) px = pk[r];
+      px = warp_sum(px);                           // at most one lane holds x
+      if (u_accept[c] * __ldg(qrow + x) < px) {
+        outcome = c;
+        break;
+      }
+      float part = 0.f;
+      for (int r = lane; r < nk; r += 32) part += fmaxf(pk[r] - qk[r], 0.f);
+      const float S = warp_sum(part);
+      if (S > 0.f)
+        for (int r = lane; r < nk; r += 32) pk[r] = __fdiv_rn(fmaxf(pk[r] - qk[r], 0.f), S);
+      __syncwarp();
+    }
+    if (outcome == 0 && nk <= kSparseBonus) {
+      // bonus: the smallest token id whose cumulative mass in id order
+      // exceeds u * total; cum(r) sums the kept tokens with id <= cid[r]
+      float tot = 0.f;
+      for (int r = lane; r < nk; r += 32) tot += pk[r];
+      tot = warp_sum(tot);
+      const float target = u_draw[i] * tot;
+      int pick = 0x7FFFFFFF, last = -1;
+      for (int r = lane; r < nk; r += 32) {
+        const int id = sm.cid[r];
+        if (pk[r] > 0.f) last = max(last, id);
+        float cum = 0.f;
+        for (int r2 = 0; r2 < nk; ++r2)
+          if (sm.cid[r2] <= id) cum += pk[r2];
+        if (pk[r] > 0.f && cum > target) pick = min(pick, id);
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        pick = min(pick, __shfl_xor_sync(0xffffffffu, pick, o));
+        last = max(last, __shfl_xor_sync(0xffffffffu, last, o));
+      }
+      // rounding can leave the target past the last cumulative sum
+      outcome = -1 - (pick != 0x7FFFFFFF ? pick : last);
+    }
+    if (lane == 0) sm.outcome = outcome;
+  }
+  __syncthreads();
+  if (sm.outcome != 0) return sm.outcome;
+  // no child accepted and a large kept set: the row p over the vocabulary
+  for (int t = tid; t < V; t += kThreads) xs[t] = 0.f;
+  __syncthreads();
+  for (int r = tid; r < nk; r += kThreads) xs[sm.cid[r]] = pk[r];
+  __syncthreads();
+  return bonus_dense(i, V, xs, u_draw, sm);
+}
+
+// The whole vocabulary row: p is materialised over x' in place (xs), each
+// rejection is a block-wide pass, the bonus a block-wide scan in id order.
+__device__ int reject_dense(int i, int T, int V, float xmax, float min_p, bool by_cut,
+                            uint32_t cut_key, uint32_t cut_rid, float ZK, float* __restrict__ xs,
+                            const float* __restrict__ qrow, const float* __restrict__ u_accept,
+                            const float* __restrict__ u_draw, SampleSmem& sm) {
+  const int tid = threadIdx.x;
+  // p(t) = kept(t) ? e_t / ZK : 0, kept = rank at or above the cut token
+  // (or, without a top-p cut, e_t >= min_p)
+  for (int t = tid; t < V; t += kThreads) {
+    const float x = xs[t];
+    const float e = expf(x - xmax);
+    bool kept;
+    if (by_cut) {
+      const uint32_t k = float_key(x), rid = kIdMask - (uint32_t)t;
+      kept = k > cut_key || (k == cut_key && rid >= cut_rid);
+    } else {
+      kept = e >= min_p;
+    }
+    xs[t] = kept ? __fdiv_rn(e, ZK) : 0.f;
+  }
+  __syncthreads();
+  int outcome = 0;
+  for (int c = i + 1; c < T; ++c) {
+    if (sm.par[c] != i) continue;
+    const int x = sm.tok[c];
+    if (x < 0 || x >= V) continue;
+    // every thread reads the same two values after the barrier above
+    if (u_accept[c] * __ldg(qrow + x) < xs[x]) {
+      outcome = c;
+      break;
+    }
+    float part = 0.f;
+    for (int t = tid; t < V; t += kThreads) part += fmaxf(xs[t] - __ldg(qrow + t), 0.f);
+    const float S = block_sum(part, sm);
+    if (S > 0.f)
+      for (int t = tid; t < V; t += kThreads)
+        xs[t] = __fdiv_rn(fmaxf(xs[t] - __ldg(qrow + t), 0.f), S);
+    __syncthreads();
+  }
+  if (outcome != 0) return outcome;
+  return bonus_dense(i, V, xs, u_draw, sm);
+}
+
 __global__ void __launch_bounds__(kThreads, 2)
 sample_accept_kernel(const float* __restrict__ logits, const int32_t* __restrict__ tree_tokens,
                      const int32_t* __restrict__ parents, int T, const int32_t* __restrict__ prior,
@@ -259,12 +459,17 @@ sample_accept_kernel(const float* __restrict__ logits, const int32_t* __restrict
                      float min_p, int mode, float eta_eps, float eta_alpha,
                      const float* __restrict__ uniforms, int32_t* sampled,
                      int32_t* __restrict__ path, int32_t* __restrict__ n_path,
-                     int32_t* __restrict__ bonus, SampleWs ws, int32_t* status) {
+                     int32_t* __restrict__ bonus, SampleWs ws,
+                     const float* __restrict__ q_draft, const float* __restrict__ u_draw,
+                     int32_t* status) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
   // mode bit 0: eta-sampling pool instead of top-p / min-p; bit 1: literal
-  // CTRL penalty (every windowed logit divided by the penalty)
+  // CTRL penalty (every windowed logit divided by the penalty); bit 2:
+  // rejection-sampling acceptance against the draft rows q_draft
+  // (`uniforms` are then the per-child acceptance uniforms)
   const bool eta_mode = (mode & 1) != 0;
   const bool literal = (mode & 2) != 0;
+  const bool reject = (mode & 4) != 0;
   SampleSmem& sm = *reinterpret_cast<SampleSmem*>(smem_raw);
   uint32_t* bitmap = reinterpret_cast<uint32_t*>(smem_raw + sizeof(SampleSmem));
   const int part = blockIdx.x, i = blockIdx.y, tid = threadIdx.x;
@@ -328,18 +533,29 @@ sample_accept_kernel(const float* __restrict__ logits, const int32_t* __restrict
   };
   float lmax = -INFINITY;
   if (vec) {
+    // kBatch float4 loads of a thread in flight together, then their x'
     const float4* in4 = reinterpret_cast<const float4*>(x_in);
     float4* xs4 = reinterpret_cast<float4*>(xs);
-#pragma unroll 2
-    for (int q = t0 / 4 + tid; q < t1 / 4; q += kThreads) {
-      float4 a = in4[q];
-      const int t = 4 * q;
-      a.x = xprime(a.x, t);
-      a.y = xprime(a.y, t + 1);
-      a.z = xprime(a.z, t + 2);
-      a.w = xprime(a.w, t + 3);
-      xs4[q] = a;
-      lmax = fmaxf(lmax, fmaxf(fmaxf(a.x, a.y), fmaxf(a.z, a.w)));
+    for (int q0 = t0 / 4 + tid; q0 < t1 / 4; q0 += kThreads * kBatch) {
+      float4 a[kBatch];
+#pragma unroll
+      for (int b = 0; b < kBatch; ++b) {
+        const int q = q0 + b * kThreads;
+        if (q < t1 / 4) a[b] = __ldcs(in4 + q);
+      }
+#pragma unroll
+      for (int b = 0; b < kBatch; ++b) {
+        const int q = q0 + b * kThreads;
+        if (q < t1 / 4) {
+          const int t = 4 * q;
+          a[b].x = xprime(a[b].x, t);
+          a[b].y = xprime(a[b].y, t + 1);
+          a[b].z = xprime(a[b].z, t + 2);
+          a[b].w = xprime(a[b].w, t + 3);
+          xs4[q] = a[b];
+          lmax = fmaxf(lmax, fmaxf(fmaxf(a[b].x, a[b].y), fmaxf(a[b].z, a[b].w)));
+        }
+      }
     }
   } else {
     for (int t = t0 + tid; t < t1; t += kThreads) {
@@ -372,15 +588,24 @@ sample_accept_kernel(const float* __restrict__ logits, const int32_t* __restrict
     }
   };
   if (vec) {
+    // this thread's own x' values (it wrote them), kBatch loads in flight
     const float4* xs4 = reinterpret_cast<const float4*>(xs);
-    for (int b0 = t0 / 4; b0 < t1 / 4; b0 += kThreads) {
-      const int q = b0 + tid;
-      const bool valid = q < t1 / 4;
-      const float4 a = valid ? xs4[q] : make_float4(0.f, 0.f, 0.f, 0.f);
-      consider(valid, a.x, 4 * q);
-      consider(valid, a.y, 4 * q + 1);
-      consider(valid, a.z, 4 * q + 2);
-      consider(valid, a.w, 4 * q + 3);
+    for (int b0 = t0 / 4; b0 < t1 / 4; b0 += kThreads * kBatch) {
+      float4 a[kBatch];
+#pragma unroll
+      for (int b = 0; b < kBatch; ++b) {
+        const int q = b0 + b * kThreads + tid;
+        a[b] = q < t1 / 4 ? xs4[q] : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+#pragma unroll
+      for (int b = 0; b < kBatch; ++b) {
+        const int q = b0 + b * kThreads + tid;
+        const bool valid = q < t1 / 4;
+        consider(valid, a[b].x, 4 * q);
+        consider(valid, a[b].y, 4 * q + 1);
+        consider(valid, a[b].z, 4 * q + 2);
+        consider(valid, a[b].w, 4 * q + 3);
+      }
     }
   } else {
     for (int b0 = t0; b0 < t1; b0 += kThreads) {
@@ -555,7 +780,11 @@ sample_accept_kernel(const float* __restrict__ logits, const int32_t* __restrict
         k_keep = n_minp;
         zk = run;
       }
-      const float target = uniforms[i] * zk;
+      if (lane == 0) {
+        sm.nkeep = k_keep;
+        sm.zk = zk;
+      }
+      const float target = reject ? -1.f : uniforms[i] * zk;
       run = 0.f;
       int pick = k_keep - 1;
       for (int b0 = 0; b0 < k_keep; b0 += 32) {
@@ -578,7 +807,8 @@ sample_accept_kernel(const float* __restrict__ logits, const int32_t* __restrict
       if (lane == 0) sm.kpre = (uint32_t)sm.cid[pick];
     }
     __syncthreads();
-    token = (int)sm.kpre;
+    token = reject ? reject_sparse(i, T, V, xmax, q_draft + (size_t)i * V, uniforms, u_draw, xs, sm)
+                   : (int)sm.kpre;
     __syncthreads();
   } else {
     // ---- general path: radix descent with (count, mass) histograms
@@ -588,15 +818,29 @@ sample_accept_kernel(const float* __restrict__ logits, const int32_t* __restrict
     }
     int k_keep = n_minp;
     float ZK = Zmin;
+    // kept tokens: the rank prefix up to the top-p cut token, else the
+    // min-p set (e >= min_p); 50-bit rank key (x' key, reversed id)
+    uint32_t cut_key = 0u, cut_rid = 0u;
+    bool by_cut = false;
     if (!eta_mode && top_p < 1.0f) {
       const Found f1 = radix_find(xs, V, xmax, kMassGT, top_p * Z, 0, sm);
       k_keep = min(n_minp, f1.rank + 1);
       ZK = (k_keep == f1.rank + 1) ? f1.cum_incl : Zmin;
+      if (k_keep == f1.rank + 1) {
+        by_cut = true;
+        cut_key = float_key(xs[f1.id]);
+        cut_rid = kIdMask - (uint32_t)f1.id;
+      }
     }
-    const float u = uniforms[i];
-    Found f2 = radix_find(xs, V, xmax, kMassGT, u * ZK, 0, sm);
-    if (f2.rank >= k_keep) f2 = radix_find(xs, V, xmax, kRank, 0.f, k_keep - 1, sm);
-    token = f2.id;
+    if (reject) {
+      token = reject_dense(i, T, V, xmax, min_p, by_cut, cut_key, cut_rid, ZK, xs,
+                           q_draft + (size_t)i * V, uniforms, u_draw, sm);
+    } else {
+      const float u = uniforms[i];
+      Found f2 = radix_find(xs, V, xmax, kMassGT, u * ZK, 0, sm);
+      if (f2.rank >= k_keep) f2 = radix_find(xs, V, xmax, kRank, 0.f, k_keep - 1, sm);
+      token = f2.id;
+    }
   }
 
   // publish this node's draw; the last CTA walks the tree
@@ -612,23 +856,44 @@ sample_accept_kernel(const float* __restrict__ logits, const int32_t* __restrict
   // in shared memory
   __threadfence();
   if (tid < T) sm.smp[tid] = __ldcg(sampled + tid);
+  if (tid == 0) sm.best = 0;
+  __syncthreads();
+  if (reject) {
+    // outcome of node n: an accepted child c >= 1, or -1 - (bonus token)
+    if (tid == 0) {
+      int node = 0, n = 1;
+      path[0] = 0;
+      while (sm.smp[node] >= 1 && n < T) {
+        node = sm.smp[node];
+        path[n++] = node;
+      }
+      *n_path = n;
+      *bonus = sm.smp[node] >= 1 ? -1 : -1 - sm.smp[node];
+      *ws.counter = 0;
+    }
+    return;
+  }
+  // node c is accepted iff every node a on its root path (root excluded)
+  // carries the token its parent drew; the deepest accepted node wins, ties
+  // to the smaller index: the largest key depth * 256 + (255 - c)
+  if (tid < T) {
+    int a = tid, depth = 0;
+    bool acc = true;
+    while (a > 0 && depth < 64) {
+      const int p = sm.par[a];
+      if (p < 0 || p >= a) {
+        acc = false;
+        break;
+      }
+      acc = acc && sm.tok[a] == sm.smp[p];
+      a = p;
+      ++depth;
+    }
+    if (acc) atomicMax(&sm.best, depth * 256 + (255 - tid));
+  }
   __syncthreads();
   if (tid == 0) {
-    sm.acc[0] = 1;
-    sm.dep[0] = 0;
-    int best = 0;
-    for (int c = 1; c < T; ++c) {
-      const int p = sm.par[c];
-      if (p < 0 || p >= c) {
-        sm.acc[c] = 0;
-        sm.dep[c] = 0;
-        continue;
-      }
-      sm.dep[c] = sm.dep[p] + 1;
-      sm.acc[c] = sm.acc[p] && sm.tok[c] == sm.smp[p];
-      if (sm.acc[c] && sm.dep[c] > sm.dep[best]) best = c;
-    }
-    const int n = sm.dep[best] + 1;
+    const int best = 255 - (sm.best & 255), n = (sm.best >> 8) + 1;
     int a = best;
     for (int d = n - 1; d >= 0; --d) {
       path[d] = a;
@@ -725,12 +990,28 @@ size_t sample_ws_bytes(int T, int V) {
          a256s((size_t)T * kParts * kCapPart * sizeof(uint2)) + a256s((size_t)T * V * sizeof(float));
 }
 
+// Rejection mode: the sampling workspace of up to 64 nodes, then the nodes'
+// outcomes (64 int32).
+size_t reject_ws_bytes(int V) { return sample_ws_bytes(64, V) + 256; }
+
+int launch_reject_accept(const float* logits, const float* q, const int32_t* tree_tokens,
+                         const int32_t* parents, int T, const int32_t* prior, int n_prior, int W,
+                         int V, float penalty, float temperature, float top_p, float min_p,
+                         int literal, const float* u_accept, const float* u_draw, int32_t* path,
+                         int32_t* n_path, int32_t* bonus, void* ws, int32_t* status,
+                         cudaStream_t st) {
+  int32_t* outcome = reinterpret_cast<int32_t*>(static_cast<char*>(ws) + sample_ws_bytes(64, V));
+  return launch_sample_accept(logits, tree_tokens, parents, T, prior, n_prior, W, V, penalty,
+                              temperature, top_p, min_p, 4 | (literal ? 2 : 0), 0.f, 0.f,
+                              u_accept, outcome, path, n_path, bonus, ws, q, u_draw, status, st);
+}
+
 int launch_sample_accept(const float* logits, const int32_t* tree_tokens, const int32_t* parents,
                          int T, const int32_t* prior, int n_prior, int W, int V, float penalty,
                          float temperature, float top_p, float min_p, int mode, float eta_eps,
                          float eta_alpha, const float* uniforms, int32_t* sampled, int32_t* path,
-                         int32_t* n_path, int32_t* bonus, void* ws, int32_t* status,
-                         cudaStream_t st) {
+                         int32_t* n_path, int32_t* bonus, void* ws, const float* q_draft,
+                         const float* u_draw, int32_t* status, cudaStream_t st) {
   const SampleWs w = carve_sample(ws, T);
   if (cudaMemsetAsync(ws, 0, kCounterBytes, st) != cudaSuccess)
     return launch_status("sample counter reset");
@@ -738,7 +1019,8 @@ int launch_sample_accept(const float* logits, const int32_t* tree_tokens, const 
   cudaFuncSetAttribute(sample_accept_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   sample_accept_kernel<<<dim3(kParts, T), kThreads, smem, st>>>(
       logits, tree_tokens, parents, T, prior, n_prior, W, V, penalty, temperature, top_p, min_p,
-      mode, eta_eps, eta_alpha, uniforms, sampled, path, n_path, bonus, w, status);
+      mode, eta_eps, eta_alpha, uniforms, sampled, path, n_path, bonus, w, q_draft, u_draw,
+      status);
   return launch_status("sample_accept_kernel");
 }
 

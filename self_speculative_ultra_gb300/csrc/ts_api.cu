@@ -328,11 +328,12 @@ int ts_penalized_sample_accept_flags(const float* logits, const int32_t* tree_to
     return fail(TS_ERR_INVALID_ARG, "%s: NULL tensor", F);
   int rc = check_ws(workspace, workspace_bytes, sample_ws_bytes(T, V), F);
   if (rc) return rc;
-  // kernel mode word: bit 0 eta pool, bit 1 literal penalty
+  // kernel mode word: bit 0 eta pool, bit 1 literal penalty, bit 2 rejection
   const int mode = (flags & TS_PENALTY_CTRL_LITERAL) ? 2 : 0;
   return launch_sample_accept(logits, tree_tokens, parents, T, prior, n_prior, W, V, penalty,
                               temperature, top_p, min_p, mode, 0.f, 0.f, uniforms, sampled, path,
-                              n_path, bonus, workspace, status, static_cast<cudaStream_t>(stream));
+                              n_path, bonus, workspace, nullptr, nullptr, status,
+                              static_cast<cudaStream_t>(stream));
 }
 
 int ts_penalized_sample_accept(const float* logits, const int32_t* tree_tokens,
@@ -372,7 +373,7 @@ int ts_penalized_sample_accept_eta(const float* logits, const int32_t* tree_toke
   if (rc) return rc;
   return launch_sample_accept(logits, tree_tokens, parents, T, prior, n_prior, W, V, penalty,
                               temperature, 1.f, 0.f, 1, eta_epsilon, eta_alpha, uniforms, sampled,
-                              path, n_path, bonus, workspace, status,
+                              path, n_path, bonus, workspace, nullptr, nullptr, status,
                               static_cast<cudaStream_t>(stream));
 }
 
@@ -444,9 +445,6 @@ int ts_rejection_sample_accept(const float* logits, const float* q, const int32_
     return fail(TS_ERR_INVALID_ARG, "%s: penalty and temperature must be > 0", F);
   if (!(top_p > 0.f) || !(min_p >= 0.f))
     return fail(TS_ERR_INVALID_ARG, "%s: need top_p > 0 and min_p >= 0", F);
-  if (min_p > 1.f) return fail(TS_ERR_INVALID_ARG, "%s: need min_p <= 1", F);
-  if (top_p < 1.f && !(min_p > 0.f) && V > 2048)
-    return fail(TS_ERR_UNSUPPORTED, "%s: a top-p cut needs min_p > 0 when V > 2048", F);
   if (!logits || !q || !tree_tokens || !parents || !u_accept || !u_draw || !path || !n_path ||
       !bonus || (n_prior > 0 && !prior))
     return fail(TS_ERR_INVALID_ARG, "%s: NULL tensor", F);

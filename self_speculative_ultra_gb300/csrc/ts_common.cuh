@@ -164,8 +164,8 @@ int launch_sample_accept(const float* logits, const int32_t* tree_tokens, const 
                          int T, const int32_t* prior, int n_prior, int W, int V, float penalty,
                          float temperature, float top_p, float min_p, int eta_mode, float eta_eps,
                          float eta_alpha, const float* uniforms, int32_t* sampled, int32_t* path,
-                         int32_t* n_path, int32_t* bonus, void* ws, int32_t* status,
-                         cudaStream_t st);
+                         int32_t* n_path, int32_t* bonus, void* ws, const float* q_draft,
+                         const float* u_draw, int32_t* status, cudaStream_t st);
 size_t ngram_table_bytes(int V, int cap);
 int launch_ngram_insert(int32_t* table, int V, int cap, const int32_t* tokens, int n_tokens,
                         int start, int32_t* status, cudaStream_t st);

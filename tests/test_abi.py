@@ -134,9 +134,13 @@ def test_binding_signatures_match_the_header(ts):
 def test_rejection_call_rejects_bad_args(ts):
     p = ctypes.c_void_p(16)
     f = _c(ts).ts_rejection_sample_accept
-    # top-p without min-p over a large vocabulary is not supported
-    assert f(p, p, p, p, 4, p, 8, 8, 100000, 1.2, 1.0, 0.9, 0.0, p, p, p, p, p, p, 1 << 30, 0,
+    # more than 64 tree nodes
+    assert f(p, p, p, p, 65, p, 8, 8, 1000, 1.2, 1.0, 0.9, 0.05, p, p, p, p, p, p, 1 << 30, 0,
              None, None) == 2
+    # a top-p cut without min-p over a large vocabulary passes the argument
+    # checks; the misaligned workspace (address 16) is then rejected
+    assert f(p, p, p, p, 4, p, 8, 8, 100000, 1.2, 1.0, 0.9, 0.0, p, p, p, p, p, p, 1 << 30, 0,
+             None, None) == 5
     # unknown flag bits
     assert f(p, p, p, p, 4, p, 8, 8, 1000, 1.2, 1.0, 0.9, 0.05, p, p, p, p, p, p, 1 << 30, 8,
              None, None) == 1

@@ -96,27 +96,47 @@ def test_literal_penalty():
     assert sum(_run(w, 20 + s, literal=True)[0] == "tie" for s in range(4)) <= 1
 
 
-def test_draft_equal_to_target_follows_first_children():
+@pytest.mark.parametrize("step", [0, 5, 7])
+def test_draft_equal_to_target_follows_first_children(step):
     """q = the oracle's own target distribution at every node (same window,
-    penalty and truncation): every first child with nonzero target mass is
-    accepted, so the path follows first children as far as they carry mass."""
+    penalty and truncation): a first child whose token carries target mass
+    is always accepted (u * q(x) < p(x) with q = p), so the path follows
+    first children while they carry mass.  Once a first child's token has no
+    mass, the residual max(p - q, 0) is rounding noise of p's two
+    computations (fp32 here, fp64 in the oracle): what follows, and the
+    bonus, is not compared."""
+    import self_speculative_ultra_gb300 as ts
     w = syn.WORKLOADS["tiny"]
-    inp = syn.sampling_inputs(w, step=3)
+    inp = syn.sampling_inputs(w, step=step)
     paths = orc.root_paths(inp["parents"])
-    q = np.stack([orc.target_distribution(
+    p = [orc.target_distribution(
         orc.penalised_logits(inp["logits"][i],
                              orc.penalty_window(inp["prior"],
                                                 [int(inp["tokens"][a]) for a in paths[i][1:]], w.W),
                              w.penalty, w.temperature), w.top_p, w.min_p)
-        for i in range(w.T)]).astype(np.float32)
-    kind, got, ref = _run(w, 3, q=q)
-    assert kind in ("exact", "tie")
-    if kind == "exact":
-        node = 0
-        for nxt in ref[0][1:]:
-            kids = [c for c in range(1, w.T) if inp["parents"][c] == node]
-            assert nxt == kids[0]
-            node = nxt
+         for i in range(w.T)]
+    q = np.stack(p).astype(np.float32)
+    expected, node = [0], 0
+    while True:
+        kids = [c for c in range(1, w.T) if inp["parents"][c] == node]
+        if not kids or p[node][int(inp["tokens"][kids[0]])] <= 0.0:
+            break
+        node = kids[0]
+        expected.append(node)
+    assert len(expected) >= 2, "the seeded tree should accept at least one first child"
+    ua = syn.node_uniforms(w.seed, step, w.T)
+    ud = syn.node_uniforms(w.seed, step + 7919, w.T)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    path, n_path, _ = ts.ts_rejection_sample_accept(
+        pu.to_dev(inp["logits"]), pu.to_dev(q), pu.to_dev(inp["tokens"]), pu.to_dev(inp["parents"]),
+        pu.to_dev(inp["prior"]), w.W, w.penalty, w.temperature, w.top_p, w.min_p, pu.to_dev(ua),
+        pu.to_dev(ud), status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    got = path.cpu().numpy()[:int(n_path.item())].tolist()
+    assert got[:len(expected)] == expected, (got, expected)
+    ref = _oracle(inp, q, w.W, w.penalty, w.temperature, w.top_p, w.min_p, ua, ud, False)
+    assert list(ref[0][:len(expected)]) == expected
 
 
 def test_one_hot_target_and_draft_off_support_child():
@@ -144,3 +164,17 @@ def test_one_hot_target_and_draft_off_support_child():
     kind, got, ref = _run(w, 5, q=q, inp=inp)
     assert kind == "exact"
     assert got == ([0], a)
+
+
+def test_large_kept_set_and_top_p_without_min_p():
+    """Kept sets of hundreds to thousands of tokens (no planted draft token,
+    min_p 0.001: the chain runs on the kept set, the bonus is drawn over the
+    vocabulary row) and a top-p cut without min-p (the kept set is found by
+    the radix descent and the chain runs over the vocabulary row)."""
+    w = syn.scaled(syn.WORKLOADS["tiny"], V=50000)
+    ties = 0
+    for s in range(3):
+        inp = syn.sampling_inputs(w, step=30 + s, plant_accept=0.0)
+        ties += _run(w, 30 + s, top_p=1.0, min_p=0.001, inp=inp)[0] == "tie"
+        ties += _run(w, 40 + s, top_p=0.9, min_p=0.0, inp=inp)[0] == "tie"
+    assert ties <= 1
