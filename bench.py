@@ -764,18 +764,41 @@ def run_reference(args, w: syn.Workload):
 
 def run_profile_case(kind: str, w: syn.Workload):
     """Small, fixed cases for ncu captures (a few GB on the device):
-    verify -- 2 layers of the workload's K/V, 3 + 5*2 ts_verify_attention calls;
+    verify -- 2 layers of the workload's K/V, 3 + 5*2 ts_verify_attention calls
+    (split kernel and merge);
     select -- 4 layers through the batched partial-KV refresh and the sampling
     step, 3 rounds;
-    imp -- 2 layers of K, 3 + 2*2 ts_importance_softmax calls."""
+    imp -- 2 layers of K, 3 + 2*2 ts_importance_softmax calls;
+    commit -- 4 layers: 3 rounds of the batched append and commit;
+    eta -- 5 eta-sampling calls;
+    reject, ngram, draft, refresh -- the timing modes of those calls with
+    3 timed and 1 warm-up call, draft on 2 layers and refresh on 4."""
     import torch
     import self_speculative_ultra_gb300 as ts
     ts.build()
+    if kind == "reject":
+        return run_reject_case(w, 3, 1)
+    if kind == "ngram":
+        return run_ngram_case(w, 3, 1)
+    if kind == "draft":
+        return run_draft_case(syn.scaled(w, layers=2), 3, 1)
+    if kind == "refresh":
+        return run_refresh_case(syn.scaled(w, layers=4), 3, 1)
+    if kind == "eta":
+        sin = syn.sampling_inputs(w)
+        t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()  # noqa: E731
+        args = (t(sin["logits"]), t(sin["tokens"]), t(sin["parents"]), t(sin["prior"]), w.W,
+                w.penalty, w.temperature, 0.0009, 0.03, t(sin["uniforms"]))
+        for _ in range(5):
+            ts.ts_penalized_sample_accept_eta(*args)
+        torch.cuda.synchronize()
+        print(json.dumps({"profile_case": kind, "workload": w.name}))
+        return
     dev = torch.device("cuda", 0)
     g = torch.Generator(device=dev)
     g.manual_seed(0)
     T, Hq, Hkv, d, L = w.T, w.Hq, w.Hkv, w.d, w.L
-    nl = 4 if kind == "select" else 2
+    nl = 4 if kind in ("select", "commit") else 2
     ks = [torch.randn((Hkv, L + T, d), generator=g, device=dev).to(torch.bfloat16) for _ in range(nl)]
     if kind == "imp":
         q = torch.randn((T, Hq, d), generator=g, device=dev).to(torch.bfloat16)
@@ -788,6 +811,18 @@ def run_profile_case(kind: str, w: syn.Workload):
     vs = [torch.randn((Hkv, L + T, d), generator=g, device=dev).to(torch.bfloat16) for _ in range(nl)]
     tree = syn.make_tree(w, np.random.default_rng(0))
     parents = torch.from_numpy(tree[0]).to(dev)
+    if kind == "commit":
+        table = ts.commit_pointer_table(ks, vs)
+        rows = [torch.randn((nl, Hkv, T, d), generator=g, device=dev).to(torch.bfloat16)
+                for _ in range(2)]
+        path = torch.tensor([0, 1, 2, 3] + [0] * (T - 4), dtype=torch.int32, device=dev)
+        n_path = torch.tensor([4], dtype=torch.int32, device=dev)
+        for _ in range(3):
+            ts.ts_kv_append_batched(ks, vs, rows[0], rows[1], L, table=table)
+            ts.ts_kv_commit_batched(ks, vs, L, T, path, n_path, table=table)
+        torch.cuda.synchronize()
+        print(json.dumps({"profile_case": kind, "workload": w.name, "layers": nl}))
+        return
     if kind == "verify":
         q = torch.randn((T, Hq, d), generator=g, device=dev).to(torch.bfloat16)
         ws = torch.empty(ts.ts_verify_workspace_bytes(T, Hq, Hkv, d, L), dtype=torch.uint8, device=dev)
@@ -1219,7 +1254,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-per-config", action="store_true",
                     help="skip the timing of the other workloads")
-    ap.add_argument("--profile", choices=["verify", "select", "imp"],
+    ap.add_argument("--profile", choices=["verify", "select", "imp", "commit", "eta", "reject",
+                                          "ngram", "draft", "refresh"],
                     help="run a small fixed case for ncu captures and exit")
     ap.add_argument("--draft", action="store_true",
                     help="time draft-side attention over the compact cache and exit")
