@@ -179,7 +179,11 @@ int ts_partial_kv_select_gather(const float* imp, const void* k, const void* v,
  * overwrites what the previous one left there (the parts that must start at
  * zero are cleared on the stream by every call), so calls that overlap on the
  * GPU -- on different streams, or from different host threads -- race and
- * must be serialised by the caller. */
+ * must be serialised by the caller.  The cached address belongs to the
+ * device's current context: after cudaDeviceReset (or any teardown of the
+ * primary context) the array lives at a new address and the cache is stale,
+ * so reload the library (a new process) before calling this again on that
+ * device. */
 int ts_partial_kv_select_gather_noalloc(const float* imp, const void* k, const void* v,
                                         int64_t L, int64_t L_cap, int Hkv, int d,
                                         int B, int S, int R,
