@@ -54,8 +54,11 @@ __device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
 }
 // Wait for the phase of `parity` to complete, for at most ~`limit_cycles`
 // SM clocks.  Returns false (and the caller must bail out) on timeout.
+// A phase that has already completed is seen by the non-blocking probe,
+// which returns at once (a blocking try_wait on it costs a few hundred
+// cycles); otherwise the thread waits in try_wait.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, long long limit_cycles) {
-  if (mbar_try_wait(bar, parity)) return true;
+  if (mbar_test_wait(bar, parity)) return true;
   const long long t0 = clock64();
   while (true) {
     if (mbar_try_wait(bar, parity)) return true;

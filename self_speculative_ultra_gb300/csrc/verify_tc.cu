@@ -36,14 +36,19 @@
 //   V conversion (4..7)  each V tile converted in place from bf16 to fp16 as
 //                        it lands (exact for |v| < 65504; larger values
 //                        saturate and are reported in the status word)
-//   softmax (8..15)      one thread per query row, its scores read from TMEM
-//                        twice (max pass, then exponent pass): tile max, lazy
-//                        running max (O and l are rescaled only when the max
-//                        grows past 2^8, after the tile's P stores), P =
-//                        2^(s*log2e/sqrt(d) - m) written back over S in fp16
-//                        (relative rounding 2^-11), row sums.  Tree mask and
-//                        split limits (as bit masks over 64 keys) only touch
-//                        the tiles that need them.
+//   softmax (8..15)      one thread per query row, all 128 scores of a tile
+//                        read from TMEM into registers at once (the softmax
+//                        warpgroups hold 192 registers a thread, the others
+//                        64).  The tile is exponentiated against the running
+//                        max m: P = 2^(s*log2e/sqrt(d) - m) in fp16 (relative
+//                        rounding 2^-11), packed in registers; while the
+//                        tile's row sum of P stays <= 2^15 it is written back
+//                        over S as is, with no pass for the tile max.  Else
+//                        (or while m is -inf) m is raised to the tile max, O
+//                        and l are rescaled (after the tile's P stores) and
+//                        P is recomputed.  Tree mask and split limits (as bit
+//                        masks over 64 keys) only touch the tiles that need
+//                        them.
 // Each stream writes an unnormalised partial (O, m, l) per row in the log2
 // domain; the merge kernel of verify_attn.cu combines the splits.
 //
@@ -66,8 +71,15 @@ constexpr int kNk = 128;                 // keys per tile
 constexpr int kSV = 3;                   // V ring depth
 constexpr int kThreadsTc = 512;          // 16 warps
 constexpr int kSoftmaxWarp0 = 8;         // warps 8..15
+// registers a thread after the role split: the launch holds 512 x 128; the
+// two softmax warpgroups take 192 (all 128 scores of a row in registers),
+// the other two keep 64, so 2 x 128 x 64 + 2 x 128 x 192 = 65,536
+constexpr int kRegsLow = 64;
+constexpr int kRegsSoftmax = 192;
+static_assert(2 * 128 * kRegsLow + 2 * 128 * kRegsSoftmax == kThreadsTc * 128,
+              "the register split must use exactly the launch's registers");
 constexpr float kLog2e = 1.4426950408889634f;
-constexpr float kLazy = 8.0f;            // running max refreshed only past +2^8
+constexpr float kFastSum = 32768.0f;     // a tile's P is kept while its row sum <= 2^15
 constexpr long long kDrainCycles = 1ll << 31;
 constexpr uint32_t kNegInf = 0xFF800000u;
 
@@ -237,7 +249,7 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
     }
     for (int g = 0; g < 2; ++g) {
       ptx::mbar_init(&aux->s_full[g], 1);
-      ptx::mbar_init(&aux->p_ready[g], 128);     // one arrival per query row
+      ptx::mbar_init(&aux->p_ready[g], 4);       // one arrival per softmax warp
     }
     ptx::mbar_init(&aux->o_final, 1);
     ptx::mbar_init(&aux->drain, 1);
@@ -388,247 +400,253 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
   ptx::tc_fence_after();
   const uint32_t tmem = aux->tmem_base;
   griddep_launch_dependents();   // the merge kernel may take SMs as CTAs retire
-  if (warp == 0) {
-    // ------------------------------------------------------------ producer
-    if (lane == 0) {
-      const uint64_t pol = ptx::l2_evict_first_policy();
-      int s = n_pre, sv_next = n_pre;   // next tile to load (K), V loads issued
-      for (; s < n_seq; ++s) {
-        int g, k;
-        seq.decode(s, g, k);
-        const int row = (int)(kv * L_cap + key0_of(g, k));
-        const int stK = s % nK;
-        if (s >= nK &&
-            !ptx::mbar_wait(&aux->k_empty[stK], (uint32_t)(s / nK - 1) & 1u, wait_limit)) {
-          timeout(aux, status);
-          break;
-        }
-        ptx::mbar_arrive_expect_tx(&aux->k_full[stK], Ly::kTile);
-        for (int p = 0; p < D / 64; ++p)
-          ptx::tma_load_2d(kaddr(stK) + p * Ly::kPanel, &tmap_k, &aux->k_full[stK], p * 64, row,
-                           pol);
-        const int stV = s % kSV;
-        if (s >= kSV &&
-            !ptx::mbar_wait(&aux->v_empty[stV], (uint32_t)(s / kSV - 1) & 1u, wait_limit)) {
-          timeout(aux, status);
-          ++s;          // this tile's K load is in flight
-          break;
-        }
-        ptx::mbar_arrive_expect_tx(&aux->v_full[stV], Ly::kTile);
-        for (int p = 0; p < D / 64; ++p)
-          ptx::tma_load_2d(sv + stV * Ly::kTile + p * Ly::kPanel, &tmap_v, &aux->v_full[stV],
-                           p * 64, row, pol);
-        sv_next = s + 1;
-        if (aux->abort_flag) {
-          ++s;
-          break;
-        }
-      }
-      // drain: the copy engine writes this CTA's shared memory, so every
-      // issued load must land before the CTA exits, whether or not a
-      // consumer gave up waiting for it (in a normal run the consumers
-      // already saw each of them and these waits return at once).  Earlier
-      // loads into a stage completed before the stage was refilled.
-      for (int t = max(0, s - nK); t < s; ++t)
-        ptx::mbar_wait(&aux->k_full[t % nK], (uint32_t)(t / nK) & 1u, kDrainCycles);
-      for (int t = max(0, sv_next - kSV); t < sv_next; ++t)
-        ptx::mbar_wait(&aux->v_full[t % kSV], (uint32_t)(t / kSV) & 1u, kDrainCycles);
-    }
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      constexpr uint32_t idesc_qk = ptx::idesc_bf16_f32(128, kNk, false);
-      constexpr uint32_t idesc_pv = ptx::idesc_f16_f32(128, D, true);
-      // operand descriptors: a descriptor's start address is its low field
-      // in 16-byte units, so tile, stage and K-step offsets are adds
-      const uint64_t qd0 = ptx::sdesc_sw128(ptx::smem_u32(sq), 16, 1024);
-      const uint64_t vd0 = ptx::sdesc_sw128(ptx::smem_u32(sv), Ly::kPanel, 1024);
-      constexpr uint32_t kTile16 = Ly::kTile >> 4;
-      auto qk = [&](int g, int stK) {
-        const uint64_t a0 = qd0 + (uint64_t)((seq.two ? 0 : g) * kTile16);
-        const uint64_t b0 = ptx::sdesc_sw128(ptx::smem_u32(kaddr(stK)), 16, 1024);
-#pragma unroll
-        for (int ks = 0; ks < D / 16; ++ks) {
-          // 64-element panels, 32-byte K-steps
-          const uint32_t off = (ks >> 2) * (Ly::kPanel >> 4) + (ks & 3) * 2;
-          ptx::mma_ss(tmem + Ly::sbase(g), a0 + off, b0 + off, idesc_qk, ks > 0 ? 1u : 0u);
-        }
-        ptx::mma_commit(&aux->s_full[g]);
-      };
-      // O += P V in fp16 once the softmax has stored P (phase ph of the P
-      // barrier).  Keys [32c, 32c+32) of the tile keep their fp16 P pairs in
-      // S_g columns [32c, 32c+16): K-step ks (16 keys) reads the 8 columns at
-      // 32*(ks/2) + 8*(ks%2); V advances 16 rows (2048 bytes).
-      auto pv = [&](int g, int stV, bool acc, uint32_t ph) {
-        if (!ptx::mbar_wait(&aux->p_ready[g], ph, wait_limit)) return false;
-        ptx::tc_fence_after();
-        const uint64_t b0 = vd0 + (uint64_t)(stV * kTile16);
-#pragma unroll
-        for (int ks = 0; ks < kNk / 16; ++ks) {
-          const uint32_t acol = 32 * (ks >> 1) + 8 * (ks & 1);
-          ptx::mma_ts(tmem + Ly::obase(g), tmem + Ly::sbase(g) + acol, b0 + (uint64_t)(ks * 128),
-                      idesc_pv, (ks > 0 || acc) ? 1u : 0u);
-        }
-        return true;
-      };
-      auto wait_k = [&](int s) {
-        if (!ptx::mbar_wait(&aux->k_full[s % nK], (uint32_t)(s / nK) & 1u, wait_limit)) return false;
-        ptx::tc_fence_after();
-        return true;
-      };
-      bool ok = true;
-      if (!seq.two) {
-        if (n_seq > 0) {
-          ok = wait_k(0);
-          if (ok) {
-            for (int g = 0; g < nt; ++g) qk(g, 0);
-            ptx::mma_commit(&aux->k_empty[0]);
-          }
-        }
-        for (int s = 0; ok && s < n_seq; ++s) {
-          if (!ptx::mbar_wait(&aux->v_conv[s % kSV], (uint32_t)(s / kSV) & 1u, wait_limit)) {
-            ok = false;
+  if (warp < kSoftmaxWarp0) {
+    // producer, MMA, importance and V conversion run in kRegsLow registers
+    // a thread; the softmax warpgroups take the registers they free
+    ptx::regs_dec<kRegsLow>();
+    if (warp == 0) {
+      // ------------------------------------------------------------ producer
+      if (lane == 0) {
+        const uint64_t pol = ptx::l2_evict_first_policy();
+        int s = n_pre, sv_next = n_pre;   // next tile to load (K), V loads issued
+        for (; s < n_seq; ++s) {
+          int g, k;
+          seq.decode(s, g, k);
+          const int row = (int)(kv * L_cap + key0_of(g, k));
+          const int stK = s % nK;
+          if (s >= nK &&
+              !ptx::mbar_wait(&aux->k_empty[stK], (uint32_t)(s / nK - 1) & 1u, wait_limit)) {
+            timeout(aux, status);
             break;
           }
-          const bool more = s + 1 < n_seq;
-          for (int g = 0; g < nt && ok; ++g) {
-            if (!pv(g, s % kSV, s > 0, (uint32_t)s & 1u)) {
+          ptx::mbar_arrive_expect_tx(&aux->k_full[stK], Ly::kTile);
+          for (int p = 0; p < D / 64; ++p)
+            ptx::tma_load_2d(kaddr(stK) + p * Ly::kPanel, &tmap_k, &aux->k_full[stK], p * 64, row,
+                             pol);
+          const int stV = s % kSV;
+          if (s >= kSV &&
+              !ptx::mbar_wait(&aux->v_empty[stV], (uint32_t)(s / kSV - 1) & 1u, wait_limit)) {
+            timeout(aux, status);
+            ++s;          // this tile's K load is in flight
+            break;
+          }
+          ptx::mbar_arrive_expect_tx(&aux->v_full[stV], Ly::kTile);
+          for (int p = 0; p < D / 64; ++p)
+            ptx::tma_load_2d(sv + stV * Ly::kTile + p * Ly::kPanel, &tmap_v, &aux->v_full[stV],
+                             p * 64, row, pol);
+          sv_next = s + 1;
+          if (aux->abort_flag) {
+            ++s;
+            break;
+          }
+        }
+        // drain: the copy engine writes this CTA's shared memory, so every
+        // issued load must land before the CTA exits, whether or not a
+        // consumer gave up waiting for it (in a normal run the consumers
+        // already saw each of them and these waits return at once).  Earlier
+        // loads into a stage completed before the stage was refilled.
+        for (int t = max(0, s - nK); t < s; ++t)
+          ptx::mbar_wait(&aux->k_full[t % nK], (uint32_t)(t / nK) & 1u, kDrainCycles);
+        for (int t = max(0, sv_next - kSV); t < sv_next; ++t)
+          ptx::mbar_wait(&aux->v_full[t % kSV], (uint32_t)(t / kSV) & 1u, kDrainCycles);
+      }
+    } else if (warp == 1) {
+      // ------------------------------------------------------------ MMA issuer
+      if (lane == 0) {
+        constexpr uint32_t idesc_qk = ptx::idesc_bf16_f32(128, kNk, false);
+        constexpr uint32_t idesc_pv = ptx::idesc_f16_f32(128, D, true);
+        // operand descriptors: a descriptor's start address is its low field
+        // in 16-byte units, so tile, stage and K-step offsets are adds
+        const uint64_t qd0 = ptx::sdesc_sw128(ptx::smem_u32(sq), 16, 1024);
+        const uint64_t vd0 = ptx::sdesc_sw128(ptx::smem_u32(sv), Ly::kPanel, 1024);
+        constexpr uint32_t kTile16 = Ly::kTile >> 4;
+        auto qk = [&](int g, int stK) {
+          const uint64_t a0 = qd0 + (uint64_t)((seq.two ? 0 : g) * kTile16);
+          const uint64_t b0 = ptx::sdesc_sw128(ptx::smem_u32(kaddr(stK)), 16, 1024);
+  #pragma unroll
+          for (int ks = 0; ks < D / 16; ++ks) {
+            // 64-element panels, 32-byte K-steps
+            const uint32_t off = (ks >> 2) * (Ly::kPanel >> 4) + (ks & 3) * 2;
+            ptx::mma_ss(tmem + Ly::sbase(g), a0 + off, b0 + off, idesc_qk, ks > 0 ? 1u : 0u);
+          }
+          ptx::mma_commit(&aux->s_full[g]);
+        };
+        // O += P V in fp16 once the softmax has stored P (phase ph of the P
+        // barrier).  The fp16 pair of keys 2x, 2x+1 sits in S_g column x:
+        // K-step ks (16 keys) reads the 8 columns at 8*ks; V advances 16 rows
+        // (2048 bytes).
+        auto pv = [&](int g, int stV, bool acc, uint32_t ph) {
+          if (!ptx::mbar_wait(&aux->p_ready[g], ph, wait_limit)) return false;
+          ptx::tc_fence_after();
+          const uint64_t b0 = vd0 + (uint64_t)(stV * kTile16);
+  #pragma unroll
+          for (int ks = 0; ks < kNk / 16; ++ks) {
+            const uint32_t acol = 8 * ks;
+            ptx::mma_ts(tmem + Ly::obase(g), tmem + Ly::sbase(g) + acol, b0 + (uint64_t)(ks * 128),
+                        idesc_pv, (ks > 0 || acc) ? 1u : 0u);
+          }
+          return true;
+        };
+        auto wait_k = [&](int s) {
+          if (!ptx::mbar_wait(&aux->k_full[s % nK], (uint32_t)(s / nK) & 1u, wait_limit)) return false;
+          ptx::tc_fence_after();
+          return true;
+        };
+        bool ok = true;
+        if (!seq.two) {
+          if (n_seq > 0) {
+            ok = wait_k(0);
+            if (ok) {
+              for (int g = 0; g < nt; ++g) qk(g, 0);
+              ptx::mma_commit(&aux->k_empty[0]);
+            }
+          }
+          for (int s = 0; ok && s < n_seq; ++s) {
+            if (!ptx::mbar_wait(&aux->v_conv[s % kSV], (uint32_t)(s / kSV) & 1u, wait_limit)) {
               ok = false;
               break;
             }
-            if (more) {
-              if (g == 0 && !wait_k(s + 1)) {
+            const bool more = s + 1 < n_seq;
+            for (int g = 0; g < nt && ok; ++g) {
+              if (!pv(g, s % kSV, s > 0, (uint32_t)s & 1u)) {
                 ok = false;
                 break;
               }
-              qk(g, (s + 1) % nK);
+              if (more) {
+                if (g == 0 && !wait_k(s + 1)) {
+                  ok = false;
+                  break;
+                }
+                qk(g, (s + 1) % nK);
+              }
+            }
+            if (!ok) break;
+            ptx::mma_commit(&aux->v_empty[s % kSV]);
+            if (more) ptx::mma_commit(&aux->k_empty[(s + 1) % nK]);
+          }
+        } else {
+          // first tile of each stream
+          for (int g = 0; g < 2 && ok; ++g) {
+            if ((g ? seq.n1 : seq.n0) == 0) continue;
+            const int s = seq.index(g, 0);
+            ok = wait_k(s);
+            if (ok) {
+              qk(g, s % nK);
+              ptx::mma_commit(&aux->k_empty[s % nK]);
             }
           }
-          if (!ok) break;
-          ptx::mma_commit(&aux->v_empty[s % kSV]);
-          if (more) ptx::mma_commit(&aux->k_empty[(s + 1) % nK]);
-        }
-      } else {
-        // first tile of each stream
-        for (int g = 0; g < 2 && ok; ++g) {
-          if ((g ? seq.n1 : seq.n0) == 0) continue;
-          const int s = seq.index(g, 0);
-          ok = wait_k(s);
-          if (ok) {
-            qk(g, s % nK);
-            ptx::mma_commit(&aux->k_empty[s % nK]);
-          }
-        }
-        for (int s = 0; ok && s < n_seq; ++s) {
-          int g, k;
-          seq.decode(s, g, k);
-          if (!ptx::mbar_wait(&aux->v_conv[s % kSV], (uint32_t)(s / kSV) & 1u, wait_limit) ||
-              !pv(g, s % kSV, k > 0, (uint32_t)k & 1u)) {
-            ok = false;
-            break;
-          }
-          ptx::mma_commit(&aux->v_empty[s % kSV]);
-          if (k + 1 < (g ? seq.n1 : seq.n0)) {
-            const int s2 = seq.index(g, k + 1);
-            if (!wait_k(s2)) {
+          for (int s = 0; ok && s < n_seq; ++s) {
+            int g, k;
+            seq.decode(s, g, k);
+            if (!ptx::mbar_wait(&aux->v_conv[s % kSV], (uint32_t)(s / kSV) & 1u, wait_limit) ||
+                !pv(g, s % kSV, k > 0, (uint32_t)k & 1u)) {
               ok = false;
               break;
             }
-            qk(g, s2 % nK);
-            ptx::mma_commit(&aux->k_empty[s2 % nK]);
+            ptx::mma_commit(&aux->v_empty[s % kSV]);
+            if (k + 1 < (g ? seq.n1 : seq.n0)) {
+              const int s2 = seq.index(g, k + 1);
+              if (!wait_k(s2)) {
+                ok = false;
+                break;
+              }
+              qk(g, s2 % nK);
+              ptx::mma_commit(&aux->k_empty[s2 % nK]);
+            }
           }
         }
+        if (!ok) timeout(aux, status);
+        ptx::mma_commit(&aux->o_final);
+        // drain this thread's MMAs before TMEM is freed
+        ptx::mma_commit(&aux->drain);
+        ptx::mbar_wait(&aux->drain, 0, kDrainCycles);
       }
-      if (!ok) timeout(aux, status);
-      ptx::mma_commit(&aux->o_final);
-      // drain this thread's MMAs before TMEM is freed
-      ptx::mma_commit(&aux->drain);
-      ptx::mbar_wait(&aux->drain, 0, kDrainCycles);
-    }
-  } else if (warp < 4) {
-    // ------------------------------------------------------------ importance
-    const int t = tid - 64;   // key rows t and t + 64 of each tile
-    for (int s = 0; s < n_seq; ++s) {
-      const int stK = s % nK;
-      if (aux->abort_flag ||
-          !ptx::mbar_wait(&aux->k_full[stK], (uint32_t)(s / nK) & 1u, wait_limit)) {
-        timeout(aux, status);
-        break;
-      }
-      int g, k;
-      seq.decode(s, g, k);
-      const int ja = key0_of(g, k) + t, jb = ja + 64;
-      const int j1 = g ? st1.j1 : st0.j1;
-      if (do_imp && ja < j1) {
-        const uint8_t* ra = kaddr(stK) + t * 128;
-        const uint8_t* rb = ra + 64 * 128;
-        uint64_t a0 = 0, a1 = 0, b0 = 0, b1 = 0;
-#pragma unroll
-        for (int c = 0; c < C16; ++c) {
-          const int p = c >> 3, cc = c & 7;
-          const int off = p * Ly::kPanel + ((cc ^ (t & 7)) << 4);   // rows t, t+64: same swizzle
-          const uint4 u = *reinterpret_cast<const uint4*>(ra + off);
-          const uint4 v = *reinterpret_cast<const uint4*>(rb + off);
-          const float4 q0 = *reinterpret_cast<const float4*>(qsum + 8 * c);
-          const float4 q1 = *reinterpret_cast<const float4*>(qsum + 8 * c + 4);
-          const uint64_t qa = ptx::f2(q0.x, q0.y), qb = ptx::f2(q0.z, q0.w);
-          const uint64_t qc = ptx::f2(q1.x, q1.y), qd = ptx::f2(q1.z, q1.w);
-          auto lohi = [](uint32_t w) {
-            return ptx::f2(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
-          };
-          a0 = ptx::fma2(lohi(u.x), qa, a0);
-          a1 = ptx::fma2(lohi(u.y), qb, a1);
-          a0 = ptx::fma2(lohi(u.z), qc, a0);
-          a1 = ptx::fma2(lohi(u.w), qd, a1);
-          b0 = ptx::fma2(lohi(v.x), qa, b0);
-          b1 = ptx::fma2(lohi(v.y), qb, b1);
-          b0 = ptx::fma2(lohi(v.z), qc, b0);
-          b1 = ptx::fma2(lohi(v.w), qd, b1);
+    } else if (warp < 4) {
+      // ------------------------------------------------------------ importance
+      const int t = tid - 64;   // key rows t and t + 64 of each tile
+      for (int s = 0; s < n_seq; ++s) {
+        const int stK = s % nK;
+        if (aux->abort_flag ||
+            !ptx::mbar_wait(&aux->k_full[stK], (uint32_t)(s / nK) & 1u, wait_limit)) {
+          timeout(aux, status);
+          break;
         }
-        float x0, x1, y0, y1;
-        ptx::f2_split(ptx::add2(a0, a1), x0, x1);
-        ptx::f2_split(ptx::add2(b0, b1), y0, y1);
-        imp[(size_t)kv * L + ja] = (x0 + x1) * scale;
-        if (jb < j1) imp[(size_t)kv * L + jb] = (y0 + y1) * scale;
-      }
-      __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(&aux->k_empty[stK]);
-    }
-  } else if (warp < kSoftmaxWarp0) {
-    // ------------------------------------------------------------ V conversion
-    // V tiles are converted in place from bf16 to fp16 as soon as they land,
-    // ahead of the MMA's P V (the V ring is three tiles deep)
-    const int t = tid - 4 * 32;
-    constexpr int kChunks = Ly::kTile / 16;          // 16-byte chunks per V tile
-    constexpr int kConvThreads = 4 * 32;
-    float vmax = 0.f;                                // largest |v| (fp16 range check)
-    for (int s = 0; s < n_seq; ++s) {
-      const int stV = s % kSV;
-      const bool got = !aux->abort_flag &&
-                       ptx::mbar_wait(&aux->v_full[stV], (uint32_t)(s / kSV) & 1u, wait_limit);
-      if (!__all_sync(0xffffffffu, got)) {
-        timeout(aux, status);
-        break;
-      }
-      uint4* vt = reinterpret_cast<uint4*>(sv + stV * Ly::kTile);
-#pragma unroll 4
-      for (int e = t; e < kChunks; e += kConvThreads) {
-        uint4 u = vt[e];
-        uint32_t wd[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-        for (int x2 = 0; x2 < 4; ++x2) {
-          const float lo = __uint_as_float(wd[x2] << 16), hi = __uint_as_float(wd[x2] & 0xFFFF0000u);
-          vmax = ptx::max3(vmax, fabsf(lo), fabsf(hi));
-          wd[x2] = ptx::pack_f16x2_sat(lo, hi);
+        int g, k;
+        seq.decode(s, g, k);
+        const int ja = key0_of(g, k) + t, jb = ja + 64;
+        const int j1 = g ? st1.j1 : st0.j1;
+        if (do_imp && ja < j1) {
+          const uint8_t* ra = kaddr(stK) + t * 128;
+          const uint8_t* rb = ra + 64 * 128;
+          uint64_t a0 = 0, a1 = 0, b0 = 0, b1 = 0;
+  #pragma unroll
+          for (int c = 0; c < C16; ++c) {
+            const int p = c >> 3, cc = c & 7;
+            const int off = p * Ly::kPanel + ((cc ^ (t & 7)) << 4);   // rows t, t+64: same swizzle
+            const uint4 u = *reinterpret_cast<const uint4*>(ra + off);
+            const uint4 v = *reinterpret_cast<const uint4*>(rb + off);
+            const float4 q0 = *reinterpret_cast<const float4*>(qsum + 8 * c);
+            const float4 q1 = *reinterpret_cast<const float4*>(qsum + 8 * c + 4);
+            const uint64_t qa = ptx::f2(q0.x, q0.y), qb = ptx::f2(q0.z, q0.w);
+            const uint64_t qc = ptx::f2(q1.x, q1.y), qd = ptx::f2(q1.z, q1.w);
+            auto lohi = [](uint32_t w) {
+              return ptx::f2(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
+            };
+            a0 = ptx::fma2(lohi(u.x), qa, a0);
+            a1 = ptx::fma2(lohi(u.y), qb, a1);
+            a0 = ptx::fma2(lohi(u.z), qc, a0);
+            a1 = ptx::fma2(lohi(u.w), qd, a1);
+            b0 = ptx::fma2(lohi(v.x), qa, b0);
+            b1 = ptx::fma2(lohi(v.y), qb, b1);
+            b0 = ptx::fma2(lohi(v.z), qc, b0);
+            b1 = ptx::fma2(lohi(v.w), qd, b1);
+          }
+          float x0, x1, y0, y1;
+          ptx::f2_split(ptx::add2(a0, a1), x0, x1);
+          ptx::f2_split(ptx::add2(b0, b1), y0, y1);
+          imp[(size_t)kv * L + ja] = (x0 + x1) * scale;
+          if (jb < j1) imp[(size_t)kv * L + jb] = (y0 + y1) * scale;
         }
-        vt[e] = make_uint4(wd[0], wd[1], wd[2], wd[3]);
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(&aux->k_empty[stK]);
       }
-      ptx::fence_proxy_async_smem();   // generic writes -> the MMA's async-proxy reads
-      __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(&aux->v_conv[stV]);
+    } else {
+      // ------------------------------------------------------------ V conversion
+      // V tiles are converted in place from bf16 to fp16 as soon as they land,
+      // ahead of the MMA's P V (the V ring is three tiles deep)
+      const int t = tid - 4 * 32;
+      constexpr int kChunks = Ly::kTile / 16;          // 16-byte chunks per V tile
+      constexpr int kConvThreads = 4 * 32;
+      float vmax = 0.f;                                // largest |v| (fp16 range check)
+      for (int s = 0; s < n_seq; ++s) {
+        const int stV = s % kSV;
+        const bool got = !aux->abort_flag &&
+                         ptx::mbar_wait(&aux->v_full[stV], (uint32_t)(s / kSV) & 1u, wait_limit);
+        if (!__all_sync(0xffffffffu, got)) {
+          timeout(aux, status);
+          break;
+        }
+        uint4* vt = reinterpret_cast<uint4*>(sv + stV * Ly::kTile);
+  #pragma unroll 4
+        for (int e = t; e < kChunks; e += kConvThreads) {
+          uint4 u = vt[e];
+          uint32_t wd[4] = {u.x, u.y, u.z, u.w};
+  #pragma unroll
+          for (int x2 = 0; x2 < 4; ++x2) {
+            const float lo = __uint_as_float(wd[x2] << 16), hi = __uint_as_float(wd[x2] & 0xFFFF0000u);
+            vmax = ptx::max3(vmax, fabsf(lo), fabsf(hi));
+            wd[x2] = ptx::pack_f16x2_sat(lo, hi);
+          }
+          vt[e] = make_uint4(wd[0], wd[1], wd[2], wd[3]);
+        }
+        ptx::fence_proxy_async_smem();   // generic writes -> the MMA's async-proxy reads
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(&aux->v_conv[stV]);
+      }
+      if (!(vmax <= 65504.f)) set_status(status, TS_ERR_UNSUPPORTED);
     }
-    if (!(vmax <= 65504.f)) set_status(status, TS_ERR_UNSUPPORTED);
   } else {
+    ptx::regs_inc<kRegsSoftmax>();
     // ------------------------------------------------------------ softmax
     // one thread per query row t of tile g: all 128 keys of each key tile
     const int g = sm_g;
@@ -679,75 +697,121 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
             if (!((v1 >> x2) & 1u)) r[32 + x2] = kNegInf;
           }
         };
-        auto ld64 = [&](uint32_t col, uint32_t* r) {
-          ptx::tmem_ld32(s_addr + col, *reinterpret_cast<uint32_t(*)[32]>(r));
-          ptx::tmem_ld32(s_addr + col + 32, *reinterpret_cast<uint32_t(*)[32]>(r + 32));
-          ptx::tmem_ld_wait();
-        };
-        uint32_t r[64];
-        float mh = -INFINITY;
-        if (got) {
+        // all 128 scores of the row in registers: one TMEM round trip
+        uint32_t r[kNk];
+        auto load_s = [&]() {
           ptx::tc_fence_after();
-          // keys 64..127 first (reloaded for the exponent pass), then keys
-          // 0..63, which stay in registers
-          ld64(64, r);
-          if (edge) apply(r, block_mask(1));
-          mh = fmaxf(fmax32(&r[0]), fmax32(&r[32]));
-          ld64(0, r);
-          if (edge) apply(r, block_mask(0));
-          mh = fmaxf(mh, fmaxf(fmax32(&r[0]), fmax32(&r[32])));
-        }
-        const float mx = mh;
+#pragma unroll
+          for (int c = 0; c < kNk / 32; ++c)
+            ptx::tmem_ld32(s_addr + 32 * c, *reinterpret_cast<uint32_t(*)[32]>(r + 32 * c));
+          ptx::tmem_ld_wait();
+          if (edge) {
+            apply(r, block_mask(0));
+            apply(r + 64, block_mask(1));
+          }
+        };
         if (!got) {
           ok = false;
           break;
         }
-        // lazy running max: raise it only when the tile max exceeds it by
-        // 2^8.  S_g of this tile completing implies P_g V of group g's
-        // previous tile did (MMAs of one thread complete in order), so O_g
-        // may be rescaled (below, before this tile's P is released).
-        const float ms = mx * sl2;
-        const bool raise = ms > m_used + kLazy;
-        const float f = raise ? ptx::ex2(m_used - ms) : 1.f;   // 0 when m_used = -inf
-        if (raise) {
-          l *= f;
-          m_used = ms;
-        }
-        // P = 2^(s*sl2 - m) -> fp16 pairs: keys [32c, 32c+32) of the tile go
-        // to S columns [32c, 32c+16).  While the running max is still -inf
-        // every score seen so far is -inf: reference 0 then gives 2^-inf = 0.
-        const float mref = (m_used == -INFINITY) ? 0.f : m_used;
+        load_s();
+        // P = 2^(s*sl2 - m) -> fp16 pairs, in place: the pair of keys
+        // 32c + 2i, 32c + 2i + 1 in r[32c + i] (i < 16), stored to S column
+        // 16c + i.  Returns the tile's row sum of P.
         const uint64_t sl2x2 = ptx::f2(sl2, sl2);
-        const uint64_t negm = ptx::f2(-mref, -mref);
-        uint64_t lsum = 0;
-        auto exp_store = [&](uint32_t* rr, uint32_t col) {
+        auto exp_pack = [&](float mref) -> float {
+          const uint64_t negm = ptx::f2(-mref, -mref);
+          // exponentials of 32-key chunk c (16 independent exponent pairs,
+          // then 32 independent exponentials)
+          auto chunk_exp = [&](int c, float (&pe)[32]) {
+            const uint32_t* w = r + 32 * c;
 #pragma unroll
-          for (int c = 0; c < 2; ++c) {
-            // packed pairs overwrite the chunk's scores in order (word x2 is
-            // written after scores 2*x2 and 2*x2+1 are read)
-            uint32_t* w = rr + 32 * c;
-#pragma unroll
-            for (int x2 = 0; x2 < 16; ++x2) {
-              float t0, t1;
+            for (int x2 = 0; x2 < 16; ++x2)
               ptx::f2_split(ptx::fma2(ptx::f2(__uint_as_float(w[2 * x2]),
                                               __uint_as_float(w[2 * x2 + 1])),
                                       sl2x2, negm),
-                            t0, t1);
-              const float p0 = ptx::ex2(t0), p1 = ptx::ex2(t1);
-              lsum = ptx::add2(lsum, ptx::f2(p0, p1));
-              w[x2] = ptx::pack_f16x2(p0, p1);
+                            pe[2 * x2], pe[2 * x2 + 1]);
+#pragma unroll
+            for (int x = 0; x < 32; ++x) pe[x] = ptx::ex2(pe[x]);
+          };
+          // software-pipelined: chunk c + 1's exponentials are issued before
+          // chunk c's sums and packs, which wait on the exponential unit's
+          // results; two row-sum accumulators per chunk
+          uint64_t acc[2 * (kNk / 32)];
+          float pa[32], pb[32];
+          chunk_exp(0, pa);
+#pragma unroll
+          for (int c = 0; c < kNk / 32; ++c) {
+            float (&cur)[32] = (c & 1) ? pb : pa;
+            float (&nxt)[32] = (c & 1) ? pa : pb;
+            if (c + 1 < kNk / 32) chunk_exp(c + 1, nxt);
+            uint32_t* w = r + 32 * c;
+            uint64_t s0 = ptx::f2(cur[0], cur[1]), s1 = ptx::f2(cur[2], cur[3]);
+#pragma unroll
+            for (int x2 = 2; x2 < 16; x2 += 2) {
+              s0 = ptx::add2(s0, ptx::f2(cur[2 * x2], cur[2 * x2 + 1]));
+              s1 = ptx::add2(s1, ptx::f2(cur[2 * x2 + 2], cur[2 * x2 + 3]));
             }
-            ptx::tmem_st16(s_addr + col + 32 * c, *reinterpret_cast<uint32_t(*)[16]>(w));
+            // packed pairs overwrite the chunk's first 16 score words, whose
+            // scores were read by chunk_exp(c)
+#pragma unroll
+            for (int x2 = 0; x2 < 16; ++x2) w[x2] = ptx::pack_f16x2(cur[2 * x2], cur[2 * x2 + 1]);
+            acc[2 * c] = s0;
+            acc[2 * c + 1] = s1;
           }
-        };
-        exp_store(r, 0);
-        ld64(64, r);
-        if (edge) apply(r, block_mask(1));
-        exp_store(r, 64);
-        {
+          const uint64_t t = ptx::add2(ptx::add2(ptx::add2(acc[0], acc[1]), ptx::add2(acc[2], acc[3])),
+                                       ptx::add2(ptx::add2(acc[4], acc[5]), ptx::add2(acc[6], acc[7])));
           float a, c;
-          ptx::f2_split(lsum, a, c);
-          l += a + c;
+          ptx::f2_split(t, a, c);
+          return a + c;
+        };
+        // Lazy running max, decided after the exponentials: the tile is first
+        // exponentiated against the running max m_used; if the row sum of
+        // that P is at most 2^15, every P fits fp16 (largest finite 65504)
+        // and is kept, with no pass for the tile max.  Otherwise (or while
+        // m_used is still -inf) the scores are reloaded from TMEM (P is not
+        // stored yet) and the max is raised to the tile max: a row sum above
+        // 2^15 means some P exceeded 2^8, so the tile max lies more than 8
+        // above m_used.  S_g of this tile completing implies P_g V of group
+        // g's previous tile did (MMAs of one thread complete in order), so
+        // O_g may be rescaled (below, before this tile's P is released).
+        bool fast = m_used != -INFINITY;
+        float lt = 0.f;
+        if (__all_sync(0xffffffffu, fast)) {
+          lt = exp_pack(m_used);
+          fast = lt <= kFastSum;
+        } else {
+          fast = false;
+        }
+        bool raise = false;
+        float f = 1.f;
+        if (!__all_sync(0xffffffffu, fast)) {
+          load_s();
+          const float mx = fmaxf(fmaxf(fmax32(&r[0]), fmax32(&r[32])),
+                                 fmaxf(fmax32(&r[64]), fmax32(&r[96])));
+          const float ms = mx * sl2;
+          raise = !fast && ms > m_used;
+          f = raise ? ptx::ex2(m_used - ms) : 1.f;   // 0 when m_used = -inf
+          if (raise) {
+            l *= f;
+            m_used = ms;
+          }
+          // while the running max is still -inf every score seen so far is
+          // -inf: reference 0 then gives 2^-inf = 0
+          lt = exp_pack(m_used == -INFINITY ? 0.f : m_used);
+        }
+        l += lt;
+        {
+          uint32_t lo[32], hi[32];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            lo[i] = r[i];
+            lo[16 + i] = r[32 + i];
+            hi[i] = r[64 + i];
+            hi[16 + i] = r[96 + i];
+          }
+          ptx::tmem_st32(s_addr, lo);
+          ptx::tmem_st32(s_addr + 32, hi);
         }
         ptx::tmem_st_wait();
         // O_g rescale for a raised max, once the scores and P words are no
@@ -765,8 +829,11 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
           }
           ptx::tmem_st_wait();
         }
+        // every lane has waited for its own TMEM stores; the warp's lanes
+        // meet, then one lane arrives for the warp
         ptx::tc_fence_before();
-        ptx::mbar_arrive(&aux->p_ready[g]);
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(&aux->p_ready[g]);
       }
       // epilogue: final O row -> unnormalised partial
       bool fin = ok && !aux->abort_flag && ptx::mbar_wait(&aux->o_final, 0, wait_limit);
@@ -893,6 +960,15 @@ int launch_verify_tc(const void* q, const void* k, const void* v, int64_t L, int
   auto qb = static_cast<const __nv_bfloat16*>(q);
   const long long limit = wait_limit_cycles();
   auto go = [&](auto kern, int smem) {
+    // the warpgroups' register split (setmaxnreg) adds up to 128 registers
+    // a thread at launch; any other count would leave the softmax
+    // warpgroups waiting for registers that never come free
+    cudaFuncAttributes fa{};
+    if (cudaFuncGetAttributes(&fa, kern) != cudaSuccess || fa.numRegs != 128) {
+      rc = fail(TS_ERR_CUDA, "verify kernel compiled to %d registers a thread; its register "
+                "split needs 128", fa.numRegs);
+      return;
+    }
     cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[1];
