@@ -113,21 +113,29 @@ __host__ __device__ __forceinline__ size_t part_o4_index(int kv, int s, int n_sp
   return (((size_t)kv * n_split + s) * (D / 4) + c4) * M + R;
 }
 
+// The cache [0, L) (plus the T tree rows, in the last split) is cut into
+// key splits twice: once for the pair-tile row groups (covering a) and once
+// for the last, short row group's two-stream CTAs (covering b), so that both
+// kinds of CTA finish together.  Partials of split s of either covering sit
+// at split index s, n_max = max(n_a, n_b) apart per KV head.
+struct Splits {
+  int n_a, n_b, n_max;
+  int64_t kps_a, kps_b;   // keys per split (multiples of 128)
+};
 struct VerifyPlan {
   int M;               // packed query rows per KV head (T * G)
   int n_pt;            // row groups of up to 256 rows (pair-tile CTAs, one per split)
   int n_two;           // a last group of <= 128 rows (two-stream CTAs, one per two splits)
-  int n_split;         // KV splits per head
-  int64_t keys_per_split;
+  Splits sp;
   size_t part_o_bytes, part_ml_bytes, ws_bytes;
 };
 VerifyPlan verify_plan(int T, int Hq, int Hkv, int d, int64_t L);
 int tc_splits(int Hkv, int n_rg, int64_t L, int nsm);
-int verify_splits(int Hkv, int n_pt, int n_two, int64_t L, int nsm);
+void verify_splits(int Hkv, int n_pt, int n_two, int64_t L, int nsm, int* n_a, int* n_b);
 int launch_verify_tc(const void* q, const void* k, const void* v, int64_t L, int64_t L_cap,
                      const int32_t* parents, int T, int Hq, int Hkv, int d, int n_imp,
-                     int64_t keys_per_split, int n_split, int n_pt, int n_two, float* part_o,
-                     float* part_ml, float* imp, int32_t* status, cudaStream_t st);
+                     const Splits& sp, int n_pt, int n_two, float* part_o, float* part_ml,
+                     float* imp, int32_t* status, cudaStream_t st);
 
 // Limit (SM clock cycles) of one bounded device wait in the kernels with
 // cross-warp waits; ts_set_wait_limit sets it for later launches.

@@ -7,10 +7,11 @@
 //
 // Work decomposition: for KV head kv the M = T*G query rows of its group are
 // packed (row r = node r / G, head kv*G + r % G) and the committed cache
-// [0, L) is cut into n_split key ranges; the last range also takes the T
-// tree rows under the ancestor mask.  Every (row, split) gets one
-// unnormalised partial (O, m, l) in the log2 domain; the merge kernel below
-// combines the splits of every row.
+// [0, L) is cut into key ranges (one cut for the pair-tile row groups, one
+// for the last short row group); the last range also takes the T tree rows
+// under the ancestor mask.  Every (row, split) gets one unnormalised partial
+// (O, m, l) in the log2 domain; the merge kernel below combines the splits
+// of every row.
 #include "ts_common.cuh"
 
 namespace ts {
@@ -31,11 +32,12 @@ namespace {
 constexpr int kMaxSplits = 1024;
 constexpr int kPer = 5;              // loads in flight per thread
 constexpr int kMergeThreads = 256;   // 8 warps: 8 float4 columns per CTA
-constexpr int kMergeCtasPerSm = 5;   // at <= 48 registers
+constexpr int kMergeCtasPerSm = 4;   // at <= 64 registers
 template <int NG>
 __global__ void __launch_bounds__(kMergeThreads, kMergeCtasPerSm)
 verify_merge(const float* __restrict__ part_o, const float* __restrict__ part_ml, int T, int Hq,
-             int Hkv, int D, int n_split, float* __restrict__ o, float* __restrict__ lse) {
+             int Hkv, int D, int rows_a, int n_a, int n_b, int n_max, float* __restrict__ o,
+             float* __restrict__ lse) {
   constexpr int kRows = 32 / NG;      // rows per warp
   griddep_wait();
   griddep_launch_dependents();
@@ -47,10 +49,16 @@ verify_merge(const float* __restrict__ part_o, const float* __restrict__ part_ml
   const int R = blockIdx.x * kRows + r;
   const bool live = R < M && c4 < D / 4;
   const int Rc = live ? R : 0, cc = live ? c4 : 0;
+  // rows below rows_a belong to the pair-tile row groups (covering a); a
+  // warp's rows never straddle rows_a (a multiple of 256).  A thread with no
+  // row folds no split.
+  const int n_split = live ? (R < rows_a ? n_a : n_b) : 0;
   const float4* src =
-      reinterpret_cast<const float4*>(part_o) + part_o4_index(kv, 0, n_split, cc, D, M, Rc);
-  const size_t step = (size_t)(D / 4) * M;              // float4s between splits
-  const float2* ml = reinterpret_cast<const float2*>(part_ml) + (size_t)kv * n_split * M + Rc;
+      reinterpret_cast<const float4*>(part_o) + part_o4_index(kv, 0, n_max, cc, D, M, Rc);
+  // float4s between splits; s * step < 2^31 (at most 1024 splits of at most
+  // 64 nodes x 64 query heads x 32 float4 columns)
+  const int step = (D / 4) * M;
+  const float2* ml = reinterpret_cast<const float2*>(part_ml) + (size_t)kv * n_max * M + Rc;
   float mrun = -INFINITY, lrun = 0.f;
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
   for (int s0 = j; s0 < n_split; s0 += NG * kPer) {
@@ -59,9 +67,9 @@ verify_merge(const float* __restrict__ part_o, const float* __restrict__ part_ml
 #pragma unroll
     for (int k = 0; k < kPer; ++k) {
       const int s = s0 + k * NG;
-      if (live && s < n_split) {
-        ov[k] = __ldg(&src[(size_t)s * step]);
-        mv[k] = __ldg(&ml[(size_t)s * M]);
+      if (s < n_split) {
+        ov[k] = __ldg(src + s * step);
+        mv[k] = __ldg(ml + s * M);
       } else {
         ov[k] = make_float4(0.f, 0.f, 0.f, 0.f);
         mv[k] = make_float2(-INFINITY, 0.f);
@@ -112,6 +120,20 @@ verify_merge(const float* __restrict__ part_o, const float* __restrict__ part_ml
 
 }  // namespace
 
+// Keys per split for n splits of [0, L): whole 128-key tiles, at most
+// kMaxSplits splits (bounds the partials of very long caches).
+static void cut(int64_t L, int n, int& n_out, int64_t& kps) {
+  kps = (L + n - 1) / n;
+  kps = (kps + 127) / 128 * 128;
+  if (kps < 128) kps = 128;
+  n_out = (int)((L + kps - 1) / kps);
+  if (n_out < 1) n_out = 1;
+  if (n_out > kMaxSplits) {
+    kps = ((L + kMaxSplits - 1) / kMaxSplits + 127) / 128 * 128;
+    n_out = (int)((L + kps - 1) / kps);
+  }
+}
+
 VerifyPlan verify_plan(int T, int Hq, int Hkv, int d, int64_t L) {
   VerifyPlan p{};
   p.M = T * (Hq / Hkv);
@@ -124,19 +146,13 @@ VerifyPlan verify_plan(int T, int Hq, int Hkv, int d, int64_t L) {
     rows -= 256;
   }
   p.n_two = rows > 0 ? 1 : 0;
-  int n = verify_splits(Hkv, p.n_pt, p.n_two, L, kGb300Sms);
-  int64_t kps = (L + n - 1) / n;
-  kps = (kps + 127) / 128 * 128;
-  if (kps < 128) kps = 128;
-  p.keys_per_split = kps;
-  p.n_split = (int)((L + kps - 1) / kps);
-  if (p.n_split < 1) p.n_split = 1;
-  if (p.n_split > kMaxSplits) {   // bounds the split partials of very long caches
-    p.keys_per_split = ((L + kMaxSplits - 1) / kMaxSplits + 127) / 128 * 128;
-    p.n_split = (int)((L + p.keys_per_split - 1) / p.keys_per_split);
-  }
-  p.part_o_bytes = align_up((size_t)Hkv * p.n_split * p.M * d * sizeof(float), 256);
-  p.part_ml_bytes = align_up((size_t)Hkv * p.n_split * p.M * 2 * sizeof(float), 256);
+  int na = 1, nb = 1;
+  verify_splits(Hkv, p.n_pt, p.n_two, L, kGb300Sms, &na, &nb);
+  cut(L, na, p.sp.n_a, p.sp.kps_a);
+  cut(L, nb, p.sp.n_b, p.sp.kps_b);
+  p.sp.n_max = p.sp.n_a > p.sp.n_b ? p.sp.n_a : p.sp.n_b;
+  p.part_o_bytes = align_up((size_t)Hkv * p.sp.n_max * p.M * d * sizeof(float), 256);
+  p.part_ml_bytes = align_up((size_t)Hkv * p.sp.n_max * p.M * 2 * sizeof(float), 256);
   p.ws_bytes = p.part_o_bytes + p.part_ml_bytes;
   return p;
 }
@@ -147,8 +163,8 @@ int launch_verify(const void* q, const void* k, const void* v, int64_t L, int64_
   VerifyPlan p = verify_plan(T, Hq, Hkv, d, L);
   float* part_o = static_cast<float*>(ws);
   float* part_ml = reinterpret_cast<float*>(static_cast<char*>(ws) + p.part_o_bytes);
-  int rc = launch_verify_tc(q, k, v, L, L_cap, parents, T, Hq, Hkv, d, n_imp, p.keys_per_split,
-                            p.n_split, p.n_pt, p.n_two, part_o, part_ml, imp, status, st);
+  int rc = launch_verify_tc(q, k, v, L, L_cap, parents, T, Hq, Hkv, d, n_imp, p.sp, p.n_pt,
+                            p.n_two, part_o, part_ml, imp, status, st);
   if (rc) return rc;
   const int ny = (d / 4 + 7) / 8;
   auto ctas = [&](int ng) { return (p.M + 32 / ng - 1) / (32 / ng) * ny * Hkv; };
@@ -160,12 +176,17 @@ int launch_verify(const void* q, const void* k, const void* v, int64_t L, int64_
   pdl_config(&cfg, attr, mgrid, dim3(kMergeThreads), 0, st);
   auto po = static_cast<const float*>(part_o);
   auto pm = static_cast<const float*>(part_ml);
+  const int rows_a = 256 * p.n_pt;
+  const Splits& sp = p.sp;
   if (ng == 4)
-    cudaLaunchKernelEx(&cfg, verify_merge<4>, po, pm, T, Hq, Hkv, d, p.n_split, o, lse);
+    cudaLaunchKernelEx(&cfg, verify_merge<4>, po, pm, T, Hq, Hkv, d, rows_a, sp.n_a, sp.n_b,
+                       sp.n_max, o, lse);
   else if (ng == 2)
-    cudaLaunchKernelEx(&cfg, verify_merge<2>, po, pm, T, Hq, Hkv, d, p.n_split, o, lse);
+    cudaLaunchKernelEx(&cfg, verify_merge<2>, po, pm, T, Hq, Hkv, d, rows_a, sp.n_a, sp.n_b,
+                       sp.n_max, o, lse);
   else
-    cudaLaunchKernelEx(&cfg, verify_merge<1>, po, pm, T, Hq, Hkv, d, p.n_split, o, lse);
+    cudaLaunchKernelEx(&cfg, verify_merge<1>, po, pm, T, Hq, Hkv, d, rows_a, sp.n_a, sp.n_b,
+                       sp.n_max, o, lse);
   return launch_status("verify_merge");
 }
 

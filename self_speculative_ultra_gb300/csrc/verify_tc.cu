@@ -182,8 +182,8 @@ template <int D>
 __global__ void __launch_bounds__(kThreadsTc, 1)
 verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v,
                  const __nv_bfloat16* __restrict__ q, const int32_t* __restrict__ parents, int T,
-                 int Hq, int Hkv, int n_imp, int64_t L, int64_t L_cap, int64_t keys_per_split,
-                 int n_split, int n_pairtile_groups, long long wait_limit,
+                 int Hq, int Hkv, int n_imp, int64_t L, int64_t L_cap, Splits sp,
+                 int n_pairtile_groups, long long wait_limit,
                  float* __restrict__ part_o, float* __restrict__ part_ml, float* __restrict__ imp,
                  int32_t* status) {
   using Ly = TcLayout<D>;
@@ -205,21 +205,21 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
   // ---------------------------------------------------------------- which work
   const int kv = blockIdx.y, x = blockIdx.x;
   const int G = Hq / Hkv, M = T * G;
-  const int n_pt = n_pairtile_groups * n_split;     // pair-tile CTAs per head
+  const int n_pt = n_pairtile_groups * sp.n_a;      // pair-tile CTAs per head
   Seq seq;
   seq.two = x >= n_pt;
   int r0;
   Stream st0, st1;
   if (!seq.two) {
-    const int rg = x / n_split, split = x % n_split;
+    const int rg = x / sp.n_a, split = x % sp.n_a;
     r0 = rg * 256;
-    st0 = make_stream(split, n_split, keys_per_split, L, T);
+    st0 = make_stream(split, sp.n_a, sp.kps_a, L, T);
     st1 = st0;
   } else {
     const int pair = x - n_pt;
     r0 = n_pairtile_groups * 256;
-    st0 = make_stream(2 * pair, n_split, keys_per_split, L, T);
-    st1 = make_stream(2 * pair + 1, n_split, keys_per_split, L, T);
+    st0 = make_stream(2 * pair, sp.n_b, sp.kps_b, L, T);
+    st1 = make_stream(2 * pair + 1, sp.n_b, sp.kps_b, L, T);
   }
   seq.n0 = st0.n;
   seq.n1 = seq.two ? st1.n : 0;
@@ -658,6 +658,10 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
     const uint32_t o_addr = tmem + lane_off + Ly::obase(g);
     float m_used = -INFINITY, l = 0.f;
     bool ok = true;
+    // a warp whose 32 rows all lie past the last query row (the padding of
+    // a short row group) only releases each tile's P: the MMA then reads
+    // stale words in those rows, which feed O rows that are never written
+    const bool warp_rows = __any_sync(0xffffffffu, sm_valid);
     if (active) {
       // tcgen05.ld/st are warp-collective: every branch around them is
       // warp-uniform
@@ -713,6 +717,11 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
         if (!got) {
           ok = false;
           break;
+        }
+        if (!warp_rows) {
+          __syncwarp();
+          if (lane == 0) ptx::mbar_arrive(&aux->p_ready[g]);
+          continue;
         }
         load_s();
         // P = 2^(s*sl2 - m) -> fp16 pairs, in place: the pair of keys
@@ -837,13 +846,15 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
       }
       // epilogue: final O row -> unnormalised partial
       bool fin = ok && !aux->abort_flag && ptx::mbar_wait(&aux->o_final, 0, wait_limit);
-      if (__all_sync(0xffffffffu, fin)) {
+      if (!__all_sync(0xffffffffu, fin)) {
+        timeout(aux, status);
+      } else if (warp_rows) {
         ptx::tc_fence_after();
-        const int split = (int)(my.j0 / keys_per_split);
+        const int split = (int)(my.j0 / (seq.two ? sp.kps_b : sp.kps_a));
         // column-quad-major partial: for each float4 column the warp's 32
         // rows are 512 contiguous bytes
         float4* dst = reinterpret_cast<float4*>(part_o) +
-                      part_o4_index(kv, split, n_split, 0, D, M, sm_valid ? sm_R : 0);
+                      part_o4_index(kv, split, sp.n_max, 0, D, M, sm_valid ? sm_R : 0);
         const size_t c4_stride = (size_t)M;
 #pragma unroll 1
         for (int c = 0; c < D / 32; ++c) {
@@ -859,12 +870,10 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
           }
         }
         if (sm_valid) {
-          const size_t base = ((size_t)kv * n_split + split) * M + sm_R;
+          const size_t base = ((size_t)kv * sp.n_max + split) * M + sm_R;
           part_ml[base * 2] = m_used;
           part_ml[base * 2 + 1] = l;
         }
-      } else {
-        timeout(aux, status);
       }
     }
   }
@@ -917,29 +926,59 @@ int make_kv_map(CUtensorMap* map, const void* base, int Hkv, int64_t L_cap, int 
 // Key splits per (KV head, row group): the count minimising waves x tiles per
 // CTA (+ a fixed per-CTA cost), so the grid fills whole waves of the SMs.
 int tc_splits(int Hkv, int n_rg, int64_t L, int nsm) {
-  return verify_splits(Hkv, n_rg, 0, L, nsm);
+  int na = 1, nb = 1;
+  verify_splits(Hkv, n_rg, 0, L, nsm, &na, &nb);
+  return na;
 }
 
-// The same for the verification grid: n_pt pair-tile row groups take one CTA
-// per split, n_two two-stream row groups one CTA per two splits; both kinds
-// of CTA take about one chain step per tile of a split.
-int verify_splits(int Hkv, int n_pt, int n_two, int64_t L, int nsm) {
+// The same for the verification grid.  n_pt pair-tile row groups take one
+// CTA per split of covering a (n_a splits); the two-stream row group takes
+// one CTA per two splits of covering b (n_b splits).  Time of a CTA in
+// pair-tile tile steps: a pair-tile CTA ~ its tiles + kFixedTiles; a
+// two-stream CTA ~ 2 * kTwoStep * its tiles per split + kFixedTiles, a
+// two-stream step (one query tile, one key tile) costing kTwoStep of a
+// pair-tile step (two query tiles).  The pair minimising waves x the slower
+// CTA kind is chosen; for each n_a only the n_b around the balancing count
+// are tried.
+int64_t split_tiles(int64_t L, int n) { return ((L + n - 1) / n + kNk - 1) / kNk; }
+
+void verify_splits(int Hkv, int n_pt, int n_two, int64_t L, int nsm, int* n_a, int* n_b) {
+  constexpr double kTwoStep = 0.55;
+  constexpr double kFixedTiles = 3.0;
   int64_t max_split = (L + kNk - 1) / kNk;
   if (max_split < 1) max_split = 1;
   if (max_split > 1024) max_split = 1024;
-  int best = 1;
-  int64_t best_cost = INT64_MAX;
-  for (int n = 1; n <= max_split; ++n) {
-    int64_t kps = ((L + n - 1) / n + kNk - 1) / kNk;    // tiles per split
-    int64_t ctas = (int64_t)Hkv * ((int64_t)n_pt * n + (int64_t)n_two * ((n + 1) / 2));
-    int64_t waves = (ctas + nsm - 1) / nsm;
-    int64_t cost = waves * (kps + 3);
-    if (cost < best_cost) {
+  double best_cost = 1e300;
+  int best_a = 1, best_b = 1;
+  auto consider = [&](int a, int b) {
+    if (a < 1 || b < 1 || a > max_split || b > max_split) return;
+    const int64_t ctas = (int64_t)Hkv * ((int64_t)n_pt * a + (int64_t)n_two * ((b + 1) / 2));
+    const int64_t waves = (ctas + nsm - 1) / nsm;
+    double t = 0.0;
+    if (n_pt > 0) t = (double)split_tiles(L, a) + kFixedTiles;
+    if (n_two > 0) t = fmax(t, 2.0 * kTwoStep * (double)split_tiles(L, b) + kFixedTiles);
+    const double cost = (double)waves * t;
+    if (cost < best_cost - 1e-9) {
       best_cost = cost;
-      best = n;
+      best_a = a;
+      best_b = b;
+    }
+  };
+  if (n_pt == 0) {
+    for (int b = 1; b <= max_split; ++b) consider(1, b);
+  } else if (n_two == 0) {
+    for (int a = 1; a <= max_split; ++a) consider(a, 1);
+  } else {
+    for (int a = 1; a <= max_split; ++a) {
+      // the n_b whose two-stream CTAs take about as long as a pair-tile CTA
+      const double ta = (double)split_tiles(L, a);
+      const double tiles_b = ta / (2.0 * kTwoStep);
+      const int b0 = tiles_b > 0 ? (int)ceil((double)L / (kNk * tiles_b)) : 1;
+      for (int b = b0 - 2; b <= b0 + 2; ++b) consider(a, b);
     }
   }
-  return best;
+  *n_a = best_a;
+  *n_b = best_b;
 }
 
 size_t verify_tc_smem_bytes(int d) {
@@ -948,14 +987,14 @@ size_t verify_tc_smem_bytes(int d) {
 
 int launch_verify_tc(const void* q, const void* k, const void* v, int64_t L, int64_t L_cap,
                      const int32_t* parents, int T, int Hq, int Hkv, int d, int n_imp,
-                     int64_t keys_per_split, int n_split, int n_pt, int n_two, float* part_o,
+                     const Splits& sp, int n_pt, int n_two, float* part_o,
                      float* part_ml, float* imp, int32_t* status, cudaStream_t st) {
   CUtensorMap mk, mv;
   int rc = make_kv_map(&mk, k, Hkv, L_cap, d);
   if (rc) return rc;
   rc = make_kv_map(&mv, v, Hkv, L_cap, d);
   if (rc) return rc;
-  const int per_head = n_pt * n_split + n_two * ((n_split + 1) / 2);
+  const int per_head = n_pt * sp.n_a + n_two * ((sp.n_b + 1) / 2);
   dim3 grid(per_head, Hkv);
   auto qb = static_cast<const __nv_bfloat16*>(q);
   const long long limit = wait_limit_cycles();
@@ -974,7 +1013,7 @@ int launch_verify_tc(const void* q, const void* k, const void* v, int64_t L, int
     cudaLaunchAttribute attr[1];
     pdl_config(&cfg, attr, grid, dim3(kThreadsTc), smem, st);
     cudaLaunchKernelEx(&cfg, kern, mk, mv, qb, parents, T, Hq, Hkv, n_imp, L, L_cap,
-                       keys_per_split, n_split, n_pt, limit, part_o, part_ml, imp, status);
+                       sp, n_pt, limit, part_o, part_ml, imp, status);
   };
   if (d == 128)
     go(verify_tc_kernel<128>, TcLayout<128>::kBytes);
