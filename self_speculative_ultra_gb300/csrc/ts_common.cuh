@@ -103,14 +103,15 @@ inline void pdl_config(cudaLaunchConfig_t* cfg, cudaLaunchAttribute* attr, dim3 
 // ---------------------------------------------------------------- launchers
 constexpr int kGb300Sms = 152;   // streaming multiprocessors of one GB300
 
-// Split partials of the verification attention.  part_o is column-quad
-// major: the float4 holding columns [4*c4, 4*c4+4) of packed row R of split
-// s of KV head kv sits at ((kv * n_split + s) * (D/4) + c4) * M + R, so
-// consecutive rows are consecutive float4s (a warp holding 32 rows stores
-// 512 contiguous bytes).  part_ml holds (m, l) pairs at (kv * n_split + s) * M + R.
-__host__ __device__ __forceinline__ size_t part_o4_index(int kv, int s, int n_split, int c4,
+// Split partials of the verification attention.  part_o holds each partial
+// row normalised (O / l) in fp16, column-octet major: the 16 bytes holding
+// columns [8*c8, 8*c8+8) of packed row R of split s of KV head kv sit at
+// uint4 index ((kv * n_split + s) * (D/8) + c8) * M + R, so consecutive rows
+// are consecutive uint4s (a warp holding 32 rows stores 512 contiguous
+// bytes).  part_ml holds the fp32 (m, l) pairs at (kv * n_split + s) * M + R.
+__host__ __device__ __forceinline__ size_t part_o8_index(int kv, int s, int n_split, int c8,
                                                          int D, int M, int R) {
-  return (((size_t)kv * n_split + s) * (D / 4) + c4) * M + R;
+  return (((size_t)kv * n_split + s) * (D / 8) + c8) * M + R;
 }
 
 // The cache [0, L) (plus the T tree rows, in the last split) is cut into
@@ -134,7 +135,7 @@ int tc_splits(int Hkv, int n_rg, int64_t L, int nsm);
 void verify_splits(int Hkv, int n_pt, int n_two, int64_t L, int nsm, int* n_a, int* n_b);
 int launch_verify_tc(const void* q, const void* k, const void* v, int64_t L, int64_t L_cap,
                      const int32_t* parents, int T, int Hq, int Hkv, int d, int n_imp,
-                     const Splits& sp, int n_pt, int n_two, float* part_o, float* part_ml,
+                     const Splits& sp, int n_pt, int n_two, uint4* part_o, float* part_ml,
                      float* imp, int32_t* status, cudaStream_t st);
 
 // Limit (SM clock cycles) of one bounded device wait in the kernels with

@@ -18,24 +18,26 @@ namespace ts {
 
 namespace {
 
-// Thread (row R, float4 column c4, split group j) folds splits j, j + NG,
+// Thread (row R, 8-column octet c8, split group j) folds splits j, j + NG,
 // j + 2*NG, ... of its row with the online-softmax recurrence, kPer partial
 // loads in flight at once (one round trip for up to NG * kPer splits); the
-// NG states of a (row, column) sit in lanes 32/NG apart of one warp and are
+// NG states of a (row, octet) sit in lanes 32/NG apart of one warp and are
 // combined by shuffles.  A warp covers 32/NG consecutive rows x NG split
-// groups of one column, so each group's loads are contiguous.  NG (1, 2 or
-// 4) is the largest that keeps the grid within one wave of the SMs: a
-// second wave of merge CTAs holds SMs the next verification grid waits for.
-// Launched as a programmatic dependent of the verification kernel: it waits
-// for that grid's partials before its first load, then lets the next kernel
-// of the stream start its set-up as this grid's CTAs retire.
+// groups of one octet, so each group's loads are contiguous.  A partial is
+// stored normalised (O_s / l_s, fp16), so split s enters with weight
+// 2^(m_s - m) * l_s.  NG (1, 2 or 4) is the largest that keeps the grid
+// within one wave of the SMs: a second wave of merge CTAs holds SMs the
+// next verification grid waits for.  Launched as a programmatic dependent
+// of the verification kernel: it waits for that grid's partials before its
+// first load, then lets the next kernel of the stream start its set-up as
+// this grid's CTAs retire.
 constexpr int kMaxSplits = 1024;
 constexpr int kPer = 5;              // loads in flight per thread
-constexpr int kMergeThreads = 256;   // 8 warps: 8 float4 columns per CTA
+constexpr int kMergeThreads = 256;   // 8 warps: 8 column octets per CTA
 constexpr int kMergeCtasPerSm = 4;   // at <= 64 registers
 template <int NG>
 __global__ void __launch_bounds__(kMergeThreads, kMergeCtasPerSm)
-verify_merge(const float* __restrict__ part_o, const float* __restrict__ part_ml, int T, int Hq,
+verify_merge(const uint4* __restrict__ part_o, const float* __restrict__ part_ml, int T, int Hq,
              int Hkv, int D, int rows_a, int n_a, int n_b, int n_max, float* __restrict__ o,
              float* __restrict__ lse) {
   constexpr int kRows = 32 / NG;      // rows per warp
@@ -45,33 +47,37 @@ verify_merge(const float* __restrict__ part_o, const float* __restrict__ part_ml
   const int G = Hq / Hkv, M = T * G;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int r = lane % kRows, j = lane / kRows;                  // row in block, split group
-  const int c4 = blockIdx.y * (kMergeThreads / 32) + warp;       // float4 column
+  const int c8 = blockIdx.y * (kMergeThreads / 32) + warp;       // column octet
   const int R = blockIdx.x * kRows + r;
-  const bool live = R < M && c4 < D / 4;
-  const int Rc = live ? R : 0, cc = live ? c4 : 0;
+  const bool live = R < M && c8 < D / 8;
+  const int Rc = live ? R : 0, cc = live ? c8 : 0;
   // rows below rows_a belong to the pair-tile row groups (covering a); a
   // warp's rows never straddle rows_a (a multiple of 256).  A thread with no
   // row folds no split.
   const int n_split = live ? (R < rows_a ? n_a : n_b) : 0;
-  const float4* src =
-      reinterpret_cast<const float4*>(part_o) + part_o4_index(kv, 0, n_max, cc, D, M, Rc);
-  // float4s between splits; s * step < 2^31 (at most 1024 splits of at most
-  // 64 nodes x 64 query heads x 32 float4 columns)
-  const int step = (D / 4) * M;
+  const uint4* src = part_o + part_o8_index(kv, 0, n_max, cc, D, M, Rc);
+  const size_t step = (size_t)(D / 8) * M;              // uint4s between splits
   const float2* ml = reinterpret_cast<const float2*>(part_ml) + (size_t)kv * n_max * M + Rc;
   float mrun = -INFINITY, lrun = 0.f;
-  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  float acc[8];
+#pragma unroll
+  for (int x = 0; x < 8; ++x) acc[x] = 0.f;
+  auto unpack = [](uint32_t w, float& a, float& b) {
+    const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w));
+    a = f.x;
+    b = f.y;
+  };
   for (int s0 = j; s0 < n_split; s0 += NG * kPer) {
-    float4 ov[kPer];
+    uint4 ov[kPer];
     float2 mv[kPer];
 #pragma unroll
     for (int k = 0; k < kPer; ++k) {
       const int s = s0 + k * NG;
       if (s < n_split) {
-        ov[k] = __ldg(src + s * step);
-        mv[k] = __ldg(ml + s * M);
+        ov[k] = __ldg(&src[(size_t)s * step]);
+        mv[k] = __ldg(&ml[(size_t)s * M]);
       } else {
-        ov[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+        ov[k] = make_uint4(0u, 0u, 0u, 0u);
         mv[k] = make_float2(-INFINITY, 0.f);
       }
     }
@@ -81,15 +87,20 @@ verify_merge(const float* __restrict__ part_o, const float* __restrict__ part_ml
     if (mb == -INFINITY) continue;                      // no key seen yet
     const float fr = exp2f(mrun - mb);                  // 0 while mrun = -inf
     lrun *= fr;
-    acc = make_float4(acc.x * fr, acc.y * fr, acc.z * fr, acc.w * fr);
+#pragma unroll
+    for (int x = 0; x < 8; ++x) acc[x] *= fr;
 #pragma unroll
     for (int k = 0; k < kPer; ++k) {
-      const float w = exp2f(mv[k].x - mb);              // 0 for an empty split
-      lrun += w * mv[k].y;
-      acc.x += w * ov[k].x;
-      acc.y += w * ov[k].y;
-      acc.z += w * ov[k].z;
-      acc.w += w * ov[k].w;
+      const float w = exp2f(mv[k].x - mb) * mv[k].y;    // 0 for an empty split
+      lrun += w;
+      const uint32_t wd[4] = {ov[k].x, ov[k].y, ov[k].z, ov[k].w};
+#pragma unroll
+      for (int x = 0; x < 4; ++x) {
+        float a, b;
+        unpack(wd[x], a, b);
+        acc[2 * x] += w * a;
+        acc[2 * x + 1] += w * b;
+      }
     }
     mrun = mb;
   }
@@ -98,24 +109,24 @@ verify_merge(const float* __restrict__ part_o, const float* __restrict__ part_ml
   for (int off = kRows; off < 32; off <<= 1) {
     const float m2 = __shfl_xor_sync(0xffffffffu, mrun, off);
     const float l2 = __shfl_xor_sync(0xffffffffu, lrun, off);
-    const float4 a2 = make_float4(__shfl_xor_sync(0xffffffffu, acc.x, off),
-                                  __shfl_xor_sync(0xffffffffu, acc.y, off),
-                                  __shfl_xor_sync(0xffffffffu, acc.z, off),
-                                  __shfl_xor_sync(0xffffffffu, acc.w, off));
     const float mn = fmaxf(mrun, m2);
     const float f1 = mrun == -INFINITY ? 0.f : exp2f(mrun - mn);
     const float f2 = m2 == -INFINITY ? 0.f : exp2f(m2 - mn);
+#pragma unroll
+    for (int x = 0; x < 8; ++x) {
+      const float a2 = __shfl_xor_sync(0xffffffffu, acc[x], off);
+      acc[x] = acc[x] * f1 + a2 * f2;
+    }
     lrun = lrun * f1 + l2 * f2;
-    acc = make_float4(acc.x * f1 + a2.x * f2, acc.y * f1 + a2.y * f2, acc.z * f1 + a2.z * f2,
-                      acc.w * f1 + a2.w * f2);
     mrun = mn;
   }
   if (!live || j != 0) return;
   const float inv = 1.f / lrun;
   const int i = R / G, h = kv * G + R % G;
-  reinterpret_cast<float4*>(o + ((size_t)i * Hq + h) * D)[c4] =
-      make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
-  if (lse && c4 == 0) lse[(size_t)i * Hq + h] = (mrun + log2f(lrun)) * 0.6931471805599453f;
+  float4* orow = reinterpret_cast<float4*>(o + ((size_t)i * Hq + h) * D) + 2 * c8;
+  orow[0] = make_float4(acc[0] * inv, acc[1] * inv, acc[2] * inv, acc[3] * inv);
+  orow[1] = make_float4(acc[4] * inv, acc[5] * inv, acc[6] * inv, acc[7] * inv);
+  if (lse && c8 == 0) lse[(size_t)i * Hq + h] = (mrun + log2f(lrun)) * 0.6931471805599453f;
 }
 
 }  // namespace
@@ -151,7 +162,7 @@ VerifyPlan verify_plan(int T, int Hq, int Hkv, int d, int64_t L) {
   cut(L, na, p.sp.n_a, p.sp.kps_a);
   cut(L, nb, p.sp.n_b, p.sp.kps_b);
   p.sp.n_max = p.sp.n_a > p.sp.n_b ? p.sp.n_a : p.sp.n_b;
-  p.part_o_bytes = align_up((size_t)Hkv * p.sp.n_max * p.M * d * sizeof(float), 256);
+  p.part_o_bytes = align_up((size_t)Hkv * p.sp.n_max * p.M * d * sizeof(__half), 256);
   p.part_ml_bytes = align_up((size_t)Hkv * p.sp.n_max * p.M * 2 * sizeof(float), 256);
   p.ws_bytes = p.part_o_bytes + p.part_ml_bytes;
   return p;
@@ -161,12 +172,12 @@ int launch_verify(const void* q, const void* k, const void* v, int64_t L, int64_
                   const int32_t* parents, int T, int Hq, int Hkv, int d, int n_imp, float* o,
                   float* lse, float* imp, void* ws, int32_t* status, cudaStream_t st) {
   VerifyPlan p = verify_plan(T, Hq, Hkv, d, L);
-  float* part_o = static_cast<float*>(ws);
+  uint4* part_o = static_cast<uint4*>(ws);
   float* part_ml = reinterpret_cast<float*>(static_cast<char*>(ws) + p.part_o_bytes);
   int rc = launch_verify_tc(q, k, v, L, L_cap, parents, T, Hq, Hkv, d, n_imp, p.sp, p.n_pt,
                             p.n_two, part_o, part_ml, imp, status, st);
   if (rc) return rc;
-  const int ny = (d / 4 + 7) / 8;
+  const int ny = (d / 8 + 7) / 8;
   auto ctas = [&](int ng) { return (p.M + 32 / ng - 1) / (32 / ng) * ny * Hkv; };
   const int wave = kMergeCtasPerSm * kGb300Sms;
   const int ng = ctas(4) <= wave ? 4 : (ctas(2) <= wave ? 2 : 1);
@@ -174,7 +185,7 @@ int launch_verify(const void* q, const void* k, const void* v, int64_t L, int64_
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
   pdl_config(&cfg, attr, mgrid, dim3(kMergeThreads), 0, st);
-  auto po = static_cast<const float*>(part_o);
+  auto po = static_cast<const uint4*>(part_o);
   auto pm = static_cast<const float*>(part_ml);
   const int rows_a = 256 * p.n_pt;
   const Splits& sp = p.sp;

@@ -184,7 +184,7 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
                  const __nv_bfloat16* __restrict__ q, const int32_t* __restrict__ parents, int T,
                  int Hq, int Hkv, int n_imp, int64_t L, int64_t L_cap, Splits sp,
                  int n_pairtile_groups, long long wait_limit,
-                 float* __restrict__ part_o, float* __restrict__ part_ml, float* __restrict__ imp,
+                 uint4* __restrict__ part_o, float* __restrict__ part_ml, float* __restrict__ imp,
                  int32_t* status) {
   using Ly = TcLayout<D>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -851,22 +851,25 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
       } else if (warp_rows) {
         ptx::tc_fence_after();
         const int split = (int)(my.j0 / (seq.two ? sp.kps_b : sp.kps_a));
-        // column-quad-major partial: for each float4 column the warp's 32
-        // rows are 512 contiguous bytes
-        float4* dst = reinterpret_cast<float4*>(part_o) +
-                      part_o4_index(kv, split, sp.n_max, 0, D, M, sm_valid ? sm_R : 0);
-        const size_t c4_stride = (size_t)M;
+        // the partial row normalised (O / l: a convex combination of V rows,
+        // so |O / l| <= max |v| < 65504) in fp16, column-octet major: for
+        // each 8-column octet the warp's 32 rows are 512 contiguous bytes
+        uint4* dst = part_o + part_o8_index(kv, split, sp.n_max, 0, D, M, sm_valid ? sm_R : 0);
+        const size_t c8_stride = (size_t)M;
+        const float inv = l > 0.f ? 1.f / l : 0.f;
 #pragma unroll 1
         for (int c = 0; c < D / 32; ++c) {
           uint32_t o[32];
           ptx::tmem_ld32(o_addr + c * 32, o);
           ptx::tmem_ld_wait();
           if (sm_valid) {
+            auto h2 = [&](int x) {
+              return ptx::pack_f16x2(__uint_as_float(o[x]) * inv, __uint_as_float(o[x + 1]) * inv);
+            };
 #pragma unroll
-            for (int x2 = 0; x2 < 8; ++x2)
-              dst[(size_t)(c * 8 + x2) * c4_stride] =
-                  make_float4(__uint_as_float(o[4 * x2]), __uint_as_float(o[4 * x2 + 1]),
-                              __uint_as_float(o[4 * x2 + 2]), __uint_as_float(o[4 * x2 + 3]));
+            for (int x8 = 0; x8 < 4; ++x8)
+              dst[(size_t)(c * 4 + x8) * c8_stride] =
+                  make_uint4(h2(8 * x8), h2(8 * x8 + 2), h2(8 * x8 + 4), h2(8 * x8 + 6));
           }
         }
         if (sm_valid) {
@@ -987,7 +990,7 @@ size_t verify_tc_smem_bytes(int d) {
 
 int launch_verify_tc(const void* q, const void* k, const void* v, int64_t L, int64_t L_cap,
                      const int32_t* parents, int T, int Hq, int Hkv, int d, int n_imp,
-                     const Splits& sp, int n_pt, int n_two, float* part_o,
+                     const Splits& sp, int n_pt, int n_two, uint4* part_o,
                      float* part_ml, float* imp, int32_t* status, cudaStream_t st) {
   CUtensorMap mk, mv;
   int rc = make_kv_map(&mk, k, Hkv, L_cap, d);

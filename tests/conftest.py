@@ -12,9 +12,15 @@ def pytest_configure(config):
 
 
 def pytest_terminal_summary(terminalreporter, exitstatus, config):
-    """One line with the near-ties the parity tests counted (kind: ties of
-    compared items), so a run's tail records them."""
+    """The largest attention error the parity checks saw, and the near-ties
+    they counted (kind: ties of compared items), so a run's tail records
+    both."""
     pu = sys.modules.get("parity_util")
+    errs = getattr(pu, "ERR_MAX", None) if pu is not None else None
+    if errs and errs["attention rel"] > 0:
+        terminalreporter.write_line(
+            f"largest attention error vs the oracle: row-relative {errs['attention rel']:.3e} "
+            f"(tolerance {pu.ATTN_RTOL:g}), lse absolute {errs['lse abs']:.3e}")
     counts = getattr(pu, "TIE_COUNTS", None) if pu is not None else None
     if not counts:
         return

@@ -72,11 +72,18 @@ def attention_rel_err(o: np.ndarray, o_ref: np.ndarray) -> np.ndarray:
     return num / np.maximum(den, 1e-30)
 
 
+# largest attention row error (relative, per row) and LSE error seen by the
+# parity checks of this session, reported in the pytest summary
+ERR_MAX = {"attention rel": 0.0, "lse abs": 0.0}
+
+
 def check_attention(o, lse, o_ref, lse_ref):
     rel = attention_rel_err(o.astype(np.float64), o_ref)
+    ERR_MAX["attention rel"] = max(ERR_MAX["attention rel"], float(rel.max()))
     assert rel.max() <= ATTN_RTOL, f"attention rel err {rel.max():.3e} > {ATTN_RTOL}"
     if lse is not None:
         d = np.abs(lse.astype(np.float64) - lse_ref)
+        ERR_MAX["lse abs"] = max(ERR_MAX["lse abs"], float(d.max()))
         assert d.max() <= LSE_ATOL, f"lse abs err {d.max():.3e}"
     return float(rel.max())
 
