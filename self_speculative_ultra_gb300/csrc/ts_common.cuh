@@ -115,10 +115,12 @@ __host__ __device__ __forceinline__ size_t part_o8_index(int kv, int s, int n_sp
 }
 
 // The cache [0, L) (plus the T tree rows, in the last split) is cut into
-// key splits twice: once for the pair-tile row groups (covering a) and once
-// for the last, short row group's two-stream CTAs (covering b), so that both
-// kinds of CTA finish together.  Partials of split s of either covering sit
-// at split index s, n_max = max(n_a, n_b) apart per KV head.
+// key splits for the pair-tile row groups (cut a) and for the last, short
+// row group's two-stream CTAs (cut b).  The plan uses one cut for both
+// (n_a = n_b), so that every key tile is read by all row groups at about the
+// same time and leaves HBM once; the kernels and the merge take the two
+// separately.  Partials of split s of either cut sit at split index s,
+// n_max = max(n_a, n_b) apart per KV head.
 struct Splits {
   int n_a, n_b, n_max;
   int64_t kps_a, kps_b;   // keys per split (multiples of 128)

@@ -935,14 +935,15 @@ int tc_splits(int Hkv, int n_rg, int64_t L, int nsm) {
 }
 
 // The same for the verification grid.  n_pt pair-tile row groups take one
-// CTA per split of covering a (n_a splits); the two-stream row group takes
-// one CTA per two splits of covering b (n_b splits).  Time of a CTA in
+// CTA per split; the two-stream row group takes one CTA per two consecutive
+// splits of the same cut (n_b = n_a), so its CTAs read every key tile at
+// about the time a pair-tile CTA reads it and the second read is an L2 hit:
+// K and V leave HBM once.  (Separate cuts balanced for time were measured at
+// 1.8 x the K/V bytes from HBM on the 14B shape.)  Time of a CTA in
 // pair-tile tile steps: a pair-tile CTA ~ its tiles + kFixedTiles; a
 // two-stream CTA ~ 2 * kTwoStep * its tiles per split + kFixedTiles, a
 // two-stream step (one query tile, one key tile) costing kTwoStep of a
-// pair-tile step (two query tiles).  The pair minimising waves x the slower
-// CTA kind is chosen; for each n_a only the n_b around the balancing count
-// are tried.
+// pair-tile step (two query tiles).
 int64_t split_tiles(int64_t L, int n) { return ((L + n - 1) / n + kNk - 1) / kNk; }
 
 void verify_splits(int Hkv, int n_pt, int n_two, int64_t L, int nsm, int* n_a, int* n_b) {
@@ -952,36 +953,21 @@ void verify_splits(int Hkv, int n_pt, int n_two, int64_t L, int nsm, int* n_a, i
   if (max_split < 1) max_split = 1;
   if (max_split > 1024) max_split = 1024;
   double best_cost = 1e300;
-  int best_a = 1, best_b = 1;
-  auto consider = [&](int a, int b) {
-    if (a < 1 || b < 1 || a > max_split || b > max_split) return;
-    const int64_t ctas = (int64_t)Hkv * ((int64_t)n_pt * a + (int64_t)n_two * ((b + 1) / 2));
+  int best = 1;
+  for (int n = 1; n <= max_split; ++n) {
+    const int64_t ctas = (int64_t)Hkv * ((int64_t)n_pt * n + (int64_t)n_two * ((n + 1) / 2));
     const int64_t waves = (ctas + nsm - 1) / nsm;
     double t = 0.0;
-    if (n_pt > 0) t = (double)split_tiles(L, a) + kFixedTiles;
-    if (n_two > 0) t = fmax(t, 2.0 * kTwoStep * (double)split_tiles(L, b) + kFixedTiles);
+    if (n_pt > 0) t = (double)split_tiles(L, n) + kFixedTiles;
+    if (n_two > 0) t = fmax(t, 2.0 * kTwoStep * (double)split_tiles(L, n) + kFixedTiles);
     const double cost = (double)waves * t;
     if (cost < best_cost - 1e-9) {
       best_cost = cost;
-      best_a = a;
-      best_b = b;
-    }
-  };
-  if (n_pt == 0) {
-    for (int b = 1; b <= max_split; ++b) consider(1, b);
-  } else if (n_two == 0) {
-    for (int a = 1; a <= max_split; ++a) consider(a, 1);
-  } else {
-    for (int a = 1; a <= max_split; ++a) {
-      // the n_b whose two-stream CTAs take about as long as a pair-tile CTA
-      const double ta = (double)split_tiles(L, a);
-      const double tiles_b = ta / (2.0 * kTwoStep);
-      const int b0 = tiles_b > 0 ? (int)ceil((double)L / (kNk * tiles_b)) : 1;
-      for (int b = b0 - 2; b <= b0 + 2; ++b) consider(a, b);
+      best = n;
     }
   }
-  *n_a = best_a;
-  *n_b = best_b;
+  *n_a = best;
+  *n_b = best;
 }
 
 size_t verify_tc_smem_bytes(int d) {
