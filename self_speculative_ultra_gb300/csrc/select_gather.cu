@@ -294,44 +294,78 @@ select_collect(Layers P, int64_t L, int S, int R, int64_t n_chunks, Ws w) {
   __shared__ int warp_buf[32], s_total, s_last;
   __shared__ uint32_t s_cnt[1024];
   __shared__ int s_gt[kPerScan];
-  // bucket members gathered per CTA, then appended to the head's list with
-  // one global reservation (a global atomic round trip per warp vote stalls)
+  // bucket members gathered per warp in its own region of s_list (a
+  // warp-uniform count, no atomic per vote), then appended to the head's
+  // list with one global reservation per CTA
   constexpr int kListBuf = 2048;
+  constexpr int kWarps = kThreads / 32, kWarpCap = kListBuf / kWarps;
+  static_assert(kPerScan == 4, "the above-bucket counters are four registers");
   __shared__ uint2 s_list[kListBuf];
-  __shared__ int s_nlist, s_gbase;
+  __shared__ int s_wn[kWarps], s_gbase;
   const SelectState st0 = w.state[hh];
   const bool work = !st0.select_all && st0.bucket >= 0;
   uint2* list = w.list + (size_t)hh * L;
   if (work) {
     const uint32_t b = (uint32_t)st0.bucket;
+    const int warp = tid >> 5;
     if (tid < kPerScan) s_gt[tid] = 0;
-    if (tid == 0) s_nlist = 0;
     __syncthreads();
     const int64_t lo = imax64(S, c * kScan), hi = imin64(L - R, (c + 1) * kScan);
+    // keys above bucket b, counted per gather chunk in registers
+    int g0 = 0, g1 = 0, g2 = 0, g3 = 0;
+    uint2* wl = s_list + warp * kWarpCap;
+    int wn = 0;   // bucket members this warp found (the same in every lane)
     for_each_pos(imp_h, lo, hi, [&](int64_t j, float x, bool ok) {
       const uint32_t key = ok ? float_key(x) : 0u, bk = key >> (32 - kHistBits);
-      // keys above bucket b, counted per gather chunk
-      if (ok && bk > b) atomicAdd(&s_gt[(int)(j / kChunk - c * kPerScan)], 1);
+      if (ok && bk > b) {
+        const int ci = (int)(j / kChunk - c * kPerScan);
+        g0 += ci == 0;
+        g1 += ci == 1;
+        g2 += ci == 2;
+        g3 += ci == 3;
+      }
       const bool eq = ok && bk == b;
       const unsigned m = __ballot_sync(0xffffffffu, eq);
       if (m) {
-        int base = 0;
-        if (lane == __ffs(m) - 1) base = atomicAdd(&s_nlist, __popc(m));
-        base = __shfl_sync(0xffffffffu, base, __ffs(m) - 1);
-        const int slot = base + __popc(m & ((1u << lane) - 1));
+        const int slot = wn + __popc(m & ((1u << lane) - 1));
         if (eq) {
-          if (slot < kListBuf)
-            s_list[slot] = make_uint2(key, (uint32_t)j);
-          else   // buffer full: straight to the head's list
+          if (slot < kWarpCap)
+            wl[slot] = make_uint2(key, (uint32_t)j);
+          else   // the warp's region is full: straight to the head's list
             list[atomicAdd(&w.cnt[hh].n_list, 1u)] = make_uint2(key, (uint32_t)j);
         }
+        wn += __popc(m);
       }
     });
+    auto warp_sum = [](int v) {
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+      return v;
+    };
+    g0 = warp_sum(g0);
+    g1 = warp_sum(g1);
+    g2 = warp_sum(g2);
+    g3 = warp_sum(g3);
+    if (lane == 0) {
+      if (g0) atomicAdd(&s_gt[0], g0);
+      if (g1) atomicAdd(&s_gt[1], g1);
+      if (g2) atomicAdd(&s_gt[2], g2);
+      if (g3) atomicAdd(&s_gt[3], g3);
+      s_wn[warp] = min(wn, kWarpCap);
+    }
     __syncthreads();
-    const int nloc = min(s_nlist, kListBuf);
-    if (tid == 0) s_gbase = nloc ? (int)atomicAdd(&w.cnt[hh].n_list, (uint32_t)nloc) : 0;
+    if (tid == 0) {
+      int tot = 0;
+      for (int x = 0; x < kWarps; ++x) tot += s_wn[x];
+      s_gbase = tot ? (int)atomicAdd(&w.cnt[hh].n_list, (uint32_t)tot) : 0;
+    }
     __syncthreads();
-    for (int e = tid; e < nloc; e += nthr) list[s_gbase + e] = s_list[e];
+    {
+      // warp x's entries go after those of warps 0..x-1
+      int off = s_gbase;
+      for (int x = 0; x < warp; ++x) off += s_wn[x];
+      for (int e = lane; e < s_wn[warp]; e += 32) list[off + e] = wl[e];
+    }
     __syncthreads();
     if (tid < kPerScan && c * kPerScan + tid < n_chunks)
       w.gt[(size_t)hh * n_chunks + c * kPerScan + tid] = s_gt[tid];
@@ -353,6 +387,7 @@ select_collect(Layers P, int64_t L, int S, int R, int64_t n_chunks, Ws w) {
     uint32_t pre = (uint32_t)st.bucket << (32 - kHistBits);
     uint32_t msk = 0xFFFFFFFFu << (32 - kHistBits);
     int need = st.need;
+    int n_eq = -1;
     // the remaining 20 key bits, two 10-bit levels, largest keys first
     for (int lvl = 0; lvl < 2; ++lvl) {
       const int shift = 10 - 10 * lvl;
@@ -366,12 +401,17 @@ select_collect(Layers P, int64_t L, int S, int R, int64_t n_chunks, Ws w) {
       need -= s_before;
       pre |= (uint32_t)s_b << shift;
       msk |= 1023u << shift;
+      // after the last level the bucket holds exactly the members whose key
+      // equals tau
+      if (lvl == 1) n_eq = (int)s_cnt[s_b];
+      __syncthreads();
       for (int x = tid; x < 1024; x += nthr) s_cnt[x] = 0;
     }
     const uint32_t tau = pre;
-    // the need-th smallest position among keys == tau: four 8-bit levels
-    uint32_t ppre = 0, pmsk = 0;
-    for (int lvl = 0; lvl < 4; ++lvl) {
+    // the need-th smallest position among keys == tau: four 8-bit levels,
+    // unless every member with key tau is kept (no tie at the cut)
+    uint32_t ppre = n_eq == need ? 0x7FFFFFFFu : 0u, pmsk = 0;
+    for (int lvl = 0; lvl < 4 && n_eq != need; ++lvl) {
       const int shift = 24 - 8 * lvl;
       __syncthreads();
       for (uint32_t e = tid; e < n; e += nthr) {
