@@ -89,6 +89,52 @@ __host__ inline size_t ws_total(int Hkv, int64_t L, int64_t n_chunks) {
   return o;
 }
 
+// Incremental refresh workspace (used by select_collect when it also counts
+// the newly selected positions, and by the refresh kernels below).
+struct RefreshWs {
+  uint32_t* bits;      // [heads][W32]
+  uint32_t* ticket;    // [heads]
+  int32_t* n_freed;    // [heads]
+  int32_t* cnt;        // [heads][n_chunks]
+  int32_t* off;        // [heads][n_chunks + 1]
+  int32_t* freed;      // [heads][N_cap]
+  int64_t w32;         // bitmap words per head
+  size_t zero_bytes;   // bits + tickets, zeroed per call
+};
+
+__host__ __device__ inline RefreshWs carve_refresh(void* base, int HH, int64_t L, int64_t n_chunks,
+                                                   int64_t N_cap) {
+  RefreshWs r;
+  char* p = static_cast<char*>(base);
+  size_t o = 0;
+  r.w32 = (L + 31) / 32 > 0 ? (L + 31) / 32 : 1;
+  r.bits = reinterpret_cast<uint32_t*>(p + o);
+  o += a256((size_t)HH * r.w32 * sizeof(uint32_t));
+  r.ticket = reinterpret_cast<uint32_t*>(p + o);
+  o += a256((size_t)HH * sizeof(uint32_t));
+  r.zero_bytes = o;
+  r.n_freed = reinterpret_cast<int32_t*>(p + o);
+  o += a256((size_t)HH * sizeof(int32_t));
+  r.cnt = reinterpret_cast<int32_t*>(p + o);
+  o += a256((size_t)HH * n_chunks * sizeof(int32_t));
+  r.off = reinterpret_cast<int32_t*>(p + o);
+  o += a256((size_t)HH * (n_chunks + 1) * sizeof(int32_t));
+  r.freed = reinterpret_cast<int32_t*>(p + o);
+  return r;
+}
+
+__host__ inline size_t refresh_area_bytes(int HH, int64_t L, int64_t n_chunks, int64_t N_cap) {
+  const int64_t w32 = (L + 31) / 32 > 0 ? (L + 31) / 32 : 1;
+  return a256((size_t)HH * w32 * sizeof(uint32_t)) + a256((size_t)HH * sizeof(uint32_t)) +
+         a256((size_t)HH * sizeof(int32_t)) + a256((size_t)HH * n_chunks * sizeof(int32_t)) +
+         a256((size_t)HH * (n_chunks + 1) * sizeof(int32_t)) +
+         a256((size_t)HH * (N_cap > 0 ? N_cap : 1) * sizeof(int32_t));
+}
+
+__device__ __forceinline__ bool bit_of(const uint32_t* bits, int64_t j) {
+  return (bits[j >> 5] >> (j & 31)) & 1u;
+}
+
 // Per-layer tensors: device arrays of per-layer pointers (batched call) or,
 // when those are null, the single layer's pointers.
 struct Layers {
@@ -285,8 +331,13 @@ select_hist(Layers P, int64_t L, int B, int S, int R, int64_t n_chunks, Ws w) {
   if (tid == 0) w.state[hh] = st;
 }
 
-__global__ void __launch_bounds__(kThreads, 6)
-select_collect(Layers P, int64_t L, int S, int R, int64_t n_chunks, Ws w) {
+// With r.bits set (the incremental refresh), the same pass also counts, per
+// gather chunk, the selected positions missing from the previous slots'
+// bitmap, and the last CTA of a head lists the freed slots and turns the
+// counts into the refresh offsets (the importance rows are not read again).
+__global__ void __launch_bounds__(kThreads, 4)
+select_collect(Layers P, int64_t L, int S, int R, int64_t n_chunks, Ws w, RefreshWs r,
+               int64_t N_prev, int64_t N_new, int64_t N_cap, int32_t* status) {
   const int kv = blockIdx.y, tid = threadIdx.x, lane = tid & 31, nthr = blockDim.x;
   const int layer = blockIdx.z, hh = layer * gridDim.y + kv;
   const int64_t c = blockIdx.x;
@@ -301,18 +352,23 @@ select_collect(Layers P, int64_t L, int S, int R, int64_t n_chunks, Ws w) {
   constexpr int kWarps = kThreads / 32, kWarpCap = kListBuf / kWarps;
   static_assert(kPerScan == 4, "the above-bucket counters are four registers");
   __shared__ uint2 s_list[kListBuf];
-  __shared__ int s_wn[kWarps], s_gbase;
+  __shared__ int s_wn[kWarps], s_gbase, s_gn[kPerScan];
   const SelectState st0 = w.state[hh];
   const bool work = !st0.select_all && st0.bucket >= 0;
   uint2* list = w.list + (size_t)hh * L;
+  const uint32_t* rbits = r.bits ? r.bits + (size_t)hh * r.w32 : nullptr;
   if (work) {
     const uint32_t b = (uint32_t)st0.bucket;
     const int warp = tid >> 5;
-    if (tid < kPerScan) s_gt[tid] = 0;
+    if (tid < kPerScan) {
+      s_gt[tid] = 0;
+      s_gn[tid] = 0;
+    }
     __syncthreads();
     const int64_t lo = imax64(S, c * kScan), hi = imin64(L - R, (c + 1) * kScan);
-    // keys above bucket b, counted per gather chunk in registers
-    int g0 = 0, g1 = 0, g2 = 0, g3 = 0;
+    // keys above bucket b, counted per gather chunk in registers (and, for
+    // the refresh, those missing from the previous slots)
+    int g0 = 0, g1 = 0, g2 = 0, g3 = 0, n0 = 0, n1 = 0, n2 = 0, n3 = 0;
     uint2* wl = s_list + warp * kWarpCap;
     int wn = 0;   // bucket members this warp found (the same in every lane)
     for_each_pos(imp_h, lo, hi, [&](int64_t j, float x, bool ok) {
@@ -323,6 +379,12 @@ select_collect(Layers P, int64_t L, int S, int R, int64_t n_chunks, Ws w) {
         g1 += ci == 1;
         g2 += ci == 2;
         g3 += ci == 3;
+        if (rbits && !bit_of(rbits, j)) {
+          n0 += ci == 0;
+          n1 += ci == 1;
+          n2 += ci == 2;
+          n3 += ci == 3;
+        }
       }
       const bool eq = ok && bk == b;
       const unsigned m = __ballot_sync(0xffffffffu, eq);
@@ -346,11 +408,21 @@ select_collect(Layers P, int64_t L, int S, int R, int64_t n_chunks, Ws w) {
     g1 = warp_sum(g1);
     g2 = warp_sum(g2);
     g3 = warp_sum(g3);
+    if (rbits) {
+      n0 = warp_sum(n0);
+      n1 = warp_sum(n1);
+      n2 = warp_sum(n2);
+      n3 = warp_sum(n3);
+    }
     if (lane == 0) {
       if (g0) atomicAdd(&s_gt[0], g0);
       if (g1) atomicAdd(&s_gt[1], g1);
       if (g2) atomicAdd(&s_gt[2], g2);
       if (g3) atomicAdd(&s_gt[3], g3);
+      if (n0) atomicAdd(&s_gn[0], n0);
+      if (n1) atomicAdd(&s_gn[1], n1);
+      if (n2) atomicAdd(&s_gn[2], n2);
+      if (n3) atomicAdd(&s_gn[3], n3);
       s_wn[warp] = min(wn, kWarpCap);
     }
     __syncthreads();
@@ -367,14 +439,20 @@ select_collect(Layers P, int64_t L, int S, int R, int64_t n_chunks, Ws w) {
       for (int e = lane; e < s_wn[warp]; e += 32) list[off + e] = wl[e];
     }
     __syncthreads();
-    if (tid < kPerScan && c * kPerScan + tid < n_chunks)
+    if (tid < kPerScan && c * kPerScan + tid < n_chunks) {
       w.gt[(size_t)hh * n_chunks + c * kPerScan + tid] = s_gt[tid];
+      if (rbits) r.cnt[(size_t)hh * n_chunks + c * kPerScan + tid] = s_gn[tid];
+    }
   }
   if (!last_of_head(&w.cnt[hh].collect_ticket, (uint32_t)gridDim.x, &s_last)) return;
 
   // ---- last CTA of this head: (tau, j_tie) inside bucket b, then offsets
   SelectState st = st0;
-  for (int x = tid; x < 1024; x += nthr) s_cnt[x] = 0;
+  __shared__ uint32_t s_new[1024];   // refresh: new kept positions per gather chunk
+  for (int x = tid; x < 1024; x += nthr) {
+    s_cnt[x] = 0;
+    s_new[x] = 0;
+  }
   __syncthreads();
   __shared__ int s_b, s_before;
   if (work) {
@@ -431,7 +509,10 @@ select_collect(Layers P, int64_t L, int S, int R, int64_t n_chunks, Ws w) {
     // kept positions of bucket b per chunk (n_chunks <= 1024)
     for (uint32_t e = tid; e < n; e += nthr) {
       const uint2 v = member(e);
-      if (v.x > tau || (v.x == tau && (int32_t)v.y <= st.j_tie)) atomicAdd(&s_cnt[v.y / kChunk], 1u);
+      if (v.x > tau || (v.x == tau && (int32_t)v.y <= st.j_tie)) {
+        atomicAdd(&s_cnt[v.y / kChunk], 1u);
+        if (rbits && !bit_of(rbits, v.y)) atomicAdd(&s_new[v.y / kChunk], 1u);
+      }
     }
   }
   __syncthreads();
@@ -467,6 +548,68 @@ select_collect(Layers P, int64_t L, int S, int R, int64_t n_chunks, Ws w) {
   if (tid == 0) {
     off[n_chunks] = s_total;
     w.state[hh] = st;
+  }
+  if (!rbits) return;
+
+  // ---- refresh: new kept positions per chunk (the scan's above-bucket
+  // part, the bucket picks above, the sinks and the recent window, or with
+  // everything kept the positions missing from the bitmap), their offsets,
+  // and the previous slots whose position is no longer kept
+  if (st.select_all) {
+    for (int64_t wi = tid; wi < (L + 31) / 32; wi += nthr) {
+      const int64_t rem = L - wi * 32;
+      const uint32_t valid = rem >= 32 ? 0xFFFFFFFFu : ((1u << rem) - 1u);
+      const int cnew = __popc(~rbits[wi] & valid);
+      if (cnew) atomicAdd(&s_new[(wi * 32) / kChunk], (uint32_t)cnew);
+    }
+  } else {
+    // sinks [0, S) and the recent window [L-R, L) (disjoint here, as L > S+B+R)
+    for (int64_t x = tid; x < (int64_t)S + R; x += nthr) {
+      const int64_t j = x < S ? x : L - R + (x - S);
+      if (j >= 0 && j < L && !bit_of(rbits, j)) atomicAdd(&s_new[j / kChunk], 1u);
+    }
+  }
+  __syncthreads();
+  int ncnt[4], nmine = 0;
+#pragma unroll
+  for (int x = 0; x < 4; ++x) {
+    const int64_t ch = (int64_t)tid * 4 + x;
+    int cnt = 0;
+    if (ch < n_chunks) {
+      cnt = (int)s_new[ch];
+      if (work) cnt += __ldcg(&r.cnt[(size_t)hh * n_chunks + ch]);
+    }
+    ncnt[x] = cnt;
+    nmine += cnt;
+  }
+  int nbefore = block_excl_scan(nmine, warp_buf, &s_total);
+  int32_t* roff = r.off + (size_t)hh * (n_chunks + 1);
+#pragma unroll
+  for (int x = 0; x < 4; ++x) {
+    const int64_t ch = (int64_t)tid * 4 + x;
+    if (ch < n_chunks) roff[ch] = nbefore;
+    nbefore += ncnt[x];
+  }
+  const int n_new_total = s_total;
+  // freed slots: their position is no longer selected (or was invalid)
+  const int32_t* idx = (P.idx ? P.idx[layer] : P.idx1) + (size_t)kv * N_cap;
+  int fbase = 0;
+  for (int64_t s0 = 0; s0 < N_prev; s0 += nthr) {
+    const int64_t sl = s0 + tid;
+    int f = 0;
+    if (sl < N_prev) {
+      const int32_t p = idx[sl];
+      f = !(p >= 0 && p < L && keep_pos(imp_h, p, L, S, R, st));
+    }
+    const int pos = block_excl_scan(f, warp_buf, &s_total);
+    if (f) r.freed[(size_t)hh * N_cap + fbase + pos] = (int32_t)sl;
+    fbase += s_total;
+  }
+  if (tid == 0) {
+    roff[n_chunks] = n_new_total;
+    r.n_freed[hh] = fbase;
+    if ((int64_t)n_new_total != (int64_t)fbase + (N_new - N_prev))
+      set_status(status, TS_ERR_INVALID_ARG);   // duplicate or invalid previous slots
   }
 }
 
@@ -536,56 +679,14 @@ select_gather(Layers P, int64_t L, int64_t L_cap, int S, int R, int64_t N, int64
 // freed slots in ascending slot order, then the slots [N_prev, N_new) while
 // the cache still grows.  Only those rows are copied.  Stages after the
 // selection's histogram and collect kernels:
-//   refresh_bits    bitmap of the previous slots' positions
-//   refresh_mark    per chunk: count of selected positions not in the bitmap;
-//                   chunk 0 also lists the freed slots in slot order; the last
-//                   CTA of a head turns the counts into offsets
+//   refresh_bits    bitmap of the previous slots' positions (before the
+//                   selection's histogram)
+//   select_collect  (with the bitmap) also counts per chunk the selected
+//                   positions not in the bitmap; the last CTA of a head lists
+//                   the freed slots in slot order and turns the counts into
+//                   offsets
 //   refresh_patch   per chunk: rank the new positions, write idx and copy
 //                   their K/V rows into their slots
-struct RefreshWs {
-  uint32_t* bits;      // [heads][W32]
-  uint32_t* ticket;    // [heads]
-  int32_t* n_freed;    // [heads]
-  int32_t* cnt;        // [heads][n_chunks]
-  int32_t* off;        // [heads][n_chunks + 1]
-  int32_t* freed;      // [heads][N_cap]
-  int64_t w32;         // bitmap words per head
-  size_t zero_bytes;   // bits + tickets, zeroed per call
-};
-
-__host__ __device__ inline RefreshWs carve_refresh(void* base, int HH, int64_t L, int64_t n_chunks,
-                                                   int64_t N_cap) {
-  RefreshWs r;
-  char* p = static_cast<char*>(base);
-  size_t o = 0;
-  r.w32 = (L + 31) / 32 > 0 ? (L + 31) / 32 : 1;
-  r.bits = reinterpret_cast<uint32_t*>(p + o);
-  o += a256((size_t)HH * r.w32 * sizeof(uint32_t));
-  r.ticket = reinterpret_cast<uint32_t*>(p + o);
-  o += a256((size_t)HH * sizeof(uint32_t));
-  r.zero_bytes = o;
-  r.n_freed = reinterpret_cast<int32_t*>(p + o);
-  o += a256((size_t)HH * sizeof(int32_t));
-  r.cnt = reinterpret_cast<int32_t*>(p + o);
-  o += a256((size_t)HH * n_chunks * sizeof(int32_t));
-  r.off = reinterpret_cast<int32_t*>(p + o);
-  o += a256((size_t)HH * (n_chunks + 1) * sizeof(int32_t));
-  r.freed = reinterpret_cast<int32_t*>(p + o);
-  return r;
-}
-
-__host__ inline size_t refresh_area_bytes(int HH, int64_t L, int64_t n_chunks, int64_t N_cap) {
-  const int64_t w32 = (L + 31) / 32 > 0 ? (L + 31) / 32 : 1;
-  return a256((size_t)HH * w32 * sizeof(uint32_t)) + a256((size_t)HH * sizeof(uint32_t)) +
-         a256((size_t)HH * sizeof(int32_t)) + a256((size_t)HH * n_chunks * sizeof(int32_t)) +
-         a256((size_t)HH * (n_chunks + 1) * sizeof(int32_t)) +
-         a256((size_t)HH * (N_cap > 0 ? N_cap : 1) * sizeof(int32_t));
-}
-
-__device__ __forceinline__ bool bit_of(const uint32_t* bits, int64_t j) {
-  return (bits[j >> 5] >> (j & 31)) & 1u;
-}
-
 __global__ void __launch_bounds__(kThreads)
 refresh_bits(Layers P, int64_t L, int64_t N_prev, int64_t N_cap, RefreshWs r, int32_t* status) {
   const int kv = blockIdx.y, layer = blockIdx.z, hh = layer * gridDim.y + kv;
@@ -598,61 +699,6 @@ refresh_bits(Layers P, int64_t L, int64_t N_prev, int64_t N_cap, RefreshWs r, in
       atomicOr(bits + (p >> 5), 1u << (p & 31));
     else
       set_status(status, TS_ERR_INVALID_ARG);
-  }
-}
-
-__global__ void __launch_bounds__(kThreads)
-refresh_mark(Layers P, int64_t L, int S, int R, int64_t N_prev, int64_t N_new, int64_t N_cap,
-             int64_t n_chunks, Ws w, RefreshWs r, int32_t* status) {
-  const int64_t c = blockIdx.x;
-  const int kv = blockIdx.y, tid = threadIdx.x, layer = blockIdx.z;
-  const int hh = layer * gridDim.y + kv;
-  const float* imp_h = imp_of(P, layer) + (size_t)kv * L;
-  const int32_t* idx = (P.idx ? P.idx[layer] : P.idx1) + (size_t)kv * N_cap;
-  const uint32_t* bits = r.bits + (size_t)hh * r.w32;
-  const SelectState st = w.state[hh];
-  __shared__ int warp_buf[32];
-  __shared__ int s_total, s_flag;
-  constexpr int PER = kChunk / kThreads;
-  const int64_t a = c * kChunk + tid * PER;
-  int cnt = 0;
-#pragma unroll
-  for (int x = 0; x < PER; ++x) {
-    const int64_t j = a + x;
-    if (j < L && keep_pos(imp_h, j, L, S, R, st) && !bit_of(bits, j)) ++cnt;
-  }
-  block_excl_scan(cnt, warp_buf, &s_total);
-  if (tid == 0) r.cnt[(size_t)hh * n_chunks + c] = s_total;
-  if (c == 0) {
-    // freed slots: their position is no longer selected (or was invalid)
-    int base = 0;
-    for (int64_t s0 = 0; s0 < N_prev; s0 += kThreads) {
-      const int64_t sl = s0 + tid;
-      int f = 0;
-      if (sl < N_prev) {
-        const int32_t p = idx[sl];
-        f = !(p >= 0 && p < L && keep_pos(imp_h, p, L, S, R, st));
-      }
-      const int pos = block_excl_scan(f, warp_buf, &s_total);
-      if (f) r.freed[(size_t)hh * N_cap + base + pos] = (int32_t)sl;
-      base += s_total;
-    }
-    if (tid == 0) r.n_freed[hh] = base;
-  }
-  if (last_of_head(&r.ticket[hh], (uint32_t)n_chunks, &s_flag)) {
-    int run = 0;
-    for (int64_t c0 = 0; c0 < n_chunks; c0 += kThreads) {
-      const int64_t cc = c0 + tid;
-      const int v = cc < n_chunks ? __ldcg(r.cnt + (size_t)hh * n_chunks + cc) : 0;
-      const int pos = block_excl_scan(v, warp_buf, &s_total);
-      if (cc < n_chunks) r.off[(size_t)hh * (n_chunks + 1) + cc] = run + pos;
-      run += s_total;
-    }
-    if (tid == 0) {
-      r.off[(size_t)hh * (n_chunks + 1) + n_chunks] = run;
-      if ((int64_t)run != (int64_t)__ldcg(r.n_freed + hh) + (N_new - N_prev))
-        set_status(status, TS_ERR_INVALID_ARG);   // duplicate or invalid previous slots
-    }
   }
 }
 
@@ -746,7 +792,9 @@ static int run_select(const Layers& P, int n_layers, int64_t L, int64_t L_cap, i
   select_hist<<<sgrid, kThreads, 0, st>>>(P, L, B, S, R, p.n_chunks, w);
   int rc = launch_status("select_hist");
   if (rc) return rc;
-  select_collect<<<sgrid, kThreads, 0, st>>>(P, L, S, R, p.n_chunks, w);
+  RefreshWs no_refresh{};   // bits = null: selection only
+  select_collect<<<sgrid, kThreads, 0, st>>>(P, L, S, R, p.n_chunks, w, no_refresh, 0, 0, 0,
+                                            nullptr);
   rc = launch_status("select_collect");
   if (rc) return rc;
   if (d == 128)
@@ -859,12 +907,9 @@ int launch_refresh_incremental(int n_layers, const float* imp1, const float* con
   select_hist<<<sgrid, kThreads, 0, st>>>(P, L, B, S, R, p.n_chunks, w);
   int rc = launch_status("select_hist");
   if (rc) return rc;
-  select_collect<<<sgrid, kThreads, 0, st>>>(P, L, S, R, p.n_chunks, w);
+  select_collect<<<sgrid, kThreads, 0, st>>>(P, L, S, R, p.n_chunks, w, r, N_prev, N_new, N_cap,
+                                            status);
   rc = launch_status("select_collect");
-  if (rc) return rc;
-  refresh_mark<<<grid, kThreads, 0, st>>>(P, L, S, R, N_prev, N_new, N_cap, p.n_chunks, w, r,
-                                          status);
-  rc = launch_status("refresh_mark");
   if (rc) return rc;
   if (d == 128)
     refresh_patch<128><<<grid, kThreads, 0, st>>>(P, L, L_cap, S, R, N_prev, N_new, N_cap,
