@@ -115,30 +115,24 @@ __host__ __device__ __forceinline__ size_t part_o8_index(int kv, int s, int n_sp
 }
 
 // The cache [0, L) (plus the T tree rows, in the last split) is cut into
-// key splits for the pair-tile row groups (cut a) and for the last, short
-// row group's two-stream CTAs (cut b).  The plan uses one cut for both
-// (n_a = n_b), so that every key tile is read by all row groups at about the
-// same time and leaves HBM once; the kernels and the merge take the two
-// separately.  Partials of split s of either cut sit at split index s,
-// n_max = max(n_a, n_b) apart per KV head.
-struct Splits {
-  int n_a, n_b, n_max;
-  int64_t kps_a, kps_b;   // keys per split (multiples of 128)
-};
+// n_split key splits, the same cut for every row group of a KV head, so that
+// every key tile is read by all row groups at about the same time and leaves
+// HBM once.
 struct VerifyPlan {
   int M;               // packed query rows per KV head (T * G)
   int n_pt;            // row groups of up to 256 rows (pair-tile CTAs, one per split)
   int n_two;           // a last group of <= 128 rows (two-stream CTAs, one per two splits)
-  Splits sp;
+  int n_split;         // KV splits per head
+  int64_t keys_per_split;   // a multiple of 128
   size_t part_o_bytes, part_ml_bytes, ws_bytes;
 };
 VerifyPlan verify_plan(int T, int Hq, int Hkv, int d, int64_t L);
 int tc_splits(int Hkv, int n_rg, int64_t L, int nsm);
-void verify_splits(int Hkv, int n_pt, int n_two, int64_t L, int nsm, int* n_a, int* n_b);
+int verify_splits(int Hkv, int n_pt, int n_two, int64_t L, int nsm);
 int launch_verify_tc(const void* q, const void* k, const void* v, int64_t L, int64_t L_cap,
                      const int32_t* parents, int T, int Hq, int Hkv, int d, int n_imp,
-                     const Splits& sp, int n_pt, int n_two, uint4* part_o, float* part_ml,
-                     float* imp, int32_t* status, cudaStream_t st);
+                     int64_t keys_per_split, int n_split, int n_pt, int n_two, uint4* part_o,
+                     float* part_ml, float* imp, int32_t* status, cudaStream_t st);
 
 // Limit (SM clock cycles) of one bounded device wait in the kernels with
 // cross-warp waits; ts_set_wait_limit sets it for later launches.

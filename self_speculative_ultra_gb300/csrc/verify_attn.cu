@@ -7,11 +7,10 @@
 //
 // Work decomposition: for KV head kv the M = T*G query rows of its group are
 // packed (row r = node r / G, head kv*G + r % G) and the committed cache
-// [0, L) is cut into key ranges (one cut for the pair-tile row groups, one
-// for the last short row group); the last range also takes the T tree rows
-// under the ancestor mask.  Every (row, split) gets one unnormalised partial
-// (O, m, l) in the log2 domain; the merge kernel below combines the splits
-// of every row.
+// [0, L) is cut into n_split key ranges, the same cut for every row group;
+// the last range also takes the T tree rows under the ancestor mask.  Every
+// (row, split) gets one partial (O / l in fp16, m and l in the log2 domain);
+// the merge kernel below combines the splits of every row.
 #include "ts_common.cuh"
 
 namespace ts {
@@ -38,8 +37,7 @@ constexpr int kMergeCtasPerSm = 4;   // at <= 64 registers
 template <int NG>
 __global__ void __launch_bounds__(kMergeThreads, kMergeCtasPerSm)
 verify_merge(const uint4* __restrict__ part_o, const float* __restrict__ part_ml, int T, int Hq,
-             int Hkv, int D, int rows_a, int n_a, int n_b, int n_max, float* __restrict__ o,
-             float* __restrict__ lse) {
+             int Hkv, int D, int n_split, float* __restrict__ o, float* __restrict__ lse) {
   constexpr int kRows = 32 / NG;      // rows per warp
   griddep_wait();
   griddep_launch_dependents();
@@ -51,13 +49,11 @@ verify_merge(const uint4* __restrict__ part_o, const float* __restrict__ part_ml
   const int R = blockIdx.x * kRows + r;
   const bool live = R < M && c8 < D / 8;
   const int Rc = live ? R : 0, cc = live ? c8 : 0;
-  // rows below rows_a belong to the pair-tile row groups (covering a); a
-  // warp's rows never straddle rows_a (a multiple of 256).  A thread with no
-  // row folds no split.
-  const int n_split = live ? (R < rows_a ? n_a : n_b) : 0;
-  const uint4* src = part_o + part_o8_index(kv, 0, n_max, cc, D, M, Rc);
+  // a thread with no row folds no split
+  const int n_fold = live ? n_split : 0;
+  const uint4* src = part_o + part_o8_index(kv, 0, n_split, cc, D, M, Rc);
   const size_t step = (size_t)(D / 8) * M;              // uint4s between splits
-  const float2* ml = reinterpret_cast<const float2*>(part_ml) + (size_t)kv * n_max * M + Rc;
+  const float2* ml = reinterpret_cast<const float2*>(part_ml) + (size_t)kv * n_split * M + Rc;
   float mrun = -INFINITY, lrun = 0.f;
   float acc[8];
 #pragma unroll
@@ -67,13 +63,13 @@ verify_merge(const uint4* __restrict__ part_o, const float* __restrict__ part_ml
     a = f.x;
     b = f.y;
   };
-  for (int s0 = j; s0 < n_split; s0 += NG * kPer) {
+  for (int s0 = j; s0 < n_fold; s0 += NG * kPer) {
     uint4 ov[kPer];
     float2 mv[kPer];
 #pragma unroll
     for (int k = 0; k < kPer; ++k) {
       const int s = s0 + k * NG;
-      if (s < n_split) {
+      if (s < n_fold) {
         ov[k] = __ldg(&src[(size_t)s * step]);
         mv[k] = __ldg(&ml[(size_t)s * M]);
       } else {
@@ -157,13 +153,9 @@ VerifyPlan verify_plan(int T, int Hq, int Hkv, int d, int64_t L) {
     rows -= 256;
   }
   p.n_two = rows > 0 ? 1 : 0;
-  int na = 1, nb = 1;
-  verify_splits(Hkv, p.n_pt, p.n_two, L, kGb300Sms, &na, &nb);
-  cut(L, na, p.sp.n_a, p.sp.kps_a);
-  cut(L, nb, p.sp.n_b, p.sp.kps_b);
-  p.sp.n_max = p.sp.n_a > p.sp.n_b ? p.sp.n_a : p.sp.n_b;
-  p.part_o_bytes = align_up((size_t)Hkv * p.sp.n_max * p.M * d * sizeof(__half), 256);
-  p.part_ml_bytes = align_up((size_t)Hkv * p.sp.n_max * p.M * 2 * sizeof(float), 256);
+  cut(L, verify_splits(Hkv, p.n_pt, p.n_two, L, kGb300Sms), p.n_split, p.keys_per_split);
+  p.part_o_bytes = align_up((size_t)Hkv * p.n_split * p.M * d * sizeof(__half), 256);
+  p.part_ml_bytes = align_up((size_t)Hkv * p.n_split * p.M * 2 * sizeof(float), 256);
   p.ws_bytes = p.part_o_bytes + p.part_ml_bytes;
   return p;
 }
@@ -174,8 +166,8 @@ int launch_verify(const void* q, const void* k, const void* v, int64_t L, int64_
   VerifyPlan p = verify_plan(T, Hq, Hkv, d, L);
   uint4* part_o = static_cast<uint4*>(ws);
   float* part_ml = reinterpret_cast<float*>(static_cast<char*>(ws) + p.part_o_bytes);
-  int rc = launch_verify_tc(q, k, v, L, L_cap, parents, T, Hq, Hkv, d, n_imp, p.sp, p.n_pt,
-                            p.n_two, part_o, part_ml, imp, status, st);
+  int rc = launch_verify_tc(q, k, v, L, L_cap, parents, T, Hq, Hkv, d, n_imp, p.keys_per_split,
+                            p.n_split, p.n_pt, p.n_two, part_o, part_ml, imp, status, st);
   if (rc) return rc;
   const int ny = (d / 8 + 7) / 8;
   auto ctas = [&](int ng) { return (p.M + 32 / ng - 1) / (32 / ng) * ny * Hkv; };
@@ -187,17 +179,12 @@ int launch_verify(const void* q, const void* k, const void* v, int64_t L, int64_
   pdl_config(&cfg, attr, mgrid, dim3(kMergeThreads), 0, st);
   auto po = static_cast<const uint4*>(part_o);
   auto pm = static_cast<const float*>(part_ml);
-  const int rows_a = 256 * p.n_pt;
-  const Splits& sp = p.sp;
   if (ng == 4)
-    cudaLaunchKernelEx(&cfg, verify_merge<4>, po, pm, T, Hq, Hkv, d, rows_a, sp.n_a, sp.n_b,
-                       sp.n_max, o, lse);
+    cudaLaunchKernelEx(&cfg, verify_merge<4>, po, pm, T, Hq, Hkv, d, p.n_split, o, lse);
   else if (ng == 2)
-    cudaLaunchKernelEx(&cfg, verify_merge<2>, po, pm, T, Hq, Hkv, d, rows_a, sp.n_a, sp.n_b,
-                       sp.n_max, o, lse);
+    cudaLaunchKernelEx(&cfg, verify_merge<2>, po, pm, T, Hq, Hkv, d, p.n_split, o, lse);
   else
-    cudaLaunchKernelEx(&cfg, verify_merge<1>, po, pm, T, Hq, Hkv, d, rows_a, sp.n_a, sp.n_b,
-                       sp.n_max, o, lse);
+    cudaLaunchKernelEx(&cfg, verify_merge<1>, po, pm, T, Hq, Hkv, d, p.n_split, o, lse);
   return launch_status("verify_merge");
 }
 

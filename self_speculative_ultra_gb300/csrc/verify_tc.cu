@@ -182,8 +182,8 @@ template <int D>
 __global__ void __launch_bounds__(kThreadsTc, 1)
 verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v,
                  const __nv_bfloat16* __restrict__ q, const int32_t* __restrict__ parents, int T,
-                 int Hq, int Hkv, int n_imp, int64_t L, int64_t L_cap, Splits sp,
-                 int n_pairtile_groups, long long wait_limit,
+                 int Hq, int Hkv, int n_imp, int64_t L, int64_t L_cap, int64_t keys_per_split,
+                 int n_split, int n_pairtile_groups, long long wait_limit,
                  uint4* __restrict__ part_o, float* __restrict__ part_ml, float* __restrict__ imp,
                  int32_t* status) {
   using Ly = TcLayout<D>;
@@ -205,21 +205,21 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
   // ---------------------------------------------------------------- which work
   const int kv = blockIdx.y, x = blockIdx.x;
   const int G = Hq / Hkv, M = T * G;
-  const int n_pt = n_pairtile_groups * sp.n_a;      // pair-tile CTAs per head
+  const int n_pt = n_pairtile_groups * n_split;     // pair-tile CTAs per head
   Seq seq;
   seq.two = x >= n_pt;
   int r0;
   Stream st0, st1;
   if (!seq.two) {
-    const int rg = x / sp.n_a, split = x % sp.n_a;
+    const int rg = x / n_split, split = x % n_split;
     r0 = rg * 256;
-    st0 = make_stream(split, sp.n_a, sp.kps_a, L, T);
+    st0 = make_stream(split, n_split, keys_per_split, L, T);
     st1 = st0;
   } else {
     const int pair = x - n_pt;
     r0 = n_pairtile_groups * 256;
-    st0 = make_stream(2 * pair, sp.n_b, sp.kps_b, L, T);
-    st1 = make_stream(2 * pair + 1, sp.n_b, sp.kps_b, L, T);
+    st0 = make_stream(2 * pair, n_split, keys_per_split, L, T);
+    st1 = make_stream(2 * pair + 1, n_split, keys_per_split, L, T);
   }
   seq.n0 = st0.n;
   seq.n1 = seq.two ? st1.n : 0;
@@ -850,11 +850,11 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
         timeout(aux, status);
       } else if (warp_rows) {
         ptx::tc_fence_after();
-        const int split = (int)(my.j0 / (seq.two ? sp.kps_b : sp.kps_a));
+        const int split = (int)(my.j0 / keys_per_split);
         // the partial row normalised (O / l: a convex combination of V rows,
         // so |O / l| <= max |v| < 65504) in fp16, column-octet major: for
         // each 8-column octet the warp's 32 rows are 512 contiguous bytes
-        uint4* dst = part_o + part_o8_index(kv, split, sp.n_max, 0, D, M, sm_valid ? sm_R : 0);
+        uint4* dst = part_o + part_o8_index(kv, split, n_split, 0, D, M, sm_valid ? sm_R : 0);
         const size_t c8_stride = (size_t)M;
         const float inv = l > 0.f ? 1.f / l : 0.f;
 #pragma unroll 1
@@ -873,7 +873,7 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
           }
         }
         if (sm_valid) {
-          const size_t base = ((size_t)kv * sp.n_max + split) * M + sm_R;
+          const size_t base = ((size_t)kv * n_split + split) * M + sm_R;
           part_ml[base * 2] = m_used;
           part_ml[base * 2 + 1] = l;
         }
@@ -929,24 +929,22 @@ int make_kv_map(CUtensorMap* map, const void* base, int Hkv, int64_t L_cap, int 
 // Key splits per (KV head, row group): the count minimising waves x tiles per
 // CTA (+ a fixed per-CTA cost), so the grid fills whole waves of the SMs.
 int tc_splits(int Hkv, int n_rg, int64_t L, int nsm) {
-  int na = 1, nb = 1;
-  verify_splits(Hkv, n_rg, 0, L, nsm, &na, &nb);
-  return na;
+  return verify_splits(Hkv, n_rg, 0, L, nsm);
 }
 
 // The same for the verification grid.  n_pt pair-tile row groups take one
 // CTA per split; the two-stream row group takes one CTA per two consecutive
-// splits of the same cut (n_b = n_a), so its CTAs read every key tile at
-// about the time a pair-tile CTA reads it and the second read is an L2 hit:
-// K and V leave HBM once.  (Separate cuts balanced for time were measured at
-// 1.8 x the K/V bytes from HBM on the 14B shape.)  Time of a CTA in
+// splits of the same cut, so its CTAs read every key tile at about the time
+// a pair-tile CTA reads it and the second read is an L2 hit: K and V leave
+// HBM once.  (Separate cuts balanced for time were measured at 1.8 x the K/V
+// bytes from HBM on the 14B shape.)  Time of a CTA in
 // pair-tile tile steps: a pair-tile CTA ~ its tiles + kFixedTiles; a
 // two-stream CTA ~ 2 * kTwoStep * its tiles per split + kFixedTiles, a
 // two-stream step (one query tile, one key tile) costing kTwoStep of a
 // pair-tile step (two query tiles).
 int64_t split_tiles(int64_t L, int n) { return ((L + n - 1) / n + kNk - 1) / kNk; }
 
-void verify_splits(int Hkv, int n_pt, int n_two, int64_t L, int nsm, int* n_a, int* n_b) {
+int verify_splits(int Hkv, int n_pt, int n_two, int64_t L, int nsm) {
   constexpr double kTwoStep = 0.55;
   constexpr double kFixedTiles = 3.0;
   int64_t max_split = (L + kNk - 1) / kNk;
@@ -966,8 +964,7 @@ void verify_splits(int Hkv, int n_pt, int n_two, int64_t L, int nsm, int* n_a, i
       best = n;
     }
   }
-  *n_a = best;
-  *n_b = best;
+  return best;
 }
 
 size_t verify_tc_smem_bytes(int d) {
@@ -976,14 +973,14 @@ size_t verify_tc_smem_bytes(int d) {
 
 int launch_verify_tc(const void* q, const void* k, const void* v, int64_t L, int64_t L_cap,
                      const int32_t* parents, int T, int Hq, int Hkv, int d, int n_imp,
-                     const Splits& sp, int n_pt, int n_two, uint4* part_o,
+                     int64_t keys_per_split, int n_split, int n_pt, int n_two, uint4* part_o,
                      float* part_ml, float* imp, int32_t* status, cudaStream_t st) {
   CUtensorMap mk, mv;
   int rc = make_kv_map(&mk, k, Hkv, L_cap, d);
   if (rc) return rc;
   rc = make_kv_map(&mv, v, Hkv, L_cap, d);
   if (rc) return rc;
-  const int per_head = n_pt * sp.n_a + n_two * ((sp.n_b + 1) / 2);
+  const int per_head = n_pt * n_split + n_two * ((n_split + 1) / 2);
   dim3 grid(per_head, Hkv);
   auto qb = static_cast<const __nv_bfloat16*>(q);
   const long long limit = wait_limit_cycles();
@@ -1002,7 +999,7 @@ int launch_verify_tc(const void* q, const void* k, const void* v, int64_t L, int
     cudaLaunchAttribute attr[1];
     pdl_config(&cfg, attr, grid, dim3(kThreadsTc), smem, st);
     cudaLaunchKernelEx(&cfg, kern, mk, mv, qb, parents, T, Hq, Hkv, n_imp, L, L_cap,
-                       sp, n_pt, limit, part_o, part_ml, imp, status);
+                       keys_per_split, n_split, n_pt, limit, part_o, part_ml, imp, status);
   };
   if (d == 128)
     go(verify_tc_kernel<128>, TcLayout<128>::kBytes);
