@@ -116,11 +116,36 @@ def load_tensor_peak():
     return 1700.0, "fallback (sustained)"
 
 
+def code_of(src: str) -> str:
+    """C++/CUDA source without comments and with whitespace runs collapsed:
+    what the compiler sees, so that a comment edit keeps the hash."""
+    out, i, n = [], 0, len(src)
+    while i < n:
+        if src.startswith("//", i):
+            j = src.find("\n", i)
+            i = n if j < 0 else j
+        elif src.startswith("/*", i):
+            j = src.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+            out.append(" ")
+        elif src[i] == '"':
+            j = i + 1
+            while j < n and src[j] != '"':
+                j += 2 if src[j] == "\\" else 1
+            out.append(src[i:j + 1])
+            i = j + 1
+        else:
+            out.append(src[i])
+            i += 1
+    return " ".join("".join(out).split())
+
+
 def verify_source_sha1() -> str:
+    """Hash of the verification kernels' code (comments and layout ignored)."""
     h = hashlib.sha1()
     for name in ("verify_tc.cu", "tc_ptx.cuh", "verify_attn.cu", "ts_common.cuh"):
-        with open(os.path.join(ROOT, "self_speculative_ultra_gb300", "csrc", name), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(ROOT, "self_speculative_ultra_gb300", "csrc", name)) as f:
+            h.update(code_of(f.read()).encode())
     return h.hexdigest()[:12]
 
 

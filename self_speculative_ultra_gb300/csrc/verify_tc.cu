@@ -49,8 +49,8 @@
 //                        P is recomputed.  Tree mask and split limits (as bit
 //                        masks over 64 keys) only touch the tiles that need
 //                        them.
-// Each stream writes an unnormalised partial (O, m, l) per row in the log2
-// domain; the merge kernel of verify_attn.cu combines the splits.
+// Each stream writes its partial per row: O / l in fp16 and (m, l) in the
+// log2 domain; the merge kernel of verify_attn.cu combines the splits.
 //
 // Every mbarrier wait is bounded (a caller-settable limit, ~1 s of SM clocks
 // by default); on expiry the CTA records TS_ERR_TIMEOUT in the status word,
@@ -844,7 +844,7 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
         __syncwarp();
         if (lane == 0) ptx::mbar_arrive(&aux->p_ready[g]);
       }
-      // epilogue: final O row -> unnormalised partial
+      // epilogue: final O row -> the split's partial (O / l in fp16, m, l)
       bool fin = ok && !aux->abort_flag && ptx::mbar_wait(&aux->o_final, 0, wait_limit);
       if (!__all_sync(0xffffffffu, fin)) {
         timeout(aux, status);
