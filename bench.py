@@ -80,10 +80,21 @@ def step_bytes(w: syn.Workload) -> int:
     return w.layers * (verify_bytes(w) + select_bytes(w)) + sample_bytes(w) + commit_bytes(w)
 
 
+# Storage of the V caches: "fp16" (the precision of the P.V product; the
+# model's bf16 V rows are rounded once, when appended) or "bf16" (the kernel
+# converts every V tile it reads).  Same values either way.
+V_CACHE = "fp16"
+
+
+def v_cache_dtype():
+    import torch
+    return torch.float16 if V_CACHE == "fp16" else torch.bfloat16
+
+
 def config_dict(w: syn.Workload, world: int = 1) -> dict:
     """The workload's description, shared by the GPU arm and the oracle arm."""
     sb = step_bytes(w)
-    return {"workload": w.name, "layers": w.layers, "Hq": w.Hq, "Hkv": w.Hkv,
+    return {"workload": w.name, "layers": w.layers, "Hq": w.Hq, "Hkv": w.Hkv, "v_cache": V_CACHE,
             "d": w.d, "L": w.L, "tree_nodes": w.T, "budget_B": w.B, "sinks": w.S,
             "recent": w.R, "vocab": w.V, "penalty_window": w.W,
             "bytes_per_step": sb,
@@ -256,7 +267,7 @@ class Step:
             k.scatter_(1, pos[..., None].expand(-1, -1, d), kk)
             self.q.append(q.to(torch.bfloat16))
             self.k.append(k.to(torch.bfloat16))
-            self.v.append(v.to(torch.bfloat16))
+            self.v.append(v.to(torch.bfloat16).to(v_cache_dtype()))
             del q, k, v
         N = w.N
         self.imp = [torch.empty((Hkv, L), dtype=torch.float32, device=dev) for _ in range(w.layers)]
@@ -264,7 +275,7 @@ class Step:
         self.lse = [torch.empty((T, Hq), dtype=torch.float32, device=dev) for _ in range(w.layers)]
         self.idx = [torch.empty((Hkv, N), dtype=torch.int32, device=dev) for _ in range(w.layers)]
         self.kd = [torch.empty((Hkv, N, d), dtype=torch.bfloat16, device=dev) for _ in range(w.layers)]
-        self.vd = [torch.empty((Hkv, N, d), dtype=torch.bfloat16, device=dev) for _ in range(w.layers)]
+        self.vd = [torch.empty((Hkv, N, d), dtype=v_cache_dtype(), device=dev) for _ in range(w.layers)]
         sin = syn.sampling_inputs(w, step=0, tree=tree)
         self.logits = torch.from_numpy(sin["logits"]).to(dev)
         self.prior = torch.from_numpy(sin["prior"]).to(dev)
@@ -353,7 +364,7 @@ class Step:
         self.torch.cuda.current_stream().wait_event(self.staged[b])
         v = self.stage_views[b]
         self.ts.ts_kv_append_batched(self.k, self.v, v["k_rows"], v["v_rows"], self.L,
-                                     table=self.commit_table)
+                                     table=self.commit_table, status=self.status)
         return v
 
     def release_inputs(self, s: int):
@@ -833,7 +844,8 @@ def run_profile_case(kind: str, w: syn.Workload):
         torch.cuda.synchronize()
         print(json.dumps({"profile_case": kind, "workload": w.name, "layers": nl}))
         return
-    vs = [torch.randn((Hkv, L + T, d), generator=g, device=dev).to(torch.bfloat16) for _ in range(nl)]
+    vs = [torch.randn((Hkv, L + T, d), generator=g, device=dev).to(torch.bfloat16).to(v_cache_dtype())
+          for _ in range(nl)]
     tree = syn.make_tree(w, np.random.default_rng(0))
     parents = torch.from_numpy(tree[0]).to(dev)
     if kind == "commit":
@@ -858,7 +870,7 @@ def run_profile_case(kind: str, w: syn.Workload):
         N = w.N
         idx = [torch.empty((Hkv, N), dtype=torch.int32, device=dev) for _ in range(nl)]
         kd = [torch.empty((Hkv, N, d), dtype=torch.bfloat16, device=dev) for _ in range(nl)]
-        vd = [torch.empty((Hkv, N, d), dtype=torch.bfloat16, device=dev) for _ in range(nl)]
+        vd = [torch.empty((Hkv, N, d), dtype=v_cache_dtype(), device=dev) for _ in range(nl)]
         sin = syn.sampling_inputs(w, tree=tree)
         logits = torch.from_numpy(sin["logits"]).to(dev)
         toks = torch.from_numpy(sin["tokens"]).to(dev)
@@ -887,7 +899,8 @@ def run_draft_case(w: syn.Workload, steps: int, warmup: int):
     N = min(w.L, w.S + w.B + w.R)
     layers = w.layers
     ks = [torch.randn((Hkv, N + T_d, d), generator=g, device=dev).to(torch.bfloat16) for _ in range(layers)]
-    vs = [torch.randn((Hkv, N + T_d, d), generator=g, device=dev).to(torch.bfloat16) for _ in range(layers)]
+    vs = [torch.randn((Hkv, N + T_d, d), generator=g, device=dev).to(torch.bfloat16).to(v_cache_dtype())
+          for _ in range(layers)]
     q = torch.randn((T_d, Hq, d), generator=g, device=dev).to(torch.bfloat16)
     par = torch.tensor([-1] + list(range(T_d - 1)), dtype=torch.int32, device=dev)
     ws = torch.empty(ts.ts_verify_workspace_bytes(T_d, Hq, Hkv, d, N), dtype=torch.uint8, device=dev)
@@ -988,14 +1001,14 @@ def run_refresh_case(w: syn.Workload, steps: int, warmup: int, drift: float = 0.
     ks = [torch.empty((Hkv, L_cap, d), dtype=torch.bfloat16, device=dev).normal_(generator=g)
           for _ in range(nl)]
     vs = [torch.empty((Hkv, L_cap, d), dtype=torch.bfloat16, device=dev).normal_(generator=g)
-          for _ in range(nl)]
+          .to(v_cache_dtype()) for _ in range(nl)]
     base = [torch.randn((Hkv, w.L), generator=g, device=dev) * 4.0 for _ in range(nl)]
     imp_buf = [torch.empty(Hkv * w.L, device=dev) for _ in range(nl)]
     mk = lambda shape, dt: [torch.empty(shape, dtype=dt, device=dev) for _ in range(nl)]  # noqa: E731
     f_idx, f_kd, f_vd = mk((Hkv, N_cap), torch.int32), mk((Hkv, N_cap, d), torch.bfloat16), \
-        mk((Hkv, N_cap, d), torch.bfloat16)
+        mk((Hkv, N_cap, d), v_cache_dtype())
     i_idx, i_kd, i_vd = mk((Hkv, N_cap), torch.int32), mk((Hkv, N_cap, d), torch.bfloat16), \
-        mk((Hkv, N_cap, d), torch.bfloat16)
+        mk((Hkv, N_cap, d), v_cache_dtype())
     ws_f = torch.empty(ts.ts_select_batched_workspace_bytes(nl, Hkv, w.L), dtype=torch.uint8,
                        device=dev)
     ws_i = torch.empty(ts.ts_refresh_workspace_bytes(nl, Hkv, w.L, N_cap), dtype=torch.uint8,
@@ -1155,7 +1168,8 @@ def run_loop_case(w: syn.Workload, until: int, L0: int = 2048):
     bf = dict(dtype=torch.bfloat16, device=dev)
     i32 = dict(dtype=torch.int32, device=dev)
     ks = [torch.empty((Hkv, L_cap, d), **bf).normal_(generator=g) for _ in range(nl)]
-    vs = [torch.empty((Hkv, L_cap, d), **bf).normal_(generator=g) for _ in range(nl)]
+    vs = [torch.empty((Hkv, L_cap, d), **bf).normal_(generator=g).to(v_cache_dtype())
+          for _ in range(nl)]
     qs = [torch.empty((T, Hq, d), **bf).normal_(generator=g) for _ in range(nl)]
     # fresh N(0,1) tree K/V rows every step, drawn on the device and written
     # into every layer's cache by one batched append
@@ -1181,7 +1195,8 @@ def run_loop_case(w: syn.Workload, until: int, L0: int = 2048):
     N = w.S + w.B + w.R
     idx = [torch.empty((Hkv, N), **i32) for _ in range(nl)]
     kd = [torch.empty((Hkv, N, d), **bf) for _ in range(nl)]
-    vd = [torch.empty((Hkv, N, d), **bf) for _ in range(nl)]
+    vd = [torch.empty((Hkv, N, d), dtype=v_cache_dtype(), device=dev) for _ in range(nl)]
+    vflag = 1 if V_CACHE == "fp16" else 0     # TS_VERIFY_V_FP16 / TS_KV_V_FP16
     u8 = dict(dtype=torch.uint8, device=dev)
     ws_v = torch.empty(max(ts.ts_verify_workspace_bytes(T, Hq, Hkv, d, Lx)
                            for Lx in range(L0, until + 256, 256)), **u8)
@@ -1208,17 +1223,18 @@ def run_loop_case(w: syn.Workload, until: int, L0: int = 2048):
         t_s = time.perf_counter()
         torch.randn(tree_kv_f32.shape, generator=g, device=dev, out=tree_kv_f32)
         tree_kv.copy_(tree_kv_f32)
-        ts._check(lib.ts_kv_append_batched(nl, crow[0], crow[1], P(tree_kv[0]), P(tree_kv[1]), L, L_cap,
-                                           Hkv, d, T, stream))
+        ts._check(lib.ts_kv_append_batched_flags(nl, crow[0], crow[1], P(tree_kv[0]),
+                                                 P(tree_kv[1]), L, L_cap, Hkv, d, T, vflag,
+                                                 P(status), stream))
         torch.randn((T, V), generator=g, device=dev, out=logits)
         logits.mul_(3.0)
         plant = (torch.rand(T, generator=g, device=dev) < 0.7) & has_fc
         logits.index_put_((rows, fc_tok), plant.float() * 30.0, accumulate=True)
         torch.rand(T, generator=g, device=dev, out=uniforms)
         for (q_, k_, v_, o_, lse_, imp_) in lay:
-            ts._check(lib.ts_verify_attention(q_, k_, v_, L, L_cap, P(parents), T, Hq, Hkv, d,
-                                              w.n_imp, o_, lse_, imp_, P(ws_v), nb_v, P(status),
-                                              stream))
+            ts._check(lib.ts_verify_attention_flags(q_, k_, v_, L, L_cap, P(parents), T, Hq, Hkv,
+                                                    d, w.n_imp, o_, lse_, imp_, P(ws_v), nb_v,
+                                                    vflag, P(status), stream))
         ts._check(lib.ts_partial_kv_select_gather_batched(
             nl, trow[0], trow[1], trow[2], L, L_cap, Hkv, d, w.B, w.S, w.R, trow[3], trow[4],
             trow[5], ctypes.byref(n_out), P(ws_s), nb_s, P(status), stream))
@@ -1295,7 +1311,12 @@ def main():
                     help="time the rejection-sampling acceptance and exit")
     ap.add_argument("--ngram", action="store_true",
                     help="time the token-reutilization step (4-gram table + tree) and exit")
+    ap.add_argument("--v-cache", default="fp16", choices=["fp16", "bf16"],
+                    help="storage of the V caches (same values; fp16 skips the per-tile "
+                         "conversion in the verification kernel)")
     args = ap.parse_args()
+    global V_CACHE
+    V_CACHE = args.v_cache
     w = syn.WORKLOADS[args.workload]
     if args.reject:
         run_reject_case(w, args.steps, args.warmup)

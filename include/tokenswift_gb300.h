@@ -12,6 +12,10 @@
  *   - Every tensor pointer is a DEVICE pointer owned by the caller, unless a
  *     parameter says "host".  Tensors are dense row-major in the layout given.
  *     bf16 tensors are passed as `const void*` holding IEEE bfloat16 values.
+ *   - A V cache may hold IEEE binary16 (fp16) values instead: the calls that
+ *     only move cache rows (gather, refresh, commit) copy bytes and take
+ *     either; (1) reads an fp16 V cache with TS_VERIFY_V_FP16 and
+ *     ts_kv_append_batched_flags writes one with TS_KV_V_FP16.
  *   - The library allocates no device memory.  Scratch space is a caller
  *     buffer (`workspace`, 256-byte aligned) of at least the size reported by
  *     the matching *_workspace_bytes() query.
@@ -104,6 +108,21 @@ int ts_verify_attention(const void* q, const void* k, const void* v,
                         float* o, float* lse, float* imp,
                         void* workspace, size_t workspace_bytes,
                         int32_t* status, void* stream);
+/* The same call with flags.  TS_VERIFY_V_FP16: v [Hkv, L_cap, d] holds fp16
+ * values (a V cache kept in the precision of the P.V product, as
+ * ts_kv_append_batched_flags with TS_KV_V_FP16 writes it).  The kernel then
+ * skips its per-tile bf16 -> fp16 conversion; for V values that fp16
+ * represents exactly (normal bf16 values below 65504 in magnitude, the
+ * conversion rounding the rest exactly as the bf16 path does) the outputs are
+ * bit-identical to the bf16 call on the same values.  Unknown flag bits:
+ * TS_ERR_INVALID_ARG. */
+#define TS_VERIFY_V_FP16 1
+int ts_verify_attention_flags(const void* q, const void* k, const void* v,
+                              int64_t L, int64_t L_cap, const int32_t* parents,
+                              int T, int Hq, int Hkv, int d, int n_imp,
+                              float* o, float* lse, float* imp,
+                              void* workspace, size_t workspace_bytes, int flags,
+                              int32_t* status, void* stream);
 
 /* ------------------------------------------------------------------------
  * (1b) Softmax-weighted importance (a variant of the importance of (1)).
@@ -390,6 +409,17 @@ int ts_kv_commit_batched(int n_layers, void* const* k, void* const* v, int64_t L
 int ts_kv_append_batched(int n_layers, void* const* k, void* const* v,
                          const void* k_rows, const void* v_rows, int64_t L,
                          int64_t L_cap, int Hkv, int d, int T, void* stream);
+/* The same with flags.  TS_KV_V_FP16: the V caches hold fp16; each bf16
+ * value of v_rows is rounded to the nearest fp16 on the way in (exact for
+ * normal values below 65504 in magnitude); larger magnitudes saturate to
+ * +-65504, NaN stays NaN, and either writes TS_ERR_UNSUPPORTED to `status`
+ * (may be NULL).  K rows are copied bit for bit.  Unknown flag bits:
+ * TS_ERR_INVALID_ARG. */
+#define TS_KV_V_FP16 1
+int ts_kv_append_batched_flags(int n_layers, void* const* k, void* const* v,
+                               const void* k_rows, const void* v_rows, int64_t L,
+                               int64_t L_cap, int Hkv, int d, int T, int flags,
+                               int32_t* status, void* stream);
 
 /* ------------------------------------------------------------------------
  * (5) Token reutilization: the 4-gram table and the draft-tree builder.

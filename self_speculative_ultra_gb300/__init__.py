@@ -29,6 +29,8 @@ __all__ = [
 ]
 
 TS_OK, TS_ERR_INVALID_ARG, TS_ERR_UNSUPPORTED, TS_ERR_CUDA, TS_ERR_TIMEOUT, TS_ERR_WORKSPACE = range(6)
+TS_VERIFY_V_FP16 = 1     # ts_verify_attention_flags: the V cache holds fp16
+TS_KV_V_FP16 = 1         # ts_kv_append_batched_flags: write V rows into fp16 caches
 
 _c_void_p, _i32, _i64, _sz, _f32 = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_size_t, ctypes.c_float
 
@@ -41,6 +43,9 @@ _SIGNATURES = {
     "ts_verify_attention": (_i32, [_c_void_p, _c_void_p, _c_void_p, _i64, _i64, _c_void_p,
                                    _i32, _i32, _i32, _i32, _i32, _c_void_p, _c_void_p, _c_void_p,
                                    _c_void_p, _sz, _c_void_p, _c_void_p]),
+    "ts_verify_attention_flags": (_i32, [_c_void_p, _c_void_p, _c_void_p, _i64, _i64, _c_void_p,
+                                         _i32, _i32, _i32, _i32, _i32, _c_void_p, _c_void_p,
+                                         _c_void_p, _c_void_p, _sz, _i32, _c_void_p, _c_void_p]),
     "ts_select_workspace_bytes": (_sz, [_i32, _i64]),
     "ts_importance_softmax": (_i32, [_c_void_p, _c_void_p, _c_void_p, _i64, _i64, _i32, _i32, _i32,
                                      _i32, _i32, _c_void_p, _c_void_p, _c_void_p]),
@@ -88,6 +93,8 @@ _SIGNATURES = {
                                     _c_void_p, _c_void_p, _c_void_p, _c_void_p]),
     "ts_kv_append_batched": (_i32, [_i32, _c_void_p, _c_void_p, _c_void_p, _c_void_p, _i64, _i64,
                                     _i32, _i32, _i32, _c_void_p]),
+    "ts_kv_append_batched_flags": (_i32, [_i32, _c_void_p, _c_void_p, _c_void_p, _c_void_p, _i64,
+                                          _i64, _i32, _i32, _i32, _i32, _c_void_p, _c_void_p]),
     "ts_reject_workspace_bytes": (_sz, [_i32]),
     "ts_rejection_sample_accept": (_i32, [_c_void_p, _c_void_p, _c_void_p, _c_void_p, _i32,
                                           _c_void_p, _i32, _i32, _i32, _f32, _f32, _f32, _f32,
@@ -152,10 +159,14 @@ def _ptr(t):
     return None if t is None else ctypes.c_void_p(t.data_ptr())
 
 
+# a V cache holds bf16 or fp16 values (fp16: the precision of the P.V product)
+_V_DTYPES = (torch.bfloat16, torch.float16)
+
+
 def _dev(t, dtype, name, shape=None):
     if not isinstance(t, torch.Tensor) or not t.is_cuda:
         raise TypeError(f"{name} must be a CUDA tensor")
-    if t.dtype != dtype:
+    if t.dtype not in (dtype if isinstance(dtype, tuple) else (dtype,)):
         raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
     if not t.is_contiguous():
         raise ValueError(f"{name} must be contiguous")
@@ -185,13 +196,14 @@ def ts_verify_workspace_bytes(T, Hq, Hkv, d, L) -> int:
 
 def ts_verify_attention(q, k, v, L, parents, n_imp=0, o=None, lse=None, imp=None,
                         want_lse=True, want_imp=True, workspace=None, status=None, stream=None):
-    """Tree verification attention + importance.  q [T,Hq,d] bf16, k/v
-    [Hkv,L_cap,d] bf16, parents [T] int32.  Returns (o, lse, imp)."""
+    """Tree verification attention + importance.  q [T,Hq,d] bf16, k
+    [Hkv,L_cap,d] bf16, v [Hkv,L_cap,d] bf16 or fp16 (an fp16 V cache skips the
+    kernel's per-tile conversion), parents [T] int32.  Returns (o, lse, imp)."""
     T, Hq, d = q.shape
     Hkv, L_cap = k.shape[0], k.shape[1]
     _dev(q, torch.bfloat16, "q")
     _dev(k, torch.bfloat16, "k", (Hkv, L_cap, d))
-    _dev(v, torch.bfloat16, "v", (Hkv, L_cap, d))
+    _dev(v, _V_DTYPES, "v", (Hkv, L_cap, d))
     _dev(parents, torch.int32, "parents", (T,))
     dev = q.device
     if o is None:
@@ -201,9 +213,10 @@ def ts_verify_attention(q, k, v, L, parents, n_imp=0, o=None, lse=None, imp=None
     if imp is None and want_imp:
         imp = torch.empty((Hkv, L), dtype=torch.float32, device=dev)
     ws, nb = _workspace(ts_verify_workspace_bytes(T, Hq, Hkv, d, L), dev, workspace)
-    rc = lib().ts_verify_attention(_ptr(q), _ptr(k), _ptr(v), L, L_cap, _ptr(parents), T, Hq, Hkv,
-                                   d, n_imp, _ptr(o), _ptr(lse), _ptr(imp), _ptr(ws), nb,
-                                   _ptr(status), _stream(stream))
+    flags = TS_VERIFY_V_FP16 if v.dtype == torch.float16 else 0
+    rc = lib().ts_verify_attention_flags(_ptr(q), _ptr(k), _ptr(v), L, L_cap, _ptr(parents), T, Hq,
+                                         Hkv, d, n_imp, _ptr(o), _ptr(lse), _ptr(imp), _ptr(ws), nb,
+                                         flags, _ptr(status), _stream(stream))
     _check(rc)
     return o, lse, imp
 
@@ -236,7 +249,7 @@ def ts_partial_kv_select_gather(imp, k, v, L, B, S, R, idx=None, kd=None, vd=Non
     Hkv, L_cap, d = k.shape
     _dev(imp, torch.float32, "imp", (Hkv, L))
     _dev(k, torch.bfloat16, "k")
-    _dev(v, torch.bfloat16, "v", (Hkv, L_cap, d))
+    _dev(v, _V_DTYPES, "v", (Hkv, L_cap, d))
     N = min(L, S + B + R)
     dev = k.device
     if idx is None:
@@ -244,7 +257,7 @@ def ts_partial_kv_select_gather(imp, k, v, L, B, S, R, idx=None, kd=None, vd=Non
     if kd is None:
         kd = torch.empty((Hkv, N, d), dtype=torch.bfloat16, device=dev)
     if vd is None:
-        vd = torch.empty((Hkv, N, d), dtype=torch.bfloat16, device=dev)
+        vd = torch.empty((Hkv, N, d), dtype=v.dtype, device=dev)
     ws, nb = _workspace(ts_select_workspace_bytes(Hkv, L), dev, workspace)
     n_out = _i64(0)
     rc = lib().ts_partial_kv_select_gather(_ptr(imp), _ptr(k), _ptr(v), L, L_cap, Hkv, d, B, S, R,
@@ -264,11 +277,11 @@ def ts_partial_kv_select_gather_noalloc(imp, k, v, L, B, S, R, idx, kd, vd, stat
     Hkv, L_cap, d = k.shape
     _dev(imp, torch.float32, "imp", (Hkv, L))
     _dev(k, torch.bfloat16, "k")
-    _dev(v, torch.bfloat16, "v", (Hkv, L_cap, d))
+    _dev(v, _V_DTYPES, "v", (Hkv, L_cap, d))
     N = min(L, S + B + R)
     _dev(idx, torch.int32, "idx", (Hkv, N))
     _dev(kd, torch.bfloat16, "kd", (Hkv, N, d))
-    _dev(vd, torch.bfloat16, "vd", (Hkv, N, d))
+    _dev(vd, v.dtype, "vd", (Hkv, N, d))
     n_out = _i64(0)
     rc = lib().ts_partial_kv_select_gather_noalloc(_ptr(imp), _ptr(k), _ptr(v), L, L_cap, Hkv, d,
                                                    B, S, R, _ptr(idx), _ptr(kd), _ptr(vd),
@@ -302,7 +315,7 @@ def ts_partial_kv_select_gather_batched(imps, ks, vs, L, B, S, R, idxs, kds, vds
     for i in range(n):
         _dev(imps[i], torch.float32, "imp", (Hkv, L))
         _dev(ks[i], torch.bfloat16, "k", (Hkv, L_cap, d))
-        _dev(vs[i], torch.bfloat16, "v", (Hkv, L_cap, d))
+        _dev(vs[i], _V_DTYPES, "v", (Hkv, L_cap, d))
     if table is None:
         table = layer_pointer_table(imps, ks, vs, idxs, kds, vds)
     ws, nb = _workspace(ts_select_batched_workspace_bytes(n, Hkv, L), ks[0].device, workspace)
@@ -329,11 +342,11 @@ def ts_partial_kv_refresh_incremental(imp, k, v, L, B, S, R, idx, kd, vd, N_prev
     Hkv, L_cap, d = k.shape
     _dev(imp, torch.float32, "imp", (Hkv, L))
     _dev(k, torch.bfloat16, "k")
-    _dev(v, torch.bfloat16, "v", (Hkv, L_cap, d))
+    _dev(v, _V_DTYPES, "v", (Hkv, L_cap, d))
     N_cap = idx.shape[1]
     _dev(idx, torch.int32, "idx", (Hkv, N_cap))
     _dev(kd, torch.bfloat16, "kd", (Hkv, N_cap, d))
-    _dev(vd, torch.bfloat16, "vd", (Hkv, N_cap, d))
+    _dev(vd, v.dtype, "vd", (Hkv, N_cap, d))
     ws, nb = _workspace(ts_refresh_workspace_bytes(1, Hkv, L, N_cap), k.device, workspace)
     n_out = _i64(0)
     rc = lib().ts_partial_kv_refresh_incremental(_ptr(imp), _ptr(k), _ptr(v), L, L_cap, Hkv, d, B,
@@ -355,10 +368,10 @@ def ts_partial_kv_refresh_incremental_batched(imps, ks, vs, L, B, S, R, idxs, kd
     for i in range(n):
         _dev(imps[i], torch.float32, "imp", (Hkv, L))
         _dev(ks[i], torch.bfloat16, "k", (Hkv, L_cap, d))
-        _dev(vs[i], torch.bfloat16, "v", (Hkv, L_cap, d))
+        _dev(vs[i], _V_DTYPES, "v", (Hkv, L_cap, d))
         _dev(idxs[i], torch.int32, "idx", (Hkv, N_cap))
         _dev(kds[i], torch.bfloat16, "kd", (Hkv, N_cap, d))
-        _dev(vds[i], torch.bfloat16, "vd", (Hkv, N_cap, d))
+        _dev(vds[i], vs[i].dtype, "vd", (Hkv, N_cap, d))
     if table is None:
         table = layer_pointer_table(imps, ks, vs, idxs, kds, vds)
     ws, nb = _workspace(ts_refresh_workspace_bytes(n, Hkv, L, N_cap), ks[0].device, workspace)
@@ -439,7 +452,7 @@ def ts_kv_commit(k, v, L, T, path, n_path, status=None, stream=None):
     """Move the accepted tree rows L+path[t] to L+t (in place)."""
     Hkv, L_cap, d = k.shape
     _dev(k, torch.bfloat16, "k")
-    _dev(v, torch.bfloat16, "v", (Hkv, L_cap, d))
+    _dev(v, _V_DTYPES, "v", (Hkv, L_cap, d))
     rc = lib().ts_kv_commit(_ptr(k), _ptr(v), L, L_cap, Hkv, d, T, _ptr(path), _ptr(n_path),
                             _ptr(status), _stream(stream))
     _check(rc)
@@ -461,7 +474,7 @@ def ts_kv_commit_batched(ks, vs, L, T, path, n_path, table=None, status=None, st
     Hkv, L_cap, d = ks[0].shape
     for x, y in zip(ks, vs):
         _dev(x, torch.bfloat16, "k", (Hkv, L_cap, d))
-        _dev(y, torch.bfloat16, "v", (Hkv, L_cap, d))
+        _dev(y, _V_DTYPES, "v", (Hkv, L_cap, d))
     if table is None:
         table = commit_pointer_table(ks, vs)
     rc = lib().ts_kv_commit_batched(len(ks), ctypes.c_void_p(table[0].data_ptr()),
@@ -470,21 +483,26 @@ def ts_kv_commit_batched(ks, vs, L, T, path, n_path, table=None, status=None, st
     _check(rc)
 
 
-def ts_kv_append_batched(ks, vs, k_rows, v_rows, L, table=None, stream=None):
+def ts_kv_append_batched(ks, vs, k_rows, v_rows, L, table=None, status=None, stream=None):
     """Write the tree's K/V rows [L, L+T) into every layer's cache in one
-    launch.  k_rows, v_rows [n_layers, Hkv, T, d] bf16 (contiguous)."""
+    launch.  k_rows, v_rows [n_layers, Hkv, T, d] bf16 (contiguous); fp16 V
+    caches receive the V rows rounded to fp16."""
     Hkv, L_cap, d = ks[0].shape
     n, T = len(ks), k_rows.shape[2]
     _dev(k_rows, torch.bfloat16, "k_rows", (n, Hkv, T, d))
     _dev(v_rows, torch.bfloat16, "v_rows", (n, Hkv, T, d))
     for x, y in zip(ks, vs):
         _dev(x, torch.bfloat16, "k", (Hkv, L_cap, d))
-        _dev(y, torch.bfloat16, "v", (Hkv, L_cap, d))
+        _dev(y, _V_DTYPES, "v", (Hkv, L_cap, d))
     if table is None:
         table = commit_pointer_table(ks, vs)
-    rc = lib().ts_kv_append_batched(n, ctypes.c_void_p(table[0].data_ptr()),
-                                    ctypes.c_void_p(table[1].data_ptr()), _ptr(k_rows),
-                                    _ptr(v_rows), L, L_cap, Hkv, d, T, _stream(stream))
+    if len({y.dtype for y in vs}) != 1:
+        raise TypeError("every layer's V cache must have the same dtype")
+    flags = TS_KV_V_FP16 if vs[0].dtype == torch.float16 else 0
+    rc = lib().ts_kv_append_batched_flags(n, ctypes.c_void_p(table[0].data_ptr()),
+                                          ctypes.c_void_p(table[1].data_ptr()), _ptr(k_rows),
+                                          _ptr(v_rows), L, L_cap, Hkv, d, T, flags, _ptr(status),
+                                          _stream(stream))
     _check(rc)
 
 

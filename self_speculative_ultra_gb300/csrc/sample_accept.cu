@@ -40,6 +40,7 @@
 // residuals live on the kept set (usually tens of tokens: one warp runs the
 // chain there); when the kept set overflows shared memory, or with no
 // truncation at all, the chain runs over the node's vocabulary row.
+#include "tc_ptx.cuh"
 #include "ts_common.cuh"
 
 namespace ts {
@@ -963,13 +964,16 @@ __global__ void kv_commit_batched_kernel(__nv_bfloat16* const* __restrict__ ks,
 
 // The draft tree's own K/V rows into every layer's cache: rows [L, L+T) of
 // KV head kv of layer l come from the packed arrays [n_layers][Hkv][T][D].
-// CTA (KV head, layer); 16-byte copies (rows are 128 or 256 bytes).
-template <int D>
+// CTA (KV head, layer); 16-byte copies (rows are 128 or 256 bytes).  With an
+// fp16 V cache (kVF16) each bf16 value of v is rounded to the nearest fp16
+// (exact for normal values below 65504 in magnitude); larger magnitudes
+// saturate to +-65504 and TS_ERR_UNSUPPORTED goes to the status word.
+template <int D, bool kVF16>
 __global__ void kv_append_batched_kernel(__nv_bfloat16* const* __restrict__ ks,
                                          __nv_bfloat16* const* __restrict__ vs,
                                          const __nv_bfloat16* __restrict__ krows,
                                          const __nv_bfloat16* __restrict__ vrows, int64_t L,
-                                         int64_t L_cap, int T) {
+                                         int64_t L_cap, int T, int32_t* status) {
   constexpr int V16 = D / 8;
   const int kv = blockIdx.x, layer = blockIdx.y, Hkv = gridDim.x;
   const size_t src = ((size_t)layer * Hkv + kv) * T * V16;
@@ -977,10 +981,23 @@ __global__ void kv_append_batched_kernel(__nv_bfloat16* const* __restrict__ ks,
   const uint4* vsrc = reinterpret_cast<const uint4*>(vrows) + src;
   uint4* kdst = reinterpret_cast<uint4*>(ks[layer] + ((size_t)kv * L_cap + L) * D);
   uint4* vdst = reinterpret_cast<uint4*>(vs[layer] + ((size_t)kv * L_cap + L) * D);
+  bool over = false;
   for (int e = threadIdx.x; e < T * V16; e += blockDim.x) {
     kdst[e] = ksrc[e];
-    vdst[e] = vsrc[e];
+    uint4 u = vsrc[e];
+    if (kVF16) {
+      uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+      for (int x = 0; x < 4; ++x) {
+        const float lo = __uint_as_float(w[x] << 16), hi = __uint_as_float(w[x] & 0xFFFF0000u);
+        over |= !(fabsf(lo) <= 65504.f) || !(fabsf(hi) <= 65504.f);
+        w[x] = ptx::pack_f16x2_sat(lo, hi);   // the rounding of the in-kernel conversion
+      }
+      u = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+    vdst[e] = u;
   }
+  if (kVF16 && over && status) set_status(status, TS_ERR_UNSUPPORTED);
 }
 
 }  // namespace
@@ -1051,16 +1068,17 @@ int launch_kv_commit_batched(int n_layers, void* const* k, void* const* v, int64
 
 int launch_kv_append_batched(int n_layers, void* const* k, void* const* v, const void* krows,
                              const void* vrows, int64_t L, int64_t L_cap, int Hkv, int d, int T,
-                             cudaStream_t st) {
+                             bool v_fp16, int32_t* status, cudaStream_t st) {
   auto kb = reinterpret_cast<__nv_bfloat16* const*>(k);
   auto vb = reinterpret_cast<__nv_bfloat16* const*>(v);
   auto kr = static_cast<const __nv_bfloat16*>(krows);
   auto vr = static_cast<const __nv_bfloat16*>(vrows);
   dim3 grid(Hkv, n_layers);
+  auto go = [&](auto kern) { kern<<<grid, 256, 0, st>>>(kb, vb, kr, vr, L, L_cap, T, status); };
   if (d == 128)
-    kv_append_batched_kernel<128><<<grid, 256, 0, st>>>(kb, vb, kr, vr, L, L_cap, T);
+    v_fp16 ? go(kv_append_batched_kernel<128, true>) : go(kv_append_batched_kernel<128, false>);
   else
-    kv_append_batched_kernel<64><<<grid, 256, 0, st>>>(kb, vb, kr, vr, L, L_cap, T);
+    v_fp16 ? go(kv_append_batched_kernel<64, true>) : go(kv_append_batched_kernel<64, false>);
   return launch_status("kv_append_batched_kernel");
 }
 

@@ -65,7 +65,7 @@ int launch_reject_accept(const float* logits, const float* q, const int32_t* tre
                          cudaStream_t st);
 int launch_kv_append_batched(int n_layers, void* const* k, void* const* v, const void* krows,
                              const void* vrows, int64_t L, int64_t L_cap, int Hkv, int d, int T,
-                             cudaStream_t st);
+                             bool v_fp16, int32_t* status, cudaStream_t st);
 
 }  // namespace ts
 
@@ -100,12 +100,13 @@ size_t ts_verify_workspace_bytes(int T, int Hq, int Hkv, int d, int64_t L) {
   return verify_plan(T, Hq, Hkv, d, L).ws_bytes;
 }
 
-int ts_verify_attention(const void* q, const void* k, const void* v, int64_t L, int64_t L_cap,
-                        const int32_t* parents, int T, int Hq, int Hkv, int d, int n_imp,
-                        float* o, float* lse, float* imp, void* workspace,
-                        size_t workspace_bytes, int32_t* status, void* stream) {
+int ts_verify_attention_flags(const void* q, const void* k, const void* v, int64_t L,
+                              int64_t L_cap, const int32_t* parents, int T, int Hq, int Hkv, int d,
+                              int n_imp, float* o, float* lse, float* imp, void* workspace,
+                              size_t workspace_bytes, int flags, int32_t* status, void* stream) {
   clear_error();
   const char* W = "ts_verify_attention";
+  if (flags & ~TS_VERIFY_V_FP16) return fail(TS_ERR_INVALID_ARG, "%s: unknown flags 0x%x", W, flags);
   int rc = check_attn_shape(T, Hq, Hkv, d, W);
   if (rc) return rc;
   if (!q || !k || !v || !parents || !o) return fail(TS_ERR_INVALID_ARG, "%s: NULL tensor", W);
@@ -118,8 +119,17 @@ int ts_verify_attention(const void* q, const void* k, const void* v, int64_t L, 
   VerifyPlan p = verify_plan(T, Hq, Hkv, d, L);
   rc = check_ws(workspace, workspace_bytes, p.ws_bytes, W);
   if (rc) return rc;
-  return launch_verify(q, k, v, L, L_cap, parents, T, Hq, Hkv, d, n_imp, o, lse, imp, workspace,
-                       status, static_cast<cudaStream_t>(stream));
+  return launch_verify(q, k, v, L, L_cap, parents, T, Hq, Hkv, d, n_imp,
+                       (flags & TS_VERIFY_V_FP16) != 0, o, lse, imp, workspace, status,
+                       static_cast<cudaStream_t>(stream));
+}
+
+int ts_verify_attention(const void* q, const void* k, const void* v, int64_t L, int64_t L_cap,
+                        const int32_t* parents, int T, int Hq, int Hkv, int d, int n_imp,
+                        float* o, float* lse, float* imp, void* workspace,
+                        size_t workspace_bytes, int32_t* status, void* stream) {
+  return ts_verify_attention_flags(q, k, v, L, L_cap, parents, T, Hq, Hkv, d, n_imp, o, lse, imp,
+                                   workspace, workspace_bytes, 0, status, stream);
 }
 
 int ts_importance_softmax(const void* q, const void* k, const float* lse, int64_t L,
@@ -405,11 +415,12 @@ int ts_kv_commit_batched(int n_layers, void* const* k, void* const* v, int64_t L
                                   static_cast<cudaStream_t>(stream));
 }
 
-int ts_kv_append_batched(int n_layers, void* const* k, void* const* v, const void* k_rows,
-                         const void* v_rows, int64_t L, int64_t L_cap, int Hkv, int d, int T,
-                         void* stream) {
+int ts_kv_append_batched_flags(int n_layers, void* const* k, void* const* v, const void* k_rows,
+                               const void* v_rows, int64_t L, int64_t L_cap, int Hkv, int d,
+                               int T, int flags, int32_t* status, void* stream) {
   clear_error();
   const char* F = "ts_kv_append_batched";
+  if (flags & ~TS_KV_V_FP16) return fail(TS_ERR_INVALID_ARG, "%s: unknown flags 0x%x", F, flags);
   if (n_layers < 1 || n_layers > 65535) return fail(TS_ERR_INVALID_ARG, "%s: n_layers=%d", F, n_layers);
   if (Hkv < 1 || T < 1) return fail(TS_ERR_INVALID_ARG, "%s: Hkv, T must be >= 1", F);
   if (T > 64) return fail(TS_ERR_UNSUPPORTED, "%s: T=%d > 64", F, T);
@@ -419,7 +430,15 @@ int ts_kv_append_batched(int n_layers, void* const* k, void* const* v, const voi
   if ((reinterpret_cast<uintptr_t>(k_rows) | reinterpret_cast<uintptr_t>(v_rows)) & 15)
     return fail(TS_ERR_INVALID_ARG, "%s: k_rows and v_rows must be 16-byte aligned", F);
   return launch_kv_append_batched(n_layers, k, v, k_rows, v_rows, L, L_cap, Hkv, d, T,
+                                  (flags & TS_KV_V_FP16) != 0, status,
                                   static_cast<cudaStream_t>(stream));
+}
+
+int ts_kv_append_batched(int n_layers, void* const* k, void* const* v, const void* k_rows,
+                         const void* v_rows, int64_t L, int64_t L_cap, int Hkv, int d, int T,
+                         void* stream) {
+  return ts_kv_append_batched_flags(n_layers, k, v, k_rows, v_rows, L, L_cap, Hkv, d, T, 0,
+                                    nullptr, stream);
 }
 
 size_t ts_reject_workspace_bytes(int V) {

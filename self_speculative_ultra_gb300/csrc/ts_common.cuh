@@ -131,8 +131,9 @@ int tc_splits(int Hkv, int n_rg, int64_t L, int nsm);
 int verify_splits(int Hkv, int n_pt, int n_two, int64_t L, int nsm);
 int launch_verify_tc(const void* q, const void* k, const void* v, int64_t L, int64_t L_cap,
                      const int32_t* parents, int T, int Hq, int Hkv, int d, int n_imp,
-                     int64_t keys_per_split, int n_split, int n_pt, int n_two, uint4* part_o,
-                     float* part_ml, float* imp, int32_t* status, cudaStream_t st);
+                     int64_t keys_per_split, int n_split, int n_pt, int n_two, bool v_fp16,
+                     uint4* part_o, float* part_ml, float* imp, int32_t* status,
+                     cudaStream_t st);
 
 // Limit (SM clock cycles) of one bounded device wait in the kernels with
 // cross-warp waits; ts_set_wait_limit sets it for later launches.
@@ -140,7 +141,7 @@ constexpr long long kDefaultWaitCycles = 1ll << 31;
 long long wait_limit_cycles();
 int launch_verify(const void* q, const void* k, const void* v, int64_t L, int64_t L_cap,
                   const int32_t* parents, int T, int Hq, int Hkv, int d, int n_imp,
-                  float* o, float* lse, float* imp, void* ws, int32_t* status,
+                  bool v_fp16, float* o, float* lse, float* imp, void* ws, int32_t* status,
                   cudaStream_t st);
 
 struct SelectPlan {

@@ -161,13 +161,13 @@ VerifyPlan verify_plan(int T, int Hq, int Hkv, int d, int64_t L) {
 }
 
 int launch_verify(const void* q, const void* k, const void* v, int64_t L, int64_t L_cap,
-                  const int32_t* parents, int T, int Hq, int Hkv, int d, int n_imp, float* o,
-                  float* lse, float* imp, void* ws, int32_t* status, cudaStream_t st) {
+                  const int32_t* parents, int T, int Hq, int Hkv, int d, int n_imp, bool v_fp16,
+                  float* o, float* lse, float* imp, void* ws, int32_t* status, cudaStream_t st) {
   VerifyPlan p = verify_plan(T, Hq, Hkv, d, L);
   uint4* part_o = static_cast<uint4*>(ws);
   float* part_ml = reinterpret_cast<float*>(static_cast<char*>(ws) + p.part_o_bytes);
   int rc = launch_verify_tc(q, k, v, L, L_cap, parents, T, Hq, Hkv, d, n_imp, p.keys_per_split,
-                            p.n_split, p.n_pt, p.n_two, part_o, part_ml, imp, status, st);
+                            p.n_split, p.n_pt, p.n_two, v_fp16, part_o, part_ml, imp, status, st);
   if (rc) return rc;
   const int ny = (d / 8 + 7) / 8;
   auto ctas = [&](int ng) { return (p.M + 32 / ng - 1) / (32 / ng) * ny * Hkv; };

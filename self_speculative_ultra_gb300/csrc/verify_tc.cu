@@ -33,9 +33,11 @@
 //   importance (2, 3)    imp_j = (sum of the group's last n_imp queries) . k_j
 //                        / sqrt(d) on CUDA cores from the same shared K tile
 //                        (the importance is linear in the queries)
-//   V conversion (4..7)  each V tile converted in place from bf16 to fp16 as
-//                        it lands (exact for |v| < 65504; larger values
-//                        saturate and are reported in the status word)
+//   V conversion (4..7)  with a bf16 V cache, each V tile converted in place
+//                        to fp16 as it lands (exact for |v| < 65504; larger
+//                        values saturate and are reported in the status
+//                        word); with an fp16 V cache the MMA takes the tile as
+//                        the copy engine wrote it and these warps are idle
 //   softmax (8..15)      one thread per query row, all 128 scores of a tile
 //                        read from TMEM into registers at once (the softmax
 //                        warpgroups hold 192 registers a thread, the others
@@ -178,7 +180,7 @@ __device__ __forceinline__ float fmax32(const uint32_t* r) {
   return ptx::max3(a, b, fmaxf(__uint_as_float(r[30]), __uint_as_float(r[31])));
 }
 
-template <int D>
+template <int D, bool kVF16>
 __global__ void __launch_bounds__(kThreadsTc, 1)
 verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v,
                  const __nv_bfloat16* __restrict__ q, const int32_t* __restrict__ parents, int T,
@@ -492,6 +494,9 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
           ptx::tc_fence_after();
           return true;
         };
+        // V stages the P V product may read: converted (bf16 cache) or as
+        // landed (fp16 cache)
+        uint64_t* v_ready = kVF16 ? aux->v_full : aux->v_conv;
         bool ok = true;
         if (!seq.two) {
           if (n_seq > 0) {
@@ -502,7 +507,7 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
             }
           }
           for (int s = 0; ok && s < n_seq; ++s) {
-            if (!ptx::mbar_wait(&aux->v_conv[s % kSV], (uint32_t)(s / kSV) & 1u, wait_limit)) {
+            if (!ptx::mbar_wait(&v_ready[s % kSV], (uint32_t)(s / kSV) & 1u, wait_limit)) {
               ok = false;
               break;
             }
@@ -538,7 +543,7 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
           for (int s = 0; ok && s < n_seq; ++s) {
             int g, k;
             seq.decode(s, g, k);
-            if (!ptx::mbar_wait(&aux->v_conv[s % kSV], (uint32_t)(s / kSV) & 1u, wait_limit) ||
+            if (!ptx::mbar_wait(&v_ready[s % kSV], (uint32_t)(s / kSV) & 1u, wait_limit) ||
                 !pv(g, s % kSV, k > 0, (uint32_t)k & 1u)) {
               ok = false;
               break;
@@ -610,7 +615,7 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
         __syncwarp();
         if (lane == 0) ptx::mbar_arrive(&aux->k_empty[stK]);
       }
-    } else {
+    } else if (!kVF16) {
       // ------------------------------------------------------------ V conversion
       // V tiles are converted in place from bf16 to fp16 as soon as they land,
       // ahead of the MMA's P V (the V ring is three tiles deep)
@@ -910,14 +915,16 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
-int make_kv_map(CUtensorMap* map, const void* base, int Hkv, int64_t L_cap, int d) {
+int make_kv_map(CUtensorMap* map, const void* base, int Hkv, int64_t L_cap, int d,
+                bool fp16 = false) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return fail(TS_ERR_CUDA, "cuTensorMapEncodeTiled is unavailable");
   cuuint64_t dims[2] = {(cuuint64_t)d, (cuuint64_t)Hkv * (cuuint64_t)L_cap};
   cuuint64_t strides[1] = {(cuuint64_t)d * 2};
   cuuint32_t box[2] = {64, (cuuint32_t)kNk};
   cuuint32_t estr[2] = {1, 1};
-  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides,
+  CUresult r = fn(map, fp16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+                  const_cast<void*>(base), dims, strides,
                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return fail(TS_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
@@ -973,12 +980,13 @@ size_t verify_tc_smem_bytes(int d) {
 
 int launch_verify_tc(const void* q, const void* k, const void* v, int64_t L, int64_t L_cap,
                      const int32_t* parents, int T, int Hq, int Hkv, int d, int n_imp,
-                     int64_t keys_per_split, int n_split, int n_pt, int n_two, uint4* part_o,
-                     float* part_ml, float* imp, int32_t* status, cudaStream_t st) {
+                     int64_t keys_per_split, int n_split, int n_pt, int n_two, bool v_fp16,
+                     uint4* part_o, float* part_ml, float* imp, int32_t* status,
+                     cudaStream_t st) {
   CUtensorMap mk, mv;
   int rc = make_kv_map(&mk, k, Hkv, L_cap, d);
   if (rc) return rc;
-  rc = make_kv_map(&mv, v, Hkv, L_cap, d);
+  rc = make_kv_map(&mv, v, Hkv, L_cap, d, v_fp16);
   if (rc) return rc;
   const int per_head = n_pt * n_split + n_two * ((n_split + 1) / 2);
   dim3 grid(per_head, Hkv);
@@ -1002,9 +1010,11 @@ int launch_verify_tc(const void* q, const void* k, const void* v, int64_t L, int
                        keys_per_split, n_split, n_pt, limit, part_o, part_ml, imp, status);
   };
   if (d == 128)
-    go(verify_tc_kernel<128>, TcLayout<128>::kBytes);
+    v_fp16 ? go(verify_tc_kernel<128, true>, TcLayout<128>::kBytes)
+           : go(verify_tc_kernel<128, false>, TcLayout<128>::kBytes);
   else
-    go(verify_tc_kernel<64>, TcLayout<64>::kBytes);
+    v_fp16 ? go(verify_tc_kernel<64, true>, TcLayout<64>::kBytes)
+           : go(verify_tc_kernel<64, false>, TcLayout<64>::kBytes);
   if (rc) return rc;
   return launch_status("verify_tc_kernel");
 }

@@ -157,3 +157,54 @@ def test_kv_append_batched_matches_oracle(d):
     for i in range(n_layers):
         assert pu.bf16_dev_to_bits(ks[i]).tobytes() == orc.kv_append(kbs[i], L, kr[i]).tobytes()
         assert pu.bf16_dev_to_bits(vs[i]).tobytes() == orc.kv_append(vbs[i], L, vr[i]).tobytes()
+
+
+def _bf16_bits_to_f16(bits):
+    """bf16 bit patterns -> fp16 values, rounded to nearest even (numpy's
+    float32 -> float16 conversion; the inputs below stay in fp16 range)."""
+    return (bits.astype(np.uint32) << 16).view(np.float32).astype(np.float16)
+
+
+@pytest.mark.parametrize("d", [128, 64])
+def test_kv_append_batched_into_fp16_v_cache(d):
+    """fp16 V caches: the V rows arrive rounded to the nearest fp16 (normal
+    values exactly, tiny ones to fp16 subnormals), the K rows bit for bit."""
+    import self_speculative_ultra_gb300 as ts
+    rng = np.random.default_rng(40 + d)
+    n_layers, Hkv, L, T = 3, 4, 2000, 64
+    kbs = [rng.integers(0, 2 ** 16, size=(Hkv, L + T + 3, d), dtype=np.uint16) for _ in range(n_layers)]
+    vfs = [rng.standard_normal((Hkv, L + T + 3, d)).astype(np.float16) for _ in range(n_layers)]
+    kr = rng.integers(0, 2 ** 16, size=(n_layers, Hkv, T, d), dtype=np.uint16)
+    vals = rng.standard_normal((n_layers, Hkv, T, d)).astype(np.float32)
+    vals[..., :5] *= 1e-6          # fp16 subnormal range
+    vals[..., 5:9] = np.clip(vals[..., 5:9] * 3e4, -6e4, 6e4)   # large but representable
+    vr = syn.f32_to_bf16_bits(vals.reshape(-1)).reshape(vals.shape)
+    ks = [pu.to_dev_bf16(x) for x in kbs]
+    vs = [torch.from_numpy(x).cuda() for x in vfs]
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    ts.ts_kv_append_batched(ks, vs, pu.to_dev_bf16(kr), pu.to_dev_bf16(vr), L, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    for i in range(n_layers):
+        assert pu.bf16_dev_to_bits(ks[i]).tobytes() == orc.kv_append(kbs[i], L, kr[i]).tobytes()
+        want = orc.kv_append(vfs[i], L, _bf16_bits_to_f16(vr[i]))
+        assert vs[i].cpu().numpy().tobytes() == want.tobytes()
+
+
+def test_kv_append_fp16_v_saturates_and_reports():
+    """A V value beyond the fp16 range saturates to +-65504 and the call
+    writes TS_ERR_UNSUPPORTED (2) to the status word."""
+    import self_speculative_ultra_gb300 as ts
+    Hkv, L, T, d = 2, 100, 8, 64
+    ks = [torch.zeros((Hkv, L + T, d), dtype=torch.bfloat16, device="cuda")]
+    vs = [torch.zeros((Hkv, L + T, d), dtype=torch.float16, device="cuda")]
+    vals = np.zeros((1, Hkv, T, d), np.float32)
+    vals[0, 1, 3, 7], vals[0, 0, 2, 1] = 1e5, -2e5
+    vr = syn.f32_to_bf16_bits(vals.reshape(-1)).reshape(vals.shape)
+    kr = np.zeros_like(vr)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    ts.ts_kv_append_batched(ks, vs, pu.to_dev_bf16(kr), pu.to_dev_bf16(vr), L, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 2
+    got = vs[0].cpu().numpy()
+    assert got[1, L + 3, 7] == np.float16(65504) and got[0, L + 2, 1] == np.float16(-65504)

@@ -11,14 +11,18 @@ import parity_util as pu
 pytestmark = pytest.mark.gpu
 
 
-def _run(w, L=None, layer=0, n_imp=None, tree=None, kv_heads=None):
+def _run(w, L=None, layer=0, n_imp=None, tree=None, kv_heads=None, v_fp16=False):
     """Run the library on all heads; compare the KV heads `kv_heads` (all by
-    default) and their query heads element by element with the oracle."""
+    default) and their query heads element by element with the oracle.
+    v_fp16: the V cache is handed over in fp16 (the same values: the
+    synthetic bf16 values convert exactly, subnormals rounding to nearest)."""
     import self_speculative_ultra_gb300 as ts
     inp = syn.attention_inputs(w, layer=layer, L=L, tree=tree)
     L = inp["L"]
     n_imp = w.n_imp if n_imp is None else n_imp
     q, k, v = (pu.to_dev_bf16(inp[n]) for n in ("q", "k", "v"))
+    if v_fp16:
+        v = v.to(torch.float16)
     parents = pu.to_dev(inp["parents"])
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
     o, lse, imp = ts.ts_verify_attention(q, k, v, L, parents, n_imp=n_imp, status=status)
@@ -63,14 +67,38 @@ def test_chain_tree_and_partial_importance():
     _run(w, L=3000, n_imp=5, tree=(parents, np.zeros(64, np.int32)))
 
 
-@pytest.mark.parametrize("name,kv_heads", [("llama3.1-8b", None), ("qwen2.5-14b", None),
-                                           ("qwen2.5-1.5b", None), ("mha-7b", (0, 13, 31))])
-def test_full_size_one_layer(name, kv_heads):
+@pytest.mark.parametrize("name,kv_heads,v_fp16", [("llama3.1-8b", None, False),
+                                                  ("llama3.1-8b", None, True),
+                                                  ("qwen2.5-14b", None, True),
+                                                  ("qwen2.5-1.5b", None, True),
+                                                  ("mha-7b", (0, 13, 31), True)])
+def test_full_size_one_layer(name, kv_heads, v_fp16):
     """Every model shape at its full cache length (102,400 tokens; 32,768 for
-    Qwen2.5-1.5B), the launch configuration the benchmark times.  For the
-    32-head MHA shape three KV heads (first, middle, last) are compared in
-    full against the oracle; the others are computed by the same launch."""
-    _run(syn.WORKLOADS[name], layer=1, kv_heads=kv_heads)
+    Qwen2.5-1.5B), the launch configuration the benchmark times (an fp16 V
+    cache; LLaMA3.1-8B also with the bf16 one).  For the 32-head MHA shape
+    three KV heads (first, middle, last) are compared in full against the
+    oracle; the others are computed by the same launch."""
+    _run(syn.WORKLOADS[name], layer=1, kv_heads=kv_heads, v_fp16=v_fp16)
+
+
+@pytest.mark.parametrize("name", ["tiny", "qwen2.5-1.5b", "llama3.1-8b", "mha-7b", "qwen2.5-14b"])
+def test_fp16_v_cache_is_bit_identical(name):
+    """An fp16 V cache only moves the bf16 -> fp16 rounding of V from the
+    kernel's shared memory to the cache: on the same values every output
+    (O, LSE, importance) is bit for bit that of the bf16 call."""
+    import self_speculative_ultra_gb300 as ts
+    w = syn.WORKLOADS[name]
+    inp = syn.attention_inputs(w, L=4133)
+    q, k, v = (pu.to_dev_bf16(inp[n]) for n in ("q", "k", "v"))
+    parents = pu.to_dev(inp["parents"])
+    outs = []
+    for vv in (v, v.to(torch.float16)):
+        status = torch.zeros(1, dtype=torch.int32, device="cuda")
+        outs.append(ts.ts_verify_attention(q, k, vv, 4133, parents, n_imp=w.n_imp, status=status))
+        torch.cuda.synchronize()
+        assert int(status.item()) == 0
+    for a, b in zip(*outs):
+        assert torch.equal(a, b)
 
 
 def test_bad_parent_sets_status():
