@@ -46,7 +46,7 @@ extern "C" {
 typedef enum ts_status {
   TS_OK = 0,
   TS_ERR_INVALID_ARG = 1,  /* argument out of its documented domain        */
-  TS_ERR_UNSUPPORTED = 2,  /* valid but outside this build's limits        */
+  TS_ERR_UNSUPPORTED = 2,  /* valid but outside the library's limits       */
   TS_ERR_CUDA = 3,         /* a CUDA launch or runtime call failed          */
   TS_ERR_TIMEOUT = 4,      /* a bounded device-side wait ran out            */
   TS_ERR_WORKSPACE = 5     /* workspace missing, too small or misaligned    */
