@@ -52,10 +52,10 @@ def _run(w, step, top_p=None, min_p=None, literal=False, q=None, seed=0, inp=Non
     got = (path.cpu().numpy()[:n].tolist(), int(bonus.item()))
     args = (inp, q, w.W, w.penalty, w.temperature, top_p, min_p)
     ref = _oracle(*args, ua, ud, literal)
-    return _judge(got, ref, args, ua, ud, literal, step)
+    return _compare_outcome(got, ref, args, ua, ud, literal, step)
 
 
-def _judge(got, ref, args, ua, ud, literal, step):
+def _compare_outcome(got, ref, args, ua, ud, literal, step):
     """'exact' when got equals the oracle's result; 'tie' when the oracle's
     result moves under the 2e-5 perturbations of the uniforms and got is one
     of the perturbed results; anything else fails."""
