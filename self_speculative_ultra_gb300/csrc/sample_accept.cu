@@ -51,6 +51,7 @@ constexpr int kThreads = 512;
 constexpr int kParts = 4;                // CTAs per tree node
 constexpr int kCapPart = 4096;           // candidates one slice may publish
 constexpr int kBatch = 8;                // float4 loads of a thread in flight together
+constexpr int kScan = 8;                 // loads of a thread in flight in the per-node scans
 constexpr int kMaxBuckets = 2048;
 constexpr uint32_t kIdMask = 0x3FFFFu;   // V <= 2^18
 
@@ -156,9 +157,13 @@ __device__ int block_sum_int(int v, SampleSmem& sm) {
 // One radix level: histogram the tokens matching the digits fixed so far,
 // then (warp 0) pick the bucket holding the target and fold the buckets
 // ranked above it into (mb, cb).  Returns nothing; updates the prefixes.
+// Tokens with e = exp(x - xmax) < skip_e are left out: a caller whose target
+// lies inside the rank prefix {e >= skip_e} (the kept pool ranks first) gets
+// the same token without them, and the first levels, which put most tokens
+// into a few buckets, take far fewer contended atomics.
 __device__ void radix_level(const float* __restrict__ xs, int V, float xmax, int mode,
                             float target_mass, int target_rank, bool on_id, int shift, int bits,
-                            SampleSmem& sm) {
+                            float skip_e, SampleSmem& sm) {
   const int nb = 1 << bits;
   for (int b = threadIdx.x; b < nb; b += blockDim.x) {
     sm.cnt[b] = 0;
@@ -166,13 +171,27 @@ __device__ void radix_level(const float* __restrict__ xs, int V, float xmax, int
   }
   __syncthreads();
   const uint32_t kpre = sm.kpre, kmask = sm.kmask, ipre = sm.ipre, imask = sm.imask;
-  for (int t = threadIdx.x; t < V; t += blockDim.x) {
-    const float x = xs[t];
-    const uint32_t key = float_key(x), rid = kIdMask - (uint32_t)t;
-    if ((key & kmask) != kpre || (rid & imask) != ipre) continue;
-    const uint32_t dig = ((on_id ? rid : key) >> shift) & (uint32_t)(nb - 1);
-    atomicAdd(&sm.cnt[dig], 1);
-    if (mode != kRank) atomicAdd(&sm.mass[dig], expf(x - xmax));
+  // kScan loads of a thread in flight together, then their histogram updates
+  for (int c0 = 0; c0 < V; c0 += blockDim.x * kScan) {
+    float xv[kScan];
+#pragma unroll
+    for (int u = 0; u < kScan; ++u) {
+      const int t = c0 + u * blockDim.x + threadIdx.x;
+      xv[u] = t < V ? xs[t] : 0.f;
+    }
+#pragma unroll
+    for (int u = 0; u < kScan; ++u) {
+      const int t = c0 + u * blockDim.x + threadIdx.x;
+      if (t >= V) continue;
+      const float x = xv[u];
+      const uint32_t key = float_key(x), rid = kIdMask - (uint32_t)t;
+      if ((key & kmask) != kpre || (rid & imask) != ipre) continue;
+      const float e = expf(x - xmax);
+      if (e < skip_e) continue;
+      const uint32_t dig = ((on_id ? rid : key) >> shift) & (uint32_t)(nb - 1);
+      atomicAdd(&sm.cnt[dig], 1);
+      if (mode != kRank) atomicAdd(&sm.mass[dig], e);
+    }
   }
   __syncthreads();
   if (threadIdx.x < 32) {
@@ -249,18 +268,18 @@ __device__ void radix_level(const float* __restrict__ xs, int V, float xmax, int
 }
 
 __device__ Found radix_find(const float* __restrict__ xs, int V, float xmax, int mode,
-                            float target_mass, int target_rank, SampleSmem& sm) {
+                            float target_mass, int target_rank, float skip_e, SampleSmem& sm) {
   if (threadIdx.x == 0) {
     sm.kpre = sm.kmask = sm.ipre = sm.imask = 0;
     sm.mb = 0.f;
     sm.cb = 0;
   }
   __syncthreads();
-  radix_level(xs, V, xmax, mode, target_mass, target_rank, false, 21, 11, sm);
-  radix_level(xs, V, xmax, mode, target_mass, target_rank, false, 10, 11, sm);
-  radix_level(xs, V, xmax, mode, target_mass, target_rank, false, 0, 10, sm);
-  radix_level(xs, V, xmax, mode, target_mass, target_rank, true, 9, 9, sm);
-  radix_level(xs, V, xmax, mode, target_mass, target_rank, true, 0, 9, sm);
+  radix_level(xs, V, xmax, mode, target_mass, target_rank, false, 21, 11, skip_e, sm);
+  radix_level(xs, V, xmax, mode, target_mass, target_rank, false, 10, 11, skip_e, sm);
+  radix_level(xs, V, xmax, mode, target_mass, target_rank, false, 0, 10, skip_e, sm);
+  radix_level(xs, V, xmax, mode, target_mass, target_rank, true, 9, 9, skip_e, sm);
+  radix_level(xs, V, xmax, mode, target_mass, target_rank, true, 0, 9, skip_e, sm);
   Found f;
   f.id = (int)(kIdMask - sm.ipre);
   f.rank = sm.cb;
@@ -691,28 +710,36 @@ sample_accept_kernel(const float* __restrict__ logits, const int32_t* __restrict
     }
   } else {
     // full scan of the node's x' (a slice overflowed, or eta); members
-    // are collected while they fit
-    for (int b0 = 0; b0 < V; b0 += kThreads) {
-      const int t = b0 + tid;
-      float x = 0.f, e = 0.f;
-      if (t < V) {
-        x = __ldcg(xs + t);
-        e = expf(x - xmax);
+    // are collected while they fit.  kScan loads of a thread are in flight
+    // together: the ballots between tokens would otherwise hold every load
+    // behind the previous one.
+    for (int c0 = 0; c0 < V; c0 += kThreads * kScan) {
+      float xv[kScan];
+#pragma unroll
+      for (int u = 0; u < kScan; ++u) {
+        const int t = c0 + u * kThreads + tid;
+        xv[u] = t < V ? __ldcg(xs + t) : 0.f;
       }
-      const bool in = t < V && e >= thr;
-      if (in) {
-        zmin += e;
-        ++nmin;
-      }
-      const unsigned m = __ballot_sync(0xffffffffu, in);
-      if (m) {
-        int base = 0;
-        if (lane == __ffs(m) - 1) base = atomicAdd(&sm.ncand, __popc(m));
-        base = __shfl_sync(0xffffffffu, base, __ffs(m) - 1);
-        const int slot = base + __popc(m & ((1u << lane) - 1));
-        if (in && slot < kCap) {
-          sm.ckey[slot] = float_key(x);
-          sm.cid[slot] = t;
+#pragma unroll
+      for (int u = 0; u < kScan; ++u) {
+        const int t = c0 + u * kThreads + tid;
+        const float x = xv[u];
+        const float e = t < V ? expf(x - xmax) : 0.f;
+        const bool in = t < V && e >= thr;
+        if (in) {
+          zmin += e;
+          ++nmin;
+        }
+        const unsigned m = __ballot_sync(0xffffffffu, in);
+        if (m) {
+          int base = 0;
+          if (lane == __ffs(m) - 1) base = atomicAdd(&sm.ncand, __popc(m));
+          base = __shfl_sync(0xffffffffu, base, __ffs(m) - 1);
+          const int slot = base + __popc(m & ((1u << lane) - 1));
+          if (in && slot < kCap) {
+            sm.ckey[slot] = float_key(x);
+            sm.cid[slot] = t;
+          }
         }
       }
     }
@@ -824,7 +851,7 @@ sample_accept_kernel(const float* __restrict__ logits, const int32_t* __restrict
     uint32_t cut_key = 0u, cut_rid = 0u;
     bool by_cut = false;
     if (!eta_mode && top_p < 1.0f) {
-      const Found f1 = radix_find(xs, V, xmax, kMassGT, top_p * Z, 0, sm);
+      const Found f1 = radix_find(xs, V, xmax, kMassGT, top_p * Z, 0, 0.f, sm);
       k_keep = min(n_minp, f1.rank + 1);
       ZK = (k_keep == f1.rank + 1) ? f1.cum_incl : Zmin;
       if (k_keep == f1.rank + 1) {
@@ -838,8 +865,11 @@ sample_accept_kernel(const float* __restrict__ logits, const int32_t* __restrict
                            q_draft + (size_t)i * V, uniforms, u_draw, sm);
     } else {
       const float u = uniforms[i];
-      Found f2 = radix_find(xs, V, xmax, kMassGT, u * ZK, 0, sm);
-      if (f2.rank >= k_keep) f2 = radix_find(xs, V, xmax, kRank, 0.f, k_keep - 1, sm);
+      // the draw lies inside the kept pool, a rank prefix of {e >= thr}
+      // (with thr above 1 the pool is rank 0 alone, e = 1)
+      const float skip = fminf(thr, 1.f);
+      Found f2 = radix_find(xs, V, xmax, kMassGT, u * ZK, 0, skip, sm);
+      if (f2.rank >= k_keep) f2 = radix_find(xs, V, xmax, kRank, 0.f, k_keep - 1, skip, sm);
       token = f2.id;
     }
   }
