@@ -52,6 +52,8 @@ constexpr int kParts = 4;                // CTAs per tree node
 constexpr int kCapPart = 4096;           // candidates one slice may publish
 constexpr int kBatch = 8;                // float4 loads of a thread in flight together
 constexpr int kScan = 8;                 // loads of a thread in flight in the per-node scans
+constexpr int kPool = kParts * kCapPart; // pool entries a node's scan compacts (its slices'
+                                         // candidate area, unused once it scans the row)
 constexpr int kMaxBuckets = 2048;
 constexpr uint32_t kIdMask = 0x3FFFFu;   // V <= 2^18
 
@@ -161,9 +163,12 @@ __device__ int block_sum_int(int v, SampleSmem& sm) {
 // lies inside the rank prefix {e >= skip_e} (the kept pool ranks first) gets
 // the same token without them, and the first levels, which put most tokens
 // into a few buckets, take far fewer contended atomics.
-__device__ void radix_level(const float* __restrict__ xs, int V, float xmax, int mode,
-                            float target_mass, int target_rank, bool on_id, int shift, int bits,
-                            float skip_e, SampleSmem& sm) {
+// With kList, the level reads a `list` of n (float_key(x'), id) pairs (a
+// node's kept pool, compacted by its scan) instead of the row xs.
+template <bool kList>
+__device__ __noinline__ void radix_level(const float* __restrict__ xs, int V, const uint2* list, int n,
+                            float xmax, int mode, float target_mass, int target_rank, bool on_id,
+                            int shift, int bits, float skip_e, SampleSmem& sm) {
   const int nb = 1 << bits;
   for (int b = threadIdx.x; b < nb; b += blockDim.x) {
     sm.cnt[b] = 0;
@@ -172,18 +177,30 @@ __device__ void radix_level(const float* __restrict__ xs, int V, float xmax, int
   __syncthreads();
   const uint32_t kpre = sm.kpre, kmask = sm.kmask, ipre = sm.ipre, imask = sm.imask;
   // kScan loads of a thread in flight together, then their histogram updates
-  for (int c0 = 0; c0 < V; c0 += blockDim.x * kScan) {
-    float xv[kScan];
+  const int n_in = kList ? n : V;
+  for (int c0 = 0; c0 < n_in; c0 += blockDim.x * kScan) {
+    uint32_t kx[kScan], ki[kScan];
 #pragma unroll
     for (int u = 0; u < kScan; ++u) {
-      const int t = c0 + u * blockDim.x + threadIdx.x;
-      xv[u] = t < V ? xs[t] : 0.f;
+      const int j = c0 + u * blockDim.x + threadIdx.x;
+      kx[u] = 0u;
+      ki[u] = (uint32_t)j;
+      if (j < n_in) {
+        if (kList) {
+          const uint2 v = list[j];
+          kx[u] = v.x;
+          ki[u] = v.y;
+        } else {
+          kx[u] = __float_as_uint(xs[j]);
+        }
+      }
     }
 #pragma unroll
     for (int u = 0; u < kScan; ++u) {
-      const int t = c0 + u * blockDim.x + threadIdx.x;
-      if (t >= V) continue;
-      const float x = xv[u];
+      const int j = c0 + u * blockDim.x + threadIdx.x;
+      if (j >= n_in) continue;
+      const float x = kList ? key_float(kx[u]) : __uint_as_float(kx[u]);
+      const int t = (int)ki[u];
       const uint32_t key = float_key(x), rid = kIdMask - (uint32_t)t;
       if ((key & kmask) != kpre || (rid & imask) != ipre) continue;
       const float e = expf(x - xmax);
@@ -267,19 +284,21 @@ __device__ void radix_level(const float* __restrict__ xs, int V, float xmax, int
   __syncthreads();
 }
 
-__device__ Found radix_find(const float* __restrict__ xs, int V, float xmax, int mode,
-                            float target_mass, int target_rank, float skip_e, SampleSmem& sm) {
+template <bool kList>
+__device__ __noinline__ Found radix_find(const float* __restrict__ xs, int V, const uint2* list, int n,
+                            float xmax, int mode, float target_mass, int target_rank, float skip_e,
+                            SampleSmem& sm) {
   if (threadIdx.x == 0) {
     sm.kpre = sm.kmask = sm.ipre = sm.imask = 0;
     sm.mb = 0.f;
     sm.cb = 0;
   }
   __syncthreads();
-  radix_level(xs, V, xmax, mode, target_mass, target_rank, false, 21, 11, skip_e, sm);
-  radix_level(xs, V, xmax, mode, target_mass, target_rank, false, 10, 11, skip_e, sm);
-  radix_level(xs, V, xmax, mode, target_mass, target_rank, false, 0, 10, skip_e, sm);
-  radix_level(xs, V, xmax, mode, target_mass, target_rank, true, 9, 9, skip_e, sm);
-  radix_level(xs, V, xmax, mode, target_mass, target_rank, true, 0, 9, skip_e, sm);
+  radix_level<kList>(xs, V, list, n, xmax, mode, target_mass, target_rank, false, 21, 11, skip_e, sm);
+  radix_level<kList>(xs, V, list, n, xmax, mode, target_mass, target_rank, false, 10, 11, skip_e, sm);
+  radix_level<kList>(xs, V, list, n, xmax, mode, target_mass, target_rank, false, 0, 10, skip_e, sm);
+  radix_level<kList>(xs, V, list, n, xmax, mode, target_mass, target_rank, true, 9, 9, skip_e, sm);
+  radix_level<kList>(xs, V, list, n, xmax, mode, target_mass, target_rank, true, 0, 9, skip_e, sm);
   Found f;
   f.id = (int)(kIdMask - sm.ipre);
   f.rank = sm.cb;
@@ -678,6 +697,9 @@ sample_accept_kernel(const float* __restrict__ logits, const int32_t* __restrict
   // the node's min-p set {e >= min_p}, e = exp(x' - max x'), from the slices' supersets
   float zmin = 0.f;
   int nmin = 0;
+  // the node's pool, compacted by the row scan below (the slices' candidate
+  // lists there are not read on that path)
+  uint2* pool = ws.cand + (size_t)i * kPool;
   if (!overflow) {
     for (int p = 0; p < kParts; ++p) {
       const int np_ = vst[p].n;
@@ -740,12 +762,14 @@ sample_accept_kernel(const float* __restrict__ logits, const int32_t* __restrict
             sm.ckey[slot] = float_key(x);
             sm.cid[slot] = t;
           }
+          if (in && slot < kPool) pool[slot] = make_uint2(float_key(x), (uint32_t)t);
         }
       }
     }
   }
   float Zmin = block_sum(zmin, sm);
   int n_minp = block_sum_int(nmin, sm);
+  const int n_minp_seen = n_minp;   // members the scan counted (before the min_p > 1 rule)
   int token;
   if (n_minp >= 1 && n_minp <= kCap) {
     // ---- fast path: the kept set is a rank prefix inside the min-p set.
@@ -851,7 +875,7 @@ sample_accept_kernel(const float* __restrict__ logits, const int32_t* __restrict
     uint32_t cut_key = 0u, cut_rid = 0u;
     bool by_cut = false;
     if (!eta_mode && top_p < 1.0f) {
-      const Found f1 = radix_find(xs, V, xmax, kMassGT, top_p * Z, 0, 0.f, sm);
+      const Found f1 = radix_find<false>(xs, V, nullptr, 0, xmax, kMassGT, top_p * Z, 0, 0.f, sm);
       k_keep = min(n_minp, f1.rank + 1);
       ZK = (k_keep == f1.rank + 1) ? f1.cum_incl : Zmin;
       if (k_keep == f1.rank + 1) {
@@ -866,10 +890,19 @@ sample_accept_kernel(const float* __restrict__ logits, const int32_t* __restrict
     } else {
       const float u = uniforms[i];
       // the draw lies inside the kept pool, a rank prefix of {e >= thr}
-      // (with thr above 1 the pool is rank 0 alone, e = 1)
+      // (with thr above 1 the pool is rank 0 alone, e = 1): the descent
+      // reads the pool compacted by the scan when it holds all of it, else
+      // the row, leaving out the tokens below the pool
       const float skip = fminf(thr, 1.f);
-      Found f2 = radix_find(xs, V, xmax, kMassGT, u * ZK, 0, skip, sm);
-      if (f2.rank >= k_keep) f2 = radix_find(xs, V, xmax, kRank, 0.f, k_keep - 1, skip, sm);
+      const bool listed = overflow && n_minp_seen >= 1 && n_minp_seen <= kPool;
+      const uint2* lst = listed ? pool : nullptr;
+      const int nl = listed ? n_minp_seen : 0;
+      auto find = [&](int mode, float mass, int rank) {
+        return listed ? radix_find<true>(xs, V, lst, nl, xmax, mode, mass, rank, 0.f, sm)
+                      : radix_find<false>(xs, V, nullptr, 0, xmax, mode, mass, rank, skip, sm);
+      };
+      Found f2 = find(kMassGT, u * ZK, 0);
+      if (f2.rank >= k_keep) f2 = find(kRank, 0.f, k_keep - 1);
       token = f2.id;
     }
   }
