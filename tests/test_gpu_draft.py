@@ -15,7 +15,7 @@ import parity_util as pu
 pytestmark = pytest.mark.gpu
 
 
-def _draft(name, L, T_d, seed=0):
+def _draft(name, L, T_d, seed=0, v_fp16=False):
     import self_speculative_ultra_gb300 as ts
     w = syn.WORKLOADS[name]
     inp = syn.attention_inputs(w, L=L)
@@ -24,6 +24,8 @@ def _draft(name, L, T_d, seed=0):
     chain = np.array([-1] + list(range(T_d - 1)), dtype=np.int32)
     # library: select + gather, then attention over [compact rows ; draft rows]
     k, v = pu.to_dev_bf16(inp["k"]), pu.to_dev_bf16(inp["v"])
+    if v_fp16:
+        v = v.to(torch.float16)   # the same values: the compact V rows and the call are fp16
     idx, kd, vd = ts.ts_partial_kv_select_gather(pu.to_dev(imp), k, v, L, w.B, w.S, w.R)
     N = idx.shape[1]
     k_ext = torch.cat([kd, k[:, L:L + T_d]], dim=1).contiguous()
@@ -55,6 +57,13 @@ def test_draft_attention_over_compact_cache(name, T_d):
     N = _draft(name, 20000, T_d)
     w = syn.WORKLOADS[name]
     assert N == w.S + w.B + w.R
+
+
+@pytest.mark.parametrize("name", ["llama3.1-8b", "qwen2.5-14b"])
+def test_draft_attention_fp16_v_cache(name):
+    """fp16 V caches through the gather and the draft attention."""
+    w = syn.WORKLOADS[name]
+    assert _draft(name, 20000, 4, v_fp16=True) == w.S + w.B + w.R
 
 
 def test_draft_attention_cache_within_budget():

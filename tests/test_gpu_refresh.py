@@ -20,7 +20,10 @@ def _imp(rng, base, L, drift, grid):
     return x.astype(np.float32)
 
 
-def _sequence(Hkv, d, B, S, R, L0, steps, grid=None, n_layers=1, drift=0.3, seed=0):
+def _sequence(Hkv, d, B, S, R, L0, steps, grid=None, n_layers=1, drift=0.3, seed=0,
+              v_fp16=False):
+    """v_fp16: the V caches hold fp16 (the same random 16-bit patterns; the
+    refresh copies bytes, so the expected rows are the same bits)."""
     import self_speculative_ultra_gb300 as ts
     rng = np.random.default_rng(seed)
     N_cap = S + B + R
@@ -33,9 +36,11 @@ def _sequence(Hkv, d, B, S, R, L0, steps, grid=None, n_layers=1, drift=0.3, seed
         caches.append((kb, vb, base))
     ks = [pu.to_dev_bf16(c[0]) for c in caches]
     vs = [pu.to_dev_bf16(c[1]) for c in caches]
+    if v_fp16:
+        vs = [v.view(torch.float16) for v in vs]
     idxs = [torch.full((Hkv, N_cap), -7, dtype=torch.int32, device="cuda") for _ in range(n_layers)]
     kds = [torch.zeros((Hkv, N_cap, d), dtype=torch.bfloat16, device="cuda") for _ in range(n_layers)]
-    vds = [torch.zeros((Hkv, N_cap, d), dtype=torch.bfloat16, device="cuda") for _ in range(n_layers)]
+    vds = [torch.zeros((Hkv, N_cap, d), dtype=vs[0].dtype, device="cuda") for _ in range(n_layers)]
     # oracle state per (layer, head)
     slots = [[np.zeros(0, dtype=np.int64) for _ in range(Hkv)] for _ in range(n_layers)]
     kc = [[np.zeros((0, d), dtype=np.uint16) for _ in range(Hkv)] for _ in range(n_layers)]
@@ -63,7 +68,7 @@ def _sequence(Hkv, d, B, S, R, L0, steps, grid=None, n_layers=1, drift=0.3, seed
             kb, vb, _ = caches[layer]
             idx_g = idxs[layer].cpu().numpy()
             kd_g = pu.bf16_dev_to_bits(kds[layer])
-            vd_g = pu.bf16_dev_to_bits(vds[layer])
+            vd_g = pu.bf16_dev_to_bits(vds[layer].view(torch.bfloat16))
             for h in range(Hkv):
                 kept = orc.select_partial(imps_np[layer][h].astype(np.float64), L, B, S, R)
                 grown_k = np.zeros((N_new, d), dtype=np.uint16)
@@ -91,6 +96,11 @@ def test_sequence_matches_oracle(Hkv, d, B, L0):
     past the budget; only changed rows are written."""
     frac = _sequence(Hkv, d, B, 4, 64, L0, steps=12)
     print(f"Hkv={Hkv} d={d} B={B}: {frac:.3f} of the full gather's rows written")
+
+
+def test_sequence_fp16_v_cache():
+    """An fp16 V cache: the same slots and the same row bytes."""
+    _sequence(2, 128, 300, 4, 64, 340, steps=6, n_layers=2, v_fp16=True)
 
 
 def test_sequence_with_exact_ties():

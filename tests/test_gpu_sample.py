@@ -74,6 +74,23 @@ def test_flat_distribution_ranks_by_id():
     _run(w, logits=logits, W=0, top_p=0.5, min_p=0.0, uniforms=u)
 
 
+@pytest.mark.parametrize("layout,n_pool", [("spread", 8000), ("front", 6000), ("spread", 20000)])
+def test_large_min_p_sets(layout, n_pool):
+    """min-p sets above the 4,096 that are sorted in shared memory: a pool of
+    n_pool tokens near the top (the rest 7 below), spread over the vocabulary
+    (no slice overflows: the draw's radix descent over the row, leaving out
+    the tokens below the pool; 20,000: some slice overflows and the pool is
+    too large to list) or at its front (one slice overflows: the descent over
+    the pool compacted by the node's row scan)."""
+    w = syn.scaled(syn.WORKLOADS["tiny"], V=60000)
+    rng = np.random.default_rng(11)
+    logits = (rng.standard_normal((w.T, w.V)) * 0.3 - 5.0).astype(np.float32)
+    for i in range(w.T):
+        pos = (rng.permutation(w.V)[:n_pool] if layout == "spread" else np.arange(n_pool))
+        logits[i, pos] = (rng.standard_normal(n_pool) * 0.3 + 2.0).astype(np.float32)
+    _run(w, logits=logits, top_p=0.9, min_p=0.01)
+
+
 def test_heavily_tied_logits():
     w = syn.scaled(syn.WORKLOADS["tiny"], V=30000)
     rng = np.random.default_rng(5)
