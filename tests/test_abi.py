@@ -118,6 +118,20 @@ def test_sample_flags_reject_unknown_bits(ts):
     assert "flags" in ts.ts_last_error()
 
 
+def test_verify_and_append_flags_reject_unknown_bits(ts):
+    """The fp16-V flag variants reject flag bits they do not define, on the
+    host, before anything is enqueued."""
+    p = ctypes.c_void_p(16)
+    lib = _c(ts)
+    f = lib.ts_verify_attention_flags
+    assert f(p, p, p, 100, 200, p, 4, 8, 2, 128, 0, p, p, p, p, 1 << 20, 1 << 7, None,
+             None) == 1
+    assert "flags" in ts.ts_last_error()
+    g = lib.ts_kv_append_batched_flags
+    assert g(1, p, p, p, p, 100, 200, 2, 128, 4, 1 << 3, None, None) == 1
+    assert "flags" in ts.ts_last_error()
+
+
 def test_binding_signatures_match_the_header(ts):
     """Every function the header declares has a ctypes signature in the
     binding with the same number of parameters."""
