@@ -101,6 +101,21 @@ def test_fp16_v_cache_is_bit_identical(name):
         assert torch.equal(a, b)
 
 
+@pytest.mark.parametrize("name,T,L", [("llama3.1-8b", 4, 0), ("llama3.1-8b", 4, 65),
+                                      ("llama3.1-8b", 8, 4133), ("qwen2.5-1.5b", 5, 3000),
+                                      ("mha-7b", 8, 6000), ("tiny", 8, 777)])
+def test_draft_sized_calls_match_oracle(name, T, L):
+    """At most 32 packed rows per KV head over a short cache (the draft-side
+    shape: a 128-row tile that is mostly padding): attention and importance
+    against the oracle, random trees of T nodes, caches from empty to several
+    splits, bf16 and fp16 V caches."""
+    w = syn.scaled(syn.WORKLOADS[name], T=T, n_imp=T, planted=0 if L < 300 else None)
+    if w.planted is None:
+        w = syn.scaled(syn.WORKLOADS[name], T=T, n_imp=T)
+    _run(w, L=L)
+    _run(w, L=L, v_fp16=True)
+
+
 def test_bad_parent_sets_status():
     import self_speculative_ultra_gb300 as ts
     w = syn.scaled(syn.WORKLOADS["tiny"], planted=0)
