@@ -948,12 +948,14 @@ int tc_splits(int Hkv, int n_rg, int64_t L, int nsm) {
 // pair-tile tile steps: a pair-tile CTA ~ its tiles + kFixedTiles; a
 // two-stream CTA ~ 2 * kTwoStep * its tiles per split + kFixedTiles, a
 // two-stream step (one query tile, one key tile) costing kTwoStep of a
-// pair-tile step (two query tiles).
+// pair-tile step (two query tiles).  The fixed cost of a CTA (set-up while
+// its first tiles arrive, the last tile's drain and the epilogue, ~7 us)
+// is about four pair-tile steps.
 int64_t split_tiles(int64_t L, int n) { return ((L + n - 1) / n + kNk - 1) / kNk; }
 
 int verify_splits(int Hkv, int n_pt, int n_two, int64_t L, int nsm) {
   constexpr double kTwoStep = 0.55;
-  constexpr double kFixedTiles = 3.0;
+  constexpr double kFixedTiles = 4.0;
   int64_t max_split = (L + kNk - 1) / kNk;
   if (max_split < 1) max_split = 1;
   if (max_split > 1024) max_split = 1024;
