@@ -564,12 +564,12 @@ sample_accept_kernel(const float* __restrict__ logits, const int32_t* __restrict
   const float* x_in = logits + (size_t)i * V;
   float* xs = ws.xs + (size_t)i * V;
   const bool unit_temp = temperature == 1.0f;     // x / 1 is x exactly
-  auto xprime = [&](float x, int t) {
-    if ((bitmap[t >> 5] >> (t & 31)) & 1u)
-      x = (literal || x > 0.f) ? __fdiv_rn(x, penalty) : __fmul_rn(x, penalty);
+  auto xprime_pen = [&](float x, uint32_t pen) {
+    if (pen) x = (literal || x > 0.f) ? __fdiv_rn(x, penalty) : __fmul_rn(x, penalty);
     if (!unit_temp) x = __fdiv_rn(x, temperature);
     return x;
   };
+  auto xprime = [&](float x, int t) { return xprime_pen(x, (bitmap[t >> 5] >> (t & 31)) & 1u); };
   float lmax = -INFINITY;
   if (vec) {
     // kBatch float4 loads of a thread in flight together, then their x'
@@ -587,10 +587,12 @@ sample_accept_kernel(const float* __restrict__ logits, const int32_t* __restrict
         const int q = q0 + b * kThreads;
         if (q < t1 / 4) {
           const int t = 4 * q;
-          a[b].x = xprime(a[b].x, t);
-          a[b].y = xprime(a[b].y, t + 1);
-          a[b].z = xprime(a[b].z, t + 2);
-          a[b].w = xprime(a[b].w, t + 3);
+          // the window bits of tokens t .. t+3 (t is a multiple of 4: one word)
+          const uint32_t pb = bitmap[t >> 5] >> (t & 31);
+          a[b].x = xprime_pen(a[b].x, pb & 1u);
+          a[b].y = xprime_pen(a[b].y, (pb >> 1) & 1u);
+          a[b].z = xprime_pen(a[b].z, (pb >> 2) & 1u);
+          a[b].w = xprime_pen(a[b].w, (pb >> 3) & 1u);
           xs4[q] = a[b];
           lmax = fmaxf(lmax, fmaxf(fmaxf(a[b].x, a[b].y), fmaxf(a[b].z, a[b].w)));
         }
@@ -608,15 +610,20 @@ sample_accept_kernel(const float* __restrict__ logits, const int32_t* __restrict
   // rereads the values it wrote)
   uint2* cand = ws.cand + ((size_t)i * kParts + part) * kCapPart;
   float z = 0.f, se = 0.f;
-  auto consider = [&](bool valid, float x, int t) {
-    float e = 0.f;
-    if (valid) {
-      e = expf(x - mc);
-      z += e;
-      if (eta_mode) se += e * (x - mc);   // entropy term
-    }
-    // eta's threshold is only known after the merge: the last CTA scans
-    const bool in = valid && !eta_mode && e >= min_p;
+  // Z_c (and the entropy term) with the fast exponential: its error, below
+  // 1e-6 relative where a token carries mass, is under the fp32 rounding of
+  // the sum itself.  The candidate test is only a superset filter, loosened
+  // by 2^-16 for that error: the merge re-tests every candidate with expf.
+  const float min_p_lo = min_p * (1.0f - 1.0f / 65536.0f);
+  auto accumulate = [&](float x) -> float {
+    const float e = __expf(x - mc);
+    z += e;
+    if (eta_mode) se += e * (x - mc);   // entropy term
+    return e;
+  };
+  // eta's threshold is only known after the merge: the last CTA scans
+  auto is_cand = [&](bool valid, float e) { return valid && !eta_mode && e >= min_p_lo; };
+  auto append = [&](bool in, float x, int t) {
     const unsigned m = __ballot_sync(0xffffffffu, in);
     if (m) {
       int base = 0;
@@ -640,16 +647,32 @@ sample_accept_kernel(const float* __restrict__ logits, const int32_t* __restrict
       for (int b = 0; b < kBatch; ++b) {
         const int q = b0 + b * kThreads + tid;
         const bool valid = q < t1 / 4;
-        consider(valid, a[b].x, 4 * q);
-        consider(valid, a[b].y, 4 * q + 1);
-        consider(valid, a[b].z, 4 * q + 2);
-        consider(valid, a[b].w, 4 * q + 3);
+        float e0 = 0.f, e1 = 0.f, e2 = 0.f, e3 = 0.f;
+        if (valid) {
+          e0 = accumulate(a[b].x);
+          e1 = accumulate(a[b].y);
+          e2 = accumulate(a[b].z);
+          e3 = accumulate(a[b].w);
+        }
+        const bool c0 = is_cand(valid, e0), c1 = is_cand(valid, e1);
+        const bool c2 = is_cand(valid, e2), c3 = is_cand(valid, e3);
+        // candidates are rare: one vote for the warp's four tokens a lane,
+        // then the per-token appends only where some lane has one
+        if (__any_sync(0xffffffffu, c0 || c1 || c2 || c3)) {
+          append(c0, a[b].x, 4 * q);
+          append(c1, a[b].y, 4 * q + 1);
+          append(c2, a[b].z, 4 * q + 2);
+          append(c3, a[b].w, 4 * q + 3);
+        }
       }
     }
   } else {
     for (int b0 = t0; b0 < t1; b0 += kThreads) {
       const int t = b0 + tid;
-      consider(t < t1, t < t1 ? xs[t] : 0.f, t);
+      const bool valid = t < t1;
+      const float x = valid ? xs[t] : 0.f;
+      const float e = valid ? accumulate(x) : 0.f;
+      append(is_cand(valid, e), x, t);
     }
   }
   const float zc = block_sum(z, sm);
@@ -667,9 +690,16 @@ sample_accept_kernel(const float* __restrict__ logits, const int32_t* __restrict
   const volatile PartStat* vst = ws.stat + i * kParts;
   float xmax = -INFINITY;
   bool overflow = false;
+  // the slices' candidate counts, and where each list starts in their
+  // concatenation
+  int cat_off[kParts + 1];
+  cat_off[0] = 0;
+#pragma unroll
   for (int p = 0; p < kParts; ++p) {
+    const int np_ = vst[p].n;
     xmax = fmaxf(xmax, vst[p].m);
-    overflow |= vst[p].n > kCapPart;
+    overflow |= np_ > kCapPart;
+    cat_off[p + 1] = cat_off[p] + np_;
   }
   float Z = 0.f, Sx = 0.f;
   for (int p = 0; p < kParts; ++p) {
@@ -701,32 +731,40 @@ sample_accept_kernel(const float* __restrict__ logits, const int32_t* __restrict
   // lists there are not read on that path)
   uint2* pool = ws.cand + (size_t)i * kPool;
   if (!overflow) {
-    for (int p = 0; p < kParts; ++p) {
-      const int np_ = vst[p].n;
-      const uint2* pc = ws.cand + ((size_t)i * kParts + p) * kCapPart;
-      for (int b0 = 0; b0 < np_; b0 += kThreads) {
-        const int r = b0 + tid;
-        uint2 c = make_uint2(0u, 0u);
-        float e = 0.f;
-        if (r < np_) {
-          c = __ldcg(pc + r);
-          e = expf(key_float(c.x) - xmax);
-        }
-        const bool in = r < np_ && e >= min_p;
-        if (in) {
-          zmin += e;
-          ++nmin;
-        }
-        const unsigned m = __ballot_sync(0xffffffffu, in);
-        if (m) {
-          int base = 0;
-          if (lane == __ffs(m) - 1) base = atomicAdd(&sm.ncand, __popc(m));
-          base = __shfl_sync(0xffffffffu, base, __ffs(m) - 1);
-          const int slot = base + __popc(m & ((1u << lane) - 1));
-          if (in && slot < kCap) {
-            sm.ckey[slot] = c.x;
-            sm.cid[slot] = (int32_t)c.y;
+    // one pass over the concatenation of the slices' lists (their loads in
+    // flight together, not slice after slice); the members' order in the
+    // shared list does not matter, it is sorted below
+    const int ntot = cat_off[kParts];
+    for (int b0 = 0; b0 < ntot; b0 += kThreads) {
+      const int r = b0 + tid;
+      const bool have = r < ntot;
+      uint2 c = make_uint2(0u, 0u);
+      float e = 0.f;
+      if (have) {
+        int p = 0, off = 0;
+#pragma unroll
+        for (int x = 1; x < kParts; ++x)
+          if (r >= cat_off[x]) {
+            p = x;
+            off = cat_off[x];
           }
+        c = __ldcg(ws.cand + ((size_t)i * kParts + p) * kCapPart + (r - off));
+        e = expf(key_float(c.x) - xmax);
+      }
+      const bool in = have && e >= min_p;
+      if (in) {
+        zmin += e;
+        ++nmin;
+      }
+      const unsigned m = __ballot_sync(0xffffffffu, in);
+      if (m) {
+        int base = 0;
+        if (lane == __ffs(m) - 1) base = atomicAdd(&sm.ncand, __popc(m));
+        base = __shfl_sync(0xffffffffu, base, __ffs(m) - 1);
+        const int slot = base + __popc(m & ((1u << lane) - 1));
+        if (in && slot < kCap) {
+          sm.ckey[slot] = c.x;
+          sm.cid[slot] = (int32_t)c.y;
         }
       }
     }
