@@ -686,6 +686,8 @@ sample_accept_kernel(const float* __restrict__ logits, const int32_t* __restrict
   if (!sm.last) return;
 
   // ---- last CTA of node i: merge the slices
+  // the node's uniform (an input) is loaded now, off the draw's critical path
+  const float u_node = reject ? 0.f : uniforms[i];
   __threadfence();
   const volatile PartStat* vst = ws.stat + i * kParts;
   float xmax = -INFINITY;
@@ -811,90 +813,168 @@ sample_accept_kernel(const float* __restrict__ logits, const int32_t* __restrict
   int token;
   if (n_minp >= 1 && n_minp <= kCap) {
     // ---- fast path: the kept set is a rank prefix inside the min-p set.
-    // Sort the candidates by (x' desc, id asc) (bitonic, padded to 2^k),
-    // prefix-sum their e, cut at top-p, draw.
-    int np = 32;
-    while (np < n_minp) np <<= 1;
-    for (int q = n_minp + tid; q < np; q += kThreads) {
-      sm.ckey[q] = 0u;            // below every real key
-      sm.cid[q] = 0x7FFFFFFF;
-    }
-    __syncthreads();
-    for (int size = 2; size <= np; size <<= 1) {
-      for (int stride = size >> 1; stride > 0; stride >>= 1) {
-        for (int q = tid; q < np; q += kThreads) {
-          const int qx = q ^ stride;
-          if (qx > q) {
-            const uint32_t ka = sm.ckey[q], kb = sm.ckey[qx];
-            const int32_t ia = sm.cid[q], ib = sm.cid[qx];
-            // a ranks before b: larger key, then smaller id
-            const bool a_first = ka > kb || (ka == kb && ia < ib);
-            const bool desc = (q & size) == 0;
-            if (desc != a_first) {
-              sm.ckey[q] = kb;
-              sm.ckey[qx] = ka;
-              sm.cid[q] = ib;
-              sm.cid[qx] = ia;
-            }
-          }
+    // Sort the candidates by (x' desc, id asc), prefix-sum their e in rank
+    // order, cut at top-p (first inclusive mass > top_p*Z), draw (first
+    // inclusive mass > u * kept mass).
+    const float tp = (eta_mode || top_p >= 1.0f) ? INFINITY : top_p * Z;   // eta: no top-p cut
+    if (n_minp <= kThreads) {
+      // one candidate a thread.  (key, id) is a total order, so a
+      // candidate's count of the candidates ranked before it is its sorted
+      // position: the permutation a sorting network gives, with no network
+      uint32_t ck = 0u;
+      int32_t cv = 0;
+      int rank = 0;
+      const bool mine = tid < n_minp;
+      if (mine) {
+        ck = sm.ckey[tid];
+        cv = sm.cid[tid];
+        for (int j = 0; j < n_minp; ++j) {
+          const uint32_t kj = sm.ckey[j];
+          const int32_t ij = sm.cid[j];
+          rank += (kj > ck || (kj == ck && ij < cv)) ? 1 : 0;
         }
-        __syncthreads();
       }
-    }
-    if (tid < 32) {
-      // warp 0 walks the ranks: top-p cut (first inclusive mass > top_p*Z),
-      // then the draw (first inclusive mass > u * kept mass)
-      const float tp = (eta_mode || top_p >= 1.0f) ? INFINITY : top_p * Z;   // eta: no top-p cut
-      float run = 0.f, zk = 0.f;
-      int k_keep = 0;
-      for (int b0 = 0; b0 < n_minp; b0 += 32) {
-        const int r = b0 + lane;
-        const float e = r < n_minp ? expf(key_float(sm.ckey[r]) - xmax) : 0.f;
-        float incl = e;
+      if (tid == 0) {
+        sm.cnt[0] = n_minp;       // first rank past the top-p mass (none yet)
+        sm.cnt[1] = 0x7FFFFFFF;   // first kept rank past the draw's target
+      }
+      __syncthreads();
+      if (mine) {
+        sm.ckey[rank] = ck;
+        sm.cid[rank] = cv;
+      }
+      __syncthreads();
+      // inclusive masses in rank order, each an fp32 sum formed exactly as
+      // one warp walking 32 ranks at a time forms it: every 32-rank chunk
+      // scanned by shuffles, plus the total of the chunks before it, carried
+      // chunk after chunk (the total of a chunk is its last lane's scan)
+      const int w = tid >> 5, nchunk = (n_minp + 31) >> 5;
+      float* chunk_tot = sm.mass + kThreads;        // [kThreads / 32]
+      float* chunk_run = chunk_tot + 32;            // [kThreads / 32], then the whole total
+      float incl = 0.f;
+      if (w < nchunk) {
+        incl = mine ? expf(key_float(sm.ckey[tid]) - xmax) : 0.f;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
           const float y = __shfl_up_sync(0xffffffffu, incl, o);
           if (lane >= o) incl += y;
         }
-        incl += run;
-        const unsigned hit = __ballot_sync(0xffffffffu, r < n_minp && incl > tp);
-        if (hit) {
-          const int src = __ffs(hit) - 1;
-          k_keep = b0 + src + 1;
-          zk = __shfl_sync(0xffffffffu, incl, src);
-          break;
+        if (lane == 31) chunk_tot[w] = incl;
+      }
+      __syncthreads();
+      if (tid == 0) {
+        float run = 0.f;
+        for (int c = 0; c < nchunk; ++c) {
+          chunk_run[c] = run;
+          run = chunk_tot[c] + run;
         }
-        run = __shfl_sync(0xffffffffu, incl, 31);
+        chunk_run[32] = run;
       }
-      if (k_keep == 0) {             // top-p keeps the whole min-p set
-        k_keep = n_minp;
-        zk = run;
+      __syncthreads();
+      if (w < nchunk) incl += chunk_run[w];
+      if (mine) {
+        sm.mass[tid] = incl;
+        if (incl > tp) atomicMin(&sm.cnt[0], tid);
       }
-      if (lane == 0) {
+      __syncthreads();
+      const int hit = sm.cnt[0];
+      const int k_keep = hit < n_minp ? hit + 1 : n_minp;
+      // top-p keeps the whole min-p set: the kept mass is the last chunk's
+      // carried total
+      const float zk = hit < n_minp ? sm.mass[hit] : chunk_run[32];
+      const float target = reject ? -1.f : u_node * zk;
+      if (tid < k_keep && incl > target) atomicMin(&sm.cnt[1], tid);
+      __syncthreads();
+      if (tid == 0) {
+        const int d = sm.cnt[1];
+        const int pick = d < k_keep ? d : k_keep - 1;
         sm.nkeep = k_keep;
         sm.zk = zk;
+        sm.kpre = (uint32_t)sm.cid[pick];
       }
-      const float target = reject ? -1.f : uniforms[i] * zk;
-      run = 0.f;
-      int pick = k_keep - 1;
-      for (int b0 = 0; b0 < k_keep; b0 += 32) {
-        const int r = b0 + lane;
-        const float e = r < k_keep ? expf(key_float(sm.ckey[r]) - xmax) : 0.f;
-        float incl = e;
+    } else {
+      int np = 32;
+      while (np < n_minp) np <<= 1;
+      for (int q = n_minp + tid; q < np; q += kThreads) {
+        sm.ckey[q] = 0u;            // below every real key
+        sm.cid[q] = 0x7FFFFFFF;
+      }
+      __syncthreads();
+      for (int size = 2; size <= np; size <<= 1) {
+        for (int stride = size >> 1; stride > 0; stride >>= 1) {
+          for (int q = tid; q < np; q += kThreads) {
+            const int qx = q ^ stride;
+            if (qx > q) {
+              const uint32_t ka = sm.ckey[q], kb = sm.ckey[qx];
+              const int32_t ia = sm.cid[q], ib = sm.cid[qx];
+              // a ranks before b: larger key, then smaller id
+              const bool a_first = ka > kb || (ka == kb && ia < ib);
+              const bool desc = (q & size) == 0;
+              if (desc != a_first) {
+                sm.ckey[q] = kb;
+                sm.ckey[qx] = ka;
+                sm.cid[q] = ib;
+                sm.cid[qx] = ia;
+              }
+            }
+          }
+          __syncthreads();
+        }
+      }
+      if (tid < 32) {
+        // warp 0 walks the ranks: top-p cut (first inclusive mass > top_p*Z),
+        // then the draw (first inclusive mass > u * kept mass)
+        float run = 0.f, zk = 0.f;
+        int k_keep = 0;
+        for (int b0 = 0; b0 < n_minp; b0 += 32) {
+          const int r = b0 + lane;
+          const float e = r < n_minp ? expf(key_float(sm.ckey[r]) - xmax) : 0.f;
+          float incl = e;
 #pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-          const float y = __shfl_up_sync(0xffffffffu, incl, o);
-          if (lane >= o) incl += y;
+          for (int o = 1; o < 32; o <<= 1) {
+            const float y = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += y;
+          }
+          incl += run;
+          const unsigned hit = __ballot_sync(0xffffffffu, r < n_minp && incl > tp);
+          if (hit) {
+            const int src = __ffs(hit) - 1;
+            k_keep = b0 + src + 1;
+            zk = __shfl_sync(0xffffffffu, incl, src);
+            break;
+          }
+          run = __shfl_sync(0xffffffffu, incl, 31);
         }
-        incl += run;
-        const unsigned hit = __ballot_sync(0xffffffffu, r < k_keep && incl > target);
-        if (hit) {
-          pick = b0 + __ffs(hit) - 1;
-          break;
+        if (k_keep == 0) {             // top-p keeps the whole min-p set
+          k_keep = n_minp;
+          zk = run;
         }
-        run = __shfl_sync(0xffffffffu, incl, 31);
+        if (lane == 0) {
+          sm.nkeep = k_keep;
+          sm.zk = zk;
+        }
+        const float target = reject ? -1.f : u_node * zk;
+        run = 0.f;
+        int pick = k_keep - 1;
+        for (int b0 = 0; b0 < k_keep; b0 += 32) {
+          const int r = b0 + lane;
+          const float e = r < k_keep ? expf(key_float(sm.ckey[r]) - xmax) : 0.f;
+          float incl = e;
+#pragma unroll
+          for (int o = 1; o < 32; o <<= 1) {
+            const float y = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += y;
+          }
+          incl += run;
+          const unsigned hit = __ballot_sync(0xffffffffu, r < k_keep && incl > target);
+          if (hit) {
+            pick = b0 + __ffs(hit) - 1;
+            break;
+          }
+          run = __shfl_sync(0xffffffffu, incl, 31);
+        }
+        if (lane == 0) sm.kpre = (uint32_t)sm.cid[pick];
       }
-      if (lane == 0) sm.kpre = (uint32_t)sm.cid[pick];
     }
     __syncthreads();
     token = reject ? reject_sparse(i, T, V, xmax, q_draft + (size_t)i * V, uniforms, u_draw, xs, sm)
