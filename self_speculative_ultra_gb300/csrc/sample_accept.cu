@@ -515,6 +515,17 @@ sample_accept_kernel(const float* __restrict__ logits, const int32_t* __restrict
   const int lane = tid & 31;
   const int nwords = (V + 31) / 32;
   for (int w = tid; w < nwords; w += kThreads) bitmap[w] = 0u;
+  // the window's committed tokens lie in prior[n_prior - W, n_prior)
+  // whatever the root path's length: loaded with the tree, ahead of the
+  // path walk (two tokens a thread cover W <= 1024)
+  constexpr int kPre = 2;
+  const int plo = n_prior > W ? n_prior - W : 0;
+  int pre[kPre];
+#pragma unroll
+  for (int k = 0; k < kPre; ++k) {
+    const int c = plo + tid + k * kThreads;
+    pre[k] = c < n_prior ? prior[c] : 0;
+  }
   if (tid < T) {
     sm.par[tid] = parents[tid];
     sm.tok[tid] = tree_tokens[tid];
@@ -542,17 +553,23 @@ sample_accept_kernel(const float* __restrict__ logits, const int32_t* __restrict
     sm.ncand = 0;
   }
   __syncthreads();
-  // window = last W tokens of prior ++ path tokens
+  // window = last W tokens of prior ++ path tokens: c in [start, total)
   const int total = n_prior + sm.plen;
   const int start = total > W ? total - W : 0;
-  for (int c = start + tid; c < total; c += kThreads) {
-    int t = c < n_prior ? prior[c] : sm.ptok[c - n_prior];
-    if (t < 0 || t >= V) {
+  auto mark = [&](int t) {
+    if (t < 0 || t >= V)
       set_status(status, TS_ERR_INVALID_ARG);
-      continue;
-    }
-    atomicOr(&bitmap[t >> 5], 1u << (t & 31));
+    else
+      atomicOr(&bitmap[t >> 5], 1u << (t & 31));
+  };
+#pragma unroll
+  for (int k = 0; k < kPre; ++k) {
+    const int c = plo + tid + k * kThreads;
+    if (c >= start && c < n_prior) mark(pre[k]);
   }
+  for (int c = plo + kPre * kThreads + tid; c < n_prior; c += kThreads)
+    if (c >= start) mark(prior[c]);
+  for (int c = max(start, n_prior) + tid; c < total; c += kThreads) mark(sm.ptok[c - n_prior]);
   __syncthreads();
 
   // this CTA's slice of the vocabulary: x' = penalised / tempered logits
