@@ -293,10 +293,52 @@ __device__ __noinline__ Found radix_find(const float* __restrict__ xs, int V, co
     sm.mb = 0.f;
     sm.cb = 0;
   }
+  int key_bits = 32;   // key bits the levels resolve, from the top
+  if (kList) {
+    // a compacted pool spans a narrow range of keys: its common leading
+    // bits are fixed in the prefix, so the first level spreads the pool over
+    // its buckets instead of piling it into a few contended ones
+    uint32_t lo = 0xFFFFFFFFu, hi = 0u;
+    for (int j = threadIdx.x; j < n; j += blockDim.x) {
+      const uint32_t k = list[j].x;
+      lo = min(lo, k);
+      hi = max(hi, k);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      lo = min(lo, __shfl_xor_sync(0xffffffffu, lo, o));
+      hi = max(hi, __shfl_xor_sync(0xffffffffu, hi, o));
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      sm.red_i[0] = (int)0xFFFFFFFFu;
+      sm.red_i[1] = 0;
+    }
+    __syncthreads();
+    if ((threadIdx.x & 31) == 0) {
+      atomicMin(reinterpret_cast<unsigned*>(&sm.red_i[0]), lo);
+      atomicMax(reinterpret_cast<unsigned*>(&sm.red_i[1]), hi);
+    }
+    __syncthreads();
+    lo = (uint32_t)sm.red_i[0];
+    hi = (uint32_t)sm.red_i[1];
+    const int common = lo <= hi ? __clz(lo ^ hi) : 0;   // 32 when every key is equal
+    key_bits = 32 - common;
+    if (threadIdx.x == 0 && common > 0) {
+      const uint32_t pm = common == 32 ? 0xFFFFFFFFu : ~(0xFFFFFFFFu >> common);
+      sm.kpre = lo & pm;
+      sm.kmask = pm;
+    }
+  }
   __syncthreads();
-  radix_level<kList>(xs, V, list, n, xmax, mode, target_mass, target_rank, false, 21, 11, skip_e, sm);
-  radix_level<kList>(xs, V, list, n, xmax, mode, target_mass, target_rank, false, 10, 11, skip_e, sm);
-  radix_level<kList>(xs, V, list, n, xmax, mode, target_mass, target_rank, false, 0, 10, skip_e, sm);
+  // key levels of at most 11 bits from the highest unresolved one down,
+  // then the 18 id bits in two levels of 9
+  while (key_bits > 0) {
+    const int b = key_bits < 11 ? key_bits : 11;
+    key_bits -= b;
+    radix_level<kList>(xs, V, list, n, xmax, mode, target_mass, target_rank, false, key_bits, b,
+                       skip_e, sm);
+  }
   radix_level<kList>(xs, V, list, n, xmax, mode, target_mass, target_rank, true, 9, 9, skip_e, sm);
   radix_level<kList>(xs, V, list, n, xmax, mode, target_mass, target_rank, true, 0, 9, skip_e, sm);
   Found f;
