@@ -980,59 +980,75 @@ sample_accept_kernel(const float* __restrict__ logits, const int32_t* __restrict
           __syncthreads();
         }
       }
-      if (tid < 32) {
-        // warp 0 walks the ranks: top-p cut (first inclusive mass > top_p*Z),
-        // then the draw (first inclusive mass > u * kept mass)
-        float run = 0.f, zk = 0.f;
-        int k_keep = 0;
-        for (int b0 = 0; b0 < n_minp; b0 += 32) {
-          const int r = b0 + lane;
-          const float e = r < n_minp ? expf(key_float(sm.ckey[r]) - xmax) : 0.f;
-          float incl = e;
+      // the rank walks as a block pass, as for the smaller sets, with warp
+      // w taking chunks w, w + 16, ... (the same fp32 sums: chunk scans by
+      // shuffles, their totals carried chunk after chunk)
+      constexpr int kWarps = kThreads / 32, kRounds = kCap / kThreads;
+      const int w = tid >> 5, nchunk = (n_minp + 31) >> 5;
+      float* chunk_tot = sm.mass;                 // [kCap / 32]
+      float* chunk_run = sm.mass + kCap / 32;     // [kCap / 32], then the whole total
+      float* zk_at_hit = chunk_run + kCap / 32 + 1;
+      if (tid == 0) {
+        sm.cnt[0] = n_minp;
+        sm.cnt[1] = 0x7FFFFFFF;
+      }
+      float incl[kRounds];
+#pragma unroll
+      for (int k = 0; k < kRounds; ++k) {
+        const int c = w + k * kWarps;
+        incl[k] = 0.f;
+        if (c < nchunk) {   // warp-uniform
+          const int r = 32 * c + lane;
+          float v = r < n_minp ? expf(key_float(sm.ckey[r]) - xmax) : 0.f;
 #pragma unroll
           for (int o = 1; o < 32; o <<= 1) {
-            const float y = __shfl_up_sync(0xffffffffu, incl, o);
-            if (lane >= o) incl += y;
+            const float y = __shfl_up_sync(0xffffffffu, v, o);
+            if (lane >= o) v += y;
           }
-          incl += run;
-          const unsigned hit = __ballot_sync(0xffffffffu, r < n_minp && incl > tp);
-          if (hit) {
-            const int src = __ffs(hit) - 1;
-            k_keep = b0 + src + 1;
-            zk = __shfl_sync(0xffffffffu, incl, src);
-            break;
-          }
-          run = __shfl_sync(0xffffffffu, incl, 31);
+          if (lane == 31) chunk_tot[c] = v;
+          incl[k] = v;
         }
-        if (k_keep == 0) {             // top-p keeps the whole min-p set
-          k_keep = n_minp;
-          zk = run;
+      }
+      __syncthreads();
+      if (tid == 0) {
+        float run = 0.f;
+        for (int c = 0; c < nchunk; ++c) {
+          chunk_run[c] = run;
+          run = chunk_tot[c] + run;
         }
-        if (lane == 0) {
-          sm.nkeep = k_keep;
-          sm.zk = zk;
-        }
-        const float target = reject ? -1.f : u_node * zk;
-        run = 0.f;
-        int pick = k_keep - 1;
-        for (int b0 = 0; b0 < k_keep; b0 += 32) {
-          const int r = b0 + lane;
-          const float e = r < k_keep ? expf(key_float(sm.ckey[r]) - xmax) : 0.f;
-          float incl = e;
+        chunk_run[kCap / 32] = run;
+      }
+      __syncthreads();
 #pragma unroll
-          for (int o = 1; o < 32; o <<= 1) {
-            const float y = __shfl_up_sync(0xffffffffu, incl, o);
-            if (lane >= o) incl += y;
-          }
-          incl += run;
-          const unsigned hit = __ballot_sync(0xffffffffu, r < k_keep && incl > target);
-          if (hit) {
-            pick = b0 + __ffs(hit) - 1;
-            break;
-          }
-          run = __shfl_sync(0xffffffffu, incl, 31);
+      for (int k = 0; k < kRounds; ++k) {
+        const int c = w + k * kWarps, r = 32 * c + lane;
+        if (c < nchunk) {
+          incl[k] += chunk_run[c];
+          if (r < n_minp && incl[k] > tp) atomicMin(&sm.cnt[0], r);
         }
-        if (lane == 0) sm.kpre = (uint32_t)sm.cid[pick];
+      }
+      __syncthreads();
+      const int hit = sm.cnt[0];
+      const int k_keep = hit < n_minp ? hit + 1 : n_minp;
+#pragma unroll
+      for (int k = 0; k < kRounds; ++k)
+        if (hit < n_minp && 32 * (w + k * kWarps) + lane == hit) *zk_at_hit = incl[k];
+      __syncthreads();
+      // top-p keeps the whole min-p set: the kept mass is the carried total
+      const float zk = hit < n_minp ? *zk_at_hit : chunk_run[kCap / 32];
+      const float target = reject ? -1.f : u_node * zk;
+#pragma unroll
+      for (int k = 0; k < kRounds; ++k) {
+        const int r = 32 * (w + k * kWarps) + lane;
+        if (r < k_keep && incl[k] > target) atomicMin(&sm.cnt[1], r);
+      }
+      __syncthreads();
+      if (tid == 0) {
+        const int d = sm.cnt[1];
+        const int pick = d < k_keep ? d : k_keep - 1;
+        sm.nkeep = k_keep;
+        sm.zk = zk;
+        sm.kpre = (uint32_t)sm.cid[pick];
       }
     }
     __syncthreads();
